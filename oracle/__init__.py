@@ -1,0 +1,165 @@
+"""fp64 CPU oracle for the selective state-space (S6) scan -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and this
+package never imports the CUDA library: the two share no code.
+
+``ssm_oracle.c`` holds the arithmetic (the plain sequential recurrence in
+double precision; its header cites the passages it follows).  This module
+only marshals numpy arrays into it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_LIB = os.path.join(_HERE, "libssm_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``libssm_oracle.so`` next to its source (gcc -O2, OpenMP, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.ssm_oracle_scan.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                        i64, vp, i32, vp, i64, vp, vp, i32]
+        lib.ssm_oracle_scan.restype = i32
+        lib.ssm_oracle_step.argtypes = [i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                        i32, vp, vp, i32]
+        lib.ssm_oracle_step.restype = i32
+        lib.ssm_oracle_max_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().ssm_oracle_max_threads())
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _io(arr):
+    if arr.dtype == np.uint16:
+        return 1
+    if arr.dtype == np.float32:
+        return 0
+    raise TypeError("u/delta/z must be float32 or bfloat16 bits (uint16), got %s" % arr.dtype)
+
+
+def scan_rows(u, delta, z, unit_b, unit_d, A, B, C, D=None, delta_bias=None,
+              delta_softplus=True, init_state=None, y_stride=1, nthreads=0):
+    """Scan U units given as rows.
+
+    u, delta, z: (U, L) float32 or uint16 (bfloat16 bits); z may be None.
+    unit_b, unit_d: (U,) batch / channel of each row.
+    A: (dim, N) f32; B, C: (batch, N, L_B) f32 (L_B >= L; time index 0 aligned
+    with column 0 of the rows); D, delta_bias: (dim,) f32 or None.
+    init_state: (U, N) float64 or None.
+    Returns (y, final_state): y is (U, ceil(L / y_stride)) float64 holding
+    y_t for t = 0, y_stride, ...; final_state is (U, N) float64.
+    """
+    u = np.ascontiguousarray(u)
+    delta = np.ascontiguousarray(delta)
+    U, L = u.shape
+    io = _io(u)
+    assert delta.shape == u.shape and _io(delta) == io
+    if z is not None:
+        z = np.ascontiguousarray(z)
+        assert z.shape == u.shape and _io(z) == io
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    N = A.shape[1]
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    C = np.ascontiguousarray(C, dtype=np.float32)
+    assert B.shape == C.shape and B.shape[1] == N and B.shape[2] >= L
+    ub = np.ascontiguousarray(unit_b, dtype=np.int64)
+    ud = np.ascontiguousarray(unit_d, dtype=np.int64)
+    assert ub.shape == (U,) and ud.shape == (U,)
+    assert (ub >= 0).all() and (ub < B.shape[0]).all() and (ud >= 0).all() and (ud < A.shape[0]).all()
+    D = None if D is None else np.ascontiguousarray(D, dtype=np.float32)
+    bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
+    h0 = None
+    if init_state is not None:
+        h0 = np.ascontiguousarray(init_state, dtype=np.float64)
+        assert h0.shape == (U, N)
+    ny = (L + y_stride - 1) // y_stride
+    y = np.empty((U, ny), dtype=np.float64)
+    hN = np.empty((U, N), dtype=np.float64)
+    rc = _load().ssm_oracle_scan(U, L, N, io, _ptr(u), _ptr(delta), _ptr(z), _ptr(ub), _ptr(ud),
+                                 _ptr(bias), _ptr(A), _ptr(B), _ptr(C), B.shape[2], _ptr(D),
+                                 int(bool(delta_softplus)), _ptr(h0), int(y_stride), _ptr(y),
+                                 _ptr(hN), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
+    return y, hN
+
+
+def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+         init_state=None, nthreads=0):
+    """Full scan of (batch, dim, L) inputs.  Returns y (batch, dim, L) and
+    final_state (batch, dim, N), both float64."""
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    bb, dd = np.meshgrid(np.arange(batch), np.arange(dim), indexing="ij")
+    h0 = None if init_state is None else np.asarray(init_state, np.float64).reshape(batch * dim, N)
+    y, hN = scan_rows(u.reshape(batch * dim, L), delta.reshape(batch * dim, L),
+                      None if z is None else z.reshape(batch * dim, L), bb.ravel(), dd.ravel(),
+                      A, B, C, D, delta_bias, delta_softplus, h0, 1, nthreads)
+    return y.reshape(batch, dim, L), hN.reshape(batch, dim, N)
+
+
+def step(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+         nthreads=0):
+    """One decode step on (batch, dim, N) float64 state (returned updated, not
+    modified in place) with u, delta, z of shape (batch, dim) and B, C of shape
+    (batch, N).  Returns (y (batch, dim) float64, new_state)."""
+    batch, dim = u.shape
+    N = A.shape[1]
+    st = np.array(state, dtype=np.float64, copy=True).reshape(batch * dim, N)
+    bb, dd = np.meshgrid(np.arange(batch), np.arange(dim), indexing="ij")
+    y = np.empty(batch * dim, dtype=np.float64)
+    u_ = np.ascontiguousarray(u).reshape(-1)
+    io = _io(u_)
+    dl = np.ascontiguousarray(delta).reshape(-1)
+    zz = None if z is None else np.ascontiguousarray(z).reshape(-1)
+    ub = np.ascontiguousarray(bb.ravel(), dtype=np.int64)
+    ud = np.ascontiguousarray(dd.ravel(), dtype=np.int64)
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    C = np.ascontiguousarray(C, dtype=np.float32)
+    D = None if D is None else np.ascontiguousarray(D, dtype=np.float32)
+    bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
+    rc = _load().ssm_oracle_step(batch * dim, N, io, _ptr(u_), _ptr(dl), _ptr(zz), _ptr(ub),
+                                 _ptr(ud), _ptr(bias), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                 int(bool(delta_softplus)), _ptr(st), _ptr(y), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
+    return y.reshape(batch, dim), st.reshape(batch, dim, N)
+
+
+def rel_err(got, ref):
+    """max |got - ref| / max |ref|: the parity metric for y and final_state."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.max(np.abs(ref)) if ref.size else 0.0
+    num = np.max(np.abs(got - ref)) if ref.size else 0.0
+    if den == 0.0:
+        return float(num)
+    return float(num / den)
