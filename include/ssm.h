@@ -1,0 +1,151 @@
+/*
+ * ssm.h -- C ABI of libssm: the selective state-space (S6) scan on one B300 GPU.
+ *
+ * What the entry points compute (per batch index b and channel d, time t, state n):
+ *
+ *   Δ_t  = softplus(delta[b,d,t] + delta_bias[d])   (or without softplus)
+ *          -- selection: Δ is a function of the input; "Mamba: Linear-Time
+ *             Sequence Modeling" summary page, section 4b, Algorithm 2 and the
+ *             parameterisation under it (τ_Δ = softplus of a parameter plus a
+ *             projection); SSM/Mamba chapter, section 4.1.
+ *   Ā    = exp(Δ_t A[d,n]),  B̄ = (exp(Δ_t A[d,n]) - 1) / A[d,n] * B[b,n,t]
+ *          -- zero-order hold for a diagonal A, summary page equation (4);
+ *             chapter section 3.2.  A[d,n] = 0 takes the limit B̄ = Δ_t B.
+ *   h_t  = Ā h_{t-1} + B̄ u[b,d,t]
+ *   y_t  = C[b,:,t] · h_t + D[d] u[b,d,t]
+ *          -- recurrence and readout, summary page equations (2a), (2b); the
+ *             direct term D from the chapter's section 3.1.
+ *   y_t *= z[b,d,t] * sigmoid(z[b,d,t])
+ *          -- "SSM output × SiLU(gate)", summary page section 4a shape table.
+ *
+ * The expanded (batch, d_inner, L, N) state is never written to memory; only
+ * y and the final state are.
+ *
+ * Memory: every pointer is a DEVICE pointer on the current CUDA device, owned
+ * by the caller; the library allocates nothing and keeps no pointer after a
+ * call returns.  Layouts are dense and row-major (last index fastest):
+ *   u, delta, z, y      (batch, dim, seqlen)  in io_dtype (float32 or bfloat16)
+ *   B, C                (batch, dstate, seqlen) float32
+ *   A                   (dim, dstate) float32
+ *   D, delta_bias       (dim) float32
+ *   states              (batch, dim, dstate) float32
+ * All pointers must be 16-byte aligned (SSM_ERR_ALIGN otherwise).  Any seqlen
+ * >= 0 is accepted; rows whose length is not a multiple of 16 bytes take a
+ * slower element-wise load path.  Outputs must not overlap inputs.
+ *
+ * Execution: work is enqueued on the given stream (NULL = the legacy default
+ * stream) and the call returns without synchronising.  Argument errors are
+ * returned synchronously before anything is enqueued; a failed launch returns
+ * SSM_ERR_CUDA (details from cudaGetLastError()).
+ */
+#ifndef SSM_H
+#define SSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* I/O element types of u, delta, z and y. */
+#define SSM_F32 0
+#define SSM_BF16 1
+
+/* Status codes. */
+#define SSM_OK 0
+#define SSM_ERR_ARG (-1)         /* null required pointer, bad size, bad dtype, overlap */
+#define SSM_ERR_ALIGN (-2)       /* a pointer is not 16-byte aligned */
+#define SSM_ERR_UNSUPPORTED (-3) /* dstate not in {1, 2, 4, 8, 16, 32, 64} */
+#define SSM_ERR_CUDA (-4)        /* a CUDA call or kernel launch failed */
+#define SSM_ERR_WORKSPACE (-5)   /* workspace given but too small */
+
+/* Human-readable name of a status code (static string). */
+const char* ssm_strerror(int status);
+
+/* Library version, e.g. "0.1.0". */
+const char* ssm_version(void);
+
+/*
+ * Full-sequence scan (the summary page's Algorithm 2 with the recurrence of
+ * equation (2) evaluated as a chunked scan), on the legacy default stream,
+ * starting from a zero state.
+ *
+ *   u, delta      required, (batch, dim, seqlen) io_dtype
+ *   delta_bias    optional (NULL = 0), (dim)
+ *   A             required, (dim, dstate)
+ *   B, C          required, (batch, dstate, seqlen)
+ *   D             optional (NULL = 0), (dim)
+ *   z             optional (NULL = no gate), (batch, dim, seqlen) io_dtype
+ *   delta_softplus  nonzero: Δ = softplus(delta + bias); zero: Δ = delta + bias
+ *   y             required output, (batch, dim, seqlen) io_dtype
+ *   final_state   optional output (NULL = not written), (batch, dim, dstate) float32
+ *
+ * batch, dim >= 0 (either 0 is a no-op); seqlen >= 0 (0 writes final_state
+ * only); dstate in {1, 2, 4, 8, 16, 32, 64}.
+ */
+int ssm_scan_fwd(const void* u, const void* delta, const float* delta_bias, const float* A,
+                 const float* B, const float* C, const float* D, const void* z,
+                 int delta_softplus, void* y, float* final_state,
+                 int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype);
+
+/*
+ * Bytes of workspace that ssm_scan_fwd_ex may use for these sizes on the
+ * current device.  0 means the plan needs none.  With a workspace of at least
+ * this size the scan may split the sequence across thread blocks (two passes
+ * with a carried float32 state); with none it runs one pass per channel.
+ */
+size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                int io_dtype);
+
+/*
+ * Extended scan: as ssm_scan_fwd, plus
+ *   init_state      optional (NULL = zeros), (batch, dim, dstate) float32: h_{-1}.
+ *                   Passing the final_state of a call over u[..., :L1] as the
+ *                   init_state of a call over u[..., L1:] gives the same result
+ *                   as one call over the whole sequence (chunk-carried state).
+ *                   May equal final_state (read before it is written).
+ *   workspace       optional device scratch (NULL = none) of workspace_bytes
+ *                   bytes; contents need not be initialised and are not
+ *                   meaningful afterwards.  SSM_ERR_WORKSPACE when non-NULL and
+ *                   smaller than ssm_scan_workspace_bytes().
+ *   stream          cudaStream_t to enqueue on (NULL = legacy default stream).
+ * Concurrent calls must not share a workspace.
+ */
+int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, const float* A,
+                    const float* B, const float* C, const float* D, const void* z,
+                    int delta_softplus, void* y, float* final_state,
+                    int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                    const float* init_state, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * One-token decode: the recurrent mode of the summary page's equation (2)
+ * ("O(N) state update per token", section 4b; the efficiency table of 4c),
+ * applied in place to a stored state, on the legacy default stream.
+ *
+ *   state    required in/out, (batch, dim, dstate) float32: h_{t-1} -> h_t
+ *   u, delta required, (batch, dim) io_dtype; Δ = delta as given (no bias,
+ *            no softplus: the caller passes the step size itself)
+ *   A        required, (dim, dstate);  B, C required, (batch, dstate)
+ *   D        optional (NULL = 0), (dim);  z optional (NULL = no gate), (batch, dim)
+ *   y        required output, (batch, dim) io_dtype
+ */
+int ssm_state_update(float* state, const void* u, const void* delta, const float* A,
+                     const float* B, const float* C, const float* D, const void* z, void* y,
+                     int64_t batch, int64_t dim, int64_t dstate, int io_dtype);
+
+/*
+ * Extended decode step: as ssm_state_update, plus delta_bias (optional, (dim))
+ * and delta_softplus (nonzero: Δ = softplus(delta + bias)), on `stream`.
+ */
+int ssm_state_update_ex(float* state, const void* u, const void* delta, const float* delta_bias,
+                        int delta_softplus, const float* A, const float* B, const float* C,
+                        const float* D, const void* z, void* y,
+                        int64_t batch, int64_t dim, int64_t dstate, int io_dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_H */

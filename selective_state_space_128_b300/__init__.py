@@ -1,0 +1,202 @@
+"""Python binding of libssm, the B300 selective state-space (S6) scan library.
+
+Every entry point of ``include/ssm.h`` has a function of the same name here that
+only marshals arguments (tensor -> device pointer, shape -> sizes, current
+stream) and raises :class:`SSMError` on a non-zero status.  All arithmetic runs
+in the CUDA kernels of ``libssm.so``; there is no CPU path.  PyTorch is used
+only for device memory and streams.
+
+    y, h = scan(u, delta, A, B, C, D, z, delta_bias)          # allocating helper
+    ssm_scan_fwd(u, delta, delta_bias, A, B, C, D, z, True, y, h)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libssm.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "ssm.h")
+
+SSM_F32, SSM_BF16 = 0, 1
+SSM_OK = 0
+SSM_ERR_ARG, SSM_ERR_ALIGN, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_WORKSPACE = -1, -2, -3, -4, -5
+
+_lib = None
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__("%s: %s" % (where, strerror(status)))
+        self.status = status
+
+
+def load():
+    """Load libssm.so (built in-tree by ``python -m selective_state_space_128_b300.build``).
+    Raises if it is missing: there is no fallback implementation."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libssm.so is not built (%s); run `python -m "
+                           "selective_state_space_128_b300.build`" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.ssm_strerror.argtypes = [i32]
+    lib.ssm_strerror.restype = ctypes.c_char_p
+    lib.ssm_version.argtypes = []
+    lib.ssm_version.restype = ctypes.c_char_p
+    lib.ssm_scan_fwd.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32]
+    lib.ssm_scan_fwd.restype = i32
+    lib.ssm_scan_workspace_bytes.argtypes = [i64, i64, i64, i64, i32]
+    lib.ssm_scan_workspace_bytes.restype = sz
+    lib.ssm_scan_fwd_ex.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp, sz, vp]
+    lib.ssm_scan_fwd_ex.restype = i32
+    lib.ssm_state_update.argtypes = [vp] * 9 + [i64, i64, i64, i32]
+    lib.ssm_state_update.restype = i32
+    lib.ssm_state_update_ex.argtypes = [vp, vp, vp, vp, i32] + [vp] * 6 + [i64, i64, i64, i32, vp]
+    lib.ssm_state_update_ex.restype = i32
+    _lib = lib
+    return lib
+
+
+def strerror(status: int) -> str:
+    return load().ssm_strerror(int(status)).decode()
+
+
+def version() -> str:
+    return load().ssm_version().decode()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _io_dtype(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    if t.dtype == torch.float32:
+        return SSM_F32
+    raise TypeError("u/delta/z/y must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is None or isinstance(t, int):
+            continue
+        if not t.is_cuda:
+            raise ValueError("libssm takes device tensors; got a tensor on %s" % t.device)
+        if not t.is_contiguous():
+            raise ValueError("libssm takes contiguous tensors")
+
+
+def _call(name, rc):
+    if rc != SSM_OK:
+        raise SSMError(rc, name)
+
+
+# ---------------------------------------------------------------------------
+# entry points (same names and argument order as include/ssm.h)
+# ---------------------------------------------------------------------------
+
+def ssm_scan_fwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state):
+    """Tensor form of ``ssm_scan_fwd``: sizes come from u (batch, dim, L) and A (dim, N);
+    runs on the legacy default stream like the C entry point."""
+    _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state)
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    rc = load().ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B), _ptr(C),
+                             _ptr(D), _ptr(z), int(bool(delta_softplus)), _ptr(y),
+                             _ptr(final_state), batch, dim, L, N, _io_dtype(u))
+    _call("ssm_scan_fwd", rc)
+
+
+def ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, io_dtype) -> int:
+    return int(load().ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, io_dtype))
+
+
+def ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                    init_state=None, workspace=None, workspace_bytes=None, stream=None):
+    """Tensor form of ``ssm_scan_fwd_ex`` on the current torch stream (or ``stream``)."""
+    _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, workspace)
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    if workspace is not None and workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().ssm_scan_fwd_ex(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
+                                _ptr(C), _ptr(D), _ptr(z), int(bool(delta_softplus)), _ptr(y),
+                                _ptr(final_state), batch, dim, L, N, _io_dtype(u),
+                                _ptr(init_state), _ptr(workspace), int(workspace_bytes or 0),
+                                _stream(stream))
+    _call("ssm_scan_fwd_ex", rc)
+
+
+def ssm_state_update(state, u, delta, A, B, C, D, z, y):
+    """Tensor form of ``ssm_state_update`` (Δ = delta as given), legacy default stream."""
+    _check_dev(state, u, delta, A, B, C, D, z, y)
+    batch, dim = u.shape
+    N = A.shape[1]
+    rc = load().ssm_state_update(_ptr(state), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                 _ptr(D), _ptr(z), _ptr(y), batch, dim, N, _io_dtype(u))
+    _call("ssm_state_update", rc)
+
+
+def ssm_state_update_ex(state, u, delta, delta_bias, delta_softplus, A, B, C, D, z, y,
+                        stream=None):
+    """Tensor form of ``ssm_state_update_ex`` on the current torch stream (or ``stream``)."""
+    _check_dev(state, u, delta, delta_bias, A, B, C, D, z, y)
+    batch, dim = u.shape
+    N = A.shape[1]
+    rc = load().ssm_state_update_ex(_ptr(state), _ptr(u), _ptr(delta), _ptr(delta_bias),
+                                    int(bool(delta_softplus)), _ptr(A), _ptr(B), _ptr(C),
+                                    _ptr(D), _ptr(z), _ptr(y), batch, dim, N, _io_dtype(u),
+                                    _stream(stream))
+    _call("ssm_state_update_ex", rc)
+
+
+# ---------------------------------------------------------------------------
+# allocating helpers (torch allocates; the library computes)
+# ---------------------------------------------------------------------------
+
+def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+         init_state=None, split=True, stream=None):
+    """y, final_state = scan(...): allocates y (dtype of u) and final_state (float32), and a
+    workspace when the plan splits the sequence across blocks."""
+    import torch
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    y = torch.empty_like(u)
+    h = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device)
+    ws = None
+    if split:
+        nbytes = ssm_scan_workspace_bytes(batch, dim, L, N, _io_dtype(u))
+        if nbytes:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=u.device)
+    ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, h, init_state, ws,
+                    stream=stream)
+    return y, h
+
+
+def exported_names():
+    """Entry points declared in include/ssm.h."""
+    import re
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(ssm_\w+)\s*\(", text, re.M)))

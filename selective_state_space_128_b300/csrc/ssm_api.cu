@@ -1,0 +1,166 @@
+// C ABI of libssm: argument checks, planning and dispatch.  See include/ssm.h.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ssm.h"
+#include "ssm_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_n(int64_t n) {
+  return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
+}
+
+// [p, p + bytes) and [q, q + qbytes) intersect (null never does)
+bool overlaps(const void* p, size_t bytes, const void* q, size_t qbytes) {
+  if (!p || !q || bytes == 0 || qbytes == 0) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+  return a < b + qbytes && b < a + bytes;
+}
+
+int sm_count_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+bool sizes_ok(int64_t batch, int64_t dim, int64_t seqlen) {
+  // every flat index must fit in int64 with room to spare
+  if (batch < 0 || dim < 0 || seqlen < 0) return false;
+  if (batch > 65535) return false;  // grid.y
+  const double total = (double)batch * (double)dim * (double)(seqlen > 0 ? seqlen : 1);
+  return total < 9.0e18;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssm_strerror(int status) {
+  switch (status) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_ARG: return "SSM_ERR_ARG: invalid argument";
+    case SSM_ERR_ALIGN: return "SSM_ERR_ALIGN: pointer not 16-byte aligned";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: dstate not in {1,2,4,8,16,32,64}";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA: CUDA launch failed";
+    case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE: workspace too small";
+    default: return "unknown ssm status";
+  }
+}
+
+const char* ssm_version(void) { return "0.1.0"; }
+
+size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                int io_dtype) {
+  if (!supported_n(dstate) || !sizes_ok(batch, dim, seqlen)) return 0;
+  return ssm::scan_plan(batch, dim, seqlen, dstate, io_dtype, sm_count_current(), true)
+      .workspace_bytes;
+}
+
+int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, const float* A,
+                    const float* B, const float* C, const float* D, const void* z,
+                    int delta_softplus, void* y, float* final_state, int64_t batch, int64_t dim,
+                    int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
+  if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
+  const bool work = batch > 0 && dim > 0;
+  if (work && seqlen > 0 && (!u || !delta || !A || !B || !C || !y)) return SSM_ERR_ARG;
+  const void* ptrs[] = {u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
+  const size_t nio = (size_t)batch * (size_t)dim * (size_t)seqlen * esz;
+  const size_t nst = (size_t)batch * (size_t)dim * (size_t)dstate * 4;
+  const size_t nbc = (size_t)batch * (size_t)dstate * (size_t)seqlen * 4;
+  // outputs must not overlap inputs (final_state may equal init_state exactly)
+  const void* ins[] = {u, delta, z};
+  for (const void* q : ins)
+    if (overlaps(y, nio, q, nio)) return SSM_ERR_ARG;
+  if (overlaps(y, nio, B, nbc) || overlaps(y, nio, C, nbc) || overlaps(y, nio, final_state, nst))
+    return SSM_ERR_ARG;
+  if (final_state && init_state && final_state != init_state &&
+      overlaps(final_state, nst, init_state, nst))
+    return SSM_ERR_ARG;
+  for (const void* q : ins)
+    if (overlaps(final_state, nst, q, nio)) return SSM_ERR_ARG;
+  if (!work) return SSM_OK;
+
+  // A split plan reads init_state in every segment while the last segment
+  // writes final_state, so an in-place carry (final_state == init_state)
+  // always runs unsplit.
+  const bool in_place = final_state != nullptr && final_state == init_state;
+  const ssm::ScanPlan plan = ssm::scan_plan(batch, dim, seqlen, dstate, io_dtype,
+                                            sm_count_current(), workspace != nullptr && !in_place);
+  if (workspace && workspace_bytes < plan.workspace_bytes) return SSM_ERR_WORKSPACE;
+
+  ssm::ScanArgs a{};
+  a.u = u; a.delta = delta; a.z = z; a.bias = delta_bias; a.A = A; a.B = B; a.C = C; a.D = D;
+  a.y = y; a.final_state = final_state; a.init_state = init_state;
+  a.batch = batch; a.dim = dim; a.L = seqlen;
+  a.nseg = plan.nseg; a.seg_len = plan.seg_len;
+  a.softplus = delta_softplus != 0;
+  a.vec_io = (seqlen * (int64_t)esz) % 16 == 0;
+  a.vec_bc = (seqlen * 4) % 16 == 0;
+  a.force_precise = io_dtype == SSM_F32;
+  if (plan.nseg > 1) {
+    const size_t rows = (size_t)batch * (size_t)dim;
+    const size_t hbytes = ((size_t)(plan.nseg - 1) * rows * (size_t)dstate * 4 + 255) / 256 * 256;
+    a.carry_h = static_cast<float*>(workspace);
+    a.carry_s = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + hbytes);
+  }
+  const cudaError_t e = ssm::scan_launch(a, dstate, io_dtype, plan, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int ssm_scan_fwd(const void* u, const void* delta, const float* delta_bias, const float* A,
+                 const float* B, const float* C, const float* D, const void* z,
+                 int delta_softplus, void* y, float* final_state, int64_t batch, int64_t dim,
+                 int64_t seqlen, int64_t dstate, int io_dtype) {
+  return ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                         batch, dim, seqlen, dstate, io_dtype, nullptr, nullptr, 0, nullptr);
+}
+
+int ssm_state_update_ex(float* state, const void* u, const void* delta, const float* delta_bias,
+                        int delta_softplus, const float* A, const float* B, const float* C,
+                        const float* D, const void* z, void* y, int64_t batch, int64_t dim,
+                        int64_t dstate, int io_dtype, void* stream) {
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!sizes_ok(batch, dim, 1) || dstate <= 0) return SSM_ERR_ARG;
+  if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
+  if (batch > 0 && dim > 0 && (!state || !u || !delta || !A || !B || !C || !y)) return SSM_ERR_ARG;
+  const void* ptrs[] = {state, u, delta, delta_bias, A, B, C, D, z, y};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
+  const size_t nio = (size_t)batch * (size_t)dim * esz;
+  const size_t nst = (size_t)batch * (size_t)dim * (size_t)dstate * 4;
+  const void* ins[] = {u, delta, z, B, C, A};
+  for (const void* q : ins)
+    if (overlaps(state, nst, q, q == A ? (size_t)dim * dstate * 4 : nio)) return SSM_ERR_ARG;
+  if (overlaps(y, nio, state, nst) || overlaps(y, nio, u, nio) || overlaps(y, nio, delta, nio) ||
+      overlaps(y, nio, z, nio))
+    return SSM_ERR_ARG;
+  if (batch == 0 || dim == 0) return SSM_OK;
+  ssm::UpdateArgs a{};
+  a.state = state; a.u = u; a.delta = delta; a.z = z; a.bias = delta_bias; a.A = A; a.B = B;
+  a.C = C; a.D = D; a.y = y; a.batch = batch; a.dim = dim;
+  a.softplus = delta_softplus != 0;
+  a.force_precise = io_dtype == SSM_F32;
+  const cudaError_t e = ssm::update_launch(a, dstate, io_dtype, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int ssm_state_update(float* state, const void* u, const void* delta, const float* A,
+                     const float* B, const float* C, const float* D, const void* z, void* y,
+                     int64_t batch, int64_t dim, int64_t dstate, int io_dtype) {
+  return ssm_state_update_ex(state, u, delta, nullptr, 0, A, B, C, D, z, y, batch, dim, dstate,
+                             io_dtype, nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// Device helpers shared by the scan and decode kernels: element I/O for
+// float32 / bfloat16, the two arithmetic flavours (fast: MUFU ex2 and packed
+// f32x2 math; precise: CUDA libm), and packed-pair arithmetic in inline PTX.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace ssm {
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
+// Element I/O. bfloat16 <-> float conversions are exact widening / RNE narrowing.
+// ---------------------------------------------------------------------------
+template <typename IO> struct io_traits;
+template <> struct io_traits<float> {
+  static constexpr int kBytes = 4;
+  __device__ static float to_f32(float v) { return v; }
+  __device__ static float from_f32(float v) { return v; }
+};
+template <> struct io_traits<__nv_bfloat16> {
+  static constexpr int kBytes = 2;
+  __device__ static float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+  __device__ static __nv_bfloat16 from_f32(float v) { return __float2bfloat16_rn(v); }
+};
+
+// ---------------------------------------------------------------------------
+// Packed pairs (two fp32 lanes in one 64-bit register): one instruction issue
+// for two FP32 operations on sm_100-class SMs.
+// ---------------------------------------------------------------------------
+struct f2 {
+  unsigned long long r;
+};
+
+__device__ __forceinline__ f2 pack2(float lo, float hi) {
+  f2 v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v.r) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ void unpack2(f2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v.r));
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.r) : "l"(a.r), "l"(b.r));
+  return d;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.r) : "l"(a.r), "l"(b.r));
+  return d;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d.r) : "l"(a.r), "l"(b.r));
+  return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.r) : "l"(a.r), "l"(b.r), "l"(c.r));
+  return d;
+}
+
+// ---------------------------------------------------------------------------
+// Fast transcendental pieces (MUFU). ex2.approx.ftz: relative error ~2^-22.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_fast(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_fast(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// softplus(x) = log(1 + e^x).
+// Fast flavour: e = 2^(x log2 e) on the MUFU; for x < -4 (e < 0.0184) the
+// alternating series e - e^2/2 + e^3/3 - e^4/4 (truncation < e^5/5, relative
+// < 4e-10) avoids the rounding of 1 + e; for -4 <= x <= 15 it is
+// ln2 * log2(1 + e) (relative error below ~1e-5, from lg2.approx's absolute
+// error over log2(1+e) >= 0.026); above 15 it returns x (error < 3e-7).
+__device__ __forceinline__ float softplus_fast(float x) {
+  float e = ex2_fast(x * kLog2e);
+  float series = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 1.0f / 3.0f), -0.5f), 1.0f);
+  float logv = kLn2 * lg2_fast(1.0f + e);
+  float r = x < -4.0f ? series : logv;
+  return x > 15.0f ? x : r;
+}
+// Precise flavour: CUDA libm, both branches free of overflow and cancellation.
+__device__ __forceinline__ float softplus_precise(float x) {
+  return x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+}
+
+// silu(z) = z * sigmoid(z)
+__device__ __forceinline__ float silu_fast(float z) {
+  return z * rcp_fast(1.0f + ex2_fast(-z * kLog2e));
+}
+__device__ __forceinline__ float silu_precise(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace ssm
