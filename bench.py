@@ -1,0 +1,492 @@
+"""Benchmark of the selective-scan hot path on B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-decode]
+
+A step is one ssm_scan_fwd over the Mamba-130M-shaped layer workload (batch 8,
+d_inner 1536, L 2048, N 16, bf16 u/Δ/z/y, fp32 A/B/C/D/bias, seed 1) with inputs
+resident in HBM.  Two copies of the inputs alternate between steps, so a step
+never reads data the previous step left in L2 (each copy, 204 MB, is larger
+than the 126 MB L2).  The same line reports the one-token decode step
+(batch 256, d_inner 5120, N 16) with an L2 flush between steps, an end-to-end
+figure through the C ABI with host buffers, the oracle's CPU throughput, the
+roofline of the scan kernel and the SM clocks sampled during the timed region.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (the scan
+shards by batch and channel with no exchange: weak scaling); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "scan HBM GB/s (% of B300 peak) & channel-steps/s; decode tokens/s"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def scan_bytes(w) -> int:
+    """Algorithmic HBM bytes of one scan: u, Δ, z read and y written once (io dtype),
+    B and C read once, A/D/bias read, final state written."""
+    e = 4 if w.io == "f32" else 2
+    chsteps = w.batch * w.dim * w.seqlen
+    return (4 * e * chsteps + 2 * 4 * w.batch * w.dstate * w.seqlen
+            + 4 * (w.dim * w.dstate + 2 * w.dim) + 4 * w.batch * w.dim * w.dstate)
+
+
+def decode_bytes(batch, dim, N, e=2) -> int:
+    """Algorithmic HBM bytes of one decode step: state read + written, u/Δ/z read,
+    y written, B/C read, A/D/bias read."""
+    return (2 * 4 * batch * dim * N + 4 * e * batch * dim + 2 * 4 * batch * N
+            + 4 * (dim * N + 2 * dim))
+
+
+def fp32_ops_per_channel_step(N: int) -> int:
+    """FP32 operations the method needs per channel step, counted per state n:
+    Δ·A, B·u, scaling by 1/A, the state update (add + fma) and the C·h readout."""
+    return 6 * N
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk.get("sm_max_mhz", 2032.0)), "measured"
+    except Exception:
+        return 6400.0, 2032.0, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "selective_state_space_128_b300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None when
+    the summary is missing or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        ent = rec[kernel]
+        if ent.get("csrc_hash") != csrc_hash():
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0=None, t1=None):
+        """Summary of the samples read between host times t0 and t1 (all if None)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, ln in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1 + 0.06):
+                continue
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (torchrun: one process per GPU)
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# scan: device-resident throughput and end to end
+# ---------------------------------------------------------------------------
+
+def pinned(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+    return t.pin_memory()
+
+
+def to_dev(t_host, io_bf16=False):
+    import torch
+    d = t_host.to("cuda", non_blocking=True)
+    return d.view(torch.bfloat16) if io_bf16 else d
+
+
+def bench_scan(w, steps, warmup, world):
+    import torch
+    import selective_state_space_128_b300 as ssm
+    x = synth.make_scan_inputs(w)
+    bf = w.io == "bf16"
+    host = {k: pinned(v) for k, v in x.items()}
+    sets = []
+    for _ in range(2):
+        g = {k: to_dev(host[k], bf and k in ("u", "delta", "z")) for k in host}
+        g["y"] = torch.empty_like(g["u"])
+        g["h"] = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device="cuda")
+        sets.append(g)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(g):
+        ssm.ssm_scan_fwd_ex(g["u"], g["delta"], g["delta_bias"], g["A"], g["B"], g["C"], g["D"],
+                            g["z"], True, g["y"], g["h"], stream=stream)
+
+    for i in range(warmup):
+        step(sets[i % 2])
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0.record(stream)
+    for i in range(steps):
+        step(sets[i % 2])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    ck = clocks.stop(t0, t1)
+    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(world, ms)
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs,
+    # the scan, D2H of y and the final state, every step
+    e2e_steps = max(3, min(steps, 20))
+    g = sets[0]
+    yh = torch.empty(g["y"].shape, dtype=torch.int16 if bf else torch.float32).pin_memory()
+    hh = torch.empty(g["h"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in host)
+    d2h = yh.numel() * yh.element_size() + hh.numel() * hh.element_size()
+
+    def e2e_step():
+        for k in host:
+            dst = g[k].view(torch.int16) if (bf and k in ("u", "delta", "z")) else g[k]
+            dst.copy_(host[k], non_blocking=True)
+        step(g)
+        yh.copy_(g["y"].view(torch.int16) if bf else g["y"], non_blocking=True)
+        hh.copy_(g["h"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(world, f0.elapsed_time(f1))
+    return dict(ms=ms, clocks=ck, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h)
+
+
+# ---------------------------------------------------------------------------
+# decode: batch 256, d_inner 5120, N 16, one token per step
+# ---------------------------------------------------------------------------
+
+def bench_decode(dw, steps, world):
+    """Per-step time of ssm_state_update_ex with an L2 flush between steps (the 84 MB
+    state would otherwise stay in the 126 MB L2 across steps).  Inputs are drawn on the
+    device (seeded torch generator, the workload's distributions); the state starts from
+    a GPU scan over a 256-step prefill."""
+    import torch
+    import selective_state_space_128_b300 as ssm
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(dw.seed)
+    B_, D_, N = dw.batch, dw.dim, dw.dstate
+    A = torch.from_numpy(synth.gen_A(D_, N)).cuda()
+    Dp = torch.from_numpy(synth.fill(dw.seed, synth.S_D, 0, D_, synth.UNIFORM, 0.5, 1.5)).cuda()
+    bias = torch.from_numpy(synth.gen_delta_bias(dw.seed, D_)).cuda()
+    Lp = dw.prefill_len
+    bf = torch.bfloat16
+    pu = torch.randn((B_, D_, Lp), generator=gen, device="cuda").to(bf)
+    pd = (0.5 * torch.randn((B_, D_, Lp), generator=gen, device="cuda")).to(bf)
+    pz = torch.randn((B_, D_, Lp), generator=gen, device="cuda").to(bf)
+    pB = torch.randn((B_, N, Lp), generator=gen, device="cuda")
+    pC = torch.randn((B_, N, Lp), generator=gen, device="cuda")
+    _, state = ssm.scan(pu, pd, A, pB, pC, Dp, pz, bias)
+    del pu, pd, pz, pB, pC
+    u = torch.randn((steps, B_, D_), generator=gen, device="cuda").to(bf)
+    dl = (0.5 * torch.randn((steps, B_, D_), generator=gen, device="cuda")).to(bf)
+    z = torch.randn((steps, B_, D_), generator=gen, device="cuda").to(bf)
+    Bs = torch.randn((steps, B_, N), generator=gen, device="cuda")
+    Cs = torch.randn((steps, B_, N), generator=gen, device="cuda")
+    y = torch.empty((steps, B_, D_), dtype=bf, device="cuda")
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        ssm.ssm_state_update_ex(state, u[i], dl[i], bias, True, A, Bs[i], Cs[i], Dp, z[i], y[i],
+                                stream=stream)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = max_over_ranks(world, sum(per) / len(per))
+    # back to back, no flush (the state partly stays in L2): context only
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for i in range(steps):
+        step(i)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    b2b_ms = max_over_ranks(world, g0.elapsed_time(g1)) / steps
+    return dict(step_ms=mean_ms, b2b_ms=b2b_ms, steps=steps)
+
+
+# ---------------------------------------------------------------------------
+# the oracle as CPU baseline / reference arm
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, channels, nthreads=0):
+    """Run the fp64 oracle on batch 0, channels [0, channels) of workload w; returns
+    (seconds, sample workload)."""
+    import oracle
+    sw = synth.scaled(w, batch=1, dim=channels)
+    u = synth.gen_rows(w, "u", 0, 0, channels)
+    dl = synth.gen_rows(w, "delta", 0, 0, channels)
+    z = synth.gen_rows(w, "z", 0, 0, channels)
+    B = synth.gen_bc(synth.scaled(w, batch=1), "B")
+    C = synth.gen_bc(synth.scaled(w, batch=1), "C")
+    A = synth.gen_A(w.dim, w.dstate)
+    D = synth.gen_D(w)
+    bias = synth.gen_delta_bias(w.seed, w.dim)
+    t = time.perf_counter()
+    oracle.scan_rows(u, dl, z, np.zeros(channels, np.int64), np.arange(channels), A, B, C, D, bias,
+                     True, None, 1, nthreads)
+    return time.perf_counter() - t, sw
+
+
+def cpu_baseline(w):
+    import oracle
+    channels = min(w.dim, 1536)
+    secs, sw = oracle_sample(w, channels)
+    cs = sw.channel_steps / secs
+    return {"value": scan_bytes(sw) / secs / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "channel_steps_per_s": cs,
+            "sample": "batch 0, channels 0..%d of the workload (%d channel-steps, %.1f s wall)"
+                      % (channels - 1, sw.channel_steps, secs)}
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 oracle as it stands, on the host cores."""
+    import oracle
+    secs, _ = oracle_sample(w, 32)
+    per_ch = secs / 32
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    ch = int(max(8, min(w.dim, budget / per_ch)))
+    for _ in range(args.warmup):
+        oracle_sample(w, ch)
+    tot = 0.0
+    sw = None
+    for _ in range(args.steps):
+        s, sw = oracle_sample(w, ch)
+        tot += s
+    ms = tot / args.steps * 1e3
+    value = scan_bytes(sw) / (tot / args.steps) / 1e9
+    cpu = {"value": value, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+           "sample": "each step: batch 0, channels 0..%d of the workload" % (ch - 1)}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w), "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "channel_steps_per_s": sw.channel_steps / (tot / args.steps)}
+    print(json.dumps(line))
+
+
+def workload_config(w):
+    return {"workload": w.name, "batch": w.batch, "d_inner": w.dim, "seqlen": w.seqlen,
+            "dstate": w.dstate, "io_dtype": w.io, "state_dtype": "f32", "seed": w.seed,
+            "l2": "inputs larger than L2 (%.0f MB per copy > 126 MB), two copies alternated"
+                  % (scan_bytes(w) / 1e6)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = synth.MAMBA_130M
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+    import torch
+    torch.cuda.set_device(local)
+    import selective_state_space_128_b300 as ssm
+    ssm.load()
+    hbm_peak, sm_max, peak_kind = load_peaks()
+
+    r = bench_scan(w, args.steps, args.warmup, world)
+    dec = None if args.no_decode else bench_decode(synth.DECODE, args.decode_steps, world)
+    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank != 0:
+        return
+
+    step_s = r["ms"] / 1e3 / args.steps
+    nbytes = scan_bytes(w)
+    gbs_rank = nbytes / step_s / 1e9
+    value = gbs_rank * world
+    chsteps = w.channel_steps / step_s * world
+    ops = fp32_ops_per_channel_step(w.dstate) * w.channel_steps
+    alu_peak = 148 * 128 * sm_max * 1e6 / 1e12          # FP32 lanes x max SM clock, TOP/s
+    alu_ach = ops / step_s / 1e12
+    traffic = profiled_traffic("scan_kernel")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w),
+        "channel_steps_per_s": chsteps,
+        "hbm": {"achieved_gbs": gbs_rank, "peak_gbs": hbm_peak, "frac": gbs_rank / hbm_peak,
+                "peak_kind": peak_kind, "frac_of_8000_nominal": gbs_rank / 8000.0,
+                "bytes_per_step": nbytes},
+        "roofline": {"bound": "alu", "achieved": alu_ach, "peak": alu_peak, "unit": "TOP/s",
+                     "frac": alu_ach / alu_peak, "traffic": traffic,
+                     "kernel": "scan_kernel<bf16,16,0>",
+                     "ops_per_launch": ops,
+                     "peak_basis": "148 SMs x 128 FP32 lanes x %.0f MHz (max SM clock)" % sm_max,
+                     "hbm_frac": gbs_rank / hbm_peak},
+        "e2e": {"value": nbytes * r["e2e_steps"] / (r["e2e_ms"] / 1e3) / 1e9 * world,
+                "unit": "GB/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "steps": r["e2e_steps"]},
+        "gpu_launches": args.steps,
+        "clocks": r["clocks"],
+    }
+    if dec is not None:
+        db = decode_bytes(synth.DECODE.batch, synth.DECODE.dim, synth.DECODE.dstate)
+        st = dec["step_ms"] / 1e3
+        line["decode"] = {"workload": synth.DECODE.name, "steps": dec["steps"],
+                          "us_per_step": dec["step_ms"] * 1e3,
+                          "tokens_per_s": synth.DECODE.batch / st * world,
+                          "hbm_gbs": db / st / 1e9, "hbm_frac": db / st / 1e9 / hbm_peak,
+                          "bytes_per_step": db, "l2": "flushed (256 MB write) before every step",
+                          "us_per_step_back_to_back": dec["b2b_ms"] * 1e3,
+                          "gpu_launches": 2 * dec["steps"]}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
