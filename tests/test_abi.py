@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/ssm.h declares, and rejects bad arguments synchronously (before any CUDA
+call) with the documented status codes.  Pointers here are fake addresses that
+are never dereferenced."""
+import pytest
+
+import selective_state_space_128_b300 as ssm
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def lib():
+    return ssm.load()
+
+
+def test_exports_every_declared_symbol():
+    names = ssm.exported_names()
+    assert {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_state_update", "ssm_state_update_ex",
+            "ssm_scan_workspace_bytes", "ssm_strerror", "ssm_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib(), n), n
+
+
+def test_strerror_and_version():
+    assert ssm.version() == "0.1.0"
+    for code in (0, -1, -2, -3, -4, -5):
+        assert ssm.strerror(code).startswith("SSM_")
+    assert "unknown" in ssm.strerror(42)
+
+
+def _scan(**kw):
+    a = dict(u=FAKE, delta=FAKE + 0x1000000, bias=None, A=FAKE + 0x2000000, B=FAKE + 0x3000000,
+             C=FAKE + 0x4000000, D=None, z=None, softplus=1, y=FAKE + 0x5000000, h=None,
+             batch=2, dim=64, L=128, N=16, io=ssm.SSM_BF16, init=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib().ssm_scan_fwd_ex(a["u"], a["delta"], a["bias"], a["A"], a["B"], a["C"], a["D"],
+                                 a["z"], a["softplus"], a["y"], a["h"], a["batch"], a["dim"],
+                                 a["L"], a["N"], a["io"], a["init"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_scan_argument_errors():
+    assert _scan(u=None) == ssm.SSM_ERR_ARG
+    assert _scan(y=None) == ssm.SSM_ERR_ARG
+    assert _scan(A=None) == ssm.SSM_ERR_ARG
+    assert _scan(io=7) == ssm.SSM_ERR_ARG
+    assert _scan(batch=-1) == ssm.SSM_ERR_ARG
+    assert _scan(L=-5) == ssm.SSM_ERR_ARG
+    assert _scan(N=0) == ssm.SSM_ERR_ARG
+    assert _scan(batch=70000) == ssm.SSM_ERR_ARG
+    for n in (3, 5, 12, 128):
+        assert _scan(N=n) == ssm.SSM_ERR_UNSUPPORTED
+    assert _scan(u=FAKE + 2) == ssm.SSM_ERR_ALIGN
+    assert _scan(z=FAKE + 0x6000008) == ssm.SSM_ERR_ALIGN
+    assert _scan(h=FAKE + 0x7000004) == ssm.SSM_ERR_ALIGN
+    # y overlapping an input
+    assert _scan(y=FAKE + 0x100) == ssm.SSM_ERR_ARG
+    # final_state overlapping init_state without being the same buffer
+    assert _scan(h=FAKE + 0x8000000, init=FAKE + 0x8000010) == ssm.SSM_ERR_ARG
+    # empty problems succeed without touching the device
+    assert _scan(batch=0) == ssm.SSM_OK
+    assert _scan(dim=0) == ssm.SSM_OK
+
+
+def test_workspace_too_small_is_rejected_before_launch():
+    need = ssm.ssm_scan_workspace_bytes(1, 64, 1 << 16, 16, ssm.SSM_BF16)
+    assert need > 0
+    rc = _scan(batch=1, dim=64, L=1 << 16, ws=FAKE + 0x9000000, wsb=need - 16)
+    assert rc == ssm.SSM_ERR_WORKSPACE
+
+
+def test_workspace_plan():
+    # many channels: one pass, no workspace
+    assert ssm.ssm_scan_workspace_bytes(8, 1536, 2048, 16, 1) == 0
+    assert ssm.ssm_scan_workspace_bytes(4, 5120, 4096, 16, 1) == 0
+    # few channels, long sequence: split with carry records
+    assert ssm.ssm_scan_workspace_bytes(1, 1536, 65536, 16, 1) > 0
+    assert ssm.ssm_scan_workspace_bytes(1, 64, 100, 16, 1) == 0   # too short to split
+    assert ssm.ssm_scan_workspace_bytes(1, 64, 100, 3, 1) == 0    # unsupported N
+
+
+def _upd(**kw):
+    a = dict(state=FAKE, u=FAKE + 0x1000000, delta=FAKE + 0x2000000, bias=None, softplus=1,
+             A=FAKE + 0x3000000, B=FAKE + 0x4000000, C=FAKE + 0x5000000, D=None, z=None,
+             y=FAKE + 0x6000000, batch=4, dim=64, N=16, io=ssm.SSM_BF16, stream=None)
+    a.update(kw)
+    return lib().ssm_state_update_ex(a["state"], a["u"], a["delta"], a["bias"], a["softplus"],
+                                     a["A"], a["B"], a["C"], a["D"], a["z"], a["y"], a["batch"],
+                                     a["dim"], a["N"], a["io"], a["stream"])
+
+
+def test_update_argument_errors():
+    assert _upd(state=None) == ssm.SSM_ERR_ARG
+    assert _upd(io=2) == ssm.SSM_ERR_ARG
+    assert _upd(N=24) == ssm.SSM_ERR_UNSUPPORTED
+    assert _upd(y=FAKE + 0x6000002) == ssm.SSM_ERR_ALIGN
+    assert _upd(y=FAKE + 0x10) == ssm.SSM_ERR_ARG           # y overlaps the state
+    assert _upd(u=FAKE + 0x40) == ssm.SSM_ERR_ARG           # state overlaps u
+    assert _upd(batch=0) == ssm.SSM_OK
+
+
+def test_short_forms_validate_too():
+    L = lib()
+    rc = L.ssm_scan_fwd(None, FAKE, None, FAKE, FAKE, FAKE, None, None, 1, FAKE, None,
+                        1, 1, 1, 16, 1)
+    assert rc == ssm.SSM_ERR_ARG
+    rc = L.ssm_state_update(FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000,
+                            FAKE + 0x400000, FAKE + 0x500000, None, None, FAKE + 0x600000,
+                            1, 1, 7, 1)
+    assert rc == ssm.SSM_ERR_UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(ssm, "_lib", None)
+    monkeypatch.setattr(ssm, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        ssm.load()
