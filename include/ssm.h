@@ -144,6 +144,43 @@ int ssm_state_update_ex(float* state, const void* u, const void* delta, const fl
                         const float* D, const void* z, void* y,
                         int64_t batch, int64_t dim, int64_t dstate, int io_dtype, void* stream);
 
+/*
+ * Scan without any device allocation by the caller or the library.
+ *
+ * The paper has no counterpart; this is a deployment aid.  Some callers
+ * cannot call cudaMalloc where they run the scan (a process whose device
+ * memory is all owned by its own pool, a plug-in host that forbids
+ * allocation after start-up, a real-time loop that must not block on the
+ * allocator), so they cannot provide the workspace that ssm_scan_fwd_ex uses
+ * to split long sequences across blocks.  This entry point takes that
+ * scratch from a fixed array of SSM_STATIC_SCRATCH_BYTES compiled into the
+ * library; every GPU that loads the library holds the array until the
+ * process exits.  The caller still passes all inputs and outputs.
+ *
+ * Arguments, layouts and results are those of ssm_scan_fwd_ex (no workspace
+ * arguments).  Returns SSM_ERR_WORKSPACE when the plan for these sizes needs
+ * more than SSM_STATIC_SCRATCH_BYTES of scratch (ssm_scan_workspace_bytes()
+ * tells in advance); argument errors as ssm_scan_fwd_ex.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the device current) and caches it; make
+ * that first call before any stream capture.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * All calls on a device share the one array, which keeps whatever the last
+ * call left in it (every carry record a call reads is written earlier by the
+ * same call, so nothing needs clearing).  Calls that can overlap on the GPU
+ * (different streams without an ordering between them) race on the array:
+ * order them, e.g. on one stream.
+ */
+#define SSM_STATIC_SCRATCH_BYTES (2u << 20) /* 2 MiB */
+
+int ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* delta_bias,
+                         const float* A, const float* B, const float* C, const float* D,
+                         const void* z, int delta_softplus, void* y, float* final_state,
+                         int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                         int io_dtype, const float* init_state, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

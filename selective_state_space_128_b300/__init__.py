@@ -56,6 +56,8 @@ def load():
     lib.ssm_state_update.restype = i32
     lib.ssm_state_update_ex.argtypes = [vp, vp, vp, vp, i32] + [vp] * 6 + [i64, i64, i64, i32, vp]
     lib.ssm_state_update_ex.restype = i32
+    lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp]
+    lib.ssm_scan_fwd_noalloc.restype = i32
     _lib = lib
     return lib
 
@@ -170,6 +172,29 @@ def ssm_state_update_ex(state, u, delta, delta_bias, delta_softplus, A, B, C, D,
                                     _ptr(D), _ptr(z), _ptr(y), batch, dim, N, _io_dtype(u),
                                     _stream(stream))
     _call("ssm_state_update_ex", rc)
+
+
+def ssm_scan_fwd_noalloc(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                         init_state=None, stream=None):
+    """Tensor form of ``ssm_scan_fwd_noalloc``: as ``ssm_scan_fwd_ex`` without a workspace;
+    the library's fixed scratch array (SSM_STATIC_SCRATCH_BYTES per GPU) stands in for it,
+    for callers that cannot allocate device memory.  Calls that may overlap on the GPU
+    share that array and must be ordered (e.g. issued on one stream)."""
+    _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state)
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    rc = load().ssm_scan_fwd_noalloc(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
+                                     _ptr(C), _ptr(D), _ptr(z), int(bool(delta_softplus)),
+                                     _ptr(y), _ptr(final_state), batch, dim, L, N,
+                                     _io_dtype(u), _ptr(init_state), _stream(stream))
+    _call("ssm_scan_fwd_noalloc", rc)
+
+
+def static_scratch_bytes() -> int:
+    """SSM_STATIC_SCRATCH_BYTES as defined in include/ssm.h."""
+    import re
+    m = re.search(r"#define\s+SSM_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", open(HEADER).read())
+    return int(m.group(1)) << int(m.group(2))
 
 
 # ---------------------------------------------------------------------------
