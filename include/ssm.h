@@ -59,6 +59,7 @@ extern "C" {
 #define SSM_ERR_UNSUPPORTED (-3) /* dstate not in {1, 2, 4, 8, 16, 32, 64} */
 #define SSM_ERR_CUDA (-4)        /* a CUDA call or kernel launch failed */
 #define SSM_ERR_WORKSPACE (-5)   /* workspace given but too small */
+#define SSM_ERR_TIMEOUT (-6)     /* a kernel gave up waiting for its own data (see ssm_status) */
 
 /* Human-readable name of a status code (static string). */
 const char* ssm_strerror(int status);
@@ -118,6 +119,18 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
                     int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                     const float* init_state, void* workspace, size_t workspace_bytes,
                     void* stream);
+
+/*
+ * Device-side status of the scans enqueued so far on this device.
+ *
+ * Synchronises `stream` (NULL = legacy default stream), then reads and clears
+ * the library's device error word.  Returns SSM_OK, SSM_ERR_TIMEOUT when a
+ * scan block gave up waiting for one of its own chunk copies (the block then
+ * left its outputs unwritten; the CUDA context stays usable), or SSM_ERR_CUDA
+ * when the synchronisation itself failed.  The pages have no counterpart:
+ * this is the library's failure report.
+ */
+int ssm_status(void* stream);
 
 /*
  * One-token decode: the recurrent mode of the summary page's equation (2)

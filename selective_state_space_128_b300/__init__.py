@@ -21,6 +21,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "ssm.h")
 SSM_F32, SSM_BF16 = 0, 1
 SSM_OK = 0
 SSM_ERR_ARG, SSM_ERR_ALIGN, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_WORKSPACE = -1, -2, -3, -4, -5
+SSM_ERR_TIMEOUT = -6
 
 _lib = None
 
@@ -58,6 +59,8 @@ def load():
     lib.ssm_state_update_ex.restype = i32
     lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp]
     lib.ssm_scan_fwd_noalloc.restype = i32
+    lib.ssm_status.argtypes = [vp]
+    lib.ssm_status.restype = i32
     _lib = lib
     return lib
 
@@ -149,6 +152,12 @@ def ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, fina
                                 _ptr(init_state), _ptr(workspace), int(workspace_bytes or 0),
                                 _stream(stream))
     _call("ssm_scan_fwd_ex", rc)
+
+
+def ssm_status(stream=None) -> int:
+    """Synchronise the stream and return the library's device-side status
+    (SSM_OK or SSM_ERR_TIMEOUT), clearing it."""
+    return int(load().ssm_status(_stream(stream)))
 
 
 def ssm_state_update(state, u, delta, A, B, C, D, z, y):

@@ -48,6 +48,7 @@ const char* ssm_strerror(int status) {
     case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: dstate not in {1,2,4,8,16,32,64}";
     case SSM_ERR_CUDA: return "SSM_ERR_CUDA: CUDA launch failed";
     case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE: workspace too small";
+    case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT: a kernel gave up waiting for its data";
     default: return "unknown ssm status";
   }
 }
@@ -116,6 +117,13 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
   }
   const cudaError_t e = ssm::scan_launch(a, dstate, io_dtype, plan, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int ssm_status(void* stream) {
+  int code = 0;
+  if (ssm::scan_device_error(&code, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  return code == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
 }
 
 int ssm_scan_fwd(const void* u, const void* delta, const float* delta_bias, const float* A,

@@ -34,6 +34,7 @@ struct ScanArgs {
   int vec_io;       // rows of u/delta/z/y are 16-byte aligned
   int vec_bc;       // rows of B/C are 16-byte aligned
   int force_precise;
+  int use_tma;      // set by the launcher: chunks staged by TMA
 };
 
 struct ScanPlan {
@@ -67,6 +68,10 @@ struct UpdateArgs {
   int softplus;
   int force_precise;
 };
+
+// Synchronises `stream`, then reads and clears the scan kernels' device error
+// word (0 = none, 1 = a TMA wait timed out).
+cudaError_t scan_device_error(int* code, cudaStream_t stream);
 
 cudaError_t update_launch(const UpdateArgs& a, int64_t N, int io_dtype, cudaStream_t stream);
 

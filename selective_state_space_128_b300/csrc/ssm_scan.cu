@@ -7,181 +7,255 @@
 // (2), (4) and Algorithm 2; section 4a shape table for the gate; the SSM/Mamba
 // chapter's section 3.1 for D).
 //
-// Design (B300): a block owns CH channels of one batch row and walks the
-// sequence in chunks of T steps.  Chunk tiles of u/Δ/z (bf16 or fp32) and of
-// B/C (fp32, shared by all channels of the block) are staged into shared
-// memory with cp.async (double-buffered), then a cooperative "prep" pass turns
-// them into fp32 tiles of Δ (softplus applied once per element), u and the
-// gate silu(z), and transposes B/C to [t][n].  Each channel is handled by G
-// lanes holding NPT = N/G states each in registers; the state is carried in
-// fp32 registers across chunks and the expanded (L, N) state never leaves the
-// SM.  Per step and state the fast path costs one MUFU ex2 and six FP32
-// operations issued as packed f32x2 pairs; the G partial readouts of a channel
-// are combined by a shuffle reduce-scatter so that each lane finishes one time
-// step of the block (D term, gate, bf16 rounding), staged to shared memory and
-// written back with 16-byte stores.
+// Design (B300).  The work is bound by the SM's FP32 pipe, not by HBM: per
+// channel step it moves 8 bytes (bf16 u, Δ, z in, y out) but needs N
+// exponentials and about 6N FP32 operations.  So the kernel is organised to
+// spend as few issue slots as possible per state update:
+//
+//  * a block owns CH channels of one batch row; each channel is handled by G
+//    lanes holding NPT = N/G states each in fp32 registers for the whole
+//    sequence (the expanded (L, N) state never leaves the SM);
+//  * chunks of T steps of u/Δ/z (a CH x T box) and of B/C (an N x T box,
+//    shared by all channels of the block) are fetched by TMA
+//    (cp.async.bulk.tensor, mbarrier completion) into a ring of raw stages,
+//    prefetched S chunks ahead;
+//  * a cooperative "prep" pass turns a raw stage into fp32 working tiles once
+//    per channel step -- Δ (softplus applied once, not once per lane), u, the
+//    gate silu(z) -- and transposes B/C to [t][n], so that every lane reads
+//    (Δ, Δ, u, u) and its NPT values of B and C with 16-byte shared loads that
+//    land directly in packed register pairs;
+//  * the state update runs on packed f32x2 pairs (one issue for two lanes of
+//    FP32 work) with one MUFU ex2 per state: Ā = 2^(Δ·A·log2 e),
+//    v = -B u / A, h = Ā (h - v) + v, which equals Ā h + (Ā - 1)/A · B u;
+//  * the G partial readouts of a channel are combined by a shuffle
+//    reduce-scatter, after which lane g finishes time step g of each group of
+//    G steps (D term, gate, rounding) into a y tile that the block writes back
+//    with 16-byte stores.
 //
 // Long sequences with few channels are split into segments (grid.z): pass 1
 // computes each segment's end state from zero and its ΣΔ, pass 0 folds the
 // carries of earlier segments (h <- exp(A ΣΔ_k) h + h_k) into its initial state
 // and recomputes its segment with outputs.  There is no inter-block waiting.
-#include <cuda_pipeline_primitives.h>
+// The only waits are on the block's own TMA barriers; they give up after a
+// time limit, record it in a device error word (read by ssm_status) and end the block.
+#include <cuda.h>
+
+#include <cstring>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
 namespace ssm {
 
+// Device-side error word (0 = none).  Read and cleared by scan_device_error().
+__device__ int g_scan_error;
+
 // Per-N tiling: NPT states per lane, G lanes per channel, CH channels per
-// block, T steps per chunk.
+// block, T steps per chunk, S raw stages in flight.
 template <int N> struct ScanCfg {
   static constexpr int NPT = N <= 4 ? N : (N <= 16 ? 4 : N / 4);
   static constexpr int G = N / NPT;
   static constexpr int CH = kScanThreads / G;
-  static constexpr int T = (2048 / CH) < 64 ? (2048 / CH) : 64;
+  static constexpr int T = 32;
+  static constexpr int S = 2;
   static_assert(G * NPT == N, "tiling");
   static_assert(T % G == 0 && T % 8 == 0, "chunk");
 };
 
-constexpr int kPadF = 4;  // fp32 tile row padding (floats)
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Shared-memory layout of one block.  Raw stages are TMA destinations
+// (128-byte aligned); the working tiles are padded so that the lanes of a warp
+// hit distinct banks.
 template <typename IO, int N> struct ScanSmem {
   using Cf = ScanCfg<N>;
-  static constexpr int CH = Cf::CH, T = Cf::T;
-  static constexpr int RowF = T + kPadF;            // fp32 tile row stride
-  static constexpr int RowY = T + 16 / sizeof(IO);  // y tile row stride (elements)
-  static constexpr int RowBC = N + 4;               // transposed B/C row stride
-  // raw stage (one of two)
-  static constexpr size_t kRawIO = (size_t)CH * T * sizeof(IO);
-  static constexpr size_t kRawBC = (size_t)N * T * sizeof(float);
-  static constexpr size_t kStage = 3 * kRawIO + 2 * kRawBC;
-  static constexpr size_t oStage0 = 0;
-  static constexpr size_t oStage1 = kStage;
-  static constexpr size_t oDt = 2 * kStage;
-  static constexpr size_t oU = oDt + (size_t)CH * RowF * 4;
-  static constexpr size_t oG = oU + (size_t)CH * RowF * 4;
-  static constexpr size_t oB = oG + (size_t)CH * RowF * 4;
-  static constexpr size_t oC = oB + (size_t)T * RowBC * 4;
-  static constexpr size_t oY = oC + (size_t)T * RowBC * 4;
-  static constexpr size_t oBias = oY + (((size_t)CH * RowY * sizeof(IO) + 15) / 16) * 16;
-  static constexpr size_t kBytes = oBias + (size_t)CH * 4;
-  static_assert(kStage % 16 == 0 && kRawIO % 16 == 0 && kRawBC % 16 == 0, "align");
+  static constexpr int CH = Cf::CH, T = Cf::T, S = Cf::S;
+  static constexpr size_t kRawIO = (size_t)CH * T * sizeof(IO);  // one of u / Δ / z
+  static constexpr size_t kRawBC = (size_t)N * T * 4;              // one of B / C
+  static constexpr size_t oRawU = 0;
+  static constexpr size_t oRawD = align_up(oRawU + kRawIO, 128);
+  static constexpr size_t oRawZ = align_up(oRawD + kRawIO, 128);
+  static constexpr size_t oRawB = align_up(oRawZ + kRawIO, 128);
+  static constexpr size_t oRawC = align_up(oRawB + kRawBC, 128);
+  static constexpr size_t kStage = align_up(oRawC + kRawBC, 128);
+  static constexpr int RowDU = T + 1;                 // float4 per row (+1 breaks bank aliasing)
+  static constexpr int RowG = T + 4;                  // floats per gate row
+  static constexpr int RowBC = N + 4;                 // floats per transposed B/C row
+  static constexpr int RowY = T + 16 / (int)sizeof(IO);  // elements per y row (16-byte multiple)
+  static constexpr size_t oDU = (size_t)S * kStage;
+  static constexpr size_t oGate = align_up(oDU + (size_t)CH * RowDU * 16, 16);
+  static constexpr size_t oBt = align_up(oGate + (size_t)CH * RowG * 4, 16);
+  static constexpr size_t oCt = align_up(oBt + (size_t)T * RowBC * 4, 16);
+  static constexpr size_t oY = align_up(oCt + (size_t)T * RowBC * 4, 16);
+  static constexpr size_t oBias = align_up(oY + (size_t)CH * RowY * sizeof(IO), 16);
+  static constexpr size_t oBar = align_up(oBias + (size_t)CH * 4, 8);
+  static constexpr size_t kBytes = oBar + 8 * S;
+  static constexpr size_t kLaunchBytes = kBytes + 128;  // room to align the base to 128
 };
 
 // ---------------------------------------------------------------------------
-// Chunk staging
+// TMA and mbarrier primitives (inline PTX)
 // ---------------------------------------------------------------------------
-template <typename IO, int N>
-__device__ __forceinline__ void stage_chunk(const ScanArgs& p, unsigned char* stage, int64_t b,
-                                            int64_t d0, int64_t t0, int tcount) {
-  using S = ScanSmem<IO, N>;
-  constexpr int CH = S::CH, T = S::T;
-  constexpr int VEC = 16 / sizeof(IO);
-  const int tid = threadIdx.x;
-  IO* su = reinterpret_cast<IO*>(stage);
-  IO* sd = su + CH * T;
-  IO* sz = sd + CH * T;
-  float* sB = reinterpret_cast<float*>(stage + 3 * S::kRawIO);
-  float* sC = sB + N * T;
-  const IO* gu = static_cast<const IO*>(p.u);
-  const IO* gd = static_cast<const IO*>(p.delta);
-  const IO* gz = static_cast<const IO*>(p.z);
-  const int nrows = (int)min64(CH, p.dim - d0);
-  const int narr = gz ? 3 : 2;
-  if (p.vec_io) {
-    // tcount is a multiple of VEC here (L and segment starts are)
-    const int pieces = tcount / VEC;
-    const int per_arr = nrows * pieces;
-    for (int i = tid; i < narr * per_arr; i += kScanThreads) {
-      const int arr = i / per_arr, rem = i - arr * per_arr;
-      const int r = rem / pieces, k = rem - r * pieces;
-      const IO* src = arr == 0 ? gu : (arr == 1 ? gd : gz);
-      IO* dst = arr == 0 ? su : (arr == 1 ? sd : sz);
-      const int64_t off = ((b * p.dim + d0 + r) * p.L + t0) + (int64_t)k * VEC;
-      __pipeline_memcpy_async(dst + r * T + k * VEC, src + off, 16);
-    }
-  } else {
-    const int per_arr = nrows * tcount;
-    for (int i = tid; i < narr * per_arr; i += kScanThreads) {
-      const int arr = i / per_arr, rem = i - arr * per_arr;
-      const int r = rem / tcount, k = rem - r * tcount;
-      const IO* src = arr == 0 ? gu : (arr == 1 ? gd : gz);
-      IO* dst = arr == 0 ? su : (arr == 1 ? sd : sz);
-      dst[r * T + k] = src[(b * p.dim + d0 + r) * p.L + t0 + k];
-    }
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a TMA chunk lands in microseconds
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
-  if (p.vec_bc) {
-    const int pieces = tcount / 4;
-    const int per_arr = N * pieces;
-    for (int i = tid; i < 2 * per_arr; i += kScanThreads) {
-      const int arr = i / per_arr, rem = i - arr * per_arr;
-      const int n = rem / pieces, k = rem - n * pieces;
-      const float* src = arr == 0 ? p.B : p.C;
-      float* dst = arr == 0 ? sB : sC;
-      __pipeline_memcpy_async(dst + n * T + k * 4, src + (b * N + n) * p.L + t0 + k * 4, 16);
-    }
-  } else {
-    const int per_arr = N * tcount;
-    for (int i = tid; i < 2 * per_arr; i += kScanThreads) {
-      const int arr = i / per_arr, rem = i - arr * per_arr;
-      const int n = rem / tcount, k = rem - n * tcount;
-      const float* src = arr == 0 ? p.B : p.C;
-      float* dst = arr == 0 ? sB : sC;
-      dst[n * T + k] = src[(b * N + n) * p.L + t0 + k];
-    }
-  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// 16-byte shared load into two packed pairs.
+__device__ __forceinline__ void lds_pairs(const void* p, f2& a, f2& b) {
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a.r), "=l"(b.r) : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void lds_pair(const void* p, f2& a) {
+  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(a.r) : "r"(smem_u32(p)));
 }
 
-// Turn a raw stage into the fp32 working tiles.  Steps past tcount and rows past
-// dim get Δ = 0 and u = 0, which makes them exact no-ops of the recurrence
-// (Ā = 1, B̄ u = 0).
-template <typename IO, int N, int PASS>
+// The four tensor maps of a launch (u, Δ, z: box CH x T; B, C: box N x T).
+struct ScanMaps {
+  CUtensorMap u, d, z, b, c;
+};
+
+// ---------------------------------------------------------------------------
+// Staging and prep
+// ---------------------------------------------------------------------------
+template <typename IO> __device__ __forceinline__ void load8(const IO* p, float (&v)[8]);
+template <> __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(ws[i] << 16);
+    v[2 * i + 1] = __uint_as_float(ws[i] & 0xffff0000u);
+  }
+}
+template <> __device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Per element of the chunk: Δ (softplus once), u and the gate into the fp32
+// working tiles.  Steps past tcount and rows past the channel count get Δ = 0
+// and u = 0, exact no-ops of the recurrence (Ā = 1, B̄ u = 0).
+template <typename IO, int N, int PASS, bool TMA>
 __device__ __forceinline__ void prep_chunk(const ScanArgs& p, const unsigned char* stage,
-                                           unsigned char* smem, int64_t d0, int tcount,
-                                           bool precise) {
+                                           unsigned char* sm, int64_t b, int64_t d0, int64_t t0,
+                                           int tcount, bool precise) {
   using S = ScanSmem<IO, N>;
   constexpr int CH = S::CH, T = S::T;
   const int tid = threadIdx.x;
-  const IO* su = reinterpret_cast<const IO*>(stage);
-  const IO* sd = su + CH * T;
-  const IO* sz = sd + CH * T;
-  const float* sB = reinterpret_cast<const float*>(stage + 3 * S::kRawIO);
-  const float* sC = sB + N * T;
-  float* pDt = reinterpret_cast<float*>(smem + S::oDt);
-  float* pU = reinterpret_cast<float*>(smem + S::oU);
-  float* pG = reinterpret_cast<float*>(smem + S::oG);
-  float* pB = reinterpret_cast<float*>(smem + S::oB);
-  float* pC = reinterpret_cast<float*>(smem + S::oC);
-  const float* sBias = reinterpret_cast<const float*>(smem + S::oBias);
+  float4* DU = reinterpret_cast<float4*>(sm + S::oDU);
+  float* Gt = reinterpret_cast<float*>(sm + S::oGate);
+  float* Bt = reinterpret_cast<float*>(sm + S::oBt);
+  float* Ct = reinterpret_cast<float*>(sm + S::oCt);
+  const float* sBias = reinterpret_cast<const float*>(sm + S::oBias);
   const int nrows = (int)min64(CH, p.dim - d0);
-  const bool has_z = p.z != nullptr;
-  for (int e = tid; e < CH * T; e += kScanThreads) {
-    const int r = e / T, t = e - r * T;
-    const bool ok = r < nrows && t < tcount;
-    float dt = 0.f, uu = 0.f, gate = 1.f;
-    if (ok) {
-      const float x = io_traits<IO>::to_f32(sd[e]) + sBias[r];
-      dt = p.softplus ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
-      uu = io_traits<IO>::to_f32(su[e]);
-      if (PASS == 0 && has_z) {
-        const float zz = io_traits<IO>::to_f32(sz[e]);
-        gate = precise ? silu_precise(zz) : silu_fast(zz);
+  const bool has_z = PASS == 0 && p.z != nullptr;
+
+  for (int e = tid; e < CH * (T / 8); e += kScanThreads) {
+    const int r = e / (T / 8), t8 = (e - r * (T / 8)) * 8;
+    float dl[8], uu[8], zz[8];
+    if (TMA) {
+      load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawD) + r * T + t8, dl);
+      load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawU) + r * T + t8, uu);
+      if (has_z) load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawZ) + r * T + t8, zz);
+    } else {
+      const int64_t row = (b * p.dim + d0 + r) * p.L + t0 + t8;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool ok = r < nrows && t8 + j < tcount;
+        dl[j] = ok ? io_traits<IO>::to_f32(static_cast<const IO*>(p.delta)[row + j]) : 0.f;
+        uu[j] = ok ? io_traits<IO>::to_f32(static_cast<const IO*>(p.u)[row + j]) : 0.f;
+        zz[j] = (ok && has_z) ? io_traits<IO>::to_f32(static_cast<const IO*>(p.z)[row + j]) : 0.f;
       }
     }
-    pDt[r * S::RowF + t] = dt;
-    pU[r * S::RowF + t] = uu;
-    if (PASS == 0) pG[r * S::RowF + t] = gate;
+    const float bias = sBias[r];
+    float gate[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool ok = r < nrows && t8 + j < tcount;
+      const float x = dl[j] + bias;
+      float dt = p.softplus ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
+      dt = ok ? dt : 0.f;
+      const float u = ok ? uu[j] : 0.f;
+      DU[r * S::RowDU + t8 + j] = make_float4(dt, dt, u, u);
+      gate[j] = has_z ? (precise ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
+    }
+    if (PASS == 0) {
+      float4* g4 = reinterpret_cast<float4*>(Gt + r * S::RowG + t8);
+      g4[0] = make_float4(gate[0], gate[1], gate[2], gate[3]);
+      g4[1] = make_float4(gate[4], gate[5], gate[6], gate[7]);
+    }
   }
-  for (int e = tid; e < N * T; e += kScanThreads) {
-    const int t = e % T, n = e / T;
-    const bool ok = t < tcount;
-    pB[t * S::RowBC + n] = ok ? sB[n * T + t] : 0.f;
-    if (PASS == 0) pC[t * S::RowBC + n] = ok ? sC[n * T + t] : 0.f;
+  // B / C transposed to [t][n]
+  constexpr int NARR = PASS == 0 ? 2 : 1;
+  for (int e = tid; e < NARR * N * (T / 4); e += kScanThreads) {
+    const int arr = e / (N * (T / 4));
+    const int rem = e - arr * (N * (T / 4));
+    const int n = rem / (T / 4), t4 = (rem - n * (T / 4)) * 4;
+    float v[4];
+    if (TMA) {
+      const float4 q = *reinterpret_cast<const float4*>(
+          reinterpret_cast<const float*>(stage + (arr == 0 ? S::oRawB : S::oRawC)) + n * T + t4);
+      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    } else {
+      const float* src = (arr == 0 ? p.B : p.C) + (b * N + n) * p.L + t0 + t4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = t4 + j < tcount ? src[j] : 0.f;
+    }
+    float* dst = arr == 0 ? Bt : Ct;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[(t4 + j) * S::RowBC + n] = v[j];
   }
 }
 
 // Combine the G partial readouts of a channel: afterwards lane g holds the full
-// sum for time step g of the block (shuffle reduce-scatter, log2(G) stages).
+// sum for time step g of the group (shuffle reduce-scatter, log2(G) stages).
 template <int G>
 __device__ __forceinline__ float reduce_scatter(float (&part)[G], int g) {
 #pragma unroll
@@ -197,17 +271,37 @@ __device__ __forceinline__ float reduce_scatter(float (&part)[G], int g) {
   return part[0];
 }
 
+// Issue the TMA loads of one chunk into a raw stage (one thread).
+template <typename IO, int N, int PASS>
+__device__ __forceinline__ void issue_chunk(const ScanArgs& p, const ScanMaps& m,
+                                            unsigned char* stage, uint64_t* bar, int64_t b,
+                                            int64_t d0, int64_t t0) {
+  using S = ScanSmem<IO, N>;
+  const bool has_z = PASS == 0 && p.z != nullptr;
+  const uint32_t bytes = (uint32_t)(S::kRawIO * (has_z ? 3 : 2) + S::kRawBC * (PASS == 0 ? 2 : 1));
+  mbar_arrive_expect_tx(bar, bytes);
+  const int x = (int)t0, y = (int)d0, z = (int)b;
+  tma_load_3d(stage + S::oRawU, &m.u, bar, x, y, z);
+  tma_load_3d(stage + S::oRawD, &m.d, bar, x, y, z);
+  if (has_z) tma_load_3d(stage + S::oRawZ, &m.z, bar, x, y, z);
+  tma_load_3d(stage + S::oRawB, &m.b, bar, x, 0, z);
+  if (PASS == 0) tma_load_3d(stage + S::oRawC, &m.c, bar, x, 0, z);
+}
+
 // ---------------------------------------------------------------------------
 // The kernel.  PASS 0: outputs (y, final state).  PASS 1: segment end state
 // from a zero start and ΣΔ, for the split plan.
 // ---------------------------------------------------------------------------
 template <typename IO, int N, int PASS>
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p,
+                                                            const __grid_constant__ ScanMaps maps) {
   using Cf = ScanCfg<N>;
   using S = ScanSmem<IO, N>;
-  constexpr int NPT = Cf::NPT, G = Cf::G, CH = Cf::CH, T = Cf::T;
+  constexpr int NPT = Cf::NPT, G = Cf::G, CH = Cf::CH, T = Cf::T, NS = Cf::S;
   constexpr int NP = NPT / 2;  // packed pairs per lane (0 when NPT == 1)
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
   const int tid = threadIdx.x;
   const int c = tid / G, g = tid - (tid / G) * G;
@@ -219,11 +313,19 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
   const int64_t t_begin = (int64_t)seg * p.seg_len;
   const int64_t t_end = min(p.L, t_begin + p.seg_len);
   const int64_t nchunks = (t_end - t_begin + T - 1) / T;
+  const bool use_tma = p.use_tma != 0;
 
-  // per-row bias into shared memory
-  float* sBias = reinterpret_cast<float*>(smem + S::oBias);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::oBar);
+  float* sBias = reinterpret_cast<float*>(sm + S::oBias);
   for (int r = tid; r < CH; r += kScanThreads)
     sBias[r] = (p.bias && d0 + r < p.dim) ? p.bias[d0 + r] : 0.f;
+  if (use_tma && tid == 0) {
+    prefetch_tmap(&maps.u);
+    prefetch_tmap(&maps.d);
+    prefetch_tmap(&maps.b);
+    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
 
   // this lane's states: n = g*NPT + j
   float Aj[NPT];
@@ -234,6 +336,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
     zeroA |= (Aj[j] == 0.f);
   }
   const bool precise = __syncthreads_or(zeroA) || p.force_precise;
+
+  // prologue: the first NS chunks in flight
+  if (use_tma && tid == 0) {
+    for (int k = 0; k < NS && k < nchunks; ++k)
+      issue_chunk<IO, N, PASS>(p, maps, sm + (size_t)k * S::kStage, &bars[k], b, d0,
+                               t_begin + (int64_t)k * T);
+  }
 
   float h[NPT];
 #pragma unroll
@@ -253,17 +362,18 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
   }
   const float Dd = (PASS == 0 && chan_ok && p.D) ? p.D[d] : 0.f;
 
-  // fast-path constants
+  // fast-path constants: A·log2(e) and -1/A per state, as packed pairs
   f2 A2p[NP > 0 ? NP : 1], nIp[NP > 0 ? NP : 1], hp[NP > 0 ? NP : 1];
   float A2s = 0.f, nIs = 0.f;
   if constexpr (NPT == 1) {
     A2s = Aj[0] * kLog2e;
-    nIs = -1.f / Aj[0];
+    nIs = Aj[0] != 0.f ? -1.f / Aj[0] : 0.f;
   } else {
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
       A2p[q] = pack2(Aj[2 * q] * kLog2e, Aj[2 * q + 1] * kLog2e);
-      nIp[q] = pack2(-1.f / Aj[2 * q], -1.f / Aj[2 * q + 1]);
+      nIp[q] = pack2(Aj[2 * q] != 0.f ? -1.f / Aj[2 * q] : 0.f,
+                     Aj[2 * q + 1] != 0.f ? -1.f / Aj[2 * q + 1] : 0.f);
     }
   }
   float invA[NPT];
@@ -271,76 +381,79 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
   for (int j = 0; j < NPT; ++j) invA[j] = Aj[j] != 0.f ? 1.f / Aj[j] : 0.f;
 
   float sumDt = 0.f;
+  const float4* DUrow = reinterpret_cast<const float4*>(sm + S::oDU) + c * S::RowDU;
+  const float* Grow = reinterpret_cast<const float*>(sm + S::oGate) + c * S::RowG;
+  const float* Bt = reinterpret_cast<const float*>(sm + S::oBt) + g * NPT;
+  const float* Ct = reinterpret_cast<const float*>(sm + S::oCt) + g * NPT;
+  IO* yT = reinterpret_cast<IO*>(sm + S::oY);
+  bool failed = false;
+  int64_t i = 0;
 
-  unsigned char* stages[2] = {smem + S::oStage0, smem + S::oStage1};
-  // prologue: chunks 0 and 1 in flight
-  for (int k = 0; k < 2; ++k) {
-    if (k < nchunks) {
-      const int64_t t0 = t_begin + (int64_t)k * T;
-      stage_chunk<IO, N>(p, stages[k], b, d0, t0, (int)min64(T, t_end - t0));
-    }
-    __pipeline_commit();
-  }
-
-  const float* pDt = reinterpret_cast<const float*>(smem + S::oDt) + c * S::RowF;
-  const float* pU = reinterpret_cast<const float*>(smem + S::oU) + c * S::RowF;
-  const float* pG = reinterpret_cast<const float*>(smem + S::oG) + c * S::RowF;
-  const float* pB = reinterpret_cast<const float*>(smem + S::oB) + g * NPT;
-  const float* pC = reinterpret_cast<const float*>(smem + S::oC) + g * NPT;
-  IO* yT = reinterpret_cast<IO*>(smem + S::oY);
-
-  for (int64_t i = 0; i < nchunks; ++i) {
+  for (; i < nchunks; ++i) {
+    const int s = (int)(i % NS);
     const int64_t t0 = t_begin + i * T;
     const int tcount = (int)min64(T, t_end - t0);
-    __pipeline_wait_prior(1);
-    __syncthreads();
-    prep_chunk<IO, N, PASS>(p, stages[i & 1], smem, d0, tcount, precise);
-    __syncthreads();
-    // the raw stage is consumed: refill it with chunk i + 2
-    if (i + 2 < nchunks) {
-      const int64_t t2 = t_begin + (i + 2) * T;
-      stage_chunk<IO, N>(p, stages[i & 1], b, d0, t2, (int)min64(T, t_end - t2));
+    unsigned char* stage = sm + (size_t)s * S::kStage;
+    bool ok = true;
+    if (use_tma) {
+      ok = mbar_wait_bounded(&bars[s], (uint32_t)((i / NS) & 1));
+      prep_chunk<IO, N, PASS, true>(p, stage, sm, b, d0, t0, tcount, precise);
+    } else {
+      prep_chunk<IO, N, PASS, false>(p, stage, sm, b, d0, t0, tcount, precise);
     }
-    __pipeline_commit();
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    // the raw stage is consumed: refill it with chunk i + NS
+    if (use_tma && tid == 0 && i + NS < nchunks)
+      issue_chunk<IO, N, PASS>(p, maps, stage, &bars[s], b, d0, t0 + (int64_t)NS * T);
 
-    const int tround = ((tcount + G - 1) / G) * G;
     if (!precise) {
       if constexpr (NPT > 1) {
 #pragma unroll
         for (int q = 0; q < NP; ++q) hp[q] = pack2(h[2 * q], h[2 * q + 1]);
       }
-      for (int tb = 0; tb < tround; tb += G) {
+#pragma unroll 2
+      for (int tb = 0; tb < T; tb += G) {
         float part[G];
 #pragma unroll
         for (int k = 0; k < G; ++k) {
           const int t = tb + k;
-          const float dt = pDt[t];
-          const float ut = pU[t];
-          if (PASS == 1) sumDt += dt;
           if constexpr (NPT == 1) {
-            const float a = ex2_fast(dt * A2s);
-            const float nv = pB[t * S::RowBC] * ut * nIs;
+            const float4 du = DUrow[t];
+            if (PASS == 1) sumDt += du.x;
+            const float a = ex2_fast(du.x * A2s);
+            const float nv = Bt[t * S::RowBC] * du.z * nIs;
             h[0] = fmaf(a, h[0] - nv, nv);
-            part[k] = PASS == 0 ? pC[t * S::RowBC] * h[0] : 0.f;
+            part[k] = PASS == 0 ? Ct[t * S::RowBC] * h[0] : 0.f;
           } else {
-            const f2 dt2 = pack2(dt, dt);
-            const f2 u2 = pack2(ut, ut);
+            f2 dt2, u2;
+            lds_pairs(DUrow + t, dt2, u2);
+            if (PASS == 1) {
+              float lo, hi;
+              unpack2(dt2, lo, hi);
+              sumDt += lo;
+            }
+            f2 bq[NP], cq[NP];
+#pragma unroll
+            for (int q = 0; q + 1 < NP; q += 2) lds_pairs(Bt + t * S::RowBC + 2 * q, bq[q], bq[q + 1]);
+            if constexpr (NP % 2 == 1) lds_pair(Bt + t * S::RowBC + 2 * (NP - 1), bq[NP - 1]);
+            if (PASS == 0) {
+#pragma unroll
+              for (int q = 0; q + 1 < NP; q += 2) lds_pairs(Ct + t * S::RowBC + 2 * q, cq[q], cq[q + 1]);
+              if constexpr (NP % 2 == 1) lds_pair(Ct + t * S::RowBC + 2 * (NP - 1), cq[NP - 1]);
+            }
             f2 acc2 = pack2(0.f, 0.f);
-            const float* brow = pB + t * S::RowBC;
-            const float* crow = pC + t * S::RowBC;
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
-              const float2 bq = *reinterpret_cast<const float2*>(brow + 2 * q);
               const f2 x = mul2(dt2, A2p[q]);
               float x0, x1;
               unpack2(x, x0, x1);
               const f2 a = pack2(ex2_fast(x0), ex2_fast(x1));
-              const f2 nv = mul2(mul2(pack2(bq.x, bq.y), u2), nIp[q]);
+              const f2 nv = mul2(mul2(bq[q], u2), nIp[q]);
               hp[q] = fma2(a, sub2(hp[q], nv), nv);
-              if (PASS == 0) {
-                const float2 cq = *reinterpret_cast<const float2*>(crow + 2 * q);
-                acc2 = fma2(pack2(cq.x, cq.y), hp[q], acc2);
-              }
+              if (PASS == 0) acc2 = fma2(cq[q], hp[q], acc2);
             }
             float lo, hi;
             unpack2(acc2, lo, hi);
@@ -350,7 +463,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
         if (PASS == 0) {
           const float yv = reduce_scatter<G>(part, g);
           const int t = tb + g;
-          yT[c * S::RowY + t] = io_traits<IO>::from_f32(fmaf(Dd, pU[t], yv) * pG[t]);
+          const float ut = DUrow[t].z;
+          yT[c * S::RowY + t] = io_traits<IO>::from_f32(fmaf(Dd, ut, yv) * Grow[t]);
         }
       }
       if constexpr (NPT > 1) {
@@ -358,13 +472,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
         for (int q = 0; q < NP; ++q) unpack2(hp[q], h[2 * q], h[2 * q + 1]);
       }
     } else {
-      for (int tb = 0; tb < tround; tb += G) {
+      for (int tb = 0; tb < T; tb += G) {
         float part[G];
 #pragma unroll
         for (int k = 0; k < G; ++k) {
           const int t = tb + k;
-          const float dt = pDt[t];
-          const float bu = pU[t];
+          const float4 du = DUrow[t];
+          const float dt = du.x, ut = du.z;
           if (PASS == 1) sumDt += dt;
           float acc = 0.f;
 #pragma unroll
@@ -372,26 +486,26 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
             const float x = dt * Aj[j];
             const float a = expf(x);
             const float coef = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
-            h[j] = fmaf(a, h[j], coef * (pB[t * S::RowBC + j] * bu));
-            if (PASS == 0) acc = fmaf(pC[t * S::RowBC + j], h[j], acc);
+            h[j] = fmaf(a, h[j], coef * (Bt[t * S::RowBC + j] * ut));
+            if (PASS == 0) acc = fmaf(Ct[t * S::RowBC + j], h[j], acc);
           }
           part[k] = acc;
         }
         if (PASS == 0) {
           const float yv = reduce_scatter<G>(part, g);
           const int t = tb + g;
-          yT[c * S::RowY + t] = io_traits<IO>::from_f32(fmaf(Dd, pU[t], yv) * pG[t]);
+          yT[c * S::RowY + t] = io_traits<IO>::from_f32(fmaf(Dd, DUrow[t].z, yv) * Grow[t]);
         }
       }
     }
+    __syncthreads();
     if (PASS == 0) {
-      __syncthreads();
       // write the y tile back
       IO* gy = static_cast<IO*>(p.y);
       const int nrows = (int)min64(CH, p.dim - d0);
       constexpr int VEC = 16 / sizeof(IO);
       if (p.vec_io) {
-        const int pieces = tcount / VEC;
+        const int pieces = tcount / VEC;  // tcount is a multiple of VEC here
         for (int e = tid; e < nrows * pieces; e += kScanThreads) {
           const int r = e / pieces, k = e - r * pieces;
           const uint4 v = *reinterpret_cast<const uint4*>(yT + r * S::RowY + k * VEC);
@@ -404,6 +518,18 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p) {
         }
       }
     }
+  }
+
+  if (failed) {
+    // a TMA chunk did not land in time: record it, let the copies still in
+    // flight into this block's shared memory finish (bounded), and leave
+    // without writing a state
+    if (tid == 0) {
+      atomicExch(&g_scan_error, 1);
+      for (int64_t j = i; j < nchunks && j < i + NS; ++j)
+        (void)mbar_wait_bounded(&bars[j % NS], (uint32_t)((j / NS) & 1));
+    }
+    return;
   }
 
   if (!chan_ok) return;
@@ -451,7 +577,7 @@ static bool cfg_for(int64_t N, int& chans, int& chunk) {
 ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtype, int sm_count,
                    bool allow_split) {
   (void)io_dtype;
-  ScanPlan pl{1, L, 0, 64, 32};
+  ScanPlan pl{1, L, 0, 32, 32};
   if (!cfg_for(N, pl.chans, pl.chunk)) return pl;
   pl.seg_len = L > 0 ? L : 1;
   if (!allow_split || L <= 0 || batch <= 0 || dim <= 0) return pl;
@@ -459,7 +585,7 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
   const int64_t want = (int64_t)sm_count * 2;  // blocks that keep every SM busy
   if (blocks >= want) return pl;
   int64_t nseg = (want + blocks - 1) / blocks;
-  const int64_t max_by_len = L / (8 * (int64_t)pl.chunk);  // at least 8 chunks per segment
+  const int64_t max_by_len = L / (16 * (int64_t)pl.chunk);  // at least 16 chunks per segment
   if (nseg > max_by_len) nseg = max_by_len;
   if (nseg > 64) nseg = 64;
   if (nseg < 2) return pl;
@@ -475,10 +601,56 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
   return pl;
 }
 
-template <typename IO, int N, int PASS>
-static cudaError_t launch_one(const ScanArgs& a, int nz, cudaStream_t stream) {
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// 3-D map over a (d2, d1, d0) row-major tensor (d0 fastest) with box (1, b1, b0).
+static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t esz,
+                     uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !base) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * esz, d0 * d1 * esz};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename IO, int N>
+static bool make_maps(ScanMaps& m, const ScanArgs& a) {
   using Cf = ScanCfg<N>;
-  constexpr size_t bytes = ScanSmem<IO, N>::kBytes;
+  const CUtensorMapDataType dt =
+      sizeof(IO) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const uint64_t L = (uint64_t)a.L, D = (uint64_t)a.dim, Bt = (uint64_t)a.batch;
+  bool ok = make_map(&m.u, a.u, dt, sizeof(IO), L, D, Bt, Cf::T, Cf::CH) &&
+            make_map(&m.d, a.delta, dt, sizeof(IO), L, D, Bt, Cf::T, Cf::CH) &&
+            make_map(&m.b, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, N, Bt, Cf::T, N) &&
+            make_map(&m.c, a.C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, N, Bt, Cf::T, N);
+  if (ok && a.z) ok = make_map(&m.z, a.z, dt, sizeof(IO), L, D, Bt, Cf::T, Cf::CH);
+  return ok;
+}
+
+template <typename IO, int N, int PASS>
+static cudaError_t launch_one(const ScanArgs& a, const ScanMaps& m, int nz, cudaStream_t stream) {
+  using Cf = ScanCfg<N>;
+  constexpr size_t bytes = ScanSmem<IO, N>::kLaunchBytes;
   auto kern = scan_kernel<IO, N, PASS>;
   static int configured_dev = -1;  // attribute set once per device change
   int dev = 0;
@@ -489,17 +661,24 @@ static cudaError_t launch_one(const ScanArgs& a, int nz, cudaStream_t stream) {
     configured_dev = dev;
   }
   dim3 grid((unsigned)((a.dim + Cf::CH - 1) / Cf::CH), (unsigned)a.batch, (unsigned)nz);
-  kern<<<grid, kScanThreads, bytes, stream>>>(a);
+  kern<<<grid, kScanThreads, bytes, stream>>>(a, m);
   return cudaGetLastError();
 }
 
 template <typename IO, int N>
-static cudaError_t launch_typed(const ScanArgs& a, cudaStream_t stream) {
+static cudaError_t launch_typed(ScanArgs a, cudaStream_t stream) {
+  ScanMaps m;
+  memset(&m, 0, sizeof m);
+  // TMA needs 16-byte row strides (rows of u/Δ/z and B/C) and coordinates
+  // that fit in int32
+  const bool rows16 = a.vec_io && a.vec_bc;
+  const bool fits = a.L < (int64_t(1) << 31) && a.dim < (int64_t(1) << 31);
+  a.use_tma = rows16 && fits && make_maps<IO, N>(m, a);
   if (a.nseg > 1) {
-    cudaError_t e = launch_one<IO, N, 1>(a, a.nseg - 1, stream);
+    cudaError_t e = launch_one<IO, N, 1>(a, m, a.nseg - 1, stream);
     if (e != cudaSuccess) return e;
   }
-  return launch_one<IO, N, 0>(a, a.nseg, stream);
+  return launch_one<IO, N, 0>(a, m, a.nseg, stream);
 }
 
 template <typename IO>
@@ -528,6 +707,15 @@ cudaError_t scan_launch(const ScanArgs& a, int64_t N, int io_dtype, const ScanPl
   }
   if (io_dtype == 0) return launch_io<float>(a, N, stream);
   return launch_io<__nv_bfloat16>(a, N, stream);
+}
+
+cudaError_t scan_device_error(int* code, cudaStream_t stream) {
+  int zero = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(code, g_scan_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_scan_error, &zero, sizeof(int));
 }
 
 }  // namespace ssm
