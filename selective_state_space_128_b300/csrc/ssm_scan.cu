@@ -41,6 +41,7 @@
 #include <cuda.h>
 
 #include <cstring>
+#include <type_traits>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -181,29 +182,26 @@ template <> __device__ __forceinline__ void load8<float>(const float* p, float (
 
 // Per element of the chunk: Δ (softplus once), u and the gate into the fp32
 // working tiles.  Steps past tcount and rows past the channel count get Δ = 0
-// and u = 0, exact no-ops of the recurrence (Ā = 1, B̄ u = 0).
-template <typename IO, int N, int PASS, bool TMA>
-__device__ __forceinline__ void prep_chunk(const ScanArgs& p, const unsigned char* stage,
+// and u = 0, exact no-ops of the recurrence (Ā = 1, B̄ u = 0).  The flags are
+// template parameters so that the element loop carries no per-element branch.
+template <typename IO, int N, int PASS, bool TMA, bool PRECISE, bool SP, bool HZ, bool MASK>
+__device__ __forceinline__ void prep_elems(const ScanArgs& p, const unsigned char* stage,
                                            unsigned char* sm, int64_t b, int64_t d0, int64_t t0,
-                                           int tcount, bool precise) {
+                                           int tcount, int nrows) {
   using S = ScanSmem<IO, N>;
   constexpr int CH = S::CH, T = S::T;
   const int tid = threadIdx.x;
   float4* DU = reinterpret_cast<float4*>(sm + S::oDU);
   float* Gt = reinterpret_cast<float*>(sm + S::oGate);
-  float* Bt = reinterpret_cast<float*>(sm + S::oBt);
-  float* Ct = reinterpret_cast<float*>(sm + S::oCt);
   const float* sBias = reinterpret_cast<const float*>(sm + S::oBias);
-  const int nrows = (int)min64(CH, p.dim - d0);
-  const bool has_z = PASS == 0 && p.z != nullptr;
-
+#pragma unroll 1
   for (int e = tid; e < CH * (T / 8); e += kScanThreads) {
     const int r = e / (T / 8), t8 = (e - r * (T / 8)) * 8;
     float dl[8], uu[8], zz[8];
     if (TMA) {
       load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawD) + r * T + t8, dl);
       load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawU) + r * T + t8, uu);
-      if (has_z) load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawZ) + r * T + t8, zz);
+      if (HZ) load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawZ) + r * T + t8, zz);
     } else {
       const int64_t row = (b * p.dim + d0 + r) * p.L + t0 + t8;
 #pragma unroll
@@ -211,20 +209,23 @@ __device__ __forceinline__ void prep_chunk(const ScanArgs& p, const unsigned cha
         const bool ok = r < nrows && t8 + j < tcount;
         dl[j] = ok ? io_traits<IO>::to_f32(static_cast<const IO*>(p.delta)[row + j]) : 0.f;
         uu[j] = ok ? io_traits<IO>::to_f32(static_cast<const IO*>(p.u)[row + j]) : 0.f;
-        zz[j] = (ok && has_z) ? io_traits<IO>::to_f32(static_cast<const IO*>(p.z)[row + j]) : 0.f;
+        zz[j] = (ok && HZ) ? io_traits<IO>::to_f32(static_cast<const IO*>(p.z)[row + j]) : 0.f;
       }
     }
     const float bias = sBias[r];
     float gate[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const bool ok = r < nrows && t8 + j < tcount;
       const float x = dl[j] + bias;
-      float dt = p.softplus ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
-      dt = ok ? dt : 0.f;
-      const float u = ok ? uu[j] : 0.f;
+      float dt = SP ? (PRECISE ? softplus_precise(x) : softplus_fast(x)) : x;
+      float u = uu[j];
+      if (MASK) {
+        const bool ok = r < nrows && t8 + j < tcount;
+        dt = ok ? dt : 0.f;
+        u = ok ? u : 0.f;
+      }
       DU[r * S::RowDU + t8 + j] = make_float4(dt, dt, u, u);
-      gate[j] = has_z ? (precise ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
+      gate[j] = HZ ? (PRECISE ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
     }
     if (PASS == 0) {
       float4* g4 = reinterpret_cast<float4*>(Gt + r * S::RowG + t8);
@@ -232,8 +233,33 @@ __device__ __forceinline__ void prep_chunk(const ScanArgs& p, const unsigned cha
       g4[1] = make_float4(gate[4], gate[5], gate[6], gate[7]);
     }
   }
+}
+
+template <typename IO, int N, int PASS, bool TMA, bool PRECISE>
+__device__ __forceinline__ void prep_chunk(const ScanArgs& p, const unsigned char* stage,
+                                           unsigned char* sm, int64_t b, int64_t d0, int64_t t0,
+                                           int tcount) {
+  using S = ScanSmem<IO, N>;
+  constexpr int CH = S::CH, T = S::T;
+  const int tid = threadIdx.x;
+  const int nrows = (int)min64(CH, p.dim - d0);
+  const bool mask = tcount < T || nrows < CH;
+  const bool hz = PASS == 0 && p.z != nullptr;
+#define SSM_PREP(SP, HZ, MASK) \
+  prep_elems<IO, N, PASS, TMA, PRECISE, SP, HZ, MASK>(p, stage, sm, b, d0, t0, tcount, nrows)
+  if (p.softplus) {
+    if (hz) { if (mask) SSM_PREP(true, true, true); else SSM_PREP(true, true, false); }
+    else    { if (mask) SSM_PREP(true, false, true); else SSM_PREP(true, false, false); }
+  } else {
+    if (hz) { if (mask) SSM_PREP(false, true, true); else SSM_PREP(false, true, false); }
+    else    { if (mask) SSM_PREP(false, false, true); else SSM_PREP(false, false, false); }
+  }
+#undef SSM_PREP
   // B / C transposed to [t][n]
+  float* Bt = reinterpret_cast<float*>(sm + S::oBt);
+  float* Ct = reinterpret_cast<float*>(sm + S::oCt);
   constexpr int NARR = PASS == 0 ? 2 : 1;
+#pragma unroll 1
   for (int e = tid; e < NARR * N * (T / 4); e += kScanThreads) {
     const int arr = e / (N * (T / 4));
     const int rem = e - arr * (N * (T / 4));
@@ -286,6 +312,232 @@ __device__ __forceinline__ void issue_chunk(const ScanArgs& p, const ScanMaps& m
   if (has_z) tma_load_3d(stage + S::oRawZ, &m.z, bar, x, y, z);
   tma_load_3d(stage + S::oRawB, &m.b, bar, x, 0, z);
   if (PASS == 0) tma_load_3d(stage + S::oRawC, &m.c, bar, x, 0, z);
+}
+
+// ---------------------------------------------------------------------------
+// One chunk of T steps for one lane, fast flavour (MUFU ex2, packed f32x2).
+// The step loop is fully unrolled and the Ā / v pairs of step t+1 are formed
+// while step t updates the state, so that the serial chain per step is just
+// h <- Ā (h - v) + v and the readout.
+// ---------------------------------------------------------------------------
+template <typename IO, int N, int PASS>
+__device__ __forceinline__ void chunk_fast(unsigned char* sm, int c, int g, float Dd,
+                                           f2 (&hp)[ScanCfg<N>::NPT / 2],
+                                           const f2 (&A2p)[ScanCfg<N>::NPT / 2],
+                                           const f2 (&nIp)[ScanCfg<N>::NPT / 2], float& sumDt) {
+  using Cf = ScanCfg<N>;
+  using S = ScanSmem<IO, N>;
+  constexpr int NPT = Cf::NPT, G = Cf::G, T = Cf::T, NP = NPT / 2;
+  const float4* DUrow = reinterpret_cast<const float4*>(sm + S::oDU) + c * S::RowDU;
+  const float* Grow = reinterpret_cast<const float*>(sm + S::oGate) + c * S::RowG;
+  const float* Bt = reinterpret_cast<const float*>(sm + S::oBt) + g * NPT;
+  const float* Ct = reinterpret_cast<const float*>(sm + S::oCt) + g * NPT;
+  IO* yT = reinterpret_cast<IO*>(sm + S::oY) + c * S::RowY;
+
+  auto load_row = [](const float* row, f2 (&v)[NP]) {
+#pragma unroll
+    for (int q = 0; q + 1 < NP; q += 2) lds_pairs(row + 2 * q, v[q], v[q + 1]);
+    if constexpr (NP % 2 == 1) lds_pair(row + 2 * (NP - 1), v[NP - 1]);
+  };
+  // Three-deep software pipeline over the fully unrolled steps: the shared
+  // loads of step t+2, the exponentials and v of step t+1 and the state
+  // update of step t are independent, so their latencies overlap.
+  f2 dt_l, u_l, b_l[NP], c_l[NP];      // loaded for step t+1
+  f2 a_c[NP], v_c[NP], c_c[NP];        // ready for step t
+  auto load_step = [&](int t, f2& dt2, f2& u2, f2 (&bq)[NP], f2 (&cq)[NP]) {
+    lds_pairs(DUrow + t, dt2, u2);
+    load_row(Bt + t * S::RowBC, bq);
+    if (PASS == 0) load_row(Ct + t * S::RowBC, cq);
+  };
+  auto discretise = [&](const f2& dt2, const f2& u2, const f2 (&bq)[NP], f2 (&ao)[NP],
+                        f2 (&vo)[NP]) {
+    if (PASS == 1) {
+      float lo, hi;
+      unpack2(dt2, lo, hi);
+      sumDt += lo;
+    }
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      const f2 x = mul2(dt2, A2p[q]);
+      float x0, x1;
+      unpack2(x, x0, x1);
+      ao[q] = pack2(ex2_fast(x0), ex2_fast(x1));
+      vo[q] = mul2(mul2(bq[q], u2), nIp[q]);
+    }
+  };
+
+  {
+    f2 dt0, u0, b0[NP];
+    load_step(0, dt0, u0, b0, c_c);
+    discretise(dt0, u0, b0, a_c, v_c);
+    load_step(1, dt_l, u_l, b_l, c_l);
+  }
+  float part[G];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    f2 dt_n, u_n, b_n[NP], c_n[NP], a_n[NP], v_n[NP];
+    if (t + 2 < T) load_step(t + 2, dt_n, u_n, b_n, c_n);
+    if (t + 1 < T) discretise(dt_l, u_l, b_l, a_n, v_n);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) hp[q] = fma2(a_c[q], sub2(hp[q], v_c[q]), v_c[q]);
+    if (PASS == 0) {
+      f2 acc2 = mul2(c_c[0], hp[0]);
+#pragma unroll
+      for (int q = 1; q < NP; ++q) acc2 = fma2(c_c[q], hp[q], acc2);
+      float lo, hi;
+      unpack2(acc2, lo, hi);
+      part[t % G] = lo + hi;
+      if (t % G == G - 1) {
+        const float yv = reduce_scatter<G>(part, g);
+        const int ty = t - (G - 1) + g;
+        yT[ty] = io_traits<IO>::from_f32(fmaf(Dd, DUrow[ty].z, yv) * Grow[ty]);
+      }
+    }
+    if (t + 1 < T) {
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        a_c[q] = a_n[q];
+        v_c[q] = v_n[q];
+        c_c[q] = c_l[q];
+      }
+    }
+    if (t + 2 < T) {
+      dt_l = dt_n;
+      u_l = u_n;
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        b_l[q] = b_n[q];
+        c_l[q] = c_n[q];
+      }
+    }
+  }
+}
+
+// One chunk, one state per lane (N = 1), fast flavour.
+template <typename IO, int PASS>
+__device__ __forceinline__ void chunk_fast_scalar(unsigned char* sm, int c, float Dd, float& h,
+                                                  float A2s, float nIs, float& sumDt) {
+  using S = ScanSmem<IO, 1>;
+  constexpr int T = ScanCfg<1>::T;
+  const float4* DUrow = reinterpret_cast<const float4*>(sm + S::oDU) + c * S::RowDU;
+  const float* Grow = reinterpret_cast<const float*>(sm + S::oGate) + c * S::RowG;
+  const float* Bt = reinterpret_cast<const float*>(sm + S::oBt);
+  const float* Ct = reinterpret_cast<const float*>(sm + S::oCt);
+  IO* yT = reinterpret_cast<IO*>(sm + S::oY) + c * S::RowY;
+#pragma unroll 8
+  for (int t = 0; t < T; ++t) {
+    const float4 du = DUrow[t];
+    if (PASS == 1) sumDt += du.x;
+    const float a = ex2_fast(du.x * A2s);
+    const float nv = Bt[t * S::RowBC] * du.z * nIs;
+    h = fmaf(a, h - nv, nv);
+    if (PASS == 0) yT[t] = io_traits<IO>::from_f32(fmaf(Dd, du.z, Ct[t * S::RowBC] * h) * Grow[t]);
+  }
+}
+
+// One chunk, precise flavour (CUDA libm expf / expm1f; A = 0 takes the limit).
+template <typename IO, int N, int PASS>
+__device__ __forceinline__ void chunk_precise(unsigned char* sm, int c, int g, float Dd,
+                                              float (&h)[ScanCfg<N>::NPT],
+                                              const float (&Aj)[ScanCfg<N>::NPT],
+                                              const float (&invA)[ScanCfg<N>::NPT], float& sumDt) {
+  using Cf = ScanCfg<N>;
+  using S = ScanSmem<IO, N>;
+  constexpr int NPT = Cf::NPT, G = Cf::G, T = Cf::T;
+  const float4* DUrow = reinterpret_cast<const float4*>(sm + S::oDU) + c * S::RowDU;
+  const float* Grow = reinterpret_cast<const float*>(sm + S::oGate) + c * S::RowG;
+  const float* Bt = reinterpret_cast<const float*>(sm + S::oBt) + g * NPT;
+  const float* Ct = reinterpret_cast<const float*>(sm + S::oCt) + g * NPT;
+  IO* yT = reinterpret_cast<IO*>(sm + S::oY) + c * S::RowY;
+  for (int tb = 0; tb < T; tb += G) {
+    float part[G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const int t = tb + k;
+      const float4 du = DUrow[t];
+      const float dt = du.x, ut = du.z;
+      if (PASS == 1) sumDt += dt;
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) {
+        const float x = dt * Aj[j];
+        const float a = expf(x);
+        const float coef = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
+        h[j] = fmaf(a, h[j], coef * (Bt[t * S::RowBC + j] * ut));
+        if (PASS == 0) acc = fmaf(Ct[t * S::RowBC + j], h[j], acc);
+      }
+      part[k] = acc;
+    }
+    if (PASS == 0) {
+      const float yv = reduce_scatter<G>(part, g);
+      const int t = tb + g;
+      yT[t] = io_traits<IO>::from_f32(fmaf(Dd, DUrow[t].z, yv) * Grow[t]);
+    }
+  }
+}
+
+// The chunk loop of one block: wait for chunk i's TMA stage, prep it, refill
+// the stage with chunk i + S, run the steps, write the y tile back.  Returns
+// the index of a chunk whose wait timed out, or -1.
+template <typename IO, int N, int PASS, bool PRECISE>
+__device__ __forceinline__ int64_t run_chunks(
+    const ScanArgs& p, const ScanMaps& maps, unsigned char* sm, uint64_t* bars, int64_t b,
+    int64_t d0, int64_t t_begin, int64_t t_end, int64_t nchunks, bool use_tma, int c, int g,
+    float Dd, float (&h)[ScanCfg<N>::NPT], f2 (&hp)[ScanCfg<N>::NPT / 2 > 0 ? ScanCfg<N>::NPT / 2 : 1],
+    const f2 (&A2p)[ScanCfg<N>::NPT / 2 > 0 ? ScanCfg<N>::NPT / 2 : 1],
+    const f2 (&nIp)[ScanCfg<N>::NPT / 2 > 0 ? ScanCfg<N>::NPT / 2 : 1], float A2s, float nIs,
+    const float (&Aj)[ScanCfg<N>::NPT], const float (&invA)[ScanCfg<N>::NPT], float& sumDt) {
+  using Cf = ScanCfg<N>;
+  using S = ScanSmem<IO, N>;
+  constexpr int NPT = Cf::NPT, CH = Cf::CH, T = Cf::T, NS = Cf::S;
+  const int tid = threadIdx.x;
+  const IO* yTile = reinterpret_cast<const IO*>(sm + S::oY);
+  for (int64_t i = 0; i < nchunks; ++i) {
+    const int s = (int)(i % NS);
+    const int64_t t0 = t_begin + i * T;
+    const int tcount = (int)min64(T, t_end - t0);
+    unsigned char* stage = sm + (size_t)s * S::kStage;
+    bool ok = true;
+    if (use_tma) {
+      ok = mbar_wait_bounded(&bars[s], (uint32_t)((i / NS) & 1));
+      prep_chunk<IO, N, PASS, true, PRECISE>(p, stage, sm, b, d0, t0, tcount);
+    } else {
+      prep_chunk<IO, N, PASS, false, PRECISE>(p, stage, sm, b, d0, t0, tcount);
+    }
+    if (__syncthreads_or(!ok)) return i;
+    // the raw stage is consumed: refill it with chunk i + NS
+    if (use_tma && tid == 0 && i + NS < nchunks)
+      issue_chunk<IO, N, PASS>(p, maps, stage, &bars[s], b, d0, t0 + (int64_t)NS * T);
+
+    if constexpr (PRECISE) {
+      chunk_precise<IO, N, PASS>(sm, c, g, Dd, h, Aj, invA, sumDt);
+    } else if constexpr (NPT == 1) {
+      chunk_fast_scalar<IO, PASS>(sm, c, Dd, h[0], A2s, nIs, sumDt);
+    } else {
+      chunk_fast<IO, N, PASS>(sm, c, g, Dd, hp, A2p, nIp, sumDt);
+    }
+    __syncthreads();
+    if (PASS == 0) {
+      // write the y tile back
+      IO* gy = static_cast<IO*>(p.y);
+      const int nrows = (int)min64(CH, p.dim - d0);
+      constexpr int VEC = 16 / sizeof(IO);
+      if (p.vec_io) {
+        const int pieces = tcount / VEC;  // tcount is a multiple of VEC here
+        for (int e = tid; e < nrows * pieces; e += kScanThreads) {
+          const int r = e / pieces, k = e - r * pieces;
+          const uint4 v = *reinterpret_cast<const uint4*>(yTile + r * S::RowY + k * VEC);
+          *reinterpret_cast<uint4*>(gy + (b * p.dim + d0 + r) * p.L + t0 + k * VEC) = v;
+        }
+      } else {
+        for (int e = tid; e < nrows * tcount; e += kScanThreads) {
+          const int r = e / tcount, k = e - r * tcount;
+          gy[(b * p.dim + d0 + r) * p.L + t0 + k] = yTile[r * S::RowY + k];
+        }
+      }
+    }
+  }
+  return -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -374,6 +626,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p,
       A2p[q] = pack2(Aj[2 * q] * kLog2e, Aj[2 * q + 1] * kLog2e);
       nIp[q] = pack2(Aj[2 * q] != 0.f ? -1.f / Aj[2 * q] : 0.f,
                      Aj[2 * q + 1] != 0.f ? -1.f / Aj[2 * q + 1] : 0.f);
+      hp[q] = pack2(h[2 * q], h[2 * q + 1]);
     }
   }
   float invA[NPT];
@@ -381,144 +634,20 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p,
   for (int j = 0; j < NPT; ++j) invA[j] = Aj[j] != 0.f ? 1.f / Aj[j] : 0.f;
 
   float sumDt = 0.f;
-  const float4* DUrow = reinterpret_cast<const float4*>(sm + S::oDU) + c * S::RowDU;
-  const float* Grow = reinterpret_cast<const float*>(sm + S::oGate) + c * S::RowG;
-  const float* Bt = reinterpret_cast<const float*>(sm + S::oBt) + g * NPT;
-  const float* Ct = reinterpret_cast<const float*>(sm + S::oCt) + g * NPT;
-  IO* yT = reinterpret_cast<IO*>(sm + S::oY);
-  bool failed = false;
-  int64_t i = 0;
-
-  for (; i < nchunks; ++i) {
-    const int s = (int)(i % NS);
-    const int64_t t0 = t_begin + i * T;
-    const int tcount = (int)min64(T, t_end - t0);
-    unsigned char* stage = sm + (size_t)s * S::kStage;
-    bool ok = true;
-    if (use_tma) {
-      ok = mbar_wait_bounded(&bars[s], (uint32_t)((i / NS) & 1));
-      prep_chunk<IO, N, PASS, true>(p, stage, sm, b, d0, t0, tcount, precise);
-    } else {
-      prep_chunk<IO, N, PASS, false>(p, stage, sm, b, d0, t0, tcount, precise);
-    }
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    // the raw stage is consumed: refill it with chunk i + NS
-    if (use_tma && tid == 0 && i + NS < nchunks)
-      issue_chunk<IO, N, PASS>(p, maps, stage, &bars[s], b, d0, t0 + (int64_t)NS * T);
-
-    if (!precise) {
-      if constexpr (NPT > 1) {
+  int64_t i = -1;  // chunk whose wait timed out, or -1
+  if (precise) {
+    i = run_chunks<IO, N, PASS, true>(p, maps, sm, bars, b, d0, t_begin, t_end, nchunks, use_tma,
+                                      c, g, Dd, h, hp, A2p, nIp, A2s, nIs, Aj, invA, sumDt);
+  } else {
+    i = run_chunks<IO, N, PASS, false>(p, maps, sm, bars, b, d0, t_begin, t_end, nchunks,
+                                       use_tma, c, g, Dd, h, hp, A2p, nIp, A2s, nIs, Aj, invA,
+                                       sumDt);
+    if constexpr (NPT > 1) {
 #pragma unroll
-        for (int q = 0; q < NP; ++q) hp[q] = pack2(h[2 * q], h[2 * q + 1]);
-      }
-#pragma unroll 2
-      for (int tb = 0; tb < T; tb += G) {
-        float part[G];
-#pragma unroll
-        for (int k = 0; k < G; ++k) {
-          const int t = tb + k;
-          if constexpr (NPT == 1) {
-            const float4 du = DUrow[t];
-            if (PASS == 1) sumDt += du.x;
-            const float a = ex2_fast(du.x * A2s);
-            const float nv = Bt[t * S::RowBC] * du.z * nIs;
-            h[0] = fmaf(a, h[0] - nv, nv);
-            part[k] = PASS == 0 ? Ct[t * S::RowBC] * h[0] : 0.f;
-          } else {
-            f2 dt2, u2;
-            lds_pairs(DUrow + t, dt2, u2);
-            if (PASS == 1) {
-              float lo, hi;
-              unpack2(dt2, lo, hi);
-              sumDt += lo;
-            }
-            f2 bq[NP], cq[NP];
-#pragma unroll
-            for (int q = 0; q + 1 < NP; q += 2) lds_pairs(Bt + t * S::RowBC + 2 * q, bq[q], bq[q + 1]);
-            if constexpr (NP % 2 == 1) lds_pair(Bt + t * S::RowBC + 2 * (NP - 1), bq[NP - 1]);
-            if (PASS == 0) {
-#pragma unroll
-              for (int q = 0; q + 1 < NP; q += 2) lds_pairs(Ct + t * S::RowBC + 2 * q, cq[q], cq[q + 1]);
-              if constexpr (NP % 2 == 1) lds_pair(Ct + t * S::RowBC + 2 * (NP - 1), cq[NP - 1]);
-            }
-            f2 acc2 = pack2(0.f, 0.f);
-#pragma unroll
-            for (int q = 0; q < NP; ++q) {
-              const f2 x = mul2(dt2, A2p[q]);
-              float x0, x1;
-              unpack2(x, x0, x1);
-              const f2 a = pack2(ex2_fast(x0), ex2_fast(x1));
-              const f2 nv = mul2(mul2(bq[q], u2), nIp[q]);
-              hp[q] = fma2(a, sub2(hp[q], nv), nv);
-              if (PASS == 0) acc2 = fma2(cq[q], hp[q], acc2);
-            }
-            float lo, hi;
-            unpack2(acc2, lo, hi);
-            part[k] = lo + hi;
-          }
-        }
-        if (PASS == 0) {
-          const float yv = reduce_scatter<G>(part, g);
-          const int t = tb + g;
-          const float ut = DUrow[t].z;
-          yT[c * S::RowY + t] = io_traits<IO>::from_f32(fmaf(Dd, ut, yv) * Grow[t]);
-        }
-      }
-      if constexpr (NPT > 1) {
-#pragma unroll
-        for (int q = 0; q < NP; ++q) unpack2(hp[q], h[2 * q], h[2 * q + 1]);
-      }
-    } else {
-      for (int tb = 0; tb < T; tb += G) {
-        float part[G];
-#pragma unroll
-        for (int k = 0; k < G; ++k) {
-          const int t = tb + k;
-          const float4 du = DUrow[t];
-          const float dt = du.x, ut = du.z;
-          if (PASS == 1) sumDt += dt;
-          float acc = 0.f;
-#pragma unroll
-          for (int j = 0; j < NPT; ++j) {
-            const float x = dt * Aj[j];
-            const float a = expf(x);
-            const float coef = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
-            h[j] = fmaf(a, h[j], coef * (Bt[t * S::RowBC + j] * ut));
-            if (PASS == 0) acc = fmaf(Ct[t * S::RowBC + j], h[j], acc);
-          }
-          part[k] = acc;
-        }
-        if (PASS == 0) {
-          const float yv = reduce_scatter<G>(part, g);
-          const int t = tb + g;
-          yT[c * S::RowY + t] = io_traits<IO>::from_f32(fmaf(Dd, DUrow[t].z, yv) * Grow[t]);
-        }
-      }
-    }
-    __syncthreads();
-    if (PASS == 0) {
-      // write the y tile back
-      IO* gy = static_cast<IO*>(p.y);
-      const int nrows = (int)min64(CH, p.dim - d0);
-      constexpr int VEC = 16 / sizeof(IO);
-      if (p.vec_io) {
-        const int pieces = tcount / VEC;  // tcount is a multiple of VEC here
-        for (int e = tid; e < nrows * pieces; e += kScanThreads) {
-          const int r = e / pieces, k = e - r * pieces;
-          const uint4 v = *reinterpret_cast<const uint4*>(yT + r * S::RowY + k * VEC);
-          *reinterpret_cast<uint4*>(gy + (b * p.dim + d0 + r) * p.L + t0 + k * VEC) = v;
-        }
-      } else {
-        for (int e = tid; e < nrows * tcount; e += kScanThreads) {
-          const int r = e / tcount, k = e - r * tcount;
-          gy[(b * p.dim + d0 + r) * p.L + t0 + k] = yT[r * S::RowY + k];
-        }
-      }
+      for (int q = 0; q < NP; ++q) unpack2(hp[q], h[2 * q], h[2 * q + 1]);
     }
   }
+  const bool failed = i >= 0;
 
   if (failed) {
     // a TMA chunk did not land in time: record it, let the copies still in
