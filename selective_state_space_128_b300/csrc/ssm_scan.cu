@@ -7,41 +7,40 @@
 // (2), (4) and Algorithm 2; section 4a shape table for the gate; the SSM/Mamba
 // chapter's section 3.1 for D).
 //
-// Design (B300).  The work is bound by the SM's FP32 pipe, not by HBM: per
-// channel step it moves 8 bytes (bf16 u, Δ, z in, y out) but needs N
-// exponentials and about 6N FP32 operations.  So the kernel is organised to
-// spend as few issue slots as possible per state update:
+// Design (B300).  The work is bound by the SM's issue slots and FP32 pipe, not
+// by HBM: per channel step it moves 8 bytes (bf16 u, Δ, z in, y out) but needs
+// N exponentials and about 6N FP32 operations.  A block of 128 threads owns CH
+// channels of one batch row and walks the sequence in chunks of T steps:
 //
-//  * a block owns CH channels of one batch row; each channel is handled by G
-//    lanes holding NPT = N/G states each in fp32 registers for the whole
-//    sequence (the expanded (L, N) state never leaves the SM);
-//  * chunks of T steps of u/Δ/z (a CH x T box) and of B/C (an N x T box,
-//    shared by all channels of the block) are fetched by TMA
-//    (cp.async.bulk.tensor, mbarrier completion) into a ring of raw stages,
-//    prefetched S chunks ahead;
-//  * a cooperative "prep" pass turns a raw stage into fp32 working tiles once
-//    per channel step -- Δ (softplus applied once, not once per lane), u, the
-//    gate silu(z) -- and transposes B/C to [t][n], so that every lane reads
-//    (Δ, Δ, u, u) and its NPT values of B and C with 16-byte shared loads that
-//    land directly in packed register pairs;
-//  * the state update runs on packed f32x2 pairs (one issue for two lanes of
-//    FP32 work) with one MUFU ex2 per state: Ā = 2^(Δ·A·log2 e),
-//    v = -B u / A, h = Ā (h - v) + v, which equals Ā h + (Ā - 1)/A · B u;
-//  * the G partial readouts of a channel are combined by a shuffle
-//    reduce-scatter, after which lane g finishes time step g of each group of
-//    G steps (D term, gate, rounding) into a y tile that the block writes back
-//    with 16-byte stores.
+//  * TMA (cp.async.bulk.tensor, mbarrier completion) fetches each chunk into a
+//    ring of NS raw stages: a CH x T box of u/Δ/z and the N x T box of B/C,
+//    which all channels of the block share;
+//  * each channel is handled by G lanes holding NPT = N/G states in fp32
+//    registers for the whole sequence (the expanded (L, N) state never leaves
+//    the SM).  A state update is one MUFU ex2 and packed f32x2 arithmetic:
+//    Ā = 2^(Δ·A·log2 e), v = -B u / A, h = Ā (h - v) + v  (= Ā h + B̄ u);
+//    each lane writes its partial readout Σ_{its n} C_n h_n per step to a
+//    partial tile, so the recurrence carries no cross-lane reduction;
+//  * the per-channel-step work that is not per state -- Δ = softplus(.) once
+//    (not once per lane), the gate silu(z), the transposition of B/C to
+//    [t][n], and the finalisation y = (Σ partials + D u) · gate with 16-byte
+//    stores -- is software-pipelined across chunks: while its lanes run the
+//    recurrence of chunk i, every thread also converts its share of chunk i+1
+//    (into a second of three working buffers) and finalises its share of
+//    chunk i-1 (from a second partial buffer).  The three streams are
+//    independent, so the compiler interleaves them and each hides the others'
+//    latencies; one block barrier per chunk hands the buffers over.
 //
 // Long sequences with few channels are split into segments (grid.z): pass 1
 // computes each segment's end state from zero and its ΣΔ, pass 0 folds the
 // carries of earlier segments (h <- exp(A ΣΔ_k) h + h_k) into its initial state
 // and recomputes its segment with outputs.  There is no inter-block waiting.
-// The only waits are on the block's own TMA barriers; they give up after a
-// time limit, record it in a device error word (read by ssm_status) and end the block.
+// The only waits are on the block's own TMA barriers; they are bounded, and a
+// wait that runs out records an error in a device word (read by ssm_status)
+// and ends the block after its copies in flight have landed.
 #include <cuda.h>
 
 #include <cstring>
-#include <type_traits>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -52,25 +51,35 @@ namespace ssm {
 __device__ int g_scan_error;
 
 // Per-N tiling: NPT states per lane, G lanes per channel, CH channels per
-// block, T steps per chunk, S raw stages in flight.
+// block, T steps per chunk, NS raw stages, E channel steps per thread in the
+// per-step (conversion and finalisation) work.
 template <int N> struct ScanCfg {
-  static constexpr int NPT = N <= 4 ? N : (N <= 16 ? 4 : N / 4);
+  static constexpr int NPT = N <= 2 ? N : (N == 4 ? 2 : (N <= 16 ? 4 : N / 4));
   static constexpr int G = N / NPT;
   static constexpr int CH = kScanThreads / G;
-  static constexpr int T = 32;
-  static constexpr int S = 2;
+  static constexpr int T = 16;
+  static constexpr int NS = 3;
+  static constexpr int E = CH * T / kScanThreads;
+  // warp layout: a warp holds CW channels x GW state groups, so that a shared
+  // load of B/C rows touches at most two distinct addresses per warp
+  static constexpr int GW = G < 2 ? G : 2;
+  static constexpr int CW = 32 / GW;
+  static constexpr int WPC = G / GW;  // warps per set of CW channels
   static_assert(G * NPT == N, "tiling");
-  static_assert(T % G == 0 && T % 8 == 0, "chunk");
+  static_assert(T == 16, "the partial-tile swizzle assumes 4 units of 4 steps");
+  static_assert(E == 4 || E == 8 || E == 16, "per-thread step count");
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Shared-memory layout of one block.  Raw stages are TMA destinations
-// (128-byte aligned); the working tiles are padded so that the lanes of a warp
-// hit distinct banks.
+// (128-byte aligned); the working tiles are padded or swizzled so that the
+// lanes of a warp hit distinct banks.
 template <typename IO, int N> struct ScanSmem {
   using Cf = ScanCfg<N>;
-  static constexpr int CH = Cf::CH, T = Cf::T, S = Cf::S;
+  static constexpr int CH = Cf::CH, T = Cf::T, NS = Cf::NS;
+  static constexpr int NBT = 3;  // working-tile buffers (chunks i-1, i, i+1)
+  static constexpr int NBP = 2;  // partial buffers (chunks i-1, i)
   static constexpr size_t kRawIO = (size_t)CH * T * sizeof(IO);  // one of u / Δ / z
   static constexpr size_t kRawBC = (size_t)N * T * 4;              // one of B / C
   static constexpr size_t oRawU = 0;
@@ -79,18 +88,24 @@ template <typename IO, int N> struct ScanSmem {
   static constexpr size_t oRawB = align_up(oRawZ + kRawIO, 128);
   static constexpr size_t oRawC = align_up(oRawB + kRawBC, 128);
   static constexpr size_t kStage = align_up(oRawC + kRawBC, 128);
-  static constexpr int RowDU = T + 1;                 // float4 per row (+1 breaks bank aliasing)
-  static constexpr int RowG = T + 4;                  // floats per gate row
-  static constexpr int RowBC = N + 4;                 // floats per transposed B/C row
-  static constexpr int RowY = T + 16 / (int)sizeof(IO);  // elements per y row (16-byte multiple)
-  static constexpr size_t oDU = (size_t)S * kStage;
-  static constexpr size_t oGate = align_up(oDU + (size_t)CH * RowDU * 16, 16);
-  static constexpr size_t oBt = align_up(oGate + (size_t)CH * RowG * 4, 16);
-  static constexpr size_t oCt = align_up(oBt + (size_t)T * RowBC * 4, 16);
-  static constexpr size_t oY = align_up(oCt + (size_t)T * RowBC * 4, 16);
-  static constexpr size_t oBias = align_up(oY + (size_t)CH * RowY * sizeof(IO), 16);
-  static constexpr size_t oBar = align_up(oBias + (size_t)CH * 4, 8);
-  static constexpr size_t kBytes = oBar + 8 * S;
+  static constexpr int RowF = T + 1;   // floats per Δ / u row (odd: lanes of a warp read
+                                       // 16 channels at one step from distinct banks)
+  static constexpr int RowG = T + 4;   // floats per gate row
+  static constexpr int RowBC = N + 4;  // floats per transposed B/C row
+  // a working buffer: Δ [CH][RowF], u [CH][RowF], gate [CH][RowG], Bt/Ct [T][RowBC]
+  static constexpr size_t bDT = 0;
+  static constexpr size_t bU = align_up(bDT + (size_t)CH * RowF * 4, 16);
+  static constexpr size_t bGate = align_up(bU + (size_t)CH * RowF * 4, 16);
+  static constexpr size_t bBt = align_up(bGate + (size_t)CH * RowG * 4, 16);
+  static constexpr size_t bCt = align_up(bBt + (size_t)T * RowBC * 4, 16);
+  static constexpr size_t kBuf = align_up(bCt + (size_t)T * RowBC * 4, 128);
+  static constexpr size_t kPart = (size_t)kScanThreads * T * 4;  // partials [lane][T], swizzled
+  static constexpr size_t oBuf = (size_t)NS * kStage;
+  static constexpr size_t oPart = oBuf + (size_t)NBT * kBuf;
+  static constexpr size_t oBias = oPart + (size_t)NBP * kPart;
+  static constexpr size_t oD = align_up(oBias + (size_t)CH * 4, 16);
+  static constexpr size_t oBar = align_up(oD + (size_t)CH * 4, 8);
+  static constexpr size_t kBytes = oBar + 8 * NS;
   static constexpr size_t kLaunchBytes = kBytes + 128;  // room to align the base to 128
 };
 
@@ -105,6 +120,9 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
@@ -127,7 +145,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 // Wait for phase `parity` of `bar`, giving up after kWaitLimitNs.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a TMA chunk lands in microseconds
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: every hand-over takes microseconds
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -147,7 +165,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
-// 16-byte shared load into two packed pairs.
+// 16-byte shared load into two packed pairs; 8-byte load into one.
 __device__ __forceinline__ void lds_pairs(const void* p, f2& a, f2& b) {
   asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a.r), "=l"(b.r) : "r"(smem_u32(p)));
 }
@@ -155,147 +173,72 @@ __device__ __forceinline__ void lds_pair(const void* p, f2& a) {
   asm volatile("ld.shared.b64 %0, [%1];" : "=l"(a.r) : "r"(smem_u32(p)));
 }
 
-// The four tensor maps of a launch (u, Δ, z: box CH x T; B, C: box N x T).
+// Index (in floats) of steps 4u..4u+3 of partial row `row` in a P tile: the
+// 16-byte unit is XOR-swizzled so that 8 consecutive rows hit distinct banks.
+__device__ __forceinline__ int p_index(int row, int unit) {
+  return row * 16 + ((unit ^ ((row >> 1) & 3)) << 2);
+}
+
+// The five tensor maps of a launch (u, Δ, z: box CH x T; B, C: box N x T).
 struct ScanMaps {
   CUtensorMap u, d, z, b, c;
 };
 
-// ---------------------------------------------------------------------------
-// Staging and prep
-// ---------------------------------------------------------------------------
-template <typename IO> __device__ __forceinline__ void load8(const IO* p, float (&v)[8]);
-template <> __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 w = *reinterpret_cast<const uint4*>(p);
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(ws[i] << 16);
-    v[2 * i + 1] = __uint_as_float(ws[i] & 0xffff0000u);
-  }
-}
-template <> __device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
-// Per element of the chunk: Δ (softplus once), u and the gate into the fp32
-// working tiles.  Steps past tcount and rows past the channel count get Δ = 0
-// and u = 0, exact no-ops of the recurrence (Ā = 1, B̄ u = 0).  The flags are
-// template parameters so that the element loop carries no per-element branch.
-template <typename IO, int N, int PASS, bool TMA, bool PRECISE, bool SP, bool HZ, bool MASK>
-__device__ __forceinline__ void prep_elems(const ScanArgs& p, const unsigned char* stage,
-                                           unsigned char* sm, int64_t b, int64_t d0, int64_t t0,
-                                           int tcount, int nrows) {
-  using S = ScanSmem<IO, N>;
-  constexpr int CH = S::CH, T = S::T;
-  const int tid = threadIdx.x;
-  float4* DU = reinterpret_cast<float4*>(sm + S::oDU);
-  float* Gt = reinterpret_cast<float*>(sm + S::oGate);
-  const float* sBias = reinterpret_cast<const float*>(sm + S::oBias);
-#pragma unroll 1
-  for (int e = tid; e < CH * (T / 8); e += kScanThreads) {
-    const int r = e / (T / 8), t8 = (e - r * (T / 8)) * 8;
-    float dl[8], uu[8], zz[8];
-    if (TMA) {
-      load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawD) + r * T + t8, dl);
-      load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawU) + r * T + t8, uu);
-      if (HZ) load8<IO>(reinterpret_cast<const IO*>(stage + S::oRawZ) + r * T + t8, zz);
+template <typename IO, int E> struct vecio;
+template <int E> struct vecio<__nv_bfloat16, E> {
+  // E consecutive bf16 -> float (E = 4: 8 bytes, 8: 16 bytes, 16: 32 bytes)
+  __device__ static void load(const __nv_bfloat16* p, float (&v)[E]) {
+    uint32_t w[E / 2];
+    if constexpr (E == 4) {
+      const uint2 q = *reinterpret_cast<const uint2*>(p);
+      w[0] = q.x; w[1] = q.y;
     } else {
-      const int64_t row = (b * p.dim + d0 + r) * p.L + t0 + t8;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool ok = r < nrows && t8 + j < tcount;
-        dl[j] = ok ? io_traits<IO>::to_f32(static_cast<const IO*>(p.delta)[row + j]) : 0.f;
-        uu[j] = ok ? io_traits<IO>::to_f32(static_cast<const IO*>(p.u)[row + j]) : 0.f;
-        zz[j] = (ok && HZ) ? io_traits<IO>::to_f32(static_cast<const IO*>(p.z)[row + j]) : 0.f;
+      for (int k = 0; k < E / 8; ++k) {
+        const uint4 q = reinterpret_cast<const uint4*>(p)[k];
+        w[4 * k] = q.x; w[4 * k + 1] = q.y; w[4 * k + 2] = q.z; w[4 * k + 3] = q.w;
       }
     }
-    const float bias = sBias[r];
-    float gate[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float x = dl[j] + bias;
-      float dt = SP ? (PRECISE ? softplus_precise(x) : softplus_fast(x)) : x;
-      float u = uu[j];
-      if (MASK) {
-        const bool ok = r < nrows && t8 + j < tcount;
-        dt = ok ? dt : 0.f;
-        u = ok ? u : 0.f;
-      }
-      DU[r * S::RowDU + t8 + j] = make_float4(dt, dt, u, u);
-      gate[j] = HZ ? (PRECISE ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
-    }
-    if (PASS == 0) {
-      float4* g4 = reinterpret_cast<float4*>(Gt + r * S::RowG + t8);
-      g4[0] = make_float4(gate[0], gate[1], gate[2], gate[3]);
-      g4[1] = make_float4(gate[4], gate[5], gate[6], gate[7]);
+    for (int i = 0; i < E / 2; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
   }
-}
-
-template <typename IO, int N, int PASS, bool TMA, bool PRECISE>
-__device__ __forceinline__ void prep_chunk(const ScanArgs& p, const unsigned char* stage,
-                                           unsigned char* sm, int64_t b, int64_t d0, int64_t t0,
-                                           int tcount) {
-  using S = ScanSmem<IO, N>;
-  constexpr int CH = S::CH, T = S::T;
-  const int tid = threadIdx.x;
-  const int nrows = (int)min64(CH, p.dim - d0);
-  const bool mask = tcount < T || nrows < CH;
-  const bool hz = PASS == 0 && p.z != nullptr;
-#define SSM_PREP(SP, HZ, MASK) \
-  prep_elems<IO, N, PASS, TMA, PRECISE, SP, HZ, MASK>(p, stage, sm, b, d0, t0, tcount, nrows)
-  if (p.softplus) {
-    if (hz) { if (mask) SSM_PREP(true, true, true); else SSM_PREP(true, true, false); }
-    else    { if (mask) SSM_PREP(true, false, true); else SSM_PREP(true, false, false); }
-  } else {
-    if (hz) { if (mask) SSM_PREP(false, true, true); else SSM_PREP(false, true, false); }
-    else    { if (mask) SSM_PREP(false, false, true); else SSM_PREP(false, false, false); }
-  }
-#undef SSM_PREP
-  // B / C transposed to [t][n]
-  float* Bt = reinterpret_cast<float*>(sm + S::oBt);
-  float* Ct = reinterpret_cast<float*>(sm + S::oCt);
-  constexpr int NARR = PASS == 0 ? 2 : 1;
-#pragma unroll 1
-  for (int e = tid; e < NARR * N * (T / 4); e += kScanThreads) {
-    const int arr = e / (N * (T / 4));
-    const int rem = e - arr * (N * (T / 4));
-    const int n = rem / (T / 4), t4 = (rem - n * (T / 4)) * 4;
-    float v[4];
-    if (TMA) {
-      const float4 q = *reinterpret_cast<const float4*>(
-          reinterpret_cast<const float*>(stage + (arr == 0 ? S::oRawB : S::oRawC)) + n * T + t4);
-      v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  __device__ static void store(__nv_bfloat16* p, const float (&v)[E]) {
+    uint32_t w[E / 2];
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
     } else {
-      const float* src = (arr == 0 ? p.B : p.C) + (b * N + n) * p.L + t0 + t4;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = t4 + j < tcount ? src[j] : 0.f;
+      for (int k = 0; k < E / 8; ++k)
+        reinterpret_cast<uint4*>(p)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
     }
-    float* dst = arr == 0 ? Bt : Ct;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) dst[(t4 + j) * S::RowBC + n] = v[j];
   }
-}
+};
+template <int E> struct vecio<float, E> {
+  __device__ static void load(const float* p, float (&v)[E]) {
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k) {
+      const float4 q = reinterpret_cast<const float4*>(p)[k];
+      v[4 * k] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
+    }
+  }
+  __device__ static void store(float* p, const float (&v)[E]) {
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k)
+      reinterpret_cast<float4*>(p)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+};
 
-// Combine the G partial readouts of a channel: afterwards lane g holds the full
-// sum for time step g of the group (shuffle reduce-scatter, log2(G) stages).
-template <int G>
-__device__ __forceinline__ float reduce_scatter(float (&part)[G], int g) {
-#pragma unroll
-  for (int s = G / 2; s >= 1; s /= 2) {
-    const bool upper = (g & s) != 0;
-#pragma unroll
-    for (int k = 0; k < s; ++k) {
-      const float send = upper ? part[k] : part[k + s];
-      const float keep = upper ? part[k + s] : part[k];
-      part[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-    }
-  }
-  return part[0];
-}
+// ---------------------------------------------------------------------------
+// Chunk staging
+// ---------------------------------------------------------------------------
 
 // Issue the TMA loads of one chunk into a raw stage (one thread).
 template <typename IO, int N, int PASS>
@@ -314,68 +257,200 @@ __device__ __forceinline__ void issue_chunk(const ScanArgs& p, const ScanMaps& m
   if (PASS == 0) tma_load_3d(stage + S::oRawC, &m.c, bar, x, 0, z);
 }
 
-// ---------------------------------------------------------------------------
-// One chunk of T steps for one lane, fast flavour (MUFU ex2, packed f32x2).
-// The step loop is fully unrolled and the Ā / v pairs of step t+1 are formed
-// while step t updates the state, so that the serial chain per step is just
-// h <- Ā (h - v) + v and the readout.
-// ---------------------------------------------------------------------------
+// Without TMA (rows not 16-byte aligned): all threads copy one chunk into a
+// raw stage with bounds-checked element loads, zero outside the data.
 template <typename IO, int N, int PASS>
-__device__ __forceinline__ void chunk_fast(unsigned char* sm, int c, int g, float Dd,
-                                           f2 (&hp)[ScanCfg<N>::NPT / 2],
-                                           const f2 (&A2p)[ScanCfg<N>::NPT / 2],
+__device__ __forceinline__ void load_chunk_plain(const ScanArgs& p, unsigned char* stage, int tid,
+                                                 int64_t b, int64_t d0, int64_t t0) {
+  using S = ScanSmem<IO, N>;
+  constexpr int CH = S::CH, T = S::T;
+  const bool has_z = PASS == 0 && p.z != nullptr;
+  const IO zero = io_traits<IO>::from_f32(0.f);
+  for (int e = tid; e < CH * T; e += kScanThreads) {
+    const int r = e / T, t = e - r * T;
+    const bool ok = d0 + r < p.dim && t0 + t < p.L;
+    const int64_t gi = ((b * p.dim + d0 + r) * p.L + t0 + t);
+    reinterpret_cast<IO*>(stage + S::oRawU)[e] = ok ? static_cast<const IO*>(p.u)[gi] : zero;
+    reinterpret_cast<IO*>(stage + S::oRawD)[e] = ok ? static_cast<const IO*>(p.delta)[gi] : zero;
+    if (has_z) reinterpret_cast<IO*>(stage + S::oRawZ)[e] = ok ? static_cast<const IO*>(p.z)[gi] : zero;
+  }
+  for (int e = tid; e < N * T; e += kScanThreads) {
+    const int n = e / T, t = e - n * T;
+    const bool ok = t0 + t < p.L;
+    const int64_t gi = (b * N + n) * p.L + t0 + t;
+    reinterpret_cast<float*>(stage + S::oRawB)[e] = ok ? p.B[gi] : 0.f;
+    if (PASS == 0) reinterpret_cast<float*>(stage + S::oRawC)[e] = ok ? p.C[gi] : 0.f;
+  }
+}
+
+// Flags of the per-step work.  FAST fixes the common case at compile time
+// (fast arithmetic, softplus on, gate present); otherwise they are read at run
+// time.
+struct StepFlags {
+  bool precise, softplus, gate;
+};
+
+// This thread's share of converting a raw stage into a working buffer: E
+// consecutive steps of channel row r.  Δ gets softplus once per channel step;
+// steps past tcount and rows past nrows get Δ = 0 and u = 0, exact no-ops of
+// the recurrence (Ā = 1, B̄ u = 0).  B/C are transposed to [t][n].
+template <typename IO, int N, int PASS, bool FAST>
+__device__ __forceinline__ void prep_share(const unsigned char* stage, unsigned char* buf,
+                                           const float* sBias, int tid, int tcount, int nrows,
+                                           StepFlags f) {
+  using S = ScanSmem<IO, N>;
+  using Cf = ScanCfg<N>;
+  constexpr int T = S::T, E = Cf::E;
+  const bool precise = FAST ? false : f.precise;
+  const bool sp = FAST ? true : f.softplus;
+  const bool hz = PASS == 0 && (FAST ? true : f.gate);
+  const int r = tid / (T / E), te = (tid - r * (T / E)) * E;
+  float dl[E], uu[E], zz[E];
+  vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawD) + r * T + te, dl);
+  vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawU) + r * T + te, uu);
+  if (hz) vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawZ) + r * T + te, zz);
+  const float bias = sBias[r];
+  float* DT = reinterpret_cast<float*>(buf + S::bDT) + r * S::RowF + te;
+  float* Ut = reinterpret_cast<float*>(buf + S::bU) + r * S::RowF + te;
+  float gate[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    const float x = dl[j] + bias;
+    float dt = sp ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
+    const bool ok = r < nrows && te + j < tcount;
+    dt = ok ? dt : 0.f;
+    const float u = ok ? uu[j] : 0.f;
+    DT[j] = dt;
+    Ut[j] = u;
+    gate[j] = hz ? (precise ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
+  }
+  if (PASS == 0) {
+    float4* g4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(buf + S::bGate) + r * S::RowG + te);
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k)
+      g4[k] = make_float4(gate[4 * k], gate[4 * k + 1], gate[4 * k + 2], gate[4 * k + 3]);
+  }
+  // B / C transposed to [t][n]
+  constexpr int NT = N * T;
+  constexpr int PER = (NT + kScanThreads - 1) / kScanThreads;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int e = tid + k * kScanThreads;
+    if (NT % kScanThreads == 0 || e < NT) {
+      const int n = e / T, t = e - n * T;
+      reinterpret_cast<float*>(buf + S::bBt)[t * S::RowBC + n] =
+          reinterpret_cast<const float*>(stage + S::oRawB)[e];
+      if (PASS == 0)
+        reinterpret_cast<float*>(buf + S::bCt)[t * S::RowBC + n] =
+            reinterpret_cast<const float*>(stage + S::oRawC)[e];
+    }
+  }
+}
+
+// This thread's share of finalising a chunk: E consecutive outputs of channel
+// row r: y = (Σ_g partials + D u) · gate, rounded, stored at `dst` (this
+// thread's first output of the chunk in HBM) when `store`.
+template <typename IO, int N>
+__device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned char* buf,
+                                               const float* part, const float* sD, int tid,
+                                               IO* dst, int tcount, int nrows, bool store) {
+  using S = ScanSmem<IO, N>;
+  using Cf = ScanCfg<N>;
+  constexpr int T = S::T, G = Cf::G, E = Cf::E;
+  const int r = tid / (T / E), te = (tid - r * (T / E)) * E;
+  float acc[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) acc[j] = 0.f;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k) {
+      const float4 q = *reinterpret_cast<const float4*>(part + p_index(g * S::CH + r, te / 4 + k));
+      acc[4 * k] += q.x; acc[4 * k + 1] += q.y; acc[4 * k + 2] += q.z; acc[4 * k + 3] += q.w;
+    }
+  }
+  const float Dd = sD[r];
+  const float* Ut = reinterpret_cast<const float*>(buf + S::bU) + r * S::RowF + te;
+  const float4* g4 = reinterpret_cast<const float4*>(
+      reinterpret_cast<const float*>(buf + S::bGate) + r * S::RowG + te);
+  float y[E];
+#pragma unroll
+  for (int k = 0; k < E / 4; ++k) {
+    const float4 gk = g4[k];
+    const float gg[4] = {gk.x, gk.y, gk.z, gk.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) y[4 * k + j] = fmaf(Dd, Ut[4 * k + j], acc[4 * k + j]) * gg[j];
+  }
+  if (!store || r >= nrows) return;
+  if (p.vec_io && te + E <= tcount) {
+    vecio<IO, E>::store(dst, y);
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+      if (te + j < tcount) dst[j] = io_traits<IO>::from_f32(y[j]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The recurrence over one chunk for one lane
+// ---------------------------------------------------------------------------
+
+// Fast flavour (MUFU ex2, packed f32x2).  The step loop is fully unrolled and
+// software-pipelined three deep: the shared loads of step t+2, the
+// exponentials and v of step t+1 and the state update of step t are
+// independent, so their latencies overlap.  Per step a lane reads Δ and u of
+// its channel (one 4-byte load each: a warp covers 16 channels in one
+// wavefront) and its NPT values of B and C (16-byte loads that touch at most
+// two distinct addresses per warp).
+template <typename IO, int N, int PASS>
+__device__ __forceinline__ void chunk_fast(const unsigned char* buf, float* part, int prow, int c,
+                                           int g, f2 (&hp)[ScanCfg<N>::NPT / 2],
+                                           const float (&A2)[ScanCfg<N>::NPT],
                                            const f2 (&nIp)[ScanCfg<N>::NPT / 2], float& sumDt) {
   using Cf = ScanCfg<N>;
   using S = ScanSmem<IO, N>;
-  constexpr int NPT = Cf::NPT, G = Cf::G, T = Cf::T, NP = NPT / 2;
-  const float4* DUrow = reinterpret_cast<const float4*>(sm + S::oDU) + c * S::RowDU;
-  const float* Grow = reinterpret_cast<const float*>(sm + S::oGate) + c * S::RowG;
-  const float* Bt = reinterpret_cast<const float*>(sm + S::oBt) + g * NPT;
-  const float* Ct = reinterpret_cast<const float*>(sm + S::oCt) + g * NPT;
-  IO* yT = reinterpret_cast<IO*>(sm + S::oY) + c * S::RowY;
+  constexpr int NPT = Cf::NPT, T = Cf::T, NP = NPT / 2;
+  const float* DTrow = reinterpret_cast<const float*>(buf + S::bDT) + c * S::RowF;
+  const float* Urow = reinterpret_cast<const float*>(buf + S::bU) + c * S::RowF;
+  const float* Bt = reinterpret_cast<const float*>(buf + S::bBt) + g * NPT;
+  const float* Ct = reinterpret_cast<const float*>(buf + S::bCt) + g * NPT;
 
   auto load_row = [](const float* row, f2 (&v)[NP]) {
 #pragma unroll
     for (int q = 0; q + 1 < NP; q += 2) lds_pairs(row + 2 * q, v[q], v[q + 1]);
     if constexpr (NP % 2 == 1) lds_pair(row + 2 * (NP - 1), v[NP - 1]);
   };
-  // Three-deep software pipeline over the fully unrolled steps: the shared
-  // loads of step t+2, the exponentials and v of step t+1 and the state
-  // update of step t are independent, so their latencies overlap.
-  f2 dt_l, u_l, b_l[NP], c_l[NP];      // loaded for step t+1
-  f2 a_c[NP], v_c[NP], c_c[NP];        // ready for step t
-  auto load_step = [&](int t, f2& dt2, f2& u2, f2 (&bq)[NP], f2 (&cq)[NP]) {
-    lds_pairs(DUrow + t, dt2, u2);
+  auto load_step = [&](int t, float& dt, float& u, f2 (&bq)[NP], f2 (&cq)[NP]) {
+    dt = DTrow[t];
+    u = Urow[t];
     load_row(Bt + t * S::RowBC, bq);
     if (PASS == 0) load_row(Ct + t * S::RowBC, cq);
   };
-  auto discretise = [&](const f2& dt2, const f2& u2, const f2 (&bq)[NP], f2 (&ao)[NP],
-                        f2 (&vo)[NP]) {
-    if (PASS == 1) {
-      float lo, hi;
-      unpack2(dt2, lo, hi);
-      sumDt += lo;
-    }
+  auto discretise = [&](float dt, float u, const f2 (&bq)[NP], f2 (&ao)[NP], f2 (&vo)[NP]) {
+    if (PASS == 1) sumDt += dt;
+    const f2 u2 = pack2(u, u);
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-      const f2 x = mul2(dt2, A2p[q]);
-      float x0, x1;
-      unpack2(x, x0, x1);
-      ao[q] = pack2(ex2_fast(x0), ex2_fast(x1));
+      ao[q] = pack2(ex2_fast(dt * A2[2 * q]), ex2_fast(dt * A2[2 * q + 1]));
       vo[q] = mul2(mul2(bq[q], u2), nIp[q]);
     }
   };
 
+  float dt_l, u_l;                 // loaded for step t+1
+  f2 b_l[NP], c_l[NP];
+  f2 a_c[NP], v_c[NP], c_c[NP];    // ready for step t
   {
-    f2 dt0, u0, b0[NP];
+    float dt0, u0;
+    f2 b0[NP];
     load_step(0, dt0, u0, b0, c_c);
     discretise(dt0, u0, b0, a_c, v_c);
     load_step(1, dt_l, u_l, b_l, c_l);
   }
-  float part[G];
+  float acc[4];
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    f2 dt_n, u_n, b_n[NP], c_n[NP], a_n[NP], v_n[NP];
+    float dt_n, u_n;
+    f2 b_n[NP], c_n[NP], a_n[NP], v_n[NP];
     if (t + 2 < T) load_step(t + 2, dt_n, u_n, b_n, c_n);
     if (t + 1 < T) discretise(dt_l, u_l, b_l, a_n, v_n);
 #pragma unroll
@@ -386,12 +461,10 @@ __device__ __forceinline__ void chunk_fast(unsigned char* sm, int c, int g, floa
       for (int q = 1; q < NP; ++q) acc2 = fma2(c_c[q], hp[q], acc2);
       float lo, hi;
       unpack2(acc2, lo, hi);
-      part[t % G] = lo + hi;
-      if (t % G == G - 1) {
-        const float yv = reduce_scatter<G>(part, g);
-        const int ty = t - (G - 1) + g;
-        yT[ty] = io_traits<IO>::from_f32(fmaf(Dd, DUrow[ty].z, yv) * Grow[ty]);
-      }
+      acc[t % 4] = lo + hi;
+      if (t % 4 == 3)
+        *reinterpret_cast<float4*>(part + p_index(prow, t / 4)) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
     if (t + 1 < T) {
 #pragma unroll
@@ -413,49 +486,53 @@ __device__ __forceinline__ void chunk_fast(unsigned char* sm, int c, int g, floa
   }
 }
 
-// One chunk, one state per lane (N = 1), fast flavour.
+// Fast flavour, one state per lane (N = 1).
 template <typename IO, int PASS>
-__device__ __forceinline__ void chunk_fast_scalar(unsigned char* sm, int c, float Dd, float& h,
-                                                  float A2s, float nIs, float& sumDt) {
+__device__ __forceinline__ void chunk_fast_scalar(const unsigned char* buf, float* part, int prow,
+                                                  int c, float& h, float A2s, float nIs,
+                                                  float& sumDt) {
   using S = ScanSmem<IO, 1>;
   constexpr int T = ScanCfg<1>::T;
-  const float4* DUrow = reinterpret_cast<const float4*>(sm + S::oDU) + c * S::RowDU;
-  const float* Grow = reinterpret_cast<const float*>(sm + S::oGate) + c * S::RowG;
-  const float* Bt = reinterpret_cast<const float*>(sm + S::oBt);
-  const float* Ct = reinterpret_cast<const float*>(sm + S::oCt);
-  IO* yT = reinterpret_cast<IO*>(sm + S::oY) + c * S::RowY;
-#pragma unroll 8
+  const float* DTrow = reinterpret_cast<const float*>(buf + S::bDT) + c * S::RowF;
+  const float* Urow = reinterpret_cast<const float*>(buf + S::bU) + c * S::RowF;
+  const float* Bt = reinterpret_cast<const float*>(buf + S::bBt);
+  const float* Ct = reinterpret_cast<const float*>(buf + S::bCt);
+  float acc[4];
+#pragma unroll
   for (int t = 0; t < T; ++t) {
-    const float4 du = DUrow[t];
-    if (PASS == 1) sumDt += du.x;
-    const float a = ex2_fast(du.x * A2s);
-    const float nv = Bt[t * S::RowBC] * du.z * nIs;
+    const float dt = DTrow[t], u = Urow[t];
+    if (PASS == 1) sumDt += dt;
+    const float a = ex2_fast(dt * A2s);
+    const float nv = Bt[t * S::RowBC] * u * nIs;
     h = fmaf(a, h - nv, nv);
-    if (PASS == 0) yT[t] = io_traits<IO>::from_f32(fmaf(Dd, du.z, Ct[t * S::RowBC] * h) * Grow[t]);
+    if (PASS == 0) {
+      acc[t % 4] = Ct[t * S::RowBC] * h;
+      if (t % 4 == 3)
+        *reinterpret_cast<float4*>(part + p_index(prow, t / 4)) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
   }
 }
 
-// One chunk, precise flavour (CUDA libm expf / expm1f; A = 0 takes the limit).
+// Precise flavour (CUDA libm expf / expm1f; A = 0 takes the limit Δ B).
 template <typename IO, int N, int PASS>
-__device__ __forceinline__ void chunk_precise(unsigned char* sm, int c, int g, float Dd,
-                                              float (&h)[ScanCfg<N>::NPT],
+__device__ __forceinline__ void chunk_precise(const unsigned char* buf, float* part, int prow,
+                                              int c, int g, float (&h)[ScanCfg<N>::NPT],
                                               const float (&Aj)[ScanCfg<N>::NPT],
                                               const float (&invA)[ScanCfg<N>::NPT], float& sumDt) {
   using Cf = ScanCfg<N>;
   using S = ScanSmem<IO, N>;
-  constexpr int NPT = Cf::NPT, G = Cf::G, T = Cf::T;
-  const float4* DUrow = reinterpret_cast<const float4*>(sm + S::oDU) + c * S::RowDU;
-  const float* Grow = reinterpret_cast<const float*>(sm + S::oGate) + c * S::RowG;
-  const float* Bt = reinterpret_cast<const float*>(sm + S::oBt) + g * NPT;
-  const float* Ct = reinterpret_cast<const float*>(sm + S::oCt) + g * NPT;
-  IO* yT = reinterpret_cast<IO*>(sm + S::oY) + c * S::RowY;
-  for (int tb = 0; tb < T; tb += G) {
-    float part[G];
+  constexpr int NPT = Cf::NPT, T = Cf::T;
+  const float* DTrow = reinterpret_cast<const float*>(buf + S::bDT) + c * S::RowF;
+  const float* Urow = reinterpret_cast<const float*>(buf + S::bU) + c * S::RowF;
+  const float* Bt = reinterpret_cast<const float*>(buf + S::bBt) + g * NPT;
+  const float* Ct = reinterpret_cast<const float*>(buf + S::bCt) + g * NPT;
+  for (int t4 = 0; t4 < T; t4 += 4) {
+    float acc4[4];
 #pragma unroll
-    for (int k = 0; k < G; ++k) {
-      const int t = tb + k;
-      const float4 du = DUrow[t];
-      const float dt = du.x, ut = du.z;
+    for (int k = 0; k < 4; ++k) {
+      const int t = t4 + k;
+      const float dt = DTrow[t], ut = Urow[t];
       if (PASS == 1) sumDt += dt;
       float acc = 0.f;
 #pragma unroll
@@ -466,78 +543,45 @@ __device__ __forceinline__ void chunk_precise(unsigned char* sm, int c, int g, f
         h[j] = fmaf(a, h[j], coef * (Bt[t * S::RowBC + j] * ut));
         if (PASS == 0) acc = fmaf(Ct[t * S::RowBC + j], h[j], acc);
       }
-      part[k] = acc;
+      acc4[k] = acc;
     }
-    if (PASS == 0) {
-      const float yv = reduce_scatter<G>(part, g);
-      const int t = tb + g;
-      yT[t] = io_traits<IO>::from_f32(fmaf(Dd, DUrow[t].z, yv) * Grow[t]);
-    }
+    if (PASS == 0)
+      *reinterpret_cast<float4*>(part + p_index(prow, t4 / 4)) =
+          make_float4(acc4[0], acc4[1], acc4[2], acc4[3]);
   }
 }
 
-// The chunk loop of one block: wait for chunk i's TMA stage, prep it, refill
-// the stage with chunk i + S, run the steps, write the y tile back.  Returns
-// the index of a chunk whose wait timed out, or -1.
-template <typename IO, int N, int PASS, bool PRECISE>
-__device__ __forceinline__ int64_t run_chunks(
-    const ScanArgs& p, const ScanMaps& maps, unsigned char* sm, uint64_t* bars, int64_t b,
-    int64_t d0, int64_t t_begin, int64_t t_end, int64_t nchunks, bool use_tma, int c, int g,
-    float Dd, float (&h)[ScanCfg<N>::NPT], f2 (&hp)[ScanCfg<N>::NPT / 2 > 0 ? ScanCfg<N>::NPT / 2 : 1],
-    const f2 (&A2p)[ScanCfg<N>::NPT / 2 > 0 ? ScanCfg<N>::NPT / 2 : 1],
-    const f2 (&nIp)[ScanCfg<N>::NPT / 2 > 0 ? ScanCfg<N>::NPT / 2 : 1], float A2s, float nIs,
-    const float (&Aj)[ScanCfg<N>::NPT], const float (&invA)[ScanCfg<N>::NPT], float& sumDt) {
-  using Cf = ScanCfg<N>;
-  using S = ScanSmem<IO, N>;
-  constexpr int NPT = Cf::NPT, CH = Cf::CH, T = Cf::T, NS = Cf::S;
-  const int tid = threadIdx.x;
-  const IO* yTile = reinterpret_cast<const IO*>(sm + S::oY);
-  for (int64_t i = 0; i < nchunks; ++i) {
-    const int s = (int)(i % NS);
-    const int64_t t0 = t_begin + i * T;
-    const int tcount = (int)min64(T, t_end - t0);
-    unsigned char* stage = sm + (size_t)s * S::kStage;
-    bool ok = true;
-    if (use_tma) {
-      ok = mbar_wait_bounded(&bars[s], (uint32_t)((i / NS) & 1));
-      prep_chunk<IO, N, PASS, true, PRECISE>(p, stage, sm, b, d0, t0, tcount);
-    } else {
-      prep_chunk<IO, N, PASS, false, PRECISE>(p, stage, sm, b, d0, t0, tcount);
-    }
-    if (__syncthreads_or(!ok)) return i;
-    // the raw stage is consumed: refill it with chunk i + NS
-    if (use_tma && tid == 0 && i + NS < nchunks)
-      issue_chunk<IO, N, PASS>(p, maps, stage, &bars[s], b, d0, t0 + (int64_t)NS * T);
+// Per-lane state of the recurrence.
+template <int N> struct LaneState {
+  static constexpr int NPT = ScanCfg<N>::NPT, NP = NPT / 2 > 0 ? NPT / 2 : 1;
+  float h[NPT], Aj[NPT], invA[NPT], A2[NPT];
+  f2 hp[NP], nIp[NP];
+  float A2s, nIs, sumDt;
+};
 
-    if constexpr (PRECISE) {
-      chunk_precise<IO, N, PASS>(sm, c, g, Dd, h, Aj, invA, sumDt);
-    } else if constexpr (NPT == 1) {
-      chunk_fast_scalar<IO, PASS>(sm, c, Dd, h[0], A2s, nIs, sumDt);
-    } else {
-      chunk_fast<IO, N, PASS>(sm, c, g, Dd, hp, A2p, nIp, sumDt);
-    }
-    __syncthreads();
-    if (PASS == 0) {
-      // write the y tile back
-      IO* gy = static_cast<IO*>(p.y);
-      const int nrows = (int)min64(CH, p.dim - d0);
-      constexpr int VEC = 16 / sizeof(IO);
-      if (p.vec_io) {
-        const int pieces = tcount / VEC;  // tcount is a multiple of VEC here
-        for (int e = tid; e < nrows * pieces; e += kScanThreads) {
-          const int r = e / pieces, k = e - r * pieces;
-          const uint4 v = *reinterpret_cast<const uint4*>(yTile + r * S::RowY + k * VEC);
-          *reinterpret_cast<uint4*>(gy + (b * p.dim + d0 + r) * p.L + t0 + k * VEC) = v;
-        }
-      } else {
-        for (int e = tid; e < nrows * tcount; e += kScanThreads) {
-          const int r = e / tcount, k = e - r * tcount;
-          gy[(b * p.dim + d0 + r) * p.L + t0 + k] = yTile[r * S::RowY + k];
-        }
-      }
-    }
+// One pipelined chunk iteration: the recurrence of chunk i, the conversion of
+// chunk i+1 (stage `rawN` -> buffer `bufN`) and the finalisation of chunk i-1
+// (buffer `bufF`, partials `partF`; stored only when `fin`).
+template <typename IO, int N, int PASS, bool FAST>
+__device__ __forceinline__ void chunk_iteration(
+    const ScanArgs& p, LaneState<N>& ls, bool precise, int tid, int prow, int c, int g,
+    const float* sBias,
+    const float* sD, int nrows,
+    const unsigned char* bufM, float* partM,                          // chunk i
+    const unsigned char* rawN, unsigned char* bufN, int tcountN,      // chunk i+1
+    const unsigned char* bufF, const float* partF, IO* yF, int tcountF,  // chunk i-1
+    bool fin, StepFlags fl) {
+  constexpr int NPT = ScanCfg<N>::NPT;
+  prep_share<IO, N, PASS, FAST>(rawN, bufN, sBias, tid, tcountN, nrows, fl);
+  if (PASS == 0)
+    finalize_share<IO, N>(p, bufF, partF, sD, tid, yF, tcountF, nrows, fin);
+  if (!FAST && precise) {
+    chunk_precise<IO, N, PASS>(bufM, partM, prow, c, g, ls.h, ls.Aj, ls.invA, ls.sumDt);
+  } else if constexpr (NPT == 1) {
+    chunk_fast_scalar<IO, PASS>(bufM, partM, prow, c, ls.h[0], ls.A2s, ls.nIs, ls.sumDt);
+  } else {
+    chunk_fast<IO, N, PASS>(bufM, partM, prow, c, g, ls.hp, ls.A2, ls.nIp, ls.sumDt);
   }
-  return -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -545,134 +589,197 @@ __device__ __forceinline__ int64_t run_chunks(
 // from a zero start and ΣΔ, for the split plan.
 // ---------------------------------------------------------------------------
 template <typename IO, int N, int PASS>
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs p,
+__global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
                                                             const __grid_constant__ ScanMaps maps) {
   using Cf = ScanCfg<N>;
   using S = ScanSmem<IO, N>;
-  constexpr int NPT = Cf::NPT, G = Cf::G, CH = Cf::CH, T = Cf::T, NS = Cf::S;
+  constexpr int NPT = Cf::NPT, G = Cf::G, CH = Cf::CH, T = Cf::T, NS = Cf::NS;
   constexpr int NP = NPT / 2;  // packed pairs per lane (0 when NPT == 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
   const int tid = threadIdx.x;
-  const int c = tid / G, g = tid - (tid / G) * G;
+  // this lane: channel c, state group g (see the warp layout of ScanCfg); its
+  // partial readouts go to row prow of the partial tile
+  const int wid = tid >> 5, lid = tid & 31;
+  const int g = (wid % Cf::WPC) * Cf::GW + lid / Cf::CW;
+  const int c = (wid / Cf::WPC) * Cf::CW + lid % Cf::CW;
+  const int prow = g * CH + c;
   const int64_t b = blockIdx.y;
   const int64_t d0 = (int64_t)blockIdx.x * CH;
   const int64_t d = d0 + c;
   const bool chan_ok = d < p.dim;
+  const int nrows = (int)min64(CH, p.dim - d0);
   const int seg = blockIdx.z;
   const int64_t t_begin = (int64_t)seg * p.seg_len;
   const int64_t t_end = min(p.L, t_begin + p.seg_len);
-  const int64_t nchunks = (t_end - t_begin + T - 1) / T;
+  // chunk bookkeeping in 32 bits: a segment has fewer than 2^31 steps
+  const int seg_steps = (int)(t_end - t_begin);
+  const int nchunks = (seg_steps + T - 1) / T;
   const bool use_tma = p.use_tma != 0;
+  auto stage_of = [&](int k) { return sm + (k % NS) * S::kStage; };
+  auto buf_of = [&](int k) { return sm + S::oBuf + (k % S::NBT) * S::kBuf; };
+  auto part_of = [&](int k) {
+    return reinterpret_cast<float*>(sm + S::oPart + (k % S::NBP) * S::kPart);
+  };
+  auto tcount_of = [&](int k) { return min(T, seg_steps - k * T); };
+  auto t0_of = [&](int k) { return t_begin + (int64_t)k * T; };
+  // this thread's first output of a chunk in HBM, for the finalisation
+  const int fr = tid / (T / Cf::E), fte = (tid - fr * (T / Cf::E)) * Cf::E;
+  IO* const y_base = PASS == 0 ? static_cast<IO*>(p.y) + ((b * p.dim + d0 + min(fr, nrows - 1)) * p.L +
+                                                          t_begin + fte)
+                               : nullptr;
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::oBar);
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(sm + S::oBar);
   float* sBias = reinterpret_cast<float*>(sm + S::oBias);
-  for (int r = tid; r < CH; r += kScanThreads)
-    sBias[r] = (p.bias && d0 + r < p.dim) ? p.bias[d0 + r] : 0.f;
+  float* sD = reinterpret_cast<float*>(sm + S::oD);
+  for (int r = tid; r < CH; r += kScanThreads) {
+    const bool ok = d0 + r < p.dim;
+    sBias[r] = (p.bias && ok) ? p.bias[d0 + r] : 0.f;
+    sD[r] = (p.D && ok) ? p.D[d0 + r] : 0.f;
+  }
   if (use_tma && tid == 0) {
     prefetch_tmap(&maps.u);
     prefetch_tmap(&maps.d);
     prefetch_tmap(&maps.b);
-    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&raw_full[s], 1);
     fence_mbar_init();
   }
 
   // this lane's states: n = g*NPT + j
-  float Aj[NPT];
+  LaneState<N> ls;
   bool zeroA = false;
 #pragma unroll
   for (int j = 0; j < NPT; ++j) {
-    Aj[j] = chan_ok ? p.A[d * N + g * NPT + j] : -1.f;
-    zeroA |= (Aj[j] == 0.f);
+    ls.Aj[j] = chan_ok ? p.A[d * N + g * NPT + j] : -1.f;
+    zeroA |= (ls.Aj[j] == 0.f);
   }
   const bool precise = __syncthreads_or(zeroA) || p.force_precise;
+  const StepFlags fl{precise, p.softplus != 0, p.z != nullptr};
+  const bool fast = !precise && fl.softplus && (PASS == 1 || fl.gate);
 
-  // prologue: the first NS chunks in flight
-  if (use_tma && tid == 0) {
-    for (int k = 0; k < NS && k < nchunks; ++k)
-      issue_chunk<IO, N, PASS>(p, maps, sm + (size_t)k * S::kStage, &bars[k], b, d0,
-                               t_begin + (int64_t)k * T);
+  // the first NS chunks in flight
+  int issued = 0;  // the same count in every thread
+  if (use_tma) {
+    for (; issued < NS && issued < nchunks; ++issued)
+      if (tid == 0)
+        issue_chunk<IO, N, PASS>(p, maps, stage_of(issued), &raw_full[issued % NS], b, d0,
+                                 t0_of(issued));
+  } else {
+    for (; issued < NS && issued < nchunks; ++issued)
+      load_chunk_plain<IO, N, PASS>(p, stage_of(issued), tid, b, d0, t0_of(issued));
+    __syncthreads();
   }
 
-  float h[NPT];
 #pragma unroll
-  for (int j = 0; j < NPT; ++j) h[j] = 0.f;
+  for (int j = 0; j < NPT; ++j) ls.h[j] = 0.f;
   if (PASS == 0 && chan_ok) {
     const int64_t row = b * p.dim + d;
     if (p.init_state) {
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) h[j] = p.init_state[row * N + g * NPT + j];
+      for (int j = 0; j < NPT; ++j) ls.h[j] = p.init_state[row * N + g * NPT + j];
     }
     for (int k = 0; k < seg; ++k) {
       const float sk = p.carry_s[(int64_t)k * p.batch * p.dim + row];
       const float* hk = p.carry_h + ((int64_t)k * p.batch * p.dim + row) * N + g * NPT;
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) h[j] = fmaf(expf(sk * Aj[j]), h[j], hk[j]);
+      for (int j = 0; j < NPT; ++j) ls.h[j] = fmaf(expf(sk * ls.Aj[j]), ls.h[j], hk[j]);
     }
   }
-  const float Dd = (PASS == 0 && chan_ok && p.D) ? p.D[d] : 0.f;
-
   // fast-path constants: A·log2(e) and -1/A per state, as packed pairs
-  f2 A2p[NP > 0 ? NP : 1], nIp[NP > 0 ? NP : 1], hp[NP > 0 ? NP : 1];
-  float A2s = 0.f, nIs = 0.f;
+  ls.A2s = 0.f;
+  ls.nIs = 0.f;
+  ls.sumDt = 0.f;
   if constexpr (NPT == 1) {
-    A2s = Aj[0] * kLog2e;
-    nIs = Aj[0] != 0.f ? -1.f / Aj[0] : 0.f;
+    ls.A2s = ls.Aj[0] * kLog2e;
+    ls.nIs = ls.Aj[0] != 0.f ? -1.f / ls.Aj[0] : 0.f;
   } else {
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-      A2p[q] = pack2(Aj[2 * q] * kLog2e, Aj[2 * q + 1] * kLog2e);
-      nIp[q] = pack2(Aj[2 * q] != 0.f ? -1.f / Aj[2 * q] : 0.f,
-                     Aj[2 * q + 1] != 0.f ? -1.f / Aj[2 * q + 1] : 0.f);
-      hp[q] = pack2(h[2 * q], h[2 * q + 1]);
+      ls.nIp[q] = pack2(ls.Aj[2 * q] != 0.f ? -1.f / ls.Aj[2 * q] : 0.f,
+                        ls.Aj[2 * q + 1] != 0.f ? -1.f / ls.Aj[2 * q + 1] : 0.f);
+      ls.hp[q] = pack2(ls.h[2 * q], ls.h[2 * q + 1]);
     }
   }
-  float invA[NPT];
 #pragma unroll
-  for (int j = 0; j < NPT; ++j) invA[j] = Aj[j] != 0.f ? 1.f / Aj[j] : 0.f;
-
-  float sumDt = 0.f;
-  int64_t i = -1;  // chunk whose wait timed out, or -1
-  if (precise) {
-    i = run_chunks<IO, N, PASS, true>(p, maps, sm, bars, b, d0, t_begin, t_end, nchunks, use_tma,
-                                      c, g, Dd, h, hp, A2p, nIp, A2s, nIs, Aj, invA, sumDt);
-  } else {
-    i = run_chunks<IO, N, PASS, false>(p, maps, sm, bars, b, d0, t_begin, t_end, nchunks,
-                                       use_tma, c, g, Dd, h, hp, A2p, nIp, A2s, nIs, Aj, invA,
-                                       sumDt);
-    if constexpr (NPT > 1) {
-#pragma unroll
-      for (int q = 0; q < NP; ++q) unpack2(hp[q], h[2 * q], h[2 * q + 1]);
-    }
+  for (int j = 0; j < NPT; ++j) {
+    ls.invA[j] = ls.Aj[j] != 0.f ? 1.f / ls.Aj[j] : 0.f;
+    ls.A2[j] = ls.Aj[j] * kLog2e;
   }
-  const bool failed = i >= 0;
 
+  // chunk 0 is converted on its own; afterwards each iteration overlaps three chunks
+  bool ok = !use_tma || mbar_wait_bounded(&raw_full[0], 0);
+  if (ok) {
+    if (fast) prep_share<IO, N, PASS, true>(stage_of(0), buf_of(0), sBias, tid, tcount_of(0), nrows, fl);
+    else prep_share<IO, N, PASS, false>(stage_of(0), buf_of(0), sBias, tid, tcount_of(0), nrows, fl);
+  }
+  bool failed = __syncthreads_or(!ok);
+  int i = 0;
+  for (; i < nchunks && !failed; ++i) {
+    // stage (i % NS) is free again (chunk i was converted before the last barrier)
+    if (issued < nchunks) {
+      if (use_tma) {
+        if (tid == 0)
+          issue_chunk<IO, N, PASS>(p, maps, stage_of(issued), &raw_full[issued % NS], b, d0,
+                                   t0_of(issued));
+      } else {
+        load_chunk_plain<IO, N, PASS>(p, stage_of(issued), tid, b, d0, t0_of(issued));
+      }
+      ++issued;  // uniform: every thread counts the chunks issued
+    }
+    const bool has_next = i + 1 < nchunks;
+    ok = true;
+    if (use_tma && has_next) ok = mbar_wait_bounded(&raw_full[(i + 1) % NS], (uint32_t)(((i + 1) / NS) & 1));
+    if (!use_tma) __syncthreads();  // the plain copy of chunk i + NS is complete
+    // without a next chunk the conversion reads a stale stage into a spare buffer
+    const int tcN = has_next ? tcount_of(i + 1) : 0;
+    const int f = i > 0 ? i - 1 : 0;
+    IO* const yF = PASS == 0 ? y_base + (int64_t)f * T : nullptr;
+    if (fast)
+      chunk_iteration<IO, N, PASS, true>(p, ls, precise, tid, prow, c, g, sBias, sD, nrows, buf_of(i),
+                                         part_of(i), stage_of(i + 1), buf_of(i + 1), tcN,
+                                         buf_of(f), part_of(f), yF, tcount_of(f), i > 0, fl);
+    else
+      chunk_iteration<IO, N, PASS, false>(p, ls, precise, tid, prow, c, g, sBias, sD, nrows, buf_of(i),
+                                          part_of(i), stage_of(i + 1), buf_of(i + 1), tcN,
+                                          buf_of(f), part_of(f), yF, tcount_of(f), i > 0, fl);
+    failed = __syncthreads_or(!ok);
+  }
   if (failed) {
-    // a TMA chunk did not land in time: record it, let the copies still in
-    // flight into this block's shared memory finish (bounded), and leave
-    // without writing a state
+    // a TMA chunk did not land in time: record it, let this block's copies
+    // still in flight land (bounded) and leave without writing a state
     if (tid == 0) {
       atomicExch(&g_scan_error, 1);
-      for (int64_t j = i; j < nchunks && j < i + NS; ++j)
-        (void)mbar_wait_bounded(&bars[j % NS], (uint32_t)((j / NS) & 1));
+      for (int k = i; k < issued; ++k)
+        (void)mbar_wait_bounded(&raw_full[k % NS], (uint32_t)((k / NS) & 1));
     }
     return;
   }
+  if (PASS == 0 && nchunks > 0) {
+    const int f = nchunks - 1;
+    finalize_share<IO, N>(p, buf_of(f), part_of(f), sD, tid, y_base + (int64_t)f * T, tcount_of(f),
+                          nrows, true);
+  }
 
+  if constexpr (NPT > 1) {
+    if (!precise) {
+#pragma unroll
+      for (int q = 0; q < NP; ++q) unpack2(ls.hp[q], ls.h[2 * q], ls.h[2 * q + 1]);
+    }
+  }
   if (!chan_ok) return;
   const int64_t row = b * p.dim + d;
   if (PASS == 0) {
     if (p.final_state && seg == p.nseg - 1) {
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) p.final_state[row * N + g * NPT + j] = h[j];
+      for (int j = 0; j < NPT; ++j) p.final_state[row * N + g * NPT + j] = ls.h[j];
     }
   } else {
     float* hk = p.carry_h + ((int64_t)seg * p.batch * p.dim + row) * N + g * NPT;
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) hk[j] = h[j];
-    if (g == 0) p.carry_s[(int64_t)seg * p.batch * p.dim + row] = sumDt;
+    for (int j = 0; j < NPT; ++j) hk[j] = ls.h[j];
+    if (g == 0) p.carry_s[(int64_t)seg * p.batch * p.dim + row] = ls.sumDt;
   }
 }
 
@@ -706,7 +813,7 @@ static bool cfg_for(int64_t N, int& chans, int& chunk) {
 ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtype, int sm_count,
                    bool allow_split) {
   (void)io_dtype;
-  ScanPlan pl{1, L, 0, 32, 32};
+  ScanPlan pl{1, L, 0, 16, 32};
   if (!cfg_for(N, pl.chans, pl.chunk)) return pl;
   pl.seg_len = L > 0 ? L : 1;
   if (!allow_split || L <= 0 || batch <= 0 || dim <= 0) return pl;
@@ -714,7 +821,7 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
   const int64_t want = (int64_t)sm_count * 2;  // blocks that keep every SM busy
   if (blocks >= want) return pl;
   int64_t nseg = (want + blocks - 1) / blocks;
-  const int64_t max_by_len = L / (16 * (int64_t)pl.chunk);  // at least 16 chunks per segment
+  const int64_t max_by_len = L / (32 * (int64_t)pl.chunk);  // at least 32 chunks per segment
   if (nseg > max_by_len) nseg = max_by_len;
   if (nseg > 64) nseg = 64;
   if (nseg < 2) return pl;
@@ -786,6 +893,10 @@ static cudaError_t launch_one(const ScanArgs& a, const ScanMaps& m, int nz, cuda
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    // as much shared memory per SM as possible: several blocks per SM
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
