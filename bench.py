@@ -285,8 +285,8 @@ def bench_scan(w, steps, warmup, world):
 # ---------------------------------------------------------------------------
 
 def bench_decode(dw, steps, world):
-    """Per-step time of ssm_state_update_ex with an L2 flush between steps (the 84 MB
-    state would otherwise stay in the 126 MB L2 across steps).  Inputs are drawn on the
+    """Per-step time of ssm_state_update_ex with an L2 flush (a 256 MB read) between steps
+    (the 84 MB state would otherwise stay in the 126 MB L2 across steps).  Inputs are drawn on the
     device (seeded torch generator, the workload's distributions); the state starts from
     a GPU scan over a 256-step prefill."""
     import torch
@@ -312,7 +312,8 @@ def bench_decode(dw, steps, world):
     Bs = torch.randn((steps, B_, N), generator=gen, device="cuda")
     Cs = torch.randn((steps, B_, N), generator=gen, device="cuda")
     y = torch.empty((steps, B_, D_), dtype=bf, device="cuda")
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush_sink = torch.zeros((), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step(i):
@@ -327,7 +328,9 @@ def bench_decode(dw, steps, world):
     barrier(world)
     torch.cuda.synchronize()
     for i in range(steps):
-        flush.fill_(float(i))
+        # read (not write) a buffer twice the L2 size: evicts the state without
+        # leaving dirty lines whose write-back would land in the timed step
+        flush_sink.add_(flush.sum())
         ev[i][0].record(stream)
         step(i)
         ev[i][1].record(stream)
@@ -480,7 +483,7 @@ def main():
                           "us_per_step": dec["step_ms"] * 1e3,
                           "tokens_per_s": synth.DECODE.batch / st * world,
                           "hbm_gbs": db / st / 1e9, "hbm_frac": db / st / 1e9 / hbm_peak,
-                          "bytes_per_step": db, "l2": "flushed (256 MB write) before every step",
+                          "bytes_per_step": db, "l2": "flushed (256 MB read) before every step",
                           "us_per_step_back_to_back": dec["b2b_ms"] * 1e3,
                           "gpu_launches": 2 * dec["steps"]}
     if cpu is not None:

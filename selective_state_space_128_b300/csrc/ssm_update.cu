@@ -7,114 +7,141 @@
 // with Ā, B̄ from the zero-order hold of equation (4).
 //
 // The step reads and writes the float32 state once (64 bytes per channel at
-// N = 16) and is bound by HBM bandwidth.  G = 4 lanes share a channel; each
-// holds N/4 contiguous states, loaded and stored as 16-byte vectors so that a
-// warp touches 8 whole channels (512 contiguous bytes per access).  The G
-// partial readouts are summed with two xor-shuffles.
+// N = 16) and is bound by HBM bandwidth, so the kernel is built to keep many
+// bytes in flight with few instructions:
+//  * G = 4 lanes share a channel, each holding N/4 contiguous states that it
+//    loads and stores as 16-byte vectors, so a warp touches 8 whole channels
+//    (512 contiguous bytes per access);
+//  * each thread handles K channels spaced one warp-width of channels apart
+//    and issues all of their loads before any arithmetic, so 64 bytes of
+//    state per thread are in flight at once;
+//  * the grid is (channel blocks, batch): no integer division per thread, and
+//    the block's B/C row is shared by all of its channels.
+// The G partial readouts of a channel are summed with two xor-shuffles.
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
 namespace ssm {
 
 constexpr int kUpdThreads = 256;
+constexpr int kUpdK = 4;  // channels per thread
 
 template <typename IO, int N>
 __global__ void __launch_bounds__(kUpdThreads) update_kernel(const UpdateArgs p) {
   constexpr int G = N >= 4 ? 4 : N;
   constexpr int NPT = N / G;
-  const int64_t gid = (int64_t)blockIdx.x * kUpdThreads + threadIdx.x;
-  const int64_t row = gid / G;  // b * dim + d
-  const int g = (int)(gid - row * G);
-  const int64_t nrows = p.batch * p.dim;
-  const bool ok = row < nrows;
-  const int64_t rr = ok ? row : 0;
-  const int64_t b = rr / p.dim, d = rr - (rr / p.dim) * p.dim;
+  constexpr int CPB = kUpdThreads / G;  // channels per block per k
+  const int tid = threadIdx.x;
+  const int g = tid % G;
+  const int64_t b = blockIdx.y;
+  const int64_t dbase = (int64_t)blockIdx.x * (CPB * kUpdK) + tid / G;
 
-  float st[NPT], A[NPT], Bv[NPT], Cv[NPT];
-  float* sp = p.state + rr * N + g * NPT;
-  const float* Ap = p.A + d * N + g * NPT;
-  const float* Bp = p.B + b * N + g * NPT;
-  const float* Cp = p.C + b * N + g * NPT;
-  if (ok) {
+  // B, C of this batch row for this lane's states (shared by all channels)
+  float Bv[NPT], Cv[NPT];
+  {
+    const float* Bp = p.B + b * N + g * NPT;
+    const float* Cp = p.C + b * N + g * NPT;
     if constexpr (NPT % 4 == 0) {
 #pragma unroll
       for (int j = 0; j < NPT; j += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(sp + j);
-        const float4 a4 = __ldg(reinterpret_cast<const float4*>(Ap + j));
         const float4 b4 = __ldg(reinterpret_cast<const float4*>(Bp + j));
         const float4 c4 = __ldg(reinterpret_cast<const float4*>(Cp + j));
-        st[j] = s4.x; st[j + 1] = s4.y; st[j + 2] = s4.z; st[j + 3] = s4.w;
-        A[j] = a4.x; A[j + 1] = a4.y; A[j + 2] = a4.z; A[j + 3] = a4.w;
         Bv[j] = b4.x; Bv[j + 1] = b4.y; Bv[j + 2] = b4.z; Bv[j + 3] = b4.w;
         Cv[j] = c4.x; Cv[j + 1] = c4.y; Cv[j + 2] = c4.z; Cv[j + 3] = c4.w;
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        st[j] = sp[j]; A[j] = Ap[j]; Bv[j] = Bp[j]; Cv[j] = Cp[j];
-      }
+      for (int j = 0; j < NPT; ++j) { Bv[j] = __ldg(Bp + j); Cv[j] = __ldg(Cp + j); }
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < NPT; ++j) { st[j] = 0.f; A[j] = -1.f; Bv[j] = 0.f; Cv[j] = 0.f; }
   }
 
+  // issue every load of the K channels first
+  float st[kUpdK][NPT], Av[kUpdK][NPT], uu[kUpdK], xx[kUpdK], zz[kUpdK], Dd[kUpdK];
+  bool ok[kUpdK];
   const IO* gu = static_cast<const IO*>(p.u);
   const IO* gd = static_cast<const IO*>(p.delta);
   const IO* gz = static_cast<const IO*>(p.z);
-  const float uu = ok ? io_traits<IO>::to_f32(gu[rr]) : 0.f;
-  const float x = (ok ? io_traits<IO>::to_f32(gd[rr]) : 0.f) + ((ok && p.bias) ? p.bias[d] : 0.f);
-  bool precise = p.force_precise != 0;
 #pragma unroll
-  for (int j = 0; j < NPT; ++j) precise |= (A[j] == 0.f);
-  const float dt = p.softplus ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
-
-  float acc = 0.f;
-  if (!precise) {
+  for (int k = 0; k < kUpdK; ++k) {
+    const int64_t d = dbase + (int64_t)k * CPB;
+    ok[k] = d < p.dim;
+    const int64_t dd = ok[k] ? d : 0;
+    const int64_t row = b * p.dim + dd;
+    const float* sp = p.state + row * N + g * NPT;
+    const float* Ap = p.A + dd * N + g * NPT;
+    if constexpr (NPT % 4 == 0) {
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) {
-      const float a = ex2_fast(dt * (A[j] * kLog2e));
-      const float nv = Bv[j] * uu * (-1.f / A[j]);
-      st[j] = fmaf(a, st[j] - nv, nv);
-      acc = fmaf(Cv[j], st[j], acc);
+      for (int j = 0; j < NPT; j += 4) {
+        const float4 s4 = *reinterpret_cast<const float4*>(sp + j);
+        const float4 a4 = __ldg(reinterpret_cast<const float4*>(Ap + j));
+        st[k][j] = s4.x; st[k][j + 1] = s4.y; st[k][j + 2] = s4.z; st[k][j + 3] = s4.w;
+        Av[k][j] = a4.x; Av[k][j + 1] = a4.y; Av[k][j + 2] = a4.z; Av[k][j + 3] = a4.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) { st[k][j] = sp[j]; Av[k][j] = __ldg(Ap + j); }
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < NPT; ++j) {
-      const float xa = dt * A[j];
-      const float coef = A[j] != 0.f ? expm1f(xa) / A[j] : dt;
-      st[j] = fmaf(expf(xa), st[j], coef * (Bv[j] * uu));
-      acc = fmaf(Cv[j], st[j], acc);
-    }
+    uu[k] = io_traits<IO>::to_f32(gu[row]);
+    xx[k] = io_traits<IO>::to_f32(gd[row]) + (p.bias ? __ldg(p.bias + dd) : 0.f);
+    zz[k] = gz ? io_traits<IO>::to_f32(gz[row]) : 0.f;
+    Dd[k] = p.D ? __ldg(p.D + dd) : 0.f;
   }
-#pragma unroll
-  for (int s = G / 2; s >= 1; s /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, s);
 
-  if (!ok) return;
-  if constexpr (NPT % 4 == 0) {
 #pragma unroll
-    for (int j = 0; j < NPT; j += 4)
-      *reinterpret_cast<float4*>(sp + j) = make_float4(st[j], st[j + 1], st[j + 2], st[j + 3]);
-  } else {
+  for (int k = 0; k < kUpdK; ++k) {
+    bool precise = p.force_precise != 0;
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) sp[j] = st[j];
-  }
-  if (g == 0) {
-    float yv = acc + (p.D ? p.D[d] * uu : 0.f);
-    if (gz) {
-      const float zz = io_traits<IO>::to_f32(gz[rr]);
-      yv *= precise ? silu_precise(zz) : silu_fast(zz);
+    for (int j = 0; j < NPT; ++j) precise |= (Av[k][j] == 0.f);
+    const float x = xx[k];
+    const float dt = p.softplus ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
+    float acc = 0.f;
+    if (!precise) {
+      // h = Ā (h - v) + v with Ā = 2^(Δ A log2 e), v = -B u / A
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) {
+        const float a = ex2_fast(dt * (Av[k][j] * kLog2e));
+        const float nv = Bv[j] * uu[k] * -rcp_fast(Av[k][j]);
+        st[k][j] = fmaf(a, st[k][j] - nv, nv);
+        acc = fmaf(Cv[j], st[k][j], acc);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) {
+        const float xa = dt * Av[k][j];
+        const float coef = Av[k][j] != 0.f ? expm1f(xa) / Av[k][j] : dt;
+        st[k][j] = fmaf(expf(xa), st[k][j], coef * (Bv[j] * uu[k]));
+        acc = fmaf(Cv[j], st[k][j], acc);
+      }
     }
-    static_cast<IO*>(p.y)[rr] = io_traits<IO>::from_f32(yv);
+#pragma unroll
+    for (int s = G / 2; s >= 1; s /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+
+    if (!ok[k]) continue;
+    const int64_t row = b * p.dim + dbase + (int64_t)k * CPB;
+    float* sp = p.state + row * N + g * NPT;
+    if constexpr (NPT % 4 == 0) {
+#pragma unroll
+      for (int j = 0; j < NPT; j += 4)
+        *reinterpret_cast<float4*>(sp + j) =
+            make_float4(st[k][j], st[k][j + 1], st[k][j + 2], st[k][j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) sp[j] = st[k][j];
+    }
+    if (g == 0) {
+      float yv = fmaf(Dd[k], uu[k], acc);
+      if (gz) yv *= precise ? silu_precise(zz[k]) : silu_fast(zz[k]);
+      static_cast<IO*>(p.y)[row] = io_traits<IO>::from_f32(yv);
+    }
   }
 }
 
 template <typename IO, int N>
 static cudaError_t upd_typed(const UpdateArgs& a, cudaStream_t stream) {
   constexpr int G = N >= 4 ? 4 : N;
-  const int64_t threads = a.batch * a.dim * G;
-  const int64_t blocks = (threads + kUpdThreads - 1) / kUpdThreads;
-  update_kernel<IO, N><<<(unsigned)blocks, kUpdThreads, 0, stream>>>(a);
+  constexpr int per_block = kUpdThreads / G * kUpdK;
+  const dim3 grid((unsigned)((a.dim + per_block - 1) / per_block), (unsigned)a.batch);
+  update_kernel<IO, N><<<grid, kUpdThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
