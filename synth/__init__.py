@@ -218,6 +218,11 @@ def make_decode_step_inputs(dw: DecodeWorkload, step0: int, nsteps: int, b0=0, n
     streams = {"u": (S_DEC_U, 1.0), "delta": (S_DEC_DELTA, dw.sigma_delta), "z": (S_DEC_Z, 1.0)}
     for k, (s, std) in streams.items():
         for i in range(nsteps):
+            if d0 == 0 and nd == dw.dim:   # whole rows: one contiguous block per step
+                off = ((step0 + i) * dw.batch + b0) * dw.dim
+                fill(dw.seed, s, off, nb * nd, NORMAL, 0.0, std, dtype=io,
+                     out=out[k][i].reshape(-1))
+                continue
             for j in range(nb):
                 off = ((step0 + i) * dw.batch + b0 + j) * dw.dim + d0
                 fill(dw.seed, s, off, nd, NORMAL, 0.0, std, dtype=io, out=out[k][i, j])
