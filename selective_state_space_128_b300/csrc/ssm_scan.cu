@@ -349,8 +349,10 @@ __device__ __forceinline__ void prep_share(const unsigned char* stage, unsigned 
 
 // This thread's share of finalising a chunk: E consecutive outputs of channel
 // row r: y = (Σ_g partials + D u) · gate, rounded, stored at `dst` (this
-// thread's first output of the chunk in HBM) when `store`.
-template <typename IO, int N>
+// thread's first output of the chunk in HBM) when `store`.  WHOLE: the chunk
+// has all T steps and rows are 16-byte aligned, so the store is one vector
+// store under a predicate (no branch that would split the caller's block).
+template <typename IO, int N, bool WHOLE>
 __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned char* buf,
                                                const float* part, const float* sD, int tid,
                                                IO* dst, int tcount, int nrows, bool store) {
@@ -358,17 +360,25 @@ __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned
   using Cf = ScanCfg<N>;
   constexpr int T = S::T, G = Cf::G, E = Cf::E;
   const int r = tid / (T / E), te = (tid - r * (T / E)) * E;
-  float acc[E];
-#pragma unroll
-  for (int j = 0; j < E; ++j) acc[j] = 0.f;
+  // the G partials of each step, summed pairwise
+  float pg[G][E];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
 #pragma unroll
     for (int k = 0; k < E / 4; ++k) {
       const float4 q = *reinterpret_cast<const float4*>(part + p_index(g * S::CH + r, te / 4 + k));
-      acc[4 * k] += q.x; acc[4 * k + 1] += q.y; acc[4 * k + 2] += q.z; acc[4 * k + 3] += q.w;
+      pg[g][4 * k] = q.x; pg[g][4 * k + 1] = q.y; pg[g][4 * k + 2] = q.z; pg[g][4 * k + 3] = q.w;
     }
   }
+#pragma unroll
+  for (int w = 1; w < G; w *= 2) {
+#pragma unroll
+    for (int g = 0; g + w < G; g += 2 * w) {
+#pragma unroll
+      for (int j = 0; j < E; ++j) pg[g][j] += pg[g + w][j];
+    }
+  }
+  const float (&acc)[E] = pg[0];
   const float Dd = sD[r];
   const float* Ut = reinterpret_cast<const float*>(buf + S::bU) + r * S::RowF + te;
   const float4* g4 = reinterpret_cast<const float4*>(
@@ -380,6 +390,10 @@ __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned
     const float gg[4] = {gk.x, gk.y, gk.z, gk.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) y[4 * k + j] = fmaf(Dd, Ut[4 * k + j], acc[4 * k + j]) * gg[j];
+  }
+  if constexpr (WHOLE) {
+    if (store && r < nrows) vecio<IO, E>::store(dst, y);
+    return;
   }
   if (!store || r >= nrows) return;
   if (p.vec_io && te + E <= tcount) {
@@ -402,11 +416,12 @@ __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned
 // its channel (one 4-byte load each: a warp covers 16 channels in one
 // wavefront) and its NPT values of B and C (16-byte loads that touch at most
 // two distinct addresses per warp).
-template <typename IO, int N, int PASS>
+template <typename IO, int N, int PASS, typename Side>
 __device__ __forceinline__ void chunk_fast(const unsigned char* buf, float* part, int prow, int c,
                                            int g, f2 (&hp)[ScanCfg<N>::NPT / 2],
                                            const float (&A2)[ScanCfg<N>::NPT],
-                                           const f2 (&nIp)[ScanCfg<N>::NPT / 2], float& sumDt) {
+                                           const f2 (&nIp)[ScanCfg<N>::NPT / 2], float& sumDt,
+                                           Side&& side) {
   using Cf = ScanCfg<N>;
   using S = ScanSmem<IO, N>;
   constexpr int NPT = Cf::NPT, T = Cf::T, NP = NPT / 2;
@@ -452,6 +467,7 @@ __device__ __forceinline__ void chunk_fast(const unsigned char* buf, float* part
     float dt_n, u_n;
     f2 b_n[NP], c_n[NP], a_n[NP], v_n[NP];
     if (t + 2 < T) load_step(t + 2, dt_n, u_n, b_n, c_n);
+    side(t);  // independent per-step work of other chunks, placed inside this block
     if (t + 1 < T) discretise(dt_l, u_l, b_l, a_n, v_n);
 #pragma unroll
     for (int q = 0; q < NP; ++q) hp[q] = fma2(a_c[q], sub2(hp[q], v_c[q]), v_c[q]);
@@ -562,7 +578,7 @@ template <int N> struct LaneState {
 // One pipelined chunk iteration: the recurrence of chunk i, the conversion of
 // chunk i+1 (stage `rawN` -> buffer `bufN`) and the finalisation of chunk i-1
 // (buffer `bufF`, partials `partF`; stored only when `fin`).
-template <typename IO, int N, int PASS, bool FAST>
+template <typename IO, int N, int PASS, bool FAST, bool WHOLE>
 __device__ __forceinline__ void chunk_iteration(
     const ScanArgs& p, LaneState<N>& ls, bool precise, int tid, int prow, int c, int g,
     const float* sBias,
@@ -572,15 +588,26 @@ __device__ __forceinline__ void chunk_iteration(
     const unsigned char* bufF, const float* partF, IO* yF, int tcountF,  // chunk i-1
     bool fin, StepFlags fl) {
   constexpr int NPT = ScanCfg<N>::NPT;
-  prep_share<IO, N, PASS, FAST>(rawN, bufN, sBias, tid, tcountN, nrows, fl);
-  if (PASS == 0)
-    finalize_share<IO, N>(p, bufF, partF, sD, tid, yF, tcountF, nrows, fin);
+  auto other_chunks = [&]() {
+    prep_share<IO, N, PASS, FAST>(rawN, bufN, sBias, tid, tcountN, nrows, fl);
+    if (PASS == 0)
+      finalize_share<IO, N, WHOLE>(p, bufF, partF, sD, tid, yF, tcountF, nrows, fin);
+  };
+  if constexpr (FAST && WHOLE && NPT > 1) {
+    // the conversion and finalisation go inside the unrolled step loop so that
+    // their instructions fill the recurrence's dependency gaps
+    chunk_fast<IO, N, PASS>(bufM, partM, prow, c, g, ls.hp, ls.A2, ls.nIp, ls.sumDt,
+                            [&](int t) { if (t == 3) other_chunks(); });
+    return;
+  }
+  other_chunks();
   if (!FAST && precise) {
     chunk_precise<IO, N, PASS>(bufM, partM, prow, c, g, ls.h, ls.Aj, ls.invA, ls.sumDt);
   } else if constexpr (NPT == 1) {
     chunk_fast_scalar<IO, PASS>(bufM, partM, prow, c, ls.h[0], ls.A2s, ls.nIs, ls.sumDt);
   } else {
-    chunk_fast<IO, N, PASS>(bufM, partM, prow, c, g, ls.hp, ls.A2, ls.nIp, ls.sumDt);
+    chunk_fast<IO, N, PASS>(bufM, partM, prow, c, g, ls.hp, ls.A2, ls.nIp, ls.sumDt,
+                            [](int) {});
   }
 }
 
@@ -596,8 +623,9 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
   constexpr int NPT = Cf::NPT, G = Cf::G, CH = Cf::CH, T = Cf::T, NS = Cf::NS;
   constexpr int NP = NPT / 2;  // packed pairs per lane (0 when NPT == 1)
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  // 128-byte aligned base, derived by pointer arithmetic (not an integer round
+  // trip) so that the compiler keeps every access in the shared address space
+  unsigned char* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
 
   const int tid = threadIdx.x;
   // this lane: channel c, state group g (see the warp layout of ScanCfg); its
@@ -736,14 +764,20 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     const int tcN = has_next ? tcount_of(i + 1) : 0;
     const int f = i > 0 ? i - 1 : 0;
     IO* const yF = PASS == 0 ? y_base + (int64_t)f * T : nullptr;
-    if (fast)
-      chunk_iteration<IO, N, PASS, true>(p, ls, precise, tid, prow, c, g, sBias, sD, nrows, buf_of(i),
-                                         part_of(i), stage_of(i + 1), buf_of(i + 1), tcN,
-                                         buf_of(f), part_of(f), yF, tcount_of(f), i > 0, fl);
-    else
-      chunk_iteration<IO, N, PASS, false>(p, ls, precise, tid, prow, c, g, sBias, sD, nrows, buf_of(i),
-                                          part_of(i), stage_of(i + 1), buf_of(i + 1), tcN,
-                                          buf_of(f), part_of(f), yF, tcount_of(f), i > 0, fl);
+    // steady state: both neighbouring chunks whole and rows 16-byte aligned
+    const bool whole = p.vec_io && tcN == T && tcount_of(f) == T;
+#define SSM_ITER(FASTV, WHOLEV)                                                                \
+  chunk_iteration<IO, N, PASS, FASTV, WHOLEV>(p, ls, precise, tid, prow, c, g, sBias, sD, nrows, \
+                                             buf_of(i), part_of(i), stage_of(i + 1),          \
+                                             buf_of(i + 1), tcN, buf_of(f), part_of(f), yF,   \
+                                             tcount_of(f), i > 0, fl)
+    if (fast) {
+      if (whole) SSM_ITER(true, true);
+      else SSM_ITER(true, false);
+    } else {
+      SSM_ITER(false, false);
+    }
+#undef SSM_ITER
     failed = __syncthreads_or(!ok);
   }
   if (failed) {
@@ -758,8 +792,8 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
   }
   if (PASS == 0 && nchunks > 0) {
     const int f = nchunks - 1;
-    finalize_share<IO, N>(p, buf_of(f), part_of(f), sD, tid, y_base + (int64_t)f * T, tcount_of(f),
-                          nrows, true);
+    finalize_share<IO, N, false>(p, buf_of(f), part_of(f), sD, tid, y_base + (int64_t)f * T,
+                                 tcount_of(f), nrows, true);
   }
 
   if constexpr (NPT > 1) {
