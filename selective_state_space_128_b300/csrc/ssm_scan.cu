@@ -292,9 +292,9 @@ struct StepFlags {
 
 // This thread's share of converting a raw stage into a working buffer: E
 // consecutive steps of channel row r.  Δ gets softplus once per channel step;
-// steps past tcount and rows past nrows get Δ = 0 and u = 0, exact no-ops of
-// the recurrence (Ā = 1, B̄ u = 0).  B/C are transposed to [t][n].
-template <typename IO, int N, int PASS, bool FAST>
+// with MASK, steps past tcount and rows past nrows get Δ = 0 and u = 0, exact
+// no-ops of the recurrence (Ā = 1, B̄ u = 0).  B/C are transposed to [t][n].
+template <typename IO, int N, int PASS, bool FAST, bool MASK = true>
 __device__ __forceinline__ void prep_share(const unsigned char* stage, unsigned char* buf,
                                            const float* sBias, int tid, int tcount, int nrows,
                                            StepFlags f) {
@@ -317,9 +317,12 @@ __device__ __forceinline__ void prep_share(const unsigned char* stage, unsigned 
   for (int j = 0; j < E; ++j) {
     const float x = dl[j] + bias;
     float dt = sp ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
-    const bool ok = r < nrows && te + j < tcount;
-    dt = ok ? dt : 0.f;
-    const float u = ok ? uu[j] : 0.f;
+    float u = uu[j];
+    if (MASK) {
+      const bool ok = r < nrows && te + j < tcount;
+      dt = ok ? dt : 0.f;
+      u = ok ? u : 0.f;
+    }
     DT[j] = dt;
     Ut[j] = u;
     gate[j] = hz ? (precise ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
@@ -589,7 +592,9 @@ __device__ __forceinline__ void chunk_iteration(
     bool fin, StepFlags fl) {
   constexpr int NPT = ScanCfg<N>::NPT;
   auto other_chunks = [&]() {
-    prep_share<IO, N, PASS, FAST>(rawN, bufN, sBias, tid, tcountN, nrows, fl);
+    // a whole chunk needs no step mask, and rows past the channel count need
+    // none either: TMA fills them with zeros, so u = 0 keeps their state at 0
+    prep_share<IO, N, PASS, FAST, !WHOLE>(rawN, bufN, sBias, tid, tcountN, nrows, fl);
     if (PASS == 0)
       finalize_share<IO, N, WHOLE>(p, bufF, partF, sD, tid, yF, tcountF, nrows, fin);
   };
