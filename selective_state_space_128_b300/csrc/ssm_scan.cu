@@ -105,7 +105,7 @@ template <typename IO, int N> struct ScanSmem {
   static constexpr size_t oBias = oPart + (size_t)NBP * kPart;
   static constexpr size_t oD = align_up(oBias + (size_t)CH * 4, 16);
   static constexpr size_t oBar = align_up(oD + (size_t)CH * 4, 8);
-  static constexpr size_t kBytes = oBar + 8 * NS;
+  static constexpr size_t kBytes = oBar + 8 * (NS + 1);  // raw_full[NS], hand-over
   static constexpr size_t kLaunchBytes = kBytes + 128;  // room to align the base to 128
 };
 
@@ -294,10 +294,19 @@ struct StepFlags {
 // consecutive steps of channel row r.  Δ gets softplus once per channel step;
 // with MASK, steps past tcount and rows past nrows get Δ = 0 and u = 0, exact
 // no-ops of the recurrence (Ā = 1, B̄ u = 0).  B/C are transposed to [t][n].
+// The conversion is split: prep_compute reads the raw stage (data no other
+// thread writes) into registers, prep_store writes the working buffer (which
+// other threads may still be reading until the block's hand-over).
+template <typename IO, int N, int PASS> struct PrepVals {
+  static constexpr int E = ScanCfg<N>::E;
+  static constexpr int PER = (N * ScanCfg<N>::T + kScanThreads - 1) / kScanThreads;
+  float dt[E], u[E], gate[E], bv[PER], cv[PER];
+};
+
 template <typename IO, int N, int PASS, bool FAST, bool MASK = true>
-__device__ __forceinline__ void prep_share(const unsigned char* stage, unsigned char* buf,
-                                           const float* sBias, int tid, int tcount, int nrows,
-                                           StepFlags f) {
+__device__ __forceinline__ void prep_compute(const unsigned char* stage, const float* sBias,
+                                             int tid, int tcount, int nrows, StepFlags f,
+                                             PrepVals<IO, N, PASS>& v) {
   using S = ScanSmem<IO, N>;
   using Cf = ScanCfg<N>;
   constexpr int T = S::T, E = Cf::E;
@@ -305,47 +314,61 @@ __device__ __forceinline__ void prep_share(const unsigned char* stage, unsigned 
   const bool sp = FAST ? true : f.softplus;
   const bool hz = PASS == 0 && (FAST ? true : f.gate);
   const int r = tid / (T / E), te = (tid - r * (T / E)) * E;
-  float dl[E], uu[E], zz[E];
+  float dl[E], zz[E];
   vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawD) + r * T + te, dl);
-  vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawU) + r * T + te, uu);
+  vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawU) + r * T + te, v.u);
   if (hz) vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawZ) + r * T + te, zz);
   const float bias = sBias[r];
-  float* DT = reinterpret_cast<float*>(buf + S::bDT) + r * S::RowF + te;
-  float* Ut = reinterpret_cast<float*>(buf + S::bU) + r * S::RowF + te;
-  float gate[E];
 #pragma unroll
   for (int j = 0; j < E; ++j) {
     const float x = dl[j] + bias;
-    float dt = sp ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
-    float u = uu[j];
+    v.dt[j] = sp ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
     if (MASK) {
       const bool ok = r < nrows && te + j < tcount;
-      dt = ok ? dt : 0.f;
-      u = ok ? u : 0.f;
+      v.dt[j] = ok ? v.dt[j] : 0.f;
+      v.u[j] = ok ? v.u[j] : 0.f;
     }
-    DT[j] = dt;
-    Ut[j] = u;
-    gate[j] = hz ? (precise ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
+    v.gate[j] = hz ? (precise ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
+  }
+  constexpr int NT = N * T;
+#pragma unroll
+  for (int k = 0; k < PrepVals<IO, N, PASS>::PER; ++k) {
+    const int e = tid + k * kScanThreads;
+    if (NT % kScanThreads == 0 || e < NT) {
+      v.bv[k] = reinterpret_cast<const float*>(stage + S::oRawB)[e];
+      if (PASS == 0) v.cv[k] = reinterpret_cast<const float*>(stage + S::oRawC)[e];
+    }
+  }
+}
+
+template <typename IO, int N, int PASS>
+__device__ __forceinline__ void prep_store(unsigned char* buf, int tid,
+                                           const PrepVals<IO, N, PASS>& v) {
+  using S = ScanSmem<IO, N>;
+  using Cf = ScanCfg<N>;
+  constexpr int T = S::T, E = Cf::E;
+  const int r = tid / (T / E), te = (tid - r * (T / E)) * E;
+  float* DT = reinterpret_cast<float*>(buf + S::bDT) + r * S::RowF + te;
+  float* Ut = reinterpret_cast<float*>(buf + S::bU) + r * S::RowF + te;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    DT[j] = v.dt[j];
+    Ut[j] = v.u[j];
   }
   if (PASS == 0) {
     float4* g4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(buf + S::bGate) + r * S::RowG + te);
 #pragma unroll
     for (int k = 0; k < E / 4; ++k)
-      g4[k] = make_float4(gate[4 * k], gate[4 * k + 1], gate[4 * k + 2], gate[4 * k + 3]);
+      g4[k] = make_float4(v.gate[4 * k], v.gate[4 * k + 1], v.gate[4 * k + 2], v.gate[4 * k + 3]);
   }
-  // B / C transposed to [t][n]
   constexpr int NT = N * T;
-  constexpr int PER = (NT + kScanThreads - 1) / kScanThreads;
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
+  for (int k = 0; k < PrepVals<IO, N, PASS>::PER; ++k) {
     const int e = tid + k * kScanThreads;
     if (NT % kScanThreads == 0 || e < NT) {
       const int n = e / T, t = e - n * T;
-      reinterpret_cast<float*>(buf + S::bBt)[t * S::RowBC + n] =
-          reinterpret_cast<const float*>(stage + S::oRawB)[e];
-      if (PASS == 0)
-        reinterpret_cast<float*>(buf + S::bCt)[t * S::RowBC + n] =
-            reinterpret_cast<const float*>(stage + S::oRawC)[e];
+      reinterpret_cast<float*>(buf + S::bBt)[t * S::RowBC + n] = v.bv[k];
+      if (PASS == 0) reinterpret_cast<float*>(buf + S::bCt)[t * S::RowBC + n] = v.cv[k];
     }
   }
 }
@@ -578,23 +601,21 @@ template <int N> struct LaneState {
   float A2s, nIs, sumDt;
 };
 
-// One pipelined chunk iteration: the recurrence of chunk i, the conversion of
-// chunk i+1 (stage `rawN` -> buffer `bufN`) and the finalisation of chunk i-1
+// One pipelined chunk iteration, after the block's hand-over: the recurrence
+// of chunk i, the stores of chunk i+1's conversion (computed into `pv` before
+// the hand-over) into buffer `bufN`, and the finalisation of chunk i-1
 // (buffer `bufF`, partials `partF`; stored only when `fin`).
 template <typename IO, int N, int PASS, bool FAST, bool WHOLE>
 __device__ __forceinline__ void chunk_iteration(
     const ScanArgs& p, LaneState<N>& ls, bool precise, int tid, int prow, int c, int g,
-    const float* sBias,
     const float* sD, int nrows,
-    const unsigned char* bufM, float* partM,                          // chunk i
-    const unsigned char* rawN, unsigned char* bufN, int tcountN,      // chunk i+1
+    const unsigned char* bufM, float* partM,                             // chunk i
+    const PrepVals<IO, N, PASS>& pv, unsigned char* bufN,                // chunk i+1
     const unsigned char* bufF, const float* partF, IO* yF, int tcountF,  // chunk i-1
-    bool fin, StepFlags fl) {
+    bool fin) {
   constexpr int NPT = ScanCfg<N>::NPT;
   auto other_chunks = [&]() {
-    // a whole chunk needs no step mask, and rows past the channel count need
-    // none either: TMA fills them with zeros, so u = 0 keeps their state at 0
-    prep_share<IO, N, PASS, FAST, !WHOLE>(rawN, bufN, sBias, tid, tcountN, nrows, fl);
+    prep_store<IO, N, PASS>(bufN, tid, pv);
     if (PASS == 0)
       finalize_share<IO, N, WHOLE>(p, bufF, partF, sD, tid, yF, tcountF, nrows, fin);
   };
@@ -625,7 +646,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
                                                             const __grid_constant__ ScanMaps maps) {
   using Cf = ScanCfg<N>;
   using S = ScanSmem<IO, N>;
-  constexpr int NPT = Cf::NPT, G = Cf::G, CH = Cf::CH, T = Cf::T, NS = Cf::NS;
+  constexpr int NPT = Cf::NPT, CH = Cf::CH, T = Cf::T, NS = Cf::NS;
   constexpr int NP = NPT / 2;  // packed pairs per lane (0 when NPT == 1)
   extern __shared__ unsigned char smem_raw[];
   // 128-byte aligned base, derived by pointer arithmetic (not an integer round
@@ -665,6 +686,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
                                : nullptr;
 
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(sm + S::oBar);
+  uint64_t* iter_bar = raw_full + NS;
   float* sBias = reinterpret_cast<float*>(sm + S::oBias);
   float* sD = reinterpret_cast<float*>(sm + S::oD);
   for (int r = tid; r < CH; r += kScanThreads) {
@@ -672,11 +694,14 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     sBias[r] = (p.bias && ok) ? p.bias[d0 + r] : 0.f;
     sD[r] = (p.D && ok) ? p.D[d0 + r] : 0.f;
   }
-  if (use_tma && tid == 0) {
-    prefetch_tmap(&maps.u);
-    prefetch_tmap(&maps.d);
-    prefetch_tmap(&maps.b);
+  if (tid == 0) {
+    if (use_tma) {
+      prefetch_tmap(&maps.u);
+      prefetch_tmap(&maps.d);
+      prefetch_tmap(&maps.b);
+    }
     for (int s = 0; s < NS; ++s) mbar_init(&raw_full[s], 1);
+    mbar_init(iter_bar, kScanThreads);
     fence_mbar_init();
   }
 
@@ -741,16 +766,54 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     ls.A2[j] = ls.Aj[j] * kLog2e;
   }
 
-  // chunk 0 is converted on its own; afterwards each iteration overlaps three chunks
+  // One iteration per chunk i:
+  //   A. (own data) wait for chunk i+1's TMA stage and convert this thread's
+  //      share of it into registers;
+  //   B. hand-over: wait until every thread has finished iteration i-1 (an
+  //      mbarrier every thread arrives on at the end of an iteration, so a
+  //      warp that is early does step A instead of idling at a barrier);
+  //   C. refill the stage chunk i left, store the conversion of i+1, run the
+  //      recurrence of chunk i and finalise chunk i-1; arrive.
+  auto convert = [&](int k, bool whole_k, PrepVals<IO, N, PASS>& v) {
+    // a whole chunk needs no step mask, and rows past the channel count need
+    // none either: their inputs are zero-filled, so u = 0 keeps their state at 0
+    if (fast) {
+      if (whole_k) prep_compute<IO, N, PASS, true, false>(stage_of(k), sBias, tid, tcount_of(k), nrows, fl, v);
+      else prep_compute<IO, N, PASS, true, true>(stage_of(k), sBias, tid, tcount_of(k), nrows, fl, v);
+    } else {
+      prep_compute<IO, N, PASS, false, true>(stage_of(k), sBias, tid, tcount_of(k), nrows, fl, v);
+    }
+  };
   bool ok = !use_tma || mbar_wait_bounded(&raw_full[0], 0);
   if (ok) {
-    if (fast) prep_share<IO, N, PASS, true>(stage_of(0), buf_of(0), sBias, tid, tcount_of(0), nrows, fl);
-    else prep_share<IO, N, PASS, false>(stage_of(0), buf_of(0), sBias, tid, tcount_of(0), nrows, fl);
+    PrepVals<IO, N, PASS> v0;
+    convert(0, false, v0);
+    prep_store<IO, N, PASS>(buf_of(0), tid, v0);
   }
-  bool failed = __syncthreads_or(!ok);
+  mbar_arrive(iter_bar);  // completes hand-over phase 0
+  bool failed = !ok;
   int i = 0;
   for (; i < nchunks && !failed; ++i) {
-    // stage (i % NS) is free again (chunk i was converted before the last barrier)
+    const bool has_next = i + 1 < nchunks;
+    const int tcN = has_next ? tcount_of(i + 1) : 0;
+    const int f = i > 0 ? i - 1 : 0;
+    // steady state: both neighbouring chunks whole and rows 16-byte aligned
+    const bool whole = p.vec_io && tcN == T && tcount_of(f) == T;
+    // A
+    PrepVals<IO, N, PASS> pv;
+    if (has_next) {
+      if (use_tma) ok = mbar_wait_bounded(&raw_full[(i + 1) % NS], (uint32_t)(((i + 1) / NS) & 1));
+      if (ok) convert(i + 1, whole, pv);
+    } else {
+      // no next chunk: a spare buffer receives zeros
+      pv = PrepVals<IO, N, PASS>{};
+    }
+    // B
+    if (!ok || !mbar_wait_bounded(iter_bar, (uint32_t)(i & 1))) {
+      failed = true;
+      break;
+    }
+    // C: stage (i % NS) is free again (every thread converted chunk i in iteration i-1)
     if (issued < nchunks) {
       if (use_tma) {
         if (tid == 0)
@@ -761,21 +824,11 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
       }
       ++issued;  // uniform: every thread counts the chunks issued
     }
-    const bool has_next = i + 1 < nchunks;
-    ok = true;
-    if (use_tma && has_next) ok = mbar_wait_bounded(&raw_full[(i + 1) % NS], (uint32_t)(((i + 1) / NS) & 1));
-    if (!use_tma) __syncthreads();  // the plain copy of chunk i + NS is complete
-    // without a next chunk the conversion reads a stale stage into a spare buffer
-    const int tcN = has_next ? tcount_of(i + 1) : 0;
-    const int f = i > 0 ? i - 1 : 0;
     IO* const yF = PASS == 0 ? y_base + (int64_t)f * T : nullptr;
-    // steady state: both neighbouring chunks whole and rows 16-byte aligned
-    const bool whole = p.vec_io && tcN == T && tcount_of(f) == T;
-#define SSM_ITER(FASTV, WHOLEV)                                                                \
-  chunk_iteration<IO, N, PASS, FASTV, WHOLEV>(p, ls, precise, tid, prow, c, g, sBias, sD, nrows, \
-                                             buf_of(i), part_of(i), stage_of(i + 1),          \
-                                             buf_of(i + 1), tcN, buf_of(f), part_of(f), yF,   \
-                                             tcount_of(f), i > 0, fl)
+#define SSM_ITER(FASTV, WHOLEV)                                                                  \
+  chunk_iteration<IO, N, PASS, FASTV, WHOLEV>(p, ls, precise, tid, prow, c, g, sD, nrows,        \
+                                             buf_of(i), part_of(i), pv, buf_of(i + 1),          \
+                                             buf_of(f), part_of(f), yF, tcount_of(f), i > 0)
     if (fast) {
       if (whole) SSM_ITER(true, true);
       else SSM_ITER(true, false);
@@ -783,13 +836,15 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
       SSM_ITER(false, false);
     }
 #undef SSM_ITER
-    failed = __syncthreads_or(!ok);
+    mbar_arrive(iter_bar);  // completes hand-over phase i + 1
   }
+  // the last chunk's partials are complete once every thread has arrived
+  if (!failed && !mbar_wait_bounded(iter_bar, (uint32_t)(nchunks & 1))) failed = true;
   if (failed) {
-    // a TMA chunk did not land in time: record it, let this block's copies
-    // still in flight land (bounded) and leave without writing a state
-    if (tid == 0) {
-      atomicExch(&g_scan_error, 1);
+    // a wait ran out: record it, let this block's copies still in flight
+    // land (bounded) and leave without writing a state
+    atomicExch(&g_scan_error, 1);
+    if (tid == 0 && use_tma) {
       for (int k = i; k < issued; ++k)
         (void)mbar_wait_bounded(&raw_full[k % NS], (uint32_t)((k / NS) & 1));
     }
