@@ -792,18 +792,38 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
   }
   mbar_arrive(iter_bar);  // completes hand-over phase 0
   bool failed = !ok;
+  // rotating buffer indices (no division in the loop): working buffers of
+  // chunks i-1, i, i+1; partial buffers of i-1, i; raw stages of i+1 and of
+  // the next chunk to fetch, with the parity of their next barrier phase
+  int bprev = 2, bcur = 0, bnext = 1 % S::NBT, pcur = 0;
+  int snext = 1 % NS;
+  uint32_t phnext = NS == 1 ? 1u : 0u;
+  int sissue = issued % NS;
   int i = 0;
   for (; i < nchunks && !failed; ++i) {
     const bool has_next = i + 1 < nchunks;
     const int tcN = has_next ? tcount_of(i + 1) : 0;
-    const int f = i > 0 ? i - 1 : 0;
+    const int tcF = i > 0 ? tcount_of(i - 1) : T;
     // steady state: both neighbouring chunks whole and rows 16-byte aligned
-    const bool whole = p.vec_io && tcN == T && tcount_of(f) == T;
+    const bool whole = p.vec_io && tcN == T && tcF == T;
+    unsigned char* const bufM = sm + S::oBuf + bcur * S::kBuf;
+    unsigned char* const bufN = sm + S::oBuf + bnext * S::kBuf;
+    unsigned char* const bufF = sm + S::oBuf + bprev * S::kBuf;
+    float* const partM = reinterpret_cast<float*>(sm + S::oPart + pcur * S::kPart);
+    float* const partF = reinterpret_cast<float*>(sm + S::oPart + (pcur ^ 1) * S::kPart);
     // A
     PrepVals<IO, N, PASS> pv;
     if (has_next) {
-      if (use_tma) ok = mbar_wait_bounded(&raw_full[(i + 1) % NS], (uint32_t)(((i + 1) / NS) & 1));
-      if (ok) convert(i + 1, whole, pv);
+      if (use_tma) ok = mbar_wait_bounded(&raw_full[snext], phnext);
+      if (ok) {
+        const unsigned char* st = sm + snext * S::kStage;
+        if (fast) {
+          if (whole) prep_compute<IO, N, PASS, true, false>(st, sBias, tid, tcN, nrows, fl, pv);
+          else prep_compute<IO, N, PASS, true, true>(st, sBias, tid, tcN, nrows, fl, pv);
+        } else {
+          prep_compute<IO, N, PASS, false, true>(st, sBias, tid, tcN, nrows, fl, pv);
+        }
+      }
     } else {
       // no next chunk: a spare buffer receives zeros
       pv = PrepVals<IO, N, PASS>{};
@@ -817,18 +837,18 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     if (issued < nchunks) {
       if (use_tma) {
         if (tid == 0)
-          issue_chunk<IO, N, PASS>(p, maps, stage_of(issued), &raw_full[issued % NS], b, d0,
+          issue_chunk<IO, N, PASS>(p, maps, sm + sissue * S::kStage, &raw_full[sissue], b, d0,
                                    t0_of(issued));
       } else {
-        load_chunk_plain<IO, N, PASS>(p, stage_of(issued), tid, b, d0, t0_of(issued));
+        load_chunk_plain<IO, N, PASS>(p, sm + sissue * S::kStage, tid, b, d0, t0_of(issued));
       }
       ++issued;  // uniform: every thread counts the chunks issued
+      sissue = sissue + 1 == NS ? 0 : sissue + 1;
     }
-    IO* const yF = PASS == 0 ? y_base + (int64_t)f * T : nullptr;
+    IO* const yF = PASS == 0 ? y_base + (int64_t)(i > 0 ? i - 1 : 0) * T : nullptr;
 #define SSM_ITER(FASTV, WHOLEV)                                                                  \
-  chunk_iteration<IO, N, PASS, FASTV, WHOLEV>(p, ls, precise, tid, prow, c, g, sD, nrows,        \
-                                             buf_of(i), part_of(i), pv, buf_of(i + 1),          \
-                                             buf_of(f), part_of(f), yF, tcount_of(f), i > 0)
+  chunk_iteration<IO, N, PASS, FASTV, WHOLEV>(p, ls, precise, tid, prow, c, g, sD, nrows, bufM,  \
+                                             partM, pv, bufN, bufF, partF, yF, tcF, i > 0)
     if (fast) {
       if (whole) SSM_ITER(true, true);
       else SSM_ITER(true, false);
@@ -837,6 +857,16 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     }
 #undef SSM_ITER
     mbar_arrive(iter_bar);  // completes hand-over phase i + 1
+    // rotate
+    const int bt = bprev;
+    bprev = bcur;
+    bcur = bnext;
+    bnext = bt;
+    pcur ^= 1;
+    if (++snext == NS) {
+      snext = 0;
+      phnext ^= 1u;
+    }
   }
   // the last chunk's partials are complete once every thread has arrived
   if (!failed && !mbar_wait_bounded(iter_bar, (uint32_t)(nchunks & 1))) failed = true;
