@@ -43,6 +43,10 @@ def _load():
         lib.ssm_oracle_step.argtypes = [i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                         i32, vp, vp, i32]
         lib.ssm_oracle_step.restype = i32
+        lib.ssm_oracle_scan_bwd.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            i64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            i64, vp, vp, i32]
+        lib.ssm_oracle_scan_bwd.restype = i32
         lib.ssm_oracle_max_threads.restype = i32
         _lib = lib
     return _lib
@@ -152,6 +156,81 @@ def step(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softpl
     if rc != 0:
         raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
     return y.reshape(batch, dim), st.reshape(batch, dim, N)
+
+
+def scan_bwd_rows(u, delta, z, unit_b, unit_d, A, B, C, D, delta_bias, delta_softplus,
+                  dy, init_state=None, d_final_state=None, nbatch=None, nthreads=0):
+    """Backward of ``scan_rows`` for U units given as rows (same conventions; every
+    row spans the whole time axis, L = u.shape[1]).
+
+    dy: (U, L) upstream derivative of y; d_final_state: (U, N) or None.
+    Returns a dict of float64 arrays: du, ddelta, dz (U, L; dz None without z);
+    dA_unit (U, N), dD_unit (U,), dbias_unit (U,), dinit (U, N): per-unit terms
+    (sum them by channel for the parameter gradients); dB, dC (nbatch, N, L):
+    summed over the given units of each batch."""
+    u = np.ascontiguousarray(u)
+    delta = np.ascontiguousarray(delta)
+    U, L = u.shape
+    io = _io(u)
+    assert delta.shape == u.shape and _io(delta) == io
+    if z is not None:
+        z = np.ascontiguousarray(z)
+        assert z.shape == u.shape and _io(z) == io
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    N = A.shape[1]
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    C = np.ascontiguousarray(C, dtype=np.float32)
+    assert B.shape == C.shape and B.shape[1] == N and B.shape[2] >= L
+    nbatch = B.shape[0] if nbatch is None else nbatch
+    ub = np.ascontiguousarray(unit_b, dtype=np.int64)
+    ud = np.ascontiguousarray(unit_d, dtype=np.int64)
+    assert ub.shape == (U,) and ud.shape == (U,)
+    assert (ud >= 0).all() and (ud < A.shape[0]).all()
+    D = None if D is None else np.ascontiguousarray(D, dtype=np.float32)
+    bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
+    h0 = None if init_state is None else np.ascontiguousarray(init_state, dtype=np.float64)
+    dfin = None if d_final_state is None else np.ascontiguousarray(d_final_state, dtype=np.float64)
+    assert h0 is None or h0.shape == (U, N)
+    assert dfin is None or dfin.shape == (U, N)
+    dy = np.ascontiguousarray(dy, dtype=np.float64)
+    assert dy.shape == (U, L)
+    out = dict(du=np.empty((U, L)), ddelta=np.empty((U, L)),
+               dz=None if z is None else np.empty((U, L)),
+               dA_unit=np.empty((U, N)), dD_unit=np.empty(U), dbias_unit=np.empty(U),
+               dinit=np.empty((U, N)), dB=np.empty((nbatch, N, L)), dC=np.empty((nbatch, N, L)))
+    rc = _load().ssm_oracle_scan_bwd(
+        U, L, N, io, _ptr(u), _ptr(delta), _ptr(z), _ptr(ub), _ptr(ud), _ptr(bias), _ptr(A),
+        _ptr(B), _ptr(C), B.shape[2], _ptr(D), int(bool(delta_softplus)), _ptr(h0), _ptr(dy),
+        _ptr(dfin), _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dz"]), _ptr(out["dA_unit"]),
+        _ptr(out["dD_unit"]), _ptr(out["dbias_unit"]), _ptr(out["dinit"]), nbatch,
+        _ptr(out["dB"]), _ptr(out["dC"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
+    return out
+
+
+def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+             init_state=None, dy=None, d_final_state=None, nthreads=0):
+    """Backward of ``scan`` for (batch, dim, L) inputs: the derivatives of
+    Σ y·dy + Σ final_state·d_final_state.  Returns float64 arrays du, ddelta,
+    dz (batch, dim, L), dA (dim, N), dB, dC (batch, N, L), dD, dbias (dim,) and
+    dinit (batch, dim, N)."""
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    bb, dd = np.meshgrid(np.arange(batch), np.arange(dim), indexing="ij")
+    U = batch * dim
+    r = scan_bwd_rows(u.reshape(U, L), delta.reshape(U, L),
+                      None if z is None else z.reshape(U, L), bb.ravel(), dd.ravel(), A, B, C, D,
+                      delta_bias, delta_softplus, np.asarray(dy, np.float64).reshape(U, L),
+                      None if init_state is None else np.asarray(init_state).reshape(U, N),
+                      None if d_final_state is None else np.asarray(d_final_state).reshape(U, N),
+                      batch, nthreads)
+    return dict(du=r["du"].reshape(batch, dim, L), ddelta=r["ddelta"].reshape(batch, dim, L),
+                dz=None if z is None else r["dz"].reshape(batch, dim, L),
+                dA=r["dA_unit"].reshape(batch, dim, N).sum(0),
+                dD=r["dD_unit"].reshape(batch, dim).sum(0),
+                dbias=r["dbias_unit"].reshape(batch, dim).sum(0),
+                dinit=r["dinit"].reshape(batch, dim, N), dB=r["dB"], dC=r["dC"])
 
 
 def rel_err(got, ref):

@@ -29,6 +29,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -142,6 +143,179 @@ int ssm_oracle_step(int64_t U, int64_t N, int io_bf16, const void* u, const void
               state + i * N, 1, y + i, state + i * N);
   }
   return 0;
+}
+
+/*
+ * Backward pass (reverse-mode derivative) of the scan above.
+ *
+ * The summary page ("Mamba: Linear-Time Sequence Modeling", section 4c,
+ * "hardware-aware algorithm") trains the layer by recomputing the states in
+ * the backward pass instead of storing the expanded (B, L, D, N) tensor; it
+ * gives no formula for the gradients.  This oracle takes them from the chain
+ * rule applied to the forward definition, one unit at a time, in double
+ * precision.  For a loss with upstream derivatives dy_t = dLoss/dy_t and
+ * dfinal = dLoss/dh_{L-1}:
+ *
+ *   g_t  = silu(z_t) (1 without a gate),   s_t = C_t·h_t + D u_t,  y_t = s_t g_t
+ *   ds_t = dy_t g_t,   dz_t = dy_t s_t silu'(z_t),  silu'(z) = σ(z)(1 + z(1 - σ(z)))
+ *   λ_t  = dLoss/dh_t = ds_t C_t + Ā_{t+1} λ_{t+1},  λ_{L-1} = ds_{L-1} C_{L-1} + dfinal
+ *   with h_t = Ā_t h_{t-1} + B̄_t B_t u_t (B̄_t here the scalar factor expm1(ΔA)/A):
+ *   du_t    = ds_t D + Σ_n λ_{t,n} B̄_{t,n} B_{t,n}
+ *   dB_{t,n} += λ_{t,n} B̄_{t,n} u_t           (summed over the channels of a batch)
+ *   dC_{t,n} += ds_t h_{t,n}                  (summed over the channels of a batch)
+ *   dΔ_t    = Σ_n λ_{t,n} (h_{t-1,n} A_n Ā_{t,n} + B_{t,n} u_t Ā_{t,n})
+ *             [dĀ/dΔ = A Ā, d(expm1(ΔA)/A)/dΔ = Ā]
+ *   dA_n   += λ_{t,n} (h_{t-1,n} Δ_t Ā_{t,n} + B_{t,n} u_t (Δ_t Ā_{t,n} - B̄_{t,n}) / A_n)
+ *             [A_n = 0: the limit Δ_t^2 / 2 for the second factor]
+ *   dΔraw_t = dΔ_t σ(Δraw_t + bias) with softplus, else dΔ_t;  dbias += dΔraw_t
+ *   dD     += ds_t u_t;   dh_{-1} = Ā_0 λ_0
+ */
+static double sigmoid(double x) {
+  return x >= 0.0 ? 1.0 / (1.0 + exp(-x)) : exp(x) / (1.0 + exp(x));
+}
+
+/* One unit.  dB_b / dC_b: this unit's batch slice of the accumulators
+ * (element (n, t) at [n * L + t]).  Scratch: L*N doubles for the states and L
+ * doubles each for Δ, Δraw + bias and s. */
+static void scan_bwd_unit(int64_t L, int64_t N, int bf16, const void* u, const void* delta,
+                          const void* z, int64_t row, double bias, const float* A_row,
+                          const float* B_b, const float* C_b, int64_t bc_ld, double Dd,
+                          int softplus_on, const double* h0, const double* dy_row,
+                          const double* dfinal, double* du_row, double* ddelta_row,
+                          double* dz_row, double* dA_out, double* dD_out, double* dbias_out,
+                          double* dinit_out, double* dB_b, double* dC_b, double* hs,
+                          double* dts, double* xs, double* ss) {
+  /* forward, keeping every state h_t (hs[t*N + n]), Δ_t, Δraw_t + bias and s_t */
+  for (int64_t t = 0; t < L; ++t) {
+    double ut = in_val(u, bf16, row * L + t);
+    double x = in_val(delta, bf16, row * L + t) + bias;
+    double dt = softplus_on ? softplus(x) : x;
+    double acc = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      double An = (double)A_row[n];
+      double prev = t > 0 ? hs[(t - 1) * N + n] : (h0 ? h0[n] : 0.0);
+      double abar = exp(dt * An);
+      double bbar = (An != 0.0) ? expm1(dt * An) / An : dt;
+      double h = abar * prev + bbar * (double)B_b[n * bc_ld + t] * ut;
+      hs[t * N + n] = h;
+      acc += (double)C_b[n * bc_ld + t] * h;
+    }
+    dts[t] = dt;
+    xs[t] = x;
+    ss[t] = acc + Dd * ut;
+  }
+  /* reverse */
+  double lam[512];
+  for (int64_t n = 0; n < N; ++n) {
+    lam[n] = dfinal ? dfinal[n] : 0.0;
+    dA_out[n] = 0.0;
+  }
+  double dD = 0.0, dbias = 0.0;
+  for (int64_t t = L - 1; t >= 0; --t) {
+    double ut = in_val(u, bf16, row * L + t);
+    double dt = dts[t];
+    double g = 1.0;
+    if (z) {
+      double zt = in_val(z, bf16, row * L + t);
+      double sg = sigmoid(zt);
+      g = zt * sg;
+      if (dz_row) dz_row[t] = dy_row[t] * ss[t] * sg * (1.0 + zt * (1.0 - sg));
+    }
+    double ds = dy_row[t] * g;
+    dD += ds * ut;
+    double du = ds * Dd;
+    double ddt = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      double An = (double)A_row[n];
+      double Bn = (double)B_b[n * bc_ld + t];
+      double Cn = (double)C_b[n * bc_ld + t];
+      double prev = t > 0 ? hs[(t - 1) * N + n] : (h0 ? h0[n] : 0.0);
+      double abar = exp(dt * An);
+      double bbar = (An != 0.0) ? expm1(dt * An) / An : dt;
+      double dbbar_dA = (An != 0.0) ? (dt * abar - bbar) / An : 0.5 * dt * dt;
+      lam[n] += ds * Cn;
+      dC_b[n * L + t] += ds * hs[t * N + n];
+      dB_b[n * L + t] += lam[n] * bbar * ut;
+      du += lam[n] * bbar * Bn;
+      ddt += lam[n] * (prev * An * abar + Bn * ut * abar);
+      dA_out[n] += lam[n] * (prev * dt * abar + Bn * ut * dbbar_dA);
+      lam[n] *= abar;
+    }
+    du_row[t] = du;
+    double dx = softplus_on ? ddt * sigmoid(xs[t]) : ddt;
+    ddelta_row[t] = dx;
+    dbias += dx;
+  }
+  *dD_out = dD;
+  *dbias_out = dbias;
+  if (dinit_out)
+    for (int64_t n = 0; n < N; ++n) dinit_out[n] = lam[n];
+}
+
+/*
+ * Backward of ssm_oracle_scan over U units (same input conventions).  dy is
+ * U x L doubles; dfinal (optional) U x N.  Outputs: du, ddelta (U x L), dz
+ * (U x L, optional; only with z), per-unit dA (U x N), dD (U), dbias (U) and
+ * dinit (U x N, optional); dB and dC (nbatch x N x L) receive the sums over
+ * the units of each batch (they are overwritten, not accumulated into).
+ * Returns 0, -1 on bad sizes, -2 when scratch memory runs out.
+ */
+int ssm_oracle_scan_bwd(int64_t U, int64_t L, int64_t N, int io_bf16, const void* u,
+                        const void* delta, const void* z, const int64_t* unit_b,
+                        const int64_t* unit_d, const float* delta_bias, const float* A,
+                        const float* B, const float* C, int64_t bc_ld, const float* D,
+                        int delta_softplus, const double* init_state, const double* dy,
+                        const double* dfinal, double* du, double* ddelta, double* dz,
+                        double* dA, double* dD, double* dbias, double* dinit, int64_t nbatch,
+                        double* dB, double* dC, int nthreads) {
+  if (N > 512 || N < 1 || L < 0 || U < 0 || nbatch < 1) return -1;
+  for (int64_t i = 0; i < U; ++i)
+    if (unit_b[i] < 0 || unit_b[i] >= nbatch) return -1;
+  const int64_t nbc = nbatch * N * L;
+  memset(dB, 0, sizeof(double) * (size_t)nbc);
+  memset(dC, 0, sizeof(double) * (size_t)nbc);
+  int failed = 0;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+#pragma omp parallel
+  {
+    double* acc = (double*)calloc((size_t)(2 * nbc), sizeof(double));
+    double* scratch = (double*)malloc(sizeof(double) * (size_t)(L * N + 3 * L + 1));
+    const int ok = acc && scratch;
+    if (!ok) {
+#pragma omp atomic write
+      failed = 1;
+    }
+    /* every thread reaches the loop (a work-sharing construct); one without
+       scratch skips its units and the call reports the failure */
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t i = 0; i < U; ++i) {
+      if (!ok) continue;
+      int64_t b = unit_b[i], d = unit_d[i];
+      scan_bwd_unit(L, N, io_bf16, u, delta, z, i, delta_bias ? (double)delta_bias[d] : 0.0,
+                    A + d * N, B + b * N * bc_ld, C + b * N * bc_ld, bc_ld,
+                    D ? (double)D[d] : 0.0, delta_softplus, init_state ? init_state + i * N : 0,
+                    dy + i * L, dfinal ? dfinal + i * N : 0, du + i * L, ddelta + i * L,
+                    (z && dz) ? dz + i * L : 0, dA + i * N, dD + i, dbias + i,
+                    dinit ? dinit + i * N : 0, acc + b * N * L, acc + nbc + b * N * L,
+                    scratch, scratch + L * N, scratch + L * N + L, scratch + L * N + 2 * L);
+    }
+    if (ok) {
+#pragma omp critical
+      {
+        for (int64_t k = 0; k < nbc; ++k) {
+          dB[k] += acc[k];
+          dC[k] += acc[nbc + k];
+        }
+      }
+    }
+    free(acc);
+    free(scratch);
+  }
+  return failed ? -2 : 0;
 }
 
 /* Threads OpenMP will use (the CPU baseline reports it). */

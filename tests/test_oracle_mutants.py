@@ -9,6 +9,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_bwd_pins as bwd_pins
 import test_oracle_pins as pins
 
 MUTANTS = {
@@ -30,9 +31,29 @@ MUTANTS = {
 }
 
 
-def _pin_calls():
+# mistakes in the backward (derivative) part of the oracle
+BWD_MUTANTS = {
+    "bwd_no_state_carry": ("      lam[n] *= abar;\n", ""),
+    "bwd_dbbar_dA_sign": ("(dt * abar - bbar) / An", "(bbar - dt * abar) / An"),
+    "bwd_zero_A_limit": ("0.5 * dt * dt", "dt * dt"),
+    "bwd_softplus_chain_dropped": ("double dx = softplus_on ? ddt * sigmoid(xs[t]) : ddt;",
+                                   "double dx = ddt;"),
+    "bwd_dC_uses_previous_state": ("dC_b[n * L + t] += ds * hs[t * N + n];",
+                                   "dC_b[n * L + t] += ds * prev;"),
+    "bwd_dB_without_bbar": ("dB_b[n * L + t] += lam[n] * bbar * ut;",
+                            "dB_b[n * L + t] += lam[n] * ut;"),
+    "bwd_ddelta_without_A": ("ddt += lam[n] * (prev * An * abar + Bn * ut * abar);",
+                             "ddt += lam[n] * (prev * abar + Bn * ut * abar);"),
+    "bwd_dz_without_silu_slope": ("sg * (1.0 + zt * (1.0 - sg))", "sg"),
+    "bwd_dfinal_ignored": ("lam[n] = dfinal ? dfinal[n] : 0.0;", "lam[n] = 0.0;"),
+    "bwd_du_without_D": ("double du = ds * Dd;", "double du = 0.0;"),
+    "bwd_gate_missing_in_ds": ("double ds = dy_row[t] * g;", "double ds = dy_row[t];"),
+}
+
+
+def _pin_calls(module=pins):
     calls = []
-    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+    for name, fn in inspect.getmembers(module, inspect.isfunction):
         if not name.startswith("test_") or name == "test_rel_err_metric":
             continue
         marks = getattr(fn, "pytestmark", [])
@@ -46,26 +67,47 @@ def _pin_calls():
     return calls
 
 
-@pytest.mark.parametrize("mutant", sorted(MUTANTS))
-def test_pins_catch_planted_mistake(mutant, tmp_path, monkeypatch):
-    old, new = MUTANTS[mutant]
+def _run_mutant(old, new, tmp_path, monkeypatch, module, part):
+    """Plant `old` -> `new` in one part of the oracle source: "fwd" (the scan and
+    the decode step) or "bwd" (the derivatives, from the sigmoid helper on)."""
     src = open(oracle._SRC).read()
-    assert src.count(old) == 1, "mutation site not found: " + mutant
+    cut = src.index("static double sigmoid(")
+    head, tail = src[:cut], src[cut:]
+    region = head if part == "fwd" else tail
+    assert region.count(old) == 1, "mutation site not found: " + old
+    region = region.replace(old, new)
     path = os.path.join(tmp_path, "mutant.c")
     with open(path, "w") as f:
-        f.write(src.replace(old, new))
+        f.write(region + tail if part == "fwd" else head + region)
     so = os.path.join(tmp_path, "libmutant.so")
     subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-o", so, path, "-lm"])
     real = oracle._load()
     lib = ctypes.CDLL(so)
-    for fname in ("ssm_oracle_scan", "ssm_oracle_step", "ssm_oracle_max_threads"):
+    for fname in ("ssm_oracle_scan", "ssm_oracle_step", "ssm_oracle_scan_bwd",
+                  "ssm_oracle_max_threads"):
         getattr(lib, fname).argtypes = getattr(real, fname).argtypes
         getattr(lib, fname).restype = getattr(real, fname).restype
     monkeypatch.setattr(oracle, "_lib", lib)
     caught = []
-    for name, call in _pin_calls():
+    for name, call in _pin_calls(module):
         try:
             call()
         except AssertionError:
             caught.append(name)
-    assert caught, "no pin caught mutant " + mutant
+    return caught
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(mutant, tmp_path, monkeypatch):
+    old, new = MUTANTS[mutant]
+    assert _run_mutant(old, new, tmp_path, monkeypatch, pins, "fwd"), "no pin caught mutant " + mutant
+
+
+@pytest.mark.parametrize("mutant", sorted(BWD_MUTANTS))
+def test_backward_pins_catch_planted_mistake(mutant, tmp_path, monkeypatch):
+    """The backward pins (finite differences of the forward, the transposed
+    convolution, the transition product) catch each planted derivative mistake;
+    the forward part of the oracle is left intact, so the finite differences
+    still see the true forward."""
+    old, new = BWD_MUTANTS[mutant]
+    assert _run_mutant(old, new, tmp_path, monkeypatch, bwd_pins, "bwd"), "no pin caught " + mutant
