@@ -278,7 +278,53 @@ def bench_scan(w, steps, warmup, world):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, f0.elapsed_time(f1))
-    return dict(ms=ms, clocks=ck, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h)
+    return dict(ms=ms, clocks=ck, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
+                inputs=sets[0])
+
+
+# ---------------------------------------------------------------------------
+# backward pass on the same layer
+# ---------------------------------------------------------------------------
+
+def bench_backward(w, g, steps, warmup, world):
+    """Per-step time of ssm_scan_bwd on the scan workload's device inputs `g`, with a
+    seeded dy (N(0, 1), the I/O dtype) drawn on the device; outputs and workspace are
+    allocated once.  u, delta, z and dy are 4 x 50 MB, larger than L2."""
+    import torch
+    import selective_state_space_128_b300 as ssm
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(w.seed + 1000)
+    dy = torch.randn(g["u"].shape, generator=gen, device="cuda").to(g["u"].dtype)
+    N = w.dstate
+    f32 = dict(dtype=torch.float32, device="cuda")
+    out = dict(du=torch.empty_like(g["u"]), ddelta=torch.empty_like(g["u"]),
+               dz=torch.empty_like(g["u"]), dA=torch.empty((w.dim, N), **f32),
+               dB=torch.empty((w.batch, N, w.seqlen), **f32),
+               dC=torch.empty((w.batch, N, w.seqlen), **f32), dD=torch.empty(w.dim, **f32),
+               dbias=torch.empty(w.dim, **f32))
+    nbytes = ssm.ssm_scan_bwd_workspace_bytes(w.batch, w.dim, w.seqlen, N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ssm.ssm_scan_bwd(g["u"], g["delta"], g["delta_bias"], g["A"], g["B"], g["C"], g["D"],
+                         g["z"], True, None, dy, None, out["du"], out["ddelta"], out["dA"],
+                         out["dB"], out["dC"], out["dD"], out["dz"], out["dbias"], None, ws,
+                         nbytes, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / steps
+    return dict(step_ms=ms, steps=steps, workspace_bytes=nbytes)
 
 
 # ---------------------------------------------------------------------------
@@ -429,6 +475,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--bwd-steps", type=int, default=20)
+    ap.add_argument("--no-bwd", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = synth.MAMBA_130M
@@ -444,6 +492,9 @@ def main():
     hbm_peak, sm_max, peak_kind = load_peaks()
 
     r = bench_scan(w, args.steps, args.warmup, world)
+    bwd = None if args.no_bwd else bench_backward(w, r["inputs"], args.bwd_steps, args.warmup,
+                                                  world)
+    r.pop("inputs")
     dec = None if args.no_decode else bench_decode(synth.DECODE, args.decode_steps, world)
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
@@ -493,6 +544,16 @@ def main():
                                     synth.DECODE.dim * synth.DECODE.dstate / 1e6),
                           "us_per_step_state_in_l2": dec["l2_resident_ms"] * 1e3,
                           "gpu_launches": 2 * dec["steps"]}
+    if bwd is not None:
+        bs = bwd["step_ms"] / 1e3
+        line["backward"] = {"workload": w.name, "steps": bwd["steps"],
+                            "us_per_step": bwd["step_ms"] * 1e3,
+                            "channel_steps_per_s": w.channel_steps / bs * world,
+                            "time_vs_forward": bs / step_s,
+                            "workspace_bytes": bwd["workspace_bytes"],
+                            "gpu_launches": 2 * bwd["steps"],
+                            "l2": "u, delta, z, dy: 4 x %.0f MB, larger than L2"
+                                  % (w.channel_steps * 2 / 1e6)}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line))

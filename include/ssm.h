@@ -194,6 +194,57 @@ int ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* delta_bi
                          int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                          int io_dtype, const float* init_state, void* stream);
 
+/*
+ * Backward pass (training).  The summary page ("Mamba: Linear-Time Sequence
+ * Modeling", section 4c, hardware-aware algorithm) trains the layer with the
+ * states recomputed in the backward pass rather than stored; this entry point
+ * does that.  It returns the derivatives of
+ *
+ *     Loss = Σ_{b,d,t} y[b,d,t] dy[b,d,t] + Σ_{b,d,n} final_state[b,d,n] d_final_state[b,d,n]
+ *
+ * with respect to every input of ssm_scan_fwd_ex, for the same inputs (u,
+ * delta, delta_bias, A, B, C, D, z, delta_softplus, init_state as in the
+ * forward call; y and final_state need not be kept: the pass recomputes them).
+ * The chain rule of equations (2) and (4) with the selection of Algorithm 2
+ * (see the kernel source for the formulas).
+ *
+ * Inputs (device, caller-owned; layouts as above):
+ *   dy             (batch, dim, seqlen) io_dtype   dLoss/dy, required
+ *   d_final_state  (batch, dim, dstate) float32    nullable (= 0)
+ * Outputs (device, caller-owned, written in full, never accumulated into):
+ *   du, ddelta     (batch, dim, seqlen) io_dtype   required; ddelta is dLoss/d(delta),
+ *                                                  the raw input before bias/softplus
+ *   dz             (batch, dim, seqlen) io_dtype   required when z is given; must be
+ *                                                  NULL when z is NULL
+ *   dA             (dim, dstate) float32           required (summed over the batch)
+ *   dB, dC         (batch, dstate, seqlen) float32 required (summed over the channels)
+ *   dD, d_delta_bias (dim) float32                 nullable (not written); with D or
+ *                                                  delta_bias NULL they hold the
+ *                                                  derivative at D = 0 / bias = 0
+ *   d_init_state   (batch, dim, dstate) float32    nullable; dLoss/d(init_state)
+ *                                                  (init_state NULL = zeros)
+ * Workspace: ssm_scan_bwd_workspace_bytes() bytes of device memory (16-byte
+ * aligned), required whenever batch, dim and seqlen are all non-zero; it
+ * holds the chunk-start states of the recomputation and per-block partial
+ * sums, nothing that outlives the call.
+ *
+ * Precision: fp32 arithmetic; bf16 outputs are rounded to nearest even.  The
+ * channel sums (dB, dC) and batch sums (dA, dD, d_delta_bias) are added in a
+ * fixed order, so results are the same from run to run.
+ * Errors: as ssm_scan_fwd_ex; outputs may not overlap inputs or each other.
+ * Execution: asynchronous on `stream` (two kernels: the pass and the
+ * fixed-order sums; memsets and a copy instead when a size is zero).
+ */
+size_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
+
+int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, const float* A,
+                 const float* B, const float* C, const float* D, const void* z,
+                 int delta_softplus, const float* init_state, const void* dy,
+                 const float* d_final_state, void* du, void* ddelta, float* dA, float* dB,
+                 float* dC, float* dD, void* dz, float* d_delta_bias, float* d_init_state,
+                 int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

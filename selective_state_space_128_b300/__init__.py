@@ -61,6 +61,10 @@ def load():
     lib.ssm_scan_fwd_noalloc.restype = i32
     lib.ssm_status.argtypes = [vp]
     lib.ssm_status.restype = i32
+    lib.ssm_scan_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    lib.ssm_scan_bwd_workspace_bytes.restype = sz
+    lib.ssm_scan_bwd.argtypes = [vp] * 8 + [i32] + [vp] * 12 + [i64, i64, i64, i64, i32, vp, sz, vp]
+    lib.ssm_scan_bwd.restype = i32
     _lib = lib
     return lib
 
@@ -199,6 +203,29 @@ def ssm_scan_fwd_noalloc(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y,
     _call("ssm_scan_fwd_noalloc", rc)
 
 
+def ssm_scan_bwd_workspace_bytes(batch, dim, seqlen, dstate) -> int:
+    return int(load().ssm_scan_bwd_workspace_bytes(batch, dim, seqlen, dstate))
+
+
+def ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, init_state, dy,
+                 d_final_state, du, ddelta, dA, dB, dC, dD, dz, d_delta_bias, d_init_state,
+                 workspace, workspace_bytes=None, stream=None):
+    """Tensor form of ``ssm_scan_bwd`` on the current torch stream (or ``stream``)."""
+    _check_dev(u, delta, delta_bias, A, B, C, D, z, init_state, dy, d_final_state, du, ddelta,
+               dA, dB, dC, dD, dz, d_delta_bias, d_init_state, workspace)
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    if workspace is not None and workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().ssm_scan_bwd(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B), _ptr(C),
+                             _ptr(D), _ptr(z), int(bool(delta_softplus)), _ptr(init_state),
+                             _ptr(dy), _ptr(d_final_state), _ptr(du), _ptr(ddelta), _ptr(dA),
+                             _ptr(dB), _ptr(dC), _ptr(dD), _ptr(dz), _ptr(d_delta_bias),
+                             _ptr(d_init_state), batch, dim, L, N, _io_dtype(u),
+                             _ptr(workspace), int(workspace_bytes or 0), _stream(stream))
+    _call("ssm_scan_bwd", rc)
+
+
 def static_scratch_bytes() -> int:
     """SSM_STATIC_SCRATCH_BYTES as defined in include/ssm.h."""
     import re
@@ -227,6 +254,31 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True
     ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, h, init_state, ws,
                     stream=stream)
     return y, h
+
+
+def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+             init_state=None, dy=None, d_final_state=None, want_init_grad=False, stream=None):
+    """Derivatives of Σ y·dy + Σ final_state·d_final_state for the inputs of ``scan``.
+    Allocates every output and the workspace; returns a dict with du, ddelta, dz (dtype of
+    u; dz None without z), dA, dB, dC, dD, dbias (float32; dD / dbias always computed) and
+    dinit (float32, when ``want_init_grad``)."""
+    import torch
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(du=torch.empty_like(u), ddelta=torch.empty_like(u),
+               dz=None if z is None else torch.empty_like(u),
+               dA=torch.empty((dim, N), **f32), dB=torch.empty((batch, N, L), **f32),
+               dC=torch.empty((batch, N, L), **f32), dD=torch.empty(dim, **f32),
+               dbias=torch.empty(dim, **f32),
+               dinit=torch.empty((batch, dim, N), **f32) if want_init_grad else None)
+    nbytes = ssm_scan_bwd_workspace_bytes(batch, dim, L, N)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, init_state, dy,
+                 d_final_state, out["du"], out["ddelta"], out["dA"], out["dB"], out["dC"],
+                 out["dD"], out["dz"], out["dbias"], out["dinit"], ws, nbytes, stream)
+    return out
 
 
 def exported_names():

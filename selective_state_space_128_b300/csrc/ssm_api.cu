@@ -171,4 +171,91 @@ int ssm_state_update(float* state, const void* u, const void* delta, const float
                              io_dtype, nullptr);
 }
 
+size_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
+  if (!supported_n(dstate) || !sizes_ok(batch, dim, seqlen)) return 0;
+  if (batch == 0 || dim == 0 || seqlen == 0) return 0;
+  return ssm::bwd_layout(batch, dim, seqlen, dstate).bytes;
+}
+
+int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, const float* A,
+                 const float* B, const float* C, const float* D, const void* z,
+                 int delta_softplus, const float* init_state, const void* dy,
+                 const float* d_final_state, void* du, void* ddelta, float* dA, float* dB,
+                 float* dC, float* dD, void* dz, float* d_delta_bias, float* d_init_state,
+                 int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
+  if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
+  if (dz && !z) return SSM_ERR_ARG;
+  const bool rows = batch > 0 && dim > 0;
+  const bool steps = rows && seqlen > 0;
+  if (steps && (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dB || !dC ||
+                (z && !dz)))
+    return SSM_ERR_ARG;
+  if (dim > 0 && !dA) return SSM_ERR_ARG;
+  if (batch > 0 && seqlen > 0 && (!dB || !dC)) return SSM_ERR_ARG;
+  const void* ptrs[] = {u, delta, delta_bias, A, B, C, D, z, init_state, dy, d_final_state,
+                        du, ddelta, dA, dB, dC, dD, dz, d_delta_bias, d_init_state, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
+  const size_t nio = (size_t)batch * (size_t)dim * (size_t)seqlen * esz;
+  const size_t nst = (size_t)batch * (size_t)dim * (size_t)dstate * 4;
+  const size_t nbc = (size_t)batch * (size_t)dstate * (size_t)seqlen * 4;
+  const size_t nA = (size_t)dim * (size_t)dstate * 4, nd = (size_t)dim * 4;
+  struct Span { const void* p; size_t n; };
+  const Span ins[] = {{u, nio}, {delta, nio}, {z, nio}, {dy, nio}, {delta_bias, nd}, {A, nA},
+                      {B, nbc}, {C, nbc}, {D, nd}, {init_state, nst}, {d_final_state, nst}};
+  const Span outs[] = {{du, nio}, {ddelta, nio}, {dz, nio}, {dA, nA}, {dB, nbc}, {dC, nbc},
+                       {dD, nd}, {d_delta_bias, nd}, {d_init_state, nst}};
+  for (size_t i = 0; i < sizeof outs / sizeof outs[0]; ++i) {
+    for (const Span& in : ins)
+      if (overlaps(outs[i].p, outs[i].n, in.p, in.n)) return SSM_ERR_ARG;
+    for (size_t j = i + 1; j < sizeof outs / sizeof outs[0]; ++j)
+      if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return SSM_ERR_ARG;
+  }
+  const ssm::BwdLayout lay = ssm::bwd_layout(batch, dim, seqlen, dstate);
+  if (steps) {
+    if (!workspace || workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
+    for (const Span& q : outs)
+      if (overlaps(workspace, lay.bytes, q.p, q.n)) return SSM_ERR_ARG;
+    for (const Span& q : ins)
+      if (overlaps(workspace, lay.bytes, q.p, q.n)) return SSM_ERR_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!steps) {
+    // empty sums are zero; with no steps the initial state passes its
+    // derivative through unchanged
+    cudaError_t e = cudaSuccess;
+    if (dA && nA) e = cudaMemsetAsync(dA, 0, nA, st);
+    if (e == cudaSuccess && dD && nd) e = cudaMemsetAsync(dD, 0, nd, st);
+    if (e == cudaSuccess && d_delta_bias && nd) e = cudaMemsetAsync(d_delta_bias, 0, nd, st);
+    if (e == cudaSuccess && nbc) e = cudaMemsetAsync(dB, 0, nbc, st);
+    if (e == cudaSuccess && nbc) e = cudaMemsetAsync(dC, 0, nbc, st);
+    if (e == cudaSuccess && d_init_state && nst)
+      e = d_final_state ? cudaMemcpyAsync(d_init_state, d_final_state, nst,
+                                          cudaMemcpyDeviceToDevice, st)
+                        : cudaMemsetAsync(d_init_state, 0, nst, st);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  }
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  ssm::BwdArgs a{};
+  a.u = u; a.delta = delta; a.z = z; a.bias = delta_bias; a.A = A; a.B = B; a.C = C; a.D = D;
+  a.init_state = init_state; a.dy = dy; a.d_final_state = d_final_state;
+  a.du = du; a.ddelta = ddelta; a.dz = dz; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD;
+  a.d_bias = d_delta_bias; a.d_init_state = d_init_state;
+  a.ckpt = reinterpret_cast<float*>(ws + lay.o_ckpt);
+  a.ws_B = reinterpret_cast<float*>(ws + lay.o_B);
+  a.ws_C = reinterpret_cast<float*>(ws + lay.o_C);
+  a.ws_A = reinterpret_cast<float*>(ws + lay.o_A);
+  a.ws_D = reinterpret_cast<float*>(ws + lay.o_D);
+  a.ws_bias = reinterpret_cast<float*>(ws + lay.o_bias);
+  a.batch = batch; a.dim = dim; a.L = seqlen; a.nblk = lay.nblk;
+  a.softplus = delta_softplus != 0;
+  a.force_precise = io_dtype == SSM_F32;
+  const cudaError_t e = ssm::bwd_launch(a, dstate, io_dtype, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 }  // extern "C"

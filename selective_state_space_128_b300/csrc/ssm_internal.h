@@ -75,4 +75,50 @@ cudaError_t scan_device_error(int* code, cudaStream_t stream);
 
 cudaError_t update_launch(const UpdateArgs& a, int64_t N, int io_dtype, cudaStream_t stream);
 
+// Arguments of the backward pass (device pointers; layouts as in include/ssm.h).
+struct BwdArgs {
+  const void* u;
+  const void* delta;
+  const void* z;
+  const float* bias;
+  const float* A;
+  const float* B;
+  const float* C;
+  const float* D;
+  const float* init_state;
+  const void* dy;
+  const float* d_final_state;
+  void* du;
+  void* ddelta;
+  void* dz;
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;
+  float* d_bias;
+  float* d_init_state;
+  // workspace parts (see BwdLayout)
+  float* ckpt;     // [batch][nch][dim][N]: state at the start of every chunk
+  float* ws_B;     // [batch][nblk][N][L]: per-block sums over the block's channels
+  float* ws_C;     // [batch][nblk][N][L]
+  float* ws_A;     // [batch][dim][N]: per-batch-row dA
+  float* ws_D;     // [batch][dim]
+  float* ws_bias;  // [batch][dim]
+  int64_t batch, dim, L, nblk;
+  int softplus;
+  int force_precise;
+};
+
+// Workspace of the backward pass: byte offsets of its parts (256-byte aligned)
+// and the total; nblk = channel blocks per batch row, nch = chunks per sequence.
+struct BwdLayout {
+  int64_t nblk, nch;
+  size_t o_ckpt, o_B, o_C, o_A, o_D, o_bias, bytes;
+};
+
+BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t L, int64_t N);
+
+// Enqueue the backward pass (two kernels).
+cudaError_t bwd_launch(const BwdArgs& a, int64_t N, int io_dtype, cudaStream_t stream);
+
 }  // namespace ssm

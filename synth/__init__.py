@@ -33,6 +33,7 @@ _lib = None
 # stream ids, one per tensor
 S_U, S_DELTA, S_Z, S_B, S_C, S_D, S_DT = 1, 2, 3, 4, 5, 6, 7
 S_DEC_U, S_DEC_DELTA, S_DEC_Z, S_DEC_B, S_DEC_C = 11, 12, 13, 14, 15
+S_DY, S_DFIN, S_H0 = 21, 22, 23          # backward: upstream derivatives, initial state
 
 NORMAL, UNIFORM, LOGUNIFORM = 0, 1, 2
 
@@ -197,6 +198,21 @@ def make_scan_inputs(w: ScanWorkload):
     C = fill(w.seed, S_C, 0, nbc, NORMAL, 0.0, 1.0).reshape(w.batch, w.dstate, w.seqlen)
     return dict(u=u, delta=delta, z=z, B=B, C=C, A=gen_A(w.dim, w.dstate), D=gen_D(w),
                 delta_bias=gen_delta_bias(w.seed, w.dim))
+
+
+def make_bwd_inputs(w: ScanWorkload, init_state=True, d_final_state=True):
+    """Inputs of the backward pass beyond the forward's: dy ~ N(0, 1) in the workload's
+    I/O dtype, (batch, dim, L); d_final_state and init_state ~ N(0, 1) float32,
+    (batch, dim, N) (None when not asked for)."""
+    n = w.batch * w.dim * w.seqlen
+    ns = w.batch * w.dim * w.dstate
+    out = dict(dy=fill(w.seed, S_DY, 0, n, NORMAL, 0.0, 1.0, dtype=w.io)
+               .reshape(w.batch, w.dim, w.seqlen))
+    out["d_final_state"] = (fill(w.seed, S_DFIN, 0, ns, NORMAL, 0.0, 1.0)
+                            .reshape(w.batch, w.dim, w.dstate) if d_final_state else None)
+    out["init_state"] = (fill(w.seed, S_H0, 0, ns, NORMAL, 0.0, 1.0)
+                         .reshape(w.batch, w.dim, w.dstate) if init_state else None)
+    return out
 
 
 def prefill_workload(dw: DecodeWorkload) -> ScanWorkload:

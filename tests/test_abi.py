@@ -114,3 +114,49 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ssm, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         ssm.load()
+
+
+def _bwd(**kw):
+    a = dict(u=FAKE, delta=FAKE + 0x1000000, bias=None, A=FAKE + 0x2000000, B=FAKE + 0x3000000,
+             C=FAKE + 0x4000000, D=None, z=None, softplus=1, init=None, dy=FAKE + 0x5000000,
+             dfin=None, du=FAKE + 0x6000000, ddelta=FAKE + 0x7000000, dA=FAKE + 0x8000000,
+             dB=FAKE + 0x9000000, dC=FAKE + 0xA000000, dD=None, dz=None, dbias=None, dinit=None,
+             batch=2, dim=64, L=128, N=16, io=ssm.SSM_BF16, ws=FAKE + 0x10000000,
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib().ssm_scan_bwd(a["u"], a["delta"], a["bias"], a["A"], a["B"], a["C"], a["D"],
+                              a["z"], a["softplus"], a["init"], a["dy"], a["dfin"], a["du"],
+                              a["ddelta"], a["dA"], a["dB"], a["dC"], a["dD"], a["dz"],
+                              a["dbias"], a["dinit"], a["batch"], a["dim"], a["L"], a["N"],
+                              a["io"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_backward_argument_errors():
+    for name in ("u", "delta", "A", "B", "C", "dy", "du", "ddelta", "dA", "dB", "dC"):
+        assert _bwd(**{name: None}) == ssm.SSM_ERR_ARG, name
+    assert _bwd(io=3) == ssm.SSM_ERR_ARG
+    assert _bwd(N=12) == ssm.SSM_ERR_UNSUPPORTED
+    # dz is required with a gate and refused without one
+    assert _bwd(z=FAKE + 0xB000000) == ssm.SSM_ERR_ARG
+    assert _bwd(dz=FAKE + 0xB000000) == ssm.SSM_ERR_ARG
+    assert _bwd(du=FAKE + 0x6000004) == ssm.SSM_ERR_ALIGN
+    assert _bwd(dinit=FAKE + 0xC000008) == ssm.SSM_ERR_ALIGN
+    # outputs overlapping an input or each other
+    assert _bwd(du=FAKE + 0x100) == ssm.SSM_ERR_ARG
+    assert _bwd(dB=FAKE + 0x8000100) == ssm.SSM_ERR_ARG
+    # the workspace is required and sized by ssm_scan_bwd_workspace_bytes
+    need = ssm.ssm_scan_bwd_workspace_bytes(2, 64, 128, 16)
+    assert need > 0
+    assert _bwd(ws=None) == ssm.SSM_ERR_WORKSPACE
+    assert _bwd(wsb=need - 1) == ssm.SSM_ERR_WORKSPACE
+    assert _bwd(ws=FAKE + 0x8000000, wsb=need) == ssm.SSM_ERR_ARG   # workspace over dA
+
+
+def test_backward_workspace_size():
+    # checkpoints [batch][chunks][dim][N] + per-block dB/dC partials + per-row sums
+    need = ssm.ssm_scan_bwd_workspace_bytes(8, 1536, 2048, 16)
+    ckpt = 8 * (2048 // 16) * 1536 * 16 * 4
+    parts = 2 * 8 * (1536 // 32) * 16 * 2048 * 4
+    assert ckpt + parts <= need <= ckpt + parts + 8 * 1536 * 18 * 4 + 6 * 256
+    assert ssm.ssm_scan_bwd_workspace_bytes(0, 1536, 2048, 16) == 0
+    assert ssm.ssm_scan_bwd_workspace_bytes(8, 1536, 2048, 3) == 0

@@ -1,0 +1,170 @@
+"""GPU parity of ssm_scan_bwd (the backward pass) against the fp64 backward oracle.
+
+Every derivative is compared element by element: du, ddelta, dz (batch, dim, L),
+dA (dim, N), dB, dC (batch, N, L), dD, dbias (dim), d_init_state (batch, dim, N).
+Bar, per output: max|gpu - ref| / max|ref| <= 1e-4 for float32 I/O and <= 1e-2 for
+bfloat16 I/O (the forward's bar; the bf16 outputs du/ddelta/dz are rounded to
+bfloat16, a relative 2^-9 of each value).  Sizes span several chunks and channel
+blocks with ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_128_b300 as ssm
+import synth
+from _gpu import dev_f32, dev_io, host64, upload_scan
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 1e-2}
+KEYS = ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "dbias", "dinit")
+
+
+def _as64(a):
+    a = np.asarray(a)
+    return synth.bf16_to_f32(a).astype(np.float64) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def _run(w, z=True, D=True, bias=True, softplus=True, init=True, dfin=True, zero_a=False):
+    x = synth.make_scan_inputs(w)
+    if zero_a:
+        x["A"][1, ::2] = 0.0           # channel 1: the A = 0 limit on half its states
+    if not softplus:
+        # Δ is used as given: make it a step size (positive, the recipe's range)
+        dpos = (np.abs(_as64(x["delta"])) * 0.2).astype(np.float32)
+        x["delta"] = dpos if w.io == "f32" else synth.f32_to_bf16(dpos)
+        x["delta_bias"] = np.full_like(x["delta_bias"], 0.01)
+    e = synth.make_bwd_inputs(w, init_state=init, d_final_state=dfin)
+    ref = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"] if D else None,
+                          x["z"] if z else None, x["delta_bias"] if bias else None, softplus,
+                          None if e["init_state"] is None else e["init_state"].astype(np.float64),
+                          _as64(e["dy"]),
+                          None if e["d_final_state"] is None else e["d_final_state"].astype(np.float64))
+    g = upload_scan(x)
+    out = ssm.scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"] if D else None,
+                       g["z"] if z else None, g["delta_bias"] if bias else None, softplus,
+                       init_state=dev_f32(e["init_state"]), dy=dev_io(e["dy"]),
+                       d_final_state=dev_f32(e["d_final_state"]), want_init_grad=True)
+    torch.cuda.synchronize()
+    return ref, out
+
+
+def _check(w, tol=None, **kw):
+    tol = TOL[w.io] if tol is None else tol
+    ref, out = _run(w, **kw)
+    errs = {}
+    for k in KEYS:
+        if ref[k] is None:
+            assert out[k] is None, k
+            continue
+        got = host64(out[k])
+        assert got.shape == ref[k].shape, k
+        assert np.isfinite(got).all(), k
+        errs[k] = oracle.rel_err(got, ref[k])
+    bad = {k: v for k, v in errs.items() if v > tol}
+    assert not bad, bad
+    return errs
+
+
+def test_fp32_all_inputs_ragged():
+    """float32 I/O, N 16: 3 channel blocks (70 = 2 x 32 + 6), 5 chunks (77 = 4 x 16 + 13)."""
+    w = synth.scaled(synth.TINY, name="bwd_f32", batch=2, dim=70, seqlen=77, dstate=16, seed=31,
+                     d_one=False)
+    errs = _check(w)
+    assert max(errs.values()) < 2e-5
+
+
+def test_bf16_mamba_value_recipe():
+    w = synth.scaled(synth.MAMBA_130M, name="bwd_bf16", batch=2, dim=96, seqlen=200, seed=32)
+    _check(w)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 32, 64])
+def test_bf16_every_state_size(N):
+    w = synth.scaled(synth.MAMBA_130M, name="bwd_n%d" % N, batch=2, dim=150, seqlen=45,
+                     dstate=N, seed=40 + N)
+    _check(w)
+
+
+@pytest.mark.parametrize("N", [1, 4, 64])
+def test_fp32_state_sizes(N):
+    w = synth.scaled(synth.TINY, name="bwd_f32_n%d" % N, batch=1, dim=33, seqlen=37, dstate=N,
+                     seed=50 + N, d_one=False)
+    _check(w)
+
+
+@pytest.mark.parametrize("variant", ["no_gate", "no_softplus", "no_D_no_bias", "no_init_no_dfinal",
+                                     "zero_A"])
+def test_bf16_variants(variant):
+    w = synth.scaled(synth.MAMBA_130M, name="bwd_" + variant, batch=2, dim=40, seqlen=70,
+                     seed=60)
+    kw = dict(no_gate=dict(z=False), no_softplus=dict(softplus=False),
+              no_D_no_bias=dict(D=False, bias=False),
+              no_init_no_dfinal=dict(init=False, dfin=False), zero_A=dict(zero_a=True))[variant]
+    _check(w, **kw)
+
+
+def test_fp32_zero_A_precise_limit():
+    w = synth.scaled(synth.TINY, name="bwd_f32_zeroA", batch=1, dim=20, seqlen=50, dstate=16,
+                     seed=61, d_one=False)
+    _check(w, zero_a=True)
+
+
+def test_single_step_and_single_channel():
+    for (b, d, L) in ((1, 1, 1), (3, 1, 17), (1, 5, 1)):
+        w = synth.scaled(synth.MAMBA_130M, name="bwd_small", batch=b, dim=d, seqlen=L, seed=62)
+        _check(w)
+
+
+def test_chunked_backward_equals_one_shot():
+    """A sequence split in two launches, the second's d_init_state feeding the first's
+    d_final_state (and the first's final state the second's init_state), gives the
+    same derivatives as one launch over the whole sequence."""
+    w = synth.scaled(synth.MAMBA_130M, name="bwd_chunked", batch=2, dim=64, seqlen=96, seed=63,
+                     io="f32")
+    x = synth.make_scan_inputs(w)
+    e = synth.make_bwd_inputs(w, init_state=False)
+    g = upload_scan(x)
+    dy = dev_io(e["dy"])
+    dfin = dev_f32(e["d_final_state"])
+    whole = ssm.scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                         g["delta_bias"], True, dy=dy, d_final_state=dfin)
+    cut = 40
+    part = {k: (g[k][..., :cut].contiguous(), g[k][..., cut:].contiguous())
+            for k in ("u", "delta", "z", "B", "C")}
+    _, h_mid = ssm.scan(part["u"][0], part["delta"][0], g["A"], part["B"][0], part["C"][0], g["D"],
+                        part["z"][0], g["delta_bias"])
+    second = ssm.scan_bwd(part["u"][1], part["delta"][1], g["A"], part["B"][1], part["C"][1],
+                          g["D"], part["z"][1], g["delta_bias"], True, init_state=h_mid,
+                          dy=dy[..., cut:].contiguous(), d_final_state=dfin, want_init_grad=True)
+    first = ssm.scan_bwd(part["u"][0], part["delta"][0], g["A"], part["B"][0], part["C"][0],
+                         g["D"], part["z"][0], g["delta_bias"], True,
+                         dy=dy[..., :cut].contiguous(), d_final_state=second["dinit"])
+    torch.cuda.synchronize()
+    for k in ("du", "ddelta", "dz", "dB", "dC"):
+        got = torch.cat([first[k], second[k]], dim=-1)
+        assert oracle.rel_err(host64(got), host64(whole[k])) < 1e-5, k
+    for k in ("dA", "dD", "dbias"):
+        assert oracle.rel_err(host64(first[k] + second[k]), host64(whole[k])) < 1e-5, k
+
+
+def test_empty_sizes():
+    dev = "cuda"
+    A = torch.full((8, 16), -1.0, device=dev)
+    # no steps: sums are zero, d_init_state = d_final_state
+    u = torch.zeros((2, 8, 0), dtype=torch.bfloat16, device=dev)
+    B = torch.zeros((2, 16, 0), device=dev)
+    dfin = torch.randn((2, 8, 16), device=dev)
+    out = ssm.scan_bwd(u, u, A, B, B, torch.ones(8, device=dev), None, None, True, dy=u,
+                       d_final_state=dfin, want_init_grad=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out["dinit"], dfin)
+    assert out["dA"].abs().max().item() == 0.0 and out["dD"].abs().max().item() == 0.0
+    assert out["dbias"].abs().max().item() == 0.0
+    # no channels: dB and dC are zero sums
+    u = torch.zeros((2, 0, 5), dtype=torch.bfloat16, device=dev)
+    B = torch.randn((2, 16, 5), device=dev)
+    out = ssm.scan_bwd(u, u, torch.zeros((0, 16), device=dev), B, B, dy=u)
+    torch.cuda.synchronize()
+    assert out["dB"].abs().max().item() == 0.0 and out["dC"].abs().max().item() == 0.0
