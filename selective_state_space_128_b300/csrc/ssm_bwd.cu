@@ -58,6 +58,9 @@ template <int N> struct BwdCfg {
   // channel reductions: threads per reduced vector and channels per thread
   static constexpr int RS = kBwdThreads / (T * G * QN);
   static constexpr int RCH = CH / RS;
+  // resident blocks per SM the register budget is sized for (the lanes with 16
+  // states, and the 16-step rows of N = 4, need more than a third of the file)
+  static constexpr int MINB = (NPT >= 16 || (NPT == 4 && E >= 16)) ? 2 : 3;
   static_assert(G * NPT == N && E >= 1 && TPR <= 4 && RS >= 1 && RCH * RS == CH, "tiling");
 };
 
@@ -134,15 +137,51 @@ template <typename IO> __device__ __forceinline__ float ld_io(const void* p, int
   return io_traits<IO>::to_f32(static_cast<const IO*>(p)[i]);
 }
 
+// Raw global inputs of one thread's share of a chunk (E steps of one channel row;
+// PER elements of each of B and C), fetched one chunk ahead so that the loads
+// are in flight while the block works on the current chunk.
+template <int N> struct BwdPre {
+  static constexpr int E = BwdCfg<N>::E;
+  static constexpr int PER = (N * BwdCfg<N>::T + kBwdThreads - 1) / kBwdThreads;
+  float dl[E], u[E], dy[E], z[E];
+  float b[PER], c[PER];
+  float h[BwdCfg<N>::NPT];  // the lane's chunk-start state (adjoint sweep)
+};
+
+// One recurrence step of a lane, fast flavour, packed pairs:
+// h = Ā (h - v) + v with Ā = 2^(Δ A log2 e), v = -B u / A.
+template <int NP>
+__device__ __forceinline__ void step_pairs(f2 (&hq)[NP], float dt, float u, const f2 (&Bq)[NP],
+                                           const f2 (&A2p)[NP], const f2 (&nIp)[NP]) {
+  const f2 dt2 = pack2(dt, dt), u2 = pack2(u, u);
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    float x0, x1;
+    unpack2(mul2(dt2, A2p[q]), x0, x1);
+    const f2 a = pack2(ex2_fast(x0), ex2_fast(x1));
+    const f2 v = mul2(mul2(Bq[q], u2), nIp[q]);
+    hq[q] = fma2(a, sub2(hq[q], v), v);
+  }
+}
+
+template <int K> __device__ __forceinline__ void lds_f2(const float* p, f2 (&v)[K]) {
+#pragma unroll
+  for (int q = 0; q + 1 < K; q += 2) lds_pairs(p + 2 * q, v[q], v[q + 1]);
+  if constexpr (K % 2 == 1) lds_pair(p + 2 * (K - 1), v[K - 1]);
+}
+
 // ---------------------------------------------------------------------------
 // The per-block kernel
 // ---------------------------------------------------------------------------
 template <typename IO, int N>
-__global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs p) {
+__global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(const BwdArgs p) {
   using Cf = BwdCfg<N>;
   using S = BwdSmem<N>;
   constexpr int NPT = Cf::NPT, CH = Cf::CH, T = Cf::T, E = Cf::E, TPR = Cf::TPR;
   constexpr int VW = Cf::VW, QN = Cf::QN, G = Cf::G;
+  constexpr int NP = NPT / 2 > 0 ? NPT / 2 : 1;  // packed pairs per lane (fast flavour)
+  constexpr bool PAIRS = NPT % 2 == 0;
+  constexpr int PER = BwdPre<N>::PER;
   extern __shared__ float4 smem_f4[];
   float* sm = reinterpret_cast<float*>(smem_f4);
   float* sDT = sm + S::oDT;
@@ -173,137 +212,228 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   const int r = tid / TPR, te = (tid % TPR) * E;
   const bool row_ok = r < nrows;
   const int64_t io_row = (b * p.dim + d0 + (row_ok ? r : 0)) * L;
+  const bool vec = E % 4 == 0 && L % 4 == 0;  // E-step runs are 8- / 16-byte aligned
 
   for (int i = tid; i < CH; i += kBwdThreads) {
     const bool ok = d0 + i < p.dim;
     sBias[i] = (p.bias && ok) ? p.bias[d0 + i] : 0.f;
     sD[i] = (p.D && ok) ? p.D[d0 + i] : 0.f;
   }
-  float Aj[NPT], A2[NPT], invA[NPT];
+  float Aj[NPT], invA[NPT];
+  f2 A2p[NP], nIp[NP], iAp[NP], Ajp[NP];
   bool zeroA = false;
 #pragma unroll
   for (int j = 0; j < NPT; ++j) {
     Aj[j] = chan_ok ? p.A[d * N + g * NPT + j] : -1.f;
     zeroA |= Aj[j] == 0.f;
-    A2[j] = Aj[j] * kLog2e;
     invA[j] = Aj[j] != 0.f ? 1.f / Aj[j] : 0.f;
   }
+  if constexpr (PAIRS) {
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      A2p[q] = pack2(Aj[2 * q] * kLog2e, Aj[2 * q + 1] * kLog2e);
+      nIp[q] = pack2(-invA[2 * q], -invA[2 * q + 1]);
+      iAp[q] = pack2(invA[2 * q], invA[2 * q + 1]);
+      Ajp[q] = pack2(Aj[2 * q], Aj[2 * q + 1]);
+    }
+  }
   const bool precise = __syncthreads_or(zeroA) || p.force_precise;
+  const bool fast_pairs = PAIRS && !precise;  // block-uniform
   const bool sp = p.softplus != 0;
 
-  // one recurrence step of this lane (states in h), for recompute and the checkpoint sweep
-  auto lane_step = [&](float (&h)[NPT], float dt, float u, const float* Brow) {
-    float Bv[NPT];
-    lds_vec<NPT>(Brow, Bv);
-#pragma unroll
-    for (int j = 0; j < NPT; ++j) {
-      const float Bn = Bv[j];
-      if (!precise) {
-        const float a = ex2_fast(dt * A2[j]);
-        const float v = -Bn * u * invA[j];  // fixed point -B u / A
-        h[j] = fmaf(a, h[j] - v, v);
-      } else {
-        const float x = dt * Aj[j];
-        const float bb = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
-        h[j] = fmaf(expf(x), h[j], bb * (Bn * u));
-      }
-    }
-  };
-  // Δ, u (and, with `full`, ds, z, dy, σ) of this thread's E steps of chunk k
-  auto load_steps = [&](int k, bool full, float (&dyv)[E], float (&zz)[E], float (&sg)[E]) {
+  // ---- global -> registers (one chunk ahead) ----
+  auto fetch = [&](int k, bool full, BwdPre<N>& pr) {
     const int64_t t0 = (int64_t)k * T;
     const int tc = (int)min64(T, L - t0);
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-      const int t = te + j;
-      const bool ok = row_ok && t < tc;
-      const int64_t gi = io_row + t0 + t;
-      float dt = 0.f, u = 0.f, ds = 0.f;
-      dyv[j] = 0.f;
-      zz[j] = 0.f;
-      sg[j] = 1.f;
-      if (ok) {
-        u = ld_io<IO>(p.u, gi);
-        const float x = ld_io<IO>(p.delta, gi) + sBias[r];
-        dt = sp ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
+    const int64_t gi = io_row + t0 + te;
+    bool done = false;
+    if constexpr (E % 4 == 0) {
+      if (row_ok && vec && te + E <= tc) {
+        vecio<IO, E>::load(static_cast<const IO*>(p.delta) + gi, pr.dl);
+        vecio<IO, E>::load(static_cast<const IO*>(p.u) + gi, pr.u);
         if (full) {
-          if (sp) sg[j] = precise ? sigmoid_precise(x) : sigmoid_fast(x);
-          dyv[j] = ld_io<IO>(p.dy, gi);
-          float gate = 1.f;
-          if (p.z) {
-            zz[j] = ld_io<IO>(p.z, gi);
-            gate = precise ? silu_precise(zz[j]) : silu_fast(zz[j]);
-          }
-          ds = dyv[j] * gate;
+          vecio<IO, E>::load(static_cast<const IO*>(p.dy) + gi, pr.dy);
+          if (p.z) vecio<IO, E>::load(static_cast<const IO*>(p.z) + gi, pr.z);
+        }
+        done = true;
+      }
+    }
+    if (!done) {
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const bool ok = row_ok && te + j < tc;
+        pr.dl[j] = ok ? ld_io<IO>(p.delta, gi + j) : 0.f;
+        pr.u[j] = ok ? ld_io<IO>(p.u, gi + j) : 0.f;
+        if (full) {
+          pr.dy[j] = ok ? ld_io<IO>(p.dy, gi + j) : 0.f;
+          pr.z[j] = (ok && p.z) ? ld_io<IO>(p.z, gi + j) : 0.f;
         }
       }
-      sDT[r * Cf::RowF + t] = dt;
-      sU[r * Cf::RowF + t] = u;
-      if (full) sDS[r * Cf::RowF + t] = ds;
     }
-    // B (and C) transposed to [t][n]; zero past the end of the sequence
-    for (int e = tid; e < N * T; e += kBwdThreads) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = tid + i * kBwdThreads;
       const int n = e / T, t = e - n * T;
-      const bool ok = t < tc;
+      const bool ok = (N * T % kBwdThreads == 0 || e < N * T) && t < tc;
       const int64_t bi = (b * N + n) * L + t0 + t;
-      sBt[t * Cf::RowBC + n] = ok ? p.B[bi] : 0.f;
-      if (full) sCt[t * Cf::RowBC + n] = ok ? p.C[bi] : 0.f;
+      pr.b[i] = ok ? p.B[bi] : 0.f;
+      if (full) pr.c[i] = ok ? p.C[bi] : 0.f;
+    }
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) pr.h[j] = chan_ok ? p.ckpt[((b * nch + k) * p.dim + d) * N + g * NPT + j] : 0.f;
+    }
+  };
+  // ---- registers -> shared tiles; Δ, σ, gate, ds per channel step ----
+  auto stage = [&](int k, bool full, const BwdPre<N>& pr, float (&dyv)[E], float (&zz)[E],
+                   float (&sg)[E]) {
+    const int64_t t0 = (int64_t)k * T;
+    const int tc = (int)min64(T, L - t0);
+    const float bias = sBias[r];
+    float dtv[E], dsv[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const bool ok = row_ok && te + j < tc;
+      const float x = pr.dl[j] + bias;
+      const float dt = sp ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
+      dtv[j] = ok ? dt : 0.f;
+      if (full) {
+        sg[j] = sp ? (precise ? sigmoid_precise(x) : sigmoid_fast(x)) : 1.f;
+        dyv[j] = pr.dy[j];
+        zz[j] = pr.z[j];
+        const float gate = p.z ? (precise ? silu_precise(zz[j]) : silu_fast(zz[j])) : 1.f;
+        dsv[j] = ok ? dyv[j] * gate : 0.f;
+      }
+    }
+    float* rowDT = sDT + r * Cf::RowF + te;
+    float* rowU = sU + r * Cf::RowF + te;
+    float* rowDS = sDS + r * Cf::RowF + te;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      rowDT[j] = dtv[j];
+      rowU[j] = pr.u[j];
+      if (full) rowDS[j] = dsv[j];
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = tid + i * kBwdThreads;
+      if (N * T % kBwdThreads == 0 || e < N * T) {
+        const int n = e / T, t = e - n * T;
+        sBt[t * Cf::RowBC + n] = pr.b[i];
+        if (full) sCt[t * Cf::RowBC + n] = pr.c[i];
+      }
     }
   };
   auto hs_vec = [&](int slot, int q, int lane) {
     return sHs + ((slot * QN + q) * kBwdThreads + lane) * VW;
   };
-  auto ckpt_ptr = [&](int k) {
-    return p.ckpt + ((b * nch + k) * p.dim + d) * N + g * NPT;
+  // this lane's NPT states of a slot as packed pairs (VW / 2 pairs per vector)
+  auto hs_store_pairs = [&](int slot, const f2 (&v)[NP]) {
+#pragma unroll
+    for (int q = 0; q < QN; ++q) {
+      if constexpr (VW == 4) sts_pairs(hs_vec(slot, q, tid), v[2 * q], v[2 * q + 1]);
+      else sts_pair(hs_vec(slot, q, tid), v[q]);
+    }
+  };
+  auto hs_load_pairs = [&](int slot, f2 (&v)[NP]) {
+#pragma unroll
+    for (int q = 0; q < QN; ++q) {
+      if constexpr (VW == 4) lds_pairs(hs_vec(slot, q, tid), v[2 * q], v[2 * q + 1]);
+      else lds_pair(hs_vec(slot, q, tid), v[q]);
+    }
   };
 
   // ---------------- sweep 1: chunk-start states ----------------
   float h[NPT];
+  f2 hq[NP];
 #pragma unroll
   for (int j = 0; j < NPT; ++j)
     h[j] = (p.init_state && chan_ok) ? p.init_state[(b * p.dim + d) * N + g * NPT + j] : 0.f;
-  {
-    float dyv[E], zz[E], sg[E];
-    for (int k = 0; k < nch; ++k) {
-      if (chan_ok) {
-        float* cp = ckpt_ptr(k);
+  if constexpr (PAIRS) {
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) cp[j] = h[j];
-      }
-      load_steps(k, false, dyv, zz, sg);
-      __syncthreads();
-#pragma unroll 4
-      for (int t = 0; t < T; ++t)
-        lane_step(h, sDT[c * Cf::RowF + t], sU[c * Cf::RowF + t], sBt + t * Cf::RowBC + g * NPT);
-      __syncthreads();
+    for (int q = 0; q < NP; ++q) hq[q] = pack2(h[2 * q], h[2 * q + 1]);
+  }
+  float dyv[E], zz[E], sg[E];
+  BwdPre<N> pre;
+  if (nch > 0) fetch(0, false, pre);
+  for (int k = 0; k < nch; ++k) {
+    if (fast_pairs) {
+#pragma unroll
+      for (int q = 0; q < NP; ++q) unpack2(hq[q], h[2 * q], h[2 * q + 1]);
     }
+    if (chan_ok) {
+      float* cp = p.ckpt + ((b * nch + k) * p.dim + d) * N + g * NPT;
+      sts_vec<NPT>(cp, h);  // (a global store; sts_vec only packs the vector)
+    }
+    stage(k, false, pre, dyv, zz, sg);
+    if (k + 1 < nch) fetch(k + 1, false, pre);
+    __syncthreads();
+    const float* rDT = sDT + c * Cf::RowF;
+    const float* rU = sU + c * Cf::RowF;
+    if (fast_pairs) {
+#pragma unroll 4
+      for (int t = 0; t < T; ++t) {
+        f2 Bq[NP];
+        lds_f2<NP>(sBt + t * Cf::RowBC + g * NPT, Bq);
+        step_pairs<NP>(hq, rDT[t], rU[t], Bq, A2p, nIp);
+      }
+    } else {
+#pragma unroll 4
+      for (int t = 0; t < T; ++t) {
+        float Bv[NPT];
+        lds_vec<NPT>(sBt + t * Cf::RowBC + g * NPT, Bv);
+        const float dt = rDT[t], u = rU[t];
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+          if (!precise) {
+            const float a = ex2_fast(dt * Aj[j] * kLog2e);
+            const float v = -Bv[j] * u * invA[j];
+            h[j] = fmaf(a, h[j] - v, v);
+          } else {
+            const float x = dt * Aj[j];
+            const float bb = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
+            h[j] = fmaf(expf(x), h[j], bb * (Bv[j] * u));
+          }
+        }
+      }
+    }
+    __syncthreads();
   }
 
   // ---------------- sweep 2: adjoint, chunk by chunk from the end ----------------
   float lam[NPT], dAacc[NPT];
+  f2 lq[NP], dAq[NP];
 #pragma unroll
   for (int j = 0; j < NPT; ++j) {
     lam[j] = (p.d_final_state && chan_ok) ? p.d_final_state[(b * p.dim + d) * N + g * NPT + j] : 0.f;
     dAacc[j] = 0.f;
   }
+  if constexpr (PAIRS) {
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      lq[q] = pack2(lam[2 * q], lam[2 * q + 1]);
+      dAq[q] = pack2(0.f, 0.f);
+    }
+  }
   float dD_acc = 0.f, dbias_acc = 0.f;
   float* wsB_blk = p.ws_B + ((b * p.nblk + blk) * N) * L;
   float* wsC_blk = p.ws_C + ((b * p.nblk + blk) * N) * L;
+  // channel reductions: this thread's output vector (step rt, state group rg, part rq)
+  const int vid = tid / Cf::RS, part = tid % Cf::RS;
+  const int rt = vid / (G * QN), rg = (vid % (G * QN)) / QN, rq = vid % QN;
 
+  if (nch > 0) fetch(nch - 1, true, pre);
   for (int k = nch - 1; k >= 0; --k) {
     const int64_t t0 = (int64_t)k * T;
     const int tc = (int)min64(T, L - t0);
-    // P1: per-step inputs of the chunk; this lane's start state
-    float dyv[E], zz[E], sg[E];
-    load_steps(k, true, dyv, zz, sg);
-    if (chan_ok) {
-      const float* cp = ckpt_ptr(k);
+    // P1: stage the chunk; the next (earlier) chunk's loads go in flight
+    stage(k, true, pre, dyv, zz, sg);
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) h[j] = cp[j];
-    } else {
-#pragma unroll
-      for (int j = 0; j < NPT; ++j) h[j] = 0.f;
-    }
+    for (int j = 0; j < NPT; ++j) h[j] = pre.h[j];
+    if (k > 0) fetch(k - 1, true, pre);
+    const float* rDT = sDT + c * Cf::RowF;
+    const float* rU = sU + c * Cf::RowF;
+    const float* rDS = sDS + c * Cf::RowF;
     __syncthreads();
 
     // P2: recompute the chunk's states into slots 1..T, readout partials
@@ -311,56 +441,115 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
 #pragma unroll
       for (int q = 0; q < QN; ++q) sts_vec<VW>(hs_vec(0, q, tid), h + q * VW);
       float acc4[4];
+      if (fast_pairs) {
+#pragma unroll
+        for (int q = 0; q < NP; ++q) hq[q] = pack2(h[2 * q], h[2 * q + 1]);
 #pragma unroll 4
-      for (int t = 0; t < T; ++t) {
-        const float* Brow = sBt + t * Cf::RowBC + g * NPT;
-        const float* Crow = sCt + t * Cf::RowBC + g * NPT;
-        lane_step(h, sDT[c * Cf::RowF + t], sU[c * Cf::RowF + t], Brow);
-        float Cv[NPT];
-        lds_vec<NPT>(Crow, Cv);
-        float s = 0.f;
+        for (int t = 0; t < T; ++t) {
+          f2 Bq[NP], Cq[NP];
+          lds_f2<NP>(sBt + t * Cf::RowBC + g * NPT, Bq);
+          lds_f2<NP>(sCt + t * Cf::RowBC + g * NPT, Cq);
+          step_pairs<NP>(hq, rDT[t], rU[t], Bq, A2p, nIp);
+          f2 s2 = mul2(Cq[0], hq[0]);
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) s = fmaf(Cv[j], h[j], s);
+          for (int q = 1; q < NP; ++q) s2 = fma2(Cq[q], hq[q], s2);
+          float lo, hi;
+          unpack2(s2, lo, hi);
+          hs_store_pairs(t + 1, hq);
+          acc4[t & 3] = lo + hi;
+          if ((t & 3) == 3)
+            *reinterpret_cast<float4*>(sPa + bwd_pidx<N>(prow, t - 3)) =
+                make_float4(acc4[0], acc4[1], acc4[2], acc4[3]);
+        }
+      } else {
+#pragma unroll 4
+        for (int t = 0; t < T; ++t) {
+          float Bv[NPT], Cv[NPT];
+          lds_vec<NPT>(sBt + t * Cf::RowBC + g * NPT, Bv);
+          lds_vec<NPT>(sCt + t * Cf::RowBC + g * NPT, Cv);
+          const float dt = rDT[t], u = rU[t];
+          float s = 0.f;
 #pragma unroll
-        for (int q = 0; q < QN; ++q) sts_vec<VW>(hs_vec(t + 1, q, tid), h + q * VW);
-        acc4[t & 3] = s;
-        if ((t & 3) == 3)
-          *reinterpret_cast<float4*>(sPa + bwd_pidx<N>(prow, t - 3)) =
-              make_float4(acc4[0], acc4[1], acc4[2], acc4[3]);
+          for (int j = 0; j < NPT; ++j) {
+            if (!precise) {
+              const float a = ex2_fast(dt * Aj[j] * kLog2e);
+              const float v = -Bv[j] * u * invA[j];
+              h[j] = fmaf(a, h[j] - v, v);
+            } else {
+              const float x = dt * Aj[j];
+              const float bb = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
+              h[j] = fmaf(expf(x), h[j], bb * (Bv[j] * u));
+            }
+            s = fmaf(Cv[j], h[j], s);
+          }
+#pragma unroll
+          for (int q = 0; q < QN; ++q) sts_vec<VW>(hs_vec(t + 1, q, tid), h + q * VW);
+          acc4[t & 3] = s;
+          if ((t & 3) == 3)
+            *reinterpret_cast<float4*>(sPa + bwd_pidx<N>(prow, t - 3)) =
+                make_float4(acc4[0], acc4[1], acc4[2], acc4[3]);
+        }
       }
     }
     __syncthreads();
 
     // P3: dz (needs s = Σ_g partials + D u), dD; dC reduced over the block's channels
     {
+      float sp_[E];
+#pragma unroll
+      for (int j = 0; j < E; ++j) sp_[j] = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        if constexpr (E % 4 == 0) {
+#pragma unroll
+          for (int kq = 0; kq < E / 4; ++kq) {
+            const float4 v4 = *reinterpret_cast<const float4*>(sPa + bwd_pidx<N>(gg * CH + r, te + 4 * kq));
+            sp_[4 * kq] += v4.x; sp_[4 * kq + 1] += v4.y; sp_[4 * kq + 2] += v4.z; sp_[4 * kq + 3] += v4.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < E; ++j) sp_[j] += sPa[bwd_pidx<N>(gg * CH + r, te + j)];
+        }
+      }
+      const float Dr = sD[r];
 #pragma unroll
       for (int j = 0; j < E; ++j) {
         const int t = te + j;
-        float s = 0.f;
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) s += sPa[bwd_pidx<N>(gg * CH + r, t)];
         const float u = sU[r * Cf::RowF + t];
-        s = fmaf(sD[r], u, s);
+        const float s = fmaf(Dr, u, sp_[j]);
         dD_acc = fmaf(sDS[r * Cf::RowF + t], u, dD_acc);  // zero past the end
-        if (p.z && row_ok && t < tc) {
+        if (p.z) {
           const float zg = zz[j];
           const float sz = precise ? sigmoid_precise(zg) : sigmoid_fast(zg);
-          const float dz = dyv[j] * s * sz * fmaf(zg, 1.f - sz, 1.f);
-          static_cast<IO*>(p.dz)[io_row + t0 + t] = io_traits<IO>::from_f32(dz);
+          sp_[j] = dyv[j] * s * sz * fmaf(zg, 1.f - sz, 1.f);
+        }
+      }
+      if (p.z && row_ok) {
+        IO* dzp = static_cast<IO*>(p.dz) + io_row + t0 + te;
+        bool done = false;
+        if constexpr (E % 4 == 0) {
+          if (vec && te + E <= tc) {
+            vecio<IO, E>::store(dzp, sp_);
+            done = true;
+          }
+        }
+        if (!done) {
+#pragma unroll
+          for (int j = 0; j < E; ++j)
+            if (te + j < tc) dzp[j] = io_traits<IO>::from_f32(sp_[j]);
         }
       }
       // dC[t][n] = Σ_c ds[c][t] h_t[c][n]
-      const int vid = tid / Cf::RS, part = tid % Cf::RS;
-      const int t = vid / (G * QN), gq = vid % (G * QN), gg = gq / QN, q = gq % QN;
       float acc[VW];
 #pragma unroll
       for (int v = 0; v < VW; ++v) acc[v] = 0.f;
+      const float* dsCol = sDS + rt;
 #pragma unroll 4
       for (int i = 0; i < Cf::RCH; ++i) {
-        const int cc = part * Cf::RCH + (i + vid * Cf::RS + part) % Cf::RCH;
-        const float w = sDS[cc * Cf::RowF + t];
+        const int cc = part * Cf::RCH + ((i + vid * Cf::RS + part) & (Cf::RCH - 1));
+        const float w = dsCol[cc * Cf::RowF];
         float hv[VW];
-        lds_vec<VW>(hs_vec(t + 1, q, bwd_lane_of<N>(cc, gg)), hv);
+        lds_vec<VW>(hs_vec(rt + 1, rq, bwd_lane_of<N>(cc, rg)), hv);
 #pragma unroll
         for (int v = 0; v < VW; ++v) acc[v] = fmaf(w, hv[v], acc[v]);
       }
@@ -368,9 +557,10 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       for (int s = Cf::RS / 2; s >= 1; s /= 2)
 #pragma unroll
         for (int v = 0; v < VW; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], s);
-      if (part == 0 && t < tc) {
+      if (part == 0 && rt < tc) {
 #pragma unroll
-        for (int v = 0; v < VW; ++v) wsC_blk[(int64_t)(gg * NPT + q * VW + v) * L + t0 + t] = acc[v];
+        for (int v = 0; v < VW; ++v)
+          wsC_blk[(int64_t)(rg * NPT + rq * VW + v) * L + t0 + rt] = acc[v];
       }
     }
     __syncthreads();
@@ -378,52 +568,91 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     // P4: the adjoint recurrence over the chunk, from its last step to its first
     {
       float pa4[4], pb4[4];
+      if (fast_pairs) {
 #pragma unroll 4
-      for (int t = T - 1; t >= 0; --t) {
-        const float dt = sDT[c * Cf::RowF + t];
-        const float u = sU[c * Cf::RowF + t];
-        const float ds = sDS[c * Cf::RowF + t];
-        const float* Brow = sBt + t * Cf::RowBC + g * NPT;
-        const float* Crow = sCt + t * Cf::RowBC + g * NPT;
-        float hp[NPT], dbv[NPT], Bv[NPT], Cv[NPT];
+        for (int t = T - 1; t >= 0; --t) {
+          const float dt = rDT[t], u = rU[t], ds = rDS[t];
+          const f2 dt2 = pack2(dt, dt), u2 = pack2(u, u), ds2 = pack2(ds, ds);
+          f2 Bq[NP], Cq[NP], hpq[NP], dbq[NP];
+          lds_f2<NP>(sBt + t * Cf::RowBC + g * NPT, Bq);
+          lds_f2<NP>(sCt + t * Cf::RowBC + g * NPT, Cq);
+          hs_load_pairs(t, hpq);
+          f2 du2 = pack2(0.f, 0.f), dd2 = pack2(0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < QN; ++q) lds_vec<VW>(hs_vec(t, q, tid), hp + q * VW);
-        lds_vec<NPT>(Brow, Bv);
-        lds_vec<NPT>(Crow, Cv);
-        float du_p = 0.f, dd_p = 0.f;
-#pragma unroll
-        for (int j = 0; j < NPT; ++j) {
-          const float Bn = Bv[j];
-          lam[j] = fmaf(ds, Cv[j], lam[j]);
-          float a, bb, w;
-          if (!precise) {
-            a = ex2_fast(dt * A2[j]);
-            bb = fmaf(a, invA[j], -invA[j]);       // (Ā - 1) / A
-            w = (dt * a - bb) * invA[j];           // (Δ Ā - B̄) / A
-          } else {
-            const float x = dt * Aj[j];
-            a = expf(x);
-            bb = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
-            w = Aj[j] != 0.f ? (dt * a - bb) * invA[j] : 0.5f * dt * dt;
+          for (int q = 0; q < NP; ++q) {
+            lq[q] = fma2(ds2, Cq[q], lq[q]);
+            float x0, x1;
+            unpack2(mul2(dt2, A2p[q]), x0, x1);
+            const f2 a = pack2(ex2_fast(x0), ex2_fast(x1));
+            const f2 bb = fma2(a, iAp[q], nIp[q]);               // (Ā - 1) / A
+            const f2 da = mul2(dt2, a);                           // Δ Ā
+            const f2 w = mul2(sub2(da, bb), iAp[q]);              // (Δ Ā - B̄) / A
+            const f2 x1v = mul2(lq[q], hpq[q]);
+            const f2 x2v = mul2(lq[q], mul2(Bq[q], u2));
+            const f2 lb = mul2(lq[q], bb);
+            du2 = fma2(lb, Bq[q], du2);
+            dbq[q] = mul2(lb, u2);
+            dd2 = fma2(a, fma2(Ajp[q], x1v, x2v), dd2);
+            dAq[q] = fma2(x2v, w, fma2(x1v, da, dAq[q]));
+            lq[q] = mul2(lq[q], a);
           }
-          const float x1 = lam[j] * hp[j];
-          const float x2 = lam[j] * (Bn * u);
-          const float lb = lam[j] * bb;
-          du_p = fmaf(lb, Bn, du_p);
-          dbv[j] = lb * u;
-          dd_p = fmaf(a, fmaf(Aj[j], x1, x2), dd_p);
-          dAacc[j] = fmaf(x2, w, fmaf(x1, dt * a, dAacc[j]));
-          lam[j] *= a;
+          hs_store_pairs(t + 1, dbq);
+          float lo, hi;
+          unpack2(du2, lo, hi);
+          pa4[t & 3] = lo + hi;
+          unpack2(dd2, lo, hi);
+          pb4[t & 3] = lo + hi;
+          if ((t & 3) == 0) {
+            *reinterpret_cast<float4*>(sPa + bwd_pidx<N>(prow, t)) =
+                make_float4(pa4[0], pa4[1], pa4[2], pa4[3]);
+            *reinterpret_cast<float4*>(sPb + bwd_pidx<N>(prow, t)) =
+                make_float4(pb4[0], pb4[1], pb4[2], pb4[3]);
+          }
         }
+      } else {
+#pragma unroll 4
+        for (int t = T - 1; t >= 0; --t) {
+          const float dt = rDT[t], u = rU[t], ds = rDS[t];
+          float hp[NPT], dbv[NPT], Bv[NPT], Cv[NPT];
 #pragma unroll
-        for (int q = 0; q < QN; ++q) sts_vec<VW>(hs_vec(t + 1, q, tid), dbv + q * VW);
-        pa4[t & 3] = du_p;
-        pb4[t & 3] = dd_p;
-        if ((t & 3) == 0) {
-          *reinterpret_cast<float4*>(sPa + bwd_pidx<N>(prow, t)) =
-              make_float4(pa4[0], pa4[1], pa4[2], pa4[3]);
-          *reinterpret_cast<float4*>(sPb + bwd_pidx<N>(prow, t)) =
-              make_float4(pb4[0], pb4[1], pb4[2], pb4[3]);
+          for (int q = 0; q < QN; ++q) lds_vec<VW>(hs_vec(t, q, tid), hp + q * VW);
+          lds_vec<NPT>(sBt + t * Cf::RowBC + g * NPT, Bv);
+          lds_vec<NPT>(sCt + t * Cf::RowBC + g * NPT, Cv);
+          float du_p = 0.f, dd_p = 0.f;
+#pragma unroll
+          for (int j = 0; j < NPT; ++j) {
+            const float Bn = Bv[j];
+            lam[j] = fmaf(ds, Cv[j], lam[j]);
+            float a, bb, w;
+            if (!precise) {
+              a = ex2_fast(dt * Aj[j] * kLog2e);
+              bb = fmaf(a, invA[j], -invA[j]);
+              w = (dt * a - bb) * invA[j];
+            } else {
+              const float x = dt * Aj[j];
+              a = expf(x);
+              bb = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
+              w = Aj[j] != 0.f ? (dt * a - bb) * invA[j] : 0.5f * dt * dt;
+            }
+            const float x1 = lam[j] * hp[j];
+            const float x2 = lam[j] * (Bn * u);
+            const float lb = lam[j] * bb;
+            du_p = fmaf(lb, Bn, du_p);
+            dbv[j] = lb * u;
+            dd_p = fmaf(a, fmaf(Aj[j], x1, x2), dd_p);
+            dAacc[j] = fmaf(x2, w, fmaf(x1, dt * a, dAacc[j]));
+            lam[j] *= a;
+          }
+#pragma unroll
+          for (int q = 0; q < QN; ++q) sts_vec<VW>(hs_vec(t + 1, q, tid), dbv + q * VW);
+          pa4[t & 3] = du_p;
+          pb4[t & 3] = dd_p;
+          if ((t & 3) == 0) {
+            *reinterpret_cast<float4*>(sPa + bwd_pidx<N>(prow, t)) =
+                make_float4(pa4[0], pa4[1], pa4[2], pa4[3]);
+            *reinterpret_cast<float4*>(sPb + bwd_pidx<N>(prow, t)) =
+                make_float4(pb4[0], pb4[1], pb4[2], pb4[3]);
+          }
         }
       }
     }
@@ -431,33 +660,64 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
 
     // P5: du, dΔraw, dbias; dB reduced over the block's channels
     {
+      float du_[E], dd_[E];
 #pragma unroll
-      for (int j = 0; j < E; ++j) {
-        const int t = te + j;
-        float du = 0.f, dd = 0.f;
+      for (int j = 0; j < E; ++j) du_[j] = dd_[j] = 0.f;
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          du += sPa[bwd_pidx<N>(gg * CH + r, t)];
-          dd += sPb[bwd_pidx<N>(gg * CH + r, t)];
-        }
-        du = fmaf(sDS[r * Cf::RowF + t], sD[r], du);
-        const float dx = dd * sg[j];
-        if (row_ok && t < tc) {
-          static_cast<IO*>(p.du)[io_row + t0 + t] = io_traits<IO>::from_f32(du);
-          static_cast<IO*>(p.ddelta)[io_row + t0 + t] = io_traits<IO>::from_f32(dx);
-          dbias_acc += dx;
+      for (int gg = 0; gg < G; ++gg) {
+        if constexpr (E % 4 == 0) {
+#pragma unroll
+          for (int kq = 0; kq < E / 4; ++kq) {
+            const int ix = bwd_pidx<N>(gg * CH + r, te + 4 * kq);
+            const float4 a4 = *reinterpret_cast<const float4*>(sPa + ix);
+            const float4 b4 = *reinterpret_cast<const float4*>(sPb + ix);
+            du_[4 * kq] += a4.x; du_[4 * kq + 1] += a4.y; du_[4 * kq + 2] += a4.z; du_[4 * kq + 3] += a4.w;
+            dd_[4 * kq] += b4.x; dd_[4 * kq + 1] += b4.y; dd_[4 * kq + 2] += b4.z; dd_[4 * kq + 3] += b4.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < E; ++j) {
+            du_[j] += sPa[bwd_pidx<N>(gg * CH + r, te + j)];
+            dd_[j] += sPb[bwd_pidx<N>(gg * CH + r, te + j)];
+          }
         }
       }
-      const int vid = tid / Cf::RS, part = tid % Cf::RS;
-      const int t = vid / (G * QN), gq = vid % (G * QN), gg = gq / QN, q = gq % QN;
+      const float Dr = sD[r];
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        du_[j] = fmaf(sDS[r * Cf::RowF + te + j], Dr, du_[j]);
+        dd_[j] *= sg[j];
+        if (te + j < tc) dbias_acc += dd_[j];
+      }
+      if (row_ok) {
+        IO* dup = static_cast<IO*>(p.du) + io_row + t0 + te;
+        IO* ddp = static_cast<IO*>(p.ddelta) + io_row + t0 + te;
+        bool done = false;
+        if constexpr (E % 4 == 0) {
+          if (vec && te + E <= tc) {
+            vecio<IO, E>::store(dup, du_);
+            vecio<IO, E>::store(ddp, dd_);
+            done = true;
+          }
+        }
+        if (!done) {
+#pragma unroll
+          for (int j = 0; j < E; ++j) {
+            if (te + j < tc) {
+              dup[j] = io_traits<IO>::from_f32(du_[j]);
+              ddp[j] = io_traits<IO>::from_f32(dd_[j]);
+            }
+          }
+        }
+      }
       float acc[VW];
 #pragma unroll
       for (int v = 0; v < VW; ++v) acc[v] = 0.f;
 #pragma unroll 4
       for (int i = 0; i < Cf::RCH; ++i) {
-        const int cc = part * Cf::RCH + (i + vid * Cf::RS + part) % Cf::RCH;
+        const int cc = part * Cf::RCH + ((i + vid * Cf::RS + part) & (Cf::RCH - 1));
         float hv[VW];
-        lds_vec<VW>(hs_vec(t + 1, q, bwd_lane_of<N>(cc, gg)), hv);
+        lds_vec<VW>(hs_vec(rt + 1, rq, bwd_lane_of<N>(cc, rg)), hv);
 #pragma unroll
         for (int v = 0; v < VW; ++v) acc[v] += hv[v];
       }
@@ -465,15 +725,23 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       for (int s = Cf::RS / 2; s >= 1; s /= 2)
 #pragma unroll
         for (int v = 0; v < VW; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], s);
-      if (part == 0 && t < tc) {
+      if (part == 0 && rt < tc) {
 #pragma unroll
-        for (int v = 0; v < VW; ++v) wsB_blk[(int64_t)(gg * NPT + q * VW + v) * L + t0 + t] = acc[v];
+        for (int v = 0; v < VW; ++v)
+          wsB_blk[(int64_t)(rg * NPT + rq * VW + v) * L + t0 + rt] = acc[v];
       }
     }
     __syncthreads();
   }
 
   // per-channel results
+  if (fast_pairs) {
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      unpack2(lq[q], lam[2 * q], lam[2 * q + 1]);
+      unpack2(dAq[q], dAacc[2 * q], dAacc[2 * q + 1]);
+    }
+  }
   if (chan_ok) {
     const int64_t st = (b * p.dim + d) * N + g * NPT;
 #pragma unroll

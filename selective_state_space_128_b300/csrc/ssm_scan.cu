@@ -112,9 +112,6 @@ template <typename IO, int N> struct ScanSmem {
 // ---------------------------------------------------------------------------
 // TMA and mbarrier primitives (inline PTX)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
@@ -166,12 +163,6 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 // 16-byte shared load into two packed pairs; 8-byte load into one.
-__device__ __forceinline__ void lds_pairs(const void* p, f2& a, f2& b) {
-  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a.r), "=l"(b.r) : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void lds_pair(const void* p, f2& a) {
-  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(a.r) : "r"(smem_u32(p)));
-}
 
 // Index (in floats) of steps 4u..4u+3 of partial row `row` in a P tile: the
 // 16-byte unit is XOR-swizzled so that 8 consecutive rows hit distinct banks.
@@ -184,57 +175,6 @@ struct ScanMaps {
   CUtensorMap u, d, z, b, c;
 };
 
-template <typename IO, int E> struct vecio;
-template <int E> struct vecio<__nv_bfloat16, E> {
-  // E consecutive bf16 -> float (E = 4: 8 bytes, 8: 16 bytes, 16: 32 bytes)
-  __device__ static void load(const __nv_bfloat16* p, float (&v)[E]) {
-    uint32_t w[E / 2];
-    if constexpr (E == 4) {
-      const uint2 q = *reinterpret_cast<const uint2*>(p);
-      w[0] = q.x; w[1] = q.y;
-    } else {
-#pragma unroll
-      for (int k = 0; k < E / 8; ++k) {
-        const uint4 q = reinterpret_cast<const uint4*>(p)[k];
-        w[4 * k] = q.x; w[4 * k + 1] = q.y; w[4 * k + 2] = q.z; w[4 * k + 3] = q.w;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < E / 2; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-  }
-  __device__ static void store(__nv_bfloat16* p, const float (&v)[E]) {
-    uint32_t w[E / 2];
-#pragma unroll
-    for (int i = 0; i < E / 2; ++i) {
-      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-      w[i] = *reinterpret_cast<const uint32_t*>(&h2);
-    }
-    if constexpr (E == 4) {
-      *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < E / 8; ++k)
-        reinterpret_cast<uint4*>(p)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-    }
-  }
-};
-template <int E> struct vecio<float, E> {
-  __device__ static void load(const float* p, float (&v)[E]) {
-#pragma unroll
-    for (int k = 0; k < E / 4; ++k) {
-      const float4 q = reinterpret_cast<const float4*>(p)[k];
-      v[4 * k] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
-    }
-  }
-  __device__ static void store(float* p, const float (&v)[E]) {
-#pragma unroll
-    for (int k = 0; k < E / 4; ++k)
-      reinterpret_cast<float4*>(p)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-  }
-};
 
 // ---------------------------------------------------------------------------
 // Chunk staging
