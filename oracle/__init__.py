@@ -47,6 +47,8 @@ def _load():
                                             i64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                             i64, vp, vp, i32]
         lib.ssm_oracle_scan_bwd.restype = i32
+        lib.ssm_oracle_conv1d.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, i32, vp, vp, i32]
+        lib.ssm_oracle_conv1d.restype = i32
         lib.ssm_oracle_max_threads.restype = i32
         _lib = lib
     return _lib
@@ -231,6 +233,31 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                 dD=r["dD_unit"].reshape(batch, dim).sum(0),
                 dbias=r["dbias_unit"].reshape(batch, dim).sum(0),
                 dinit=r["dinit"].reshape(batch, dim, N), dB=r["dB"], dC=r["dC"])
+
+
+def conv1d(x, weight, bias=None, state_in=None, silu=True, nthreads=0):
+    """Causal depthwise conv1d (+ SiLU) of x (batch, dim, L) (float32 or bfloat16 bits)
+    with weight (dim, K) and bias (dim,); state_in (batch, dim, K-1) float64 or None
+    holds the K-1 inputs before the sequence.  Returns (out (batch, dim, L) float64,
+    state_out (batch, dim, K-1) float64: the last K-1 inputs)."""
+    x = np.ascontiguousarray(x)
+    batch, dim, L = x.shape
+    io = _io(x)
+    w = np.ascontiguousarray(weight, dtype=np.float32)
+    K = w.shape[1]
+    assert w.shape == (dim, K)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    st = None if state_in is None else np.ascontiguousarray(state_in, dtype=np.float64)
+    assert st is None or st.shape == (batch, dim, K - 1)
+    ud = np.ascontiguousarray(np.tile(np.arange(dim, dtype=np.int64), batch))
+    out = np.empty((batch, dim, L))
+    sout = np.empty((batch, dim, max(K - 1, 0)))
+    rc = _load().ssm_oracle_conv1d(batch * dim, L, K, io, _ptr(x), _ptr(ud), _ptr(w), _ptr(b),
+                                   _ptr(st), int(bool(silu)), _ptr(out),
+                                   _ptr(sout) if K > 1 else None, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
+    return out, sout
 
 
 def rel_err(got, ref):

@@ -318,6 +318,58 @@ int ssm_oracle_scan_bwd(int64_t U, int64_t L, int64_t N, int io_bf16, const void
   return failed ? -2 : 0;
 }
 
+/*
+ * Front end of the scan: causal depthwise convolution over time followed by
+ * SiLU.  The summary page's shape table (section 4a, "Conv1d -> SiLU" on
+ * (B, L, ED): local features and a non-linearity ahead of the SSM) and the
+ * configuration-framework page's d_conv = 4 (the kernel width) fix the
+ * operation; per channel d, with width K,
+ *
+ *     v[t]   = bias[d] + Σ_{k=0}^{K-1} w[d, k] · x[t - (K-1) + k]
+ *     out[t] = silu(v[t]) = v[t] σ(v[t])          (or v[t] with silu off)
+ *
+ * where x[t] for t < 0 comes from the carried state (the K-1 inputs before
+ * the sequence; zeros when absent).  The new state is the last K-1 inputs of
+ * the extended sequence (state, x).
+ */
+int ssm_oracle_conv1d(int64_t U, int64_t L, int64_t K, int io_bf16, const void* x,
+                      const int64_t* unit_d, const float* w, const float* bias,
+                      const double* state_in, int silu_on, double* out, double* state_out,
+                      int nthreads) {
+  if (K < 1 || K > 64 || L < 0 || U < 0) return -1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < U; ++i) {
+    const int64_t d = unit_d[i];
+    /* xe[j] = x[j - (K-1)] for j >= K-1, the state for j < K-1 */
+    for (int64_t t = 0; t < L; ++t) {
+      double v = bias ? (double)bias[d] : 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const int64_t s = t - (K - 1) + k;  /* input time */
+        double xv;
+        if (s >= 0) xv = in_val(x, io_bf16, i * L + s);
+        else xv = state_in ? state_in[i * (K - 1) + (K - 1 + s)] : 0.0;
+        v += (double)w[d * K + k] * xv;
+      }
+      out[i * L + t] = silu_on ? v / (1.0 + exp(-v)) : v;
+    }
+    if (state_out) {
+      for (int64_t j = 0; j < K - 1; ++j) {
+        const int64_t s = L - (K - 1) + j;  /* input time of state slot j */
+        double xv;
+        if (s >= 0) xv = in_val(x, io_bf16, i * L + s);
+        else xv = state_in ? state_in[i * (K - 1) + (K - 1 + s)] : 0.0;
+        state_out[i * (K - 1) + j] = xv;
+      }
+    }
+  }
+  return 0;
+}
+
 /* Threads OpenMP will use (the CPU baseline reports it). */
 int ssm_oracle_max_threads(void) {
 #ifdef _OPENMP

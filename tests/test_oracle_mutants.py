@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 import test_oracle_bwd_pins as bwd_pins
+import test_oracle_conv_pins as conv_pins
 import test_oracle_pins as pins
 
 MUTANTS = {
@@ -51,6 +52,19 @@ BWD_MUTANTS = {
 }
 
 
+# mistakes in the front end (causal conv1d + SiLU)
+CONV_MUTANTS = {
+    "conv_anticausal": ("const int64_t s = t - (K - 1) + k;  /* input time */",
+                        "const int64_t s = t + k;  /* input time */"),
+    "conv_kernel_flipped": ("v += (double)w[d * K + k] * xv;", "v += (double)w[d * K + (K - 1 - k)] * xv;"),
+    "conv_bias_dropped": ("double v = bias ? (double)bias[d] : 0.0;", "double v = 0.0;"),
+    "conv_silu_sign": ("v / (1.0 + exp(-v))", "v / (1.0 + exp(v))"),
+    "conv_state_ignored": ("else xv = state_in ? state_in[i * (K - 1) + (K - 1 + s)] : 0.0;\n        v +=",
+                           "else xv = 0.0;\n        v +="),
+    "conv_state_out_shift": ("const int64_t s = L - (K - 1) + j;", "const int64_t s = L - K + j;"),
+}
+
+
 def _pin_calls(module=pins):
     calls = []
     for name, fn in inspect.getmembers(module, inspect.isfunction):
@@ -69,22 +83,23 @@ def _pin_calls(module=pins):
 
 def _run_mutant(old, new, tmp_path, monkeypatch, module, part):
     """Plant `old` -> `new` in one part of the oracle source: "fwd" (the scan and
-    the decode step) or "bwd" (the derivatives, from the sigmoid helper on)."""
+    the decode step), "bwd" (the derivatives, from the sigmoid helper on) or
+    "conv" (the front end)."""
     src = open(oracle._SRC).read()
-    cut = src.index("static double sigmoid(")
-    head, tail = src[:cut], src[cut:]
-    region = head if part == "fwd" else tail
+    c1 = src.index("static double sigmoid(")
+    c2 = src.index("/*\n * Front end of the scan")
+    bounds = {"fwd": (0, c1), "bwd": (c1, c2), "conv": (c2, len(src))}[part]
+    region = src[bounds[0]:bounds[1]]
     assert region.count(old) == 1, "mutation site not found: " + old
-    region = region.replace(old, new)
     path = os.path.join(tmp_path, "mutant.c")
     with open(path, "w") as f:
-        f.write(region + tail if part == "fwd" else head + region)
+        f.write(src[:bounds[0]] + region.replace(old, new) + src[bounds[1]:])
     so = os.path.join(tmp_path, "libmutant.so")
     subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-o", so, path, "-lm"])
     real = oracle._load()
     lib = ctypes.CDLL(so)
     for fname in ("ssm_oracle_scan", "ssm_oracle_step", "ssm_oracle_scan_bwd",
-                  "ssm_oracle_max_threads"):
+                  "ssm_oracle_conv1d", "ssm_oracle_max_threads"):
         getattr(lib, fname).argtypes = getattr(real, fname).argtypes
         getattr(lib, fname).restype = getattr(real, fname).restype
     monkeypatch.setattr(oracle, "_lib", lib)
@@ -111,3 +126,9 @@ def test_backward_pins_catch_planted_mistake(mutant, tmp_path, monkeypatch):
     still see the true forward."""
     old, new = BWD_MUTANTS[mutant]
     assert _run_mutant(old, new, tmp_path, monkeypatch, bwd_pins, "bwd"), "no pin caught " + mutant
+
+
+@pytest.mark.parametrize("mutant", sorted(CONV_MUTANTS))
+def test_conv_pins_catch_planted_mistake(mutant, tmp_path, monkeypatch):
+    old, new = CONV_MUTANTS[mutant]
+    assert _run_mutant(old, new, tmp_path, monkeypatch, conv_pins, "conv"), "no pin caught " + mutant
