@@ -283,6 +283,40 @@ def bench_scan(w, steps, warmup, world):
 
 
 # ---------------------------------------------------------------------------
+# front end: causal conv1d (d_conv 4) + SiLU over the same layer's input
+# ---------------------------------------------------------------------------
+
+def bench_conv(w, steps, warmup, world, width=4, copies=3):
+    """Per-launch time of ssm_conv1d_fwd on (batch, d_inner, L) bf16 input with a
+    (d_inner, 4) kernel; `copies` input/output pairs (100 MB each) are rotated so
+    the working set (300 MB) is larger than L2.  Seeded inputs drawn on the device."""
+    import torch
+    import selective_state_space_128_b300 as ssm
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(w.seed + 2000)
+    shape = (w.batch, w.dim, w.seqlen)
+    xs = [torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16) for _ in range(copies)]
+    outs = [torch.empty_like(xs[0]) for _ in range(copies)]
+    wt = 0.5 * torch.randn((w.dim, width), generator=gen, device="cuda")
+    bias = 0.2 * torch.randn(w.dim, generator=gen, device="cuda")
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        ssm.ssm_conv1d_fwd(xs[i % copies], wt, bias, None, True, outs[i % copies], None, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        ssm.ssm_conv1d_fwd(xs[i % copies], wt, bias, None, True, outs[i % copies], None, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / steps
+    nbytes = 2 * xs[0].numel() * 2 + wt.numel() * 4 + bias.numel() * 4
+    return dict(step_ms=ms, steps=steps, bytes=nbytes)
+
+
+# ---------------------------------------------------------------------------
 # backward pass on the same layer
 # ---------------------------------------------------------------------------
 
@@ -477,6 +511,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--bwd-steps", type=int, default=20)
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-conv", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = synth.MAMBA_130M
@@ -495,6 +530,7 @@ def main():
     bwd = None if args.no_bwd else bench_backward(w, r["inputs"], args.bwd_steps, args.warmup,
                                                   world)
     r.pop("inputs")
+    conv = None if args.no_conv else bench_conv(w, 50, args.warmup, world)
     dec = None if args.no_decode else bench_decode(synth.DECODE, args.decode_steps, world)
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
@@ -554,6 +590,15 @@ def main():
                             "gpu_launches": 2 * bwd["steps"],
                             "l2": "u, delta, z, dy: 4 x %.0f MB, larger than L2"
                                   % (w.channel_steps * 2 / 1e6)}
+    if conv is not None:
+        cs = conv["step_ms"] / 1e3
+        line["conv1d"] = {"workload": "conv1d_silu d_conv 4 on %d x %d x %d bf16" % (
+                              w.batch, w.dim, w.seqlen),
+                          "steps": conv["steps"], "us_per_step": conv["step_ms"] * 1e3,
+                          "hbm_gbs": conv["bytes"] / cs / 1e9,
+                          "hbm_frac": conv["bytes"] / cs / 1e9 / hbm_peak,
+                          "bytes_per_step": conv["bytes"], "gpu_launches": conv["steps"],
+                          "l2": "3 input/output pairs rotated: 300 MB, larger than L2"}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line))

@@ -245,6 +245,42 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
                  int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Front end of the scan: causal depthwise conv1d followed by SiLU.  The
+ * summary page's shape table (section 4a) puts "Conv1d -> SiLU" on the
+ * (B, L, ED) path right before the SSM (its output is the scan's u); the
+ * configuration page ("2. Mamba 상세") gives the kernel width d_conv = 4.
+ * Per channel d with width K = `width` (1..4):
+ *
+ *     out[b,d,t] = silu(bias[d] + Σ_{k<K} weight[d,k] · x[b,d,t-(K-1)+k])
+ *
+ * (or the bare sum with silu = 0).  x[t < 0] comes from conv_state_in, the
+ * K-1 inputs before the sequence (NULL = zeros); conv_state_out (nullable)
+ * receives the last K-1 inputs of (conv_state_in, x), so a sequence split
+ * over calls gives the same outputs as one call.  conv_state_out may be
+ * conv_state_in itself (updated in place); no other overlap is allowed.
+ *
+ * Layouts: x, out (batch, dim, seqlen) io_dtype; weight (dim, width) float32;
+ * bias (dim) float32, nullable; conv states (batch, dim, width-1) io_dtype.
+ * Arithmetic in fp32; bf16 outputs rounded to nearest even.  Errors as the
+ * scan (SSM_ERR_UNSUPPORTED for width outside 1..4).  Asynchronous on stream.
+ */
+int ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
+                   const void* conv_state_in, int silu, void* out, void* conv_state_out,
+                   int64_t batch, int64_t dim, int64_t seqlen, int64_t width, int io_dtype,
+                   void* stream);
+
+/*
+ * One token of the front end on a rolling state (decode): for every (b, d),
+ * window = (conv_state[b,d,0..K-2], x[b,d]); out[b,d] = silu(bias[d] +
+ * Σ_k weight[d,k] window[k]); conv_state[b,d] <- window[1..K-1] (in place).
+ * x, out (batch, dim) io_dtype; conv_state (batch, dim, width-1) io_dtype
+ * (required when width > 1).  Errors and execution as ssm_conv1d_fwd.
+ */
+int ssm_conv1d_update(void* conv_state, const void* x, const float* weight, const float* bias,
+                      int silu, void* out, int64_t batch, int64_t dim, int64_t width,
+                      int io_dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

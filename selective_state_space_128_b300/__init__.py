@@ -65,6 +65,10 @@ def load():
     lib.ssm_scan_bwd_workspace_bytes.restype = sz
     lib.ssm_scan_bwd.argtypes = [vp] * 8 + [i32] + [vp] * 12 + [i64, i64, i64, i64, i32, vp, sz, vp]
     lib.ssm_scan_bwd.restype = i32
+    lib.ssm_conv1d_fwd.argtypes = [vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, i64, i32, vp]
+    lib.ssm_conv1d_fwd.restype = i32
+    lib.ssm_conv1d_update.argtypes = [vp, vp, vp, vp, i32, vp, i64, i64, i64, i32, vp]
+    lib.ssm_conv1d_update.restype = i32
     _lib = lib
     return lib
 
@@ -226,6 +230,26 @@ def ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, init_state
     _call("ssm_scan_bwd", rc)
 
 
+def ssm_conv1d_fwd(x, weight, bias, conv_state_in, silu, out, conv_state_out, stream=None):
+    """Tensor form of ``ssm_conv1d_fwd``: x (batch, dim, L), weight (dim, width)."""
+    _check_dev(x, weight, bias, conv_state_in, out, conv_state_out)
+    batch, dim, L = x.shape
+    rc = load().ssm_conv1d_fwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state_in),
+                               int(bool(silu)), _ptr(out), _ptr(conv_state_out), batch, dim, L,
+                               weight.shape[1], _io_dtype(x), _stream(stream))
+    _call("ssm_conv1d_fwd", rc)
+
+
+def ssm_conv1d_update(conv_state, x, weight, bias, silu, out, stream=None):
+    """Tensor form of ``ssm_conv1d_update``: x (batch, dim), conv_state (batch, dim, width-1)."""
+    _check_dev(conv_state, x, weight, bias, out)
+    batch, dim = x.shape
+    rc = load().ssm_conv1d_update(_ptr(conv_state), _ptr(x), _ptr(weight), _ptr(bias),
+                                  int(bool(silu)), _ptr(out), batch, dim, weight.shape[1],
+                                  _io_dtype(x), _stream(stream))
+    _call("ssm_conv1d_update", rc)
+
+
 def static_scratch_bytes() -> int:
     """SSM_STATIC_SCRATCH_BYTES as defined in include/ssm.h."""
     import re
@@ -279,6 +303,18 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                  d_final_state, out["du"], out["ddelta"], out["dA"], out["dB"], out["dC"],
                  out["dD"], out["dz"], out["dbias"], out["dinit"], ws, nbytes, stream)
     return out
+
+
+def conv1d(x, weight, bias=None, conv_state=None, silu=True, want_state=False, stream=None):
+    """out[, new_state] = conv1d(...): causal depthwise conv1d (+ SiLU) of x (batch, dim, L);
+    conv_state (batch, dim, width-1) holds the inputs before the sequence."""
+    import torch
+    out = torch.empty_like(x)
+    st = None
+    if want_state:
+        st = torch.empty(x.shape[:2] + (weight.shape[1] - 1,), dtype=x.dtype, device=x.device)
+    ssm_conv1d_fwd(x, weight, bias, conv_state, silu, out, st, stream)
+    return (out, st) if want_state else out
 
 
 def exported_names():

@@ -258,4 +258,71 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+int ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
+                   const void* conv_state_in, int silu, void* out, void* conv_state_out,
+                   int64_t batch, int64_t dim, int64_t seqlen, int64_t width, int io_dtype,
+                   void* stream) {
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!sizes_ok(batch, dim, seqlen) || width <= 0) return SSM_ERR_ARG;
+  if (width > 4) return SSM_ERR_UNSUPPORTED;
+  const bool rows = batch > 0 && dim > 0;
+  if (rows && seqlen > 0 && (!x || !weight || !out)) return SSM_ERR_ARG;
+  if (rows && conv_state_out && !weight) return SSM_ERR_ARG;
+  const void* ptrs[] = {x, weight, bias, conv_state_in, out, conv_state_out};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
+  const size_t nio = (size_t)batch * (size_t)dim * (size_t)seqlen * esz;
+  const size_t nst = (size_t)batch * (size_t)dim * (size_t)(width - 1) * esz;
+  const size_t nw = (size_t)dim * (size_t)width * 4, nb = (size_t)dim * 4;
+  if (overlaps(out, nio, x, nio) || overlaps(out, nio, weight, nw) || overlaps(out, nio, bias, nb) ||
+      overlaps(out, nio, conv_state_in, nst) || overlaps(out, nio, conv_state_out, nst))
+    return SSM_ERR_ARG;
+  if (conv_state_out && (overlaps(conv_state_out, nst, x, nio) ||
+                         overlaps(conv_state_out, nst, weight, nw) ||
+                         overlaps(conv_state_out, nst, bias, nb) ||
+                         (conv_state_out != conv_state_in &&
+                          overlaps(conv_state_out, nst, conv_state_in, nst))))
+    return SSM_ERR_ARG;
+  if (!rows) return SSM_OK;
+  ssm::ConvArgs a{};
+  a.x = x; a.w = weight; a.bias = bias; a.state_in = conv_state_in; a.out = out;
+  a.state_out = width > 1 ? conv_state_out : nullptr;
+  a.batch = batch; a.dim = dim; a.L = seqlen;
+  a.silu = silu != 0;
+  a.precise = io_dtype == SSM_F32;
+  const cudaError_t e = ssm::conv_launch(a, width, io_dtype, false, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+int ssm_conv1d_update(void* conv_state, const void* x, const float* weight, const float* bias,
+                      int silu, void* out, int64_t batch, int64_t dim, int64_t width,
+                      int io_dtype, void* stream) {
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!sizes_ok(batch, dim, 1) || width <= 0) return SSM_ERR_ARG;
+  if (width > 4) return SSM_ERR_UNSUPPORTED;
+  const bool rows = batch > 0 && dim > 0;
+  if (rows && (!x || !weight || !out || (width > 1 && !conv_state))) return SSM_ERR_ARG;
+  const void* ptrs[] = {conv_state, x, weight, bias, out};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
+  const size_t nio = (size_t)batch * (size_t)dim * esz;
+  const size_t nst = (size_t)batch * (size_t)dim * (size_t)(width - 1) * esz;
+  const size_t nw = (size_t)dim * (size_t)width * 4, nb = (size_t)dim * 4;
+  if (overlaps(out, nio, x, nio) || overlaps(out, nio, conv_state, nst) ||
+      overlaps(out, nio, weight, nw) || overlaps(out, nio, bias, nb) ||
+      overlaps(conv_state, nst, x, nio) || overlaps(conv_state, nst, weight, nw) ||
+      overlaps(conv_state, nst, bias, nb))
+    return SSM_ERR_ARG;
+  if (!rows) return SSM_OK;
+  ssm::ConvArgs a{};
+  a.x = x; a.w = weight; a.bias = bias; a.out = out; a.state_out = conv_state;
+  a.batch = batch; a.dim = dim; a.L = 1;
+  a.silu = silu != 0;
+  a.precise = io_dtype == SSM_F32;
+  const cudaError_t e = ssm::conv_launch(a, width, io_dtype, true, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -121,4 +121,23 @@ BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t L, int64_t N);
 // Enqueue the backward pass (two kernels).
 cudaError_t bwd_launch(const BwdArgs& a, int64_t N, int io_dtype, cudaStream_t stream);
 
+// Arguments of the conv1d + SiLU front end (device pointers; layouts as in
+// include/ssm.h).  For the one-token update, state_out is the in/out state.
+struct ConvArgs {
+  const void* x;
+  const float* w;
+  const float* bias;
+  const void* state_in;
+  void* out;
+  void* state_out;
+  int64_t batch, dim, L;
+  bool silu;
+  bool precise;
+};
+
+// Enqueue the conv pass (update = false: over a sequence, then the new state)
+// or the one-token update on the rolling state.
+cudaError_t conv_launch(const ConvArgs& a, int64_t width, int io_dtype, bool update,
+                        cudaStream_t stream);
+
 }  // namespace ssm

@@ -160,3 +160,27 @@ def test_backward_workspace_size():
     assert ckpt + parts <= need <= ckpt + parts + 8 * 1536 * 18 * 4 + 6 * 256
     assert ssm.ssm_scan_bwd_workspace_bytes(0, 1536, 2048, 16) == 0
     assert ssm.ssm_scan_bwd_workspace_bytes(8, 1536, 2048, 3) == 0
+
+
+def test_conv_argument_errors():
+    L_ = lib()
+    ok = dict(x=FAKE, w=FAKE + 0x1000000, b=None, sin=None, silu=1, out=FAKE + 0x2000000,
+              sout=None, batch=2, dim=8, L=64, K=4, io=ssm.SSM_BF16)
+
+    def fwd(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return L_.ssm_conv1d_fwd(a["x"], a["w"], a["b"], a["sin"], a["silu"], a["out"], a["sout"],
+                                 a["batch"], a["dim"], a["L"], a["K"], a["io"], None)
+
+    assert fwd(x=None) == ssm.SSM_ERR_ARG
+    assert fwd(K=5) == ssm.SSM_ERR_UNSUPPORTED
+    assert fwd(K=0) == ssm.SSM_ERR_ARG
+    assert fwd(out=FAKE + 0x2000004) == ssm.SSM_ERR_ALIGN
+    assert fwd(out=FAKE + 0x100) == ssm.SSM_ERR_ARG                       # out over x
+    assert fwd(sin=FAKE + 0x3000000, sout=FAKE + 0x3000010) == ssm.SSM_ERR_ARG  # partial overlap
+    assert fwd(batch=0) == ssm.SSM_OK
+    assert L_.ssm_conv1d_update(None, FAKE, FAKE + 0x1000000, None, 1, FAKE + 0x2000000, 2, 8, 4,
+                                ssm.SSM_BF16, None) == ssm.SSM_ERR_ARG    # state required
+    assert L_.ssm_conv1d_update(FAKE + 0x3000000, FAKE, FAKE + 0x1000000, None, 1,
+                                FAKE + 0x3000010, 2, 8, 4, ssm.SSM_BF16, None) == ssm.SSM_ERR_ARG
