@@ -62,6 +62,11 @@ def _ptr(a):
     return None if a is None else a.ctypes.data
 
 
+def _mode(delta_softplus, euler):
+    """The oracle's mode bits: 1 = softplus on Δ, 2 = Euler B̄ = Δ B."""
+    return int(bool(delta_softplus)) | (2 if euler else 0)
+
+
 def _io(arr):
     if arr.dtype == np.uint16:
         return 1
@@ -71,7 +76,7 @@ def _io(arr):
 
 
 def scan_rows(u, delta, z, unit_b, unit_d, A, B, C, D=None, delta_bias=None,
-              delta_softplus=True, init_state=None, y_stride=1, nthreads=0):
+              delta_softplus=True, init_state=None, y_stride=1, nthreads=0, euler=False):
     """Scan U units given as rows.
 
     u, delta, z: (U, L) float32 or uint16 (bfloat16 bits); z may be None.
@@ -110,7 +115,7 @@ def scan_rows(u, delta, z, unit_b, unit_d, A, B, C, D=None, delta_bias=None,
     hN = np.empty((U, N), dtype=np.float64)
     rc = _load().ssm_oracle_scan(U, L, N, io, _ptr(u), _ptr(delta), _ptr(z), _ptr(ub), _ptr(ud),
                                  _ptr(bias), _ptr(A), _ptr(B), _ptr(C), B.shape[2], _ptr(D),
-                                 int(bool(delta_softplus)), _ptr(h0), int(y_stride), _ptr(y),
+                                 _mode(delta_softplus, euler), _ptr(h0), int(y_stride), _ptr(y),
                                  _ptr(hN), int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
@@ -118,7 +123,7 @@ def scan_rows(u, delta, z, unit_b, unit_d, A, B, C, D=None, delta_bias=None,
 
 
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-         init_state=None, nthreads=0):
+         init_state=None, nthreads=0, euler=False):
     """Full scan of (batch, dim, L) inputs.  Returns y (batch, dim, L) and
     final_state (batch, dim, N), both float64."""
     batch, dim, L = u.shape
@@ -127,12 +132,12 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True
     h0 = None if init_state is None else np.asarray(init_state, np.float64).reshape(batch * dim, N)
     y, hN = scan_rows(u.reshape(batch * dim, L), delta.reshape(batch * dim, L),
                       None if z is None else z.reshape(batch * dim, L), bb.ravel(), dd.ravel(),
-                      A, B, C, D, delta_bias, delta_softplus, h0, 1, nthreads)
+                      A, B, C, D, delta_bias, delta_softplus, h0, 1, nthreads, euler)
     return y.reshape(batch, dim, L), hN.reshape(batch, dim, N)
 
 
 def step(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-         nthreads=0):
+         nthreads=0, euler=False):
     """One decode step on (batch, dim, N) float64 state (returned updated, not
     modified in place) with u, delta, z of shape (batch, dim) and B, C of shape
     (batch, N).  Returns (y (batch, dim) float64, new_state)."""
@@ -154,14 +159,14 @@ def step(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softpl
     bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, dtype=np.float32)
     rc = _load().ssm_oracle_step(batch * dim, N, io, _ptr(u_), _ptr(dl), _ptr(zz), _ptr(ub),
                                  _ptr(ud), _ptr(bias), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                                 int(bool(delta_softplus)), _ptr(st), _ptr(y), int(nthreads))
+                                 _mode(delta_softplus, euler), _ptr(st), _ptr(y), int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
     return y.reshape(batch, dim), st.reshape(batch, dim, N)
 
 
 def scan_bwd_rows(u, delta, z, unit_b, unit_d, A, B, C, D, delta_bias, delta_softplus,
-                  dy, init_state=None, d_final_state=None, nbatch=None, nthreads=0):
+                  dy, init_state=None, d_final_state=None, nbatch=None, nthreads=0, euler=False):
     """Backward of ``scan_rows`` for U units given as rows (same conventions; every
     row spans the whole time axis, L = u.shape[1]).
 
@@ -202,7 +207,7 @@ def scan_bwd_rows(u, delta, z, unit_b, unit_d, A, B, C, D, delta_bias, delta_sof
                dinit=np.empty((U, N)), dB=np.empty((nbatch, N, L)), dC=np.empty((nbatch, N, L)))
     rc = _load().ssm_oracle_scan_bwd(
         U, L, N, io, _ptr(u), _ptr(delta), _ptr(z), _ptr(ub), _ptr(ud), _ptr(bias), _ptr(A),
-        _ptr(B), _ptr(C), B.shape[2], _ptr(D), int(bool(delta_softplus)), _ptr(h0), _ptr(dy),
+        _ptr(B), _ptr(C), B.shape[2], _ptr(D), _mode(delta_softplus, euler), _ptr(h0), _ptr(dy),
         _ptr(dfin), _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dz"]), _ptr(out["dA_unit"]),
         _ptr(out["dD_unit"]), _ptr(out["dbias_unit"]), _ptr(out["dinit"]), nbatch,
         _ptr(out["dB"]), _ptr(out["dC"]), int(nthreads))
@@ -212,7 +217,7 @@ def scan_bwd_rows(u, delta, z, unit_b, unit_d, A, B, C, D, delta_bias, delta_sof
 
 
 def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-             init_state=None, dy=None, d_final_state=None, nthreads=0):
+             init_state=None, dy=None, d_final_state=None, nthreads=0, euler=False):
     """Backward of ``scan`` for (batch, dim, L) inputs: the derivatives of
     Σ y·dy + Σ final_state·d_final_state.  Returns float64 arrays du, ddelta,
     dz (batch, dim, L), dA (dim, N), dB, dC (batch, N, L), dD, dbias (dim,) and
@@ -226,7 +231,7 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                       delta_bias, delta_softplus, np.asarray(dy, np.float64).reshape(U, L),
                       None if init_state is None else np.asarray(init_state).reshape(U, N),
                       None if d_final_state is None else np.asarray(d_final_state).reshape(U, N),
-                      batch, nthreads)
+                      batch, nthreads, euler)
     return dict(du=r["du"].reshape(batch, dim, L), ddelta=r["ddelta"].reshape(batch, dim, L),
                 dz=None if z is None else r["dz"].reshape(batch, dim, L),
                 dA=r["dA_unit"].reshape(batch, dim, N).sum(0),

@@ -21,6 +21,10 @@
  *   Gate (summary page, section 4a shape table, "SSM output × SiLU(gate)"):
  *       y_t <- y_t * z_t * sigmoid(z_t)       (z absent = no gate)
  *
+ * Variant (the `mode` bit 2, "Euler"): B̄ = Δ B_{n,t}, the first-order form the
+ * summary page gives beside equation (4) as the small-Δ limit of the ZOH.
+ * The `mode` argument of every entry point: bit 1 = softplus on Δ, bit 2 = Euler.
+ *
  * Readings where the pages leave a step open: h_{-1} = 0 unless an initial
  * state is given; y_t reads the state after the update at t; D sits inside
  * the gate; Δ_raw + bias with softplus off is used as Δ directly.
@@ -54,8 +58,9 @@ static double softplus(double x) {
 static void scan_unit(int64_t L, int64_t N, int bf16,
                       const void* u, const void* delta, const void* z, int64_t row,
                       double bias, const float* A_row, const float* B_b, const float* C_b,
-                      int64_t bc_ld, double Dd, int softplus_on,
+                      int64_t bc_ld, double Dd, int mode,
                       const double* h0, int64_t y_stride, double* y_row, double* h_out) {
+  const int softplus_on = mode & 1, euler = (mode & 2) != 0;
   double h[512];
   for (int64_t n = 0; n < N; ++n) h[n] = h0 ? h0[n] : 0.0;
   for (int64_t t = 0; t < L; ++t) {
@@ -67,7 +72,7 @@ static void scan_unit(int64_t L, int64_t N, int bf16,
       double An = (double)A_row[n];
       double dA = dt * An;
       double abar = exp(dA);
-      double bbar = (An != 0.0) ? expm1(dA) / An : dt;   /* times B below */
+      double bbar = euler ? dt : ((An != 0.0) ? expm1(dA) / An : dt);   /* times B below */
       h[n] = abar * h[n] + bbar * (double)B_b[n * bc_ld + t] * ut;
       acc += (double)C_b[n * bc_ld + t] * h[n];
     }
@@ -164,7 +169,7 @@ int ssm_oracle_step(int64_t U, int64_t N, int io_bf16, const void* u, const void
  *   dB_{t,n} += λ_{t,n} B̄_{t,n} u_t           (summed over the channels of a batch)
  *   dC_{t,n} += ds_t h_{t,n}                  (summed over the channels of a batch)
  *   dΔ_t    = Σ_n λ_{t,n} (h_{t-1,n} A_n Ā_{t,n} + B_{t,n} u_t Ā_{t,n})
- *             [dĀ/dΔ = A Ā, d(expm1(ΔA)/A)/dΔ = Ā]
+ *             [dĀ/dΔ = A Ā, d(expm1(ΔA)/A)/dΔ = Ā; Euler B̄ = Δ: 1 and 0]
  *   dA_n   += λ_{t,n} (h_{t-1,n} Δ_t Ā_{t,n} + B_{t,n} u_t (Δ_t Ā_{t,n} - B̄_{t,n}) / A_n)
  *             [A_n = 0: the limit Δ_t^2 / 2 for the second factor]
  *   dΔraw_t = dΔ_t σ(Δraw_t + bias) with softplus, else dΔ_t;  dbias += dΔraw_t
@@ -180,11 +185,12 @@ static double sigmoid(double x) {
 static void scan_bwd_unit(int64_t L, int64_t N, int bf16, const void* u, const void* delta,
                           const void* z, int64_t row, double bias, const float* A_row,
                           const float* B_b, const float* C_b, int64_t bc_ld, double Dd,
-                          int softplus_on, const double* h0, const double* dy_row,
+                          int mode, const double* h0, const double* dy_row,
                           const double* dfinal, double* du_row, double* ddelta_row,
                           double* dz_row, double* dA_out, double* dD_out, double* dbias_out,
                           double* dinit_out, double* dB_b, double* dC_b, double* hs,
                           double* dts, double* xs, double* ss) {
+  const int softplus_on = mode & 1, euler = (mode & 2) != 0;
   /* forward, keeping every state h_t (hs[t*N + n]), Δ_t, Δraw_t + bias and s_t */
   for (int64_t t = 0; t < L; ++t) {
     double ut = in_val(u, bf16, row * L + t);
@@ -195,7 +201,7 @@ static void scan_bwd_unit(int64_t L, int64_t N, int bf16, const void* u, const v
       double An = (double)A_row[n];
       double prev = t > 0 ? hs[(t - 1) * N + n] : (h0 ? h0[n] : 0.0);
       double abar = exp(dt * An);
-      double bbar = (An != 0.0) ? expm1(dt * An) / An : dt;
+      double bbar = euler ? dt : ((An != 0.0) ? expm1(dt * An) / An : dt);
       double h = abar * prev + bbar * (double)B_b[n * bc_ld + t] * ut;
       hs[t * N + n] = h;
       acc += (double)C_b[n * bc_ld + t] * h;
@@ -231,13 +237,15 @@ static void scan_bwd_unit(int64_t L, int64_t N, int bf16, const void* u, const v
       double Cn = (double)C_b[n * bc_ld + t];
       double prev = t > 0 ? hs[(t - 1) * N + n] : (h0 ? h0[n] : 0.0);
       double abar = exp(dt * An);
-      double bbar = (An != 0.0) ? expm1(dt * An) / An : dt;
-      double dbbar_dA = (An != 0.0) ? (dt * abar - bbar) / An : 0.5 * dt * dt;
+      double bbar = euler ? dt : ((An != 0.0) ? expm1(dt * An) / An : dt);
+      /* d B̄/dA and d B̄/dΔ: ZOH (A = 0: the limit), Euler: 0 and 1 */
+      double dbbar_dA = euler ? 0.0 : ((An != 0.0) ? (dt * abar - bbar) / An : 0.5 * dt * dt);
+      double dbbar_ddt = euler ? 1.0 : abar;
       lam[n] += ds * Cn;
       dC_b[n * L + t] += ds * hs[t * N + n];
       dB_b[n * L + t] += lam[n] * bbar * ut;
       du += lam[n] * bbar * Bn;
-      ddt += lam[n] * (prev * An * abar + Bn * ut * abar);
+      ddt += lam[n] * (prev * An * abar + Bn * ut * dbbar_ddt);
       dA_out[n] += lam[n] * (prev * dt * abar + Bn * ut * dbbar_dA);
       lam[n] *= abar;
     }

@@ -46,13 +46,13 @@ def _problem(seed, batch=2, dim=3, L=19, N=3, softplus=True, with_z=True, zero_a
     return x, dy, dfin
 
 
-def _loss(x, dy, dfin, softplus):
+def _loss(x, dy, dfin, softplus, euler=False):
     y, hN = oracle.scan(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["bias"],
-                        softplus, x["h0"])
+                        softplus, x["h0"], euler=euler)
     return float(np.sum(y * dy) + np.sum(hN * dfin))
 
 
-def _fd(x, dy, dfin, softplus, name, step=2.0 ** -11):
+def _fd(x, dy, dfin, softplus, name, step=2.0 ** -11, euler=False):
     """Central differences of the loss over every element of input `name`, dividing by
     the difference of the values actually fed (float32 inputs round)."""
     base = x[name]
@@ -64,37 +64,39 @@ def _fd(x, dy, dfin, softplus, name, step=2.0 ** -11):
         arr[idx] = v0 + step
         hi = float(arr[idx])
         xp[name] = arr
-        lp = _loss(xp, dy, dfin, softplus)
+        lp = _loss(xp, dy, dfin, softplus, euler)
         arr = base.copy()
         arr[idx] = v0 - step
         lo = float(arr[idx])
         xp[name] = arr
-        lm = _loss(xp, dy, dfin, softplus)
+        lm = _loss(xp, dy, dfin, softplus, euler)
         g[idx] = (lp - lm) / (hi - lo)
     return g
 
 
-def _grads(x, dy, dfin, softplus):
+def _grads(x, dy, dfin, softplus, euler=False):
     return oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["bias"],
-                           softplus, x["h0"], dy, dfin)
+                           softplus, x["h0"], dy, dfin, euler=euler)
 
 
 NAMES = {"u": "du", "delta": "ddelta", "z": "dz", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
          "bias": "dbias", "h0": "dinit"}
 
 
-@pytest.mark.parametrize("case", ["softplus_gate", "no_softplus_no_gate", "zero_A"])
+@pytest.mark.parametrize("case", ["softplus_gate", "no_softplus_no_gate", "zero_A", "euler"])
 def test_gradients_match_finite_differences(case):
     softplus = case != "no_softplus_no_gate"
-    x, dy, dfin = _problem({"softplus_gate": 1, "no_softplus_no_gate": 2, "zero_A": 3}[case],
+    euler = case == "euler"
+    x, dy, dfin = _problem({"softplus_gate": 1, "no_softplus_no_gate": 2, "zero_A": 3,
+                            "euler": 5}[case],
                            softplus=softplus, with_z=case != "no_softplus_no_gate",
-                           zero_a=case == "zero_A")
-    g = _grads(x, dy, dfin, softplus)
+                           zero_a=case in ("zero_A", "euler"))
+    g = _grads(x, dy, dfin, softplus, euler)
     for name, key in NAMES.items():
         if x[name] is None:
             assert g[key] is None
             continue
-        fd = _fd(x, dy, dfin, softplus, name)
+        fd = _fd(x, dy, dfin, softplus, name, euler=euler)
         scale = np.max(np.abs(fd))
         assert scale > 1e-3, name
         err = np.max(np.abs(g[key] - fd)) / scale

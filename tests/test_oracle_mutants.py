@@ -29,6 +29,7 @@ MUTANTS = {
                      "bbar * (double)B_b[n * bc_ld + (t > 0 ? t - 1 : 0)] * ut"),
     "C_uses_B": ("acc += (double)C_b[n * bc_ld + t] * h[n];", "acc += (double)B_b[n * bc_ld + t] * h[n];"),
     "init_state_ignored": ("h[n] = h0 ? h0[n] : 0.0;", "h[n] = 0.0;"),
+    "euler_flag_ignored": ("double bbar = euler ? dt : ((An != 0.0)", "double bbar = 0 ? dt : ((An != 0.0)"),
 }
 
 
@@ -43,8 +44,10 @@ BWD_MUTANTS = {
                                    "dC_b[n * L + t] += ds * prev;"),
     "bwd_dB_without_bbar": ("dB_b[n * L + t] += lam[n] * bbar * ut;",
                             "dB_b[n * L + t] += lam[n] * ut;"),
-    "bwd_ddelta_without_A": ("ddt += lam[n] * (prev * An * abar + Bn * ut * abar);",
-                             "ddt += lam[n] * (prev * abar + Bn * ut * abar);"),
+    "bwd_ddelta_without_A": ("ddt += lam[n] * (prev * An * abar + Bn * ut * dbbar_ddt);",
+                             "ddt += lam[n] * (prev * abar + Bn * ut * dbbar_ddt);"),
+    "bwd_euler_slope": ("double dbbar_ddt = euler ? 1.0 : abar;", "double dbbar_ddt = abar;"),
+    "bwd_euler_dA": ("double dbbar_dA = euler ? 0.0 :", "double dbbar_dA = euler ? 0.5 * dt * dt :"),
     "bwd_dz_without_silu_slope": ("sg * (1.0 + zt * (1.0 - sg))", "sg"),
     "bwd_dfinal_ignored": ("lam[n] = dfinal ? dfinal[n] : 0.0;", "lam[n] = 0.0;"),
     "bwd_du_without_D": ("double du = ds * Dd;", "double du = 0.0;"),

@@ -322,3 +322,24 @@ def test_golden_snapshot_of_tiny_workload():
         assert abs(got - float(v)) <= 1e-14 * max(1.0, abs(float(v)))
         n += 1
     assert n == w.dim * (7 + w.dstate)
+
+
+# --- Euler variant of B̄ ([S] §4b, the first-order form beside equation (4)) -----------
+
+def test_euler_variant_closed_form_and_first_step():
+    """Euler B̄ = Δ B with the exact Ā: for constant inputs (N = 1, softplus off)
+    h_t = Δ B u (1 - Ā^{t+1}) / (1 - Ā), a geometric series; the first step from a zero
+    state differs from the ZOH one by exactly the factor expm1(ΔA) / (ΔA)."""
+    L, dt, a_, b_, u_ = 40, 0.37, -1.7, 0.8, 1.3
+    u = np.full(L, u_, np.float32)
+    dl = np.full(L, dt, np.float32)
+    dtf, af, bf, uf = (float(np.float32(v)) for v in (dt, a_, b_, u_))
+    ye, he = oracle.scan_rows(_rows(u)[None], _rows(dl)[None], None, [0], [0], _rows([[a_]]),
+                              _rows(np.full((1, 1, L), b_)), _rows(np.ones((1, 1, L))), None, None,
+                              False, None, 1, 0, euler=True)
+    abar = np.exp(dtf * af)
+    t = np.arange(L)
+    ref = dtf * bf * uf * (1.0 - abar ** (t + 1)) / (1.0 - abar)
+    assert np.max(np.abs(ye[0] - ref)) < 1e-13
+    yz, _ = _scan1(u, dl, [a_], np.full((1, L), b_), np.ones((1, L)), softplus=False)
+    assert abs(yz[0] / ye[0, 0] - np.expm1(dtf * af) / (dtf * af)) < 1e-14
