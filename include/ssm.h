@@ -52,6 +52,10 @@ extern "C" {
 #define SSM_F32 0
 #define SSM_BF16 1
 
+/* Bits of the delta_softplus flag word. */
+#define SSM_SOFTPLUS 1 /* Δ = softplus(delta + delta_bias) */
+#define SSM_EULER_B 2  /* B̄ = Δ B instead of the zero-order hold (A̅ stays exp(Δ A)) */
+
 /* Status codes. */
 #define SSM_OK 0
 #define SSM_ERR_ARG (-1)         /* null required pointer, bad size, bad dtype, overlap */
@@ -78,7 +82,10 @@ const char* ssm_version(void);
  *   B, C          required, (batch, dstate, seqlen)
  *   D             optional (NULL = 0), (dim)
  *   z             optional (NULL = no gate), (batch, dim, seqlen) io_dtype
- *   delta_softplus  nonzero: Δ = softplus(delta + bias); zero: Δ = delta + bias
+ *   delta_softplus  flag word: SSM_SOFTPLUS set: Δ = softplus(delta + bias), else
+ *                   Δ = delta + bias; SSM_EULER_B set: B̄ = Δ B (the first-order
+ *                   form the summary page gives beside equation (4)) instead of
+ *                   the exact zero-order hold; any other bit: SSM_ERR_ARG
  *   y             required output, (batch, dim, seqlen) io_dtype
  *   final_state   optional output (NULL = not written), (batch, dim, dstate) float32
  *
@@ -150,7 +157,8 @@ int ssm_state_update(float* state, const void* u, const void* delta, const float
 
 /*
  * Extended decode step: as ssm_state_update, plus delta_bias (optional, (dim))
- * and delta_softplus (nonzero: Δ = softplus(delta + bias)), on `stream`.
+ * and the delta_softplus flag word (as for ssm_scan_fwd: SSM_SOFTPLUS,
+ * SSM_EULER_B), on `stream`.
  */
 int ssm_state_update_ex(float* state, const void* u, const void* delta, const float* delta_bias,
                         int delta_softplus, const float* A, const float* B, const float* C,

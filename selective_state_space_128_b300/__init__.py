@@ -22,6 +22,7 @@ SSM_F32, SSM_BF16 = 0, 1
 SSM_OK = 0
 SSM_ERR_ARG, SSM_ERR_ALIGN, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_WORKSPACE = -1, -2, -3, -4, -5
 SSM_ERR_TIMEOUT = -6
+SSM_SOFTPLUS, SSM_EULER_B = 1, 2
 
 _lib = None
 
@@ -121,6 +122,12 @@ def _check_dev(*ts):
             raise ValueError("libssm takes contiguous tensors")
 
 
+def _flags(delta_softplus, euler=False):
+    """The delta_softplus flag word: a bool (softplus on/off) or the int bits
+    SSM_SOFTPLUS | SSM_EULER_B; `euler` adds SSM_EULER_B."""
+    return int(delta_softplus) | (SSM_EULER_B if euler else 0)
+
+
 def _call(name, rc):
     if rc != SSM_OK:
         raise SSMError(rc, name)
@@ -137,7 +144,7 @@ def ssm_scan_fwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_s
     batch, dim, L = u.shape
     N = A.shape[1]
     rc = load().ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B), _ptr(C),
-                             _ptr(D), _ptr(z), int(bool(delta_softplus)), _ptr(y),
+                             _ptr(D), _ptr(z), _flags(delta_softplus), _ptr(y),
                              _ptr(final_state), batch, dim, L, N, _io_dtype(u))
     _call("ssm_scan_fwd", rc)
 
@@ -155,7 +162,7 @@ def ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, fina
     if workspace is not None and workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
     rc = load().ssm_scan_fwd_ex(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
-                                _ptr(C), _ptr(D), _ptr(z), int(bool(delta_softplus)), _ptr(y),
+                                _ptr(C), _ptr(D), _ptr(z), _flags(delta_softplus), _ptr(y),
                                 _ptr(final_state), batch, dim, L, N, _io_dtype(u),
                                 _ptr(init_state), _ptr(workspace), int(workspace_bytes or 0),
                                 _stream(stream))
@@ -185,7 +192,7 @@ def ssm_state_update_ex(state, u, delta, delta_bias, delta_softplus, A, B, C, D,
     batch, dim = u.shape
     N = A.shape[1]
     rc = load().ssm_state_update_ex(_ptr(state), _ptr(u), _ptr(delta), _ptr(delta_bias),
-                                    int(bool(delta_softplus)), _ptr(A), _ptr(B), _ptr(C),
+                                    _flags(delta_softplus), _ptr(A), _ptr(B), _ptr(C),
                                     _ptr(D), _ptr(z), _ptr(y), batch, dim, N, _io_dtype(u),
                                     _stream(stream))
     _call("ssm_state_update_ex", rc)
@@ -201,7 +208,7 @@ def ssm_scan_fwd_noalloc(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y,
     batch, dim, L = u.shape
     N = A.shape[1]
     rc = load().ssm_scan_fwd_noalloc(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
-                                     _ptr(C), _ptr(D), _ptr(z), int(bool(delta_softplus)),
+                                     _ptr(C), _ptr(D), _ptr(z), _flags(delta_softplus),
                                      _ptr(y), _ptr(final_state), batch, dim, L, N,
                                      _io_dtype(u), _ptr(init_state), _stream(stream))
     _call("ssm_scan_fwd_noalloc", rc)
@@ -222,7 +229,7 @@ def ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, init_state
     if workspace is not None and workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
     rc = load().ssm_scan_bwd(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B), _ptr(C),
-                             _ptr(D), _ptr(z), int(bool(delta_softplus)), _ptr(init_state),
+                             _ptr(D), _ptr(z), _flags(delta_softplus), _ptr(init_state),
                              _ptr(dy), _ptr(d_final_state), _ptr(du), _ptr(ddelta), _ptr(dA),
                              _ptr(dB), _ptr(dC), _ptr(dD), _ptr(dz), _ptr(d_delta_bias),
                              _ptr(d_init_state), batch, dim, L, N, _io_dtype(u),
@@ -262,7 +269,7 @@ def static_scratch_bytes() -> int:
 # ---------------------------------------------------------------------------
 
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-         init_state=None, split=True, stream=None):
+         init_state=None, split=True, stream=None, euler=False):
     """y, final_state = scan(...): allocates y (dtype of u) and final_state (float32), and a
     workspace when the plan splits the sequence across blocks."""
     import torch
@@ -275,13 +282,14 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True
         nbytes = ssm_scan_workspace_bytes(batch, dim, L, N, _io_dtype(u))
         if nbytes:
             ws = torch.empty(nbytes, dtype=torch.uint8, device=u.device)
-    ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, h, init_state, ws,
-                    stream=stream)
+    ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler), y, h,
+                    init_state, ws, stream=stream)
     return y, h
 
 
 def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-             init_state=None, dy=None, d_final_state=None, want_init_grad=False, stream=None):
+             init_state=None, dy=None, d_final_state=None, want_init_grad=False, stream=None,
+             euler=False):
     """Derivatives of Σ y·dy + Σ final_state·d_final_state for the inputs of ``scan``.
     Allocates every output and the workspace; returns a dict with du, ddelta, dz (dtype of
     u; dz None without z), dA, dB, dC, dD, dbias (float32; dD / dbias always computed) and
@@ -299,8 +307,8 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                dinit=torch.empty((batch, dim, N), **f32) if want_init_grad else None)
     nbytes = ssm_scan_bwd_workspace_bytes(batch, dim, L, N)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-    ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, init_state, dy,
-                 d_final_state, out["du"], out["ddelta"], out["dA"], out["dB"], out["dC"],
+    ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler), init_state,
+                 dy, d_final_state, out["du"], out["ddelta"], out["dA"], out["dB"], out["dC"],
                  out["dD"], out["dz"], out["dbias"], out["dinit"], ws, nbytes, stream)
     return out
 

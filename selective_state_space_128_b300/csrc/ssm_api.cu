@@ -28,6 +28,9 @@ int sm_count_current() {
   return n;
 }
 
+// the delta_softplus flag word: SSM_SOFTPLUS | SSM_EULER_B, nothing else
+bool flags_ok(int f) { return (f & ~(SSM_SOFTPLUS | SSM_EULER_B)) == 0; }
+
 bool sizes_ok(int64_t batch, int64_t dim, int64_t seqlen) {
   // every flat index must fit in int64 with room to spare
   if (batch < 0 || dim < 0 || seqlen < 0) return false;
@@ -68,6 +71,7 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
                     int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
                     void* workspace, size_t workspace_bytes, void* stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!flags_ok(delta_softplus)) return SSM_ERR_ARG;
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   const bool work = batch > 0 && dim > 0;
@@ -105,7 +109,8 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
   a.y = y; a.final_state = final_state; a.init_state = init_state;
   a.batch = batch; a.dim = dim; a.L = seqlen;
   a.nseg = plan.nseg; a.seg_len = plan.seg_len;
-  a.softplus = delta_softplus != 0;
+  a.softplus = (delta_softplus & SSM_SOFTPLUS) != 0;
+  a.euler = (delta_softplus & SSM_EULER_B) != 0;
   a.vec_io = (seqlen * (int64_t)esz) % 16 == 0;
   a.vec_bc = (seqlen * 4) % 16 == 0;
   a.force_precise = io_dtype == SSM_F32;
@@ -139,6 +144,7 @@ int ssm_state_update_ex(float* state, const void* u, const void* delta, const fl
                         const float* D, const void* z, void* y, int64_t batch, int64_t dim,
                         int64_t dstate, int io_dtype, void* stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!flags_ok(delta_softplus)) return SSM_ERR_ARG;
   if (!sizes_ok(batch, dim, 1) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   if (batch > 0 && dim > 0 && (!state || !u || !delta || !A || !B || !C || !y)) return SSM_ERR_ARG;
@@ -158,7 +164,8 @@ int ssm_state_update_ex(float* state, const void* u, const void* delta, const fl
   ssm::UpdateArgs a{};
   a.state = state; a.u = u; a.delta = delta; a.z = z; a.bias = delta_bias; a.A = A; a.B = B;
   a.C = C; a.D = D; a.y = y; a.batch = batch; a.dim = dim;
-  a.softplus = delta_softplus != 0;
+  a.softplus = (delta_softplus & SSM_SOFTPLUS) != 0;
+  a.euler = (delta_softplus & SSM_EULER_B) != 0;
   a.force_precise = io_dtype == SSM_F32;
   const cudaError_t e = ssm::update_launch(a, dstate, io_dtype, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
@@ -185,6 +192,7 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
                  int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                  void* workspace, size_t workspace_bytes, void* stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!flags_ok(delta_softplus)) return SSM_ERR_ARG;
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   if (dz && !z) return SSM_ERR_ARG;
@@ -252,7 +260,8 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
   a.ws_D = reinterpret_cast<float*>(ws + lay.o_D);
   a.ws_bias = reinterpret_cast<float*>(ws + lay.o_bias);
   a.batch = batch; a.dim = dim; a.L = seqlen; a.nblk = lay.nblk;
-  a.softplus = delta_softplus != 0;
+  a.softplus = (delta_softplus & SSM_SOFTPLUS) != 0;
+  a.euler = (delta_softplus & SSM_EULER_B) != 0;
   a.force_precise = io_dtype == SSM_F32;
   const cudaError_t e = ssm::bwd_launch(a, dstate, io_dtype, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

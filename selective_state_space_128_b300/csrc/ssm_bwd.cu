@@ -11,6 +11,7 @@
 //   λ_t  = ds_t C_t + Ā_{t+1} λ_{t+1}        (λ_{L-1} also receives dfinal)
 //   du_t = ds_t D + Σ_n λ B̄ B,               dB_t += λ B̄ u,   dC_t += ds_t h_t
 //   dΔ_t = Σ_n Ā λ (A h_{t-1} + B u),        dA += λ (Δ Ā h_{t-1} + B u (Δ Ā - B̄)/A)
+//   (the Euler variant B̄ = Δ: dΔ_t = Σ_n λ (A Ā h_{t-1} + B u), and no B u term in dA)
 //   dΔraw_t = dΔ_t σ(Δraw_t + bias) (softplus), dbias += dΔraw,  dD += ds u,
 //   dh_{-1} = Ā_0 λ_0
 // where B̄ = (Ā - 1)/A is the scalar zero-order-hold factor (A = 0: Δ, and
@@ -237,7 +238,8 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
       Ajp[q] = pack2(Aj[2 * q], Aj[2 * q + 1]);
     }
   }
-  const bool precise = __syncthreads_or(zeroA) || p.force_precise;
+  const bool euler = p.euler != 0;  // B̄ = Δ B: runs on the precise flavour
+  const bool precise = __syncthreads_or(zeroA) || p.force_precise || euler;
   const bool fast_pairs = PAIRS && !precise;  // block-uniform
   const bool sp = p.softplus != 0;
 
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
             h[j] = fmaf(a, h[j] - v, v);
           } else {
             const float x = dt * Aj[j];
-            const float bb = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
+            const float bb = (Aj[j] != 0.f && !euler) ? expm1f(x) * invA[j] : dt;
             h[j] = fmaf(expf(x), h[j], bb * (Bv[j] * u));
           }
         }
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
               h[j] = fmaf(a, h[j] - v, v);
             } else {
               const float x = dt * Aj[j];
-              const float bb = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
+              const float bb = (Aj[j] != 0.f && !euler) ? expm1f(x) * invA[j] : dt;
               h[j] = fmaf(expf(x), h[j], bb * (Bv[j] * u));
             }
             s = fmaf(Cv[j], h[j], s);
@@ -623,23 +625,31 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
           for (int j = 0; j < NPT; ++j) {
             const float Bn = Bv[j];
             lam[j] = fmaf(ds, Cv[j], lam[j]);
-            float a, bb, w;
+            // a = Ā, bb = B̄, w = dB̄/dA, sl = dB̄/dΔ
+            float a, bb, w, sl;
             if (!precise) {
               a = ex2_fast(dt * Aj[j] * kLog2e);
               bb = fmaf(a, invA[j], -invA[j]);
               w = (dt * a - bb) * invA[j];
+              sl = a;
+            } else if (euler) {
+              a = expf(dt * Aj[j]);
+              bb = dt;
+              w = 0.f;
+              sl = 1.f;
             } else {
               const float x = dt * Aj[j];
               a = expf(x);
               bb = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
               w = Aj[j] != 0.f ? (dt * a - bb) * invA[j] : 0.5f * dt * dt;
+              sl = a;
             }
             const float x1 = lam[j] * hp[j];
             const float x2 = lam[j] * (Bn * u);
             const float lb = lam[j] * bb;
             du_p = fmaf(lb, Bn, du_p);
             dbv[j] = lb * u;
-            dd_p = fmaf(a, fmaf(Aj[j], x1, x2), dd_p);
+            dd_p = fmaf(a * Aj[j], x1, fmaf(sl, x2, dd_p));
             dAacc[j] = fmaf(x2, w, fmaf(x1, dt * a, dAacc[j]));
             lam[j] *= a;
           }

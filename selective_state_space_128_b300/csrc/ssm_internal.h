@@ -34,6 +34,7 @@ struct ScanArgs {
   int vec_io;       // rows of u/delta/z/y are 16-byte aligned
   int vec_bc;       // rows of B/C are 16-byte aligned
   int force_precise;
+  int euler;        // B̄ = Δ B (runs on the precise flavour)
   int use_tma;      // set by the launcher: chunks staged by TMA
 };
 
@@ -67,6 +68,7 @@ struct UpdateArgs {
   int64_t batch, dim;
   int softplus;
   int force_precise;
+  int euler;
 };
 
 // Synchronises `stream`, then reads and clears the scan kernels' device error
@@ -107,6 +109,7 @@ struct BwdArgs {
   int64_t batch, dim, L, nblk;
   int softplus;
   int force_precise;
+  int euler;
 };
 
 // Workspace of the backward pass: byte offsets of its parts (256-byte aligned)

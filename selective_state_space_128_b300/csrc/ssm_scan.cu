@@ -496,12 +496,14 @@ __device__ __forceinline__ void chunk_fast_scalar(const unsigned char* buf, floa
   }
 }
 
-// Precise flavour (CUDA libm expf / expm1f; A = 0 takes the limit Δ B).
+// Precise flavour (CUDA libm expf / expm1f; A = 0 takes the limit Δ B; with
+// `euler`, B̄ = Δ B for every state).
 template <typename IO, int N, int PASS>
 __device__ __forceinline__ void chunk_precise(const unsigned char* buf, float* part, int prow,
                                               int c, int g, float (&h)[ScanCfg<N>::NPT],
                                               const float (&Aj)[ScanCfg<N>::NPT],
-                                              const float (&invA)[ScanCfg<N>::NPT], float& sumDt) {
+                                              const float (&invA)[ScanCfg<N>::NPT], float& sumDt,
+                                              bool euler) {
   using Cf = ScanCfg<N>;
   using S = ScanSmem<IO, N>;
   constexpr int NPT = Cf::NPT, T = Cf::T;
@@ -521,7 +523,7 @@ __device__ __forceinline__ void chunk_precise(const unsigned char* buf, float* p
       for (int j = 0; j < NPT; ++j) {
         const float x = dt * Aj[j];
         const float a = expf(x);
-        const float coef = Aj[j] != 0.f ? expm1f(x) * invA[j] : dt;
+        const float coef = (Aj[j] != 0.f && !euler) ? expm1f(x) * invA[j] : dt;
         h[j] = fmaf(a, h[j], coef * (Bt[t * S::RowBC + j] * ut));
         if (PASS == 0) acc = fmaf(Ct[t * S::RowBC + j], h[j], acc);
       }
@@ -568,7 +570,8 @@ __device__ __forceinline__ void chunk_iteration(
   }
   other_chunks();
   if (!FAST && precise) {
-    chunk_precise<IO, N, PASS>(bufM, partM, prow, c, g, ls.h, ls.Aj, ls.invA, ls.sumDt);
+    chunk_precise<IO, N, PASS>(bufM, partM, prow, c, g, ls.h, ls.Aj, ls.invA, ls.sumDt,
+                                  p.euler != 0);
   } else if constexpr (NPT == 1) {
     chunk_fast_scalar<IO, PASS>(bufM, partM, prow, c, ls.h[0], ls.A2s, ls.nIs, ls.sumDt);
   } else {
@@ -653,7 +656,8 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     ls.Aj[j] = chan_ok ? p.A[d * N + g * NPT + j] : -1.f;
     zeroA |= (ls.Aj[j] == 0.f);
   }
-  const bool precise = __syncthreads_or(zeroA) || p.force_precise;
+  // the precise flavour: fp32 I/O, a channel with A = 0, or the Euler B̄
+  const bool precise = __syncthreads_or(zeroA) || p.force_precise || p.euler;
   const StepFlags fl{precise, p.softplus != 0, p.z != nullptr};
   const bool fast = !precise && fl.softplus && (PASS == 1 || fl.gate);
 

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kUpdThreads) update_kernel(const UpdateArgs p)
 
 #pragma unroll
   for (int k = 0; k < kUpdK; ++k) {
-    bool precise = p.force_precise != 0;
+    bool precise = p.force_precise != 0 || p.euler != 0;
 #pragma unroll
     for (int j = 0; j < NPT; ++j) precise |= (Av[k][j] == 0.f);
     const float x = xx[k];
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kUpdThreads) update_kernel(const UpdateArgs p)
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const float xa = dt * Av[k][j];
-        const float coef = Av[k][j] != 0.f ? expm1f(xa) / Av[k][j] : dt;
+        const float coef = (Av[k][j] != 0.f && !p.euler) ? expm1f(xa) / Av[k][j] : dt;
         st[k][j] = fmaf(expf(xa), st[k][j], coef * (Bv[j] * uu[k]));
         acc = fmaf(Cv[j], st[k][j], acc);
       }

@@ -184,3 +184,13 @@ def test_conv_argument_errors():
                                 ssm.SSM_BF16, None) == ssm.SSM_ERR_ARG    # state required
     assert L_.ssm_conv1d_update(FAKE + 0x3000000, FAKE, FAKE + 0x1000000, None, 1,
                                 FAKE + 0x3000010, 2, 8, 4, ssm.SSM_BF16, None) == ssm.SSM_ERR_ARG
+
+
+def test_flag_word_is_checked():
+    assert _scan(softplus=4) == ssm.SSM_ERR_ARG
+    assert _scan(softplus=-1) == ssm.SSM_ERR_ARG
+    assert _upd(softplus=8) == ssm.SSM_ERR_ARG
+    assert _bwd(softplus=16) == ssm.SSM_ERR_ARG
+    # the defined bits pass validation (empty problem: nothing is launched)
+    for f in (0, ssm.SSM_SOFTPLUS, ssm.SSM_EULER_B, ssm.SSM_SOFTPLUS | ssm.SSM_EULER_B):
+        assert _scan(softplus=f, batch=0) == ssm.SSM_OK
