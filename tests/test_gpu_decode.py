@@ -96,3 +96,34 @@ def test_zero_A_decode():
     torch.cuda.synchronize()
     assert oracle.rel_err(host64(y), y_ref) <= 1e-2
     assert oracle.rel_err(host64(st), st_ref) <= 1e-2
+
+
+@pytest.mark.parametrize("gate,softplus", [(True, True), (False, True), (True, False)])
+def test_whole_channel_blocks_with_zero_A(gate, softplus):
+    """d_inner a multiple of the block's channels (192 = 3 x 64), N 16, bf16, with and
+    without gate and softplus, including a channel with A = 0 states (that channel
+    takes the precise flavour, the exact limit Ā = 1, B̄ = Δ B)."""
+    dw, s = _decode_case(7, 192, 16, 4, "bf16", seed=44)
+    A = synth.gen_A(dw.dim, 16)
+    A[5, ::3] = 0.0
+    D = synth.fill(45, synth.S_D, 0, dw.dim, synth.UNIFORM, 0.5, 1.5)
+    bias = synth.gen_delta_bias(45, dw.dim)
+    st0 = np.random.default_rng(7).standard_normal((dw.batch, dw.dim, 16)).astype(np.float32)
+    st_ref = st0.astype(np.float64)
+    st = dev_f32(st0)
+    for i in range(dw.steps):
+        dl = s["delta"][i]
+        if not softplus:
+            dl = synth.f32_to_bf16(np.abs(synth.bf16_to_f32(dl)) * 0.1 + 1e-3)
+        z = s["z"][i] if gate else None
+        y_ref, st_ref = oracle.step(st_ref, s["u"][i], dl, A, s["B"][i], s["C"][i], D, z,
+                                    bias if softplus else None, softplus)
+        u = dev_io(s["u"][i])
+        y = torch.empty_like(u)
+        ssm.ssm_state_update_ex(st, u, dev_io(dl), dev_f32(bias) if softplus else None, softplus,
+                                dev_f32(A), dev_f32(s["B"][i]), dev_f32(s["C"][i]), dev_f32(D),
+                                dev_io(z), y)
+        torch.cuda.synchronize()
+        assert oracle.rel_err(host64(y), y_ref) <= 1e-2
+        assert oracle.rel_err(host64(st), st_ref) <= 1e-2
+    assert ssm.ssm_status() == ssm.SSM_OK
