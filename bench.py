@@ -340,25 +340,39 @@ def bench_backward(w, g, steps, warmup, world):
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step():
+    y = torch.empty_like(g["u"])
+    h = torch.empty((w.batch, w.dim, N), **f32)
+
+    def step(flags=ssm.SSM_SOFTPLUS):
         ssm.ssm_scan_bwd(g["u"], g["delta"], g["delta_bias"], g["A"], g["B"], g["C"], g["D"],
-                         g["z"], True, None, dy, None, out["du"], out["ddelta"], out["dA"],
+                         g["z"], flags, None, dy, None, out["du"], out["ddelta"], out["dA"],
                          out["dB"], out["dC"], out["dD"], out["dz"], out["dbias"], None, ws,
                          nbytes, stream=stream)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(world, e0.elapsed_time(e1)) / steps
-    return dict(step_ms=ms, steps=steps, workspace_bytes=nbytes)
+    def fwd_train():
+        ssm.ssm_scan_fwd_train(g["u"], g["delta"], g["delta_bias"], g["A"], g["B"], g["C"],
+                               g["D"], g["z"], True, y, h, None, None, 0, ws, nbytes, stream)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(world, e0.elapsed_time(e1)) / steps
+
+    ms = timed(step)
+    fwd_train()  # the workspace now holds the saved chunk-start states
+    saved_ms = timed(lambda: step(ssm.SSM_SOFTPLUS | ssm.SSM_SAVED_STATES))
+    train_ms = timed(lambda: (fwd_train(), step(ssm.SSM_SOFTPLUS | ssm.SSM_SAVED_STATES)))
+    return dict(step_ms=ms, saved_ms=saved_ms, train_ms=train_ms, steps=steps,
+                workspace_bytes=nbytes)
 
 
 # ---------------------------------------------------------------------------
@@ -586,6 +600,9 @@ def main():
                             "us_per_step": bwd["step_ms"] * 1e3,
                             "channel_steps_per_s": w.channel_steps / bs * world,
                             "time_vs_forward": bs / step_s,
+                            "us_per_step_from_saved_states": bwd["saved_ms"] * 1e3,
+                            "train_step_us": bwd["train_ms"] * 1e3,
+                            "train_step": "ssm_scan_fwd_train + ssm_scan_bwd(SSM_SAVED_STATES)",
                             "workspace_bytes": bwd["workspace_bytes"],
                             "gpu_launches": 2 * bwd["steps"],
                             "l2": "u, delta, z, dy: 4 x %.0f MB, larger than L2"

@@ -55,6 +55,8 @@ extern "C" {
 /* Bits of the delta_softplus flag word. */
 #define SSM_SOFTPLUS 1 /* Δ = softplus(delta + delta_bias) */
 #define SSM_EULER_B 2  /* B̄ = Δ B instead of the zero-order hold (A̅ stays exp(Δ A)) */
+#define SSM_SAVED_STATES 4 /* ssm_scan_bwd only: its workspace holds the states that
+                              ssm_scan_fwd_train saved for these inputs */
 
 /* Status codes. */
 #define SSM_OK 0
@@ -288,6 +290,24 @@ int ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
 int ssm_conv1d_update(void* conv_state, const void* x, const float* weight, const float* bias,
                       int silu, void* out, int64_t batch, int64_t dim, int64_t width,
                       int io_dtype, void* stream);
+
+/*
+ * Training forward: ssm_scan_fwd_ex (same arguments, same results) that also
+ * saves, in the backward pass's workspace `bwd_workspace` (at least
+ * ssm_scan_bwd_workspace_bytes() bytes, 16-byte aligned), the state at the
+ * start of every chunk of the sequence.  A following ssm_scan_bwd on the same
+ * inputs, with that workspace and SSM_SAVED_STATES in its flag word, then
+ * skips its own forward sweep.  Saving applies to dstate <= 16 (the backward's
+ * chunk equals the forward's there); for larger dstate nothing is saved and
+ * the backward recomputes whatever its flags say.  The workspace must not be
+ * used for anything else between the two calls.
+ */
+int ssm_scan_fwd_train(const void* u, const void* delta, const float* delta_bias, const float* A,
+                       const float* B, const float* C, const float* D, const void* z,
+                       int delta_softplus, void* y, float* final_state, int64_t batch,
+                       int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                       const float* init_state, void* workspace, size_t workspace_bytes,
+                       void* bwd_workspace, size_t bwd_workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ SSM_F32, SSM_BF16 = 0, 1
 SSM_OK = 0
 SSM_ERR_ARG, SSM_ERR_ALIGN, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_WORKSPACE = -1, -2, -3, -4, -5
 SSM_ERR_TIMEOUT = -6
-SSM_SOFTPLUS, SSM_EULER_B = 1, 2
+SSM_SOFTPLUS, SSM_EULER_B, SSM_SAVED_STATES = 1, 2, 4
 
 _lib = None
 
@@ -66,6 +66,9 @@ def load():
     lib.ssm_scan_bwd_workspace_bytes.restype = sz
     lib.ssm_scan_bwd.argtypes = [vp] * 8 + [i32] + [vp] * 12 + [i64, i64, i64, i64, i32, vp, sz, vp]
     lib.ssm_scan_bwd.restype = i32
+    lib.ssm_scan_fwd_train.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp, sz,
+                                                   vp, sz, vp]
+    lib.ssm_scan_fwd_train.restype = i32
     lib.ssm_conv1d_fwd.argtypes = [vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, i64, i32, vp]
     lib.ssm_conv1d_fwd.restype = i32
     lib.ssm_conv1d_update.argtypes = [vp, vp, vp, vp, i32, vp, i64, i64, i64, i32, vp]
@@ -167,6 +170,24 @@ def ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, fina
                                 _ptr(init_state), _ptr(workspace), int(workspace_bytes or 0),
                                 _stream(stream))
     _call("ssm_scan_fwd_ex", rc)
+
+
+def ssm_scan_fwd_train(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                       init_state, workspace, workspace_bytes, bwd_workspace, bwd_workspace_bytes,
+                       stream=None):
+    """Tensor form of ``ssm_scan_fwd_train`` (the forward that saves the backward's
+    chunk-start states into ``bwd_workspace``)."""
+    _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, workspace,
+               bwd_workspace)
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    rc = load().ssm_scan_fwd_train(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
+                                   _ptr(C), _ptr(D), _ptr(z), _flags(delta_softplus), _ptr(y),
+                                   _ptr(final_state), batch, dim, L, N, _io_dtype(u),
+                                   _ptr(init_state), _ptr(workspace), int(workspace_bytes or 0),
+                                   _ptr(bwd_workspace), int(bwd_workspace_bytes or 0),
+                                   _stream(stream))
+    _call("ssm_scan_fwd_train", rc)
 
 
 def ssm_status(stream=None) -> int:
@@ -287,9 +308,27 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True
     return y, h
 
 
+def scan_train(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+               init_state=None, stream=None, euler=False):
+    """y, final_state, saved = scan_train(...): the forward of ``scan`` that also keeps
+    what the backward needs; pass ``saved`` to ``scan_bwd(..., saved=saved)``."""
+    import torch
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    y = torch.empty_like(u)
+    h = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device)
+    nbytes = ssm_scan_workspace_bytes(batch, dim, L, N, _io_dtype(u))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=u.device) if nbytes else None
+    bbytes = ssm_scan_bwd_workspace_bytes(batch, dim, L, N)
+    bws = torch.empty(max(bbytes, 16), dtype=torch.uint8, device=u.device)
+    ssm_scan_fwd_train(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler), y, h,
+                       init_state, ws, nbytes, bws, bbytes, stream)
+    return y, h, bws
+
+
 def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
              init_state=None, dy=None, d_final_state=None, want_init_grad=False, stream=None,
-             euler=False):
+             euler=False, saved=None):
     """Derivatives of Σ y·dy + Σ final_state·d_final_state for the inputs of ``scan``.
     Allocates every output and the workspace; returns a dict with du, ddelta, dz (dtype of
     u; dz None without z), dA, dB, dC, dD, dbias (float32; dD / dbias always computed) and
@@ -306,8 +345,13 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                dbias=torch.empty(dim, **f32),
                dinit=torch.empty((batch, dim, N), **f32) if want_init_grad else None)
     nbytes = ssm_scan_bwd_workspace_bytes(batch, dim, L, N)
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-    ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler), init_state,
+    flags = _flags(delta_softplus, euler)
+    if saved is not None:
+        ws = saved
+        flags |= SSM_SAVED_STATES
+    else:
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, flags, init_state,
                  dy, d_final_state, out["du"], out["ddelta"], out["dA"], out["dB"], out["dC"],
                  out["dD"], out["dz"], out["dbias"], out["dinit"], ws, nbytes, stream)
     return out

@@ -65,18 +65,25 @@ size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int6
       .workspace_bytes;
 }
 
-int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, const float* A,
-                    const float* B, const float* C, const float* D, const void* z,
-                    int delta_softplus, void* y, float* final_state, int64_t batch, int64_t dim,
-                    int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
-                    void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// ssm_scan_fwd_ex, plus an optional training save into a backward workspace
+int scan_fwd_impl(const void* u, const void* delta, const float* delta_bias, const float* A,
+                  const float* B, const float* C, const float* D, const void* z,
+                  int delta_softplus, void* y, float* final_state, int64_t batch, int64_t dim,
+                  int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
+                  void* workspace, size_t workspace_bytes, void* bwd_workspace,
+                  size_t bwd_workspace_bytes, bool train, void* stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
   if (!flags_ok(delta_softplus)) return SSM_ERR_ARG;
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   const bool work = batch > 0 && dim > 0;
   if (work && seqlen > 0 && (!u || !delta || !A || !B || !C || !y)) return SSM_ERR_ARG;
-  const void* ptrs[] = {u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, workspace};
+  const void* ptrs[] = {u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, workspace,
+                        bwd_workspace};
   for (const void* q : ptrs)
     if (!aligned16(q)) return SSM_ERR_ALIGN;
   const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
@@ -103,8 +110,29 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
   const ssm::ScanPlan plan = ssm::scan_plan(batch, dim, seqlen, dstate, io_dtype,
                                             sm_count_current(), workspace != nullptr && !in_place);
   if (workspace && workspace_bytes < plan.workspace_bytes) return SSM_ERR_WORKSPACE;
+  // the training save: the backward's checkpoint part of its workspace
+  float* ckpt = nullptr;
+  int64_t ckpt_nch = 0;
+  if (train && seqlen > 0) {
+    const ssm::BwdLayout lay = ssm::bwd_layout(batch, dim, seqlen, dstate);
+    if (!bwd_workspace || bwd_workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
+    const void* others[] = {u, delta, z, y, workspace};
+    const size_t sizes[] = {nio, nio, nio, nio, plan.workspace_bytes};
+    for (int k = 0; k < 5; ++k)
+      if (overlaps(bwd_workspace, lay.bytes, others[k], sizes[k])) return SSM_ERR_ARG;
+    if (overlaps(bwd_workspace, lay.bytes, final_state, nst) ||
+        overlaps(bwd_workspace, lay.bytes, init_state, nst) ||
+        overlaps(bwd_workspace, lay.bytes, B, nbc) || overlaps(bwd_workspace, lay.bytes, C, nbc))
+      return SSM_ERR_ARG;
+    if (ssm::bwd_chunk(dstate) == plan.chunk) {
+      ckpt = reinterpret_cast<float*>(static_cast<unsigned char*>(bwd_workspace) + lay.o_ckpt);
+      ckpt_nch = lay.nch;
+    }
+  }
 
   ssm::ScanArgs a{};
+  a.ckpt = ckpt;
+  a.ckpt_nch = ckpt_nch;
   a.u = u; a.delta = delta; a.z = z; a.bias = delta_bias; a.A = A; a.B = B; a.C = C; a.D = D;
   a.y = y; a.final_state = final_state; a.init_state = init_state;
   a.batch = batch; a.dim = dim; a.L = seqlen;
@@ -122,6 +150,31 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
   }
   const cudaError_t e = ssm::scan_launch(a, dstate, io_dtype, plan, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, const float* A,
+                    const float* B, const float* C, const float* D, const void* z,
+                    int delta_softplus, void* y, float* final_state, int64_t batch, int64_t dim,
+                    int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  return scan_fwd_impl(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state, batch,
+                       dim, seqlen, dstate, io_dtype, init_state, workspace, workspace_bytes,
+                       nullptr, 0, false, stream);
+}
+
+int ssm_scan_fwd_train(const void* u, const void* delta, const float* delta_bias, const float* A,
+                       const float* B, const float* C, const float* D, const void* z,
+                       int delta_softplus, void* y, float* final_state, int64_t batch,
+                       int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                       const float* init_state, void* workspace, size_t workspace_bytes,
+                       void* bwd_workspace, size_t bwd_workspace_bytes, void* stream) {
+  return scan_fwd_impl(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state, batch,
+                       dim, seqlen, dstate, io_dtype, init_state, workspace, workspace_bytes,
+                       bwd_workspace, bwd_workspace_bytes, true, stream);
 }
 
 int ssm_status(void* stream) {
@@ -192,7 +245,7 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
                  int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                  void* workspace, size_t workspace_bytes, void* stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
-  if (!flags_ok(delta_softplus)) return SSM_ERR_ARG;
+  if (!flags_ok(delta_softplus & ~SSM_SAVED_STATES)) return SSM_ERR_ARG;
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   if (dz && !z) return SSM_ERR_ARG;
@@ -260,6 +313,10 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
   a.ws_D = reinterpret_cast<float*>(ws + lay.o_D);
   a.ws_bias = reinterpret_cast<float*>(ws + lay.o_bias);
   a.batch = batch; a.dim = dim; a.L = seqlen; a.nblk = lay.nblk;
+  // saved states are used where the training forward saves them (same chunk length)
+  a.saved = (delta_softplus & SSM_SAVED_STATES) != 0 &&
+            ssm::bwd_chunk(dstate) ==
+                ssm::scan_plan(batch, dim, seqlen, dstate, io_dtype, sm_count_current(), false).chunk;
   a.softplus = (delta_softplus & SSM_SOFTPLUS) != 0;
   a.euler = (delta_softplus & SSM_EULER_B) != 0;
   a.force_precise = io_dtype == SSM_F32;

@@ -21,7 +21,8 @@
 // lane layout as the forward kernel: G lanes per channel, NPT states per lane
 // in registers.  It walks the sequence twice:
 //  1. forward, recurrence only, storing the state at the start of every chunk
-//     of T steps to a checkpoint workspace (N floats per channel per chunk);
+//     of T steps to a checkpoint workspace (N floats per channel per chunk) --
+//     skipped when a training forward (ssm_scan_fwd_train) saved them;
 //  2. backward, chunk by chunk from the end: reload the chunk's start state,
 //     recompute the T states into shared memory, finalise the gate's
 //     derivative from the recomputed readout, then run the adjoint recurrence
@@ -213,7 +214,10 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
   const int r = tid / TPR, te = (tid % TPR) * E;
   const bool row_ok = r < nrows;
   const int64_t io_row = (b * p.dim + d0 + (row_ok ? r : 0)) * L;
-  const bool vec = E % 4 == 0 && L % 4 == 0;  // E-step runs are 8- / 16-byte aligned
+  // E-step runs as vectors: vecio moves 4 bf16 as 8 bytes and 8 or 16 bf16 (or
+  // 4+ floats) as 16-byte accesses, so every row must start on that boundary
+  constexpr int kVecBytes = (sizeof(IO) == 2 && E == 4) ? 8 : 16;
+  const bool vec = E % 4 == 0 && (L * (int64_t)sizeof(IO)) % kVecBytes == 0;
 
   for (int i = tid; i < CH; i += kBwdThreads) {
     const bool ok = d0 + i < p.dim;
@@ -357,8 +361,9 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
   }
   float dyv[E], zz[E], sg[E];
   BwdPre<N> pre;
-  if (nch > 0) fetch(0, false, pre);
-  for (int k = 0; k < nch; ++k) {
+  const int nch1 = p.saved ? 0 : nch;  // a training forward already saved them
+  if (nch1 > 0) fetch(0, false, pre);
+  for (int k = 0; k < nch1; ++k) {
     if (fast_pairs) {
 #pragma unroll
       for (int q = 0; q < NP; ++q) unpack2(hq[q], h[2 * q], h[2 * q + 1]);
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
       sts_vec<NPT>(cp, h);  // (a global store; sts_vec only packs the vector)
     }
     stage(k, false, pre, dyv, zz, sg);
-    if (k + 1 < nch) fetch(k + 1, false, pre);
+    if (k + 1 < nch1) fetch(k + 1, false, pre);
     __syncthreads();
     const float* rDT = sDT + c * Cf::RowF;
     const float* rU = sU + c * Cf::RowF;
@@ -828,6 +833,19 @@ static bool bwd_geometry(int64_t N, int64_t dim, int64_t L, int64_t& nblk, int64
 }
 
 static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+int bwd_chunk(int64_t N) {
+  switch (N) {
+    case 1: return BwdCfg<1>::T;
+    case 2: return BwdCfg<2>::T;
+    case 4: return BwdCfg<4>::T;
+    case 8: return BwdCfg<8>::T;
+    case 16: return BwdCfg<16>::T;
+    case 32: return BwdCfg<32>::T;
+    case 64: return BwdCfg<64>::T;
+    default: return 0;
+  }
+}
 
 BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t L, int64_t N) {
   BwdLayout w{};

@@ -36,6 +36,11 @@ struct ScanArgs {
   int force_precise;
   int euler;        // B̄ = Δ B (runs on the precise flavour)
   int use_tma;      // set by the launcher: chunks staged by TMA
+  // training forward: the state at the start of every 16-step chunk of the
+  // sequence, [batch][ckpt_nch][dim][N] (the backward pass's checkpoints); null
+  // when not saving
+  float* ckpt;
+  int64_t ckpt_nch;
 };
 
 struct ScanPlan {
@@ -110,7 +115,11 @@ struct BwdArgs {
   int softplus;
   int force_precise;
   int euler;
+  int saved;  // ckpt already holds the chunk-start states (a training forward wrote them)
 };
+
+// Chunk length of the backward pass for state size N (the checkpoint interval).
+int bwd_chunk(int64_t N);
 
 // Workspace of the backward pass: byte offsets of its parts (256-byte aligned)
 // and the total; nblk = channel blocks per batch row, nch = chunks per sequence.

@@ -750,6 +750,27 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
       ++issued;  // uniform: every thread counts the chunks issued
       sissue = sissue + 1 == NS ? 0 : sissue + 1;
     }
+    // training forward: save the state at the start of chunk i for the backward
+    if (PASS == 0 && p.ckpt != nullptr && chan_ok) {
+      float* cp = p.ckpt + ((b * p.ckpt_nch + t_begin / T + i) * p.dim + d) * N + g * NPT;
+      float hv[NPT];
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) hv[j] = ls.h[j];
+      if constexpr (NPT > 1) {
+        if (fast) {
+#pragma unroll
+          for (int q = 0; q < NP; ++q) unpack2(ls.hp[q], hv[2 * q], hv[2 * q + 1]);
+        }
+      }
+      if constexpr (NPT % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < NPT; j += 4)
+          *reinterpret_cast<float4*>(cp + j) = make_float4(hv[j], hv[j + 1], hv[j + 2], hv[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) cp[j] = hv[j];
+      }
+    }
     IO* const yF = PASS == 0 ? y_base + (int64_t)(i > 0 ? i - 1 : 0) * T : nullptr;
 #define SSM_ITER(FASTV, WHOLEV)                                                                  \
   chunk_iteration<IO, N, PASS, FASTV, WHOLEV>(p, ls, precise, tid, prow, c, g, sD, nrows, bufM,  \

@@ -194,3 +194,26 @@ def test_flag_word_is_checked():
     # the defined bits pass validation (empty problem: nothing is launched)
     for f in (0, ssm.SSM_SOFTPLUS, ssm.SSM_EULER_B, ssm.SSM_SOFTPLUS | ssm.SSM_EULER_B):
         assert _scan(softplus=f, batch=0) == ssm.SSM_OK
+
+
+def test_training_forward_argument_errors():
+    L_ = lib()
+
+    def tr(**kw):
+        a = dict(u=FAKE, delta=FAKE + 0x1000000, bias=None, A=FAKE + 0x2000000,
+                 B=FAKE + 0x3000000, C=FAKE + 0x4000000, D=None, z=None, softplus=1,
+                 y=FAKE + 0x5000000, h=None, batch=2, dim=64, L=128, N=16, io=ssm.SSM_BF16,
+                 init=None, ws=None, wsb=0, bws=FAKE + 0x10000000, bwsb=1 << 30)
+        a.update(kw)
+        return L_.ssm_scan_fwd_train(a["u"], a["delta"], a["bias"], a["A"], a["B"], a["C"],
+                                     a["D"], a["z"], a["softplus"], a["y"], a["h"], a["batch"],
+                                     a["dim"], a["L"], a["N"], a["io"], a["init"], a["ws"],
+                                     a["wsb"], a["bws"], a["bwsb"], None)
+
+    need = ssm.ssm_scan_bwd_workspace_bytes(2, 64, 128, 16)
+    assert tr(bws=None) == ssm.SSM_ERR_WORKSPACE
+    assert tr(bwsb=need - 16) == ssm.SSM_ERR_WORKSPACE
+    assert tr(bws=FAKE + 0x5000000) == ssm.SSM_ERR_ARG      # over y
+    assert tr(bws=FAKE + 0x10000008) == ssm.SSM_ERR_ALIGN
+    assert tr(softplus=ssm.SSM_SAVED_STATES) == ssm.SSM_ERR_ARG  # a backward-only bit
+    assert _bwd(softplus=ssm.SSM_SOFTPLUS | ssm.SSM_SAVED_STATES, u=None) == ssm.SSM_ERR_ARG
