@@ -57,6 +57,9 @@ extern "C" {
 #define SSM_EULER_B 2  /* B̄ = Δ B instead of the zero-order hold (A̅ stays exp(Δ A)) */
 #define SSM_SAVED_STATES 4 /* ssm_scan_bwd only: its workspace holds the states that
                               ssm_scan_fwd_train saved for these inputs */
+#define SSM_LAYOUT_BLD 8   /* scan, training forward, backward and conv1d: the
+                              (batch, dim, seqlen) tensors are (batch, seqlen, dim)
+                              instead (channels innermost; Algorithm 2's (B, L, D)) */
 
 /* Status codes. */
 #define SSM_OK 0
@@ -87,7 +90,8 @@ const char* ssm_version(void);
  *   delta_softplus  flag word: SSM_SOFTPLUS set: Δ = softplus(delta + bias), else
  *                   Δ = delta + bias; SSM_EULER_B set: B̄ = Δ B (the first-order
  *                   form the summary page gives beside equation (4)) instead of
- *                   the exact zero-order hold; any other bit: SSM_ERR_ARG
+ *                   the exact zero-order hold; SSM_LAYOUT_BLD set: u, delta,
+ *                   z and y are (batch, seqlen, dim); any other bit: SSM_ERR_ARG
  *   y             required output, (batch, dim, seqlen) io_dtype
  *   final_state   optional output (NULL = not written), (batch, dim, dstate) float32
  *
@@ -264,7 +268,9 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
  *
  *     out[b,d,t] = silu(bias[d] + Σ_{k<K} weight[d,k] · x[b,d,t-(K-1)+k])
  *
- * (or the bare sum with silu = 0).  x[t < 0] comes from conv_state_in, the
+ * (or the bare sum when bit 1 of `silu` is clear; `silu` may also carry
+ * SSM_LAYOUT_BLD: x and out are then (batch, seqlen, dim); the states keep
+ * their (batch, dim, width-1) layout).  x[t < 0] comes from conv_state_in, the
  * K-1 inputs before the sequence (NULL = zeros); conv_state_out (nullable)
  * receives the last K-1 inputs of (conv_state_in, x), so a sequence split
  * over calls gives the same outputs as one call.  conv_state_out may be

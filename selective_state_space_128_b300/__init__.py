@@ -22,7 +22,7 @@ SSM_F32, SSM_BF16 = 0, 1
 SSM_OK = 0
 SSM_ERR_ARG, SSM_ERR_ALIGN, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_WORKSPACE = -1, -2, -3, -4, -5
 SSM_ERR_TIMEOUT = -6
-SSM_SOFTPLUS, SSM_EULER_B, SSM_SAVED_STATES = 1, 2, 4
+SSM_SOFTPLUS, SSM_EULER_B, SSM_SAVED_STATES, SSM_LAYOUT_BLD = 1, 2, 4, 8
 
 _lib = None
 
@@ -125,10 +125,17 @@ def _check_dev(*ts):
             raise ValueError("libssm takes contiguous tensors")
 
 
-def _flags(delta_softplus, euler=False):
+def _flags(delta_softplus, euler=False, bld=False):
     """The delta_softplus flag word: a bool (softplus on/off) or the int bits
-    SSM_SOFTPLUS | SSM_EULER_B; `euler` adds SSM_EULER_B."""
-    return int(delta_softplus) | (SSM_EULER_B if euler else 0)
+    SSM_SOFTPLUS | SSM_EULER_B | SSM_LAYOUT_BLD; `euler` and `bld` add their bits."""
+    return (int(delta_softplus) | (SSM_EULER_B if euler else 0)
+            | (SSM_LAYOUT_BLD if bld else 0))
+
+
+def _sizes(u, A, B):
+    """(batch, dim, L) from A (dim, N) and B (batch, N, L): the same for both layouts
+    of u ((batch, dim, L), or (batch, L, dim) with SSM_LAYOUT_BLD)."""
+    return int(B.shape[0]), int(A.shape[0]), int(B.shape[2])
 
 
 def _call(name, rc):
@@ -144,7 +151,7 @@ def ssm_scan_fwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_s
     """Tensor form of ``ssm_scan_fwd``: sizes come from u (batch, dim, L) and A (dim, N);
     runs on the legacy default stream like the C entry point."""
     _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state)
-    batch, dim, L = u.shape
+    batch, dim, L = _sizes(u, A, B)
     N = A.shape[1]
     rc = load().ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B), _ptr(C),
                              _ptr(D), _ptr(z), _flags(delta_softplus), _ptr(y),
@@ -160,7 +167,7 @@ def ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, fina
                     init_state=None, workspace=None, workspace_bytes=None, stream=None):
     """Tensor form of ``ssm_scan_fwd_ex`` on the current torch stream (or ``stream``)."""
     _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, workspace)
-    batch, dim, L = u.shape
+    batch, dim, L = _sizes(u, A, B)
     N = A.shape[1]
     if workspace is not None and workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
@@ -179,7 +186,7 @@ def ssm_scan_fwd_train(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, f
     chunk-start states into ``bwd_workspace``)."""
     _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, workspace,
                bwd_workspace)
-    batch, dim, L = u.shape
+    batch, dim, L = _sizes(u, A, B)
     N = A.shape[1]
     rc = load().ssm_scan_fwd_train(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
                                    _ptr(C), _ptr(D), _ptr(z), _flags(delta_softplus), _ptr(y),
@@ -226,7 +233,7 @@ def ssm_scan_fwd_noalloc(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y,
     for callers that cannot allocate device memory.  Calls that may overlap on the GPU
     share that array and must be ordered (e.g. issued on one stream)."""
     _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state)
-    batch, dim, L = u.shape
+    batch, dim, L = _sizes(u, A, B)
     N = A.shape[1]
     rc = load().ssm_scan_fwd_noalloc(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
                                      _ptr(C), _ptr(D), _ptr(z), _flags(delta_softplus),
@@ -245,7 +252,7 @@ def ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, init_state
     """Tensor form of ``ssm_scan_bwd`` on the current torch stream (or ``stream``)."""
     _check_dev(u, delta, delta_bias, A, B, C, D, z, init_state, dy, d_final_state, du, ddelta,
                dA, dB, dC, dD, dz, d_delta_bias, d_init_state, workspace)
-    batch, dim, L = u.shape
+    batch, dim, L = _sizes(u, A, B)
     N = A.shape[1]
     if workspace is not None and workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
@@ -261,9 +268,10 @@ def ssm_scan_bwd(u, delta, delta_bias, A, B, C, D, z, delta_softplus, init_state
 def ssm_conv1d_fwd(x, weight, bias, conv_state_in, silu, out, conv_state_out, stream=None):
     """Tensor form of ``ssm_conv1d_fwd``: x (batch, dim, L), weight (dim, width)."""
     _check_dev(x, weight, bias, conv_state_in, out, conv_state_out)
-    batch, dim, L = x.shape
+    batch = x.shape[0]
+    dim, L = (x.shape[2], x.shape[1]) if int(silu) & SSM_LAYOUT_BLD else (x.shape[1], x.shape[2])
     rc = load().ssm_conv1d_fwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state_in),
-                               int(bool(silu)), _ptr(out), _ptr(conv_state_out), batch, dim, L,
+                               int(silu), _ptr(out), _ptr(conv_state_out), batch, dim, L,
                                weight.shape[1], _io_dtype(x), _stream(stream))
     _call("ssm_conv1d_fwd", rc)
 
@@ -290,11 +298,11 @@ def static_scratch_bytes() -> int:
 # ---------------------------------------------------------------------------
 
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-         init_state=None, split=True, stream=None, euler=False):
+         init_state=None, split=True, stream=None, euler=False, bld=False):
     """y, final_state = scan(...): allocates y (dtype of u) and final_state (float32), and a
     workspace when the plan splits the sequence across blocks."""
     import torch
-    batch, dim, L = u.shape
+    batch, dim, L = _sizes(u, A, B)
     N = A.shape[1]
     y = torch.empty_like(u)
     h = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device)
@@ -303,17 +311,17 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True
         nbytes = ssm_scan_workspace_bytes(batch, dim, L, N, _io_dtype(u))
         if nbytes:
             ws = torch.empty(nbytes, dtype=torch.uint8, device=u.device)
-    ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler), y, h,
-                    init_state, ws, stream=stream)
+    ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler, bld), y,
+                    h, init_state, ws, stream=stream)
     return y, h
 
 
 def scan_train(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-               init_state=None, stream=None, euler=False):
+               init_state=None, stream=None, euler=False, bld=False):
     """y, final_state, saved = scan_train(...): the forward of ``scan`` that also keeps
     what the backward needs; pass ``saved`` to ``scan_bwd(..., saved=saved)``."""
     import torch
-    batch, dim, L = u.shape
+    batch, dim, L = _sizes(u, A, B)
     N = A.shape[1]
     y = torch.empty_like(u)
     h = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device)
@@ -321,20 +329,20 @@ def scan_train(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplu
     ws = torch.empty(nbytes, dtype=torch.uint8, device=u.device) if nbytes else None
     bbytes = ssm_scan_bwd_workspace_bytes(batch, dim, L, N)
     bws = torch.empty(max(bbytes, 16), dtype=torch.uint8, device=u.device)
-    ssm_scan_fwd_train(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler), y, h,
-                       init_state, ws, nbytes, bws, bbytes, stream)
+    ssm_scan_fwd_train(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler, bld),
+                       y, h, init_state, ws, nbytes, bws, bbytes, stream)
     return y, h, bws
 
 
 def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
              init_state=None, dy=None, d_final_state=None, want_init_grad=False, stream=None,
-             euler=False, saved=None):
+             euler=False, saved=None, bld=False):
     """Derivatives of Σ y·dy + Σ final_state·d_final_state for the inputs of ``scan``.
     Allocates every output and the workspace; returns a dict with du, ddelta, dz (dtype of
     u; dz None without z), dA, dB, dC, dD, dbias (float32; dD / dbias always computed) and
     dinit (float32, when ``want_init_grad``)."""
     import torch
-    batch, dim, L = u.shape
+    batch, dim, L = _sizes(u, A, B)
     N = A.shape[1]
     dev = u.device
     f32 = dict(dtype=torch.float32, device=dev)
@@ -345,7 +353,7 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
                dbias=torch.empty(dim, **f32),
                dinit=torch.empty((batch, dim, N), **f32) if want_init_grad else None)
     nbytes = ssm_scan_bwd_workspace_bytes(batch, dim, L, N)
-    flags = _flags(delta_softplus, euler)
+    flags = _flags(delta_softplus, euler, bld)
     if saved is not None:
         ws = saved
         flags |= SSM_SAVED_STATES
@@ -357,15 +365,19 @@ def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     return out
 
 
-def conv1d(x, weight, bias=None, conv_state=None, silu=True, want_state=False, stream=None):
-    """out[, new_state] = conv1d(...): causal depthwise conv1d (+ SiLU) of x (batch, dim, L);
-    conv_state (batch, dim, width-1) holds the inputs before the sequence."""
+def conv1d(x, weight, bias=None, conv_state=None, silu=True, want_state=False, stream=None,
+           bld=False):
+    """out[, new_state] = conv1d(...): causal depthwise conv1d (+ SiLU) of x (batch, dim, L),
+    or (batch, L, dim) with ``bld``; conv_state (batch, dim, width-1) holds the inputs
+    before the sequence."""
     import torch
     out = torch.empty_like(x)
     st = None
     if want_state:
-        st = torch.empty(x.shape[:2] + (weight.shape[1] - 1,), dtype=x.dtype, device=x.device)
-    ssm_conv1d_fwd(x, weight, bias, conv_state, silu, out, st, stream)
+        st = torch.empty((x.shape[0], weight.shape[0], weight.shape[1] - 1), dtype=x.dtype,
+                         device=x.device)
+    ssm_conv1d_fwd(x, weight, bias, conv_state, int(bool(silu)) | (SSM_LAYOUT_BLD if bld else 0),
+                   out, st, stream)
     return (out, st) if want_state else out
 
 

@@ -77,7 +77,8 @@ int scan_fwd_impl(const void* u, const void* delta, const float* delta_bias, con
                   void* workspace, size_t workspace_bytes, void* bwd_workspace,
                   size_t bwd_workspace_bytes, bool train, void* stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
-  if (!flags_ok(delta_softplus)) return SSM_ERR_ARG;
+  if (!flags_ok(delta_softplus & ~SSM_LAYOUT_BLD)) return SSM_ERR_ARG;
+  const bool bld = (delta_softplus & SSM_LAYOUT_BLD) != 0;
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   const bool work = batch > 0 && dim > 0;
@@ -139,7 +140,9 @@ int scan_fwd_impl(const void* u, const void* delta, const float* delta_bias, con
   a.nseg = plan.nseg; a.seg_len = plan.seg_len;
   a.softplus = (delta_softplus & SSM_SOFTPLUS) != 0;
   a.euler = (delta_softplus & SSM_EULER_B) != 0;
-  a.vec_io = (seqlen * (int64_t)esz) % 16 == 0;
+  a.bld = bld;
+  // 16-byte rows: of L steps, or of dim channels in the (batch, L, dim) layout
+  a.vec_io = ((bld ? dim : seqlen) * (int64_t)esz) % 16 == 0;
   a.vec_bc = (seqlen * 4) % 16 == 0;
   a.force_precise = io_dtype == SSM_F32;
   if (plan.nseg > 1) {
@@ -245,7 +248,7 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
                  int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                  void* workspace, size_t workspace_bytes, void* stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
-  if (!flags_ok(delta_softplus & ~SSM_SAVED_STATES)) return SSM_ERR_ARG;
+  if (!flags_ok(delta_softplus & ~(SSM_SAVED_STATES | SSM_LAYOUT_BLD))) return SSM_ERR_ARG;
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   if (dz && !z) return SSM_ERR_ARG;
@@ -313,6 +316,7 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
   a.ws_D = reinterpret_cast<float*>(ws + lay.o_D);
   a.ws_bias = reinterpret_cast<float*>(ws + lay.o_bias);
   a.batch = batch; a.dim = dim; a.L = seqlen; a.nblk = lay.nblk;
+  a.bld = (delta_softplus & SSM_LAYOUT_BLD) != 0;
   // saved states are used where the training forward saves them (same chunk length)
   a.saved = (delta_softplus & SSM_SAVED_STATES) != 0 &&
             ssm::bwd_chunk(dstate) ==
@@ -329,6 +333,7 @@ int ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
                    int64_t batch, int64_t dim, int64_t seqlen, int64_t width, int io_dtype,
                    void* stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if ((silu & ~(1 | SSM_LAYOUT_BLD)) != 0) return SSM_ERR_ARG;
   if (!sizes_ok(batch, dim, seqlen) || width <= 0) return SSM_ERR_ARG;
   if (width > 4) return SSM_ERR_UNSUPPORTED;
   const bool rows = batch > 0 && dim > 0;
@@ -355,7 +360,8 @@ int ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
   a.x = x; a.w = weight; a.bias = bias; a.state_in = conv_state_in; a.out = out;
   a.state_out = width > 1 ? conv_state_out : nullptr;
   a.batch = batch; a.dim = dim; a.L = seqlen;
-  a.silu = silu != 0;
+  a.silu = (silu & 1) != 0;
+  a.bld = (silu & SSM_LAYOUT_BLD) != 0;
   a.precise = io_dtype == SSM_F32;
   const cudaError_t e = ssm::conv_launch(a, width, io_dtype, false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

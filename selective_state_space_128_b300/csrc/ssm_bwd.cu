@@ -213,11 +213,16 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
   // this thread's row and steps in the per-step (cooperative) phases
   const int r = tid / TPR, te = (tid % TPR) * E;
   const bool row_ok = r < nrows;
-  const int64_t io_row = (b * p.dim + d0 + (row_ok ? r : 0)) * L;
+  // element (this row, step t) of u/Δ/z/dy and their derivatives is at
+  // io_row + t * io_ts: rows of L steps, or steps dim apart in (batch, L, dim)
+  const bool bld = p.bld != 0;
+  const int64_t io_row = bld ? b * L * p.dim + d0 + (row_ok ? r : 0)
+                             : (b * p.dim + d0 + (row_ok ? r : 0)) * L;
+  const int64_t io_ts = bld ? p.dim : 1;
   // E-step runs as vectors: vecio moves 4 bf16 as 8 bytes and 8 or 16 bf16 (or
   // 4+ floats) as 16-byte accesses, so every row must start on that boundary
   constexpr int kVecBytes = (sizeof(IO) == 2 && E == 4) ? 8 : 16;
-  const bool vec = E % 4 == 0 && (L * (int64_t)sizeof(IO)) % kVecBytes == 0;
+  const bool vec = !bld && E % 4 == 0 && (L * (int64_t)sizeof(IO)) % kVecBytes == 0;
 
   for (int i = tid; i < CH; i += kBwdThreads) {
     const bool ok = d0 + i < p.dim;
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
   auto fetch = [&](int k, bool full, BwdPre<N>& pr) {
     const int64_t t0 = (int64_t)k * T;
     const int tc = (int)min64(T, L - t0);
-    const int64_t gi = io_row + t0 + te;
+    const int64_t gi = io_row + (t0 + te) * io_ts;
     bool done = false;
     if constexpr (E % 4 == 0) {
       if (row_ok && vec && te + E <= tc) {
@@ -268,11 +273,12 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
 #pragma unroll
       for (int j = 0; j < E; ++j) {
         const bool ok = row_ok && te + j < tc;
-        pr.dl[j] = ok ? ld_io<IO>(p.delta, gi + j) : 0.f;
-        pr.u[j] = ok ? ld_io<IO>(p.u, gi + j) : 0.f;
+        const int64_t gj = gi + j * io_ts;
+        pr.dl[j] = ok ? ld_io<IO>(p.delta, gj) : 0.f;
+        pr.u[j] = ok ? ld_io<IO>(p.u, gj) : 0.f;
         if (full) {
-          pr.dy[j] = ok ? ld_io<IO>(p.dy, gi + j) : 0.f;
-          pr.z[j] = (ok && p.z) ? ld_io<IO>(p.z, gi + j) : 0.f;
+          pr.dy[j] = ok ? ld_io<IO>(p.dy, gj) : 0.f;
+          pr.z[j] = (ok && p.z) ? ld_io<IO>(p.z, gj) : 0.f;
         }
       }
     }
@@ -532,7 +538,7 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
         }
       }
       if (p.z && row_ok) {
-        IO* dzp = static_cast<IO*>(p.dz) + io_row + t0 + te;
+        IO* dzp = static_cast<IO*>(p.dz) + io_row + (t0 + te) * io_ts;
         bool done = false;
         if constexpr (E % 4 == 0) {
           if (vec && te + E <= tc) {
@@ -543,7 +549,7 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
         if (!done) {
 #pragma unroll
           for (int j = 0; j < E; ++j)
-            if (te + j < tc) dzp[j] = io_traits<IO>::from_f32(sp_[j]);
+            if (te + j < tc) dzp[j * io_ts] = io_traits<IO>::from_f32(sp_[j]);
         }
       }
       // dC[t][n] = Σ_c ds[c][t] h_t[c][n]
@@ -705,8 +711,8 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
         if (te + j < tc) dbias_acc += dd_[j];
       }
       if (row_ok) {
-        IO* dup = static_cast<IO*>(p.du) + io_row + t0 + te;
-        IO* ddp = static_cast<IO*>(p.ddelta) + io_row + t0 + te;
+        IO* dup = static_cast<IO*>(p.du) + io_row + (t0 + te) * io_ts;
+        IO* ddp = static_cast<IO*>(p.ddelta) + io_row + (t0 + te) * io_ts;
         bool done = false;
         if constexpr (E % 4 == 0) {
           if (vec && te + E <= tc) {
@@ -719,8 +725,8 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
 #pragma unroll
           for (int j = 0; j < E; ++j) {
             if (te + j < tc) {
-              dup[j] = io_traits<IO>::from_f32(du_[j]);
-              ddp[j] = io_traits<IO>::from_f32(dd_[j]);
+              dup[j * io_ts] = io_traits<IO>::from_f32(du_[j]);
+              ddp[j * io_ts] = io_traits<IO>::from_f32(dd_[j]);
             }
           }
         }

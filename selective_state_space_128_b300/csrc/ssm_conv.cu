@@ -142,6 +142,65 @@ __global__ void __launch_bounds__(256, 8) conv1d_wide_kernel(const ConvArgs p) {
   }
 }
 
+// (batch, L, dim) layout, dim a multiple of one 16-byte vector: a thread
+// produces VE consecutive channels of one step from the K input vectors of
+// steps t-K+1..t (rows of neighbouring threads overlap: L1 hits).
+template <typename IO, int K>
+__global__ void __launch_bounds__(256) conv1d_bld_vec_kernel(const ConvArgs p) {
+  constexpr int VE = Vec16<IO>::n;
+  const int64_t nv = p.dim / VE;  // vectors per step
+  const int64_t total = p.batch * p.L * nv;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t bt = v / nv, j = v - bt * nv;
+    const int64_t b = bt / p.L, t = bt - b * p.L;
+    const int64_t d0 = j * VE;
+    float acc[VE];
+#pragma unroll
+    for (int i = 0; i < VE; ++i) acc[i] = p.bias ? __ldg(p.bias + d0 + i) : 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int64_t s = t - (K - 1) + k;
+      float xv[VE];
+      if (s >= 0) {
+        Vec16<IO>::load(static_cast<const IO*>(p.x) + (b * p.L + s) * p.dim + d0, xv);
+      } else {
+        const IO* st = static_cast<const IO*>(p.state_in);
+#pragma unroll
+        for (int i = 0; i < VE; ++i)
+          xv[i] = st ? io_traits<IO>::to_f32(st[((b * p.dim) + d0 + i) * (K - 1) + (K - 1 + s)]) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < VE; ++i) acc[i] = fmaf(__ldg(p.w + (d0 + i) * K + k), xv[i], acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < VE; ++i) acc[i] = conv_act(acc[i], p.silu, p.precise);
+    Vec16<IO>::store(static_cast<IO*>(p.out) + (b * p.L + t) * p.dim + d0, acc);
+  }
+}
+
+// (batch, L, dim) layout, any dim: one output per thread.
+template <typename IO, int K>
+__global__ void __launch_bounds__(256) conv1d_bld_scalar_kernel(const ConvArgs p) {
+  const int64_t total = p.batch * p.dim * p.L;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t bt = e / p.dim, d = e - bt * p.dim;
+    const int64_t b = bt / p.L, t = bt - b * p.L;
+    const IO* st = p.state_in ? static_cast<const IO*>(p.state_in) + (b * p.dim + d) * (K - 1)
+                              : nullptr;
+    float acc = p.bias ? __ldg(p.bias + d) : 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int64_t s = t - (K - 1) + k;
+      const float xv = s >= 0 ? io_traits<IO>::to_f32(static_cast<const IO*>(p.x)[(b * p.L + s) * p.dim + d])
+                              : (st ? io_traits<IO>::to_f32(st[K - 1 + s]) : 0.f);
+      acc = fmaf(__ldg(p.w + d * K + k), xv, acc);
+    }
+    static_cast<IO*>(p.out)[e] = io_traits<IO>::from_f32(conv_act(acc, p.silu, p.precise));
+  }
+}
+
 // Any row length: one output per thread.
 template <typename IO, int K>
 __global__ void __launch_bounds__(256) conv1d_scalar_kernel(const ConvArgs p) {
@@ -171,13 +230,16 @@ __global__ void conv1d_state_kernel(const ConvArgs p) {
   const int64_t rows = p.batch * p.dim;
   for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < rows;
        row += (int64_t)gridDim.x * blockDim.x) {
-    const IO* xr = static_cast<const IO*>(p.x) + row * p.L;
+    // input step s of this row: row * L + s, or (b * L + s) * dim + d in (batch, L, dim)
+    const int64_t b = row / p.dim, d = row - b * p.dim;
+    const IO* x = static_cast<const IO*>(p.x);
     const IO* st = p.state_in ? static_cast<const IO*>(p.state_in) + row * (K - 1) : nullptr;
     IO v[K > 1 ? K - 1 : 1];
 #pragma unroll
     for (int j = 0; j < K - 1; ++j) {
       const int64_t s = p.L - (K - 1) + j;
-      v[j] = s >= 0 ? xr[s] : (st ? st[K - 1 + s] : io_traits<IO>::from_f32(0.f));
+      const int64_t xi = p.bld ? (b * p.L + s) * p.dim + d : row * p.L + s;
+      v[j] = s >= 0 ? x[xi] : (st ? st[K - 1 + s] : io_traits<IO>::from_f32(0.f));
     }
     IO* so = static_cast<IO*>(p.state_out) + row * (K - 1);
 #pragma unroll
@@ -222,7 +284,14 @@ static cudaError_t conv_typed(const ConvArgs& a, bool update, cudaStream_t s) {
   }
   constexpr int VE = Vec16<IO>::n;
   const int64_t rows = a.batch * a.dim;
-  if (a.L > 0) {
+  if (a.L > 0 && a.bld) {
+    if (a.dim % VE == 0)
+      conv1d_bld_vec_kernel<IO, K><<<grid_for(a.batch * a.L * (a.dim / VE), 256), 256, 0, s>>>(a);
+    else
+      conv1d_bld_scalar_kernel<IO, K><<<grid_for(rows * a.L, 256), 256, 0, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else if (a.L > 0) {
     constexpr int VPT = 2;
     if (a.L % (VE * VPT) == 0) {
       const int64_t threads = rows * (a.L / (VE * VPT));

@@ -31,7 +31,8 @@ struct ScanArgs {
   int64_t seg_len;  // steps per segment, a multiple of the chunk length
   int nseg;
   int softplus;
-  int vec_io;       // rows of u/delta/z/y are 16-byte aligned
+  int vec_io;       // rows of u/delta/z/y (L steps, or dim channels with bld) are 16-byte aligned
+  int bld;          // u/delta/z/y are (batch, L, dim) instead of (batch, dim, L)
   int vec_bc;       // rows of B/C are 16-byte aligned
   int force_precise;
   int euler;        // B̄ = Δ B (runs on the precise flavour)
@@ -116,6 +117,7 @@ struct BwdArgs {
   int force_precise;
   int euler;
   int saved;  // ckpt already holds the chunk-start states (a training forward wrote them)
+  int bld;    // u/delta/z/dy/du/ddelta/dz are (batch, L, dim)
 };
 
 // Chunk length of the backward pass for state size N (the checkpoint interval).
@@ -145,6 +147,7 @@ struct ConvArgs {
   int64_t batch, dim, L;
   bool silu;
   bool precise;
+  bool bld;  // x and out are (batch, L, dim)
 };
 
 // Enqueue the conv pass (update = false: over a sequence, then the new state)

@@ -150,12 +150,14 @@ __device__ __forceinline__ void issue_chunk(const ScanArgs& p, const ScanMaps& m
   const bool has_z = PASS == 0 && p.z != nullptr;
   const uint32_t bytes = (uint32_t)(S::kRawIO * (has_z ? 3 : 2) + S::kRawBC * (PASS == 0 ? 2 : 1));
   mbar_arrive_expect_tx(bar, bytes);
-  const int x = (int)t0, y = (int)d0, z = (int)b;
+  // u/Δ/z boxes: (T steps, CH channels) of a (batch, dim, L) tensor, or
+  // (CH channels, T steps) of a (batch, L, dim) one -- the stage is then [t][c]
+  const int x = p.bld ? (int)d0 : (int)t0, y = p.bld ? (int)t0 : (int)d0, z = (int)b;
   tma_load_3d(stage + S::oRawU, &m.u, bar, x, y, z);
   tma_load_3d(stage + S::oRawD, &m.d, bar, x, y, z);
   if (has_z) tma_load_3d(stage + S::oRawZ, &m.z, bar, x, y, z);
-  tma_load_3d(stage + S::oRawB, &m.b, bar, x, 0, z);
-  if (PASS == 0) tma_load_3d(stage + S::oRawC, &m.c, bar, x, 0, z);
+  tma_load_3d(stage + S::oRawB, &m.b, bar, (int)t0, 0, z);
+  if (PASS == 0) tma_load_3d(stage + S::oRawC, &m.c, bar, (int)t0, 0, z);
 }
 
 // Without TMA (rows not 16-byte aligned): all threads copy one chunk into a
@@ -168,9 +170,11 @@ __device__ __forceinline__ void load_chunk_plain(const ScanArgs& p, unsigned cha
   const bool has_z = PASS == 0 && p.z != nullptr;
   const IO zero = io_traits<IO>::from_f32(0.f);
   for (int e = tid; e < CH * T; e += kScanThreads) {
-    const int r = e / T, t = e - r * T;
+    // stage element e is (row r, step t): [r][t], or [t][r] for the (batch, L, dim) layout
+    const int r = p.bld ? e % CH : e / T, t = p.bld ? e / CH : e - (e / T) * T;
     const bool ok = d0 + r < p.dim && t0 + t < p.L;
-    const int64_t gi = ((b * p.dim + d0 + r) * p.L + t0 + t);
+    const int64_t gi = p.bld ? (b * p.L + t0 + t) * p.dim + d0 + r
+                             : ((b * p.dim + d0 + r) * p.L + t0 + t);
     reinterpret_cast<IO*>(stage + S::oRawU)[e] = ok ? static_cast<const IO*>(p.u)[gi] : zero;
     reinterpret_cast<IO*>(stage + S::oRawD)[e] = ok ? static_cast<const IO*>(p.delta)[gi] : zero;
     if (has_z) reinterpret_cast<IO*>(stage + S::oRawZ)[e] = ok ? static_cast<const IO*>(p.z)[gi] : zero;
@@ -188,7 +192,7 @@ __device__ __forceinline__ void load_chunk_plain(const ScanArgs& p, unsigned cha
 // (fast arithmetic, softplus on, gate present); otherwise they are read at run
 // time.
 struct StepFlags {
-  bool precise, softplus, gate;
+  bool precise, softplus, gate, bld;
 };
 
 // This thread's share of converting a raw stage into a working buffer: E
@@ -216,9 +220,22 @@ __device__ __forceinline__ void prep_compute(const unsigned char* stage, const f
   const bool hz = PASS == 0 && (FAST ? true : f.gate);
   const int r = tid / (T / E), te = (tid - r * (T / E)) * E;
   float dl[E], zz[E];
-  vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawD) + r * T + te, dl);
-  vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawU) + r * T + te, v.u);
-  if (hz) vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawZ) + r * T + te, zz);
+  if (!f.bld) {
+    vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawD) + r * T + te, dl);
+    vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawU) + r * T + te, v.u);
+    if (hz) vecio<IO, E>::load(reinterpret_cast<const IO*>(stage + S::oRawZ) + r * T + te, zz);
+  } else {
+    // [t][c] stage: the row's steps are CH elements apart
+    const IO* sD = reinterpret_cast<const IO*>(stage + S::oRawD) + te * S::CH + r;
+    const IO* sU = reinterpret_cast<const IO*>(stage + S::oRawU) + te * S::CH + r;
+    const IO* sZ = reinterpret_cast<const IO*>(stage + S::oRawZ) + te * S::CH + r;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      dl[j] = io_traits<IO>::to_f32(sD[j * S::CH]);
+      v.u[j] = io_traits<IO>::to_f32(sU[j * S::CH]);
+      if (hz) zz[j] = io_traits<IO>::to_f32(sZ[j * S::CH]);
+    }
+  }
   const float bias = sBias[r];
 #pragma unroll
   for (int j = 0; j < E; ++j) {
@@ -317,6 +334,15 @@ __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned
     const float gg[4] = {gk.x, gk.y, gk.z, gk.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) y[4 * k + j] = fmaf(Dd, Ut[4 * k + j], acc[4 * k + j]) * gg[j];
+  }
+  if (p.bld) {
+    // (batch, L, dim) layout: this row's steps are dim elements apart
+    if (store && r < nrows) {
+#pragma unroll
+      for (int j = 0; j < E; ++j)
+        if (WHOLE || te + j < tcount) dst[(int64_t)j * p.dim] = io_traits<IO>::from_f32(y[j]);
+    }
+    return;
   }
   if constexpr (WHOLE) {
     if (store && r < nrows) vecio<IO, E>::store(dst, y);
@@ -585,9 +611,12 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
   auto t0_of = [&](int k) { return t_begin + (int64_t)k * T; };
   // this thread's first output of a chunk in HBM, for the finalisation
   const int fr = tid / (T / Cf::E), fte = (tid - fr * (T / Cf::E)) * Cf::E;
-  IO* const y_base = PASS == 0 ? static_cast<IO*>(p.y) + ((b * p.dim + d0 + min(fr, nrows - 1)) * p.L +
-                                                          t_begin + fte)
-                               : nullptr;
+  const int64_t fr_c = d0 + min(fr, nrows - 1);  // the finalised row's channel (clamped)
+  IO* const y_base =
+      PASS == 0 ? static_cast<IO*>(p.y) + (p.bld ? (b * p.L + t_begin + fte) * p.dim + fr_c
+                                                 : (b * p.dim + fr_c) * p.L + t_begin + fte)
+                : nullptr;
+  const int64_t y_chunk = p.bld ? (int64_t)T * p.dim : (int64_t)T;  // y offset per chunk
 
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(sm + S::oBar);
   uint64_t* iter_bar = raw_full + NS;
@@ -619,7 +648,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
   }
   // the precise flavour: fp32 I/O, a channel with A = 0, or the Euler B̄
   const bool precise = __syncthreads_or(zeroA) || p.force_precise || p.euler;
-  const StepFlags fl{precise, p.softplus != 0, p.z != nullptr};
+  const StepFlags fl{precise, p.softplus != 0, p.z != nullptr, p.bld != 0};
   const bool fast = !precise && fl.softplus && (PASS == 1 || fl.gate);
 
   // the first NS chunks in flight
@@ -710,7 +739,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     const int tcN = has_next ? tcount_of(i + 1) : 0;
     const int tcF = i > 0 ? tcount_of(i - 1) : T;
     // steady state: both neighbouring chunks whole and rows 16-byte aligned
-    const bool whole = p.vec_io && tcN == T && tcF == T;
+    const bool whole = (p.vec_io || p.bld) && tcN == T && tcF == T;
     unsigned char* const bufM = sm + S::oBuf + bcur * S::kBuf;
     unsigned char* const bufN = sm + S::oBuf + bnext * S::kBuf;
     unsigned char* const bufF = sm + S::oBuf + bprev * S::kBuf;
@@ -771,7 +800,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
         for (int j = 0; j < NPT; ++j) cp[j] = hv[j];
       }
     }
-    IO* const yF = PASS == 0 ? y_base + (int64_t)(i > 0 ? i - 1 : 0) * T : nullptr;
+    IO* const yF = PASS == 0 ? y_base + (int64_t)(i > 0 ? i - 1 : 0) * y_chunk : nullptr;
 #define SSM_ITER(FASTV, WHOLEV)                                                                  \
   chunk_iteration<IO, N, PASS, FASTV, WHOLEV>(p, ls, precise, tid, prow, c, g, sD, nrows, bufM,  \
                                              partM, pv, bufN, bufF, partF, yF, tcF, i > 0)
@@ -808,7 +837,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
   }
   if (PASS == 0 && nchunks > 0) {
     const int f = nchunks - 1;
-    finalize_share<IO, N, false>(p, buf_of(f), part_of(f), sD, tid, y_base + (int64_t)f * T,
+    finalize_share<IO, N, false>(p, buf_of(f), part_of(f), sD, tid, y_base + (int64_t)f * y_chunk,
                                  tcount_of(f), nrows, true);
   }
 
@@ -925,11 +954,14 @@ static bool make_maps(ScanMaps& m, const ScanArgs& a) {
   const CUtensorMapDataType dt =
       sizeof(IO) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const uint64_t L = (uint64_t)a.L, D = (uint64_t)a.dim, Bt = (uint64_t)a.batch;
-  bool ok = make_map(&m.u, a.u, dt, sizeof(IO), L, D, Bt, Cf::T, Cf::CH) &&
-            make_map(&m.d, a.delta, dt, sizeof(IO), L, D, Bt, Cf::T, Cf::CH) &&
+  // u/Δ/z: (batch, dim, L) with (T, CH) boxes, or (batch, L, dim) with (CH, T) boxes
+  const uint64_t i0 = a.bld ? D : L, i1 = a.bld ? L : D;
+  const uint32_t b0 = a.bld ? Cf::CH : Cf::T, b1 = a.bld ? Cf::T : Cf::CH;
+  bool ok = make_map(&m.u, a.u, dt, sizeof(IO), i0, i1, Bt, b0, b1) &&
+            make_map(&m.d, a.delta, dt, sizeof(IO), i0, i1, Bt, b0, b1) &&
             make_map(&m.b, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, N, Bt, Cf::T, N) &&
             make_map(&m.c, a.C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, N, Bt, Cf::T, N);
-  if (ok && a.z) ok = make_map(&m.z, a.z, dt, sizeof(IO), L, D, Bt, Cf::T, Cf::CH);
+  if (ok && a.z) ok = make_map(&m.z, a.z, dt, sizeof(IO), i0, i1, Bt, b0, b1);
   return ok;
 }
 
@@ -961,6 +993,7 @@ static cudaError_t launch_typed(ScanArgs a, cudaStream_t stream) {
   memset(&m, 0, sizeof m);
   // TMA needs 16-byte row strides (rows of u/Δ/z and B/C) and coordinates
   // that fit in int32
+  // (in the (batch, L, dim) layout the caller sets vec_io from the dim rows)
   const bool rows16 = a.vec_io && a.vec_bc;
   const bool fits = a.L < (int64_t(1) << 31) && a.dim < (int64_t(1) << 31);
   a.use_tma = rows16 && fits && make_maps<IO, N>(m, a);
