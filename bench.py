@@ -283,6 +283,39 @@ def bench_scan(w, steps, warmup, world):
 
 
 # ---------------------------------------------------------------------------
+# the same scan with u/delta/z/y in the (batch, L, dim) layout
+# ---------------------------------------------------------------------------
+
+def bench_scan_bld(w, g, steps, warmup, world):
+    """Per-launch time of the scan on the transposed (batch, L, dim) copies of the
+    workload's inputs (one copy: 204 MB, larger than L2)."""
+    import torch
+    import selective_state_space_128_b300 as ssm
+    t = {k: g[k].transpose(1, 2).contiguous() for k in ("u", "delta", "z")}
+    y = torch.empty_like(t["u"])
+    h = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    flags = ssm.SSM_SOFTPLUS | ssm.SSM_LAYOUT_BLD
+
+    def step():
+        ssm.ssm_scan_fwd_ex(t["u"], t["delta"], g["delta_bias"], g["A"], g["B"], g["C"], g["D"],
+                            t["z"], flags, y, h, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return max_over_ranks(world, e0.elapsed_time(e1)) / steps
+
+
+# ---------------------------------------------------------------------------
 # front end: causal conv1d (d_conv 4) + SiLU over the same layer's input
 # ---------------------------------------------------------------------------
 
@@ -543,6 +576,7 @@ def main():
     r = bench_scan(w, args.steps, args.warmup, world)
     bwd = None if args.no_bwd else bench_backward(w, r["inputs"], args.bwd_steps, args.warmup,
                                                   world)
+    bld_ms = bench_scan_bld(w, r["inputs"], 50, args.warmup, world)
     r.pop("inputs")
     conv = None if args.no_conv else bench_conv(w, 50, args.warmup, world)
     dec = None if args.no_decode else bench_decode(synth.DECODE, args.decode_steps, world)
@@ -607,6 +641,10 @@ def main():
                             "gpu_launches": 2 * bwd["steps"],
                             "l2": "u, delta, z, dy: 4 x %.0f MB, larger than L2"
                                   % (w.channel_steps * 2 / 1e6)}
+    line["scan_bld_layout"] = {"us_per_step": bld_ms * 1e3,
+                               "channel_steps_per_s": w.channel_steps / (bld_ms / 1e3) * world,
+                               "layout": "u, delta, z, y as (batch, L, d_inner)", "steps": 50,
+                               "gpu_launches": 50}
     if conv is not None:
         cs = conv["step_ms"] / 1e3
         line["conv1d"] = {"workload": "conv1d_silu d_conv 4 on %d x %d x %d bf16" % (
