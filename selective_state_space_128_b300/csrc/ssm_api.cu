@@ -10,8 +10,12 @@ namespace {
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool supported_n(int64_t n) {
-  return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
+  return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64 || n == 128;
 }
+
+// the backward keeps NPT states per lane and its recomputed chunk in shared
+// memory; it is built for dstate up to 64
+bool supported_bwd_n(int64_t n) { return supported_n(n) && n <= 64; }
 
 // [p, p + bytes) and [q, q + qbytes) intersect (null never does)
 bool overlaps(const void* p, size_t bytes, const void* q, size_t qbytes) {
@@ -48,7 +52,9 @@ const char* ssm_strerror(int status) {
     case SSM_OK: return "SSM_OK";
     case SSM_ERR_ARG: return "SSM_ERR_ARG: invalid argument";
     case SSM_ERR_ALIGN: return "SSM_ERR_ALIGN: pointer not 16-byte aligned";
-    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: dstate not in {1,2,4,8,16,32,64}";
+    case SSM_ERR_UNSUPPORTED:
+      return "SSM_ERR_UNSUPPORTED: dstate not in {1,2,4,8,16,32,64,128} (backward: up to 64), "
+             "or conv width not in 1..4";
     case SSM_ERR_CUDA: return "SSM_ERR_CUDA: CUDA launch failed";
     case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE: workspace too small";
     case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT: a kernel gave up waiting for its data";
@@ -210,9 +216,11 @@ int ssm_state_update_ex(float* state, const void* u, const void* delta, const fl
   const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
   const size_t nio = (size_t)batch * (size_t)dim * esz;
   const size_t nst = (size_t)batch * (size_t)dim * (size_t)dstate * 4;
+  const size_t nbc = (size_t)batch * (size_t)dstate * 4, nA = (size_t)dim * (size_t)dstate * 4;
   const void* ins[] = {u, delta, z, B, C, A};
-  for (const void* q : ins)
-    if (overlaps(state, nst, q, q == A ? (size_t)dim * dstate * 4 : nio)) return SSM_ERR_ARG;
+  const size_t in_bytes[] = {nio, nio, nio, nbc, nbc, nA};
+  for (int k = 0; k < 6; ++k)
+    if (overlaps(state, nst, ins[k], in_bytes[k])) return SSM_ERR_ARG;
   if (overlaps(y, nio, state, nst) || overlaps(y, nio, u, nio) || overlaps(y, nio, delta, nio) ||
       overlaps(y, nio, z, nio))
     return SSM_ERR_ARG;
@@ -235,7 +243,7 @@ int ssm_state_update(float* state, const void* u, const void* delta, const float
 }
 
 size_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
-  if (!supported_n(dstate) || !sizes_ok(batch, dim, seqlen)) return 0;
+  if (!supported_bwd_n(dstate) || !sizes_ok(batch, dim, seqlen)) return 0;
   if (batch == 0 || dim == 0 || seqlen == 0) return 0;
   return ssm::bwd_layout(batch, dim, seqlen, dstate).bytes;
 }
@@ -250,7 +258,7 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
   if (!flags_ok(delta_softplus & ~(SSM_SAVED_STATES | SSM_LAYOUT_BLD))) return SSM_ERR_ARG;
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
-  if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
+  if (!supported_bwd_n(dstate)) return SSM_ERR_UNSUPPORTED;
   if (dz && !z) return SSM_ERR_ARG;
   const bool rows = batch > 0 && dim > 0;
   const bool steps = rows && seqlen > 0;

@@ -162,14 +162,20 @@ __device__ __forceinline__ float softplus_precise(float x) {
   return x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
 }
 
-// E consecutive I/O elements <-> float, as 8-, 16- or 32-byte accesses (the
-// caller guarantees the alignment).
+// E consecutive I/O elements <-> float, as one access of E elements (up to
+// 16 bytes) or several 16-byte ones (the caller guarantees the alignment).
 template <typename IO, int E> struct vecio;
 template <int E> struct vecio<__nv_bfloat16, E> {
-  // E consecutive bf16 -> float (E = 4: 8 bytes, 8: 16 bytes, 16: 32 bytes)
+  // E consecutive bf16 -> float (E = 1: 2 bytes, 2: 4, 4: 8, 8: 16, 16: 32)
   __device__ static void load(const __nv_bfloat16* p, float (&v)[E]) {
-    uint32_t w[E / 2];
-    if constexpr (E == 4) {
+    if constexpr (E == 1) {
+      v[0] = __bfloat162float(*p);
+      return;
+    }
+    uint32_t w[E / 2 > 0 ? E / 2 : 1];
+    if constexpr (E == 2) {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    } else if constexpr (E == 4) {
       const uint2 q = *reinterpret_cast<const uint2*>(p);
       w[0] = q.x; w[1] = q.y;
     } else {
@@ -186,13 +192,19 @@ template <int E> struct vecio<__nv_bfloat16, E> {
     }
   }
   __device__ static void store(__nv_bfloat16* p, const float (&v)[E]) {
-    uint32_t w[E / 2];
+    if constexpr (E == 1) {
+      *p = __float2bfloat16_rn(v[0]);
+      return;
+    }
+    uint32_t w[E / 2 > 0 ? E / 2 : 1];
 #pragma unroll
     for (int i = 0; i < E / 2; ++i) {
       const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
       w[i] = *reinterpret_cast<const uint32_t*>(&h2);
     }
-    if constexpr (E == 4) {
+    if constexpr (E == 2) {
+      *reinterpret_cast<uint32_t*>(p) = w[0];
+    } else if constexpr (E == 4) {
       *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
     } else {
 #pragma unroll
@@ -203,6 +215,14 @@ template <int E> struct vecio<__nv_bfloat16, E> {
 };
 template <int E> struct vecio<float, E> {
   __device__ static void load(const float* p, float (&v)[E]) {
+    if constexpr (E == 1) {
+      v[0] = *p;
+      return;
+    } else if constexpr (E == 2) {
+      const float2 q = *reinterpret_cast<const float2*>(p);
+      v[0] = q.x; v[1] = q.y;
+      return;
+    }
 #pragma unroll
     for (int k = 0; k < E / 4; ++k) {
       const float4 q = reinterpret_cast<const float4*>(p)[k];
@@ -210,6 +230,13 @@ template <int E> struct vecio<float, E> {
     }
   }
   __device__ static void store(float* p, const float (&v)[E]) {
+    if constexpr (E == 1) {
+      *p = v[0];
+      return;
+    } else if constexpr (E == 2) {
+      *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+      return;
+    }
 #pragma unroll
     for (int k = 0; k < E / 4; ++k)
       reinterpret_cast<float4*>(p)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);

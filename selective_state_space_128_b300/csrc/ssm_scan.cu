@@ -54,20 +54,24 @@ __device__ int g_scan_error;
 // block, T steps per chunk, NS raw stages, E channel steps per thread in the
 // per-step (conversion and finalisation) work.
 template <int N> struct ScanCfg {
-  static constexpr int NPT = N <= 2 ? N : (N == 4 ? 2 : (N <= 16 ? 4 : N / 4));
+  // at most 8 states per lane (larger N spreads over more lanes: 8 lanes of a
+  // channel at N = 64, 16 at N = 128)
+  static constexpr int NPT = N <= 2 ? N : (N == 4 ? 2 : (N <= 16 ? 4 : 8));
   static constexpr int G = N / NPT;
   static constexpr int CH = kScanThreads / G;
   static constexpr int T = 16;
   static constexpr int NS = 3;
   static constexpr int E = CH * T / kScanThreads;
   // warp layout: a warp holds CW channels x GW state groups, so that a shared
-  // load of B/C rows touches at most two distinct addresses per warp
-  static constexpr int GW = G < 2 ? G : 2;
+  // load of B/C rows touches at most two distinct addresses per warp (four
+  // when a block has fewer than 16 channels)
+  static constexpr int GW = G < 2 ? G : (CH < 16 ? 32 / CH : 2);
   static constexpr int CW = 32 / GW;
   static constexpr int WPC = G / GW;  // warps per set of CW channels
   static_assert(G * NPT == N, "tiling");
+  static_assert(CW <= CH && WPC * GW == G && (CH / CW) * WPC * 32 == kScanThreads, "warp layout");
   static_assert(T == 16, "the partial-tile swizzle assumes 4 units of 4 steps");
-  static_assert(E == 4 || E == 8 || E == 16, "per-thread step count");
+  static_assert(E == 1 || E == 2 || E == 4 || E == 8 || E == 16, "per-thread step count");
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -274,10 +278,16 @@ __device__ __forceinline__ void prep_store(unsigned char* buf, int tid,
     Ut[j] = v.u[j];
   }
   if (PASS == 0) {
-    float4* g4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(buf + S::bGate) + r * S::RowG + te);
+    float* gr = reinterpret_cast<float*>(buf + S::bGate) + r * S::RowG + te;
+    if constexpr (E % 4 == 0) {
+      float4* g4 = reinterpret_cast<float4*>(gr);
 #pragma unroll
-    for (int k = 0; k < E / 4; ++k)
-      g4[k] = make_float4(v.gate[4 * k], v.gate[4 * k + 1], v.gate[4 * k + 2], v.gate[4 * k + 3]);
+      for (int k = 0; k < E / 4; ++k)
+        g4[k] = make_float4(v.gate[4 * k], v.gate[4 * k + 1], v.gate[4 * k + 2], v.gate[4 * k + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < E; ++j) gr[j] = v.gate[j];
+    }
   }
   constexpr int NT = N * T;
 #pragma unroll
@@ -308,10 +318,17 @@ __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned
   float pg[G][E];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
+    if constexpr (E % 4 == 0) {
 #pragma unroll
-    for (int k = 0; k < E / 4; ++k) {
-      const float4 q = *reinterpret_cast<const float4*>(part + p_index(g * S::CH + r, te / 4 + k));
-      pg[g][4 * k] = q.x; pg[g][4 * k + 1] = q.y; pg[g][4 * k + 2] = q.z; pg[g][4 * k + 3] = q.w;
+      for (int k = 0; k < E / 4; ++k) {
+        const float4 q = *reinterpret_cast<const float4*>(part + p_index(g * S::CH + r, te / 4 + k));
+        pg[g][4 * k] = q.x; pg[g][4 * k + 1] = q.y; pg[g][4 * k + 2] = q.z; pg[g][4 * k + 3] = q.w;
+      }
+    } else {
+      // fewer than 4 steps per thread: element reads inside one 4-step unit
+#pragma unroll
+      for (int j = 0; j < E; ++j)
+        pg[g][j] = part[p_index(g * S::CH + r, (te + j) >> 2) + ((te + j) & 3)];
     }
   }
 #pragma unroll
@@ -325,15 +342,20 @@ __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned
   const float (&acc)[E] = pg[0];
   const float Dd = sD[r];
   const float* Ut = reinterpret_cast<const float*>(buf + S::bU) + r * S::RowF + te;
-  const float4* g4 = reinterpret_cast<const float4*>(
-      reinterpret_cast<const float*>(buf + S::bGate) + r * S::RowG + te);
+  const float* gr = reinterpret_cast<const float*>(buf + S::bGate) + r * S::RowG + te;
   float y[E];
+  if constexpr (E % 4 == 0) {
+    const float4* g4 = reinterpret_cast<const float4*>(gr);
 #pragma unroll
-  for (int k = 0; k < E / 4; ++k) {
-    const float4 gk = g4[k];
-    const float gg[4] = {gk.x, gk.y, gk.z, gk.w};
+    for (int k = 0; k < E / 4; ++k) {
+      const float4 gk = g4[k];
+      const float gg[4] = {gk.x, gk.y, gk.z, gk.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) y[4 * k + j] = fmaf(Dd, Ut[4 * k + j], acc[4 * k + j]) * gg[j];
+      for (int j = 0; j < 4; ++j) y[4 * k + j] = fmaf(Dd, Ut[4 * k + j], acc[4 * k + j]) * gg[j];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < E; ++j) y[j] = fmaf(Dd, Ut[j], acc[j]) * gr[j];
   }
   if (p.bld) {
     // (batch, L, dim) layout: this row's steps are dim elements apart
@@ -885,6 +907,7 @@ static bool cfg_for(int64_t N, int& chans, int& chunk) {
     case 16: cfg_of<16>(chans, chunk); return true;
     case 32: cfg_of<32>(chans, chunk); return true;
     case 64: cfg_of<64>(chans, chunk); return true;
+    case 128: cfg_of<128>(chans, chunk); return true;
     default: return false;
   }
 }
@@ -1014,6 +1037,7 @@ static cudaError_t launch_io(const ScanArgs& a, int64_t N, cudaStream_t stream) 
     case 16: return launch_typed<IO, 16>(a, stream);
     case 32: return launch_typed<IO, 32>(a, stream);
     case 64: return launch_typed<IO, 64>(a, stream);
+    case 128: return launch_typed<IO, 128>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

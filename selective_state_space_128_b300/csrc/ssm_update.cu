@@ -9,9 +9,10 @@
 // The step reads and writes the float32 state once (64 bytes per channel at
 // N = 16) and is bound by HBM bandwidth, so the kernel is built to keep many
 // bytes in flight with few instructions:
-//  * G = 4 lanes share a channel, each holding N/4 contiguous states that it
-//    loads and stores as 16-byte vectors, so a warp touches 8 whole channels
-//    (512 contiguous bytes per access);
+//  * G = 4 lanes share a channel (N <= 16; beyond, G = N/8 lanes of 8 states),
+//    each holding N/G contiguous states that it loads and stores as 16-byte
+//    vectors, so a warp touches whole channels (512 contiguous bytes per access
+//    at N = 16);
 //  * each thread handles K channels spaced one warp-width of channels apart
 //    and issues all of their loads before any arithmetic, so 64 bytes of
 //    state per thread are in flight at once;
@@ -28,7 +29,9 @@ constexpr int kUpdK = 4;  // channels per thread
 
 template <typename IO, int N>
 __global__ void __launch_bounds__(kUpdThreads) update_kernel(const UpdateArgs p) {
-  constexpr int G = N >= 4 ? 4 : N;
+  // lanes per channel: 4 up to N = 16, then 8 states per lane (8 lanes at N = 64,
+  // 16 at N = 128)
+  constexpr int G = N <= 16 ? (N >= 4 ? 4 : N) : N / 8;
   constexpr int NPT = N / G;
   constexpr int CPB = kUpdThreads / G;  // channels per block per k
   const int tid = threadIdx.x;
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kUpdThreads) update_kernel(const UpdateArgs p)
 
 template <typename IO, int N>
 static cudaError_t upd_typed(const UpdateArgs& a, cudaStream_t stream) {
-  constexpr int G = N >= 4 ? 4 : N;
+  constexpr int G = N <= 16 ? (N >= 4 ? 4 : N) : N / 8;
   constexpr int per_block = kUpdThreads / G * kUpdK;
   const dim3 grid((unsigned)((a.dim + per_block - 1) / per_block), (unsigned)a.batch);
   update_kernel<IO, N><<<grid, kUpdThreads, 0, stream>>>(a);
@@ -155,6 +158,7 @@ static cudaError_t upd_io(const UpdateArgs& a, int64_t N, cudaStream_t stream) {
     case 16: return upd_typed<IO, 16>(a, stream);
     case 32: return upd_typed<IO, 32>(a, stream);
     case 64: return upd_typed<IO, 64>(a, stream);
+    case 128: return upd_typed<IO, 128>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -47,7 +47,7 @@ def test_scan_argument_errors():
     assert _scan(L=-5) == ssm.SSM_ERR_ARG
     assert _scan(N=0) == ssm.SSM_ERR_ARG
     assert _scan(batch=70000) == ssm.SSM_ERR_ARG
-    for n in (3, 5, 12, 128):
+    for n in (3, 5, 12, 256):
         assert _scan(N=n) == ssm.SSM_ERR_UNSUPPORTED
     assert _scan(u=FAKE + 2) == ssm.SSM_ERR_ALIGN
     assert _scan(z=FAKE + 0x6000008) == ssm.SSM_ERR_ALIGN
@@ -136,6 +136,8 @@ def test_backward_argument_errors():
         assert _bwd(**{name: None}) == ssm.SSM_ERR_ARG, name
     assert _bwd(io=3) == ssm.SSM_ERR_ARG
     assert _bwd(N=12) == ssm.SSM_ERR_UNSUPPORTED
+    assert _bwd(N=128) == ssm.SSM_ERR_UNSUPPORTED          # the backward stops at 64
+    assert ssm.ssm_scan_bwd_workspace_bytes(2, 64, 128, 128) == 0
     # dz is required with a gate and refused without one
     assert _bwd(z=FAKE + 0xB000000) == ssm.SSM_ERR_ARG
     assert _bwd(dz=FAKE + 0xB000000) == ssm.SSM_ERR_ARG

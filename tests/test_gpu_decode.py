@@ -17,7 +17,7 @@ def _decode_case(batch, dim, N, steps, io="bf16", seed=40):
     return dw, synth.make_decode_step_inputs(dw, 0, steps)
 
 
-@pytest.mark.parametrize("N", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16, 32, 64, 128])
 @pytest.mark.parametrize("io", ["bf16", "f32"])
 def test_decode_steps_match_oracle(N, io):
     dw, s = _decode_case(3, 50, N, 6, io)

@@ -19,7 +19,7 @@ TOL = {"f32": 1e-4, "bf16": 1e-2}
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-@pytest.mark.parametrize("N", [1, 4, 16, 64])
+@pytest.mark.parametrize("N", [1, 4, 16, 64, 128])
 def test_scan_euler_matches_oracle(io, N):
     w = synth.scaled(synth.MAMBA_130M, name="euler_scan", batch=2, dim=70, seqlen=150,
                      dstate=N, io=io, seed=90 + N)

@@ -59,7 +59,7 @@ def test_tiny_fp32_short_entry_point():
     _check(synth.TINY, synth.make_scan_inputs(synth.TINY), short=True)
 
 
-@pytest.mark.parametrize("N", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16, 32, 64, 128])
 @pytest.mark.parametrize("io", ["bf16", "f32"])
 def test_state_sizes(N, io):
     w = synth.scaled(synth.MAMBA_130M, batch=2, dim=72, seqlen=200, dstate=N, io=io, seed=30 + N)
@@ -210,4 +210,13 @@ def test_streams_and_errors():
 def test_mamba130m_layer_full_size():
     """batch 8, d_inner 1536, L 2048, N 16, bf16 I/O: every output against the oracle."""
     w = synth.MAMBA_130M
+    _check(w, synth.make_scan_inputs(w))
+
+
+@pytest.mark.parametrize("N", [64, 128])
+def test_large_state_split_plan(N):
+    """N = 64 and 128 spread a channel over 8 and 16 lanes (8 states each); few
+    channels and a long sequence also take the split plan."""
+    w = synth.scaled(synth.MAMBA_130M, batch=1, dim=48, seqlen=4096, dstate=N, seed=200 + N)
+    assert ssm.ssm_scan_workspace_bytes(1, 48, 4096, N, ssm.SSM_BF16) > 0
     _check(w, synth.make_scan_inputs(w))
