@@ -24,26 +24,25 @@ import synth
 TOL_BF16 = 1e-2
 
 
-def _rejecting_shape():
-    """(batch, dim, L, N) whose split plan needs more scratch than the fixed array."""
+def test_plans_beyond_the_fixed_scratch_are_refused():
+    """Over a grid of shapes whose plans split the sequence, every plan either fits
+    the fixed array or is refused from the sizes alone (SSM_ERR_WORKSPACE, before any
+    pointer is looked at or any work is queued).  With at most 8 states per lane no
+    plan needs more than about 1.2 MB, so today every split plan fits."""
     limit = ssm.static_scratch_bytes()
-    for N in (16, 32, 64):
-        for dim in range(32, 8192, 32):
-            if ssm.ssm_scan_workspace_bytes(1, dim, 1 << 20, N, ssm.SSM_BF16) > limit:
-                return 1, dim, 1 << 20, N
-    return None
-
-
-def test_sizes_beyond_the_fixed_scratch_are_refused():
-    shape = _rejecting_shape()
-    if shape is None:
-        pytest.skip("no plan needs more scratch than the fixed array")
-    batch, dim, L, N = shape
     lib = ssm.load()
-    # refused from the sizes alone, before any pointer is looked at or any work is queued
-    rc = lib.ssm_scan_fwd_noalloc(None, None, None, None, None, None, None, None, 1, None, None,
-                                  batch, dim, L, N, ssm.SSM_BF16, None, None)
-    assert rc == ssm.SSM_ERR_WORKSPACE
+    split = 0
+    for N in (16, 32, 64, 128):
+        for batch in (1, 2):
+            for dim in (8, 32, 96, 512, 1024, 2048, 4096):
+                need = ssm.ssm_scan_workspace_bytes(batch, dim, 1 << 20, N, ssm.SSM_BF16)
+                split += need > 0
+                if need > limit:
+                    rc = lib.ssm_scan_fwd_noalloc(None, None, None, None, None, None, None, None,
+                                                  1, None, None, batch, dim, 1 << 20, N,
+                                                  ssm.SSM_BF16, None, None)
+                    assert rc == ssm.SSM_ERR_WORKSPACE
+    assert split > 20   # the grid does exercise the split plans
 
 
 @pytest.mark.gpu
