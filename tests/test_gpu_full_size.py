@@ -134,3 +134,76 @@ def test_decode_1000_steps_full_size_sampled():
     assert np.isfinite(y_gpu).all()
     assert oracle.rel_err(y_gpu, y_ref) <= TOL
     assert oracle.rel_err(host64(state[bi, di]), st_o) <= TOL
+
+
+def test_backward_mamba130m_layer_full_size_sampled():
+    """The backward at the bench's layer size (batch 8, d_inner 1536, L 2048, N 16, bf16):
+    dB and dC of batch row 0 in full (they sum over all 1536 channels), du, ddelta, dz
+    and d_init_state of 32 sampled channels, and dA, dD, dbias of 24 sampled channels
+    (they sum over the 8 batch rows)."""
+    w = synth.MAMBA_130M
+    x = synth.make_scan_inputs(w)
+    e = synth.make_bwd_inputs(w)
+    g = upload_scan(x)
+    out = ssm.scan_bwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                       g["delta_bias"], True, init_state=dev_f32(e["init_state"]),
+                       dy=dev_io(e["dy"]), d_final_state=dev_f32(e["d_final_state"]),
+                       want_init_grad=True)
+    torch.cuda.synchronize()
+    dy64 = synth.bf16_to_f32(e["dy"]).astype(np.float64)
+    h0 = e["init_state"].astype(np.float64)
+    dfin = e["d_final_state"].astype(np.float64)
+
+    def rows(bs, ds):
+        return oracle.scan_bwd_rows(x["u"][bs, ds], x["delta"][bs, ds], x["z"][bs, ds], bs, ds,
+                                    x["A"], x["B"], x["C"], x["D"], x["delta_bias"], True,
+                                    dy64[bs, ds], h0[bs, ds], dfin[bs, ds], nbatch=w.batch)
+
+    # batch row 0, every channel: dB[0], dC[0] in full
+    d_all = np.arange(w.dim)
+    r0 = rows(np.zeros(w.dim, np.int64), d_all)
+    assert oracle.rel_err(host64(out["dB"][0]), r0["dB"][0]) <= TOL
+    assert oracle.rel_err(host64(out["dC"][0]), r0["dC"][0]) <= TOL
+    bs, ds = _sample_rows(w.batch, w.dim, 32, seed=5)
+    rs = rows(bs, ds)
+    bi, di = torch.from_numpy(bs).cuda(), torch.from_numpy(ds).cuda()
+    for k in ("du", "ddelta", "dz"):
+        assert oracle.rel_err(host64(out[k][bi, di]), rs[k]) <= TOL, k
+    assert oracle.rel_err(host64(out["dinit"][bi, di]), rs["dinit"]) <= TOL
+    # per-channel sums over the batch for 24 channels
+    dsel = np.random.default_rng(6).choice(w.dim, 24, replace=False)
+    bb = np.repeat(np.arange(w.batch), len(dsel))
+    dd = np.tile(dsel, w.batch)
+    rc = rows(bb, dd)
+    dA_ref = rc["dA_unit"].reshape(w.batch, len(dsel), w.dstate).sum(0)
+    dD_ref = rc["dD_unit"].reshape(w.batch, len(dsel)).sum(0)
+    db_ref = rc["dbias_unit"].reshape(w.batch, len(dsel)).sum(0)
+    dsel_t = torch.from_numpy(dsel).cuda()
+    assert oracle.rel_err(host64(out["dA"][dsel_t]), dA_ref) <= TOL
+    assert oracle.rel_err(host64(out["dD"][dsel_t]), dD_ref) <= TOL
+    assert oracle.rel_err(host64(out["dbias"][dsel_t]), db_ref) <= TOL
+
+
+def test_conv1d_and_bld_scan_at_layer_size():
+    """The front end at the bench's size (8 x 1536 x 2048 bf16, width 4) on 64 sampled
+    rows, and the (batch, L, dim) scan of the layer equal, bit for bit, to the
+    (batch, dim, L) one (which the parity tests above pin to the oracle)."""
+    w = synth.MAMBA_130M
+    x = synth.make_scan_inputs(w)
+    wt = synth.fill(7, synth.S_B, 0, w.dim * 4, synth.NORMAL, 0.0, 0.5).reshape(w.dim, 4)
+    bias = synth.fill(7, synth.S_D, 0, w.dim, synth.NORMAL, 0.0, 0.2)
+    gu = dev_io(x["u"])
+    out = ssm.conv1d(gu, dev_f32(wt), dev_f32(bias))
+    torch.cuda.synchronize()
+    bs, ds = _sample_rows(w.batch, w.dim, 64, seed=8)
+    # the sampled rows as one batch row of 64 channels with their own weights
+    ref, _ = oracle.conv1d(np.ascontiguousarray(x["u"][bs, ds][None]), wt[ds], bias[ds])
+    got = host64(out[torch.from_numpy(bs).cuda(), torch.from_numpy(ds).cuda()])
+    assert oracle.rel_err(got, ref[0]) <= TOL
+    g = upload_scan(x)
+    y0, h0 = ssm.scan(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"])
+    t = {k: g[k].transpose(1, 2).contiguous() for k in ("u", "delta", "z")}
+    y1, h1 = ssm.scan(t["u"], t["delta"], g["A"], g["B"], g["C"], g["D"], t["z"], g["delta_bias"],
+                      bld=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.transpose(1, 2), y0) and torch.equal(h1, h0)
