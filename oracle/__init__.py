@@ -265,6 +265,45 @@ def conv1d(x, weight, bias=None, state_in=None, silu=True, nthreads=0):
     return out, sout
 
 
+def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, init_state=None,
+        euler=False, nthreads=0):
+    """Mamba-2's scalar-A state space model ([C] §5.1: A_t = a_t I per head), by its
+    plain recurrence: the selective scan of every channel p of head h with
+    A[n] = A[h] for all n, the head's step Δ_t shared by its P channels, and the B, C of
+    the head's group.  The recurrence is the scan oracle's, unchanged.
+
+    x, z: (batch, L, H, P) float32 or bfloat16 bits; dt: (batch, L, H) same dtype;
+    A, D, dt_bias: (H,) float32; B, C: (batch, L, G, N) float32; init_state:
+    (batch, H, P, N) float64 or None.  Returns y (batch, L, H, P) float64 and the final
+    state (batch, H, P, N) float64."""
+    x = np.asarray(x)
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    assert H % G == 0 and dt.shape == (batch, L, H) and C.shape == B.shape
+    hpg = H // G
+    # rows: unit (b, h, p); its u is x[b, :, h, p], its Δ row dt[b, :, h]
+    u = np.ascontiguousarray(np.transpose(x, (0, 2, 3, 1)).reshape(batch * H * P, L))
+    dl = np.ascontiguousarray(np.repeat(np.transpose(np.asarray(dt), (0, 2, 1)), P, axis=1)
+                              .reshape(batch * H * P, L))
+    zz = None if z is None else np.ascontiguousarray(
+        np.transpose(np.asarray(z), (0, 2, 3, 1)).reshape(batch * H * P, L))
+    bb, hh, pp = np.meshgrid(np.arange(batch), np.arange(H), np.arange(P), indexing="ij")
+    unit_b = (bb * G + hh // hpg).ravel()             # one "batch row" of B, C per group
+    unit_d = (hh * P + pp).ravel()                     # channel d = h P + p
+    A_tab = np.repeat(np.asarray(A, np.float32), P)[:, None].repeat(N, axis=1)
+    Bt = np.ascontiguousarray(np.transpose(np.asarray(B, np.float32), (0, 2, 3, 1))
+                              .reshape(batch * G, N, L))
+    Ct = np.ascontiguousarray(np.transpose(np.asarray(C, np.float32), (0, 2, 3, 1))
+                              .reshape(batch * G, N, L))
+    D_tab = None if D is None else np.repeat(np.asarray(D, np.float32), P)
+    bias_tab = None if dt_bias is None else np.repeat(np.asarray(dt_bias, np.float32), P)
+    h0 = None if init_state is None else np.asarray(init_state, np.float64).reshape(batch * H * P, N)
+    y, hN = scan_rows(u, dl, zz, unit_b, unit_d, A_tab, Bt, Ct, D_tab, bias_tab, delta_softplus,
+                      h0, 1, nthreads, euler)
+    y = np.transpose(y.reshape(batch, H, P, L), (0, 3, 1, 2))
+    return y, hN.reshape(batch, H, P, N)
+
+
 def rel_err(got, ref):
     """max |got - ref| / max |ref|: the parity metric for y and final_state."""
     got = np.asarray(got, dtype=np.float64)
