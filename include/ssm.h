@@ -315,6 +315,40 @@ int ssm_scan_fwd_train(const void* u, const void* delta, const float* delta_bias
                        const float* init_state, void* workspace, size_t workspace_bytes,
                        void* bwd_workspace, size_t bwd_workspace_bytes, void* stream);
 
+/*
+ * Mamba-2's scalar-A SSM (SSD), chunked.  The chapter page ("14.1 SSM(State
+ * Space Models)과 Mamba 아키텍처의 부상", §5.1-5.2) restricts A to a scalar per
+ * step times the identity, which makes the SSM the masked product
+ * Y = (L ∘ C Bᵀ) X, and computes it chunk by chunk: the quadratic form inside
+ * each chunk of 64 steps on the tensor cores, states passed between chunks.
+ * Per batch b, head h (P = headdim channels sharing the step; group
+ * g = h / (nheads / ngroups)), channel p, state n:
+ *
+ *   Δ_t   = softplus(dt[b,t,h] + dt_bias[h])   (SSM_SOFTPLUS in flags; else dt + bias)
+ *   h_t   = exp(Δ_t A[h]) h_{t-1} + β_t x[b,t,h,p] B[b,t,g,n]
+ *           β_t = (exp(Δ_t A[h]) - 1) / A[h]  (zero-order hold), or Δ_t (SSM_EULER_B)
+ *   y     = Σ_n C[b,t,g,n] h_t + D[h] x, then · silu(z) when z is given
+ *
+ * Layouts (dense, row-major): x, z, y (batch, seqlen, nheads, headdim) bf16;
+ * dt (batch, seqlen, nheads) bf16; B, C (batch, seqlen, ngroups, dstate) bf16;
+ * A, D, dt_bias (nheads) fp32; init_state, final_state (batch, nheads,
+ * headdim, dstate) fp32 (nullable).  Supported: headdim 64, dstate 64 or 128,
+ * nheads a multiple of ngroups (SSM_ERR_UNSUPPORTED otherwise).  Workspace:
+ * ssm_ssd_workspace_bytes() bytes (chunk states, the states entering each
+ * chunk, chunk decays), required when batch, seqlen and nheads are non-zero.
+ * Products in bf16 with fp32 accumulation; the chunk states are kept in fp32
+ * and enter the chunk outputs as bf16.  Errors as the other entry points;
+ * asynchronous on `stream` (three kernels).
+ */
+size_t ssm_ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                               int64_t dstate);
+
+int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float* A,
+                const void* B, const void* C, const float* D, const void* z, int flags, void* y,
+                float* final_state, const float* init_state, int64_t batch, int64_t seqlen,
+                int64_t nheads, int64_t headdim, int64_t ngroups, int64_t dstate,
+                void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

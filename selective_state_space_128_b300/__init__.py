@@ -69,6 +69,10 @@ def load():
     lib.ssm_scan_fwd_train.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp, sz,
                                                    vp, sz, vp]
     lib.ssm_scan_fwd_train.restype = i32
+    lib.ssm_ssd_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
+    lib.ssm_ssd_workspace_bytes.restype = sz
+    lib.ssm_ssd_fwd.argtypes = [vp] * 8 + [i32, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, sz, vp]
+    lib.ssm_ssd_fwd.restype = i32
     lib.ssm_conv1d_fwd.argtypes = [vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, i64, i32, vp]
     lib.ssm_conv1d_fwd.restype = i32
     lib.ssm_conv1d_update.argtypes = [vp, vp, vp, vp, i32, vp, i64, i64, i64, i32, vp]
@@ -286,6 +290,25 @@ def ssm_conv1d_update(conv_state, x, weight, bias, silu, out, stream=None):
     _call("ssm_conv1d_update", rc)
 
 
+def ssm_ssd_workspace_bytes(batch, seqlen, nheads, headdim, dstate) -> int:
+    return int(load().ssm_ssd_workspace_bytes(batch, seqlen, nheads, headdim, dstate))
+
+
+def ssm_ssd_fwd(x, dt, dt_bias, A, B, C, D, z, flags, y, final_state, init_state, workspace,
+                workspace_bytes=None, stream=None):
+    """Tensor form of ``ssm_ssd_fwd``: x (batch, L, H, P), B (batch, L, G, N)."""
+    _check_dev(x, dt, dt_bias, A, B, C, D, z, y, final_state, init_state, workspace)
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if workspace is not None and workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().ssm_ssd_fwd(_ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                            _ptr(z), int(flags), _ptr(y), _ptr(final_state), _ptr(init_state),
+                            batch, L, H, P, G, N, _ptr(workspace), int(workspace_bytes or 0),
+                            _stream(stream))
+    _call("ssm_ssd_fwd", rc)
+
+
 def static_scratch_bytes() -> int:
     """SSM_STATIC_SCRATCH_BYTES as defined in include/ssm.h."""
     import re
@@ -379,6 +402,22 @@ def conv1d(x, weight, bias=None, conv_state=None, silu=True, want_state=False, s
     ssm_conv1d_fwd(x, weight, bias, conv_state, int(bool(silu)) | (SSM_LAYOUT_BLD if bld else 0),
                    out, st, stream)
     return (out, st) if want_state else out
+
+
+def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, init_state=None,
+        euler=False, stream=None):
+    """y, final_state = ssd(...): Mamba-2's chunked scalar-A SSM; allocates y (bf16, like x),
+    the final state (batch, H, P, N) float32 and the workspace."""
+    import torch
+    batch, L, H, P = x.shape
+    N = B.shape[3]
+    y = torch.empty_like(x)
+    h = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device)
+    nbytes = ssm_ssd_workspace_bytes(batch, L, H, P, N)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    ssm_ssd_fwd(x, dt, dt_bias, A, B, C, D, z, _flags(delta_softplus, euler), y, h, init_state,
+                ws, nbytes, stream)
+    return y, h
 
 
 def exported_names():

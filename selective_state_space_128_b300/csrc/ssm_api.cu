@@ -71,6 +71,75 @@ size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int6
       .workspace_bytes;
 }
 
+size_t ssm_ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                               int64_t dstate) {
+  if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim != 64 || (dstate != 64 && dstate != 128))
+    return 0;
+  if (!sizes_ok(batch, nheads * headdim, seqlen)) return 0;
+  return ssm::ssd_layout(batch, seqlen, nheads, dstate).bytes;
+}
+
+int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float* A,
+                const void* B, const void* C, const float* D, const void* z, int flags, void* y,
+                float* final_state, const float* init_state, int64_t batch, int64_t seqlen,
+                int64_t nheads, int64_t headdim, int64_t ngroups, int64_t dstate,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!flags_ok(flags)) return SSM_ERR_ARG;
+  if (batch < 0 || seqlen < 0 || nheads < 0 || ngroups <= 0 || headdim <= 0 || dstate <= 0)
+    return SSM_ERR_ARG;
+  if (batch > 65535 || nheads > 65535) return SSM_ERR_ARG;
+  if (!sizes_ok(batch, nheads * headdim, seqlen)) return SSM_ERR_ARG;
+  if (headdim != 64 || (dstate != 64 && dstate != 128) || nheads % ngroups != 0)
+    return SSM_ERR_UNSUPPORTED;
+  const bool work = batch > 0 && nheads > 0 && seqlen > 0;
+  if (work && (!x || !dt || !A || !B || !C || !y)) return SSM_ERR_ARG;
+  const void* ptrs[] = {x, dt, dt_bias, A, B, C, D, z, y, final_state, init_state, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const size_t nx = (size_t)batch * (size_t)seqlen * (size_t)nheads * (size_t)headdim * 2;
+  const size_t ndt = (size_t)batch * (size_t)seqlen * (size_t)nheads * 2;
+  const size_t nbc = (size_t)batch * (size_t)seqlen * (size_t)ngroups * (size_t)dstate * 2;
+  const size_t nst = (size_t)batch * (size_t)nheads * (size_t)headdim * (size_t)dstate * 4;
+  const size_t nh = (size_t)nheads * 4;
+  struct Span { const void* p; size_t n; };
+  const Span ins[] = {{x, nx}, {dt, ndt}, {dt_bias, nh}, {A, nh}, {B, nbc}, {C, nbc}, {D, nh},
+                      {z, nx}, {init_state, nst}};
+  for (const Span& in : ins)
+    if (overlaps(y, nx, in.p, in.n) || overlaps(final_state, nst, in.p, in.n)) return SSM_ERR_ARG;
+  if (overlaps(y, nx, final_state, nst)) return SSM_ERR_ARG;
+  const ssm::SsdLayout lay = ssm::ssd_layout(batch, seqlen, nheads, dstate);
+  if (work) {
+    if (!workspace || workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
+    for (const Span& in : ins)
+      if (overlaps(workspace, lay.bytes, in.p, in.n)) return SSM_ERR_ARG;
+    if (overlaps(workspace, lay.bytes, y, nx) || overlaps(workspace, lay.bytes, final_state, nst))
+      return SSM_ERR_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!work) {
+    // no steps: the final state is the initial one (or zeros)
+    if (final_state && nst) {
+      const cudaError_t e = init_state ? cudaMemcpyAsync(final_state, init_state, nst,
+                                                         cudaMemcpyDeviceToDevice, st)
+                                       : cudaMemsetAsync(final_state, 0, nst, st);
+      if (e != cudaSuccess) return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
+  }
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  ssm::SsdArgs a{};
+  a.x = x; a.dt = dt; a.dt_bias = dt_bias; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.y = y;
+  a.final_state = final_state; a.init_state = init_state;
+  a.ws_state = reinterpret_cast<float*>(ws + lay.o_state);
+  a.ws_hin = reinterpret_cast<__nv_bfloat16*>(ws + lay.o_hin);
+  a.ws_logdecay = reinterpret_cast<float*>(ws + lay.o_logdecay);
+  a.batch = batch; a.L = seqlen; a.H = nheads; a.G = ngroups; a.nch = lay.nch;
+  a.softplus = (flags & SSM_SOFTPLUS) != 0;
+  a.euler = (flags & SSM_EULER_B) != 0;
+  const cudaError_t e = ssm::ssd_launch(a, dstate, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 }  // extern "C"
 
 namespace {

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace ssm {
@@ -154,5 +155,38 @@ struct ConvArgs {
 // or the one-token update on the rolling state.
 cudaError_t conv_launch(const ConvArgs& a, int64_t width, int io_dtype, bool update,
                         cudaStream_t stream);
+
+// Arguments of the chunked scalar-A SSM (Mamba-2 SSD).  x, z, y (batch, L, H,
+// P) bf16; dt (batch, L, H) bf16; B, C (batch, L, G, N) bf16; A, D, dt_bias (H)
+// fp32; states (batch, H, P, N) fp32.  Workspace parts: per-chunk states
+// [batch][nch][H][P][N] fp32, the states entering each chunk (same shape, bf16),
+// per-chunk log decays [batch][nch][H] fp32.
+struct SsdArgs {
+  const void* x;
+  const void* dt;
+  const float* dt_bias;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  void* y;
+  float* final_state;
+  const float* init_state;
+  float* ws_state;
+  __nv_bfloat16* ws_hin;
+  float* ws_logdecay;
+  int64_t batch, L, H, G, nch;
+  int softplus;
+  int euler;
+};
+
+struct SsdLayout {
+  int64_t nch;
+  size_t o_state, o_hin, o_logdecay, bytes;
+};
+
+SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t N);
+cudaError_t ssd_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
 
 }  // namespace ssm

@@ -1,0 +1,382 @@
+// Mamba-2's scalar-A state space model (SSD), chunked, for sm_103a.
+//
+// The chapter page ("14.1 SSM(State Space Models)과 Mamba 아키텍처의 부상",
+// §5.1-5.2) restricts A to a scalar per step times the identity, so that per
+// head the SSM is the masked product Y = (L ∘ C Bᵀ) X with L the lower-
+// triangular matrix of cumulative decays, and computes it in chunks: the
+// quadratic form inside a chunk on the tensor cores, states passed between
+// chunks.  Per head h (P channels sharing the step Δ_t and the scalar a_h; B,
+// C of the head's group), with s_t = Σ_{k<=t in the chunk} Δ_k a_h and the
+// input weight β_t = (exp(Δ_t a_h) - 1)/a_h (zero-order hold) or Δ_t (Euler):
+//
+//   chunk state    S_c = Σ_τ exp(s_end - s_τ) β_τ x_τ ⊗ B_τ                (P x N)
+//   state passing  H_c = exp(s_end(c)) H_{c-1} + S_c,  H_{-1} = init_state
+//   chunk output   y_t = Σ_{τ<=t} (C_t·B_τ) exp(s_t - s_τ) β_τ x_τ
+//                        + exp(s_t) C_t H_{c-1} + D_h x_t       (then · silu(z_t))
+//
+// Three launches: chunk states (all chunks in parallel), the state pass
+// (sequential over chunks, parallel over heads and state elements), chunk
+// outputs (all chunks in parallel).  The products run on the tensor cores as
+// mma.sync m16n8k16 bf16 with fp32 accumulation, operands staged in padded
+// shared-memory rows (144- or 272-byte rows: ldmatrix's eight row addresses
+// fall in distinct bank groups).  Layouts are Mamba-2's: x, z, y (batch, L, H,
+// P); dt (batch, L, H); B, C (batch, L, G, N); states (batch, H, P, N).
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+
+constexpr int kSsdQ = 64;        // chunk length
+constexpr int kSsdP = 64;        // head dimension
+constexpr int kSsdThreads = 128;  // 4 warps: 16 rows each
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+// d += a (16x16, row-major) * b (16x8, column-major); bf16 in, fp32 accumulate
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Per-chunk step terms of one head, shared by the chunk kernels: Δ·a (log
+// decay) cumulated over the chunk into sS, and the input weight β into sBeta.
+// Steps past the sequence get Δ = 0 (decay 1, weight 0).  128 threads.
+__device__ __forceinline__ void ssd_chunk_terms(const SsdArgs& p, int64_t b, int64_t t0, int h,
+                                                float* sS, float* sBeta) {
+  const int tid = threadIdx.x;
+  const float a = p.A[h];
+  if (tid < kSsdQ) {
+    const int64_t t = t0 + tid;
+    float dA = 0.f, beta = 0.f;
+    if (t < p.L) {
+      const float x = __bfloat162float(static_cast<const __nv_bfloat16*>(p.dt)[(b * p.L + t) * p.H + h]) +
+                      (p.dt_bias ? p.dt_bias[h] : 0.f);
+      const float dt = p.softplus ? softplus_precise(x) : x;
+      dA = dt * a;
+      beta = p.euler ? dt : (a != 0.f ? expm1f(dA) / a : dt);
+    }
+    sS[tid] = dA;
+    sBeta[tid] = beta;
+  }
+  __syncthreads();
+  if (tid < 32) {  // inclusive prefix sum of the 64 log decays: 2 per lane, a warp scan
+    const float v0 = sS[2 * tid], v1 = sS[2 * tid + 1];
+    float run = v0 + v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, run, o);
+      if (tid >= o) run += n;
+    }
+    const float excl = run - (v0 + v1);
+    sS[2 * tid] = excl + v0;
+    sS[2 * tid + 1] = run;
+  }
+  __syncthreads();
+}
+
+// Copies `rows` rows of `cols` bf16 (a multiple of 8) from global rows `gstride`
+// elements apart into shared rows `sstride` elements apart; rows at or past
+// `valid` are zero.
+__device__ __forceinline__ void ssd_stage(__nv_bfloat16* dst, int sstride,
+                                          const __nv_bfloat16* src, int64_t gstride, int rows,
+                                          int cols, int valid) {
+  const int vpr = cols / 8;  // 16-byte vectors per row
+  for (int e = threadIdx.x; e < rows * vpr; e += kSsdThreads) {
+    const int r = e / vpr, v = e - r * vpr;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (r < valid) q = *reinterpret_cast<const uint4*>(src + r * gstride + v * 8);
+    *reinterpret_cast<uint4*>(dst + r * sstride + v * 8) = q;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 1. chunk states: S_c[p][n] = Σ_τ (w_τ x_τ[p]) B_τ[n],  w_τ = exp(s_end - s_τ) β_τ
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_state_kernel(const SsdArgs p) {
+  constexpr int Q = kSsdQ, P = kSsdP, RX = P + 8, RB = N + 8;
+  __shared__ __align__(16) __nv_bfloat16 sX[Q * RX];   // w-scaled x, [τ][p]
+  __shared__ __align__(16) __nv_bfloat16 sB[Q * RB];   // B, [τ][n]
+  __shared__ float sS[Q], sBeta[Q];
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int64_t t0 = (int64_t)c * Q;
+  const int valid = (int)min64(Q, p.L - t0);
+  const int g = h / (p.H / p.G);
+  ssd_chunk_terms(p, b, t0, h, sS, sBeta);
+  const float s_end = sS[Q - 1];
+  // x rows scaled by w_τ while staging
+  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
+  for (int e = threadIdx.x; e < Q * (P / 8); e += kSsdThreads) {
+    const int r = e / (P / 8), v = e - r * (P / 8);
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (r < valid) {
+      vecio<__nv_bfloat16, 8>::load(xg + (int64_t)r * p.H * P + v * 8, f);
+      const float w = __expf(s_end - sS[r]) * sBeta[r];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] *= w;
+    }
+    vecio<__nv_bfloat16, 8>::store(sX + r * RX + v * 8, f);
+  }
+  ssd_stage(sB, RB, static_cast<const __nv_bfloat16*>(p.B) + ((b * p.L + t0) * p.G + g) * N,
+            p.G * N, Q, N, valid);
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows p in [16w, 16w+16)
+  float acc[N / 8][4];
+#pragma unroll
+  for (int j = 0; j < N / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < Q / 16; ++ks) {
+    // A = (w x)ᵀ: rows p, k = τ; stored [τ][p] -> transposed loads
+    uint32_t a[4];
+    {
+      const int i = lane >> 3;
+      ldsm_x4_t(a, sX + (16 * ks + (i >> 1) * 8 + (lane & 7)) * RX + 16 * w + (i & 1) * 8);
+    }
+#pragma unroll
+    for (int nn = 0; nn < N / 16; ++nn) {
+      // B operand: k = τ, n; stored [τ][n] -> transposed loads, two n8 tiles
+      uint32_t bf[4];
+      ldsm_x4_t(bf, sB + (16 * ks + (lane & 15)) * RB + 16 * nn + (lane >> 4) * 8);
+      mma_bf16(acc[2 * nn], a, bf[0], bf[1]);
+      mma_bf16(acc[2 * nn + 1], a, bf[2], bf[3]);
+    }
+  }
+  float* out = p.ws_state + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N);
+  const int r0 = 16 * w + (lane >> 2), cc = 2 * (lane & 3);
+#pragma unroll
+  for (int j = 0; j < N / 8; ++j) {
+    *reinterpret_cast<float2*>(out + r0 * N + 8 * j + cc) = make_float2(acc[j][0], acc[j][1]);
+    *reinterpret_cast<float2*>(out + (r0 + 8) * N + 8 * j + cc) = make_float2(acc[j][2], acc[j][3]);
+  }
+  if (threadIdx.x == 0) p.ws_logdecay[(b * p.nch + c) * p.H + h] = s_end;
+}
+
+// ---------------------------------------------------------------------------
+// 2. state passing: H_c = exp(s_end(c)) H_{c-1} + S_c; the state entering each
+//    chunk is stored as bf16 for the chunk-output products
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdArgs p) {
+  constexpr int P = kSsdP, PER = P * N / 256;
+  const int h = blockIdx.x;
+  const int64_t b = blockIdx.y;
+  float hs[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int e = threadIdx.x + k * 256;
+    hs[k] = p.init_state ? p.init_state[(b * p.H + h) * (int64_t)(P * N) + e] : 0.f;
+  }
+  for (int c = 0; c < p.nch; ++c) {
+    const int64_t base = ((b * p.nch + c) * p.H + h) * (int64_t)(P * N);
+    const float decay = __expf(p.ws_logdecay[(b * p.nch + c) * p.H + h]);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int e = threadIdx.x + k * 256;
+      p.ws_hin[base + e] = __float2bfloat16_rn(hs[k]);
+      hs[k] = fmaf(decay, hs[k], p.ws_state[base + e]);
+    }
+  }
+  if (p.final_state) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+      p.final_state[(b * p.H + h) * (int64_t)(P * N) + threadIdx.x + k * 256] = hs[k];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. chunk outputs: y = (mask ∘ C Bᵀ) X + exp(s_t) C Hᵀ + D x, gated
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdArgs p) {
+  constexpr int Q = kSsdQ, P = kSsdP, RX = P + 8, RB = N + 8;
+  extern __shared__ float4 ssd_smem[];
+  __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(ssd_smem);  // [τ][p]
+  __nv_bfloat16* sB = sX + Q * RX;                                 // [τ][n]
+  __nv_bfloat16* sC = sB + Q * RB;                                 // [t][n]
+  __nv_bfloat16* sH = sC + Q * RB;                                 // [p][n], entering state
+  float* sS = reinterpret_cast<float*>(sH + P * RB);
+  float* sBeta = sS + Q;
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int64_t t0 = (int64_t)c * Q;
+  const int valid = (int)min64(Q, p.L - t0);
+  const int g = h / (p.H / p.G);
+  ssd_chunk_terms(p, b, t0, h, sS, sBeta);
+  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
+  ssd_stage(sX, RX, xg, p.H * P, Q, P, valid);
+  const int64_t bc = ((b * p.L + t0) * p.G + g) * N;
+  ssd_stage(sB, RB, static_cast<const __nv_bfloat16*>(p.B) + bc, p.G * N, Q, N, valid);
+  ssd_stage(sC, RB, static_cast<const __nv_bfloat16*>(p.C) + bc, p.G * N, Q, N, valid);
+  ssd_stage(sH, RB, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P, N, P);
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows t in [16w, 16w+16)
+  const int i8 = lane >> 3;
+  // (a) C Bᵀ for this warp's rows and the columns τ <= its last row
+  float cb[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < N / 16; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(a, sC + (16 * w + (lane & 15)) * RB + 16 * ks + (lane >> 4) * 8);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      if (jj > w) break;
+      // B operand = Bᵀ: k = n, columns τ; stored [τ][n] -> plain loads
+      uint32_t bf[4];
+      ldsm_x4(bf, sB + (16 * jj + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
+      mma_bf16(cb[2 * jj], a, bf[0], bf[1]);
+      mma_bf16(cb[2 * jj + 1], a, bf[2], bf[3]);
+    }
+  }
+  // (b) the decay mask and input weight: M[t][τ] = (τ <= t) C_t·B_τ exp(s_t - s_τ) β_τ,
+  //     repacked as bf16 A fragments of the next product (two n8 tiles = one k16 step)
+  const int tr = 16 * w + (lane >> 2);  // this thread's rows tr, tr + 8
+  const float s_r0 = sS[tr], s_r1 = sS[tr + 8];
+  uint32_t am[4][4];
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int j = 2 * kk + half;
+      const int tau = 8 * j + 2 * (lane & 3);
+      float m[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = e < 2 ? tr : tr + 8, col = tau + (e & 1);
+        const float sr = e < 2 ? s_r0 : s_r1;
+        m[e] = (kk <= w && col <= row) ? cb[j][e] * __expf(sr - sS[col]) * sBeta[col] : 0.f;
+      }
+      am[kk][2 * half] = pack_bf16(m[0], m[1]);
+      am[kk][2 * half + 1] = pack_bf16(m[2], m[3]);
+    }
+  }
+  // (c) Y = M X (k = τ up to the warp's rows) and (d) O = C Hᵀ
+  float yv[8][4], ov[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    yv[j][0] = yv[j][1] = yv[j][2] = yv[j][3] = 0.f;
+    ov[j][0] = ov[j][1] = ov[j][2] = ov[j][3] = 0.f;
+  }
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    if (kk > w) break;
+    const uint32_t a[4] = {am[kk][0], am[kk][1], am[kk][2], am[kk][3]};
+#pragma unroll
+    for (int pp = 0; pp < P / 16; ++pp) {
+      // B operand = X: k = τ, columns p; stored [τ][p] -> transposed loads
+      uint32_t bf[4];
+      ldsm_x4_t(bf, sX + (16 * kk + (lane & 15)) * RX + 16 * pp + (lane >> 4) * 8);
+      mma_bf16(yv[2 * pp], a, bf[0], bf[1]);
+      mma_bf16(yv[2 * pp + 1], a, bf[2], bf[3]);
+    }
+  }
+#pragma unroll
+  for (int ks = 0; ks < N / 16; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(a, sC + (16 * w + (lane & 15)) * RB + 16 * ks + (lane >> 4) * 8);
+#pragma unroll
+    for (int pp = 0; pp < P / 16; ++pp) {
+      // B operand = Hᵀ: k = n, columns p; stored [p][n] -> plain loads
+      uint32_t bf[4];
+      ldsm_x4(bf, sH + (16 * pp + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
+      mma_bf16(ov[2 * pp], a, bf[0], bf[1]);
+      mma_bf16(ov[2 * pp + 1], a, bf[2], bf[3]);
+    }
+  }
+  // (e) y = Y + exp(s_t) O + D x, gated, rows inside the sequence only
+  const float Dh = p.D ? p.D[h] : 0.f;
+  const float e0 = __expf(s_r0), e1 = __expf(s_r1);
+  __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y) + ((b * p.L + t0) * p.H + h) * P;
+  const __nv_bfloat16* zg =
+      p.z ? static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P : nullptr;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int col = 8 * j + 2 * (lane & 3);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int row = half ? tr + 8 : tr;
+      if (row >= valid) continue;
+      const float ee = half ? e1 : e0;
+      const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162*>(sX + row * RX + col);
+      float v0 = fmaf(ee, ov[j][2 * half], yv[j][2 * half]) + Dh * __low2float(xv);
+      float v1 = fmaf(ee, ov[j][2 * half + 1], yv[j][2 * half + 1]) + Dh * __high2float(xv);
+      const int64_t off = (int64_t)row * p.H * P + col;
+      if (zg) {
+        const __nv_bfloat162 zv = *reinterpret_cast<const __nv_bfloat162*>(zg + off);
+        v0 *= silu_precise(__low2float(zv));
+        v1 *= silu_precise(__high2float(zv));
+      }
+      *reinterpret_cast<__nv_bfloat162*>(yg + off) = __floats2bfloat162_rn(v0, v1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t N) {
+  SsdLayout w{};
+  w.nch = (L + kSsdQ - 1) / kSsdQ;
+  const size_t units = (size_t)batch * (size_t)w.nch * (size_t)H;
+  const size_t st = units * (size_t)kSsdP * (size_t)N;
+  w.o_state = 0;
+  w.o_hin = (st * 4 + 255) / 256 * 256;
+  w.o_logdecay = w.o_hin + (st * 2 + 255) / 256 * 256;
+  w.bytes = w.o_logdecay + (units * 4 + 255) / 256 * 256;
+  return w;
+}
+
+template <int N>
+static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
+  const dim3 chunks((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch);
+  ssd_chunk_state_kernel<N><<<chunks, kSsdThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ssd_state_pass_kernel<N><<<dim3((unsigned)a.H, (unsigned)a.batch), 256, 0, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  constexpr size_t bytes = (size_t)(kSsdQ * (kSsdP + 8) + 2 * kSsdQ * (N + 8) + kSsdP * (N + 8)) * 2 +
+                           2 * kSsdQ * 4;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(ssd_chunk_scan_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bytes);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  ssd_chunk_scan_kernel<N><<<chunks, kSsdThreads, bytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t ssd_launch(const SsdArgs& a, int64_t N, cudaStream_t stream) {
+  if (a.batch == 0 || a.H == 0 || a.L == 0) return cudaSuccess;
+  switch (N) {
+    case 64: return ssd_typed<64>(a, stream);
+    case 128: return ssd_typed<128>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ssm

@@ -219,3 +219,18 @@ def test_training_forward_argument_errors():
     assert tr(bws=FAKE + 0x10000008) == ssm.SSM_ERR_ALIGN
     assert tr(softplus=ssm.SSM_SAVED_STATES) == ssm.SSM_ERR_ARG  # a backward-only bit
     assert _bwd(softplus=ssm.SSM_SOFTPLUS | ssm.SSM_SAVED_STATES, u=None) == ssm.SSM_ERR_ARG
+
+
+def test_ssd_argument_errors():
+    L_ = lib()
+    args = [FAKE, FAKE + 0x100000, None, FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x400000, None,
+            None, 1, FAKE + 0x500000, None, None]
+    ws = (FAKE + 0x10000000, 1 << 30, None)
+    # headdim other than 64, dstate other than 64/128, heads not a multiple of groups
+    assert L_.ssm_ssd_fwd(*args, 1, 64, 4, 32, 1, 64, *ws) == ssm.SSM_ERR_UNSUPPORTED
+    assert L_.ssm_ssd_fwd(*args, 1, 64, 4, 64, 1, 32, *ws) == ssm.SSM_ERR_UNSUPPORTED
+    assert L_.ssm_ssd_fwd(*args, 1, 64, 4, 64, 3, 64, *ws) == ssm.SSM_ERR_UNSUPPORTED
+    assert L_.ssm_ssd_fwd(*args, 1, 64, 4, 64, 1, 64, None, 0, None) == ssm.SSM_ERR_WORKSPACE
+    assert L_.ssm_ssd_fwd(*args[:8], 5, *args[9:], 1, 64, 4, 64, 1, 64, *ws) == ssm.SSM_ERR_ARG
+    assert L_.ssm_ssd_fwd(*args[:9], FAKE + 0x100, *args[10:], 1, 64, 4, 64, 1, 64, *ws) == ssm.SSM_ERR_ARG
+    assert ssm.ssm_ssd_workspace_bytes(8, 2048, 24, 64, 128) > 8 * 32 * 24 * 64 * 128 * 6
