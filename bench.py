@@ -350,6 +350,71 @@ def bench_conv(w, steps, warmup, world, width=4, copies=3):
 
 
 # ---------------------------------------------------------------------------
+# Mamba-2 SSD (scalar-A SSM, chunked on the tensor cores): a Mamba-2-130M-shaped
+# layer, batch 8, L 2048, 24 heads of 64, one group, N 128, bf16
+# ---------------------------------------------------------------------------
+
+SSD_SHAPE = dict(batch=8, L=2048, H=24, P=64, G=1, N=128)
+
+
+def ssd_flops(batch, L, H, P, G, N, Q=64):
+    """Tensor-core FLOPs the chunked algorithm needs per launch: the causal half of
+    C Bᵀ and of (mask ∘ C Bᵀ) X inside each chunk, C Hᵀ and the chunk state."""
+    nch = (L + Q - 1) // Q
+    tri = Q * (Q + 1) // 2
+    per = 2 * (tri * N + tri * P + Q * N * P + Q * P * N)
+    return per * nch * H * batch
+
+
+def ssd_bytes(batch, L, H, P, G, N):
+    """Algorithmic HBM bytes: x, z, dt read, y written (bf16), B and C read (bf16),
+    A, D, dt bias, and the final state written (fp32)."""
+    return (3 * batch * L * H * P * 2 + batch * L * H * 2 + 2 * batch * L * G * N * 2 + 3 * H * 4
+            + batch * H * P * N * 4)
+
+
+def bench_ssd(steps, warmup, world, seed=5):
+    import torch
+    import selective_state_space_128_b300 as ssm
+    sh = SSD_SHAPE
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    bf = torch.bfloat16
+    b, L, H, P, G, N = sh["batch"], sh["L"], sh["H"], sh["P"], sh["G"], sh["N"]
+    x = torch.randn((b, L, H, P), generator=gen, device="cuda").to(bf)
+    z = torch.randn((b, L, H, P), generator=gen, device="cuda").to(bf)
+    dt = (0.5 * torch.randn((b, L, H), generator=gen, device="cuda")).to(bf)
+    B = torch.randn((b, L, G, N), generator=gen, device="cuda").to(bf)
+    C = torch.randn((b, L, G, N), generator=gen, device="cuda").to(bf)
+    A = -(1.0 + 7.0 * torch.rand(H, generator=gen, device="cuda"))
+    D = 0.5 + torch.rand(H, generator=gen, device="cuda")
+    bias = torch.from_numpy(synth.gen_delta_bias(seed, H)).cuda()
+    y = torch.empty_like(x)
+    h = torch.empty((b, H, P, N), dtype=torch.float32, device="cuda")
+    nbytes = ssm.ssm_ssd_workspace_bytes(b, L, H, P, N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ssm.ssm_ssd_fwd(x, dt, bias, A, B, C, D, z, ssm.SSM_SOFTPLUS, y, h, None, ws, nbytes,
+                        stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / steps
+    return dict(step_ms=ms, steps=steps, workspace_bytes=nbytes)
+
+
+# ---------------------------------------------------------------------------
 # backward pass on the same layer
 # ---------------------------------------------------------------------------
 
@@ -559,6 +624,7 @@ def main():
     ap.add_argument("--bwd-steps", type=int, default=20)
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
+    ap.add_argument("--no-ssd", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = synth.MAMBA_130M
@@ -579,6 +645,7 @@ def main():
     bld_ms = bench_scan_bld(w, r["inputs"], 50, args.warmup, world)
     r.pop("inputs")
     conv = None if args.no_conv else bench_conv(w, 50, args.warmup, world)
+    ssd = None if args.no_ssd else bench_ssd(20, args.warmup, world)
     dec = None if args.no_decode else bench_decode(synth.DECODE, args.decode_steps, world)
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
@@ -654,6 +721,20 @@ def main():
                           "hbm_frac": conv["bytes"] / cs / 1e9 / hbm_peak,
                           "bytes_per_step": conv["bytes"], "gpu_launches": conv["steps"],
                           "l2": "3 input/output pairs rotated: 300 MB, larger than L2"}
+    if ssd is not None:
+        sh = SSD_SHAPE
+        ss = ssd["step_ms"] / 1e3
+        fl = ssd_flops(**sh)
+        nb = ssd_bytes(**sh)
+        line["ssd"] = {"workload": "mamba2_130m_layer_ssd: batch %d, L %d, %d heads x %d, %d group, "
+                                   "N %d, bf16, chunk 64" % (sh["batch"], sh["L"], sh["H"], sh["P"],
+                                                            sh["G"], sh["N"]),
+                       "steps": ssd["steps"], "us_per_step": ssd["step_ms"] * 1e3,
+                       "tokens_per_s": sh["batch"] * sh["L"] / ss * world,
+                       "tensor_tflops": fl / ss / 1e12, "flops_per_step": fl,
+                       "hbm_gbs_algorithmic": nb / ss / 1e9, "bytes_per_step": nb,
+                       "workspace_bytes": ssd["workspace_bytes"], "gpu_launches": 3 * ssd["steps"],
+                       "l2": "x, z, y: 3 x 50 MB plus 300 MB of chunk states per step, larger than L2"}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line))

@@ -90,18 +90,32 @@ __device__ __forceinline__ void ssd_chunk_terms(const SsdArgs& p, int64_t b, int
   __syncthreads();
 }
 
-// Copies `rows` rows of `cols` bf16 (a multiple of 8) from global rows `gstride`
-// elements apart into shared rows `sstride` elements apart; rows at or past
-// `valid` are zero.
-__device__ __forceinline__ void ssd_stage(__nv_bfloat16* dst, int sstride,
-                                          const __nv_bfloat16* src, int64_t gstride, int rows,
-                                          int cols, int valid) {
-  const int vpr = cols / 8;  // 16-byte vectors per row
-  for (int e = threadIdx.x; e < rows * vpr; e += kSsdThreads) {
-    const int r = e / vpr, v = e - r * vpr;
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    if (r < valid) q = *reinterpret_cast<const uint4*>(src + r * gstride + v * 8);
-    *reinterpret_cast<uint4*>(dst + r * sstride + v * 8) = q;
+// 16-byte asynchronous copy global -> shared; with `valid` false nothing is
+// read (source size 0) and the destination is zero-filled.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// Issues the copies of ROWS rows of COLS bf16 (a multiple of 8) from global rows
+// `gstride` elements apart into shared rows SSTRIDE elements apart; rows at or
+// past `valid` are zero-filled (their source is not read).  Every load is in
+// flight at once; the caller waits with cp_async_wait_all().
+template <int ROWS, int COLS, int SSTRIDE>
+__device__ __forceinline__ void ssd_stage(__nv_bfloat16* dst, const __nv_bfloat16* src,
+                                          int64_t gstride, int valid) {
+  constexpr int VPR = COLS / 8;  // 16-byte vectors per row
+  static_assert((ROWS * VPR) % kSsdThreads == 0, "whole copies per thread");
+#pragma unroll
+  for (int k = 0; k < ROWS * VPR / kSsdThreads; ++k) {
+    const int e = threadIdx.x + k * kSsdThreads;
+    const int r = e / VPR, v = e - r * VPR;
+    const bool ok = r < valid;
+    cp_async16(dst + r * SSTRIDE + v * 8, src + (ok ? r : 0) * gstride + v * 8, ok);
   }
 }
 
@@ -119,23 +133,25 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_state_kernel(const SsdA
   const int64_t t0 = (int64_t)c * Q;
   const int valid = (int)min64(Q, p.L - t0);
   const int g = h / (p.H / p.G);
+  // x and B into shared memory (in flight while the step terms are computed);
+  // then x rows scaled by w_τ = exp(s_end - s_τ) β_τ
+  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
+  ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
+  ssd_stage<Q, N, RB>(sB, static_cast<const __nv_bfloat16*>(p.B) + ((b * p.L + t0) * p.G + g) * N,
+                      p.G * N, valid);
   ssd_chunk_terms(p, b, t0, h, sS, sBeta);
   const float s_end = sS[Q - 1];
-  // x rows scaled by w_τ while staging
-  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
+  cp_async_wait_all();
+  __syncthreads();
   for (int e = threadIdx.x; e < Q * (P / 8); e += kSsdThreads) {
     const int r = e / (P / 8), v = e - r * (P / 8);
-    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (r < valid) {
-      vecio<__nv_bfloat16, 8>::load(xg + (int64_t)r * p.H * P + v * 8, f);
-      const float w = __expf(s_end - sS[r]) * sBeta[r];
+    float f[8];
+    vecio<__nv_bfloat16, 8>::load(sX + r * RX + v * 8, f);
+    const float w = __expf(s_end - sS[r]) * sBeta[r];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] *= w;
-    }
+    for (int i = 0; i < 8; ++i) f[i] *= w;
     vecio<__nv_bfloat16, 8>::store(sX + r * RX + v * 8, f);
   }
-  ssd_stage(sB, RB, static_cast<const __nv_bfloat16*>(p.B) + ((b * p.L + t0) * p.G + g) * N,
-            p.G * N, Q, N, valid);
   __syncthreads();
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows p in [16w, 16w+16)
@@ -171,33 +187,60 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_state_kernel(const SsdA
 
 // ---------------------------------------------------------------------------
 // 2. state passing: H_c = exp(s_end(c)) H_{c-1} + S_c; the state entering each
-//    chunk is stored as bf16 for the chunk-output products
+//    chunk is stored as bf16 for the chunk-output products.  Blocks take slices
+//    of 2048 state elements of one head; the chunk decays are staged in shared
+//    memory and each chunk's states are loaded while the previous one is used.
 // ---------------------------------------------------------------------------
+constexpr int kPassThreads = 256, kPassPer = 8;  // 8 state elements per thread
+constexpr int kPassTile = 1024;                    // chunk decays staged per pass
+
 template <int N>
-__global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdArgs p) {
-  constexpr int P = kSsdP, PER = P * N / 256;
+__global__ void __launch_bounds__(kPassThreads) ssd_state_pass_kernel(const SsdArgs p) {
+  constexpr int P = kSsdP;
+  __shared__ float sDecay[kPassTile];
   const int h = blockIdx.x;
   const int64_t b = blockIdx.y;
-  float hs[PER];
+  // this block's slice of the P x N state: blockIdx.z-th run of 256 x 8 elements
+  const int e0 = blockIdx.z * (kPassThreads * kPassPer) + threadIdx.x;
+  float hs[kPassPer], nx[kPassPer];
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int e = threadIdx.x + k * 256;
+  for (int k = 0; k < kPassPer; ++k) {
+    const int e = e0 + k * kPassThreads;
     hs[k] = p.init_state ? p.init_state[(b * p.H + h) * (int64_t)(P * N) + e] : 0.f;
   }
-  for (int c = 0; c < p.nch; ++c) {
-    const int64_t base = ((b * p.nch + c) * p.H + h) * (int64_t)(P * N);
-    const float decay = __expf(p.ws_logdecay[(b * p.nch + c) * p.H + h]);
+  auto state_at = [&](int c) { return p.ws_state + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N); };
+  if (p.nch > 0) {
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int e = threadIdx.x + k * 256;
-      p.ws_hin[base + e] = __float2bfloat16_rn(hs[k]);
-      hs[k] = fmaf(decay, hs[k], p.ws_state[base + e]);
+    for (int k = 0; k < kPassPer; ++k) nx[k] = state_at(0)[e0 + k * kPassThreads];
+  }
+  for (int c0 = 0; c0 < p.nch; c0 += kPassTile) {
+    const int cn = (int)min64(kPassTile, p.nch - c0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < cn; i += kPassThreads)
+      sDecay[i] = __expf(p.ws_logdecay[(b * p.nch + c0 + i) * p.H + h]);
+    __syncthreads();
+    for (int ci = 0; ci < cn; ++ci) {
+      const int c = c0 + ci;
+      float cur[kPassPer];
+#pragma unroll
+      for (int k = 0; k < kPassPer; ++k) cur[k] = nx[k];
+      if (c + 1 < p.nch) {  // the next chunk's states in flight during this one
+#pragma unroll
+        for (int k = 0; k < kPassPer; ++k) nx[k] = state_at(c + 1)[e0 + k * kPassThreads];
+      }
+      const float decay = sDecay[ci];
+      __nv_bfloat16* hin = p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N);
+#pragma unroll
+      for (int k = 0; k < kPassPer; ++k) {
+        hin[e0 + k * kPassThreads] = __float2bfloat16_rn(hs[k]);
+        hs[k] = fmaf(decay, hs[k], cur[k]);
+      }
     }
   }
   if (p.final_state) {
 #pragma unroll
-    for (int k = 0; k < PER; ++k)
-      p.final_state[(b * p.H + h) * (int64_t)(P * N) + threadIdx.x + k * 256] = hs[k];
+    for (int k = 0; k < kPassPer; ++k)
+      p.final_state[(b * p.H + h) * (int64_t)(P * N) + e0 + k * kPassThreads] = hs[k];
   }
 }
 
@@ -212,20 +255,25 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   __nv_bfloat16* sB = sX + Q * RX;                                 // [τ][n]
   __nv_bfloat16* sC = sB + Q * RB;                                 // [t][n]
   __nv_bfloat16* sH = sC + Q * RB;                                 // [p][n], entering state
-  float* sS = reinterpret_cast<float*>(sH + P * RB);
+  __nv_bfloat16* sZ = sH + P * RB;                                 // [t][p], the gate
+  float* sS = reinterpret_cast<float*>(sZ + Q * RX);
   float* sBeta = sS + Q;
   const int c = blockIdx.x, h = blockIdx.y;
   const int64_t b = blockIdx.z;
   const int64_t t0 = (int64_t)c * Q;
   const int valid = (int)min64(Q, p.L - t0);
   const int g = h / (p.H / p.G);
-  ssd_chunk_terms(p, b, t0, h, sS, sBeta);
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
-  ssd_stage(sX, RX, xg, p.H * P, Q, P, valid);
+  ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
   const int64_t bc = ((b * p.L + t0) * p.G + g) * N;
-  ssd_stage(sB, RB, static_cast<const __nv_bfloat16*>(p.B) + bc, p.G * N, Q, N, valid);
-  ssd_stage(sC, RB, static_cast<const __nv_bfloat16*>(p.C) + bc, p.G * N, Q, N, valid);
-  ssd_stage(sH, RB, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P, N, P);
+  ssd_stage<Q, N, RB>(sB, static_cast<const __nv_bfloat16*>(p.B) + bc, p.G * N, valid);
+  ssd_stage<Q, N, RB>(sC, static_cast<const __nv_bfloat16*>(p.C) + bc, p.G * N, valid);
+  ssd_stage<P, N, RB>(sH, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P);
+  if (p.z)
+    ssd_stage<Q, P, RX>(sZ, static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P,
+                        p.H * P, valid);
+  ssd_chunk_terms(p, b, t0, h, sS, sBeta);  // while the copies are in flight
+  cp_async_wait_all();
   __syncthreads();
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows t in [16w, 16w+16)
@@ -307,8 +355,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   const float Dh = p.D ? p.D[h] : 0.f;
   const float e0 = __expf(s_r0), e1 = __expf(s_r1);
   __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y) + ((b * p.L + t0) * p.H + h) * P;
-  const __nv_bfloat16* zg =
-      p.z ? static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P : nullptr;
+  const bool gate = p.z != nullptr;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int col = 8 * j + 2 * (lane & 3);
@@ -321,8 +368,8 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
       float v0 = fmaf(ee, ov[j][2 * half], yv[j][2 * half]) + Dh * __low2float(xv);
       float v1 = fmaf(ee, ov[j][2 * half + 1], yv[j][2 * half + 1]) + Dh * __high2float(xv);
       const int64_t off = (int64_t)row * p.H * P + col;
-      if (zg) {
-        const __nv_bfloat162 zv = *reinterpret_cast<const __nv_bfloat162*>(zg + off);
+      if (gate) {
+        const __nv_bfloat162 zv = *reinterpret_cast<const __nv_bfloat162*>(sZ + row * RX + col);
         v0 *= silu_precise(__low2float(zv));
         v1 *= silu_precise(__high2float(zv));
       }
@@ -352,11 +399,12 @@ static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
   ssd_chunk_state_kernel<N><<<chunks, kSsdThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ssd_state_pass_kernel<N><<<dim3((unsigned)a.H, (unsigned)a.batch), 256, 0, s>>>(a);
+  constexpr int kSlices = kSsdP * N / (kPassThreads * kPassPer);
+  ssd_state_pass_kernel<N><<<dim3((unsigned)a.H, (unsigned)a.batch, kSlices), kPassThreads, 0, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  constexpr size_t bytes = (size_t)(kSsdQ * (kSsdP + 8) + 2 * kSsdQ * (N + 8) + kSsdP * (N + 8)) * 2 +
-                           2 * kSsdQ * 4;
+  constexpr size_t bytes =
+      (size_t)(2 * kSsdQ * (kSsdP + 8) + 2 * kSsdQ * (N + 8) + kSsdP * (N + 8)) * 2 + 2 * kSsdQ * 4;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
