@@ -278,10 +278,15 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows t in [16w, 16w+16)
   const int i8 = lane >> 3;
-  // (a) C Bᵀ for this warp's rows and the columns τ <= its last row
-  float cb[8][4];
+  // (a) C Bᵀ for this warp's rows and the columns τ <= its last row, and (d)
+  //     O = C Hᵀ: both take the same A fragments of C, so one pass over k = n
+  //     feeds up to 16 independent accumulators
+  float cb[8][4], ov[8][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
+  for (int j = 0; j < 8; ++j) {
+    cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
+    ov[j][0] = ov[j][1] = ov[j][2] = ov[j][3] = 0.f;
+  }
 #pragma unroll
   for (int ks = 0; ks < N / 16; ++ks) {
     uint32_t a[4];
@@ -294,6 +299,14 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
       ldsm_x4(bf, sB + (16 * jj + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
       mma_bf16(cb[2 * jj], a, bf[0], bf[1]);
       mma_bf16(cb[2 * jj + 1], a, bf[2], bf[3]);
+    }
+#pragma unroll
+    for (int pp = 0; pp < P / 16; ++pp) {
+      // B operand = Hᵀ: k = n, columns p; stored [p][n] -> plain loads
+      uint32_t bf[4];
+      ldsm_x4(bf, sH + (16 * pp + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
+      mma_bf16(ov[2 * pp], a, bf[0], bf[1]);
+      mma_bf16(ov[2 * pp + 1], a, bf[2], bf[3]);
     }
   }
   // (b) the decay mask and input weight: M[t][τ] = (τ <= t) C_t·B_τ exp(s_t - s_τ) β_τ,
@@ -318,13 +331,10 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
       am[kk][2 * half + 1] = pack_bf16(m[2], m[3]);
     }
   }
-  // (c) Y = M X (k = τ up to the warp's rows) and (d) O = C Hᵀ
-  float yv[8][4], ov[8][4];
+  // (c) Y = M X (k = τ up to the warp's rows)
+  float yv[8][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    yv[j][0] = yv[j][1] = yv[j][2] = yv[j][3] = 0.f;
-    ov[j][0] = ov[j][1] = ov[j][2] = ov[j][3] = 0.f;
-  }
+  for (int j = 0; j < 8; ++j) yv[j][0] = yv[j][1] = yv[j][2] = yv[j][3] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
     if (kk > w) break;
@@ -336,19 +346,6 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
       ldsm_x4_t(bf, sX + (16 * kk + (lane & 15)) * RX + 16 * pp + (lane >> 4) * 8);
       mma_bf16(yv[2 * pp], a, bf[0], bf[1]);
       mma_bf16(yv[2 * pp + 1], a, bf[2], bf[3]);
-    }
-  }
-#pragma unroll
-  for (int ks = 0; ks < N / 16; ++ks) {
-    uint32_t a[4];
-    ldsm_x4(a, sC + (16 * w + (lane & 15)) * RB + 16 * ks + (lane >> 4) * 8);
-#pragma unroll
-    for (int pp = 0; pp < P / 16; ++pp) {
-      // B operand = Hᵀ: k = n, columns p; stored [p][n] -> plain loads
-      uint32_t bf[4];
-      ldsm_x4(bf, sH + (16 * pp + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
-      mma_bf16(ov[2 * pp], a, bf[0], bf[1]);
-      mma_bf16(ov[2 * pp + 1], a, bf[2], bf[3]);
     }
   }
   // (e) y = Y + exp(s_t) O + D x, gated, rows inside the sequence only
