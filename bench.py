@@ -180,13 +180,21 @@ def barrier(world):
 
 
 def max_over_ranks(world, value: float) -> float:
+    """The largest of every rank's value (the slowest rank's time bounds the job)."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(per_rank_units: float, max_seconds: float, world: int) -> float:
+    """Weak scaling: every rank processes its own full workload, so the job's
+    throughput is all ranks' units over the slowest rank's time."""
+    return per_rank_units * world / max_seconds
 
 
 # ---------------------------------------------------------------------------
@@ -654,8 +662,8 @@ def main():
     step_s = r["ms"] / 1e3 / args.steps
     nbytes = scan_bytes(w)
     gbs_rank = nbytes / step_s / 1e9
-    value = gbs_rank * world
-    chsteps = w.channel_steps / step_s * world
+    value = job_throughput(nbytes / 1e9, step_s, world)   # GB/s over all ranks
+    chsteps = job_throughput(w.channel_steps, step_s, world)
     ops = fp32_ops_per_channel_step(w.dstate) * w.channel_steps
     alu_peak = 148 * 128 * sm_max * 1e6 / 1e12          # FP32 lanes x max SM clock, TOP/s
     alu_ach = ops / step_s / 1e12
