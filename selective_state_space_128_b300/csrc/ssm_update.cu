@@ -18,7 +18,10 @@
 //    state per thread are in flight at once;
 //  * the grid is (channel blocks, batch): no integer division per thread, and
 //    the block's B/C row is shared by all of its channels.
-// The G partial readouts of a channel are summed with two xor-shuffles.
+// The G partial readouts of a channel are summed with two xor-shuffles.  The
+// state's 16-byte loads and stores carry streaming cache hints (evict first):
+// 40.8 -> 39.0 us per step at batch 256 x d_inner 5120 (the hint on the loads
+// alone measured 49.9 us).
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -75,7 +78,8 @@ __global__ void __launch_bounds__(kUpdThreads) update_kernel(const UpdateArgs p)
     if constexpr (NPT % 4 == 0) {
 #pragma unroll
       for (int j = 0; j < NPT; j += 4) {
-        const float4 s4 = *reinterpret_cast<const float4*>(sp + j);
+        // the state is read once and written once per step: streaming cache hints
+        const float4 s4 = __ldcs(reinterpret_cast<const float4*>(sp + j));
         const float4 a4 = __ldg(reinterpret_cast<const float4*>(Ap + j));
         st[k][j] = s4.x; st[k][j + 1] = s4.y; st[k][j + 2] = s4.z; st[k][j + 3] = s4.w;
         Av[k][j] = a4.x; Av[k][j + 1] = a4.y; Av[k][j + 2] = a4.z; Av[k][j + 3] = a4.w;
@@ -125,8 +129,8 @@ __global__ void __launch_bounds__(kUpdThreads) update_kernel(const UpdateArgs p)
     if constexpr (NPT % 4 == 0) {
 #pragma unroll
       for (int j = 0; j < NPT; j += 4)
-        *reinterpret_cast<float4*>(sp + j) =
-            make_float4(st[k][j], st[k][j + 1], st[k][j + 2], st[k][j + 3]);
+        __stcs(reinterpret_cast<float4*>(sp + j),
+               make_float4(st[k][j], st[k][j + 1], st[k][j + 2], st[k][j + 3]));
     } else {
 #pragma unroll
       for (int j = 0; j < NPT; ++j) sp[j] = st[k][j];
