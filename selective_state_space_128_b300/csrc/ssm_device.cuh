@@ -170,46 +170,46 @@ template <int E> struct vecio<__nv_bfloat16, E> {
   __device__ static void load(const __nv_bfloat16* p, float (&v)[E]) {
     if constexpr (E == 1) {
       v[0] = __bfloat162float(*p);
-      return;
-    }
-    uint32_t w[E / 2 > 0 ? E / 2 : 1];
-    if constexpr (E == 2) {
-      w[0] = *reinterpret_cast<const uint32_t*>(p);
-    } else if constexpr (E == 4) {
-      const uint2 q = *reinterpret_cast<const uint2*>(p);
-      w[0] = q.x; w[1] = q.y;
     } else {
+      uint32_t w[E / 2];
+      if constexpr (E == 2) {
+        w[0] = *reinterpret_cast<const uint32_t*>(p);
+      } else if constexpr (E == 4) {
+        const uint2 q = *reinterpret_cast<const uint2*>(p);
+        w[0] = q.x; w[1] = q.y;
+      } else {
 #pragma unroll
-      for (int k = 0; k < E / 8; ++k) {
-        const uint4 q = reinterpret_cast<const uint4*>(p)[k];
-        w[4 * k] = q.x; w[4 * k + 1] = q.y; w[4 * k + 2] = q.z; w[4 * k + 3] = q.w;
+        for (int k = 0; k < E / 8; ++k) {
+          const uint4 q = reinterpret_cast<const uint4*>(p)[k];
+          w[4 * k] = q.x; w[4 * k + 1] = q.y; w[4 * k + 2] = q.z; w[4 * k + 3] = q.w;
+        }
       }
-    }
 #pragma unroll
-    for (int i = 0; i < E / 2; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      for (int i = 0; i < E / 2; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
     }
   }
   __device__ static void store(__nv_bfloat16* p, const float (&v)[E]) {
     if constexpr (E == 1) {
       *p = __float2bfloat16_rn(v[0]);
-      return;
-    }
-    uint32_t w[E / 2 > 0 ? E / 2 : 1];
-#pragma unroll
-    for (int i = 0; i < E / 2; ++i) {
-      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-      w[i] = *reinterpret_cast<const uint32_t*>(&h2);
-    }
-    if constexpr (E == 2) {
-      *reinterpret_cast<uint32_t*>(p) = w[0];
-    } else if constexpr (E == 4) {
-      *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
     } else {
+      uint32_t w[E / 2];
 #pragma unroll
-      for (int k = 0; k < E / 8; ++k)
-        reinterpret_cast<uint4*>(p)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+      for (int i = 0; i < E / 2; ++i) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      if constexpr (E == 2) {
+        *reinterpret_cast<uint32_t*>(p) = w[0];
+      } else if constexpr (E == 4) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < E / 8; ++k)
+          reinterpret_cast<uint4*>(p)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+      }
     }
   }
 };
@@ -217,29 +217,27 @@ template <int E> struct vecio<float, E> {
   __device__ static void load(const float* p, float (&v)[E]) {
     if constexpr (E == 1) {
       v[0] = *p;
-      return;
     } else if constexpr (E == 2) {
       const float2 q = *reinterpret_cast<const float2*>(p);
       v[0] = q.x; v[1] = q.y;
-      return;
-    }
+    } else {
 #pragma unroll
-    for (int k = 0; k < E / 4; ++k) {
-      const float4 q = reinterpret_cast<const float4*>(p)[k];
-      v[4 * k] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
+      for (int k = 0; k < E / 4; ++k) {
+        const float4 q = reinterpret_cast<const float4*>(p)[k];
+        v[4 * k] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
+      }
     }
   }
   __device__ static void store(float* p, const float (&v)[E]) {
     if constexpr (E == 1) {
       *p = v[0];
-      return;
     } else if constexpr (E == 2) {
       *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
-      return;
-    }
+    } else {
 #pragma unroll
-    for (int k = 0; k < E / 4; ++k)
-      reinterpret_cast<float4*>(p)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      for (int k = 0; k < E / 4; ++k)
+        reinterpret_cast<float4*>(p)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    }
   }
 };
 
