@@ -100,6 +100,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int K> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
+}
 
 // Issues the copies of ROWS rows of COLS bf16 (a multiple of 8) from global rows
 // `gstride` elements apart into shared rows SSTRIDE elements apart; rows at or
@@ -264,16 +268,20 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   const int valid = (int)min64(Q, p.L - t0);
   const int g = h / (p.H / p.G);
   const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
-  ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
+  // two copy groups: B, C and the entering state first (the products C Bᵀ and
+  // C Hᵀ need only them), then x and z, which arrive while those run
   const int64_t bc = ((b * p.L + t0) * p.G + g) * N;
   ssd_stage<Q, N, RB>(sB, static_cast<const __nv_bfloat16*>(p.B) + bc, p.G * N, valid);
   ssd_stage<Q, N, RB>(sC, static_cast<const __nv_bfloat16*>(p.C) + bc, p.G * N, valid);
   ssd_stage<P, N, RB>(sH, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P);
+  cp_async_commit();
+  ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
   if (p.z)
     ssd_stage<Q, P, RX>(sZ, static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P,
                         p.H * P, valid);
+  cp_async_commit();
   ssd_chunk_terms(p, b, t0, h, sS, sBeta);  // while the copies are in flight
-  cp_async_wait_all();
+  cp_async_wait<1>();
   __syncthreads();
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows t in [16w, 16w+16)
@@ -309,6 +317,8 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
       mma_bf16(ov[2 * pp + 1], a, bf[2], bf[3]);
     }
   }
+  cp_async_wait<0>();  // x and z
+  __syncthreads();
   // (b) the decay mask and input weight: M[t][τ] = (τ <= t) C_t·B_τ exp(s_t - s_τ) β_τ,
   //     repacked as bf16 A fragments of the next product (two n8 tiles = one k16 step)
   const int tr = 16 * w + (lane >> 2);  // this thread's rows tr, tr + 8
