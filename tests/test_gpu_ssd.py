@@ -38,11 +38,13 @@ def _f32(bits):
 
 
 @pytest.mark.parametrize("case", ["n64_g2", "n128_g1", "ragged", "no_gate_no_D", "init_state",
-                                  "euler", "no_softplus", "one_chunk", "single_step"])
+                                  "euler", "no_softplus", "one_chunk", "single_step",
+                                  "three_heads_per_group"])
 def test_ssd_matches_oracle(case):
     cfg = dict(batch=2, L=200, H=4, G=2, N=64)
     cfg.update(dict(n128_g1=dict(N=128, G=1), ragged=dict(L=131), one_chunk=dict(L=64),
-                    single_step=dict(L=1), init_state=dict(L=150)).get(case, {}))
+                    single_step=dict(L=1), init_state=dict(L=150),
+                    three_heads_per_group=dict(H=6, G=2, L=100)).get(case, {}))
     x = _inputs(seed=300 + len(case), **cfg)
     use_z = case != "no_gate_no_D"
     use_D = case != "no_gate_no_D"
@@ -64,3 +66,23 @@ def test_ssd_matches_oracle(case):
     assert np.isfinite(host64(y)).all()
     assert ey <= TOL, ey
     assert eh <= TOL, eh
+
+
+@pytest.mark.slow
+def test_ssd_bench_shape_sampled():
+    """The bench's Mamba-2-130M-shaped layer (batch 8, L 2048, 24 heads x 64, N 128) on
+    the GPU; the oracle recomputes 3 sampled (batch, head) pairs over the whole
+    sequence (y at every step, and the final state)."""
+    cfg = dict(batch=8, L=2048, H=24, G=1, N=128)
+    x = _inputs(seed=350, **cfg)
+    y, h = ssm.ssd(dev_io(x["x"]), dev_io(x["dt"]), dev_f32(x["A"]), dev_io(x["B"]),
+                   dev_io(x["C"]), dev_f32(x["D"]), dev_io(x["z"]), dev_f32(x["bias"]))
+    torch.cuda.synchronize()
+    yh, hh = host64(y), host64(h)
+    for b, hd in ((0, 0), (3, 11), (7, 23)):
+        sl = lambda a: np.ascontiguousarray(a[b:b + 1, :, hd:hd + 1])
+        y_ref, h_ref = oracle.ssd(sl(x["x"]), sl(x["dt"]), x["A"][hd:hd + 1],
+                                  _f32(x["B"][b:b + 1]), _f32(x["C"][b:b + 1]),
+                                  x["D"][hd:hd + 1], sl(x["z"]), x["bias"][hd:hd + 1], True)
+        assert oracle.rel_err(yh[b:b + 1, :, hd:hd + 1], y_ref) <= TOL
+        assert oracle.rel_err(hh[b:b + 1, hd:hd + 1], h_ref) <= TOL
