@@ -742,7 +742,7 @@ def main():
                        "tensor_tflops": fl / ss / 1e12, "flops_per_step": fl,
                        "hbm_gbs_algorithmic": nb / ss / 1e9, "bytes_per_step": nb,
                        "workspace_bytes": ssd["workspace_bytes"], "gpu_launches": 3 * ssd["steps"],
-                       "l2": "x, z, y: 3 x 50 MB plus 300 MB of chunk states per step, larger than L2"}
+                       "l2": "x, z, y: 3 x 50 MB plus the 100 MB of bf16 chunk-entering states written and read per step, larger than L2"}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line))

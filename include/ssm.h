@@ -334,10 +334,10 @@ int ssm_scan_fwd_train(const void* u, const void* delta, const float* delta_bias
  * A, D, dt_bias (nheads) fp32; init_state, final_state (batch, nheads,
  * headdim, dstate) fp32 (nullable).  Supported: headdim 64, dstate 64 or 128,
  * nheads a multiple of ngroups (SSM_ERR_UNSUPPORTED otherwise).  Workspace:
- * ssm_ssd_workspace_bytes() bytes (chunk states, the states entering each
- * chunk, chunk decays), required when batch, seqlen and nheads are non-zero.
- * Products in bf16 with fp32 accumulation; the chunk states are kept in fp32
- * and enter the chunk outputs as bf16.  Errors as the other entry points;
+ * ssm_ssd_workspace_bytes() bytes (the states entering each chunk, the
+ * chunks' step terms), required when batch, seqlen and nheads are non-zero.
+ * Products in bf16 with fp32 accumulation; the running state is kept in fp32
+ * and enters the chunk outputs as bf16.  Errors as the other entry points;
  * asynchronous on `stream` (three kernels).
  */
 size_t ssm_ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,

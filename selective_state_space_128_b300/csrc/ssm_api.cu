@@ -130,9 +130,8 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
   ssm::SsdArgs a{};
   a.x = x; a.dt = dt; a.dt_bias = dt_bias; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.y = y;
   a.final_state = final_state; a.init_state = init_state;
-  a.ws_state = reinterpret_cast<float*>(ws + lay.o_state);
   a.ws_hin = reinterpret_cast<__nv_bfloat16*>(ws + lay.o_hin);
-  a.ws_logdecay = reinterpret_cast<float*>(ws + lay.o_logdecay);
+  a.ws_terms = reinterpret_cast<float*>(ws + lay.o_terms);
   a.batch = batch; a.L = seqlen; a.H = nheads; a.G = ngroups; a.nch = lay.nch;
   a.softplus = (flags & SSM_SOFTPLUS) != 0;
   a.euler = (flags & SSM_EULER_B) != 0;

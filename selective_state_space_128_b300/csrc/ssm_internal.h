@@ -158,9 +158,9 @@ cudaError_t conv_launch(const ConvArgs& a, int64_t width, int io_dtype, bool upd
 
 // Arguments of the chunked scalar-A SSM (Mamba-2 SSD).  x, z, y (batch, L, H,
 // P) bf16; dt (batch, L, H) bf16; B, C (batch, L, G, N) bf16; A, D, dt_bias (H)
-// fp32; states (batch, H, P, N) fp32.  Workspace parts: per-chunk states
-// [batch][nch][H][P][N] fp32, the states entering each chunk (same shape, bf16),
-// per-chunk log decays [batch][nch][H] fp32.
+// fp32; states (batch, H, P, N) fp32.  Workspace parts: the states entering
+// each chunk [batch][nch][H][P][N] bf16 and the chunks' step terms
+// [batch][nch][H][s | β | w] (3 x 64 fp32).
 struct SsdArgs {
   const void* x;
   const void* dt;
@@ -173,9 +173,8 @@ struct SsdArgs {
   void* y;
   float* final_state;
   const float* init_state;
-  float* ws_state;
   __nv_bfloat16* ws_hin;
-  float* ws_logdecay;
+  float* ws_terms;
   int64_t batch, L, H, G, nch;
   int softplus;
   int euler;
@@ -183,7 +182,7 @@ struct SsdArgs {
 
 struct SsdLayout {
   int64_t nch;
-  size_t o_state, o_hin, o_logdecay, bytes;
+  size_t o_hin, o_terms, bytes;
 };
 
 SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t N);

@@ -14,12 +14,14 @@
 //   chunk output   y_t = Σ_{τ<=t} (C_t·B_τ) exp(s_t - s_τ) β_τ x_τ
 //                        + exp(s_t) C_t H_{c-1} + D_h x_t       (then · silu(z_t))
 //
-// Three launches: chunk states (all chunks in parallel), the state pass
-// (sequential over chunks, parallel over heads and state elements), chunk
-// outputs (all chunks in parallel).  The products run on the tensor cores as
-// mma.sync m16n8k16 bf16 with fp32 accumulation, operands staged in padded
-// shared-memory rows (144- or 272-byte rows: ldmatrix's eight row addresses
-// fall in distinct bank groups).  Layouts are Mamba-2's: x, z, y (batch, L, H,
+// Three launches: the chunks' step terms (all chunks in parallel), one walk
+// over the chunks that forms each chunk's state contribution on the tensor
+// cores and passes the running state on (parallel over heads and slices of the
+// state's rows; the state never leaves the registers, only the bf16 copy each
+// chunk's outputs read), and the chunk outputs (all chunks in parallel).  The
+// products run on the tensor cores as mma.sync m16n8k16 bf16 with fp32
+// accumulation, operands staged in padded shared-memory rows (ldmatrix's eight
+// row addresses fall in distinct bank groups).  Layouts are Mamba-2's: x, z, y (batch, L, H,
 // P); dt (batch, L, H); B, C (batch, L, G, N); states (batch, H, P, N).
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -54,42 +56,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Per-chunk step terms of one head, shared by the chunk kernels: Δ·a (log
-// decay) cumulated over the chunk into sS, and the input weight β into sBeta.
-// Steps past the sequence get Δ = 0 (decay 1, weight 0).  128 threads.
-__device__ __forceinline__ void ssd_chunk_terms(const SsdArgs& p, int64_t b, int64_t t0, int h,
-                                                float* sS, float* sBeta) {
-  const int tid = threadIdx.x;
-  const float a = p.A[h];
-  if (tid < kSsdQ) {
-    const int64_t t = t0 + tid;
-    float dA = 0.f, beta = 0.f;
-    if (t < p.L) {
-      const float x = __bfloat162float(static_cast<const __nv_bfloat16*>(p.dt)[(b * p.L + t) * p.H + h]) +
-                      (p.dt_bias ? p.dt_bias[h] : 0.f);
-      const float dt = p.softplus ? softplus_precise(x) : x;
-      dA = dt * a;
-      beta = p.euler ? dt : (a != 0.f ? expm1f(dA) / a : dt);
-    }
-    sS[tid] = dA;
-    sBeta[tid] = beta;
-  }
-  __syncthreads();
-  if (tid < 32) {  // inclusive prefix sum of the 64 log decays: 2 per lane, a warp scan
-    const float v0 = sS[2 * tid], v1 = sS[2 * tid + 1];
-    float run = v0 + v1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float n = __shfl_up_sync(0xffffffffu, run, o);
-      if (tid >= o) run += n;
-    }
-    const float excl = run - (v0 + v1);
-    sS[2 * tid] = excl + v0;
-    sS[2 * tid + 1] = run;
-  }
-  __syncthreads();
-}
-
 // 16-byte asynchronous copy global -> shared; with `valid` false nothing is
 // read (source size 0) and the destination is zero-filled.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -109,14 +75,14 @@ template <int K> __device__ __forceinline__ void cp_async_wait() {
 // `gstride` elements apart into shared rows SSTRIDE elements apart; rows at or
 // past `valid` are zero-filled (their source is not read).  Every load is in
 // flight at once; the caller waits with cp_async_wait_all().
-template <int ROWS, int COLS, int SSTRIDE>
+template <int ROWS, int COLS, int SSTRIDE, int THREADS = kSsdThreads>
 __device__ __forceinline__ void ssd_stage(__nv_bfloat16* dst, const __nv_bfloat16* src,
                                           int64_t gstride, int valid) {
   constexpr int VPR = COLS / 8;  // 16-byte vectors per row
-  static_assert((ROWS * VPR) % kSsdThreads == 0, "whole copies per thread");
+  static_assert((ROWS * VPR) % THREADS == 0, "whole copies per thread");
 #pragma unroll
-  for (int k = 0; k < ROWS * VPR / kSsdThreads; ++k) {
-    const int e = threadIdx.x + k * kSsdThreads;
+  for (int k = 0; k < ROWS * VPR / THREADS; ++k) {
+    const int e = threadIdx.x + k * THREADS;
     const int r = e / VPR, v = e - r * VPR;
     const bool ok = r < valid;
     cp_async16(dst + r * SSTRIDE + v * 8, src + (ok ? r : 0) * gstride + v * 8, ok);
@@ -124,127 +90,198 @@ __device__ __forceinline__ void ssd_stage(__nv_bfloat16* dst, const __nv_bfloat1
 }
 
 // ---------------------------------------------------------------------------
-// 1. chunk states: S_c[p][n] = Σ_τ (w_τ x_τ[p]) B_τ[n],  w_τ = exp(s_end - s_τ) β_τ
+// 0. step terms, one warp per (batch, chunk, head): Δ = softplus(dt + bias),
+//    the cumulative log decay s_t = Σ_{k<=t in the chunk} Δ_k a_h, the input
+//    weight β_t ((exp(Δ a) - 1)/a, or Δ with the Euler flag) and
+//    w_t = exp(s_end - s_t) β_t, stored as [s | β | w] (64 floats each) for
+//    the two chunk kernels.  Steps past the sequence get Δ = 0 (decay 1,
+//    weight 0).  A lane takes two steps; s is a warp prefix sum.
 // ---------------------------------------------------------------------------
-template <int N>
-__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_state_kernel(const SsdArgs p) {
-  constexpr int Q = kSsdQ, P = kSsdP, RX = P + 8, RB = N + 8;
-  __shared__ __align__(16) __nv_bfloat16 sX[Q * RX];   // w-scaled x, [τ][p]
-  __shared__ __align__(16) __nv_bfloat16 sB[Q * RB];   // B, [τ][n]
-  __shared__ float sS[Q], sBeta[Q];
-  const int c = blockIdx.x, h = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int64_t t0 = (int64_t)c * Q;
-  const int valid = (int)min64(Q, p.L - t0);
-  const int g = h / (p.H / p.G);
-  // x and B into shared memory (in flight while the step terms are computed);
-  // then x rows scaled by w_τ = exp(s_end - s_τ) β_τ
-  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
-  ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
-  ssd_stage<Q, N, RB>(sB, static_cast<const __nv_bfloat16*>(p.B) + ((b * p.L + t0) * p.G + g) * N,
-                      p.G * N, valid);
-  ssd_chunk_terms(p, b, t0, h, sS, sBeta);
-  const float s_end = sS[Q - 1];
-  cp_async_wait_all();
-  __syncthreads();
-  for (int e = threadIdx.x; e < Q * (P / 8); e += kSsdThreads) {
-    const int r = e / (P / 8), v = e - r * (P / 8);
-    float f[8];
-    vecio<__nv_bfloat16, 8>::load(sX + r * RX + v * 8, f);
-    const float w = __expf(s_end - sS[r]) * sBeta[r];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) f[i] *= w;
-    vecio<__nv_bfloat16, 8>::store(sX + r * RX + v * 8, f);
-  }
-  __syncthreads();
+constexpr int kTermsThreads = 128;
+constexpr int kTermsRec = 3 * kSsdQ;  // floats per (batch, chunk, head)
 
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows p in [16w, 16w+16)
-  float acc[N / 8][4];
+__global__ void __launch_bounds__(kTermsThreads) ssd_terms_kernel(const SsdArgs p) {
+  constexpr int Q = kSsdQ;
+  const int lane = threadIdx.x & 31;
+  const int64_t unit = (int64_t)blockIdx.x * (kTermsThreads / 32) + (threadIdx.x >> 5);
+  if (unit >= p.batch * p.nch * p.H) return;  // whole warps
+  const int h = (int)(unit % p.H);
+  const int64_t bc = unit / p.H;
+  const int64_t c = bc % p.nch, b = bc / p.nch;
+  const float a = p.A[h];
+  const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
+  float dA[2], beta[2];
 #pragma unroll
-  for (int j = 0; j < N / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < Q / 16; ++ks) {
-    // A = (w x)ᵀ: rows p, k = τ; stored [τ][p] -> transposed loads
-    uint32_t a[4];
-    {
-      const int i = lane >> 3;
-      ldsm_x4_t(a, sX + (16 * ks + (i >> 1) * 8 + (lane & 7)) * RX + 16 * w + (i & 1) * 8);
-    }
-#pragma unroll
-    for (int nn = 0; nn < N / 16; ++nn) {
-      // B operand: k = τ, n; stored [τ][n] -> transposed loads, two n8 tiles
-      uint32_t bf[4];
-      ldsm_x4_t(bf, sB + (16 * ks + (lane & 15)) * RB + 16 * nn + (lane >> 4) * 8);
-      mma_bf16(acc[2 * nn], a, bf[0], bf[1]);
-      mma_bf16(acc[2 * nn + 1], a, bf[2], bf[3]);
+  for (int i = 0; i < 2; ++i) {
+    const int64_t t = c * Q + 2 * lane + i;
+    dA[i] = 0.f;
+    beta[i] = 0.f;
+    if (t < p.L) {
+      const float x = __bfloat162float(static_cast<const __nv_bfloat16*>(p.dt)[(b * p.L + t) * p.H + h]) + bias;
+      const float dt = p.softplus ? softplus_precise(x) : x;
+      dA[i] = dt * a;
+      beta[i] = p.euler ? dt : (a != 0.f ? expm1f(dA[i]) / a : dt);
     }
   }
-  float* out = p.ws_state + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N);
-  const int r0 = 16 * w + (lane >> 2), cc = 2 * (lane & 3);
+  float run = dA[0] + dA[1];
 #pragma unroll
-  for (int j = 0; j < N / 8; ++j) {
-    *reinterpret_cast<float2*>(out + r0 * N + 8 * j + cc) = make_float2(acc[j][0], acc[j][1]);
-    *reinterpret_cast<float2*>(out + (r0 + 8) * N + 8 * j + cc) = make_float2(acc[j][2], acc[j][3]);
+  for (int o = 1; o < 32; o <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, run, o);
+    if (lane >= o) run += n;
   }
-  if (threadIdx.x == 0) p.ws_logdecay[(b * p.nch + c) * p.H + h] = s_end;
+  const float s0 = (run - (dA[0] + dA[1])) + dA[0];
+  const float s_end = __shfl_sync(0xffffffffu, run, 31);
+  float* out = p.ws_terms + unit * kTermsRec + 2 * lane;
+  *reinterpret_cast<float2*>(out) = make_float2(s0, run);
+  *reinterpret_cast<float2*>(out + Q) = make_float2(beta[0], beta[1]);
+  *reinterpret_cast<float2*>(out + 2 * Q) =
+      make_float2(__expf(s_end - s0) * beta[0], __expf(s_end - run) * beta[1]);
 }
 
 // ---------------------------------------------------------------------------
-// 2. state passing: H_c = exp(s_end(c)) H_{c-1} + S_c; the state entering each
-//    chunk is stored as bf16 for the chunk-output products.  Blocks take slices
-//    of 2048 state elements of one head; the chunk decays are staged in shared
-//    memory and each chunk's states are loaded while the previous one is used.
+// 1. chunk states and state passing in one walk over the chunks.  A block
+//    owns PR rows p of one head's P x N state; each warp keeps a 16 x N piece
+//    of it in mma accumulators (fp32) for the whole sequence.  Per chunk c:
+//
+//      H_c = exp(s_end) H_{c-1} + Σ_τ w_τ x_τ ⊗ B_τ,   w_τ = exp(s_end - s_τ) β_τ
+//
+//    with the entering state H_{c-1} stored first (bf16, for the chunk-output
+//    products: through a padded shared tile, then 16-byte coalesced stores).
+//    The product (w x)ᵀ B runs on the tensor cores.  The next chunk's x slice,
+//    B tile and step terms are in flight (cp.async, two stages) while a chunk
+//    is used.
 // ---------------------------------------------------------------------------
-constexpr int kPassThreads = 256, kPassPer = 8;  // 8 state elements per thread
-constexpr int kPassTile = 1024;                    // chunk decays staged per pass
+template <int N, int PR> struct SsdStateCfg {
+  static constexpr int kWarps = PR / 16;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int RX = PR + 8;  // x slice rows [τ][p]: 80-byte rows
+  static constexpr int RB = N + 8;   // B rows [τ][n] and entering-state rows [p][n]
+  static constexpr int oB = kSsdQ * RX, oT = oB + kSsdQ * RB;  // bf16 offsets in a stage
+  static constexpr int kStage = oT + 2 * kTermsRec;             // bf16 elements per stage
+  static constexpr int oH = 2 * kStage;                         // entering-state tile [PR][RB]
+  static constexpr size_t kBytes = (size_t)(oH + PR * RB) * 2;
+  static constexpr int kTermVecs = kTermsRec * 4 / 16;
+  static constexpr int kOutVecs = PR * N / 8;                   // 16-byte vectors of the tile
+  static_assert(PR % 16 == 0 && kSsdP % PR == 0, "tiling");
+  static_assert(kTermVecs <= kThreads, "one 16-byte copy of the terms per thread");
+  static_assert(kOutVecs % kThreads == 0, "whole vectors per thread in the state copy-out");
+};
+constexpr int kWalkRows = 32;  // state rows per block: 2 warps, 2 x 24 x 8 blocks on a 24-head layer
 
-template <int N>
-__global__ void __launch_bounds__(kPassThreads) ssd_state_pass_kernel(const SsdArgs p) {
-  constexpr int P = kSsdP;
-  __shared__ float sDecay[kPassTile];
-  const int h = blockIdx.x;
-  const int64_t b = blockIdx.y;
-  // this block's slice of the P x N state: blockIdx.z-th run of 256 x 8 elements
-  const int e0 = blockIdx.z * (kPassThreads * kPassPer) + threadIdx.x;
-  float hs[kPassPer], nx[kPassPer];
+template <int N, int PR>
+__global__ void __launch_bounds__(SsdStateCfg<N, PR>::kThreads)
+    ssd_state_scan_kernel(const SsdArgs p) {
+  using Cf = SsdStateCfg<N, PR>;
+  constexpr int Q = kSsdQ, P = kSsdP, RX = Cf::RX, RB = Cf::RB, NT = Cf::kThreads;
+  extern __shared__ float4 ssd_state_smem[];
+  __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(ssd_state_smem);
+  __nv_bfloat16* sH = tiles + Cf::oH;
+  const int p0 = blockIdx.x * PR, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int g = h / (p.H / p.G);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+
+  auto stage = [&](int c) {
+    __nv_bfloat16* st = tiles + (c & 1) * Cf::kStage;
+    const int64_t t0 = (int64_t)c * Q;
+    const int valid = (int)min64(Q, p.L - t0);
+    ssd_stage<Q, PR, RX, NT>(st, static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P + p0,
+                             p.H * P, valid);
+    ssd_stage<Q, N, RB, NT>(st + Cf::oB,
+                            static_cast<const __nv_bfloat16*>(p.B) + ((b * p.L + t0) * p.G + g) * N,
+                            p.G * N, valid);
+    if (threadIdx.x < Cf::kTermVecs) {
+      const float* src = p.ws_terms + ((b * p.nch + c) * p.H + h) * kTermsRec;
+      cp_async16(reinterpret_cast<float*>(st + Cf::oT) + 4 * threadIdx.x, src + 4 * threadIdx.x, true);
+    }
+    cp_async_commit();
+  };
+
+  // this thread's accumulator elements: rows rl, rl + 8 of the block's slice
+  // (head rows p0 + rl, + 8); columns 8j + cc, +1
+  const int rl = 16 * w + (lane >> 2), cc = 2 * (lane & 3);
+  const int64_t head = (b * p.H + h) * (int64_t)(P * N) + (int64_t)(p0 + rl) * N + cc;
+  float acc[N / 8][4];
 #pragma unroll
-  for (int k = 0; k < kPassPer; ++k) {
-    const int e = e0 + k * kPassThreads;
-    hs[k] = p.init_state ? p.init_state[(b * p.H + h) * (int64_t)(P * N) + e] : 0.f;
+  for (int j = 0; j < N / 8; ++j) {
+    if (p.init_state) {
+      const float2 u = *reinterpret_cast<const float2*>(p.init_state + head + 8 * j);
+      const float2 v = *reinterpret_cast<const float2*>(p.init_state + head + 8 * N + 8 * j);
+      acc[j][0] = u.x; acc[j][1] = u.y; acc[j][2] = v.x; acc[j][3] = v.y;
+    } else {
+      acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    }
   }
-  auto state_at = [&](int c) { return p.ws_state + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N); };
-  if (p.nch > 0) {
+  __nv_bfloat16* myH = sH + rl * RB + cc;
+
+  stage(0);
+  for (int c = 0; c < p.nch; ++c) {
+    const bool more = c + 1 < p.nch;
+    if (more) stage(c + 1);
+    // the state entering chunk c, into the shared tile
 #pragma unroll
-    for (int k = 0; k < kPassPer; ++k) nx[k] = state_at(0)[e0 + k * kPassThreads];
-  }
-  for (int c0 = 0; c0 < p.nch; c0 += kPassTile) {
-    const int cn = (int)min64(kPassTile, p.nch - c0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < cn; i += kPassThreads)
-      sDecay[i] = __expf(p.ws_logdecay[(b * p.nch + c0 + i) * p.H + h]);
-    __syncthreads();
-    for (int ci = 0; ci < cn; ++ci) {
-      const int c = c0 + ci;
-      float cur[kPassPer];
+    for (int j = 0; j < N / 8; ++j) {
+      *reinterpret_cast<uint32_t*>(myH + 8 * j) = pack_bf16(acc[j][0], acc[j][1]);
+      *reinterpret_cast<uint32_t*>(myH + 8 * RB + 8 * j) = pack_bf16(acc[j][2], acc[j][3]);
+    }
+    if (more) cp_async_wait<1>(); else cp_async_wait<0>();
+    __syncthreads();  // chunk c's tiles and terms, and the entering-state tile, are visible
+    {  // entering state -> workspace [b][c][h][p][n], 16-byte vectors
+      constexpr int VPR = N / 8;
+      __nv_bfloat16* dst = p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N) + (int64_t)p0 * N;
 #pragma unroll
-      for (int k = 0; k < kPassPer; ++k) cur[k] = nx[k];
-      if (c + 1 < p.nch) {  // the next chunk's states in flight during this one
-#pragma unroll
-        for (int k = 0; k < kPassPer; ++k) nx[k] = state_at(c + 1)[e0 + k * kPassThreads];
-      }
-      const float decay = sDecay[ci];
-      __nv_bfloat16* hin = p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N);
-#pragma unroll
-      for (int k = 0; k < kPassPer; ++k) {
-        hin[e0 + k * kPassThreads] = __float2bfloat16_rn(hs[k]);
-        hs[k] = fmaf(decay, hs[k], cur[k]);
+      for (int k = 0; k < Cf::kOutVecs / NT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        const int r = v / VPR, c8 = v % VPR;
+        *reinterpret_cast<uint4*>(dst + r * N + 8 * c8) =
+            *reinterpret_cast<const uint4*>(sH + r * RB + 8 * c8);
       }
     }
+
+    const __nv_bfloat16* sx = tiles + (c & 1) * Cf::kStage;
+    const __nv_bfloat16* sb = sx + Cf::oB;
+    const float* sT = reinterpret_cast<const float*>(sx + Cf::oT);  // [s | β | w]
+    const float* wv = sT + 2 * Q;
+    const float decay = __expf(sT[Q - 1]);
+#pragma unroll
+    for (int j = 0; j < N / 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][e] *= decay;
+#pragma unroll
+    for (int ks = 0; ks < Q / 16; ++ks) {
+      // A = (w x)ᵀ: rows p, k = τ; x stored [τ][p] -> transposed loads, then each
+      // element scaled by its step's w (fp32 product, rounded to bf16)
+      uint32_t af[4];
+      {
+        const int i = lane >> 3;
+        ldsm_x4_t(af, sx + (16 * ks + (i >> 1) * 8 + (lane & 7)) * RX + 16 * w + (i & 1) * 8);
+        const int tau = 16 * ks + cc;
+        const float w0 = wv[tau], w1 = wv[tau + 1], w8 = wv[tau + 8], w9 = wv[tau + 9];
+        auto scale = [](uint32_t v, float lo_w, float hi_w) {
+          return pack_bf16(__uint_as_float(v << 16) * lo_w, __uint_as_float(v & 0xffff0000u) * hi_w);
+        };
+        af[0] = scale(af[0], w0, w1);
+        af[1] = scale(af[1], w0, w1);
+        af[2] = scale(af[2], w8, w9);
+        af[3] = scale(af[3], w8, w9);
+      }
+#pragma unroll
+      for (int nn = 0; nn < N / 16; ++nn) {
+        // B operand: k = τ, n; stored [τ][n] -> transposed loads, two n8 tiles
+        uint32_t bf[4];
+        ldsm_x4_t(bf, sb + (16 * ks + (lane & 15)) * RB + 16 * nn + (lane >> 4) * 8);
+        mma_bf16(acc[2 * nn], af, bf[0], bf[1]);
+        mma_bf16(acc[2 * nn + 1], af, bf[2], bf[3]);
+      }
+    }
+    __syncthreads();  // the next iteration's copies and entering state reuse the tiles
   }
   if (p.final_state) {
 #pragma unroll
-    for (int k = 0; k < kPassPer; ++k)
-      p.final_state[(b * p.H + h) * (int64_t)(P * N) + e0 + k * kPassThreads] = hs[k];
+    for (int j = 0; j < N / 8; ++j) {
+      *reinterpret_cast<float2*>(p.final_state + head + 8 * j) = make_float2(acc[j][0], acc[j][1]);
+      *reinterpret_cast<float2*>(p.final_state + head + 8 * N + 8 * j) = make_float2(acc[j][2], acc[j][3]);
+    }
   }
 }
 
@@ -274,13 +311,16 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   ssd_stage<Q, N, RB>(sB, static_cast<const __nv_bfloat16*>(p.B) + bc, p.G * N, valid);
   ssd_stage<Q, N, RB>(sC, static_cast<const __nv_bfloat16*>(p.C) + bc, p.G * N, valid);
   ssd_stage<P, N, RB>(sH, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P);
+  if (threadIdx.x < 2 * kSsdQ / 4) {  // s and β of the chunk's step terms
+    const float* src = p.ws_terms + ((b * p.nch + c) * p.H + h) * kTermsRec + 4 * threadIdx.x;
+    cp_async16(sS + 4 * threadIdx.x, src, true);
+  }
   cp_async_commit();
   ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
   if (p.z)
     ssd_stage<Q, P, RX>(sZ, static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P,
                         p.H * P, valid);
   cp_async_commit();
-  ssd_chunk_terms(p, b, t0, h, sS, sBeta);  // while the copies are in flight
   cp_async_wait<1>();
   __syncthreads();
 
@@ -392,24 +432,39 @@ SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t N) {
   SsdLayout w{};
   w.nch = (L + kSsdQ - 1) / kSsdQ;
   const size_t units = (size_t)batch * (size_t)w.nch * (size_t)H;
-  const size_t st = units * (size_t)kSsdP * (size_t)N;
-  w.o_state = 0;
-  w.o_hin = (st * 4 + 255) / 256 * 256;
-  w.o_logdecay = w.o_hin + (st * 2 + 255) / 256 * 256;
-  w.bytes = w.o_logdecay + (units * 4 + 255) / 256 * 256;
+  w.o_hin = 0;
+  w.o_terms = (units * (size_t)kSsdP * (size_t)N * 2 + 255) / 256 * 256;
+  w.bytes = w.o_terms + (units * (size_t)kTermsRec * 4 + 255) / 256 * 256;
   return w;
 }
 
 template <int N>
+static cudaError_t ssd_walk(const SsdArgs& a, cudaStream_t s) {
+  using SC = SsdStateCfg<N, kWalkRows>;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    const cudaError_t e = cudaFuncSetAttribute(ssd_state_scan_kernel<N, kWalkRows>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC::kBytes);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  ssd_state_scan_kernel<N, kWalkRows><<<dim3(kSsdP / kWalkRows, (unsigned)a.H, (unsigned)a.batch),
+                                        SC::kThreads, SC::kBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int N>
 static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
-  const dim3 chunks((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch);
-  ssd_chunk_state_kernel<N><<<chunks, kSsdThreads, 0, s>>>(a);
+  const int64_t units = a.batch * a.nch * a.H;
+  constexpr int kUnitsPerBlock = kTermsThreads / 32;
+  ssd_terms_kernel<<<(unsigned)((units + kUnitsPerBlock - 1) / kUnitsPerBlock), kTermsThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  constexpr int kSlices = kSsdP * N / (kPassThreads * kPassPer);
-  ssd_state_pass_kernel<N><<<dim3((unsigned)a.H, (unsigned)a.batch, kSlices), kPassThreads, 0, s>>>(a);
-  e = cudaGetLastError();
+  e = ssd_walk<N>(a, s);
   if (e != cudaSuccess) return e;
+  const dim3 chunks((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch);
   constexpr size_t bytes =
       (size_t)(2 * kSsdQ * (kSsdP + 8) + 2 * kSsdQ * (N + 8) + kSsdP * (N + 8)) * 2 + 2 * kSsdQ * 4;
   static int configured_dev = -1;
