@@ -399,7 +399,7 @@ def bench_ssd(steps, warmup, world, seed=5):
     bias = torch.from_numpy(synth.gen_delta_bias(seed, H)).cuda()
     y = torch.empty_like(x)
     h = torch.empty((b, H, P, N), dtype=torch.float32, device="cuda")
-    nbytes = ssm.ssm_ssd_workspace_bytes(b, L, H, P, N)
+    nbytes = ssm.ssm_ssd_workspace_bytes(b, L, H, P, G, N)
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -741,7 +741,7 @@ def main():
                        "tokens_per_s": sh["batch"] * sh["L"] / ss * world,
                        "tensor_tflops": fl / ss / 1e12, "flops_per_step": fl,
                        "hbm_gbs_algorithmic": nb / ss / 1e9, "bytes_per_step": nb,
-                       "workspace_bytes": ssd["workspace_bytes"], "gpu_launches": 3 * ssd["steps"],
+                       "workspace_bytes": ssd["workspace_bytes"], "gpu_launches": 4 * ssd["steps"],
                        "l2": "x, z, y: 3 x 50 MB plus the 100 MB of bf16 chunk-entering states written and read per step, larger than L2"}
     if cpu is not None:
         line["cpu_baseline"] = cpu

@@ -335,13 +335,14 @@ int ssm_scan_fwd_train(const void* u, const void* delta, const float* delta_bias
  * headdim, dstate) fp32 (nullable).  Supported: headdim 64, dstate 64 or 128,
  * nheads a multiple of ngroups (SSM_ERR_UNSUPPORTED otherwise).  Workspace:
  * ssm_ssd_workspace_bytes() bytes (the states entering each chunk, the
- * chunks' step terms), required when batch, seqlen and nheads are non-zero.
+ * chunks' step terms, each chunk's C Bᵀ per group), required when batch,
+ * seqlen and nheads are non-zero; the query returns 0 for an unsupported shape.
  * Products in bf16 with fp32 accumulation; the running state is kept in fp32
  * and enters the chunk outputs as bf16.  Errors as the other entry points;
- * asynchronous on `stream` (three kernels).
+ * asynchronous on `stream` (four kernels).
  */
 size_t ssm_ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
-                               int64_t dstate);
+                               int64_t ngroups, int64_t dstate);
 
 int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float* A,
                 const void* B, const void* C, const float* D, const void* z, int flags, void* y,

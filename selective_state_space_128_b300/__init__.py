@@ -69,7 +69,7 @@ def load():
     lib.ssm_scan_fwd_train.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp, sz,
                                                    vp, sz, vp]
     lib.ssm_scan_fwd_train.restype = i32
-    lib.ssm_ssd_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
+    lib.ssm_ssd_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
     lib.ssm_ssd_workspace_bytes.restype = sz
     lib.ssm_ssd_fwd.argtypes = [vp] * 8 + [i32, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, sz, vp]
     lib.ssm_ssd_fwd.restype = i32
@@ -290,8 +290,8 @@ def ssm_conv1d_update(conv_state, x, weight, bias, silu, out, stream=None):
     _call("ssm_conv1d_update", rc)
 
 
-def ssm_ssd_workspace_bytes(batch, seqlen, nheads, headdim, dstate) -> int:
-    return int(load().ssm_ssd_workspace_bytes(batch, seqlen, nheads, headdim, dstate))
+def ssm_ssd_workspace_bytes(batch, seqlen, nheads, headdim, ngroups, dstate) -> int:
+    return int(load().ssm_ssd_workspace_bytes(batch, seqlen, nheads, headdim, ngroups, dstate))
 
 
 def ssm_ssd_fwd(x, dt, dt_bias, A, B, C, D, z, flags, y, final_state, init_state, workspace,
@@ -410,10 +410,10 @@ def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, init_
     the final state (batch, H, P, N) float32 and the workspace."""
     import torch
     batch, L, H, P = x.shape
-    N = B.shape[3]
+    G, N = B.shape[2], B.shape[3]
     y = torch.empty_like(x)
     h = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device)
-    nbytes = ssm_ssd_workspace_bytes(batch, L, H, P, N)
+    nbytes = ssm_ssd_workspace_bytes(batch, L, H, P, G, N)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
     ssm_ssd_fwd(x, dt, dt_bias, A, B, C, D, z, _flags(delta_softplus, euler), y, h, init_state,
                 ws, nbytes, stream)

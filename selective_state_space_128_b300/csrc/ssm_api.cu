@@ -72,11 +72,12 @@ size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int6
 }
 
 size_t ssm_ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
-                               int64_t dstate) {
+                               int64_t ngroups, int64_t dstate) {
   if (batch <= 0 || seqlen <= 0 || nheads <= 0 || headdim != 64 || (dstate != 64 && dstate != 128))
     return 0;
+  if (ngroups <= 0 || nheads % ngroups != 0) return 0;
   if (!sizes_ok(batch, nheads * headdim, seqlen)) return 0;
-  return ssm::ssd_layout(batch, seqlen, nheads, dstate).bytes;
+  return ssm::ssd_layout(batch, seqlen, nheads, ngroups, dstate).bytes;
 }
 
 int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float* A,
@@ -107,7 +108,7 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
   for (const Span& in : ins)
     if (overlaps(y, nx, in.p, in.n) || overlaps(final_state, nst, in.p, in.n)) return SSM_ERR_ARG;
   if (overlaps(y, nx, final_state, nst)) return SSM_ERR_ARG;
-  const ssm::SsdLayout lay = ssm::ssd_layout(batch, seqlen, nheads, dstate);
+  const ssm::SsdLayout lay = ssm::ssd_layout(batch, seqlen, nheads, ngroups, dstate);
   if (work) {
     if (!workspace || workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
     for (const Span& in : ins)
@@ -132,6 +133,7 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
   a.final_state = final_state; a.init_state = init_state;
   a.ws_hin = reinterpret_cast<__nv_bfloat16*>(ws + lay.o_hin);
   a.ws_terms = reinterpret_cast<float*>(ws + lay.o_terms);
+  a.ws_cb = reinterpret_cast<float*>(ws + lay.o_cb);
   a.batch = batch; a.L = seqlen; a.H = nheads; a.G = ngroups; a.nch = lay.nch;
   a.softplus = (flags & SSM_SOFTPLUS) != 0;
   a.euler = (flags & SSM_EULER_B) != 0;

@@ -159,8 +159,9 @@ cudaError_t conv_launch(const ConvArgs& a, int64_t width, int io_dtype, bool upd
 // Arguments of the chunked scalar-A SSM (Mamba-2 SSD).  x, z, y (batch, L, H,
 // P) bf16; dt (batch, L, H) bf16; B, C (batch, L, G, N) bf16; A, D, dt_bias (H)
 // fp32; states (batch, H, P, N) fp32.  Workspace parts: the states entering
-// each chunk [batch][nch][H][P][N] bf16 and the chunks' step terms
-// [batch][nch][H][s | β | w] (3 x 64 fp32).
+// each chunk [batch][nch][H][P][N] bf16, the chunks' step terms
+// [batch][nch][H][s | β | w] (3 x 64 fp32) and the chunks' C Bᵀ per group
+// [batch][nch][G][64][64] fp32.
 struct SsdArgs {
   const void* x;
   const void* dt;
@@ -175,6 +176,7 @@ struct SsdArgs {
   const float* init_state;
   __nv_bfloat16* ws_hin;
   float* ws_terms;
+  float* ws_cb;
   int64_t batch, L, H, G, nch;
   int softplus;
   int euler;
@@ -182,10 +184,10 @@ struct SsdArgs {
 
 struct SsdLayout {
   int64_t nch;
-  size_t o_hin, o_terms, bytes;
+  size_t o_hin, o_terms, o_cb, bytes;
 };
 
-SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t N);
+SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t N);
 cudaError_t ssd_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
 
 }  // namespace ssm

@@ -286,55 +286,29 @@ __global__ void __launch_bounds__(SsdStateCfg<N, PR>::kThreads)
 }
 
 // ---------------------------------------------------------------------------
-// 3. chunk outputs: y = (mask ∘ C Bᵀ) X + exp(s_t) C Hᵀ + D x, gated
+// 2. the chunks' C Bᵀ, once per (batch, chunk, group): every head of a group
+//    shares it.  G[t][τ] = C_t · B_τ for τ <= t (16 x 16 tiles on and below the
+//    diagonal; the others are never read), fp32, [t][τ] rows of 64.
 // ---------------------------------------------------------------------------
 template <int N>
-__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdArgs p) {
-  constexpr int Q = kSsdQ, P = kSsdP, RX = P + 8, RB = N + 8;
-  extern __shared__ float4 ssd_smem[];
-  __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(ssd_smem);  // [τ][p]
-  __nv_bfloat16* sB = sX + Q * RX;                                 // [τ][n]
-  __nv_bfloat16* sC = sB + Q * RB;                                 // [t][n]
-  __nv_bfloat16* sH = sC + Q * RB;                                 // [p][n], entering state
-  __nv_bfloat16* sZ = sH + P * RB;                                 // [t][p], the gate
-  float* sS = reinterpret_cast<float*>(sZ + Q * RX);
-  float* sBeta = sS + Q;
-  const int c = blockIdx.x, h = blockIdx.y;
+__global__ void __launch_bounds__(kSsdThreads) ssd_cb_kernel(const SsdArgs p) {
+  constexpr int Q = kSsdQ, RB = N + 8;
+  __shared__ __align__(16) __nv_bfloat16 sB[Q * RB];  // [τ][n]
+  __shared__ __align__(16) __nv_bfloat16 sC[Q * RB];  // [t][n]
+  const int c = blockIdx.x, g = blockIdx.y;
   const int64_t b = blockIdx.z;
   const int64_t t0 = (int64_t)c * Q;
   const int valid = (int)min64(Q, p.L - t0);
-  const int g = h / (p.H / p.G);
-  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
-  // two copy groups: B, C and the entering state first (the products C Bᵀ and
-  // C Hᵀ need only them), then x and z, which arrive while those run
   const int64_t bc = ((b * p.L + t0) * p.G + g) * N;
   ssd_stage<Q, N, RB>(sB, static_cast<const __nv_bfloat16*>(p.B) + bc, p.G * N, valid);
   ssd_stage<Q, N, RB>(sC, static_cast<const __nv_bfloat16*>(p.C) + bc, p.G * N, valid);
-  ssd_stage<P, N, RB>(sH, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P);
-  if (threadIdx.x < 2 * kSsdQ / 4) {  // s and β of the chunk's step terms
-    const float* src = p.ws_terms + ((b * p.nch + c) * p.H + h) * kTermsRec + 4 * threadIdx.x;
-    cp_async16(sS + 4 * threadIdx.x, src, true);
-  }
-  cp_async_commit();
-  ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
-  if (p.z)
-    ssd_stage<Q, P, RX>(sZ, static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P,
-                        p.H * P, valid);
-  cp_async_commit();
-  cp_async_wait<1>();
+  cp_async_wait_all();
   __syncthreads();
-
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows t in [16w, 16w+16)
   const int i8 = lane >> 3;
-  // (a) C Bᵀ for this warp's rows and the columns τ <= its last row, and (d)
-  //     O = C Hᵀ: both take the same A fragments of C, so one pass over k = n
-  //     feeds up to 16 independent accumulators
-  float cb[8][4], ov[8][4];
+  float cb[8][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
-    ov[j][0] = ov[j][1] = ov[j][2] = ov[j][3] = 0.f;
-  }
+  for (int j = 0; j < 8; ++j) cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < N / 16; ++ks) {
     uint32_t a[4];
@@ -348,6 +322,81 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
       mma_bf16(cb[2 * jj], a, bf[0], bf[1]);
       mma_bf16(cb[2 * jj + 1], a, bf[2], bf[3]);
     }
+  }
+  float* out = p.ws_cb + ((b * p.nch + c) * p.G + g) * (int64_t)(Q * Q);
+  const int r0 = 16 * w + (lane >> 2), cc = 2 * (lane & 3);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j / 2 > w) break;
+    *reinterpret_cast<float2*>(out + r0 * Q + 8 * j + cc) = make_float2(cb[j][0], cb[j][1]);
+    *reinterpret_cast<float2*>(out + (r0 + 8) * Q + 8 * j + cc) = make_float2(cb[j][2], cb[j][3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. chunk outputs: y = (mask ∘ C Bᵀ) X + exp(s_t) C Hᵀ + D x, gated
+// ---------------------------------------------------------------------------
+template <int N> struct SsdScanSmem {
+  static constexpr int Q = kSsdQ, P = kSsdP, RX = P + 8, RB = N + 8;
+  static constexpr int RG = Q + 8;  // fp32 C Bᵀ rows: 288 bytes
+  // bf16 tiles: x [τ][p], C [t][n], entering state [p][n], z [t][p]; then fp32
+  // C Bᵀ [t][τ] and the step terms s, β
+  static constexpr int oC = Q * RX, oH = oC + Q * RB, oZ = oH + P * RB, kTiles = oZ + Q * RX;
+  static constexpr size_t kBytes = (size_t)kTiles * 2 + (size_t)(Q * RG + 2 * Q) * 4;
+};
+
+template <int N>
+__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdArgs p) {
+  using S = SsdScanSmem<N>;
+  constexpr int Q = kSsdQ, P = kSsdP, RX = S::RX, RB = S::RB, RG = S::RG;
+  extern __shared__ float4 ssd_smem[];
+  __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(ssd_smem);
+  __nv_bfloat16* sC = sX + S::oC;
+  __nv_bfloat16* sH = sX + S::oH;
+  __nv_bfloat16* sZ = sX + S::oZ;
+  float* sG = reinterpret_cast<float*>(sX + S::kTiles);
+  float* sS = sG + Q * RG;
+  float* sBeta = sS + Q;
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int64_t t0 = (int64_t)c * Q;
+  const int valid = (int)min64(Q, p.L - t0);
+  const int g = h / (p.H / p.G);
+  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
+  // two copy groups: C and the entering state first (the product C Hᵀ needs
+  // only them), then x, z, the group's C Bᵀ and the step terms, which arrive
+  // while it runs
+  ssd_stage<Q, N, RB>(sC, static_cast<const __nv_bfloat16*>(p.C) + ((b * p.L + t0) * p.G + g) * N, p.G * N,
+                      valid);
+  ssd_stage<P, N, RB>(sH, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P);
+  cp_async_commit();
+  ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
+  if (p.z)
+    ssd_stage<Q, P, RX>(sZ, static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P,
+                        p.H * P, valid);
+  // C Bᵀ rows of 64 fp32, copied as rows of 128 bf16-sized halves (plain bytes)
+  ssd_stage<Q, 2 * Q, 2 * RG>(reinterpret_cast<__nv_bfloat16*>(sG),
+                              reinterpret_cast<const __nv_bfloat16*>(
+                                  p.ws_cb + ((b * p.nch + c) * p.G + g) * (int64_t)(Q * Q)),
+                              2 * Q, Q);
+  if (threadIdx.x < 2 * kSsdQ / 4) {  // s and β of the chunk's step terms
+    const float* src = p.ws_terms + ((b * p.nch + c) * p.H + h) * kTermsRec + 4 * threadIdx.x;
+    cp_async16(sS + 4 * threadIdx.x, src, true);
+  }
+  cp_async_commit();
+  cp_async_wait<1>();
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows t in [16w, 16w+16)
+  const int i8 = lane >> 3;
+  // (a) O = C Hᵀ for this warp's rows
+  float ov[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ov[j][0] = ov[j][1] = ov[j][2] = ov[j][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < N / 16; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(a, sC + (16 * w + (lane & 15)) * RB + 16 * ks + (lane >> 4) * 8);
 #pragma unroll
     for (int pp = 0; pp < P / 16; ++pp) {
       // B operand = Hᵀ: k = n, columns p; stored [p][n] -> plain loads
@@ -357,10 +406,10 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
       mma_bf16(ov[2 * pp + 1], a, bf[2], bf[3]);
     }
   }
-  cp_async_wait<0>();  // x and z
+  cp_async_wait<0>();  // x, z, C Bᵀ, terms
   __syncthreads();
   // (b) the decay mask and input weight: M[t][τ] = (τ <= t) C_t·B_τ exp(s_t - s_τ) β_τ,
-  //     repacked as bf16 A fragments of the next product (two n8 tiles = one k16 step)
+  //     packed as bf16 A fragments of the next product (two n8 tiles = one k16 step)
   const int tr = 16 * w + (lane >> 2);  // this thread's rows tr, tr + 8
   const float s_r0 = sS[tr], s_r1 = sS[tr + 8];
   uint32_t am[4][4];
@@ -368,14 +417,18 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      const int j = 2 * kk + half;
-      const int tau = 8 * j + 2 * (lane & 3);
-      float m[4];
+      const int tau = 16 * kk + 8 * half + 2 * (lane & 3);
+      float m[4] = {0.f, 0.f, 0.f, 0.f};
+      if (kk <= w) {
+        const float2 g0 = *reinterpret_cast<const float2*>(sG + tr * RG + tau);
+        const float2 g1 = *reinterpret_cast<const float2*>(sG + (tr + 8) * RG + tau);
+        const float cbv[4] = {g0.x, g0.y, g1.x, g1.y};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = e < 2 ? tr : tr + 8, col = tau + (e & 1);
-        const float sr = e < 2 ? s_r0 : s_r1;
-        m[e] = (kk <= w && col <= row) ? cb[j][e] * __expf(sr - sS[col]) * sBeta[col] : 0.f;
+        for (int e = 0; e < 4; ++e) {
+          const int row = e < 2 ? tr : tr + 8, col = tau + (e & 1);
+          const float sr = e < 2 ? s_r0 : s_r1;
+          m[e] = col <= row ? cbv[e] * __expf(sr - sS[col]) * sBeta[col] : 0.f;
+        }
       }
       am[kk][2 * half] = pack_bf16(m[0], m[1]);
       am[kk][2 * half + 1] = pack_bf16(m[2], m[3]);
@@ -428,13 +481,15 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t N) {
+SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t N) {
   SsdLayout w{};
   w.nch = (L + kSsdQ - 1) / kSsdQ;
   const size_t units = (size_t)batch * (size_t)w.nch * (size_t)H;
+  const size_t gunits = (size_t)batch * (size_t)w.nch * (size_t)G;
   w.o_hin = 0;
   w.o_terms = (units * (size_t)kSsdP * (size_t)N * 2 + 255) / 256 * 256;
-  w.bytes = w.o_terms + (units * (size_t)kTermsRec * 4 + 255) / 256 * 256;
+  w.o_cb = w.o_terms + (units * (size_t)kTermsRec * 4 + 255) / 256 * 256;
+  w.bytes = w.o_cb + (gunits * (size_t)kSsdQ * kSsdQ * 4 + 255) / 256 * 256;
   return w;
 }
 
@@ -464,9 +519,10 @@ static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = ssd_walk<N>(a, s);
   if (e != cudaSuccess) return e;
-  const dim3 chunks((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch);
-  constexpr size_t bytes =
-      (size_t)(2 * kSsdQ * (kSsdP + 8) + 2 * kSsdQ * (N + 8) + kSsdP * (N + 8)) * 2 + 2 * kSsdQ * 4;
+  ssd_cb_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.G, (unsigned)a.batch), kSsdThreads, 0, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  constexpr size_t bytes = SsdScanSmem<N>::kBytes;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -476,7 +532,7 @@ static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  ssd_chunk_scan_kernel<N><<<chunks, kSsdThreads, bytes, s>>>(a);
+  ssd_chunk_scan_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch), kSsdThreads, bytes, s>>>(a);
   return cudaGetLastError();
 }
 

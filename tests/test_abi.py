@@ -234,6 +234,9 @@ def test_ssd_argument_errors():
     assert L_.ssm_ssd_fwd(*args[:8], 5, *args[9:], 1, 64, 4, 64, 1, 64, *ws) == ssm.SSM_ERR_ARG
     assert L_.ssm_ssd_fwd(*args[:9], FAKE + 0x100, *args[10:], 1, 64, 4, 64, 1, 64, *ws) == ssm.SSM_ERR_ARG
     # the states entering each of the 8 x 32 x 24 (batch, chunk, head) units as
-    # bf16 (64 x 128 each), and each unit's step terms (3 x 64 fp32)
+    # bf16 (64 x 128 each), each unit's step terms (3 x 64 fp32) and each
+    # (batch, chunk, group)'s C Bᵀ (64 x 64 fp32)
     units = 8 * 32 * 24
-    assert ssm.ssm_ssd_workspace_bytes(8, 2048, 24, 64, 128) == units * 64 * 128 * 2 + units * 3 * 64 * 4
+    assert ssm.ssm_ssd_workspace_bytes(8, 2048, 24, 64, 1, 128) == (
+        units * 64 * 128 * 2 + units * 3 * 64 * 4 + 8 * 32 * 1 * 64 * 64 * 4)
+    assert ssm.ssm_ssd_workspace_bytes(8, 2048, 24, 64, 5, 128) == 0  # 24 heads in 5 groups
