@@ -451,30 +451,41 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
       mma_bf16(yv[2 * pp + 1], a, bf[2], bf[3]);
     }
   }
-  // (e) y = Y + exp(s_t) O + D x, gated, rows inside the sequence only
+  // (e) y = Y + exp(s_t) O + D x, gated, into a shared tile [t][p] (the C tile's
+  //     space: C is no longer read), then 16-byte coalesced stores of the rows
+  //     inside the sequence
   const float Dh = p.D ? p.D[h] : 0.f;
   const float e0 = __expf(s_r0), e1 = __expf(s_r1);
-  __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y) + ((b * p.L + t0) * p.H + h) * P;
   const bool gate = p.z != nullptr;
+  __nv_bfloat16* sY = sC;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int col = 8 * j + 2 * (lane & 3);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int row = half ? tr + 8 : tr;
-      if (row >= valid) continue;
       const float ee = half ? e1 : e0;
       const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162*>(sX + row * RX + col);
       float v0 = fmaf(ee, ov[j][2 * half], yv[j][2 * half]) + Dh * __low2float(xv);
       float v1 = fmaf(ee, ov[j][2 * half + 1], yv[j][2 * half + 1]) + Dh * __high2float(xv);
-      const int64_t off = (int64_t)row * p.H * P + col;
       if (gate) {
         const __nv_bfloat162 zv = *reinterpret_cast<const __nv_bfloat162*>(sZ + row * RX + col);
         v0 *= silu_precise(__low2float(zv));
         v1 *= silu_precise(__high2float(zv));
       }
-      *reinterpret_cast<__nv_bfloat162*>(yg + off) = __floats2bfloat162_rn(v0, v1);
+      *reinterpret_cast<__nv_bfloat162*>(sY + row * RX + col) = __floats2bfloat162_rn(v0, v1);
     }
+  }
+  __syncthreads();
+  __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y) + ((b * p.L + t0) * p.H + h) * P;
+  constexpr int VPR = P / 8;
+#pragma unroll
+  for (int k = 0; k < Q * VPR / kSsdThreads; ++k) {
+    const int v = threadIdx.x + k * kSsdThreads;
+    const int row = v / VPR, c8 = v % VPR;
+    if (row < valid)
+      *reinterpret_cast<uint4*>(yg + (int64_t)row * p.H * P + 8 * c8) =
+          *reinterpret_cast<const uint4*>(sY + row * RX + 8 * c8);
   }
 }
 
