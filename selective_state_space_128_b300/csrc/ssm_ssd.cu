@@ -31,6 +31,8 @@ namespace ssm {
 constexpr int kSsdQ = 64;        // chunk length
 constexpr int kSsdP = 64;        // head dimension
 constexpr int kSsdThreads = 128;  // 4 warps: 16 rows each
+constexpr int kScanColSplit = 2;  // chunk outputs: two warps per 16-row tile, 32 columns each
+constexpr int kScanThreadsSsd = kSsdThreads * kScanColSplit;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -346,9 +348,10 @@ template <int N> struct SsdScanSmem {
 };
 
 template <int N>
-__global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdArgs p) {
+__global__ void __launch_bounds__(kScanThreadsSsd) ssd_chunk_scan_kernel(const SsdArgs p) {
   using S = SsdScanSmem<N>;
-  constexpr int Q = kSsdQ, P = kSsdP, RX = S::RX, RB = S::RB, RG = S::RG;
+  constexpr int Q = kSsdQ, P = kSsdP, RX = S::RX, RB = S::RB, RG = S::RG, NT = kScanThreadsSsd;
+  constexpr int PC = P / kScanColSplit;  // output columns per warp
   extern __shared__ float4 ssd_smem[];
   __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(ssd_smem);
   __nv_bfloat16* sC = sX + S::oC;
@@ -366,16 +369,16 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   // two copy groups: C and the entering state first (the product C Hᵀ needs
   // only them), then x, z, the group's C Bᵀ and the step terms, which arrive
   // while it runs
-  ssd_stage<Q, N, RB>(sC, static_cast<const __nv_bfloat16*>(p.C) + ((b * p.L + t0) * p.G + g) * N, p.G * N,
+  ssd_stage<Q, N, RB, NT>(sC, static_cast<const __nv_bfloat16*>(p.C) + ((b * p.L + t0) * p.G + g) * N, p.G * N,
                       valid);
-  ssd_stage<P, N, RB>(sH, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P);
+  ssd_stage<P, N, RB, NT>(sH, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P);
   cp_async_commit();
-  ssd_stage<Q, P, RX>(sX, xg, p.H * P, valid);
+  ssd_stage<Q, P, RX, NT>(sX, xg, p.H * P, valid);
   if (p.z)
-    ssd_stage<Q, P, RX>(sZ, static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P,
+    ssd_stage<Q, P, RX, NT>(sZ, static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P,
                         p.H * P, valid);
   // C Bᵀ rows of 64 fp32, copied as rows of 128 bf16-sized halves (plain bytes)
-  ssd_stage<Q, 2 * Q, 2 * RG>(reinterpret_cast<__nv_bfloat16*>(sG),
+  ssd_stage<Q, 2 * Q, 2 * RG, NT>(reinterpret_cast<__nv_bfloat16*>(sG),
                               reinterpret_cast<const __nv_bfloat16*>(
                                   p.ws_cb + ((b * p.nch + c) * p.G + g) * (int64_t)(Q * Q)),
                               2 * Q, Q);
@@ -387,21 +390,22 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   cp_async_wait<1>();
   __syncthreads();
 
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows t in [16w, 16w+16)
+  // warp w: rows t in [16 wr, 16 wr + 16), output columns p in [PC wc, PC wc + PC)
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, wr = w & 3, wc = w >> 2;
   const int i8 = lane >> 3;
-  // (a) O = C Hᵀ for this warp's rows
-  float ov[8][4];
+  // (a) O = C Hᵀ for this warp's rows and columns
+  float ov[PC / 8][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) ov[j][0] = ov[j][1] = ov[j][2] = ov[j][3] = 0.f;
+  for (int j = 0; j < PC / 8; ++j) ov[j][0] = ov[j][1] = ov[j][2] = ov[j][3] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < N / 16; ++ks) {
     uint32_t a[4];
-    ldsm_x4(a, sC + (16 * w + (lane & 15)) * RB + 16 * ks + (lane >> 4) * 8);
+    ldsm_x4(a, sC + (16 * wr + (lane & 15)) * RB + 16 * ks + (lane >> 4) * 8);
 #pragma unroll
-    for (int pp = 0; pp < P / 16; ++pp) {
+    for (int pp = 0; pp < PC / 16; ++pp) {
       // B operand = Hᵀ: k = n, columns p; stored [p][n] -> plain loads
       uint32_t bf[4];
-      ldsm_x4(bf, sH + (16 * pp + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
+      ldsm_x4(bf, sH + (PC * wc + 16 * pp + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
       mma_bf16(ov[2 * pp], a, bf[0], bf[1]);
       mma_bf16(ov[2 * pp + 1], a, bf[2], bf[3]);
     }
@@ -410,7 +414,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   __syncthreads();
   // (b) the decay mask and input weight: M[t][τ] = (τ <= t) C_t·B_τ exp(s_t - s_τ) β_τ,
   //     packed as bf16 A fragments of the next product (two n8 tiles = one k16 step)
-  const int tr = 16 * w + (lane >> 2);  // this thread's rows tr, tr + 8
+  const int tr = 16 * wr + (lane >> 2);  // this thread's rows tr, tr + 8
   const float s_r0 = sS[tr], s_r1 = sS[tr + 8];
   uint32_t am[4][4];
 #pragma unroll
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
     for (int half = 0; half < 2; ++half) {
       const int tau = 16 * kk + 8 * half + 2 * (lane & 3);
       float m[4] = {0.f, 0.f, 0.f, 0.f};
-      if (kk <= w) {
+      if (kk <= wr) {
         const float2 g0 = *reinterpret_cast<const float2*>(sG + tr * RG + tau);
         const float2 g1 = *reinterpret_cast<const float2*>(sG + (tr + 8) * RG + tau);
         const float cbv[4] = {g0.x, g0.y, g1.x, g1.y};
@@ -435,18 +439,18 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
     }
   }
   // (c) Y = M X (k = τ up to the warp's rows)
-  float yv[8][4];
+  float yv[PC / 8][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) yv[j][0] = yv[j][1] = yv[j][2] = yv[j][3] = 0.f;
+  for (int j = 0; j < PC / 8; ++j) yv[j][0] = yv[j][1] = yv[j][2] = yv[j][3] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
-    if (kk > w) break;
+    if (kk > wr) break;
     const uint32_t a[4] = {am[kk][0], am[kk][1], am[kk][2], am[kk][3]};
 #pragma unroll
-    for (int pp = 0; pp < P / 16; ++pp) {
+    for (int pp = 0; pp < PC / 16; ++pp) {
       // B operand = X: k = τ, columns p; stored [τ][p] -> transposed loads
       uint32_t bf[4];
-      ldsm_x4_t(bf, sX + (16 * kk + (lane & 15)) * RX + 16 * pp + (lane >> 4) * 8);
+      ldsm_x4_t(bf, sX + (16 * kk + (lane & 15)) * RX + PC * wc + 16 * pp + (lane >> 4) * 8);
       mma_bf16(yv[2 * pp], a, bf[0], bf[1]);
       mma_bf16(yv[2 * pp + 1], a, bf[2], bf[3]);
     }
@@ -459,8 +463,8 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   const bool gate = p.z != nullptr;
   __nv_bfloat16* sY = sC;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int col = 8 * j + 2 * (lane & 3);
+  for (int j = 0; j < PC / 8; ++j) {
+    const int col = PC * wc + 8 * j + 2 * (lane & 3);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int row = half ? tr + 8 : tr;
@@ -480,8 +484,8 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_scan_kernel(const SsdAr
   __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y) + ((b * p.L + t0) * p.H + h) * P;
   constexpr int VPR = P / 8;
 #pragma unroll
-  for (int k = 0; k < Q * VPR / kSsdThreads; ++k) {
-    const int v = threadIdx.x + k * kSsdThreads;
+  for (int k = 0; k < Q * VPR / NT; ++k) {
+    const int v = threadIdx.x + k * NT;
     const int row = v / VPR, c8 = v % VPR;
     if (row < valid)
       *reinterpret_cast<uint4*>(yg + (int64_t)row * p.H * P + 8 * c8) =
@@ -543,7 +547,8 @@ static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  ssd_chunk_scan_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch), kSsdThreads, bytes, s>>>(a);
+  ssd_chunk_scan_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch), kScanThreadsSsd, bytes,
+                             s>>>(a);
   return cudaGetLastError();
 }
 
