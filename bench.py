@@ -69,10 +69,11 @@ def load_peaks():
         return 6400.0, 2032.0, "fallback"
 
 
-def csrc_hash() -> str:
+def csrc_hash(names=None) -> str:
+    """Hash of the library sources `names` (file names under csrc/; all when None)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "selective_state_space_128_b300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in sorted(names or os.listdir(d)):
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -80,13 +81,14 @@ def csrc_hash() -> str:
 
 def profiled_traffic(kernel: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None when
-    the summary is missing or was taken on different kernel sources."""
+    the summary is missing or was taken on different sources of that kernel (the
+    entry lists the files the kernel is compiled from)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
         ent = rec[kernel]
-        if ent.get("csrc_hash") != csrc_hash():
+        if ent.get("csrc_hash") != csrc_hash(ent.get("sources")):
             return None
         return float(ent["dram_bytes_per_launch"])
     except Exception:
