@@ -134,6 +134,37 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
                     void* stream);
 
 /*
+ * The scan on HOST buffers (selective-scan summary page, section 4b equations
+ * (2), (4) and Algorithm 2, as ssm_scan_fwd_ex): the copies to and from the
+ * device are part of the call.  u, delta, z, y, B, C, A, D, delta_bias,
+ * init_state and final_state are host pointers (page-locked memory lets the
+ * copies run asynchronously and overlap; pageable memory works but the
+ * copies then synchronise), with the layouts, dtypes, flags and nullability
+ * of ssm_scan_fwd_ex (SSM_SOFTPLUS, SSM_EULER_B, SSM_LAYOUT_BLD).  workspace is
+ * DEVICE memory of at least ssm_scan_fwd_host_workspace_bytes() bytes (three
+ * staging slots, the parameters and the unit scans' scratch), 16-byte aligned.
+ *
+ * The work is cut into units that are contiguous in host memory (a batch row,
+ * or a block of a row's channels when batch < 8; a whole row with
+ * SSM_LAYOUT_BLD); the copy-in of a unit, the scan of the previous one and
+ * the copy-out of the one before run at the same time on two internal copy
+ * streams and `stream`.  Results equal ssm_scan_fwd_ex's on the same inputs up
+ * to the scan's own plan for the smaller unit (a long unit with few channels
+ * may be split along L).  Asynchronous on `stream`: y and final_state are in
+ * host memory once `stream` has reached the call's end; work queued earlier
+ * on `stream` happens before the first copy.  Errors: as ssm_scan_fwd_ex;
+ * SSM_ERR_WORKSPACE when workspace is NULL or too small; outputs may not
+ * overlap inputs (final_state may equal init_state exactly).
+ */
+size_t ssm_scan_fwd_host_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen,
+                                         int64_t dstate, int io_dtype, int flags);
+int ssm_scan_fwd_host(const void* u, const void* delta, const float* delta_bias, const float* A,
+                      const float* B, const float* C, const float* D, const void* z, int flags,
+                      void* y, float* final_state, const float* init_state, int64_t batch,
+                      int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
  * Device-side status of the scans enqueued so far on this device.
  *
  * Synchronises `stream` (NULL = legacy default stream), then reads and clears

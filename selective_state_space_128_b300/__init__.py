@@ -77,6 +77,10 @@ def load():
     lib.ssm_conv1d_fwd.restype = i32
     lib.ssm_conv1d_update.argtypes = [vp, vp, vp, vp, i32, vp, i64, i64, i64, i32, vp]
     lib.ssm_conv1d_update.restype = i32
+    lib.ssm_scan_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i32, i32]
+    lib.ssm_scan_fwd_host_workspace_bytes.restype = sz
+    lib.ssm_scan_fwd_host.argtypes = [vp] * 8 + [i32, vp, vp, vp, i64, i64, i64, i64, i32, vp, sz, vp]
+    lib.ssm_scan_fwd_host.restype = i32
     _lib = lib
     return lib
 
@@ -125,6 +129,16 @@ def _check_dev(*ts):
             continue
         if not t.is_cuda:
             raise ValueError("libssm takes device tensors; got a tensor on %s" % t.device)
+        if not t.is_contiguous():
+            raise ValueError("libssm takes contiguous tensors")
+
+
+def _check_host(*ts):
+    for t in ts:
+        if t is None or isinstance(t, int):
+            continue
+        if t.is_cuda:
+            raise ValueError("ssm_scan_fwd_host takes host tensors; got one on %s" % t.device)
         if not t.is_contiguous():
             raise ValueError("libssm takes contiguous tensors")
 
@@ -181,6 +195,27 @@ def ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, fina
                                 _ptr(init_state), _ptr(workspace), int(workspace_bytes or 0),
                                 _stream(stream))
     _call("ssm_scan_fwd_ex", rc)
+
+
+def ssm_scan_fwd_host_workspace_bytes(batch, dim, seqlen, dstate, io_dtype, flags=0) -> int:
+    return int(load().ssm_scan_fwd_host_workspace_bytes(batch, dim, seqlen, dstate, io_dtype,
+                                                         int(flags)))
+
+
+def ssm_scan_fwd_host(u, delta, delta_bias, A, B, C, D, z, flags, y, final_state, init_state,
+                      workspace, workspace_bytes, stream=None):
+    """Tensor form of ``ssm_scan_fwd_host``: every tensor but the (device) workspace
+    lives in host memory (page-locked for overlapped copies); sizes as ssm_scan_fwd_ex."""
+    _check_host(u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state)
+    _check_dev(workspace)
+    batch, dim, L = _sizes(u, A, B)
+    N = A.shape[1]
+    rc = load().ssm_scan_fwd_host(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
+                                  _ptr(C), _ptr(D), _ptr(z), int(flags), _ptr(y),
+                                  _ptr(final_state), _ptr(init_state), batch, dim, L, N,
+                                  _io_dtype(u), _ptr(workspace), int(workspace_bytes or 0),
+                                  _stream(stream))
+    _call("ssm_scan_fwd_host", rc)
 
 
 def ssm_scan_fwd_train(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
@@ -336,6 +371,25 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True
             ws = torch.empty(nbytes, dtype=torch.uint8, device=u.device)
     ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler, bld), y,
                     h, init_state, ws, stream=stream)
+    return y, h
+
+
+def scan_host(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+              init_state=None, euler=False, bld=False, stream=None):
+    """y, final_state = scan_host(...): the scan on host tensors through
+    ``ssm_scan_fwd_host`` (copies pipelined against the scan inside the library);
+    allocates page-locked outputs and the device workspace, waits for the stream."""
+    import torch
+    batch, dim, L = _sizes(u, A, B)
+    N = A.shape[1]
+    flags = _flags(delta_softplus, euler, bld)
+    y = torch.empty(u.shape, dtype=u.dtype, pin_memory=True)
+    h = torch.empty((batch, dim, N), dtype=torch.float32, pin_memory=True)
+    nbytes = ssm_scan_fwd_host_workspace_bytes(batch, dim, L, N, _io_dtype(u), flags)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    st = stream if stream is not None else torch.cuda.current_stream()
+    ssm_scan_fwd_host(u, delta, delta_bias, A, B, C, D, z, flags, y, h, init_state, ws, nbytes, st)
+    st.synchronize()
     return y, h
 
 

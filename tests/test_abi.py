@@ -240,3 +240,42 @@ def test_ssd_argument_errors():
     assert ssm.ssm_ssd_workspace_bytes(8, 2048, 24, 64, 1, 128) == (
         units * 64 * 128 * 2 + units * 3 * 64 * 4 + 8 * 32 * 1 * 64 * 64 * 4)
     assert ssm.ssm_ssd_workspace_bytes(8, 2048, 24, 64, 5, 128) == 0  # 24 heads in 5 groups
+
+
+def _host(**kw):
+    a = dict(u=FAKE, delta=FAKE + 0x1000000, bias=None, A=FAKE + 0x2000000, B=FAKE + 0x3000000,
+             C=FAKE + 0x4000000, D=None, z=None, flags=1, y=FAKE + 0x5000000, h=None, init=None,
+             batch=2, dim=64, L=128, N=16, io=ssm.SSM_BF16, ws=FAKE + 0x9000000, wsb=1 << 30,
+             stream=None)
+    a.update(kw)
+    return lib().ssm_scan_fwd_host(a["u"], a["delta"], a["bias"], a["A"], a["B"], a["C"], a["D"],
+                                   a["z"], a["flags"], a["y"], a["h"], a["init"], a["batch"],
+                                   a["dim"], a["L"], a["N"], a["io"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_scan_host_argument_errors():
+    assert _host(u=None) == ssm.SSM_ERR_ARG
+    assert _host(y=None) == ssm.SSM_ERR_ARG
+    assert _host(io=7) == ssm.SSM_ERR_ARG
+    assert _host(flags=ssm.SSM_SAVED_STATES | 1) == ssm.SSM_ERR_ARG  # a backward-only bit
+    assert _host(batch=-1) == ssm.SSM_ERR_ARG
+    assert _host(N=12) == ssm.SSM_ERR_UNSUPPORTED
+    assert _host(ws=None) == ssm.SSM_ERR_WORKSPACE
+    assert _host(wsb=1024) == ssm.SSM_ERR_WORKSPACE
+    assert _host(ws=FAKE + 8) == ssm.SSM_ERR_ALIGN
+    assert _host(batch=0) == ssm.SSM_OK and _host(dim=0) == ssm.SSM_OK
+
+
+def test_scan_host_workspace_plan():
+    # three staging slots of a whole batch row (8 rows: one unit per row): u, delta, z, y of
+    # 1536 x 2048 bf16, B and C of 16 x 2048 fp32, two states of 1536 x 16 fp32; plus A, D, bias
+    slot = 4 * 1536 * 2048 * 2 + 2 * 16 * 2048 * 4 + 2 * 1536 * 16 * 4
+    params = 1536 * 16 * 4 + 2 * 1536 * 4
+    scan_ws = ssm.ssm_scan_workspace_bytes(1, 1536, 2048, 16, ssm.SSM_BF16)
+    assert ssm.ssm_scan_fwd_host_workspace_bytes(8, 1536, 2048, 16, ssm.SSM_BF16, 1) == \
+        params + scan_ws + 3 * slot
+    # batch 1: the row is cut into 8 blocks of channels, so a slot is an eighth as large
+    small = ssm.ssm_scan_fwd_host_workspace_bytes(1, 1536, 2048, 16, ssm.SSM_BF16, 1)
+    assert small < params + scan_ws + slot
+    assert ssm.ssm_scan_fwd_host_workspace_bytes(1, 64, 0, 16, ssm.SSM_BF16, 0) == 64 * 16 * 4
+    assert ssm.ssm_scan_fwd_host_workspace_bytes(1, 64, 10, 12, ssm.SSM_BF16, 0) == 0
