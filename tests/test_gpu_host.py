@@ -105,3 +105,27 @@ def test_scan_host_empty_sequence(with_init):
     y, h = ssm.scan_host(u, u, A, B, B, init_state=init if with_init else None)
     assert y.shape == (batch, dim, 0)
     assert torch.equal(h, init if with_init else torch.zeros_like(h))
+
+
+@pytest.mark.slow
+def test_scan_host_bench_shape_sampled():
+    """The bench's Mamba-130M layer through the host path at full size (8 batch-row
+    units through three slots): sampled channels against the oracle, every output
+    against the device entry point."""
+    w = synth.MAMBA_130M
+    x = synth.make_scan_inputs(w)
+    hx = _host(x)
+    y1, h1 = ssm.scan_host(hx["u"], hx["delta"], hx["A"], hx["B"], hx["C"], hx["D"], hx["z"],
+                           hx["delta_bias"])
+    rng = np.random.default_rng(7)
+    flat = np.sort(rng.choice(w.batch * w.dim, size=96, replace=False))
+    bs, ds = flat // w.dim, flat % w.dim
+    y_ref, h_ref = oracle.scan_rows(x["u"][bs, ds], x["delta"][bs, ds], x["z"][bs, ds], bs, ds,
+                                    x["A"], x["B"], x["C"], x["D"], x["delta_bias"], True)
+    assert oracle.rel_err(y1[bs, ds].double().numpy(), y_ref) <= TOL["bf16"]
+    assert oracle.rel_err(h1[bs, ds].double().numpy(), h_ref) <= TOL["bf16"]
+    g = upload_scan(x)
+    y0, h0 = ssm.scan(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"])
+    torch.cuda.synchronize()
+    assert oracle.rel_err(y1.double().numpy(), host64(y0)) <= TOL["bf16"]
+    assert oracle.rel_err(h1.double().numpy(), host64(h0)) <= TOL["bf16"]
