@@ -129,3 +129,26 @@ def test_scan_host_bench_shape_sampled():
     torch.cuda.synchronize()
     assert oracle.rel_err(y1.double().numpy(), host64(y0)) <= TOL["bf16"]
     assert oracle.rel_err(h1.double().numpy(), host64(h0)) <= TOL["bf16"]
+
+
+def test_scan_host_in_place_carry():
+    """final_state may be init_state itself: two calls over the two halves of a
+    sequence, the state carried in place in host memory, equal one call over the whole."""
+    w = synth.scaled(synth.MAMBA_130M, name="host_carry", batch=2, dim=64, seqlen=160, seed=183)
+    x = synth.make_scan_inputs(w)
+    y_ref, h_ref = _oracle(x)
+    hx = _host(x)
+    state = torch.zeros((2, 64, 16), dtype=torch.float32).pin_memory()
+    ws_bytes = ssm.ssm_scan_fwd_host_workspace_bytes(2, 64, 80, 16, ssm.SSM_BF16, 1)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    ys = []
+    for t0 in (0, 80):
+        part = {k: hx[k][:, :, t0:t0 + 80].contiguous().pin_memory() for k in ("u", "delta", "z", "B", "C")}
+        y = torch.empty((2, 64, 80), dtype=torch.bfloat16).pin_memory()
+        ssm.ssm_scan_fwd_host(part["u"], part["delta"], hx["delta_bias"], hx["A"], part["B"], part["C"],
+                              hx["D"], part["z"], 1, y, state, state, ws, ws_bytes)
+        torch.cuda.current_stream().synchronize()
+        ys.append(y)
+    y_all = torch.cat(ys, dim=2)
+    assert oracle.rel_err(y_all.double().numpy(), y_ref) <= TOL["bf16"]
+    assert oracle.rel_err(state.double().numpy(), h_ref) <= TOL["bf16"]
