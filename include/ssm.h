@@ -65,7 +65,7 @@ extern "C" {
 #define SSM_OK 0
 #define SSM_ERR_ARG (-1)         /* null required pointer, bad size, bad dtype, overlap */
 #define SSM_ERR_ALIGN (-2)       /* a pointer is not 16-byte aligned */
-#define SSM_ERR_UNSUPPORTED (-3) /* dstate not in {1, 2, 4, 8, 16, 32, 64, 128} (backward: <= 64) */
+#define SSM_ERR_UNSUPPORTED (-3) /* dstate not in {1, 2, 4, 8, 16, 32, 64, 128} */
 #define SSM_ERR_CUDA (-4)        /* a CUDA call or kernel launch failed */
 #define SSM_ERR_WORKSPACE (-5)   /* workspace given but too small */
 #define SSM_ERR_TIMEOUT (-6)     /* a kernel gave up waiting for its own data (see ssm_status) */

@@ -13,9 +13,9 @@ bool supported_n(int64_t n) {
   return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64 || n == 128;
 }
 
-// the backward keeps NPT states per lane and its recomputed chunk in shared
-// memory; it is built for dstate up to 64
-bool supported_bwd_n(int64_t n) { return supported_n(n) && n <= 64; }
+// the backward keeps up to 16 states per lane and its recomputed chunk in
+// shared memory; it is built for every dstate the forward supports
+bool supported_bwd_n(int64_t n) { return supported_n(n); }
 
 // [p, p + bytes) and [q, q + qbytes) intersect (null never does)
 bool overlaps(const void* p, size_t bytes, const void* q, size_t qbytes) {
@@ -53,7 +53,7 @@ const char* ssm_strerror(int status) {
     case SSM_ERR_ARG: return "SSM_ERR_ARG: invalid argument";
     case SSM_ERR_ALIGN: return "SSM_ERR_ALIGN: pointer not 16-byte aligned";
     case SSM_ERR_UNSUPPORTED:
-      return "SSM_ERR_UNSUPPORTED: dstate not in {1,2,4,8,16,32,64,128} (backward: up to 64), "
+      return "SSM_ERR_UNSUPPORTED: dstate not in {1,2,4,8,16,32,64,128}, "
              "or conv width not in 1..4";
     case SSM_ERR_CUDA: return "SSM_ERR_CUDA: CUDA launch failed";
     case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE: workspace too small";

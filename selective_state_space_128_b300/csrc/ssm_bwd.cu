@@ -43,10 +43,12 @@ namespace ssm {
 constexpr int kBwdThreads = 128;
 
 template <int N> struct BwdCfg {
-  static constexpr int NPT = N <= 4 ? N : (N <= 16 ? 4 : N / 4);  // states per lane
+  // states per lane: at most 16 (N = 128 spreads over 8 lanes of a channel)
+  static constexpr int NPT = N <= 4 ? N : (N <= 16 ? 4 : (N <= 64 ? N / 4 : 16));
   static constexpr int G = N / NPT;                                // lanes per channel
   static constexpr int CH = kBwdThreads / G;                       // channels per block
-  static constexpr int T = NPT <= 4 ? 16 : (NPT == 8 ? 8 : 4);     // steps per chunk
+  // steps per chunk (at least one channel step per thread in the per-step work)
+  static constexpr int T = NPT <= 4 ? 16 : (NPT == 8 ? 8 : (CH >= 32 ? 4 : 8));
   static constexpr int E = CH * T / kBwdThreads;  // channel steps per thread (per-step work)
   static constexpr int TPR = T / E;               // threads per channel row
   static constexpr int VW = NPT < 4 ? NPT : 4;    // floats per shared-memory vector
@@ -57,13 +59,18 @@ template <int N> struct BwdCfg {
   static constexpr int RowF = T + 1;              // per-channel-step tiles (odd rows)
   static constexpr int RowBC = N < 4 ? N : N + 4; // transposed B/C rows
   static constexpr int NU = T / 4;                // 4-step units of a partial row
-  // channel reductions: threads per reduced vector and channels per thread
-  static constexpr int RS = kBwdThreads / (T * G * QN);
+  // channel reductions: NV output vectors (step, state group, part); RS threads
+  // per vector and RCH channels per thread, or VPT vectors per thread when there
+  // are more vectors than threads
+  static constexpr int NV = T * G * QN;
+  static constexpr int RS = NV >= kBwdThreads ? 1 : kBwdThreads / NV;
+  static constexpr int VPT = NV >= kBwdThreads ? NV / kBwdThreads : 1;
   static constexpr int RCH = CH / RS;
   // resident blocks per SM the register budget is sized for (the lanes with 16
   // states, and the 16-step rows of N = 4, need more than a third of the file)
   static constexpr int MINB = (NPT >= 16 || (NPT == 4 && E >= 16)) ? 2 : 3;
-  static_assert(G * NPT == N && E >= 1 && TPR <= 4 && RS >= 1 && RCH * RS == CH, "tiling");
+  static_assert(G * NPT == N && E >= 1 && TPR <= 8 && RS >= 1 && RCH * RS == CH, "tiling");
+  static_assert(VPT * kBwdThreads == NV * RS, "whole reduction vectors per thread");
 };
 
 // Shared-memory layout (float offsets).
@@ -435,9 +442,9 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
   float dD_acc = 0.f, dbias_acc = 0.f;
   float* wsB_blk = p.ws_B + ((b * p.nblk + blk) * N) * L;
   float* wsC_blk = p.ws_C + ((b * p.nblk + blk) * N) * L;
-  // channel reductions: this thread's output vector (step rt, state group rg, part rq)
-  const int vid = tid / Cf::RS, part = tid % Cf::RS;
-  const int rt = vid / (G * QN), rg = (vid % (G * QN)) / QN, rq = vid % QN;
+  // channel reductions: this thread's output vectors (step rt, state group rg,
+  // part rq), VPT of them, and its share `part` of the channels
+  const int part = tid % Cf::RS;
 
   if (nch > 0) fetch(nch - 1, true, pre);
   for (int k = nch - 1; k >= 0; --k) {
@@ -557,27 +564,32 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
         }
       }
       // dC[t][n] = Σ_c ds[c][t] h_t[c][n]
-      float acc[VW];
 #pragma unroll
-      for (int v = 0; v < VW; ++v) acc[v] = 0.f;
-      const float* dsCol = sDS + rt;
+      for (int kv = 0; kv < Cf::VPT; ++kv) {
+        const int vid = tid / Cf::RS + kv * (kBwdThreads / Cf::RS);
+        const int rt = vid / (G * QN), rg = (vid % (G * QN)) / QN, rq = vid % QN;
+        float acc[VW];
+#pragma unroll
+        for (int v = 0; v < VW; ++v) acc[v] = 0.f;
+        const float* dsCol = sDS + rt;
 #pragma unroll 4
-      for (int i = 0; i < Cf::RCH; ++i) {
-        const int cc = part * Cf::RCH + ((i + vid * Cf::RS + part) & (Cf::RCH - 1));
-        const float w = dsCol[cc * Cf::RowF];
-        float hv[VW];
-        lds_vec<VW>(hs_vec(rt + 1, rq, bwd_lane_of<N>(cc, rg)), hv);
+        for (int i = 0; i < Cf::RCH; ++i) {
+          const int cc = part * Cf::RCH + ((i + vid * Cf::RS + part) & (Cf::RCH - 1));
+          const float w = dsCol[cc * Cf::RowF];
+          float hv[VW];
+          lds_vec<VW>(hs_vec(rt + 1, rq, bwd_lane_of<N>(cc, rg)), hv);
 #pragma unroll
-        for (int v = 0; v < VW; ++v) acc[v] = fmaf(w, hv[v], acc[v]);
-      }
+          for (int v = 0; v < VW; ++v) acc[v] = fmaf(w, hv[v], acc[v]);
+        }
 #pragma unroll
-      for (int s = Cf::RS / 2; s >= 1; s /= 2)
+        for (int s = Cf::RS / 2; s >= 1; s /= 2)
 #pragma unroll
-        for (int v = 0; v < VW; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], s);
-      if (part == 0 && rt < tc) {
+          for (int v = 0; v < VW; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], s);
+        if (part == 0 && rt < tc) {
 #pragma unroll
-        for (int v = 0; v < VW; ++v)
-          wsC_blk[(int64_t)(rg * NPT + rq * VW + v) * L + t0 + rt] = acc[v];
+          for (int v = 0; v < VW; ++v)
+            wsC_blk[(int64_t)(rg * NPT + rq * VW + v) * L + t0 + rt] = acc[v];
+        }
       }
     }
     __syncthreads();
@@ -755,25 +767,30 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
           }
         }
       }
-      float acc[VW];
 #pragma unroll
-      for (int v = 0; v < VW; ++v) acc[v] = 0.f;
+      for (int kv = 0; kv < Cf::VPT; ++kv) {
+        const int vid = tid / Cf::RS + kv * (kBwdThreads / Cf::RS);
+        const int rt = vid / (G * QN), rg = (vid % (G * QN)) / QN, rq = vid % QN;
+        float acc[VW];
+#pragma unroll
+        for (int v = 0; v < VW; ++v) acc[v] = 0.f;
 #pragma unroll 4
-      for (int i = 0; i < Cf::RCH; ++i) {
-        const int cc = part * Cf::RCH + ((i + vid * Cf::RS + part) & (Cf::RCH - 1));
-        float hv[VW];
-        lds_vec<VW>(hs_vec(rt + 1, rq, bwd_lane_of<N>(cc, rg)), hv);
+        for (int i = 0; i < Cf::RCH; ++i) {
+          const int cc = part * Cf::RCH + ((i + vid * Cf::RS + part) & (Cf::RCH - 1));
+          float hv[VW];
+          lds_vec<VW>(hs_vec(rt + 1, rq, bwd_lane_of<N>(cc, rg)), hv);
 #pragma unroll
-        for (int v = 0; v < VW; ++v) acc[v] += hv[v];
-      }
+          for (int v = 0; v < VW; ++v) acc[v] += hv[v];
+        }
 #pragma unroll
-      for (int s = Cf::RS / 2; s >= 1; s /= 2)
+        for (int s = Cf::RS / 2; s >= 1; s /= 2)
 #pragma unroll
-        for (int v = 0; v < VW; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], s);
-      if (part == 0 && rt < tc) {
+          for (int v = 0; v < VW; ++v) acc[v] += __shfl_xor_sync(0xffffffffu, acc[v], s);
+        if (part == 0 && rt < tc) {
 #pragma unroll
-        for (int v = 0; v < VW; ++v)
-          wsB_blk[(int64_t)(rg * NPT + rq * VW + v) * L + t0 + rt] = acc[v];
+          for (int v = 0; v < VW; ++v)
+            wsB_blk[(int64_t)(rg * NPT + rq * VW + v) * L + t0 + rt] = acc[v];
+        }
       }
     }
     __syncthreads();
@@ -858,6 +875,7 @@ static bool bwd_geometry(int64_t N, int64_t dim, int64_t L, int64_t& nblk, int64
     case 16: bwd_geom<16>(dim, L, nblk, nch); return true;
     case 32: bwd_geom<32>(dim, L, nblk, nch); return true;
     case 64: bwd_geom<64>(dim, L, nblk, nch); return true;
+    case 128: bwd_geom<128>(dim, L, nblk, nch); return true;
     default: return false;
   }
 }
@@ -873,6 +891,7 @@ int bwd_chunk(int64_t N) {
     case 16: return BwdCfg<16>::T;
     case 32: return BwdCfg<32>::T;
     case 64: return BwdCfg<64>::T;
+    case 128: return BwdCfg<128>::T;
     default: return 0;
   }
 }
@@ -927,6 +946,7 @@ static cudaError_t bwd_io(const BwdArgs& a, int64_t N, cudaStream_t stream) {
     case 16: return bwd_typed<IO, 16>(a, stream);
     case 32: return bwd_typed<IO, 32>(a, stream);
     case 64: return bwd_typed<IO, 64>(a, stream);
+    case 128: return bwd_typed<IO, 128>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

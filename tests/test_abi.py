@@ -136,8 +136,9 @@ def test_backward_argument_errors():
         assert _bwd(**{name: None}) == ssm.SSM_ERR_ARG, name
     assert _bwd(io=3) == ssm.SSM_ERR_ARG
     assert _bwd(N=12) == ssm.SSM_ERR_UNSUPPORTED
-    assert _bwd(N=128) == ssm.SSM_ERR_UNSUPPORTED          # the backward stops at 64
-    assert ssm.ssm_scan_bwd_workspace_bytes(2, 64, 128, 128) == 0
+    assert _bwd(N=256) == ssm.SSM_ERR_UNSUPPORTED
+    assert ssm.ssm_scan_bwd_workspace_bytes(2, 64, 128, 256) == 0
+    assert ssm.ssm_scan_bwd_workspace_bytes(2, 64, 128, 128) > 0  # N = 128: 8-step chunks
     # dz is required with a gate and refused without one
     assert _bwd(z=FAKE + 0xB000000) == ssm.SSM_ERR_ARG
     assert _bwd(dz=FAKE + 0xB000000) == ssm.SSM_ERR_ARG

@@ -80,14 +80,14 @@ def test_bf16_mamba_value_recipe():
     _check(w)
 
 
-@pytest.mark.parametrize("N", [1, 2, 4, 8, 32, 64])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 32, 64, 128])
 def test_bf16_every_state_size(N):
     w = synth.scaled(synth.MAMBA_130M, name="bwd_n%d" % N, batch=2, dim=150, seqlen=45,
                      dstate=N, seed=40 + N)
     _check(w)
 
 
-@pytest.mark.parametrize("N", [1, 4, 64])
+@pytest.mark.parametrize("N", [1, 4, 64, 128])
 def test_fp32_state_sizes(N):
     w = synth.scaled(synth.TINY, name="bwd_f32_n%d" % N, batch=1, dim=33, seqlen=37, dstate=N,
                      seed=50 + N, d_one=False)
@@ -171,15 +171,15 @@ def test_empty_sizes():
 
 
 @pytest.mark.parametrize("case", ["bf16_n16", "f32_n16", "bf16_n4", "bf16_split", "bf16_n32",
-                                  "euler"])
+                                  "bf16_n128", "euler"])
 def test_training_forward_saves_what_the_backward_recomputes(case):
     """ssm_scan_fwd_train returns the forward's results and saves the chunk-start
     states; the backward that starts from them (SSM_SAVED_STATES) gives the same
-    derivatives as the backward that recomputes them (N = 32 saves nothing and the
-    flag changes nothing)."""
+    derivatives as the backward that recomputes them (N = 32 and 128 save nothing
+    and the flag changes nothing)."""
     kw = dict(bf16_n16=dict(), f32_n16=dict(io="f32"), bf16_n4=dict(dstate=4),
               bf16_split=dict(batch=1, dim=64, seqlen=8192), bf16_n32=dict(dstate=32),
-              euler=dict())[case]
+              bf16_n128=dict(dstate=128, dim=40), euler=dict())[case]
     base = dict(name="bwd_saved", batch=2, dim=96, seqlen=300, seed=120)
     base.update(kw)
     w = synth.scaled(synth.MAMBA_130M, **base)

@@ -79,10 +79,10 @@ def test_decode_euler_matches_oracle(io):
         assert oracle.rel_err(host64(st), st_ref) <= TOL[io]
 
 
-@pytest.mark.parametrize("io", ["bf16", "f32"])
-def test_backward_euler_matches_oracle(io):
+@pytest.mark.parametrize("io,N", [("bf16", 16), ("f32", 16), ("bf16", 128)])
+def test_backward_euler_matches_oracle(io, N):
     w = synth.scaled(synth.MAMBA_130M, name="euler_bwd", batch=2, dim=40, seqlen=70, io=io,
-                     seed=98)
+                     dstate=N, seed=98)
     x = synth.make_scan_inputs(w)
     x["A"][1, ::2] = 0.0
     e = synth.make_bwd_inputs(w)

@@ -61,7 +61,8 @@ def test_scan_bld_split_plan():
 
 
 @pytest.mark.parametrize("io,N,dim,L", [("bf16", 16, 96, 130), ("f32", 16, 40, 45),
-                                        ("bf16", 4, 70, 300), ("bf16", 32, 33, 40)])
+                                        ("bf16", 4, 70, 300), ("bf16", 32, 33, 40),
+                                        ("bf16", 128, 20, 70)])
 def test_backward_bld_matches_oracle(io, N, dim, L):
     w = synth.scaled(synth.MAMBA_130M, name="bld_bwd", batch=2, dim=dim, seqlen=L, dstate=N,
                      io=io, seed=160 + N)
