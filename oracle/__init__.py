@@ -265,6 +265,52 @@ def conv1d(x, weight, bias=None, state_in=None, silu=True, nthreads=0):
     return out, sout
 
 
+def _f64(arr):
+    """float32 or bfloat16 bits (uint16) -> float64 (bf16 decoded exactly)."""
+    arr = np.ascontiguousarray(arr)
+    if arr.dtype == np.uint16:
+        return (arr.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return arr.astype(np.float64)
+
+
+def conv1d_bwd(x, weight, bias, state_in, silu, dout):
+    """Derivatives of ``conv1d``'s output against a cotangent ``dout`` (batch, dim, L)
+    (the causal depthwise conv1d + SiLU of the summary page's section 4a shape
+    table, width d_conv of the configuration page), by the chain rule in fp64:
+
+        p_t = bias + Σ_k w[k] x[t-(K-1)+k]     (x before the sequence from state_in)
+        g_t = dout_t · silu'(p_t),   silu'(p) = σ(p) (1 + p (1 - σ(p)))   (g = dout without SiLU)
+        dx[s]     = Σ_k w[k] g[s+(K-1)-k]      for every input position s, the K-1
+                                               before the sequence giving d state_in
+        dw[d,k]   = Σ_{b,t} g[b,d,t] x[b,d,t-(K-1)+k]
+        dbias[d]  = Σ_{b,t} g[b,d,t]
+
+    Returns dict(dx (batch, dim, L), dweight (dim, K), dbias (dim,),
+    dstate (batch, dim, K-1)), all float64."""
+    xf = _f64(x)
+    batch, dim, L = xf.shape
+    w = np.asarray(weight, dtype=np.float64)
+    K = w.shape[1]
+    st = np.zeros((batch, dim, K - 1)) if state_in is None else np.asarray(state_in, dtype=np.float64)
+    xp = np.concatenate([st, xf], axis=2)          # input positions -(K-1) .. L-1
+    p = np.zeros((batch, dim, L))
+    for k in range(K):
+        p += w[None, :, k, None] * xp[:, :, k:k + L]
+    if bias is not None:
+        p += np.asarray(bias, dtype=np.float64)[None, :, None]
+    g = _f64(dout)
+    if silu:
+        sg = 1.0 / (1.0 + np.exp(-p))
+        g = g * sg * (1.0 + p * (1.0 - sg))
+    dxp = np.zeros_like(xp)
+    dw = np.zeros((dim, K))
+    for k in range(K):
+        dxp[:, :, k:k + L] += w[None, :, k, None] * g
+        dw[:, k] = np.sum(g * xp[:, :, k:k + L], axis=(0, 2))
+    return dict(dx=dxp[:, :, K - 1:], dweight=dw, dbias=np.sum(g, axis=(0, 2)),
+                dstate=dxp[:, :, :K - 1])
+
+
 def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, init_state=None,
         euler=False, nthreads=0):
     """Mamba-2's scalar-A state space model ([C] §5.1: A_t = a_t I per head), by its

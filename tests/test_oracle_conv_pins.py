@@ -85,3 +85,71 @@ def test_state_enters_the_first_outputs_only():
         for t in range(3):
             ref[d, t] = sum(float(w[0 + d, k]) * s0[0, d, 3 + t - 3 + k] for k in range(4) if t - 3 + k < 0)
     assert np.max(np.abs((b - a)[0, :, :3] - ref)) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# the backward of the front end (oracle.conv1d_bwd, numpy fp64) against the
+# forward oracle (the C code): finite differences, and the exact adjoint identity
+# of the linear part
+# ---------------------------------------------------------------------------
+
+def _loss(x, w, bias, s0, silu, dout):
+    out, _ = oracle.conv1d(x, w, bias, s0, silu=silu)
+    return float(np.sum(out * dout))
+
+
+@pytest.mark.parametrize("K", [1, 2, 4])
+def test_backward_linear_part_is_the_adjoint(K):
+    """Without SiLU the conv is linear in (state, x) and in (w, bias), so
+    <out, dout> = <x, dx> + <state, dstate> = Σ w·dw + Σ bias·dbias exactly (up to
+    fp64 rounding): a wrong index, sign or dropped term breaks one of the two."""
+    x = _x((2, 3, 19), 20 + K)
+    w = _x((3, K), 21)
+    bias = _x((3,), 22)
+    s0 = _x((2, 3, K - 1), 23)
+    dout = _x((2, 3, 19), 24).astype(np.float64)
+    g = oracle.conv1d_bwd(x, w, None, s0, False, dout)
+    lhs = _loss(x, w, None, s0.astype(np.float64), False, dout)
+    rhs = np.sum(x.astype(np.float64) * g["dx"]) + np.sum(s0.astype(np.float64) * g["dstate"])
+    assert abs(lhs - rhs) < 1e-11 * max(1.0, abs(lhs))
+    gb = oracle.conv1d_bwd(x, w, bias, s0, False, dout)
+    lhs_b = _loss(x, w, bias, s0.astype(np.float64), False, dout)
+    rhs_b = np.sum(w.astype(np.float64) * gb["dweight"]) + np.sum(bias.astype(np.float64) * gb["dbias"])
+    assert abs(lhs_b - rhs_b) < 1e-11 * max(1.0, abs(lhs_b))
+
+
+@pytest.mark.parametrize("K", [3, 4])
+def test_backward_matches_finite_differences(K):
+    """With SiLU: central differences of <conv1d(...), dout> (the forward oracle, float32
+    inputs perturbed by h = 2^-7, exactly representable) for sampled x, state, weight and
+    bias entries."""
+    rng = np.random.default_rng(30 + K)
+    x = _x((1, 2, 12), 31)
+    w = (0.5 * _x((2, K), 32)).astype(np.float32)
+    bias = _x((2,), 33)
+    s0 = _x((1, 2, K - 1), 34)
+    dout = _x((1, 2, 12), 35).astype(np.float64)
+    g = oracle.conv1d_bwd(x, w, bias, s0, True, dout)
+    h = np.float32(2.0 ** -7)
+
+    def fd(arr, idx, name):
+        a, b = arr.copy(), arr.copy()
+        a[idx] += h
+        b[idx] -= h
+        args = dict(x=x, w=w, bias=bias, s0=s0)
+        args[name] = a
+        up = _loss(args["x"], args["w"], args["bias"], args["s0"].astype(np.float64), True, dout)
+        args[name] = b
+        dn = _loss(args["x"], args["w"], args["bias"], args["s0"].astype(np.float64), True, dout)
+        return (up - dn) / (2 * float(h))
+
+    for _ in range(6):
+        i = (0, int(rng.integers(2)), int(rng.integers(12)))
+        assert abs(fd(x, i, "x") - g["dx"][i]) < 2e-4 * max(1.0, abs(g["dx"][i]))
+    for j in range(K - 1):
+        i = (0, 1, j)
+        assert abs(fd(s0, i, "s0") - g["dstate"][i]) < 2e-4 * max(1.0, abs(g["dstate"][i]))
+    for k in range(K):
+        i = (1, k)
+        assert abs(fd(w, i, "w") - g["dweight"][i]) < 2e-4 * max(1.0, abs(g["dweight"][i]))
+    assert abs(fd(bias, (0,), "bias") - g["dbias"][0]) < 2e-4 * max(1.0, abs(g["dbias"][0]))
