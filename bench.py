@@ -359,7 +359,29 @@ def bench_conv(w, steps, warmup, world, width=4, copies=3):
     torch.cuda.synchronize()
     ms = max_over_ranks(world, e0.elapsed_time(e1)) / steps
     nbytes = 2 * xs[0].numel() * 2 + wt.numel() * 4 + bias.numel() * 4
-    return dict(step_ms=ms, steps=steps, bytes=nbytes)
+    # the backward on the same shapes: x and dout read, dx written (the outs
+    # buffers serve as the cotangents, dxs rotate like the inputs)
+    dxs = [torch.empty_like(xs[0]) for _ in range(copies)]
+    dw = torch.empty_like(wt)
+    db = torch.empty_like(bias)
+
+    def bwd(i):
+        ssm.ssm_conv1d_bwd(xs[i % copies], wt, bias, None, 1, outs[(i + 1) % copies], dxs[i % copies],
+                           dw, db, None, stream)
+
+    for i in range(warmup):
+        bwd(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        bwd(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    bms = max_over_ranks(world, e0.elapsed_time(e1)) / steps
+    bbytes = 3 * xs[0].numel() * 2 + 2 * (wt.numel() + bias.numel()) * 4
+    return dict(step_ms=ms, steps=steps, bytes=nbytes, bwd_ms=bms, bwd_bytes=bbytes)
 
 
 # ---------------------------------------------------------------------------
@@ -735,7 +757,12 @@ def main():
                           "hbm_gbs": conv["bytes"] / cs / 1e9,
                           "hbm_frac": conv["bytes"] / cs / 1e9 / hbm_peak,
                           "bytes_per_step": conv["bytes"], "gpu_launches": conv["steps"],
-                          "l2": "3 input/output pairs rotated: 300 MB, larger than L2"}
+                          "l2": "3 input/output pairs rotated: 300 MB, larger than L2",
+                          "backward": {"us_per_step": conv["bwd_ms"] * 1e3,
+                                       "hbm_gbs": conv["bwd_bytes"] / (conv["bwd_ms"] / 1e3) / 1e9,
+                                       "bytes_per_step": conv["bwd_bytes"],
+                                       "gpu_launches": conv["steps"],
+                                       "call": "ssm_conv1d_bwd (dx, dweight, dbias; one kernel)"}}
     if ssd is not None:
         sh = SSD_SHAPE
         ss = ssd["step_ms"] / 1e3

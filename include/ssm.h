@@ -318,6 +318,31 @@ int ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
                    void* stream);
 
 /*
+ * Backward of ssm_conv1d_fwd (the front end of the summary page's section 4a
+ * shape table): for a cotangent dout of `out`, with p_t the pre-activation and
+ * g_t = dout_t · silu'(p_t), silu'(p) = σ(p)(1 + p(1 - σ(p))) (g = dout when
+ * bit 1 of `silu` is clear),
+ *
+ *     dx[b,d,s]           = Σ_k weight[d,k] g[b,d,s+(K-1)-k]   (s inside the sequence)
+ *     d_conv_state_in     = the same sum at the K-1 positions before it
+ *     dweight[d,k]        = Σ_{b,t} g[b,d,t] x[b,d,t-(K-1)+k]
+ *     dbias[d]            = Σ_{b,t} g[b,d,t]
+ *
+ * x, conv_state_in, weight, bias, silu (with SSM_LAYOUT_BLD), sizes and
+ * layouts as ssm_conv1d_fwd; dout and dx like x (io_dtype); dweight (dim,
+ * width) float32, required; dbias (dim) float32 and d_conv_state_in (batch,
+ * dim, width-1) float32, nullable.  The sums over the batch and the steps are
+ * added in a fixed order (one block per channel), so results repeat bit for
+ * bit.  Outputs may not overlap inputs or each other.  Errors as
+ * ssm_conv1d_fwd.  Asynchronous on `stream` (one kernel; memsets when a size
+ * is zero).
+ */
+int ssm_conv1d_bwd(const void* x, const float* weight, const float* bias,
+                   const void* conv_state_in, int silu, const void* dout, void* dx,
+                   float* dweight, float* dbias, float* d_conv_state_in, int64_t batch,
+                   int64_t dim, int64_t seqlen, int64_t width, int io_dtype, void* stream);
+
+/*
  * One token of the front end on a rolling state (decode): for every (b, d),
  * window = (conv_state[b,d,0..K-2], x[b,d]); out[b,d] = silu(bias[d] +
  * Σ_k weight[d,k] window[k]); conv_state[b,d] <- window[1..K-1] (in place).

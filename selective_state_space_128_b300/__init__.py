@@ -77,6 +77,9 @@ def load():
     lib.ssm_conv1d_fwd.restype = i32
     lib.ssm_conv1d_update.argtypes = [vp, vp, vp, vp, i32, vp, i64, i64, i64, i32, vp]
     lib.ssm_conv1d_update.restype = i32
+    lib.ssm_conv1d_bwd.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32,
+                                   vp]
+    lib.ssm_conv1d_bwd.restype = i32
     lib.ssm_scan_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i32, i32]
     lib.ssm_scan_fwd_host_workspace_bytes.restype = sz
     lib.ssm_scan_fwd_host.argtypes = [vp] * 8 + [i32, vp, vp, vp, i64, i64, i64, i64, i32, vp, sz, vp]
@@ -315,6 +318,19 @@ def ssm_conv1d_fwd(x, weight, bias, conv_state_in, silu, out, conv_state_out, st
     _call("ssm_conv1d_fwd", rc)
 
 
+def ssm_conv1d_bwd(x, weight, bias, conv_state_in, silu, dout, dx, dweight, dbias,
+                   d_conv_state_in, stream=None):
+    """Tensor form of ``ssm_conv1d_bwd``: x, dout, dx like the forward's x."""
+    _check_dev(x, weight, bias, conv_state_in, dout, dx, dweight, dbias, d_conv_state_in)
+    batch = x.shape[0]
+    dim, L = (x.shape[2], x.shape[1]) if int(silu) & SSM_LAYOUT_BLD else (x.shape[1], x.shape[2])
+    rc = load().ssm_conv1d_bwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state_in), int(silu),
+                               _ptr(dout), _ptr(dx), _ptr(dweight), _ptr(dbias),
+                               _ptr(d_conv_state_in), batch, dim, L, weight.shape[1], _io_dtype(x),
+                               _stream(stream))
+    _call("ssm_conv1d_bwd", rc)
+
+
 def ssm_conv1d_update(conv_state, x, weight, bias, silu, out, stream=None):
     """Tensor form of ``ssm_conv1d_update``: x (batch, dim), conv_state (batch, dim, width-1)."""
     _check_dev(conv_state, x, weight, bias, out)
@@ -456,6 +472,20 @@ def conv1d(x, weight, bias=None, conv_state=None, silu=True, want_state=False, s
     ssm_conv1d_fwd(x, weight, bias, conv_state, int(bool(silu)) | (SSM_LAYOUT_BLD if bld else 0),
                    out, st, stream)
     return (out, st) if want_state else out
+
+
+def conv1d_bwd(x, weight, dout, bias=None, conv_state=None, silu=True, bld=False, stream=None):
+    """Derivatives of ``conv1d``'s output against ``dout``: dict(dx (like x), dweight
+    (dim, width), dbias (dim,), dstate (batch, dim, width-1)), the last three float32."""
+    import torch
+    batch, dim, K = x.shape[0], weight.shape[0], weight.shape[1]
+    dx = torch.empty_like(x)
+    dw = torch.empty((dim, K), dtype=torch.float32, device=x.device)
+    db = torch.empty((dim,), dtype=torch.float32, device=x.device)
+    ds = torch.empty((batch, dim, K - 1), dtype=torch.float32, device=x.device) if K > 1 else None
+    ssm_conv1d_bwd(x, weight, bias, conv_state, int(bool(silu)) | (SSM_LAYOUT_BLD if bld else 0),
+                   dout, dx, dw, db, ds, stream)
+    return dict(dx=dx, dweight=dw, dbias=db, dstate=ds)
 
 
 def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, init_state=None,

@@ -445,6 +445,55 @@ int ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+int ssm_conv1d_bwd(const void* x, const float* weight, const float* bias,
+                   const void* conv_state_in, int silu, const void* dout, void* dx,
+                   float* dweight, float* dbias, float* d_conv_state_in, int64_t batch,
+                   int64_t dim, int64_t seqlen, int64_t width, int io_dtype, void* stream) {
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if ((silu & ~(1 | SSM_LAYOUT_BLD)) != 0) return SSM_ERR_ARG;
+  if (!sizes_ok(batch, dim, seqlen) || width <= 0) return SSM_ERR_ARG;
+  if (width > 4) return SSM_ERR_UNSUPPORTED;
+  if (dim > 0 && !dweight) return SSM_ERR_ARG;
+  const bool rows = batch > 0 && dim > 0;
+  if (rows && seqlen > 0 && (!x || !weight || !dout || !dx)) return SSM_ERR_ARG;
+  const void* ptrs[] = {x, weight, bias, conv_state_in, dout, dx, dweight, dbias, d_conv_state_in};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
+  const size_t nio = (size_t)batch * (size_t)dim * (size_t)seqlen * esz;
+  const size_t nst = (size_t)batch * (size_t)dim * (size_t)(width - 1);
+  const size_t nw = (size_t)dim * (size_t)width * 4, nb = (size_t)dim * 4;
+  // outputs overlap no input and no other output
+  const void* ins[] = {x, weight, bias, conv_state_in, dout};
+  const size_t insz[] = {nio, nw, nb, nst * esz, nio};
+  const void* outs[] = {dx, dweight, dbias, d_conv_state_in};
+  const size_t outsz[] = {nio, nw, nb, nst * 4};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 5; ++j)
+      if (overlaps(outs[i], outsz[i], ins[j], insz[j])) return SSM_ERR_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i], outsz[i], outs[j], outsz[j])) return SSM_ERR_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!rows || seqlen == 0) {
+    // no step: every derivative is zero
+    if (dim > 0 && cudaMemsetAsync(dweight, 0, nw, st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (dim > 0 && dbias && cudaMemsetAsync(dbias, 0, nb, st) != cudaSuccess) return SSM_ERR_CUDA;
+    if (d_conv_state_in && nst && cudaMemsetAsync(d_conv_state_in, 0, nst * 4, st) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    return SSM_OK;
+  }
+  ssm::ConvBwdArgs a{};
+  a.x = x; a.w = weight; a.bias = bias; a.state_in = conv_state_in; a.dout = dout; a.dx = dx;
+  a.dw = dweight; a.dbias = dbias; a.dstate = width > 1 ? d_conv_state_in : nullptr;
+  a.batch = batch; a.dim = dim; a.L = seqlen;
+  a.silu = (silu & 1) != 0;
+  a.precise = io_dtype == SSM_F32;
+  a.bld = (silu & SSM_LAYOUT_BLD) != 0;
+  const cudaError_t e = ssm::conv_bwd_launch(a, width, io_dtype, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 int ssm_conv1d_update(void* conv_state, const void* x, const float* weight, const float* bias,
                       int silu, void* out, int64_t batch, int64_t dim, int64_t width,
                       int io_dtype, void* stream) {

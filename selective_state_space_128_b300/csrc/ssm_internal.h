@@ -156,6 +156,28 @@ struct ConvArgs {
 cudaError_t conv_launch(const ConvArgs& a, int64_t width, int io_dtype, bool update,
                         cudaStream_t stream);
 
+// Arguments of the conv1d backward: x, dout, dx as the forward's x (io dtype),
+// weight (dim, K) fp32, bias (dim) fp32 or null, state_in (batch, dim, K-1) io
+// dtype or null; outputs dw (dim, K), dbias (dim) or null, dstate (batch, dim,
+// K-1) or null, fp32.
+struct ConvBwdArgs {
+  const void* x;
+  const float* w;
+  const float* bias;
+  const void* state_in;
+  const void* dout;
+  void* dx;
+  float* dw;
+  float* dbias;
+  float* dstate;
+  int64_t batch, dim, L;
+  bool silu;
+  bool precise;  // libm exponential and division (float32 I/O)
+  bool bld;
+};
+
+cudaError_t conv_bwd_launch(const ConvBwdArgs& a, int64_t width, int io_dtype, cudaStream_t stream);
+
 // Arguments of the chunked scalar-A SSM (Mamba-2 SSD).  x, z, y (batch, L, H,
 // P) bf16; dt (batch, L, H) bf16; B, C (batch, L, G, N) bf16; A, D, dt_bias (H)
 // fp32; states (batch, H, P, N) fp32.  Workspace parts: the states entering

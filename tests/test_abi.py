@@ -280,3 +280,23 @@ def test_scan_host_workspace_plan():
     assert small < params + scan_ws + slot
     assert ssm.ssm_scan_fwd_host_workspace_bytes(1, 64, 0, 16, ssm.SSM_BF16, 0) == 64 * 16 * 4
     assert ssm.ssm_scan_fwd_host_workspace_bytes(1, 64, 10, 12, ssm.SSM_BF16, 0) == 0
+
+
+def test_conv1d_bwd_argument_errors():
+    def call(**kw):
+        a = dict(x=FAKE, w=FAKE + 0x1000000, b=None, st=None, silu=1, dout=FAKE + 0x2000000,
+                 dx=FAKE + 0x3000000, dw=FAKE + 0x4000000, db=None, ds=None, batch=2, dim=64, L=128,
+                 K=4, io=ssm.SSM_BF16)
+        a.update(kw)
+        return lib().ssm_conv1d_bwd(a["x"], a["w"], a["b"], a["st"], a["silu"], a["dout"], a["dx"],
+                                    a["dw"], a["db"], a["ds"], a["batch"], a["dim"], a["L"], a["K"],
+                                    a["io"], None)
+    assert call(K=5) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(K=0) == ssm.SSM_ERR_ARG
+    assert call(io=9) == ssm.SSM_ERR_ARG
+    assert call(silu=4) == ssm.SSM_ERR_ARG
+    assert call(dw=None) == ssm.SSM_ERR_ARG
+    assert call(dout=None) == ssm.SSM_ERR_ARG
+    assert call(dx=FAKE + 0x3000008) == ssm.SSM_ERR_ALIGN
+    assert call(dx=FAKE + 0x10) == ssm.SSM_ERR_ARG          # dx overlapping x
+    assert call(db=FAKE + 0x4000010) == ssm.SSM_ERR_ARG     # dbias overlapping dweight

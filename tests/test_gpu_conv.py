@@ -111,3 +111,53 @@ def test_conv1d_feeds_the_scan():
                     dev_f32(xs["C"]), dev_f32(xs["D"]), dev_io(xs["z"]), dev_f32(xs["delta_bias"]))
     torch.cuda.synchronize()
     assert oracle.rel_err(host64(y), y_ref) <= 1e-2
+
+
+# ---------------------------------------------------------------------------
+# the backward (ssm_conv1d_bwd) against oracle.conv1d_bwd
+# ---------------------------------------------------------------------------
+
+def _dout(io, shape, seed):
+    n = int(np.prod(shape))
+    return synth.fill(seed, synth.S_DY, 0, n, synth.NORMAL, 0.0, 1.0, dtype=io).reshape(shape)
+
+
+def _check_bwd(io, batch, dim, L, K, seed, silu=True, state=True, bias=True, bld=False):
+    x, wt, b, st = _inputs(io, batch, dim, L, K, seed, state)
+    dout = _dout(io, (batch, dim, L), seed + 1)
+    ref = oracle.conv1d_bwd(x, wt, b if bias else None, _as64(st), silu, dout)
+    tr = (lambda t: t.transpose(1, 2).contiguous()) if bld else (lambda t: t)
+    out = ssm.conv1d_bwd(tr(dev_io(x)), dev_f32(wt), tr(dev_io(dout)), dev_f32(b) if bias else None,
+                         dev_io(st) if st is not None else None, silu=silu, bld=bld)
+    torch.cuda.synchronize()
+    got_dx = host64(out["dx"].transpose(1, 2) if bld else out["dx"])
+    assert oracle.rel_err(got_dx, ref["dx"]) <= TOL[io]
+    assert oracle.rel_err(host64(out["dweight"]), ref["dweight"]) <= TOL[io] / 10
+    assert oracle.rel_err(host64(out["dbias"]), ref["dbias"]) <= TOL[io] / 10
+    if K > 1:
+        assert oracle.rel_err(host64(out["dstate"]), ref["dstate"]) <= TOL[io] / 10
+    return out
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+@pytest.mark.parametrize("L", [64, 67, 5])
+def test_conv1d_bwd_matches_oracle(io, K, L):
+    _check_bwd(io, 3, 37, L, K, seed=70 + K + L)
+
+
+@pytest.mark.parametrize("case", ["no_silu", "no_state_no_bias", "long_rows", "bld", "bld_ragged"])
+def test_conv1d_bwd_variants(case):
+    kw = dict(no_silu=dict(silu=False), no_state_no_bias=dict(state=False, bias=False),
+              long_rows=dict(L=5000), bld=dict(bld=True), bld_ragged=dict(bld=True, L=29))[case]
+    args = dict(io="bf16", batch=2, dim=24, L=136, K=4, seed=90)
+    args.update(kw)
+    _check_bwd(**args)
+
+
+def test_conv1d_bwd_repeats_bit_for_bit():
+    """The sums over the batch are added in a fixed order."""
+    a = _check_bwd("bf16", 4, 16, 100, 4, seed=95)
+    b = _check_bwd("bf16", 4, 16, 100, 4, seed=95)
+    for k in ("dx", "dweight", "dbias", "dstate"):
+        assert torch.equal(a[k], b[k]), k
