@@ -135,3 +135,37 @@ def test_backward_pins_catch_planted_mistake(mutant, tmp_path, monkeypatch):
 def test_conv_pins_catch_planted_mistake(mutant, tmp_path, monkeypatch):
     old, new = CONV_MUTANTS[mutant]
     assert _run_mutant(old, new, tmp_path, monkeypatch, conv_pins, "conv"), "no pin caught " + mutant
+
+
+# mistakes in the front end's backward (oracle.conv1d_bwd, numpy): planted in a
+# copy of the function's source, which then stands in for the real one
+CONV_BWD_MUTANTS = {
+    "convbwd_taps_flipped": ("dxp[:, :, k:k + L] += w[None, :, k, None] * g",
+                             "dxp[:, :, k:k + L] += w[None, :, K - 1 - k, None] * g"),
+    "convbwd_dw_unshifted": ("dw[:, k] = np.sum(g * xp[:, :, k:k + L], axis=(0, 2))",
+                             "dw[:, k] = np.sum(g * xp[:, :, K - 1:K - 1 + L], axis=(0, 2))"),
+    "convbwd_silu_slope": ("g = g * sg * (1.0 + p * (1.0 - sg))", "g = g * sg"),
+    "convbwd_bias_not_in_p": ("p += np.asarray(bias, dtype=np.float64)[None, :, None]",
+                              "p += 0.0 * np.asarray(bias, dtype=np.float64)[None, :, None]"),
+    "convbwd_state_grad_dropped": ("dstate=dxp[:, :, :K - 1])", "dstate=0.0 * dxp[:, :, :K - 1])"),
+    "convbwd_dbias_sign": ("dbias=np.sum(g, axis=(0, 2))", "dbias=-np.sum(g, axis=(0, 2))"),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(CONV_BWD_MUTANTS))
+def test_conv_backward_pins_catch_planted_mistake(mutant, monkeypatch):
+    old, new = CONV_BWD_MUTANTS[mutant]
+    src = inspect.getsource(oracle.conv1d_bwd)
+    assert src.count(old) == 1, "mutation site not found: " + old
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "conv1d_bwd_mutant", "exec"), ns)
+    monkeypatch.setattr(oracle, "conv1d_bwd", ns["conv1d_bwd"])
+    caught = []
+    for name, call in _pin_calls(conv_pins):
+        if not name.startswith("test_backward"):
+            continue
+        try:
+            call()
+        except AssertionError:
+            caught.append(name)
+    assert caught, "no pin caught " + mutant
