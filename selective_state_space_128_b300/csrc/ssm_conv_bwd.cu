@@ -14,7 +14,8 @@
 // after them (their inputs are L1 hits, loaded by the neighbouring thread too),
 // writes dx for its steps and accumulates its share of dw and dbias over all
 // rows in registers; the block adds the shares in a fixed order, so the
-// results repeat bit for bit and no second pass is needed.
+// results repeat bit for bit and no second pass is needed.  The 16-byte x and
+// dout vectors of a thread's next unit are in flight while it works on this one.
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -25,6 +26,31 @@ constexpr int kConvBwdSteps = 8;  // steps per thread
 // 64 registers a thread, 4 blocks per SM: the pass is bound by memory latency,
 // so resident warps matter more than keeping every temporary in a register
 // (on an 8 x 1536 x 2048 bf16 input: 97 us at 120 registers and 2 blocks per SM, 70 us here)
+
+// 8 consecutive elements held as raw 16-byte words until they are used.
+template <typename IO> struct RawVec8;
+template <> struct RawVec8<__nv_bfloat16> {
+  uint4 r;
+  __device__ void load(const __nv_bfloat16* p) { r = *reinterpret_cast<const uint4*>(p); }
+  __device__ void get(float (&v)[8]) const {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+template <> struct RawVec8<float> {
+  float4 a, b;
+  __device__ void load(const float* p) {
+    a = reinterpret_cast<const float4*>(p)[0];
+    b = reinterpret_cast<const float4*>(p)[1];
+  }
+  __device__ void get(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
 
 template <typename IO, int K>
 __global__ void __launch_bounds__(kConvBwdThreads, 4) conv1d_bwd_kernel(const ConvBwdArgs p) {
@@ -44,26 +70,55 @@ __global__ void __launch_bounds__(kConvBwdThreads, 4) conv1d_bwd_kernel(const Co
   float dw[K], db = 0.f;
 #pragma unroll
   for (int k = 0; k < K; ++k) dw[k] = 0.f;
-  for (int64_t b = 0; b < p.batch; ++b) {
+  // the (row, step-chunk) units of this channel, in order; a thread's 16-byte
+  // vectors of x and dout for the next unit are loaded while it works on this one
+  const int64_t chunk = (int64_t)kConvBwdThreads * S;
+  const int64_t nt = (L + chunk - 1) / chunk;
+  const int64_t units = p.batch * nt;
+  auto unit_t0 = [&](int64_t i) { return (i % nt) * chunk + (int64_t)threadIdx.x * S; };
+  auto unit_base = [&](int64_t i) {
+    const int64_t bb = i / nt;
+    return p.bld ? bb * L * p.dim + d : (bb * p.dim + d) * L;
+  };
+  RawVec8<IO> nx, ng;  // the next unit's vectors
+  bool nvec = false;
+  auto prefetch = [&](int64_t i) {
+    nvec = false;
+    if (i < units) {
+      const int64_t t0 = unit_t0(i);
+      if (vec && t0 + S <= L) {
+        const int64_t bs = unit_base(i);
+        nx.load(x + bs + t0);
+        ng.load(dout + bs + t0);
+        nvec = true;
+      }
+    }
+  };
+  prefetch(0);
+  for (int64_t u = 0; u < units; ++u) {
+    const RawVec8<IO> cx = nx, cg = ng;
+    const bool cvec = nvec;
+    prefetch(u + 1);
+    const int64_t b = u / nt, t0 = unit_t0(u);
+    if (t0 >= L) continue;
     const int64_t row = b * p.dim + d;
     // element t of the row: base + t * ts (ts = 1, or dim in the (batch, L, dim) layout)
-    const int64_t base = p.bld ? b * L * p.dim + d : row * L;
+    const int64_t base = unit_base(u);
     const IO* st = p.state_in ? static_cast<const IO*>(p.state_in) + row * H : nullptr;
     // input position s in [-(K-1), L): the carried state before the sequence
     auto xin = [&](int64_t s) -> float {
       if (s < 0) return st ? io_traits<IO>::to_f32(st[H + s]) : 0.f;
       return s < L ? io_traits<IO>::to_f32(x[base + s * ts]) : 0.f;
     };
-    for (int64_t t0 = (int64_t)threadIdx.x * S; t0 < L; t0 += (int64_t)kConvBwdThreads * S) {
+    {
       // inputs at positions t0-(K-1) .. t0+S-1+(K-1), cotangents at t0 .. t0+S-1+(K-1)
       float xs[S + 2 * H], gs[S + H];
-      const bool whole = t0 + S <= L;
-      if (vec && whole) {  // 16-byte accesses (rows of a multiple of 16 bytes)
+      if (cvec) {  // 16-byte accesses (rows of a multiple of 16 bytes)
         float v[S];
-        vecio<IO, S>::load(x + base + t0, v);
+        cx.get(v);
 #pragma unroll
         for (int i = 0; i < S; ++i) xs[H + i] = v[i];
-        vecio<IO, S>::load(dout + base + t0, v);
+        cg.get(v);
 #pragma unroll
         for (int i = 0; i < S; ++i) gs[i] = v[i];
       } else {
@@ -103,7 +158,7 @@ __global__ void __launch_bounds__(kConvBwdThreads, 4) conv1d_bwd_kernel(const Co
 #pragma unroll
         for (int k = 0; k < K; ++k) dw[k] = fmaf(gs[i], xs[i + k], dw[k]);
       }
-      if (vec && whole) {
+      if (cvec) {
         vecio<IO, S>::store(dx + base + t0, dxv);
       } else {
 #pragma unroll
