@@ -350,6 +350,51 @@ def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, init_
     return y, hN.reshape(batch, H, P, N)
 
 
+def ssd_bwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, init_state=None,
+            dy=None, d_final_state=None, euler=False, nthreads=0):
+    """Backward of ``ssd``: the derivatives of Σ y·dy + Σ final_state·d_final_state.
+    As ``ssd`` is the selective scan of every channel (b, h, p) with the head's
+    scalar A, step and D and the group's B, C tied across channels, its derivatives
+    are the scan backward's per-channel terms summed over the channels that share
+    each parameter: the head's P channels for d dt, dA, dD, d dt_bias; the group's
+    heads and channels for dB, dC (the scan backward sums a batch row's units).
+
+    Inputs as ``ssd``; dy (batch, L, H, P), d_final_state (batch, H, P, N) or None.
+    Returns float64 dx, dz (batch, L, H, P; dz None without z), ddt (batch, L, H),
+    dA, dD, ddt_bias (H,), dB, dC (batch, L, G, N), dinit (batch, H, P, N)."""
+    x = np.asarray(x)
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    assert H % G == 0 and dt.shape == (batch, L, H) and C.shape == B.shape
+    hpg = H // G
+    U = batch * H * P
+    rows = lambda a: np.ascontiguousarray(np.transpose(np.asarray(a), (0, 2, 3, 1)).reshape(U, L))
+    u = rows(x)
+    dl = np.ascontiguousarray(np.repeat(np.transpose(np.asarray(dt), (0, 2, 1)), P, axis=1)
+                              .reshape(U, L))
+    zz = None if z is None else rows(z)
+    bb, hh, pp = np.meshgrid(np.arange(batch), np.arange(H), np.arange(P), indexing="ij")
+    unit_b = (bb * G + hh // hpg).ravel()
+    unit_d = (hh * P + pp).ravel()
+    A_tab = np.repeat(np.asarray(A, np.float32), P)[:, None].repeat(N, axis=1)
+    Bt = np.ascontiguousarray(np.transpose(np.asarray(B, np.float32), (0, 2, 3, 1)).reshape(batch * G, N, L))
+    Ct = np.ascontiguousarray(np.transpose(np.asarray(C, np.float32), (0, 2, 3, 1)).reshape(batch * G, N, L))
+    D_tab = None if D is None else np.repeat(np.asarray(D, np.float32), P)
+    bias_tab = None if dt_bias is None else np.repeat(np.asarray(dt_bias, np.float32), P)
+    h0 = None if init_state is None else np.asarray(init_state, np.float64).reshape(U, N)
+    dfin = None if d_final_state is None else np.asarray(d_final_state, np.float64).reshape(U, N)
+    r = scan_bwd_rows(u, dl, zz, unit_b, unit_d, A_tab, Bt, Ct, D_tab, bias_tab, delta_softplus,
+                      rows(np.asarray(dy, np.float64)), h0, dfin, batch * G, nthreads, euler)
+    back = lambda a: np.transpose(a.reshape(batch, H, P, L), (0, 3, 1, 2))
+    per_head = lambda a: a.reshape(batch, H, P, -1).sum(axis=(0, 2, 3))
+    bc = lambda a: np.transpose(a.reshape(batch, G, N, L), (0, 3, 1, 2))
+    return dict(dx=back(r["du"]), dz=None if z is None else back(r["dz"]),
+                ddt=np.transpose(r["ddelta"].reshape(batch, H, P, L).sum(axis=2), (0, 2, 1)),
+                dA=per_head(r["dA_unit"]), dD=per_head(r["dD_unit"]),
+                ddt_bias=per_head(r["dbias_unit"]), dB=bc(r["dB"]), dC=bc(r["dC"]),
+                dinit=r["dinit"].reshape(batch, H, P, N))
+
+
 def rel_err(got, ref):
     """max |got - ref| / max |ref|: the parity metric for y and final_state."""
     got = np.asarray(got, dtype=np.float64)

@@ -169,3 +169,36 @@ def test_conv_backward_pins_catch_planted_mistake(mutant, monkeypatch):
         except AssertionError:
             caught.append(name)
     assert caught, "no pin caught " + mutant
+
+
+# mistakes in the SSD backward's summing of the tied parameters (oracle.ssd_bwd)
+SSD_BWD_MUTANTS = {
+    "ssdbwd_ddt_one_channel": ("r[\"ddelta\"].reshape(batch, H, P, L).sum(axis=2)",
+                               "r[\"ddelta\"].reshape(batch, H, P, L)[:, :, 0]"),
+    "ssdbwd_head_sum_skips_batch": ("a.reshape(batch, H, P, -1).sum(axis=(0, 2, 3))",
+                                    "a.reshape(batch, H, P, -1)[0].sum(axis=(1, 2))"),
+    "ssdbwd_groups_swapped": ("unit_b = (bb * G + hh // hpg).ravel()",
+                              "unit_b = (bb * G + (G - 1 - hh // hpg)).ravel()"),
+    "ssdbwd_dx_time_reversed": ("back = lambda a: np.transpose(a.reshape(batch, H, P, L), (0, 3, 1, 2))",
+                                "back = lambda a: np.transpose(a.reshape(batch, H, P, L)[..., ::-1], (0, 3, 1, 2))"),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(SSD_BWD_MUTANTS))
+def test_ssd_backward_pins_catch_planted_mistake(mutant, monkeypatch):
+    import test_oracle_ssd_pins as ssd_pins
+    old, new = SSD_BWD_MUTANTS[mutant]
+    src = inspect.getsource(oracle.ssd_bwd)
+    assert src.count(old) == 1, "mutation site not found: " + old
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "ssd_bwd_mutant", "exec"), ns)
+    monkeypatch.setattr(oracle, "ssd_bwd", ns["ssd_bwd"])
+    caught = []
+    for name, call in _pin_calls(ssd_pins):
+        if not name.startswith("test_backward"):
+            continue
+        try:
+            call()
+        except AssertionError:
+            caught.append(name)
+    assert caught, "no pin caught " + mutant

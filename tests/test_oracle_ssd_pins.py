@@ -99,3 +99,43 @@ def test_chunked_decomposition(Q):
                 Hs = np.exp(sl[-1]) * Hs + (w[:, None] * X[c0:c1]).T @ Bm[c0:c1]
             assert np.max(np.abs(y[b, :, h, :] - out)) < 1e-11 * max(1.0, np.max(np.abs(out)))
             assert np.max(np.abs(hN[b, h] - Hs)) < 1e-11 * max(1.0, np.max(np.abs(Hs)))
+
+
+# ---------------------------------------------------------------------------
+# the backward (oracle.ssd_bwd: the scan backward's per-channel terms summed over
+# the tied parameters) against central finite differences of the forward oracle
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("euler", [False, True])
+def test_backward_matches_finite_differences(euler):
+    p = _problem(3, batch=2, L=11, H=4, P=2, G=2, N=3)
+    rng = np.random.default_rng(4)
+    dy = rng.standard_normal(p["x"].shape)
+    dfin = rng.standard_normal(p["h0"].shape)
+    g = oracle.ssd_bwd(p["x"], p["dt"], p["A"], p["B"], p["C"], p["D"], p["z"], p["bias"], True,
+                       p["h0"], dy=dy, d_final_state=dfin, euler=euler)
+    h = 2.0 ** -9
+
+    def loss(q):
+        y, hN = oracle.ssd(q["x"], q["dt"], q["A"], q["B"], q["C"], q["D"], q["z"], q["bias"], True,
+                           q["h0"], euler=euler)
+        return float(np.sum(y * dy) + np.sum(hN * dfin))
+
+    def fd(name, idx):
+        up, dn = dict(p), dict(p)
+        up[name] = p[name].copy()
+        dn[name] = p[name].copy()
+        up[name][idx] += h
+        dn[name][idx] -= h
+        return (loss(up) - loss(dn)) / (2 * h)
+
+    # two batch rows: the head parameters' derivatives sum over both
+    checks = [("x", "dx", (0, 5, 1, 1)), ("x", "dx", (1, 0, 3, 0)), ("z", "dz", (1, 7, 2, 1)),
+              ("dt", "ddt", (0, 3, 0)), ("dt", "ddt", (1, 10, 3)), ("A", "dA", (1,)),
+              ("A", "dA", (2,)), ("B", "dB", (0, 4, 1, 2)), ("B", "dB", (1, 9, 0, 0)),
+              ("C", "dC", (1, 6, 0, 1)), ("D", "dD", (3,)), ("bias", "ddt_bias", (0,)),
+              ("h0", "dinit", (1, 2, 1, 2))]
+    for name, gname, idx in checks:
+        ref = fd(name, idx)
+        got = g[gname][idx]
+        assert abs(got - ref) < 1e-4 * max(1.0, abs(ref)), (name, idx, got, ref)
