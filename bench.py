@@ -446,7 +446,32 @@ def bench_ssd(steps, warmup, world, seed=5):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(world, e0.elapsed_time(e1)) / steps
-    return dict(step_ms=ms, steps=steps, workspace_bytes=nbytes)
+    # the backward on the same layer (ssm_ssd_bwd: the scan backward per group), a few steps
+    dy = torch.randn((b, L, H, P), generator=gen, device="cuda").to(bf)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    dx, dz, ddt = torch.empty_like(x), torch.empty_like(z), torch.empty_like(dt)
+    dA, dD, dbias = torch.empty(H, **f32), torch.empty(H, **f32), torch.empty(H, **f32)
+    dB, dC = torch.empty(B.shape, **f32), torch.empty(C.shape, **f32)
+    bwb = ssm.ssm_ssd_bwd_workspace_bytes(b, L, H, P, G, N)
+    bws = torch.empty(bwb, dtype=torch.uint8, device="cuda")
+
+    def bstep():
+        ssm.ssm_ssd_bwd(x, dt, bias, A, B, C, D, z, ssm.SSM_SOFTPLUS, None, dy, None, dx, ddt, dA,
+                        dB, dC, dD, dz, dbias, None, bws, bwb, stream)
+
+    bsteps = 3
+    bstep()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    for _ in range(bsteps):
+        bstep()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    bms = max_over_ranks(world, e0.elapsed_time(e1)) / bsteps
+    del bws
+    return dict(step_ms=ms, steps=steps, workspace_bytes=nbytes, bwd_ms=bms, bwd_steps=bsteps,
+                bwd_workspace_bytes=bwb)
 
 
 # ---------------------------------------------------------------------------
@@ -776,7 +801,12 @@ def main():
                        "tensor_tflops": fl / ss / 1e12, "flops_per_step": fl,
                        "hbm_gbs_algorithmic": nb / ss / 1e9, "bytes_per_step": nb,
                        "workspace_bytes": ssd["workspace_bytes"], "gpu_launches": 4 * ssd["steps"],
-                       "l2": "x, z, y: 3 x 50 MB plus the 100 MB of bf16 chunk-entering states written and read per step, larger than L2"}
+                       "l2": "x, z, y: 3 x 50 MB plus the 100 MB of bf16 chunk-entering states written and read per step, larger than L2",
+                       "backward": {"us_per_step": ssd["bwd_ms"] * 1e3, "steps": ssd["bwd_steps"],
+                                    "workspace_bytes": ssd["bwd_workspace_bytes"],
+                                    "call": "ssm_ssd_bwd: per group, the selective-scan backward "
+                                            "(fp32 I/O) on the group's channels and fixed-order "
+                                            "sums over the tied head parameters"}}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line))

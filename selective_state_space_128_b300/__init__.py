@@ -77,6 +77,10 @@ def load():
     lib.ssm_conv1d_fwd.restype = i32
     lib.ssm_conv1d_update.argtypes = [vp, vp, vp, vp, i32, vp, i64, i64, i64, i32, vp]
     lib.ssm_conv1d_update.restype = i32
+    lib.ssm_ssd_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
+    lib.ssm_ssd_bwd_workspace_bytes.restype = sz
+    lib.ssm_ssd_bwd.argtypes = [vp] * 8 + [i32] + [vp] * 12 + [i64] * 6 + [vp, sz, vp]
+    lib.ssm_ssd_bwd.restype = i32
     lib.ssm_conv1d_bwd.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32,
                                    vp]
     lib.ssm_conv1d_bwd.restype = i32
@@ -360,6 +364,25 @@ def ssm_ssd_fwd(x, dt, dt_bias, A, B, C, D, z, flags, y, final_state, init_state
     _call("ssm_ssd_fwd", rc)
 
 
+def ssm_ssd_bwd_workspace_bytes(batch, seqlen, nheads, headdim, ngroups, dstate) -> int:
+    return int(load().ssm_ssd_bwd_workspace_bytes(batch, seqlen, nheads, headdim, ngroups, dstate))
+
+
+def ssm_ssd_bwd(x, dt, dt_bias, A, B, C, D, z, flags, init_state, dy, d_final_state, dx, ddt, dA,
+                dB, dC, dD, dz, d_dt_bias, d_init_state, workspace, workspace_bytes, stream=None):
+    """Tensor form of ``ssm_ssd_bwd``; sizes from x (batch, L, H, P) and B (batch, L, G, N)."""
+    _check_dev(x, dt, dt_bias, A, B, C, D, z, init_state, dy, d_final_state, dx, ddt, dA, dB, dC,
+               dD, dz, d_dt_bias, d_init_state, workspace)
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    rc = load().ssm_ssd_bwd(_ptr(x), _ptr(dt), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                            _ptr(z), int(flags), _ptr(init_state), _ptr(dy), _ptr(d_final_state),
+                            _ptr(dx), _ptr(ddt), _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dD), _ptr(dz),
+                            _ptr(d_dt_bias), _ptr(d_init_state), batch, L, H, P, G, N,
+                            _ptr(workspace), int(workspace_bytes or 0), _stream(stream))
+    _call("ssm_ssd_bwd", rc)
+
+
 def static_scratch_bytes() -> int:
     """SSM_STATIC_SCRATCH_BYTES as defined in include/ssm.h."""
     import re
@@ -472,6 +495,27 @@ def conv1d(x, weight, bias=None, conv_state=None, silu=True, want_state=False, s
     ssm_conv1d_fwd(x, weight, bias, conv_state, int(bool(silu)) | (SSM_LAYOUT_BLD if bld else 0),
                    out, st, stream)
     return (out, st) if want_state else out
+
+
+def ssd_bwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, init_state=None,
+            dy=None, d_final_state=None, euler=False, stream=None):
+    """Derivatives of ``ssd``'s outputs against dy (and d_final_state): dict(dx, dz, ddt
+    (bf16, like x, z, dt), dA, dD, ddt_bias (H,), dB, dC (like B, float32), dinit
+    (batch, H, P, N) float32)."""
+    import torch
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = dict(dx=torch.empty_like(x), ddt=torch.empty_like(dt), dz=None if z is None else torch.empty_like(z),
+               dA=torch.empty(H, **f32), dD=torch.empty(H, **f32), ddt_bias=torch.empty(H, **f32),
+               dB=torch.empty(B.shape, **f32), dC=torch.empty(C.shape, **f32),
+               dinit=torch.empty((batch, H, P, N), **f32))
+    nbytes = ssm_ssd_bwd_workspace_bytes(batch, L, H, P, G, N)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    ssm_ssd_bwd(x, dt, dt_bias, A, B, C, D, z, _flags(delta_softplus, euler), init_state, dy,
+                d_final_state, out["dx"], out["ddt"], out["dA"], out["dB"], out["dC"], out["dD"],
+                out["dz"], out["ddt_bias"], out["dinit"], ws, nbytes, stream)
+    return out
 
 
 def conv1d_bwd(x, weight, dout, bias=None, conv_state=None, silu=True, bld=False, stream=None):

@@ -300,3 +300,29 @@ def test_conv1d_bwd_argument_errors():
     assert call(dx=FAKE + 0x3000008) == ssm.SSM_ERR_ALIGN
     assert call(dx=FAKE + 0x10) == ssm.SSM_ERR_ARG          # dx overlapping x
     assert call(db=FAKE + 0x4000010) == ssm.SSM_ERR_ARG     # dbias overlapping dweight
+
+
+def test_ssd_bwd_argument_errors():
+    def call(**kw):
+        a = dict(x=FAKE, dt=FAKE + 0x1000000, bias=None, A=FAKE + 0x2000000, B=FAKE + 0x3000000,
+                 C=FAKE + 0x4000000, D=None, z=None, flags=1, init=None, dy=FAKE + 0x5000000,
+                 dfin=None, dx=FAKE + 0x6000000, ddt=FAKE + 0x7000000, dA=FAKE + 0x8000000,
+                 dB=FAKE + 0x9000000, dC=FAKE + 0xA000000, dD=None, dz=None, dbias=None, dinit=None,
+                 batch=1, L=64, H=4, P=64, G=1, N=64, ws=FAKE + 0x10000000, wsb=1 << 34)
+        a.update(kw)
+        return lib().ssm_ssd_bwd(a["x"], a["dt"], a["bias"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                 a["flags"], a["init"], a["dy"], a["dfin"], a["dx"], a["ddt"], a["dA"],
+                                 a["dB"], a["dC"], a["dD"], a["dz"], a["dbias"], a["dinit"], a["batch"],
+                                 a["L"], a["H"], a["P"], a["G"], a["N"], a["ws"], a["wsb"], None)
+    assert call(P=32) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(N=16) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(G=3) == ssm.SSM_ERR_UNSUPPORTED
+    assert call(flags=ssm.SSM_LAYOUT_BLD) == ssm.SSM_ERR_ARG
+    assert call(dz=FAKE + 0xB000000) == ssm.SSM_ERR_ARG      # dz without z
+    assert call(dy=None) == ssm.SSM_ERR_ARG
+    assert call(dA=None) == ssm.SSM_ERR_ARG
+    assert call(dx=FAKE + 0x6000008) == ssm.SSM_ERR_ALIGN
+    assert call(ws=None) == ssm.SSM_ERR_WORKSPACE
+    assert call(wsb=1024) == ssm.SSM_ERR_WORKSPACE
+    assert ssm.ssm_ssd_bwd_workspace_bytes(1, 64, 4, 64, 1, 64) > 0
+    assert ssm.ssm_ssd_bwd_workspace_bytes(1, 64, 4, 64, 3, 64) == 0

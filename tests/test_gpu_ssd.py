@@ -86,3 +86,40 @@ def test_ssd_bench_shape_sampled():
                                   x["D"][hd:hd + 1], sl(x["z"]), x["bias"][hd:hd + 1], True)
         assert oracle.rel_err(yh[b:b + 1, :, hd:hd + 1], y_ref) <= TOL
         assert oracle.rel_err(hh[b:b + 1, hd:hd + 1], h_ref) <= TOL
+
+
+# ---------------------------------------------------------------------------
+# the backward (ssm_ssd_bwd) against oracle.ssd_bwd
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", ["n64_g2", "n128_g1", "euler", "no_gate_no_D", "single_step",
+                                  "three_heads_per_group"])
+def test_ssd_backward_matches_oracle(case):
+    cfg = dict(batch=2, L=90, H=4, G=2, N=64)
+    cfg.update(dict(n128_g1=dict(N=128, G=1, L=70), single_step=dict(L=1),
+                    three_heads_per_group=dict(H=6, G=2, L=50)).get(case, {}))
+    x = _inputs(seed=400 + len(case), **cfg)
+    use_z = use_D = case != "no_gate_no_D"
+    euler = case == "euler"
+    rng = np.random.default_rng(7)
+    dy = synth.f32_to_bf16(rng.standard_normal(x["x"].shape).astype(np.float32))
+    dfin = rng.standard_normal(x["h0"].shape).astype(np.float32)
+    ref = oracle.ssd_bwd(x["x"], x["dt"], x["A"], _f32(x["B"]), _f32(x["C"]),
+                         x["D"] if use_D else None, x["z"] if use_z else None, x["bias"], True,
+                         x["h0"].astype(np.float64), dy=_f32(dy).astype(np.float64),
+                         d_final_state=dfin.astype(np.float64), euler=euler)
+    out = ssm.ssd_bwd(dev_io(x["x"]), dev_io(x["dt"]), dev_f32(x["A"]), dev_io(x["B"]), dev_io(x["C"]),
+                      dev_f32(x["D"]) if use_D else None, dev_io(x["z"]) if use_z else None,
+                      dev_f32(x["bias"]), True, dev_f32(x["h0"]), dy=dev_io(dy),
+                      d_final_state=dev_f32(dfin), euler=euler)
+    torch.cuda.synchronize()
+    pairs = [("dx", "dx", 1e-2), ("ddt", "ddt", 1e-2), ("dA", "dA", 1e-4), ("dB", "dB", 1e-4),
+             ("dC", "dC", 1e-4), ("ddt_bias", "ddt_bias", 1e-4), ("dinit", "dinit", 1e-4)]
+    if use_z:
+        pairs.append(("dz", "dz", 1e-2))
+    if use_D:
+        pairs.append(("dD", "dD", 1e-4))
+    for k, rk, tol in pairs:
+        got = host64(out[k])
+        assert np.isfinite(got).all(), k
+        assert oracle.rel_err(got, ref[rk]) <= tol, (k, oracle.rel_err(got, ref[rk]))
