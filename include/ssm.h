@@ -21,9 +21,10 @@
  * The expanded (batch, d_inner, L, N) state is never written to memory; only
  * y and the final state are.
  *
- * Memory: every pointer is a DEVICE pointer on the current CUDA device, owned
- * by the caller; the library allocates nothing and keeps no pointer after a
- * call returns.  Layouts are dense and row-major (last index fastest):
+ * Memory: every pointer is a DEVICE pointer on the current CUDA device (the
+ * one exception: ssm_scan_fwd_host takes host buffers and a device
+ * workspace), owned by the caller; the library allocates no memory and keeps
+ * no pointer after a call returns.  Layouts are dense and row-major (last index fastest):
  *   u, delta, z, y      (batch, dim, seqlen)  in io_dtype (float32 or bfloat16)
  *   B, C                (batch, dstate, seqlen) float32
  *   A                   (dim, dstate) float32
