@@ -93,7 +93,7 @@ def test_ssd_bench_shape_sampled():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("case", ["n64_g2", "n128_g1", "euler", "no_gate_no_D", "single_step",
-                                  "three_heads_per_group"])
+                                  "three_heads_per_group", "no_init_no_dfinal"])
 def test_ssd_backward_matches_oracle(case):
     cfg = dict(batch=2, L=90, H=4, G=2, N=64)
     cfg.update(dict(n128_g1=dict(N=128, G=1, L=70), single_step=dict(L=1),
@@ -104,14 +104,16 @@ def test_ssd_backward_matches_oracle(case):
     rng = np.random.default_rng(7)
     dy = synth.f32_to_bf16(rng.standard_normal(x["x"].shape).astype(np.float32))
     dfin = rng.standard_normal(x["h0"].shape).astype(np.float32)
+    states = case != "no_init_no_dfinal"
     ref = oracle.ssd_bwd(x["x"], x["dt"], x["A"], _f32(x["B"]), _f32(x["C"]),
                          x["D"] if use_D else None, x["z"] if use_z else None, x["bias"], True,
-                         x["h0"].astype(np.float64), dy=_f32(dy).astype(np.float64),
-                         d_final_state=dfin.astype(np.float64), euler=euler)
+                         x["h0"].astype(np.float64) if states else None,
+                         dy=_f32(dy).astype(np.float64),
+                         d_final_state=dfin.astype(np.float64) if states else None, euler=euler)
     out = ssm.ssd_bwd(dev_io(x["x"]), dev_io(x["dt"]), dev_f32(x["A"]), dev_io(x["B"]), dev_io(x["C"]),
                       dev_f32(x["D"]) if use_D else None, dev_io(x["z"]) if use_z else None,
-                      dev_f32(x["bias"]), True, dev_f32(x["h0"]), dy=dev_io(dy),
-                      d_final_state=dev_f32(dfin), euler=euler)
+                      dev_f32(x["bias"]), True, dev_f32(x["h0"]) if states else None, dy=dev_io(dy),
+                      d_final_state=dev_f32(dfin) if states else None, euler=euler)
     torch.cuda.synchronize()
     pairs = [("dx", "dx", 1e-2), ("ddt", "ddt", 1e-2), ("dA", "dA", 1e-4), ("dB", "dB", 1e-4),
              ("dC", "dC", 1e-4), ("ddt_bias", "ddt_bias", 1e-4), ("dinit", "dinit", 1e-4)]
@@ -123,3 +125,19 @@ def test_ssd_backward_matches_oracle(case):
         got = host64(out[k])
         assert np.isfinite(got).all(), k
         assert oracle.rel_err(got, ref[rk]) <= tol, (k, oracle.rel_err(got, ref[rk]))
+
+
+def test_ssd_backward_empty_sequence():
+    """L = 0: no step, so the head parameters' derivatives are zero and d init_state is
+    d final_state."""
+    x = _inputs(batch=2, L=1, H=4, G=2, N=64, seed=450)
+    e = lambda a: a[:, :0]
+    dfin = np.random.default_rng(8).standard_normal(x["h0"].shape).astype(np.float32)
+    out = ssm.ssd_bwd(dev_io(e(x["x"])), dev_io(e(x["dt"])), dev_f32(x["A"]), dev_io(e(x["B"])),
+                      dev_io(e(x["C"])), dev_f32(x["D"]), dev_io(e(x["z"])), dev_f32(x["bias"]), True,
+                      dev_f32(x["h0"]), dy=dev_io(e(x["x"])), d_final_state=dev_f32(dfin))
+    torch.cuda.synchronize()
+    assert out["dx"].shape == (2, 0, 4, 64)
+    for k in ("dA", "dD", "ddt_bias"):
+        assert out[k].abs().max().item() == 0.0, k
+    assert np.array_equal(host64(out["dinit"]), dfin.astype(np.float64))
