@@ -2,15 +2,22 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-decode]
 
-A step is one ssm_scan_fwd over the Mamba-130M-shaped layer workload (batch 8,
-d_inner 1536, L 2048, N 16, bf16 u/Δ/z/y, fp32 A/B/C/D/bias, seed 1) with inputs
-resident in HBM.  Two copies of the inputs alternate between steps, so a step
-never reads data the previous step left in L2 (each copy, 204 MB, is larger
-than the 126 MB L2).  The same line reports the one-token decode step
-(batch 256, d_inner 5120, N 16; four such groups advanced round-robin so that the
-336 MB of state exceeds L2), an end-to-end figure through the C ABI with host
-buffers, the oracle's CPU throughput, the roofline of the scan kernel and the SM
-clocks sampled during the timed region.
+A step is one ssm_scan_fwd_ex over the Mamba-2.8B-shaped layer workload (batch 4,
+d_inner 5120, L 4096, N 16, bf16 u/Δ/z/y, fp32 A/B/C/D/bias, seed 2), the largest
+single-launch workload, with inputs resident in HBM.  Two copies of the inputs
+alternate between steps, so a step never reads data the previous step left in L2
+(each copy, 675 MB, is larger than the 126 MB L2).  The same line reports:
+
+* the million-length sequence (batch 1, d_inner 1536, L 2^20, N 16) as 16 launches
+  of 65 536 steps with the fp32 state carried from launch to launch, the whole
+  loop timed;
+* the Mamba-130M-shaped layer (batch 8, d_inner 1536, L 2048, N 16);
+* the one-token decode step (batch 256, d_inner 5120, N 16; four such groups
+  advanced round-robin so that the 336 MB of state exceeds L2);
+* the backward, the conv1d front end and Mamba-2 SSD;
+* end-to-end figures through the C ABI with host buffers, the oracle's CPU
+  throughput, the roofline of the scan kernel and the SM clocks sampled during
+  the timed region.
 
 Under torchrun (N > 1) every rank runs its own copy of the workload (the scan
 shards by batch and channel with no exchange: weak scaling); rank 0 prints.
@@ -36,6 +43,7 @@ import synth  # noqa: E402
 
 METRIC = "scan HBM GB/s (% of B300 peak) & channel-steps/s; decode tokens/s"
 L2_BYTES = 126 * 1024 * 1024
+WS_HEADER = 256   # bytes of a scan workspace before its carry records (the status word)
 
 
 def scan_bytes(w) -> int:
@@ -216,7 +224,9 @@ def to_dev(t_host, io_bf16=False):
     return d.view(torch.bfloat16) if io_bf16 else d
 
 
-def bench_scan(w, steps, warmup, world):
+def bench_scan(w, steps, warmup, world, e2e=True, clocks=True):
+    """Per-launch time of ssm_scan_fwd_ex on workload `w` (two input copies alternated),
+    and, with `e2e`, of ssm_scan_fwd_host on page-locked host copies of the same inputs."""
     import torch
     import selective_state_space_128_b300 as ssm
     x = synth.make_scan_inputs(w)
@@ -227,25 +237,30 @@ def bench_scan(w, steps, warmup, world):
         g = {k: to_dev(host[k], bf and k in ("u", "delta", "z")) for k in host}
         g["y"] = torch.empty_like(g["u"])
         g["h"] = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device="cuda")
+        nb = ssm.ssm_scan_workspace_bytes(w.batch, w.dim, w.seqlen, w.dstate,
+                                          ssm.SSM_BF16 if bf else ssm.SSM_F32)
+        g["ws"] = torch.empty(nb, dtype=torch.uint8, device="cuda") if nb else None
         sets.append(g)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
     def step(g):
         ssm.ssm_scan_fwd_ex(g["u"], g["delta"], g["delta_bias"], g["A"], g["B"], g["C"], g["D"],
-                            g["z"], True, g["y"], g["h"], stream=stream)
+                            g["z"], True, g["y"], g["h"], None, g["ws"], stream=stream)
 
     for i in range(warmup):
         step(sets[i % 2])
     torch.cuda.synchronize()
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
-        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-    except Exception:
-        pass
-    clocks = ClockSampler(uuid)
-    clocks.start()
+    sampler = None
+    if clocks:
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        sampler = ClockSampler(uuid)
+        sampler.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -257,14 +272,20 @@ def bench_scan(w, steps, warmup, world):
     torch.cuda.synchronize()
     t1 = time.time()
     barrier(world)
-    ck = clocks.stop(t0, t1)
+    ck = sampler.stop(t0, t1) if sampler else None
     ms = e0.elapsed_time(e1)
     ms = max_over_ranks(world, ms)
+    # a workspace larger than the status header means the plan splits the sequence
+    # (two kernels per call)
+    split = sets[0]["ws"] is not None and sets[0]["ws"].numel() > WS_HEADER
+    out = dict(ms=ms, clocks=ck, inputs=sets[0], launches_per_step=2 if split else 1)
+    if not e2e:
+        return out
 
     # end to end through the C ABI with host buffers: ssm_scan_fwd_host copies the
     # step's inputs from page-locked host memory, scans and copies y and the final
     # state back, pipelined over units inside the call, every step
-    e2e_steps = max(3, min(steps, 20))
+    e2e_steps = max(3, min(steps, 10))
     hin = {k: (host[k].view(torch.bfloat16) if (bf and k in ("u", "delta", "z")) else host[k])
            for k in host}
     yh = torch.empty(sets[0]["y"].shape, dtype=sets[0]["y"].dtype).pin_memory()
@@ -291,8 +312,126 @@ def bench_scan(w, steps, warmup, world):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(world, f0.elapsed_time(f1))
-    return dict(ms=ms, clocks=ck, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
-                inputs=sets[0])
+    out.update(e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the million-length sequence: 16 launches with the fp32 state carried
+# ---------------------------------------------------------------------------
+
+def bench_million(w, reps, world, cpu=True):
+    """The million-length workload as w.launches launches of L / launches steps, each
+    starting from the previous launch's fp32 final state; the whole loop is timed.
+
+    Inputs are drawn on the device (seeded torch generator, the workload's
+    distributions: u, z ~ N(0, 1), Δ_raw ~ N(0, 0.5^2), B, C ~ N(0, 1); A, D and the
+    bias from the workload's generator): 16 chunks of u/Δ/z (3 x 201 MB each) and y,
+    13 GB in all, far larger than L2.  End to end: the same loop through
+    ssm_scan_fwd_host from page-locked host copies of every chunk.  CPU: the oracle on
+    a sample of channels of the same inputs, over the whole length."""
+    import torch
+    import selective_state_space_128_b300 as ssm
+    K = w.launches
+    Lc = w.seqlen // K
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1000 + w.seed)
+    bf = torch.bfloat16
+    shape = (w.batch, w.dim, Lc)
+    chunks = []
+    for _ in range(K):
+        c = dict(u=torch.randn(shape, generator=gen, device="cuda").to(bf),
+                 delta=(w.sigma_delta * torch.randn(shape, generator=gen, device="cuda")).to(bf),
+                 z=torch.randn(shape, generator=gen, device="cuda").to(bf),
+                 B=torch.randn((w.batch, w.dstate, Lc), generator=gen, device="cuda"),
+                 C=torch.randn((w.batch, w.dstate, Lc), generator=gen, device="cuda"))
+        c["y"] = torch.empty_like(c["u"])
+        chunks.append(c)
+    A = torch.from_numpy(synth.gen_A(w.dim, w.dstate)).cuda()
+    D = torch.from_numpy(synth.gen_D(w)).cuda()
+    bias = torch.from_numpy(synth.gen_delta_bias(w.seed, w.dim)).cuda()
+    hs = [torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device="cuda")
+          for _ in range(2)]
+    nb = ssm.ssm_scan_workspace_bytes(w.batch, w.dim, Lc, w.dstate, ssm.SSM_BF16)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def loop():
+        for k, c in enumerate(chunks):
+            ssm.ssm_scan_fwd_ex(c["u"], c["delta"], bias, A, c["B"], c["C"], D, c["z"], True,
+                                c["y"], hs[k % 2], None if k == 0 else hs[(k - 1) % 2], ws, nb,
+                                stream=stream)
+
+    loop()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        loop()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    loop_ms = max_over_ranks(world, e0.elapsed_time(e1)) / reps
+    plan_split = nb > WS_HEADER
+    out = dict(loop_ms=loop_ms, reps=reps, launches=K, chunk_len=Lc,
+               kernels_per_launch=2 if plan_split else 1, workspace_bytes=nb)
+
+    # end to end: page-locked host copies of every chunk, the same loop through
+    # ssm_scan_fwd_host (copies in and out inside each call)
+    hc = []
+    for c in chunks:
+        hc.append({k: c[k].cpu().pin_memory() for k in ("u", "delta", "z", "B", "C")})
+    yh = torch.empty(shape, dtype=bf).pin_memory()
+    hh = [torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32).pin_memory()
+          for _ in range(2)]
+    hA, hD, hb = A.cpu().pin_memory(), D.cpu().pin_memory(), bias.cpu().pin_memory()
+    flags = ssm.SSM_SOFTPLUS
+    hws_bytes = ssm.ssm_scan_fwd_host_workspace_bytes(w.batch, w.dim, Lc, w.dstate, ssm.SSM_BF16,
+                                                      flags)
+    hws = torch.empty(hws_bytes, dtype=torch.uint8, device="cuda")
+
+    def e2e_loop():
+        for k, c in enumerate(hc):
+            ssm.ssm_scan_fwd_host(c["u"], c["delta"], hb, hA, c["B"], c["C"], hD, c["z"], flags,
+                                  yh, hh[k % 2], None if k == 0 else hh[(k - 1) % 2], hws,
+                                  hws_bytes, stream=stream)
+
+    e2e_loop()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    e2e_loop()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    out["e2e_ms"] = max_over_ranks(world, e0.elapsed_time(e1))
+    out["h2d"] = sum(t.numel() * t.element_size() for c in hc for t in c.values())
+    out["d2h"] = K * (yh.numel() * yh.element_size() + hh[0].numel() * 4)
+    del hc
+
+    if cpu:
+        # the oracle over the whole length for a sample of channels of batch row 0
+        import oracle
+        nch = 32
+        rows = {k: torch.cat([c[k][0, :nch] for c in chunks], dim=1).view(torch.int16).cpu()
+                .numpy().view(np.uint16) for k in ("u", "delta", "z")}
+        Bh = torch.cat([c["B"] for c in chunks], dim=2).cpu().numpy()
+        Ch = torch.cat([c["C"] for c in chunks], dim=2).cpu().numpy()
+        t = time.perf_counter()
+        oracle.scan_rows(rows["u"], rows["delta"], rows["z"], np.zeros(nch, np.int64),
+                         np.arange(nch), A.cpu().numpy(), Bh, Ch, D.cpu().numpy(),
+                         bias.cpu().numpy(), True, None, y_stride=1021)
+        secs = time.perf_counter() - t
+        cs = nch * w.seqlen
+        cores = min(oracle.max_threads(), nch)
+        per_cs_bytes = scan_bytes(w) / w.channel_steps
+        out["cpu"] = {"value": per_cs_bytes * cs / secs / 1e9, "unit": "GB/s", "cores": cores,
+                      "kind": "oracle", "channel_steps_per_s": cs / secs,
+                      "sample": "batch 0, channels 0..%d over the whole 2^20 steps (%d "
+                                "channel-steps), %.1f s wall on %d threads; GB/s counts the "
+                                "workload's algorithmic bytes per channel-step" % (
+                                    nch - 1, cs, secs, cores)}
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -672,10 +811,27 @@ def workload_config(w):
                   % (scan_bytes(w) / 1e6)}
 
 
+def scan_roofline(w, ms_per_launch, hbm_peak, sm_max, peak_kind, traffic_key):
+    """Roofline of one scan launch on workload w: the method's FP32 operations against
+    the FP32 lanes (the bound) and its algorithmic bytes against the HBM copy peak."""
+    step_s = ms_per_launch / 1e3
+    nbytes = scan_bytes(w)
+    ops = fp32_ops_per_channel_step(w.dstate) * w.channel_steps
+    alu_peak = 148 * 128 * sm_max * 1e6 / 1e12          # FP32 lanes x max SM clock, TOP/s
+    alu_ach = ops / step_s / 1e12
+    gbs = nbytes / step_s / 1e9
+    return {"bound": "alu", "achieved": alu_ach, "peak": alu_peak, "unit": "TOP/s",
+            "frac": alu_ach / alu_peak, "traffic": profiled_traffic(traffic_key),
+            "kernel": "scan_kernel<bf16,16,0>", "ops_per_launch": ops,
+            "peak_basis": "148 SMs x 128 FP32 lanes x %.0f MHz (max SM clock)" % sm_max,
+            "hbm_achieved_gbs": gbs, "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peak_kind,
+            "hbm_frac": gbs / hbm_peak, "algorithmic_bytes_per_launch": nbytes}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=1000)
@@ -685,9 +841,13 @@ def main():
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--no-million", action="store_true")
+    ap.add_argument("--million-reps", type=int, default=3)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    w = synth.MAMBA_130M
+    w = synth.MAMBA_2P8B          # the headline: the largest single-launch workload
+    w1 = synth.MAMBA_130M
+    wm = synth.MILLION
     world, rank, local = dist_setup()
     if args.impl == "reference":
         if rank == 0:
@@ -700,11 +860,19 @@ def main():
     hbm_peak, sm_max, peak_kind = load_peaks()
 
     r = bench_scan(w, args.steps, args.warmup, world)
-    bwd = None if args.no_bwd else bench_backward(w, r["inputs"], args.bwd_steps, args.warmup,
-                                                  world)
-    bld_ms = bench_scan_bld(w, r["inputs"], 50, args.warmup, world)
     r.pop("inputs")
-    conv = None if args.no_conv else bench_conv(w, 50, args.warmup, world)
+    r1 = bench_scan(w1, max(20, min(args.steps, 200)), args.warmup, world, e2e=False,
+                    clocks=False)
+    bwd = None if args.no_bwd else bench_backward(w1, r1["inputs"], args.bwd_steps, args.warmup,
+                                                  world)
+    bld_ms = bench_scan_bld(w1, r1["inputs"], 50, args.warmup, world)
+    r1.pop("inputs")
+    torch.cuda.empty_cache()
+    mil = None if args.no_million else bench_million(wm, max(3, args.million_reps), world,
+                                                    cpu=(rank == 0 and world == 1
+                                                         and not args.no_cpu))
+    torch.cuda.empty_cache()
+    conv = None if args.no_conv else bench_conv(w1, 50, args.warmup, world)
     ssd = None if args.no_ssd else bench_ssd(20, args.warmup, world)
     dec = None if args.no_decode else bench_decode(synth.DECODE, args.decode_steps, world)
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
@@ -716,10 +884,6 @@ def main():
     gbs_rank = nbytes / step_s / 1e9
     value = job_throughput(nbytes / 1e9, step_s, world)   # GB/s over all ranks
     chsteps = job_throughput(w.channel_steps, step_s, world)
-    ops = fp32_ops_per_channel_step(w.dstate) * w.channel_steps
-    alu_peak = 148 * 128 * sm_max * 1e6 / 1e12          # FP32 lanes x max SM clock, TOP/s
-    alu_ach = ops / step_s / 1e12
-    traffic = profiled_traffic("scan_kernel")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True,
@@ -729,20 +893,58 @@ def main():
         "hbm": {"achieved_gbs": gbs_rank, "peak_gbs": hbm_peak, "frac": gbs_rank / hbm_peak,
                 "peak_kind": peak_kind, "frac_of_8000_nominal": gbs_rank / 8000.0,
                 "bytes_per_step": nbytes},
-        "roofline": {"bound": "alu", "achieved": alu_ach, "peak": alu_peak, "unit": "TOP/s",
-                     "frac": alu_ach / alu_peak, "traffic": traffic,
-                     "kernel": "scan_kernel<bf16,16,0>",
-                     "ops_per_launch": ops,
-                     "peak_basis": "148 SMs x 128 FP32 lanes x %.0f MHz (max SM clock)" % sm_max,
-                     "hbm_frac": gbs_rank / hbm_peak},
+        "roofline": scan_roofline(w, r["ms"] / args.steps, hbm_peak, sm_max, peak_kind,
+                                  "scan_kernel@" + w.name),
         "e2e": {"value": nbytes * r["e2e_steps"] / (r["e2e_ms"] / 1e3) / 1e9 * world,
                 "unit": "GB/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "steps": r["e2e_steps"],
                 "call": "ssm_scan_fwd_host: page-locked host buffers, copies pipelined over "
-                        "batch-row units inside the call"},
-        "gpu_launches": args.steps,
+                        "batch-row units inside the call",
+                "note": "bounded by the host link (about 55 GB/s each way, the two directions "
+                        "not overlapping on this box), so it cannot show kernel improvements "
+                        "at this size"},
+        "gpu_launches": args.steps * r["launches_per_step"],
         "clocks": r["clocks"],
     }
+    n1 = max(20, min(args.steps, 200))
+    s1 = r1["ms"] / 1e3 / n1
+    line["mamba130m_layer"] = {
+        "workload": w1.name, "config": workload_config(w1), "steps": n1,
+        "us_per_step": s1 * 1e6, "channel_steps_per_s": w1.channel_steps / s1 * world,
+        "hbm_gbs": scan_bytes(w1) / s1 / 1e9, "hbm_frac": scan_bytes(w1) / s1 / 1e9 / hbm_peak,
+        "roofline": scan_roofline(w1, s1 * 1e3, hbm_peak, sm_max, peak_kind,
+                                  "scan_kernel@" + w1.name),
+        "gpu_launches": n1 * r1["launches_per_step"]}
+    if mil is not None:
+        ls = mil["loop_ms"] / 1e3
+        mb = scan_bytes(wm) + (wm.launches - 1) * 4 * wm.batch * wm.dim * wm.dstate
+        mo = {"workload": wm.name, "config": dict(workload_config(wm), launches=mil["launches"],
+                                                   chunk_len=mil["chunk_len"],
+                                                   l2="13 GB of chunk inputs and outputs, far "
+                                                      "larger than L2"),
+              "reps": mil["reps"], "ms_per_loop": mil["loop_ms"],
+              "channel_steps_per_s": wm.channel_steps / ls * world,
+              "hbm_gbs": mb / ls / 1e9, "hbm_frac": mb / ls / 1e9 / hbm_peak,
+              "bytes_per_loop": mb,
+              "kernels_per_launch": mil["kernels_per_launch"],
+              "workspace_bytes": mil["workspace_bytes"],
+              "gpu_launches": mil["reps"] * mil["launches"] * mil["kernels_per_launch"],
+              "timing": "the whole 16-launch loop with the fp32 state carried, CUDA events, "
+                        "mean of %d loops after one untimed loop" % mil["reps"],
+              "e2e": {"value": mb / (mil["e2e_ms"] / 1e3) / 1e9 * world, "unit": "GB/s",
+                      "h2d_bytes_per_loop": mil["h2d"], "d2h_bytes_per_loop": mil["d2h"],
+                      "call": "ssm_scan_fwd_host per launch, state carried in host memory"}}
+        ops = fp32_ops_per_channel_step(wm.dstate) * wm.channel_steps
+        alu_peak = 148 * 128 * sm_max * 1e6 / 1e12
+        mo["roofline"] = {"bound": "alu", "achieved": ops / ls / 1e12, "peak": alu_peak,
+                          "unit": "TOP/s", "frac": ops / ls / 1e12 / alu_peak,
+                          "hbm_frac": mb / ls / 1e9 / hbm_peak,
+                          "note": "the split plan recomputes part of each segment in its "
+                                  "first pass; the ops counted are the method's 6N per "
+                                  "channel step"}
+        if "cpu" in mil:
+            mo["cpu_baseline"] = mil["cpu"]
+        line["million_length"] = mo
     if dec is not None:
         db = decode_bytes(synth.DECODE.batch, synth.DECODE.dim, synth.DECODE.dstate)
         st = dec["step_ms"] / 1e3
@@ -755,29 +957,32 @@ def main():
                                 "state, larger than L2" % (
                                     dec["groups"], dec["groups"] * 4.0 * synth.DECODE.batch *
                                     synth.DECODE.dim * synth.DECODE.dstate / 1e6),
-                          "us_per_step_state_in_l2": dec["l2_resident_ms"] * 1e3,
-                          "gpu_launches": 2 * dec["steps"]}
+                          "us_per_step_one_group_back_to_back": dec["l2_resident_ms"] * 1e3,
+                          "one_group_note": "one 84 MB state advanced back to back; the "
+                                            "state's loads and stores carry evict-first "
+                                            "hints, so it streams from HBM as well",
+                          "gpu_launches": dec["steps"]}
     if bwd is not None:
         bs = bwd["step_ms"] / 1e3
-        line["backward"] = {"workload": w.name, "steps": bwd["steps"],
+        line["backward"] = {"workload": w1.name, "steps": bwd["steps"],
                             "us_per_step": bwd["step_ms"] * 1e3,
-                            "channel_steps_per_s": w.channel_steps / bs * world,
-                            "time_vs_forward": bs / step_s,
+                            "channel_steps_per_s": w1.channel_steps / bs * world,
+                            "time_vs_forward": bs / s1,
                             "us_per_step_from_saved_states": bwd["saved_ms"] * 1e3,
                             "train_step_us": bwd["train_ms"] * 1e3,
                             "train_step": "ssm_scan_fwd_train + ssm_scan_bwd(SSM_SAVED_STATES)",
                             "workspace_bytes": bwd["workspace_bytes"],
                             "gpu_launches": 2 * bwd["steps"],
                             "l2": "u, delta, z, dy: 4 x %.0f MB, larger than L2"
-                                  % (w.channel_steps * 2 / 1e6)}
-    line["scan_bld_layout"] = {"us_per_step": bld_ms * 1e3,
-                               "channel_steps_per_s": w.channel_steps / (bld_ms / 1e3) * world,
+                                  % (w1.channel_steps * 2 / 1e6)}
+    line["scan_bld_layout"] = {"workload": w1.name, "us_per_step": bld_ms * 1e3,
+                               "channel_steps_per_s": w1.channel_steps / (bld_ms / 1e3) * world,
                                "layout": "u, delta, z, y as (batch, L, d_inner)", "steps": 50,
                                "gpu_launches": 50}
     if conv is not None:
         cs = conv["step_ms"] / 1e3
         line["conv1d"] = {"workload": "conv1d_silu d_conv 4 on %d x %d x %d bf16" % (
-                              w.batch, w.dim, w.seqlen),
+                              w1.batch, w1.dim, w1.seqlen),
                           "steps": conv["steps"], "us_per_step": conv["step_ms"] * 1e3,
                           "hbm_gbs": conv["bytes"] / cs / 1e9,
                           "hbm_frac": conv["bytes"] / cs / 1e9 / hbm_peak,
@@ -785,9 +990,11 @@ def main():
                           "l2": "3 input/output pairs rotated: 300 MB, larger than L2",
                           "backward": {"us_per_step": conv["bwd_ms"] * 1e3,
                                        "hbm_gbs": conv["bwd_bytes"] / (conv["bwd_ms"] / 1e3) / 1e9,
+                                       "hbm_frac": conv["bwd_bytes"] / (conv["bwd_ms"] / 1e3)
+                                                   / 1e9 / hbm_peak,
                                        "bytes_per_step": conv["bwd_bytes"],
                                        "gpu_launches": conv["steps"],
-                                       "call": "ssm_conv1d_bwd (dx, dweight, dbias; one kernel)"}}
+                                       "call": "ssm_conv1d_bwd (dx, dweight, dbias)"}}
     if ssd is not None:
         sh = SSD_SHAPE
         ss = ssd["step_ms"] / 1e3
@@ -804,9 +1011,7 @@ def main():
                        "l2": "x, z, y: 3 x 50 MB plus the 100 MB of bf16 chunk-entering states written and read per step, larger than L2",
                        "backward": {"us_per_step": ssd["bwd_ms"] * 1e3, "steps": ssd["bwd_steps"],
                                     "workspace_bytes": ssd["bwd_workspace_bytes"],
-                                    "call": "ssm_ssd_bwd: per group, the selective-scan backward "
-                                            "(fp32 I/O) on the group's channels and fixed-order "
-                                            "sums over the tied head parameters"}}
+                                    "time_vs_forward": ssd["bwd_ms"] / ssd["step_ms"]}}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line))

@@ -61,6 +61,9 @@ extern "C" {
 #define SSM_LAYOUT_BLD 8   /* scan, training forward, backward and conv1d: the
                               (batch, dim, seqlen) tensors are (batch, seqlen, dim)
                               instead (channels innermost; Algorithm 2's (B, L, D)) */
+#define SSM_TEST_STALL 16  /* ssm_scan_fwd_ex only, and only while ssm_set_test_mode is
+                              on (SSM_ERR_ARG otherwise): the failure-path test; one
+                              block of the call gives up waiting (see ssm_set_test_mode) */
 
 /* Status codes. */
 #define SSM_OK 0
@@ -106,9 +109,12 @@ int ssm_scan_fwd(const void* u, const void* delta, const float* delta_bias, cons
 
 /*
  * Bytes of workspace that ssm_scan_fwd_ex may use for these sizes on the
- * current device.  0 means the plan needs none.  With a workspace of at least
- * this size the scan may split the sequence across thread blocks (two passes
- * with a carried float32 state); with none it runs one pass per channel.
+ * current device: a 256-byte header holding the call's device status word
+ * (read by ssm_status), then the carry records of a plan that splits the
+ * sequence across thread blocks (two passes with a carried float32 state).
+ * 256 means the plan does not split; 0 means the sizes are not supported.
+ * With no workspace the scan runs one pass per channel and reports its status
+ * to the library-wide word.
  */
 size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                 int io_dtype);
@@ -121,9 +127,14 @@ size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int6
  *                   as one call over the whole sequence (chunk-carried state).
  *                   May equal final_state (read before it is written).
  *   workspace       optional device scratch (NULL = none) of workspace_bytes
- *                   bytes; contents need not be initialised and are not
- *                   meaningful afterwards.  SSM_ERR_WORKSPACE when non-NULL and
- *                   smaller than ssm_scan_workspace_bytes().
+ *                   bytes, 16-byte aligned; contents need not be initialised.
+ *                   The call zeroes its status word (the first 4 bytes) on
+ *                   the stream and a block that gives up waiting sets it, so
+ *                   ssm_status(workspace, stream) reports this call until the
+ *                   next call on the same workspace.  SSM_ERR_WORKSPACE when
+ *                   non-NULL and smaller than ssm_scan_workspace_bytes() (or
+ *                   than 256 bytes).  NULL: no split, and the status goes to
+ *                   the library-wide word.
  *   stream          cudaStream_t to enqueue on (NULL = legacy default stream).
  * Concurrent calls must not share a workspace.
  */
@@ -142,8 +153,10 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
  * copies run asynchronously and overlap; pageable memory works but the
  * copies then synchronise), with the layouts, dtypes, flags and nullability
  * of ssm_scan_fwd_ex (SSM_SOFTPLUS, SSM_EULER_B, SSM_LAYOUT_BLD).  workspace is
- * DEVICE memory of at least ssm_scan_fwd_host_workspace_bytes() bytes (three
- * staging slots, the parameters and the unit scans' scratch), 16-byte aligned.
+ * DEVICE memory of at least ssm_scan_fwd_host_workspace_bytes() bytes (the
+ * call's status word in its first 256 bytes, read by ssm_status(workspace,
+ * stream); the parameters, the unit scans' scratch and three staging slots),
+ * 16-byte aligned.
  *
  * The work is cut into units that are contiguous in host memory (a batch row,
  * or a block of a row's channels when batch < 8; a whole row with
@@ -166,16 +179,43 @@ int ssm_scan_fwd_host(const void* u, const void* delta, const float* delta_bias,
                       size_t workspace_bytes, void* stream);
 
 /*
- * Device-side status of the scans enqueued so far on this device.
+ * Device-side status of scan calls.  The pages have no counterpart: this is the
+ * library's failure report.  The scan kernels' only waits are on their own
+ * copies into shared memory; a wait that has not completed after 2 s gives up,
+ * the block sets the status word, lets its copies in flight land and leaves its
+ * outputs unwritten.  The CUDA context stays usable.
  *
- * Synchronises `stream` (NULL = legacy default stream), then reads and clears
- * the library's device error word.  Returns SSM_OK, SSM_ERR_TIMEOUT when a
- * scan block gave up waiting for one of its own chunk copies (the block then
- * left its outputs unwritten; the CUDA context stays usable), or SSM_ERR_CUDA
- * when the synchronisation itself failed.  The pages have no counterpart:
- * this is the library's failure report.
+ *   workspace  the workspace of a ssm_scan_fwd_ex / ssm_scan_fwd_train /
+ *              ssm_scan_fwd_host call: its status word, which the call zeroed,
+ *              so the result is that call's (the last call on this workspace;
+ *              `stream` must be the stream the call was issued on, or ordered
+ *              after it).  NULL: the library-wide word of the calls made without
+ *              a workspace (ssm_scan_fwd, ssm_scan_fwd_ex with NULL,
+ *              ssm_scan_fwd_noalloc) on the current device since the last
+ *              ssm_status(NULL, ·): read and cleared in one atomic step in stream
+ *              order, so an error set meanwhile by a kernel on another stream is
+ *              kept for the next read.  ssm_status(NULL, ·) calls must not
+ *              overlap one another.
+ *
+ * Synchronises `stream` (NULL = legacy default stream).  Returns SSM_OK,
+ * SSM_ERR_TIMEOUT (a block gave up waiting), SSM_ERR_ALIGN (workspace not
+ * 16-byte aligned) or SSM_ERR_CUDA (the copy or synchronisation failed).
  */
-int ssm_status(void* stream);
+int ssm_status(const void* workspace, void* stream);
+
+/*
+ * Failure-path test mode (the pages have no counterpart).  enable = 1 turns it
+ * on: ssm_scan_fwd_ex then accepts SSM_TEST_STALL, which makes block (0, 0) of
+ * the call's output pass arm the barrier of its second chunk's copy without
+ * issuing the copy, so that block's waits give up after wait_limit_ns (1e3 ..
+ * 2e9) instead of 2 s; the call's status word then reads SSM_ERR_TIMEOUT.  It
+ * needs a sequence of at least two 16-step chunks with 16-byte rows (the copy
+ * path the wait belongs to).  noalloc_limit_bytes > 0 lowers the scratch limit
+ * of ssm_scan_fwd_noalloc to that many bytes, so that its refusal can be
+ * tested.  enable = 0 restores the defaults.  Process-wide; for tests only.
+ * Returns SSM_OK, or SSM_ERR_ARG for a limit out of range.
+ */
+int ssm_set_test_mode(int enable, int64_t wait_limit_ns, int64_t noalloc_limit_bytes);
 
 /*
  * One-token decode: the recurrent mode of the summary page's equation (2)
@@ -217,14 +257,20 @@ int ssm_state_update_ex(float* state, const void* u, const void* delta, const fl
  * process exits.  The caller still passes all inputs and outputs.
  *
  * Arguments, layouts and results are those of ssm_scan_fwd_ex (no workspace
- * arguments).  Returns SSM_ERR_WORKSPACE when the plan for these sizes needs
- * more than SSM_STATIC_SCRATCH_BYTES of scratch (ssm_scan_workspace_bytes()
- * tells in advance); argument errors as ssm_scan_fwd_ex.
+ * arguments).  Returns SSM_ERR_WORKSPACE when the plan's carry records for
+ * these sizes need more than SSM_STATIC_SCRATCH_BYTES (ssm_scan_workspace_bytes()
+ * minus its 256-byte header tells in advance); SSM_ERR_ARG when `stream`
+ * belongs to another device than the current one (the array used is the
+ * current device's: every call needs the stream's device current); other
+ * argument errors as ssm_scan_fwd_ex.  Its device status goes to the
+ * library-wide word (ssm_status(NULL, stream)).
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with the device current) and caches it; make
- * that first call before any stream capture.  It calls no cudaMalloc,
- * cudaFree or other allocating routine.
+ * that first call before any stream capture.  A device reset
+ * (cudaDeviceReset) while the library is loaded is not supported: the cached
+ * address would be stale.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
  *
  * All calls on a device share the one array, which keeps whatever the last
  * call left in it (every carry record a call reads is written earlier by the

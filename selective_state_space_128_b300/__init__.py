@@ -23,6 +23,8 @@ SSM_OK = 0
 SSM_ERR_ARG, SSM_ERR_ALIGN, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_WORKSPACE = -1, -2, -3, -4, -5
 SSM_ERR_TIMEOUT = -6
 SSM_SOFTPLUS, SSM_EULER_B, SSM_SAVED_STATES, SSM_LAYOUT_BLD = 1, 2, 4, 8
+SSM_TEST_STALL = 16
+SCAN_STATUS_BYTES = 256   # the status header at the start of a scan workspace
 
 _lib = None
 
@@ -60,8 +62,10 @@ def load():
     lib.ssm_state_update_ex.restype = i32
     lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp]
     lib.ssm_scan_fwd_noalloc.restype = i32
-    lib.ssm_status.argtypes = [vp]
+    lib.ssm_status.argtypes = [vp, vp]
     lib.ssm_status.restype = i32
+    lib.ssm_set_test_mode.argtypes = [i32, i64, i64]
+    lib.ssm_set_test_mode.restype = i32
     lib.ssm_scan_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
     lib.ssm_scan_bwd_workspace_bytes.restype = sz
     lib.ssm_scan_bwd.argtypes = [vp] * 8 + [i32] + [vp] * 12 + [i64, i64, i64, i64, i32, vp, sz, vp]
@@ -243,10 +247,20 @@ def ssm_scan_fwd_train(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, f
     _call("ssm_scan_fwd_train", rc)
 
 
-def ssm_status(stream=None) -> int:
-    """Synchronise the stream and return the library's device-side status
-    (SSM_OK or SSM_ERR_TIMEOUT), clearing it."""
-    return int(load().ssm_status(_stream(stream)))
+def ssm_status(workspace=None, stream=None) -> int:
+    """Synchronise the stream and return the device-side status (SSM_OK or
+    SSM_ERR_TIMEOUT) of the last scan call on ``workspace`` (its status word), or,
+    with no workspace, of the calls made without one (the library-wide word, read
+    and cleared)."""
+    if workspace is not None:
+        _check_dev(workspace)
+    return int(load().ssm_status(_ptr(workspace), _stream(stream)))
+
+
+def ssm_set_test_mode(enable, wait_limit_ns=1000000, noalloc_limit_bytes=0) -> None:
+    """Tensor-free form of ``ssm_set_test_mode`` (the failure-path test mode)."""
+    _call("ssm_set_test_mode", load().ssm_set_test_mode(int(bool(enable)), int(wait_limit_ns),
+                                                        int(noalloc_limit_bytes)))
 
 
 def ssm_state_update(state, u, delta, A, B, C, D, z, y):

@@ -4,6 +4,7 @@
 """
 from __future__ import annotations
 
+import concurrent.futures
 import glob
 import os
 import subprocess
@@ -17,9 +18,10 @@ LIB = os.path.join(PKG, "libssm.so")
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
     "--expt-relaxed-constexpr",
 ]
+OBJ_DIR = os.path.join(PKG, "_build")
 
 
 def _nvcc():
@@ -44,14 +46,32 @@ def needs_build() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
+    """Compile every csrc/*.cu to an object (in parallel), then link libssm.so."""
     if not force and not needs_build():
         return LIB
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [_nvcc()] + NVCC_FLAGS + list(extra) + ["-I", os.path.join(ROOT, "include"),
-                                                    "-o", tmp] + sources()
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    inc = ["-I", os.path.join(ROOT, "include")]
+    pid = os.getpid()
+
+    def compile_one(src):
+        obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".%d.o" % pid)
+        cmd = [_nvcc()] + NVCC_FLAGS + list(extra) + inc + ["-c", "-o", obj, src]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        subprocess.check_call(cmd)
+        return obj
+
+    srcs = sources()
+    workers = max(1, min(len(srcs), os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+        objs = list(ex.map(compile_one, srcs))
+    tmp = LIB + ".tmp%d" % pid
+    cmd = [_nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", tmp] + objs
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.check_call(cmd)
+    for o in objs:
+        os.remove(o)
     os.replace(tmp, LIB)
     return LIB
 

@@ -1,4 +1,5 @@
 // C ABI of libssm: argument checks, planning and dispatch.  See include/ssm.h.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -35,6 +36,11 @@ int sm_count_current() {
 // the delta_softplus flag word: SSM_SOFTPLUS | SSM_EULER_B, nothing else
 bool flags_ok(int f) { return (f & ~(SSM_SOFTPLUS | SSM_EULER_B)) == 0; }
 
+// failure-path test mode (ssm_set_test_mode): SSM_TEST_STALL is refused unless on
+std::atomic<int> g_test_mode{0};
+std::atomic<int64_t> g_test_limit_ns{1000000};
+std::atomic<int64_t> g_test_noalloc_limit{0};
+
 bool sizes_ok(int64_t batch, int64_t dim, int64_t seqlen) {
   // every flat index must fit in int64 with room to spare
   if (batch < 0 || dim < 0 || seqlen < 0) return false;
@@ -67,8 +73,16 @@ const char* ssm_version(void) { return "0.1.0"; }
 size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                 int io_dtype) {
   if (!supported_n(dstate) || !sizes_ok(batch, dim, seqlen)) return 0;
-  return ssm::scan_plan(batch, dim, seqlen, dstate, io_dtype, sm_count_current(), true)
-      .workspace_bytes;
+  return ssm::kScanStatusBytes + ssm::scan_carry_bytes(batch, dim, seqlen, dstate, io_dtype);
+}
+
+int ssm_set_test_mode(int enable, int64_t wait_limit_ns, int64_t noalloc_limit_bytes) {
+  if (enable && (wait_limit_ns < 1000 || wait_limit_ns > 2000000000 || noalloc_limit_bytes < 0))
+    return SSM_ERR_ARG;
+  g_test_limit_ns.store(enable ? wait_limit_ns : 1000000);
+  g_test_noalloc_limit.store(enable ? noalloc_limit_bytes : 0);
+  g_test_mode.store(enable ? 1 : 0);
+  return SSM_OK;
 }
 
 size_t ssm_ssd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
@@ -143,24 +157,33 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
 
 }  // extern "C"
 
-namespace {
+namespace ssm {
 
-// ssm_scan_fwd_ex, plus an optional training save into a backward workspace
-int scan_fwd_impl(const void* u, const void* delta, const float* delta_bias, const float* A,
-                  const float* B, const float* C, const float* D, const void* z,
-                  int delta_softplus, void* y, float* final_state, int64_t batch, int64_t dim,
-                  int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
-                  void* workspace, size_t workspace_bytes, void* bwd_workspace,
-                  size_t bwd_workspace_bytes, bool train, void* stream) {
+size_t noalloc_test_limit() { return (size_t)g_test_noalloc_limit.load(); }
+
+size_t scan_carry_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype) {
+  return scan_plan(batch, dim, seqlen, dstate, io_dtype, sm_count_current(), true).workspace_bytes;
+}
+
+// the scan after the workspace has been resolved into a status word and carry scratch
+int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias, const float* A,
+                      const float* B, const float* C, const float* D, const void* z,
+                      int delta_softplus, void* y, float* final_state, int64_t batch, int64_t dim,
+                      int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
+                      int* status, bool zero_status, void* carry, size_t carry_bytes,
+                      void* bwd_workspace, size_t bwd_workspace_bytes, bool train,
+                      cudaStream_t stream) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
-  if (!flags_ok(delta_softplus & ~SSM_LAYOUT_BLD)) return SSM_ERR_ARG;
+  const bool stall = (delta_softplus & SSM_TEST_STALL) != 0;
+  if (stall && (!g_test_mode.load() || train)) return SSM_ERR_ARG;
+  if (!flags_ok(delta_softplus & ~(SSM_LAYOUT_BLD | SSM_TEST_STALL))) return SSM_ERR_ARG;
   const bool bld = (delta_softplus & SSM_LAYOUT_BLD) != 0;
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   const bool work = batch > 0 && dim > 0;
   if (work && seqlen > 0 && (!u || !delta || !A || !B || !C || !y)) return SSM_ERR_ARG;
-  const void* ptrs[] = {u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, workspace,
-                        bwd_workspace};
+  const void* ptrs[] = {u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state, carry,
+                        bwd_workspace, status};
   for (const void* q : ptrs)
     if (!aligned16(q)) return SSM_ERR_ALIGN;
   const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
@@ -185,17 +208,17 @@ int scan_fwd_impl(const void* u, const void* delta, const float* delta_bias, con
   // always runs unsplit.
   const bool in_place = final_state != nullptr && final_state == init_state;
   const ssm::ScanPlan plan = ssm::scan_plan(batch, dim, seqlen, dstate, io_dtype,
-                                            sm_count_current(), workspace != nullptr && !in_place);
-  if (workspace && workspace_bytes < plan.workspace_bytes) return SSM_ERR_WORKSPACE;
+                                            sm_count_current(), carry != nullptr && !in_place);
+  if (carry && carry_bytes < plan.workspace_bytes) return SSM_ERR_WORKSPACE;
   // the training save: the backward's checkpoint part of its workspace
   float* ckpt = nullptr;
   int64_t ckpt_nch = 0;
   if (train && seqlen > 0) {
     const ssm::BwdLayout lay = ssm::bwd_layout(batch, dim, seqlen, dstate);
     if (!bwd_workspace || bwd_workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
-    const void* others[] = {u, delta, z, y, workspace};
-    const size_t sizes[] = {nio, nio, nio, nio, plan.workspace_bytes};
-    for (int k = 0; k < 5; ++k)
+    const void* others[] = {u, delta, z, y, carry, status};
+    const size_t sizes[] = {nio, nio, nio, nio, plan.workspace_bytes, sizeof(int)};
+    for (int k = 0; k < 6; ++k)
       if (overlaps(bwd_workspace, lay.bytes, others[k], sizes[k])) return SSM_ERR_ARG;
     if (overlaps(bwd_workspace, lay.bytes, final_state, nst) ||
         overlaps(bwd_workspace, lay.bytes, init_state, nst) ||
@@ -206,6 +229,8 @@ int scan_fwd_impl(const void* u, const void* delta, const float* delta_bias, con
       ckpt_nch = lay.nch;
     }
   }
+  if (zero_status && status && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
+    return SSM_ERR_CUDA;
 
   ssm::ScanArgs a{};
   a.ckpt = ckpt;
@@ -217,6 +242,9 @@ int scan_fwd_impl(const void* u, const void* delta, const float* delta_bias, con
   a.softplus = (delta_softplus & SSM_SOFTPLUS) != 0;
   a.euler = (delta_softplus & SSM_EULER_B) != 0;
   a.bld = bld;
+  a.status = status;
+  a.test_stall = stall ? 1 : 0;
+  a.test_limit_ns = g_test_limit_ns.load();
   // 16-byte rows: of L steps, or of dim channels in the (batch, L, dim) layout
   a.vec_io = ((bld ? dim : seqlen) * (int64_t)esz) % 16 == 0;
   a.vec_bc = (seqlen * 4) % 16 == 0;
@@ -224,11 +252,52 @@ int scan_fwd_impl(const void* u, const void* delta, const float* delta_bias, con
   if (plan.nseg > 1) {
     const size_t rows = (size_t)batch * (size_t)dim;
     const size_t hbytes = ((size_t)(plan.nseg - 1) * rows * (size_t)dstate * 4 + 255) / 256 * 256;
-    a.carry_h = static_cast<float*>(workspace);
-    a.carry_s = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + hbytes);
+    a.carry_h = static_cast<float*>(carry);
+    a.carry_s = reinterpret_cast<float*>(static_cast<unsigned char*>(carry) + hbytes);
   }
-  const cudaError_t e = ssm::scan_launch(a, dstate, io_dtype, plan, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = ssm::scan_launch(a, dstate, io_dtype, plan, stream);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // namespace ssm
+
+namespace {
+
+// A caller's scan workspace: the status word in its first kScanStatusBytes, the
+// split plan's carry records after them.
+int scan_with_workspace(const void* u, const void* delta, const float* delta_bias, const float* A,
+                        const float* B, const float* C, const float* D, const void* z,
+                        int delta_softplus, void* y, float* final_state, int64_t batch,
+                        int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                        const float* init_state, void* workspace, size_t workspace_bytes,
+                        void* bwd_workspace, size_t bwd_workspace_bytes, bool train,
+                        void* stream) {
+  int* status = nullptr;
+  void* carry = nullptr;
+  size_t carry_bytes = 0;
+  if (workspace) {
+    if (workspace_bytes < ssm::kScanStatusBytes) return SSM_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SSM_ERR_ALIGN;
+    status = static_cast<int*>(workspace);
+    carry_bytes = workspace_bytes - ssm::kScanStatusBytes;
+    carry = carry_bytes ? static_cast<unsigned char*>(workspace) + ssm::kScanStatusBytes : nullptr;
+    // the workspace overlaps no input or output
+    const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
+    const size_t nio = (size_t)(batch > 0 ? batch : 0) * (size_t)(dim > 0 ? dim : 0) *
+                       (size_t)(seqlen > 0 ? seqlen : 0) * esz;
+    const size_t nst = (size_t)(batch > 0 ? batch : 0) * (size_t)(dim > 0 ? dim : 0) *
+                       (size_t)(dstate > 0 ? dstate : 0) * 4;
+    const void* io[] = {u, delta, z, y};
+    for (const void* q : io)
+      if (overlaps(workspace, workspace_bytes, q, nio)) return SSM_ERR_ARG;
+    if (overlaps(workspace, workspace_bytes, final_state, nst) ||
+        overlaps(workspace, workspace_bytes, init_state, nst))
+      return SSM_ERR_ARG;
+  }
+  return ssm::scan_fwd_internal(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y,
+                                final_state, batch, dim, seqlen, dstate, io_dtype, init_state,
+                                status, true, carry, carry_bytes, bwd_workspace,
+                                bwd_workspace_bytes, train, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -240,9 +309,9 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
                     int delta_softplus, void* y, float* final_state, int64_t batch, int64_t dim,
                     int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
                     void* workspace, size_t workspace_bytes, void* stream) {
-  return scan_fwd_impl(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state, batch,
-                       dim, seqlen, dstate, io_dtype, init_state, workspace, workspace_bytes,
-                       nullptr, 0, false, stream);
+  return scan_with_workspace(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                             batch, dim, seqlen, dstate, io_dtype, init_state, workspace,
+                             workspace_bytes, nullptr, 0, false, stream);
 }
 
 int ssm_scan_fwd_train(const void* u, const void* delta, const float* delta_bias, const float* A,
@@ -251,15 +320,22 @@ int ssm_scan_fwd_train(const void* u, const void* delta, const float* delta_bias
                        int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                        const float* init_state, void* workspace, size_t workspace_bytes,
                        void* bwd_workspace, size_t bwd_workspace_bytes, void* stream) {
-  return scan_fwd_impl(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state, batch,
-                       dim, seqlen, dstate, io_dtype, init_state, workspace, workspace_bytes,
-                       bwd_workspace, bwd_workspace_bytes, true, stream);
+  return scan_with_workspace(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                             batch, dim, seqlen, dstate, io_dtype, init_state, workspace,
+                             workspace_bytes, bwd_workspace, bwd_workspace_bytes, true, stream);
 }
 
-int ssm_status(void* stream) {
+int ssm_status(const void* workspace, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   int code = 0;
-  if (ssm::scan_device_error(&code, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (workspace) {
+    if (!aligned16(workspace)) return SSM_ERR_ALIGN;
+    if (cudaMemcpyAsync(&code, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return SSM_ERR_CUDA;
+  } else if (ssm::scan_library_status(&code, st) != cudaSuccess) {
     return SSM_ERR_CUDA;
+  }
   return code == 0 ? SSM_OK : SSM_ERR_TIMEOUT;
 }
 

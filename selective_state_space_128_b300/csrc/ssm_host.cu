@@ -9,7 +9,7 @@
 //
 //   copy-in stream:   wait until the slot is free, copy u, delta, z, B, C
 //                     (and init_state) of unit i into slot i % 3
-//   caller's stream:  the scan of unit i on its slot (ssm_scan_fwd_ex)
+//   caller's stream:  the scan of unit i on its slot
 //   copy-out stream:  copy y and final_state of unit i back to the host, then
 //                     mark the slot free
 //
@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/ssm.h"
+#include "ssm_internal.h"
 
 namespace {
 
@@ -38,7 +39,7 @@ struct HostPlan {
   int64_t dchunk = 0;        // channels per unit
   int64_t blocks = 0;        // units per batch row
   size_t io = 0, bc = 0, st = 0;  // bytes of one unit's u (and delta, z, y), B (and C), state
-  size_t scan_ws = 0;        // the unit scan's own workspace
+  size_t scan_ws = 0;        // the unit scan's carry scratch
   size_t o_params = 0, o_scan = 0, o_slots = 0, slot = 0, bytes = 0;
 };
 
@@ -55,10 +56,11 @@ HostPlan host_plan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, i
   p.io = up256((size_t)p.dchunk * (size_t)seqlen * esz);
   p.bc = up256((size_t)dstate * (size_t)seqlen * 4);
   p.st = up256((size_t)p.dchunk * (size_t)dstate * 4);
-  p.scan_ws = up256(ssm_scan_workspace_bytes(1, p.dchunk, seqlen, dstate, io_dtype));
+  p.scan_ws = up256(ssm::scan_carry_bytes(1, p.dchunk, seqlen, dstate, io_dtype));
   const size_t params = up256((size_t)dim * (size_t)dstate * 4) + 2 * up256((size_t)dim * 4);
-  p.o_params = 0;
-  p.o_scan = params;
+  // the status word first (ssm_status reads it there), then the parameters
+  p.o_params = ssm::kScanStatusBytes;
+  p.o_scan = p.o_params + params;
   p.o_slots = p.o_scan + p.scan_ws;
   p.slot = 4 * p.io + 2 * p.bc + 2 * p.st;
   p.bytes = p.o_slots + kSlots * p.slot;
@@ -106,7 +108,8 @@ size_t ssm_scan_fwd_host_workspace_bytes(int64_t batch, int64_t dim, int64_t seq
   if (batch <= 0 || dim <= 0 || seqlen < 0 || batch > 65535) return 0;
   if ((io_dtype != SSM_F32 && io_dtype != SSM_BF16) || !supported_n(dstate)) return 0;
   if ((double)batch * (double)dim * (double)(seqlen > 0 ? seqlen : 1) >= 9.0e18) return 0;
-  if (seqlen == 0) return up256((size_t)dim * (size_t)dstate * 4);  // a row of zeros
+  if (seqlen == 0)  // the status word and a row of zeros
+    return ssm::kScanStatusBytes + up256((size_t)dim * (size_t)dstate * 4);
   return host_plan(batch, dim, seqlen, dstate, io_dtype, (flags & SSM_LAYOUT_BLD) != 0).bytes;
 }
 
@@ -128,15 +131,18 @@ int ssm_scan_fwd_host(const void* u, const void* delta, const float* delta_bias,
   const size_t row_st = (size_t)dim * (size_t)dstate * 4;
   if (seqlen == 0) {
     // no steps: final_state = init_state, or zeros (a device row of zeros copied per row)
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), main) != cudaSuccess) return SSM_ERR_CUDA;
     if (!final_state) return SSM_OK;
     if (init_state)
       return cudaMemcpyAsync(final_state, init_state, (size_t)batch * row_st, cudaMemcpyDefault,
                              main) == cudaSuccess
                  ? SSM_OK
                  : SSM_ERR_CUDA;
-    if (cudaMemsetAsync(workspace, 0, row_st, main) != cudaSuccess) return SSM_ERR_CUDA;
+    unsigned char* zeros = static_cast<unsigned char*>(workspace) + ssm::kScanStatusBytes;
+    if (cudaMemsetAsync(workspace, 0, ssm::kScanStatusBytes + row_st, main) != cudaSuccess)
+      return SSM_ERR_CUDA;
     for (int64_t b = 0; b < batch; ++b)
-      if (cudaMemcpyAsync(reinterpret_cast<unsigned char*>(final_state) + (size_t)b * row_st, workspace,
+      if (cudaMemcpyAsync(reinterpret_cast<unsigned char*>(final_state) + (size_t)b * row_st, zeros,
                           row_st, cudaMemcpyDefault, main) != cudaSuccess)
         return SSM_ERR_CUDA;
     return SSM_OK;
@@ -151,6 +157,9 @@ int ssm_scan_fwd_host(const void* u, const void* delta, const float* delta_bias,
   float* dD = reinterpret_cast<float*>(ws + pl.o_params + up256((size_t)dim * (size_t)dstate * 4));
   float* dBias = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(dD) + up256((size_t)dim * 4));
   void* scan_ws = pl.scan_ws ? ws + pl.o_scan : nullptr;
+  // one status word for the whole call: zeroed here, set by any unit's scan
+  int* status = reinterpret_cast<int*>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(int), main) != cudaSuccess) return SSM_ERR_CUDA;
 
   Pipeline pp;
   if (!pp.ok) return SSM_ERR_CUDA;
@@ -199,10 +208,11 @@ int ssm_scan_fwd_host(const void* u, const void* delta, const float* delta_bias,
     if (cudaEventRecord(pp.ready[s], pp.in) != cudaSuccess ||
         cudaStreamWaitEvent(main, pp.ready[s], 0) != cudaSuccess)
       return SSM_ERR_CUDA;
-    const int rc = ssm_scan_fwd_ex(su, sd, delta_bias ? dBias + d0 : nullptr, dA + (size_t)d0 * dstate,
-                                   sB, sC, D ? dD + d0 : nullptr, z ? sz : nullptr, flags, sy,
-                                   final_state ? sh : nullptr, 1, dn, seqlen, dstate, io_dtype,
-                                   init_state ? sh0 : nullptr, scan_ws, pl.scan_ws, main);
+    const int rc = ssm::scan_fwd_internal(
+        su, sd, delta_bias ? dBias + d0 : nullptr, dA + (size_t)d0 * dstate, sB, sC,
+        D ? dD + d0 : nullptr, z ? sz : nullptr, flags, sy, final_state ? sh : nullptr, 1, dn,
+        seqlen, dstate, io_dtype, init_state ? sh0 : nullptr, status, false, scan_ws, pl.scan_ws,
+        nullptr, 0, false, main);
     if (rc != SSM_OK) return rc;
     if (cudaEventRecord(pp.done[s], main) != cudaSuccess ||
         cudaStreamWaitEvent(pp.out, pp.done[s], 0) != cudaSuccess)

@@ -43,6 +43,14 @@ struct ScanArgs {
   // when not saving
   float* ckpt;
   int64_t ckpt_nch;
+  // device status word that a block which gives up waiting sets to 1 (null: the
+  // library-wide word)
+  int* status;
+  // test of the failure path: block (0, 0, 0) of the output pass arms its
+  // second chunk's barrier without issuing the copies, so its wait runs out
+  // after test_limit_ns (its other waits use the same limit)
+  int test_stall;
+  int64_t test_limit_ns;
 };
 
 struct ScanPlan {
@@ -78,9 +86,32 @@ struct UpdateArgs {
   int euler;
 };
 
-// Synchronises `stream`, then reads and clears the scan kernels' device error
-// word (0 = none, 1 = a TMA wait timed out).
-cudaError_t scan_device_error(int* code, cudaStream_t stream);
+// Reads and clears, in stream order, the library-wide device status word of the
+// scans that ran without a workspace (0 = none, 1 = a wait timed out), then
+// synchronises `stream`.
+cudaError_t scan_library_status(int* code, cudaStream_t stream);
+
+// Bytes at the start of a scan workspace that hold its status word.
+constexpr size_t kScanStatusBytes = 256;
+
+// The scan after the C ABI's argument checks (ssm_api.cu), for the entry points
+// that manage the workspace themselves: `status` is the device status word (null:
+// the library-wide word), zeroed on the stream first when `zero_status`; `carry`
+// (carry_bytes) the split plan's scratch (null: the sequence is not split).
+int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias, const float* A,
+                      const float* B, const float* C, const float* D, const void* z, int flags,
+                      void* y, float* final_state, int64_t batch, int64_t dim, int64_t seqlen,
+                      int64_t dstate, int io_dtype, const float* init_state, int* status,
+                      bool zero_status, void* carry, size_t carry_bytes, void* bwd_workspace,
+                      size_t bwd_workspace_bytes, bool train, cudaStream_t stream);
+
+// The smaller scratch limit that the failure-path test mode sets for the
+// no-allocation scan (0: none).
+size_t noalloc_test_limit();
+
+// Carry-record bytes of the split plan for these sizes on the current device (0:
+// the plan does not split).
+size_t scan_carry_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype);
 
 cudaError_t update_launch(const UpdateArgs& a, int64_t N, int io_dtype, cudaStream_t stream);
 

@@ -47,8 +47,10 @@
 
 namespace ssm {
 
-// Device-side error word (0 = none).  Read and cleared by scan_device_error().
+// Library-wide device status word (0 = none) of the scans that run without a
+// workspace; read and cleared by scan_library_status().
 __device__ int g_scan_error;
+__device__ int g_scan_error_taken;
 
 // Per-N tiling: NPT states per lane, G lanes per channel, CH channels per
 // block, T steps per chunk, NS raw stages, E channel steps per thread in the
@@ -146,14 +148,17 @@ struct ScanMaps {
 // ---------------------------------------------------------------------------
 
 // Issue the TMA loads of one chunk into a raw stage (one thread).
+// With `no_copy` (the failure-path test) the barrier is armed and no copy is
+// issued, so its phase never completes and the waits on it run out.
 template <typename IO, int N, int PASS>
 __device__ __forceinline__ void issue_chunk(const ScanArgs& p, const ScanMaps& m,
                                             unsigned char* stage, uint64_t* bar, int64_t b,
-                                            int64_t d0, int64_t t0) {
+                                            int64_t d0, int64_t t0, bool no_copy = false) {
   using S = ScanSmem<IO, N>;
   const bool has_z = PASS == 0 && p.z != nullptr;
   const uint32_t bytes = (uint32_t)(S::kRawIO * (has_z ? 3 : 2) + S::kRawBC * (PASS == 0 ? 2 : 1));
   mbar_arrive_expect_tx(bar, bytes);
+  if (no_copy) return;
   // u/Δ/z boxes: (T steps, CH channels) of a (batch, dim, L) tensor, or
   // (CH channels, T steps) of a (batch, L, dim) one -- the stage is then [t][c]
   const int x = p.bld ? (int)d0 : (int)t0, y = p.bld ? (int)t0 : (int)d0, z = (int)b;
@@ -624,6 +629,11 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
   const int seg_steps = (int)(t_end - t_begin);
   const int nchunks = (seg_steps + T - 1) / T;
   const bool use_tma = p.use_tma != 0;
+  // the failure-path test: this block's second chunk is never copied and its
+  // waits give up after the test's short limit
+  const bool stall = PASS == 0 && p.test_stall && blockIdx.x == 0 && blockIdx.y == 0 &&
+                     blockIdx.z == 0;
+  const uint64_t wlim = stall ? (uint64_t)p.test_limit_ns : kWaitLimitNs;
   auto stage_of = [&](int k) { return sm + (k % NS) * S::kStage; };
   auto buf_of = [&](int k) { return sm + S::oBuf + (k % S::NBT) * S::kBuf; };
   auto part_of = [&](int k) {
@@ -679,7 +689,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     for (; issued < NS && issued < nchunks; ++issued)
       if (tid == 0)
         issue_chunk<IO, N, PASS>(p, maps, stage_of(issued), &raw_full[issued % NS], b, d0,
-                                 t0_of(issued));
+                                 t0_of(issued), stall && issued == 1);
   } else {
     for (; issued < NS && issued < nchunks; ++issued)
       load_chunk_plain<IO, N, PASS>(p, stage_of(issued), tid, b, d0, t0_of(issued));
@@ -740,7 +750,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
       prep_compute<IO, N, PASS, false, true>(stage_of(k), sBias, tid, tcount_of(k), nrows, fl, v);
     }
   };
-  bool ok = !use_tma || mbar_wait_bounded(&raw_full[0], 0);
+  bool ok = !use_tma || mbar_wait_bounded(&raw_full[0], 0, wlim);
   if (ok) {
     PrepVals<IO, N, PASS> v0;
     convert(0, false, v0);
@@ -770,7 +780,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     // A
     PrepVals<IO, N, PASS> pv;
     if (has_next) {
-      if (use_tma) ok = mbar_wait_bounded(&raw_full[snext], phnext);
+      if (use_tma) ok = mbar_wait_bounded(&raw_full[snext], phnext, wlim);
       if (ok) {
         const unsigned char* st = sm + snext * S::kStage;
         if (fast) {
@@ -785,7 +795,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
       pv = PrepVals<IO, N, PASS>{};
     }
     // B
-    if (!ok || !mbar_wait_bounded(iter_bar, (uint32_t)(i & 1))) {
+    if (!ok || !mbar_wait_bounded(iter_bar, (uint32_t)(i & 1), wlim)) {
       failed = true;
       break;
     }
@@ -846,14 +856,14 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     }
   }
   // the last chunk's partials are complete once every thread has arrived
-  if (!failed && !mbar_wait_bounded(iter_bar, (uint32_t)(nchunks & 1))) failed = true;
+  if (!failed && !mbar_wait_bounded(iter_bar, (uint32_t)(nchunks & 1), wlim)) failed = true;
   if (failed) {
     // a wait ran out: record it, let this block's copies still in flight
     // land (bounded) and leave without writing a state
-    atomicExch(&g_scan_error, 1);
+    atomicExch(p.status ? p.status : &g_scan_error, 1);
     if (tid == 0 && use_tma) {
       for (int k = i; k < issued; ++k)
-        (void)mbar_wait_bounded(&raw_full[k % NS], (uint32_t)((k / NS) & 1));
+        (void)mbar_wait_bounded(&raw_full[k % NS], (uint32_t)((k / NS) & 1), wlim);
     }
     return;
   }
@@ -1056,13 +1066,18 @@ cudaError_t scan_launch(const ScanArgs& a, int64_t N, int io_dtype, const ScanPl
   return launch_io<__nv_bfloat16>(a, N, stream);
 }
 
-cudaError_t scan_device_error(int* code, cudaStream_t stream) {
-  int zero = 0;
-  cudaError_t e = cudaStreamSynchronize(stream);
+// One thread takes the library-wide word (read and cleared in one atomic step, so
+// an error a kernel on another stream records meanwhile is kept for the next call).
+__global__ void take_status_kernel() { g_scan_error_taken = atomicExch(&g_scan_error, 0); }
+
+cudaError_t scan_library_status(int* code, cudaStream_t stream) {
+  take_status_kernel<<<1, 1, 0, stream>>>();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaMemcpyFromSymbol(code, g_scan_error, sizeof(int));
+  e = cudaMemcpyFromSymbolAsync(code, g_scan_error_taken, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                stream);
   if (e != cudaSuccess) return e;
-  return cudaMemcpyToSymbol(g_scan_error, &zero, sizeof(int));
+  return cudaStreamSynchronize(stream);
 }
 
 }  // namespace ssm

@@ -69,13 +69,32 @@ def test_workspace_too_small_is_rejected_before_launch():
 
 
 def test_workspace_plan():
-    # many channels: one pass, no workspace
-    assert ssm.ssm_scan_workspace_bytes(8, 1536, 2048, 16, 1) == 0
-    assert ssm.ssm_scan_workspace_bytes(4, 5120, 4096, 16, 1) == 0
-    # few channels, long sequence: split with carry records
-    assert ssm.ssm_scan_workspace_bytes(1, 1536, 65536, 16, 1) > 0
-    assert ssm.ssm_scan_workspace_bytes(1, 64, 100, 16, 1) == 0   # too short to split
-    assert ssm.ssm_scan_workspace_bytes(1, 64, 100, 3, 1) == 0    # unsupported N
+    hdr = ssm.SCAN_STATUS_BYTES
+    # many channels: one pass, the status header only
+    assert ssm.ssm_scan_workspace_bytes(8, 1536, 2048, 16, 1) == hdr
+    assert ssm.ssm_scan_workspace_bytes(4, 5120, 4096, 16, 1) == hdr
+    # few channels, long sequence: split with carry records after the header
+    assert ssm.ssm_scan_workspace_bytes(1, 1536, 65536, 16, 1) > hdr
+    assert ssm.ssm_scan_workspace_bytes(1, 64, 100, 16, 1) == hdr   # too short to split
+    assert ssm.ssm_scan_workspace_bytes(1, 64, 100, 3, 1) == 0      # unsupported N
+
+
+def test_workspace_smaller_than_the_status_header_is_rejected():
+    rc = _scan(ws=FAKE + 0x9000000, wsb=ssm.SCAN_STATUS_BYTES - 16)
+    assert rc == ssm.SSM_ERR_WORKSPACE
+    assert _scan(ws=FAKE + 0x9000008, wsb=4096) == ssm.SSM_ERR_ALIGN
+
+
+def test_stall_flag_is_refused_outside_test_mode():
+    """SSM_TEST_STALL (the failure-path test) is an argument error unless the test
+    mode is on; the test mode checks its limits."""
+    assert _scan(softplus=1 | ssm.SSM_TEST_STALL) == ssm.SSM_ERR_ARG
+    l = lib()
+    assert l.ssm_set_test_mode(1, 10, 0) == ssm.SSM_ERR_ARG            # limit below 1 us
+    assert l.ssm_set_test_mode(1, 3_000_000_000, 0) == ssm.SSM_ERR_ARG  # above 2 s
+    assert l.ssm_set_test_mode(1, 1_000_000, -1) == ssm.SSM_ERR_ARG
+    assert l.ssm_set_test_mode(0, 0, 0) == ssm.SSM_OK
+    assert _scan(softplus=1 | ssm.SSM_TEST_STALL) == ssm.SSM_ERR_ARG
 
 
 def _upd(**kw):
@@ -268,17 +287,21 @@ def test_scan_host_argument_errors():
 
 
 def test_scan_host_workspace_plan():
-    # three staging slots of a whole batch row (8 rows: one unit per row): u, delta, z, y of
-    # 1536 x 2048 bf16, B and C of 16 x 2048 fp32, two states of 1536 x 16 fp32; plus A, D, bias
+    # the status header, then three staging slots of a whole batch row (8 rows: one unit per
+    # row): u, delta, z, y of 1536 x 2048 bf16, B and C of 16 x 2048 fp32, two states of
+    # 1536 x 16 fp32; plus A, D, bias and the unit scan's carry records
     slot = 4 * 1536 * 2048 * 2 + 2 * 16 * 2048 * 4 + 2 * 1536 * 16 * 4
     params = 1536 * 16 * 4 + 2 * 1536 * 4
-    scan_ws = ssm.ssm_scan_workspace_bytes(1, 1536, 2048, 16, ssm.SSM_BF16)
+    hdr = ssm.SCAN_STATUS_BYTES
+    carry = ssm.ssm_scan_workspace_bytes(1, 1536, 2048, 16, ssm.SSM_BF16) - hdr
+    scan_ws = hdr + (carry + 255) // 256 * 256
     assert ssm.ssm_scan_fwd_host_workspace_bytes(8, 1536, 2048, 16, ssm.SSM_BF16, 1) == \
         params + scan_ws + 3 * slot
     # batch 1: the row is cut into 8 blocks of channels, so a slot is an eighth as large
     small = ssm.ssm_scan_fwd_host_workspace_bytes(1, 1536, 2048, 16, ssm.SSM_BF16, 1)
     assert small < params + scan_ws + slot
-    assert ssm.ssm_scan_fwd_host_workspace_bytes(1, 64, 0, 16, ssm.SSM_BF16, 0) == 64 * 16 * 4
+    assert ssm.ssm_scan_fwd_host_workspace_bytes(1, 64, 0, 16, ssm.SSM_BF16, 0) == \
+        hdr + 64 * 16 * 4
     assert ssm.ssm_scan_fwd_host_workspace_bytes(1, 64, 10, 12, ssm.SSM_BF16, 0) == 0
 
 

@@ -126,4 +126,4 @@ def test_whole_channel_blocks_with_zero_A(gate, softplus):
         torch.cuda.synchronize()
         assert oracle.rel_err(host64(y), y_ref) <= 1e-2
         assert oracle.rel_err(host64(st), st_ref) <= 1e-2
-    assert ssm.ssm_status() == ssm.SSM_OK
+    assert ssm.ssm_status(None) == ssm.SSM_OK
