@@ -146,6 +146,36 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* delta_bias, c
                     void* stream);
 
 /*
+ * Scan on strided views: as ssm_scan_fwd_ex, with u, delta, z and y given as
+ * views with arbitrary element strides, so that, for instance, u and z can be
+ * the two halves of one input projection's output without a copy (the summary
+ * page's section 4a shape table splits Linear(2ED) into the SSM input and the
+ * gate; Algorithm 2's (B, L, D) with a row stride of 2ED).
+ *
+ *   strides   12 int64 element strides, (batch, channel, time) for u, delta, z
+ *             and y in that order (z's are ignored when z is NULL).  NULL: dense
+ *             (batch, dim, seqlen).  Element (b, d, t) of u is
+ *             u[b * strides[0] + d * strides[1] + t * strides[2]], and so on.
+ *
+ * u, delta and z must share one orientation: unit time stride (time-major rows)
+ * or unit channel stride (channel-major rows; SSM_ERR_UNSUPPORTED otherwise).
+ * Strides are >= 0 and non-zero over extents above one; y's must not map two
+ * elements to one place (SSM_ERR_ARG).  Views whose other strides are multiples
+ * of 16 bytes are staged by TMA; others take the element-wise path.  y may be
+ * any non-overlapping view; with unit time stride and 16-byte aligned rows it is
+ * stored in 16-byte vectors.  SSM_LAYOUT_BLD is refused (the strides say the
+ * layout); other flags, the workspace and the status word as ssm_scan_fwd_ex.
+ * Results equal ssm_scan_fwd_ex's on contiguous copies of the views, bit for
+ * bit.  Overlap checks use each view's span (first to last element).
+ */
+int ssm_scan_fwd_strided(const void* u, const void* delta, const float* delta_bias,
+                         const float* A, const float* B, const float* C, const float* D,
+                         const void* z, int delta_softplus, void* y, float* final_state,
+                         int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                         int io_dtype, const int64_t* strides, const float* init_state,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The scan on HOST buffers (selective-scan summary page, section 4b equations
  * (2), (4) and Algorithm 2, as ssm_scan_fwd_ex): the copies to and from the
  * device are part of the call.  u, delta, z, y, B, C, A, D, delta_bias,

@@ -60,6 +60,9 @@ def load():
     lib.ssm_state_update.restype = i32
     lib.ssm_state_update_ex.argtypes = [vp, vp, vp, vp, i32] + [vp] * 6 + [i64, i64, i64, i32, vp]
     lib.ssm_state_update_ex.restype = i32
+    lib.ssm_scan_fwd_strided.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp,
+                                                     vp, sz, vp]
+    lib.ssm_scan_fwd_strided.restype = i32
     lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp]
     lib.ssm_scan_fwd_noalloc.restype = i32
     lib.ssm_status.argtypes = [vp, vp]
@@ -144,6 +147,16 @@ def _check_dev(*ts):
             raise ValueError("libssm takes contiguous tensors")
 
 
+def _check_dev_strided(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("libssm takes device tensors; got a tensor on %s" % t.device)
+        if t.dim() != 3:
+            raise ValueError("strided views are (batch, dim, L)")
+
+
 def _check_host(*ts):
     for t in ts:
         if t is None or isinstance(t, int):
@@ -206,6 +219,27 @@ def ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, fina
                                 _ptr(init_state), _ptr(workspace), int(workspace_bytes or 0),
                                 _stream(stream))
     _call("ssm_scan_fwd_ex", rc)
+
+
+def ssm_scan_fwd_strided(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                         init_state=None, workspace=None, workspace_bytes=None, stream=None):
+    """Tensor form of ``ssm_scan_fwd_strided``: u, delta, z, y are (batch, dim, L) views
+    with any element strides (``tensor.stride()``); sizes from u, A and B."""
+    _check_dev_strided(u, delta, z, y)
+    _check_dev(delta_bias, A, B, C, D, final_state, init_state, workspace)
+    batch, dim, L = int(u.shape[0]), int(u.shape[1]), int(u.shape[2])
+    N = A.shape[1]
+    if workspace is not None and workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = (ctypes.c_int64 * 12)(*(list(u.stride()) + list(delta.stride())
+                                 + list(z.stride() if z is not None else (0, 0, 0))
+                                 + list(y.stride())))
+    rc = load().ssm_scan_fwd_strided(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
+                                     _ptr(C), _ptr(D), _ptr(z), _flags(delta_softplus), _ptr(y),
+                                     _ptr(final_state), batch, dim, L, N, _io_dtype(u),
+                                     ctypes.cast(st, ctypes.c_void_p), _ptr(init_state),
+                                     _ptr(workspace), int(workspace_bytes or 0), _stream(stream))
+    _call("ssm_scan_fwd_strided", rc)
 
 
 def ssm_scan_fwd_host_workspace_bytes(batch, dim, seqlen, dstate, io_dtype, flags=0) -> int:

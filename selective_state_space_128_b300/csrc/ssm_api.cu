@@ -33,6 +33,30 @@ int sm_count_current() {
   return n;
 }
 
+// bytes from the first to one past the last element of a (batch, dim, seqlen)
+// tensor with element strides t (0 when empty)
+size_t span_bytes(const int64_t* t, int64_t batch, int64_t dim, int64_t seqlen, size_t esz) {
+  if (batch <= 0 || dim <= 0 || seqlen <= 0) return 0;
+  return (size_t)(1 + (batch - 1) * t[0] + (dim - 1) * t[1] + (seqlen - 1) * t[2]) * esz;
+}
+
+// distinct (b, d, t) map to distinct elements: sorted by stride, each stride is at
+// least the span of the dimensions with smaller strides
+bool strides_injective(const int64_t* t, const int64_t* ext) {
+  int idx[3] = {0, 1, 2};
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (t[idx[j]] < t[idx[i]]) { const int q = idx[i]; idx[i] = idx[j]; idx[j] = q; }
+  int64_t span = 1;
+  for (int i = 0; i < 3; ++i) {
+    const int k = idx[i];
+    if (ext[k] <= 1) continue;
+    if (t[k] < span) return false;
+    span = t[k] * (ext[k] - 1) + span;
+  }
+  return true;
+}
+
 // the delta_softplus flag word: SSM_SOFTPLUS | SSM_EULER_B, nothing else
 bool flags_ok(int f) { return (f & ~(SSM_SOFTPLUS | SSM_EULER_B)) == 0; }
 
@@ -172,12 +196,13 @@ int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias,
                       int64_t seqlen, int64_t dstate, int io_dtype, const float* init_state,
                       int* status, bool zero_status, void* carry, size_t carry_bytes,
                       void* bwd_workspace, size_t bwd_workspace_bytes, bool train,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, const int64_t* strides) {
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
   const bool stall = (delta_softplus & SSM_TEST_STALL) != 0;
   if (stall && (!g_test_mode.load() || train)) return SSM_ERR_ARG;
   if (!flags_ok(delta_softplus & ~(SSM_LAYOUT_BLD | SSM_TEST_STALL))) return SSM_ERR_ARG;
-  const bool bld = (delta_softplus & SSM_LAYOUT_BLD) != 0;
+  bool bld = (delta_softplus & SSM_LAYOUT_BLD) != 0;
+  if (strides && bld) return SSM_ERR_ARG;  // the strides say the layout
   if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
   if (!supported_n(dstate)) return SSM_ERR_UNSUPPORTED;
   const bool work = batch > 0 && dim > 0;
@@ -187,20 +212,46 @@ int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias,
   for (const void* q : ptrs)
     if (!aligned16(q)) return SSM_ERR_ALIGN;
   const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
-  const size_t nio = (size_t)batch * (size_t)dim * (size_t)seqlen * esz;
+  // element strides (batch, channel, time) of u, delta, z, y
+  int64_t st[4][3];
+  for (int k = 0; k < 4; ++k) {
+    if (strides) {
+      for (int e = 0; e < 3; ++e) st[k][e] = strides[3 * k + e];
+    } else {
+      st[k][0] = dim * seqlen;
+      st[k][1] = bld ? 1 : seqlen;
+      st[k][2] = bld ? dim : 1;
+    }
+  }
+  if (strides) {
+    const int64_t ext[3] = {batch, dim, seqlen};
+    for (int k = 0; k < 4; ++k)
+      for (int e = 0; e < 3; ++e)
+        if (st[k][e] < 0 || (ext[e] > 1 && st[k][e] == 0)) return SSM_ERR_ARG;
+    if (!strides_injective(st[3], ext)) return SSM_ERR_ARG;  // y would write an element twice
+    // u, delta (and z) share one orientation: unit time stride, or unit channel stride
+    const bool tmaj = st[0][2] == 1 && st[1][2] == 1 && (!z || st[2][2] == 1);
+    const bool cmaj = st[0][1] == 1 && st[1][1] == 1 && (!z || st[2][1] == 1);
+    if (seqlen > 1 && dim > 1 && !tmaj && !cmaj) return SSM_ERR_UNSUPPORTED;
+    bld = !tmaj && cmaj;
+  }
+  const size_t nio_u = span_bytes(st[0], batch, dim, seqlen, esz);
+  const size_t nio_d = span_bytes(st[1], batch, dim, seqlen, esz);
+  const size_t nio_z = z ? span_bytes(st[2], batch, dim, seqlen, esz) : 0;
+  const size_t nio = span_bytes(st[3], batch, dim, seqlen, esz);  // y
   const size_t nst = (size_t)batch * (size_t)dim * (size_t)dstate * 4;
   const size_t nbc = (size_t)batch * (size_t)dstate * (size_t)seqlen * 4;
   // outputs must not overlap inputs (final_state may equal init_state exactly)
-  const void* ins[] = {u, delta, z};
-  for (const void* q : ins)
-    if (overlaps(y, nio, q, nio)) return SSM_ERR_ARG;
+  if (overlaps(y, nio, u, nio_u) || overlaps(y, nio, delta, nio_d) || overlaps(y, nio, z, nio_z))
+    return SSM_ERR_ARG;
   if (overlaps(y, nio, B, nbc) || overlaps(y, nio, C, nbc) || overlaps(y, nio, final_state, nst))
     return SSM_ERR_ARG;
   if (final_state && init_state && final_state != init_state &&
       overlaps(final_state, nst, init_state, nst))
     return SSM_ERR_ARG;
-  for (const void* q : ins)
-    if (overlaps(final_state, nst, q, nio)) return SSM_ERR_ARG;
+  if (overlaps(final_state, nst, u, nio_u) || overlaps(final_state, nst, delta, nio_d) ||
+      overlaps(final_state, nst, z, nio_z))
+    return SSM_ERR_ARG;
   if (!work) return SSM_OK;
 
   // A split plan reads init_state in every segment while the last segment
@@ -217,7 +268,7 @@ int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias,
     const ssm::BwdLayout lay = ssm::bwd_layout(batch, dim, seqlen, dstate);
     if (!bwd_workspace || bwd_workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
     const void* others[] = {u, delta, z, y, carry, status};
-    const size_t sizes[] = {nio, nio, nio, nio, plan.workspace_bytes, sizeof(int)};
+    const size_t sizes[] = {nio_u, nio_d, nio_z, nio, plan.workspace_bytes, sizeof(int)};
     for (int k = 0; k < 6; ++k)
       if (overlaps(bwd_workspace, lay.bytes, others[k], sizes[k])) return SSM_ERR_ARG;
     if (overlaps(bwd_workspace, lay.bytes, final_state, nst) ||
@@ -245,8 +296,22 @@ int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias,
   a.status = status;
   a.test_stall = stall ? 1 : 0;
   a.test_limit_ns = g_test_limit_ns.load();
-  // 16-byte rows: of L steps, or of dim channels in the (batch, L, dim) layout
-  a.vec_io = ((bld ? dim : seqlen) * (int64_t)esz) % 16 == 0;
+  for (int e = 0; e < 3; ++e) {
+    a.st_u[e] = st[0][e];
+    a.st_d[e] = st[1][e];
+    a.st_z[e] = st[2][e];
+    a.st_y[e] = st[3][e];
+  }
+  // staging by TMA: the strides other than the unit one are multiples of 16 bytes
+  {
+    const int o = bld ? 2 : 1;
+    auto m16 = [&](const int64_t* t) { return (t[o] * (int64_t)esz) % 16 == 0 && (t[0] * (int64_t)esz) % 16 == 0; };
+    a.vec_io = m16(st[0]) && m16(st[1]) && (!z || m16(st[2]));
+    if (bld ? st[0][1] != 1 : st[0][2] != 1) a.vec_io = 0;
+  }
+  // vector stores of y: unit time stride and 16-byte aligned rows
+  a.vec_y = st[3][2] == 1 && (st[3][1] * (int64_t)esz) % 16 == 0 &&
+            (st[3][0] * (int64_t)esz) % 16 == 0;
   a.vec_bc = (seqlen * 4) % 16 == 0;
   a.force_precise = io_dtype == SSM_F32;
   if (plan.nseg > 1) {
@@ -271,7 +336,7 @@ int scan_with_workspace(const void* u, const void* delta, const float* delta_bia
                         int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                         const float* init_state, void* workspace, size_t workspace_bytes,
                         void* bwd_workspace, size_t bwd_workspace_bytes, bool train,
-                        void* stream) {
+                        void* stream, const int64_t* strides = nullptr) {
   int* status = nullptr;
   void* carry = nullptr;
   size_t carry_bytes = 0;
@@ -283,13 +348,20 @@ int scan_with_workspace(const void* u, const void* delta, const float* delta_bia
     carry = carry_bytes ? static_cast<unsigned char*>(workspace) + ssm::kScanStatusBytes : nullptr;
     // the workspace overlaps no input or output
     const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
-    const size_t nio = (size_t)(batch > 0 ? batch : 0) * (size_t)(dim > 0 ? dim : 0) *
-                       (size_t)(seqlen > 0 ? seqlen : 0) * esz;
     const size_t nst = (size_t)(batch > 0 ? batch : 0) * (size_t)(dim > 0 ? dim : 0) *
                        (size_t)(dstate > 0 ? dstate : 0) * 4;
     const void* io[] = {u, delta, z, y};
-    for (const void* q : io)
-      if (overlaps(workspace, workspace_bytes, q, nio)) return SSM_ERR_ARG;
+    for (int k = 0; k < 4; ++k) {
+      int64_t t[3] = {dim * seqlen, seqlen, 1};
+      if (strides) {
+        for (int e = 0; e < 3; ++e) t[e] = strides[3 * k + e] < 0 ? 0 : strides[3 * k + e];
+      } else if (delta_softplus & SSM_LAYOUT_BLD) {
+        t[1] = 1;
+        t[2] = dim;
+      }
+      if (overlaps(workspace, workspace_bytes, io[k], span_bytes(t, batch, dim, seqlen, esz)))
+        return SSM_ERR_ARG;
+    }
     if (overlaps(workspace, workspace_bytes, final_state, nst) ||
         overlaps(workspace, workspace_bytes, init_state, nst))
       return SSM_ERR_ARG;
@@ -297,7 +369,8 @@ int scan_with_workspace(const void* u, const void* delta, const float* delta_bia
   return ssm::scan_fwd_internal(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y,
                                 final_state, batch, dim, seqlen, dstate, io_dtype, init_state,
                                 status, true, carry, carry_bytes, bwd_workspace,
-                                bwd_workspace_bytes, train, static_cast<cudaStream_t>(stream));
+                                bwd_workspace_bytes, train, static_cast<cudaStream_t>(stream),
+                                strides);
 }
 
 }  // namespace
@@ -323,6 +396,17 @@ int ssm_scan_fwd_train(const void* u, const void* delta, const float* delta_bias
   return scan_with_workspace(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
                              batch, dim, seqlen, dstate, io_dtype, init_state, workspace,
                              workspace_bytes, bwd_workspace, bwd_workspace_bytes, true, stream);
+}
+
+int ssm_scan_fwd_strided(const void* u, const void* delta, const float* delta_bias,
+                         const float* A, const float* B, const float* C, const float* D,
+                         const void* z, int delta_softplus, void* y, float* final_state,
+                         int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                         int io_dtype, const int64_t* strides, const float* init_state,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return scan_with_workspace(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                             batch, dim, seqlen, dstate, io_dtype, init_state, workspace,
+                             workspace_bytes, nullptr, 0, false, stream, strides);
 }
 
 int ssm_status(const void* workspace, void* stream) {

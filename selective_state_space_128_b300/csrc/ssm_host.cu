@@ -212,7 +212,7 @@ int ssm_scan_fwd_host(const void* u, const void* delta, const float* delta_bias,
         su, sd, delta_bias ? dBias + d0 : nullptr, dA + (size_t)d0 * dstate, sB, sC,
         D ? dD + d0 : nullptr, z ? sz : nullptr, flags, sy, final_state ? sh : nullptr, 1, dn,
         seqlen, dstate, io_dtype, init_state ? sh0 : nullptr, status, false, scan_ws, pl.scan_ws,
-        nullptr, 0, false, main);
+        nullptr, 0, false, main, nullptr);
     if (rc != SSM_OK) return rc;
     if (cudaEventRecord(pp.done[s], main) != cudaSuccess ||
         cudaStreamWaitEvent(pp.out, pp.done[s], 0) != cudaSuccess)

@@ -32,8 +32,14 @@ struct ScanArgs {
   int64_t seg_len;  // steps per segment, a multiple of the chunk length
   int nseg;
   int softplus;
-  int vec_io;       // rows of u/delta/z/y (L steps, or dim channels with bld) are 16-byte aligned
-  int bld;          // u/delta/z/y are (batch, L, dim) instead of (batch, dim, L)
+  int vec_io;       // u/delta/z can be staged by TMA: their strides other than the unit one
+                    // are multiples of 16 bytes
+  int bld;          // u/delta/z are channel-major (unit channel stride) instead of
+                    // time-major (unit time stride)
+  // element strides (batch, channel, time) of u, delta, z and y; dense (batch, dim, L)
+  // or (batch, L, dim) unless the caller gave others
+  int64_t st_u[3], st_d[3], st_z[3], st_y[3];
+  int vec_y;        // y has unit time stride and 16-byte aligned rows: vector stores
   int vec_bc;       // rows of B/C are 16-byte aligned
   int force_precise;
   int euler;        // B̄ = Δ B (runs on the precise flavour)
@@ -69,6 +75,16 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
 cudaError_t scan_launch(const ScanArgs& a, int64_t N, int io_dtype, const ScanPlan& plan,
                         cudaStream_t stream);
 
+// The warp-autonomous scan (ssm_scan_fast.cu) for N = 16 and bf16 I/O in the
+// (batch, dim, L) layout with 16-byte rows, zero-order hold: whether it applies,
+// and its launch (a.status must point at a device word).
+bool scan_fast_applies(const ScanArgs& a, int64_t N, int io_dtype);
+cudaError_t scan_fast_launch(const ScanArgs& a, cudaStream_t stream);
+
+// Channels per unit of work that the plan sizes the split for (the fast scan's
+// warp: 16 channels at N = 16).
+constexpr int kFastChannels = 16;
+
 struct UpdateArgs {
   float* state;
   const void* u;
@@ -97,13 +113,16 @@ constexpr size_t kScanStatusBytes = 256;
 // The scan after the C ABI's argument checks (ssm_api.cu), for the entry points
 // that manage the workspace themselves: `status` is the device status word (null:
 // the library-wide word), zeroed on the stream first when `zero_status`; `carry`
-// (carry_bytes) the split plan's scratch (null: the sequence is not split).
+// (carry_bytes) the split plan's scratch (null: the sequence is not split);
+// `strides` the 12 element strides (batch, channel, time) of u, delta, z, y (null:
+// dense, as the SSM_LAYOUT_BLD flag says).
 int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias, const float* A,
                       const float* B, const float* C, const float* D, const void* z, int flags,
                       void* y, float* final_state, int64_t batch, int64_t dim, int64_t seqlen,
                       int64_t dstate, int io_dtype, const float* init_state, int* status,
                       bool zero_status, void* carry, size_t carry_bytes, void* bwd_workspace,
-                      size_t bwd_workspace_bytes, bool train, cudaStream_t stream);
+                      size_t bwd_workspace_bytes, bool train, cudaStream_t stream,
+                      const int64_t* strides);
 
 // The smaller scratch limit that the failure-path test mode sets for the
 // no-allocation scan (0: none).

@@ -84,5 +84,5 @@ extern "C" int ssm_scan_fwd_noalloc(const void* u, const void* delta, const floa
   return ssm::scan_fwd_internal(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y,
                                 final_state, batch, dim, seqlen, dstate, io_dtype, init_state,
                                 nullptr, false, scratch, (size_t)SSM_STATIC_SCRATCH_BYTES, nullptr,
-                                0, false, st);
+                                0, false, st, nullptr);
 }

@@ -41,6 +41,7 @@
 #include <cuda.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -182,11 +183,13 @@ __device__ __forceinline__ void load_chunk_plain(const ScanArgs& p, unsigned cha
     // stage element e is (row r, step t): [r][t], or [t][r] for the (batch, L, dim) layout
     const int r = p.bld ? e % CH : e / T, t = p.bld ? e / CH : e - (e / T) * T;
     const bool ok = d0 + r < p.dim && t0 + t < p.L;
-    const int64_t gi = p.bld ? (b * p.L + t0 + t) * p.dim + d0 + r
-                             : ((b * p.dim + d0 + r) * p.L + t0 + t);
-    reinterpret_cast<IO*>(stage + S::oRawU)[e] = ok ? static_cast<const IO*>(p.u)[gi] : zero;
-    reinterpret_cast<IO*>(stage + S::oRawD)[e] = ok ? static_cast<const IO*>(p.delta)[gi] : zero;
-    if (has_z) reinterpret_cast<IO*>(stage + S::oRawZ)[e] = ok ? static_cast<const IO*>(p.z)[gi] : zero;
+    const int64_t dd = d0 + r, tt = t0 + t;
+    const int64_t iu = b * p.st_u[0] + dd * p.st_u[1] + tt * p.st_u[2];
+    const int64_t id = b * p.st_d[0] + dd * p.st_d[1] + tt * p.st_d[2];
+    const int64_t iz = b * p.st_z[0] + dd * p.st_z[1] + tt * p.st_z[2];
+    reinterpret_cast<IO*>(stage + S::oRawU)[e] = ok ? static_cast<const IO*>(p.u)[iu] : zero;
+    reinterpret_cast<IO*>(stage + S::oRawD)[e] = ok ? static_cast<const IO*>(p.delta)[id] : zero;
+    if (has_z) reinterpret_cast<IO*>(stage + S::oRawZ)[e] = ok ? static_cast<const IO*>(p.z)[iz] : zero;
   }
   for (int e = tid; e < N * T; e += kScanThreads) {
     const int n = e / T, t = e - n * T;
@@ -362,12 +365,12 @@ __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned
 #pragma unroll
     for (int j = 0; j < E; ++j) y[j] = fmaf(Dd, Ut[j], acc[j]) * gr[j];
   }
-  if (p.bld) {
-    // (batch, L, dim) layout: this row's steps are dim elements apart
+  if (!p.vec_y) {
+    // element stores: this row's steps are st_y[2] elements apart
     if (store && r < nrows) {
 #pragma unroll
       for (int j = 0; j < E; ++j)
-        if (WHOLE || te + j < tcount) dst[(int64_t)j * p.dim] = io_traits<IO>::from_f32(y[j]);
+        if (WHOLE || te + j < tcount) dst[(int64_t)j * p.st_y[2]] = io_traits<IO>::from_f32(y[j]);
     }
     return;
   }
@@ -376,7 +379,7 @@ __device__ __forceinline__ void finalize_share(const ScanArgs& p, const unsigned
     return;
   }
   if (!store || r >= nrows) return;
-  if (p.vec_io && te + E <= tcount) {
+  if (te + E <= tcount) {
     vecio<IO, E>::store(dst, y);
   } else {
 #pragma unroll
@@ -645,10 +648,10 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
   const int fr = tid / (T / Cf::E), fte = (tid - fr * (T / Cf::E)) * Cf::E;
   const int64_t fr_c = d0 + min(fr, nrows - 1);  // the finalised row's channel (clamped)
   IO* const y_base =
-      PASS == 0 ? static_cast<IO*>(p.y) + (p.bld ? (b * p.L + t_begin + fte) * p.dim + fr_c
-                                                 : (b * p.dim + fr_c) * p.L + t_begin + fte)
+      PASS == 0 ? static_cast<IO*>(p.y) + b * p.st_y[0] + fr_c * p.st_y[1] +
+                      (t_begin + fte) * p.st_y[2]
                 : nullptr;
-  const int64_t y_chunk = p.bld ? (int64_t)T * p.dim : (int64_t)T;  // y offset per chunk
+  const int64_t y_chunk = (int64_t)T * p.st_y[2];  // y offset per chunk
 
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(sm + S::oBar);
   uint64_t* iter_bar = raw_full + NS;
@@ -771,7 +774,7 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanArgs p,
     const int tcN = has_next ? tcount_of(i + 1) : 0;
     const int tcF = i > 0 ? tcount_of(i - 1) : T;
     // steady state: both neighbouring chunks whole and rows 16-byte aligned
-    const bool whole = (p.vec_io || p.bld) && tcN == T && tcF == T;
+    const bool whole = tcN == T && tcF == T;
     unsigned char* const bufM = sm + S::oBuf + bcur * S::kBuf;
     unsigned char* const bufN = sm + S::oBuf + bnext * S::kBuf;
     unsigned char* const bufF = sm + S::oBuf + bprev * S::kBuf;
@@ -924,13 +927,16 @@ static bool cfg_for(int64_t N, int& chans, int& chunk) {
 
 ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtype, int sm_count,
                    bool allow_split) {
-  (void)io_dtype;
   ScanPlan pl{1, L, 0, 16, 32};
   if (!cfg_for(N, pl.chans, pl.chunk)) return pl;
   pl.seg_len = L > 0 ? L : 1;
   if (!allow_split || L <= 0 || batch <= 0 || dim <= 0) return pl;
-  const int64_t blocks = ((dim + pl.chans - 1) / pl.chans) * batch;
-  const int64_t want = (int64_t)sm_count * 2;  // blocks that keep every SM busy
+  // units of work that run at once: the fast scan's 16-channel warps (N = 16,
+  // bf16; split when fewer than 4 per SM) or this kernel's blocks (2 per SM)
+  const bool fast = N == 16 && io_dtype == 1;
+  const int64_t unit = fast ? kFastChannels : pl.chans;
+  const int64_t blocks = ((dim + unit - 1) / unit) * batch;
+  const int64_t want = (int64_t)sm_count * (fast ? 4 : 2);
   if (blocks >= want) return pl;
   int64_t nseg = (want + blocks - 1) / blocks;
   const int64_t max_by_len = L / (32 * (int64_t)pl.chunk);  // at least 32 chunks per segment
@@ -967,13 +973,15 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a (d2, d1, d0) row-major tensor (d0 fastest) with box (1, b1, b0).
+// 3-D map over a (d2, d1, d0) tensor (d0 fastest, unit stride) with element strides
+// s1, s2 of d1, d2 (0: dense) and box (1, b1, b0).
 static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t esz,
-                     uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+                     uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+                     uint64_t s1 = 0, uint64_t s2 = 0) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !base) return false;
   const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * esz, d0 * d1 * esz};
+  const cuuint64_t strides[2] = {(s1 ? s1 : d0) * esz, (s2 ? s2 : d0 * d1) * esz};
   const cuuint32_t box[3] = {b0, b1, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -987,14 +995,17 @@ static bool make_maps(ScanMaps& m, const ScanArgs& a) {
   const CUtensorMapDataType dt =
       sizeof(IO) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const uint64_t L = (uint64_t)a.L, D = (uint64_t)a.dim, Bt = (uint64_t)a.batch;
-  // u/Δ/z: (batch, dim, L) with (T, CH) boxes, or (batch, L, dim) with (CH, T) boxes
+  // u/Δ/z: time-major (L, dim, batch) with (T, CH) boxes, or channel-major
+  // (dim, L, batch) with (CH, T) boxes; the strides of the outer two dimensions
   const uint64_t i0 = a.bld ? D : L, i1 = a.bld ? L : D;
   const uint32_t b0 = a.bld ? Cf::CH : Cf::T, b1 = a.bld ? Cf::T : Cf::CH;
-  bool ok = make_map(&m.u, a.u, dt, sizeof(IO), i0, i1, Bt, b0, b1) &&
-            make_map(&m.d, a.delta, dt, sizeof(IO), i0, i1, Bt, b0, b1) &&
+  const int o1 = a.bld ? 2 : 1;
+  bool ok = make_map(&m.u, a.u, dt, sizeof(IO), i0, i1, Bt, b0, b1, a.st_u[o1], a.st_u[0]) &&
+            make_map(&m.d, a.delta, dt, sizeof(IO), i0, i1, Bt, b0, b1, a.st_d[o1], a.st_d[0]) &&
             make_map(&m.b, a.B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, N, Bt, Cf::T, N) &&
             make_map(&m.c, a.C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, L, N, Bt, Cf::T, N);
-  if (ok && a.z) ok = make_map(&m.z, a.z, dt, sizeof(IO), i0, i1, Bt, b0, b1);
+  if (ok && a.z)
+    ok = make_map(&m.z, a.z, dt, sizeof(IO), i0, i1, Bt, b0, b1, a.st_z[o1], a.st_z[0]);
   return ok;
 }
 
@@ -1052,6 +1063,22 @@ static cudaError_t launch_io(const ScanArgs& a, int64_t N, cudaStream_t stream) 
   }
 }
 
+// Device address of the library-wide status word on the current device (cached
+// per device; null on error).
+static int* library_status_ptr() {
+  static std::mutex mu;
+  static int* ptrs[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_scan_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(q);
+  }
+  return ptrs[dev];
+}
+
 cudaError_t scan_launch(const ScanArgs& a, int64_t N, int io_dtype, const ScanPlan& plan,
                         cudaStream_t stream) {
   (void)plan;
@@ -1061,6 +1088,12 @@ cudaError_t scan_launch(const ScanArgs& a, int64_t N, int io_dtype, const ScanPl
     const int64_t n = a.batch * a.dim * N;
     copy_state_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a.final_state, a.init_state, n);
     return cudaGetLastError();
+  }
+  if (scan_fast_applies(a, N, io_dtype)) {
+    ScanArgs f = a;
+    if (!f.status) f.status = library_status_ptr();
+    if (!f.status) return cudaErrorInvalidValue;
+    return scan_fast_launch(f, stream);
   }
   if (io_dtype == 0) return launch_io<float>(a, N, stream);
   return launch_io<__nv_bfloat16>(a, N, stream);

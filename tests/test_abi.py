@@ -349,3 +349,33 @@ def test_ssd_bwd_argument_errors():
     assert call(wsb=1024) == ssm.SSM_ERR_WORKSPACE
     assert ssm.ssm_ssd_bwd_workspace_bytes(1, 64, 4, 64, 1, 64) > 0
     assert ssm.ssm_ssd_bwd_workspace_bytes(1, 64, 4, 64, 3, 64) == 0
+
+
+def _strided(strides, **kw):
+    import ctypes
+    a = dict(u=FAKE, delta=FAKE + 0x1000000, A=FAKE + 0x2000000, B=FAKE + 0x3000000,
+             C=FAKE + 0x4000000, z=FAKE + 0x6000000, softplus=1, y=FAKE + 0x5000000,
+             batch=2, dim=64, L=128, N=16, io=ssm.SSM_BF16)
+    a.update(kw)
+    st = None if strides is None else (ctypes.c_int64 * 12)(*strides)
+    return lib().ssm_scan_fwd_strided(a["u"], a["delta"], None, a["A"], a["B"], a["C"], None,
+                                      a["z"], a["softplus"], a["y"], None, a["batch"], a["dim"],
+                                      a["L"], a["N"], a["io"], st, None, None, 0, None)
+
+
+def test_strided_argument_errors():
+    dense = [64 * 128, 128, 1]
+    bld = [64 * 128, 1, 64]
+    # mixed orientations of u / delta / z are not supported
+    assert _strided(dense + bld + dense + dense) == ssm.SSM_ERR_UNSUPPORTED
+    # negative or zero strides over extents above one
+    assert _strided([-1, 128, 1] + dense * 3) == ssm.SSM_ERR_ARG
+    assert _strided(dense * 3 + [64 * 128, 0, 1]) == ssm.SSM_ERR_ARG
+    # y writing one element twice (channel and time strides that collide)
+    assert _strided(dense * 3 + [64 * 128, 1, 1]) == ssm.SSM_ERR_ARG
+    # the layout flag with strides
+    assert _strided(dense * 4, softplus=1 | ssm.SSM_LAYOUT_BLD) == ssm.SSM_ERR_ARG
+    # y overlapping u's span
+    assert _strided(dense * 4, y=FAKE + 0x200) == ssm.SSM_ERR_ARG
+    # empty problems succeed without touching the device
+    assert _strided(dense * 4, batch=0) == ssm.SSM_OK
