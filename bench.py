@@ -320,7 +320,7 @@ def bench_scan(w, steps, warmup, world, e2e=True, clocks=True):
 # the million-length sequence: 16 launches with the fp32 state carried
 # ---------------------------------------------------------------------------
 
-def bench_million(w, reps, world, cpu=True):
+def bench_million(w, reps, world, cpu=True, launches=None):
     """The million-length workload as w.launches launches of L / launches steps, each
     starting from the previous launch's fp32 final state; the whole loop is timed.
 
@@ -332,8 +332,8 @@ def bench_million(w, reps, world, cpu=True):
     a sample of channels of the same inputs, over the whole length."""
     import torch
     import selective_state_space_128_b300 as ssm
-    K = w.launches
-    Lc = w.seqlen // K
+    Lc = w.seqlen // w.launches
+    K = w.launches if launches is None else max(1, min(w.launches, launches))
     gen = torch.Generator(device="cuda")
     gen.manual_seed(1000 + w.seed)
     bf = torch.bfloat16
@@ -811,7 +811,7 @@ def workload_config(w):
                   % (scan_bytes(w) / 1e6)}
 
 
-def scan_roofline(w, ms_per_launch, hbm_peak, sm_max, peak_kind, traffic_key):
+def scan_roofline(w, ms_per_launch, hbm_peak, sm_max, peak_kind, traffic_key, kernel):
     """Roofline of one scan launch on workload w: the method's FP32 operations against
     the FP32 lanes (the bound) and its algorithmic bytes against the HBM copy peak."""
     step_s = ms_per_launch / 1e3
@@ -822,7 +822,7 @@ def scan_roofline(w, ms_per_launch, hbm_peak, sm_max, peak_kind, traffic_key):
     gbs = nbytes / step_s / 1e9
     return {"bound": "alu", "achieved": alu_ach, "peak": alu_peak, "unit": "TOP/s",
             "frac": alu_ach / alu_peak, "traffic": profiled_traffic(traffic_key),
-            "kernel": "scan_kernel<bf16,16,0>", "ops_per_launch": ops,
+            "kernel": kernel, "ops_per_launch": ops,
             "peak_basis": "148 SMs x 128 FP32 lanes x %.0f MHz (max SM clock)" % sm_max,
             "hbm_achieved_gbs": gbs, "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peak_kind,
             "hbm_frac": gbs / hbm_peak, "algorithmic_bytes_per_launch": nbytes}
@@ -843,6 +843,8 @@ def main():
     ap.add_argument("--no-ssd", action="store_true")
     ap.add_argument("--no-million", action="store_true")
     ap.add_argument("--million-reps", type=int, default=3)
+    ap.add_argument("--million-launches", type=int, default=None,
+                    help="time only the first K of the 16 launches (for profiling a smaller case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = synth.MAMBA_2P8B          # the headline: the largest single-launch workload
@@ -868,9 +870,10 @@ def main():
     bld_ms = bench_scan_bld(w1, r1["inputs"], 50, args.warmup, world)
     r1.pop("inputs")
     torch.cuda.empty_cache()
-    mil = None if args.no_million else bench_million(wm, max(3, args.million_reps), world,
+    mil = None if args.no_million else bench_million(wm, max(1, args.million_reps), world,
                                                     cpu=(rank == 0 and world == 1
-                                                         and not args.no_cpu))
+                                                         and not args.no_cpu),
+                                                    launches=args.million_launches)
     torch.cuda.empty_cache()
     conv = None if args.no_conv else bench_conv(w1, 50, args.warmup, world)
     ssd = None if args.no_ssd else bench_ssd(20, args.warmup, world)
@@ -894,7 +897,8 @@ def main():
                 "peak_kind": peak_kind, "frac_of_8000_nominal": gbs_rank / 8000.0,
                 "bytes_per_step": nbytes},
         "roofline": scan_roofline(w, r["ms"] / args.steps, hbm_peak, sm_max, peak_kind,
-                                  "scan_kernel@" + w.name),
+                                  "scan_kernel@" + w.name,
+                                  "scan_fast_kernel<4,0> (the warp kernel: 8 channels a warp)"),
         "e2e": {"value": nbytes * r["e2e_steps"] / (r["e2e_ms"] / 1e3) / 1e9 * world,
                 "unit": "GB/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "steps": r["e2e_steps"],
@@ -913,17 +917,19 @@ def main():
         "us_per_step": s1 * 1e6, "channel_steps_per_s": w1.channel_steps / s1 * world,
         "hbm_gbs": scan_bytes(w1) / s1 / 1e9, "hbm_frac": scan_bytes(w1) / s1 / 1e9 / hbm_peak,
         "roofline": scan_roofline(w1, s1 * 1e3, hbm_peak, sm_max, peak_kind,
-                                  "scan_kernel@" + w1.name),
+                                  "scan_kernel@" + w1.name,
+                                  "scan_kernel<bf16,16,0> (the block kernel: 32 channels a block)"),
         "gpu_launches": n1 * r1["launches_per_step"]}
     if mil is not None:
         ls = mil["loop_ms"] / 1e3
-        mb = scan_bytes(wm) + (wm.launches - 1) * 4 * wm.batch * wm.dim * wm.dstate
+        part = mil["launches"] / wm.launches   # 1 unless a prefix of the loop was timed
+        mb = (scan_bytes(wm) + (wm.launches - 1) * 4 * wm.batch * wm.dim * wm.dstate) * part
         mo = {"workload": wm.name, "config": dict(workload_config(wm), launches=mil["launches"],
                                                    chunk_len=mil["chunk_len"],
                                                    l2="13 GB of chunk inputs and outputs, far "
                                                       "larger than L2"),
               "reps": mil["reps"], "ms_per_loop": mil["loop_ms"],
-              "channel_steps_per_s": wm.channel_steps / ls * world,
+              "channel_steps_per_s": wm.channel_steps * part / ls * world,
               "hbm_gbs": mb / ls / 1e9, "hbm_frac": mb / ls / 1e9 / hbm_peak,
               "bytes_per_loop": mb,
               "kernels_per_launch": mil["kernels_per_launch"],
@@ -934,7 +940,7 @@ def main():
               "e2e": {"value": mb / (mil["e2e_ms"] / 1e3) / 1e9 * world, "unit": "GB/s",
                       "h2d_bytes_per_loop": mil["h2d"], "d2h_bytes_per_loop": mil["d2h"],
                       "call": "ssm_scan_fwd_host per launch, state carried in host memory"}}
-        ops = fp32_ops_per_channel_step(wm.dstate) * wm.channel_steps
+        ops = fp32_ops_per_channel_step(wm.dstate) * wm.channel_steps * part
         alu_peak = 148 * 128 * sm_max * 1e6 / 1e12
         mo["roofline"] = {"bound": "alu", "achieved": ops / ls / 1e12, "peak": alu_peak,
                           "unit": "TOP/s", "frac": ops / ls / 1e12 / alu_peak,

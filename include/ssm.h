@@ -234,18 +234,24 @@ int ssm_scan_fwd_host(const void* u, const void* delta, const float* delta_bias,
 int ssm_status(const void* workspace, void* stream);
 
 /*
- * Failure-path test mode (the pages have no counterpart).  enable = 1 turns it
- * on: ssm_scan_fwd_ex then accepts SSM_TEST_STALL, which makes block (0, 0) of
- * the call's output pass arm the barrier of its second chunk's copy without
- * issuing the copy, so that block's waits give up after wait_limit_ns (1e3 ..
- * 2e9) instead of 2 s; the call's status word then reads SSM_ERR_TIMEOUT.  It
- * needs a sequence of at least two 16-step chunks with 16-byte rows (the copy
- * path the wait belongs to).  noalloc_limit_bytes > 0 lowers the scratch limit
- * of ssm_scan_fwd_noalloc to that many bytes, so that its refusal can be
- * tested.  enable = 0 restores the defaults.  Process-wide; for tests only.
- * Returns SSM_OK, or SSM_ERR_ARG for a limit out of range.
+ * Test mode (the pages have no counterpart).  enable = 1 turns it on:
+ *   - ssm_scan_fwd_ex accepts SSM_TEST_STALL, which makes the first block (or
+ *     warp) of the call's output pass arm the barrier of its second chunk's
+ *     copy without issuing the copy, so its waits give up after wait_limit_ns
+ *     (1e3 .. 2e9) instead of 2 s; the call's status word then reads
+ *     SSM_ERR_TIMEOUT.  It needs a sequence of at least two 16-step chunks with
+ *     16-byte rows (the copy path the wait belongs to);
+ *   - noalloc_limit_bytes > 0 lowers the scratch limit of ssm_scan_fwd_noalloc
+ *     to that many bytes, so that its refusal can be tested;
+ *   - scan_kernel picks the forward scan's kernel: 0 = by size (the default),
+ *     1 = the block kernel, 2 = the warp kernel wherever it applies (N = 16,
+ *     bf16, zero-order hold, views TMA can stage), so that both can be tested
+ *     on small sizes.
+ * enable = 0 restores the defaults.  Process-wide; for tests and tuning only.
+ * Returns SSM_OK, or SSM_ERR_ARG for an argument out of range.
  */
-int ssm_set_test_mode(int enable, int64_t wait_limit_ns, int64_t noalloc_limit_bytes);
+int ssm_set_test_mode(int enable, int64_t wait_limit_ns, int64_t noalloc_limit_bytes,
+                      int scan_kernel);
 
 /*
  * One-token decode: the recurrent mode of the summary page's equation (2)

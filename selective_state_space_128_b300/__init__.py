@@ -67,7 +67,7 @@ def load():
     lib.ssm_scan_fwd_noalloc.restype = i32
     lib.ssm_status.argtypes = [vp, vp]
     lib.ssm_status.restype = i32
-    lib.ssm_set_test_mode.argtypes = [i32, i64, i64]
+    lib.ssm_set_test_mode.argtypes = [i32, i64, i64, i32]
     lib.ssm_set_test_mode.restype = i32
     lib.ssm_scan_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
     lib.ssm_scan_bwd_workspace_bytes.restype = sz
@@ -291,10 +291,16 @@ def ssm_status(workspace=None, stream=None) -> int:
     return int(load().ssm_status(_ptr(workspace), _stream(stream)))
 
 
-def ssm_set_test_mode(enable, wait_limit_ns=1000000, noalloc_limit_bytes=0) -> None:
-    """Tensor-free form of ``ssm_set_test_mode`` (the failure-path test mode)."""
+SCAN_KERNEL_AUTO, SCAN_KERNEL_BLOCK, SCAN_KERNEL_WARP = 0, 1, 2
+
+
+def ssm_set_test_mode(enable, wait_limit_ns=1000000, noalloc_limit_bytes=0,
+                      scan_kernel=SCAN_KERNEL_AUTO) -> None:
+    """Form of ``ssm_set_test_mode`` (the test mode: failure path, scratch limit,
+    forward scan kernel choice)."""
     _call("ssm_set_test_mode", load().ssm_set_test_mode(int(bool(enable)), int(wait_limit_ns),
-                                                        int(noalloc_limit_bytes)))
+                                                        int(noalloc_limit_bytes),
+                                                        int(scan_kernel)))
 
 
 def ssm_state_update(state, u, delta, A, B, C, D, z, y):

@@ -64,6 +64,7 @@ bool flags_ok(int f) { return (f & ~(SSM_SOFTPLUS | SSM_EULER_B)) == 0; }
 std::atomic<int> g_test_mode{0};
 std::atomic<int64_t> g_test_limit_ns{1000000};
 std::atomic<int64_t> g_test_noalloc_limit{0};
+std::atomic<int> g_test_scan_kernel{0};  // 0: by size, 1: the block kernel, 2: the warp kernel
 
 bool sizes_ok(int64_t batch, int64_t dim, int64_t seqlen) {
   // every flat index must fit in int64 with room to spare
@@ -100,11 +101,14 @@ size_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int6
   return ssm::kScanStatusBytes + ssm::scan_carry_bytes(batch, dim, seqlen, dstate, io_dtype);
 }
 
-int ssm_set_test_mode(int enable, int64_t wait_limit_ns, int64_t noalloc_limit_bytes) {
-  if (enable && (wait_limit_ns < 1000 || wait_limit_ns > 2000000000 || noalloc_limit_bytes < 0))
+int ssm_set_test_mode(int enable, int64_t wait_limit_ns, int64_t noalloc_limit_bytes,
+                      int scan_kernel) {
+  if (enable && (wait_limit_ns < 1000 || wait_limit_ns > 2000000000 || noalloc_limit_bytes < 0 ||
+                 scan_kernel < 0 || scan_kernel > 2))
     return SSM_ERR_ARG;
   g_test_limit_ns.store(enable ? wait_limit_ns : 1000000);
   g_test_noalloc_limit.store(enable ? noalloc_limit_bytes : 0);
+  g_test_scan_kernel.store(enable ? scan_kernel : 0);
   g_test_mode.store(enable ? 1 : 0);
   return SSM_OK;
 }
@@ -175,6 +179,8 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
   a.batch = batch; a.L = seqlen; a.H = nheads; a.G = ngroups; a.nch = lay.nch;
   a.softplus = (flags & SSM_SOFTPLUS) != 0;
   a.euler = (flags & SSM_EULER_B) != 0;
+  a.status = ssm::library_status_word();
+  if (!a.status) return SSM_ERR_CUDA;
   const cudaError_t e = ssm::ssd_launch(a, dstate, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
@@ -184,6 +190,7 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
 namespace ssm {
 
 size_t noalloc_test_limit() { return (size_t)g_test_noalloc_limit.load(); }
+int scan_kernel_choice() { return g_test_scan_kernel.load(); }
 
 size_t scan_carry_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype) {
   return scan_plan(batch, dim, seqlen, dstate, io_dtype, sm_count_current(), true).workspace_bytes;
@@ -265,7 +272,7 @@ int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias,
   float* ckpt = nullptr;
   int64_t ckpt_nch = 0;
   if (train && seqlen > 0) {
-    const ssm::BwdLayout lay = ssm::bwd_layout(batch, dim, seqlen, dstate);
+    const ssm::BwdLayout lay = ssm::bwd_layout(batch, dim, seqlen, dstate, sm_count_current());
     if (!bwd_workspace || bwd_workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
     const void* others[] = {u, delta, z, y, carry, status};
     const size_t sizes[] = {nio_u, nio_d, nio_z, nio, plan.workspace_bytes, sizeof(int)};
@@ -475,7 +482,7 @@ int ssm_state_update(float* state, const void* u, const void* delta, const float
 size_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
   if (!supported_bwd_n(dstate) || !sizes_ok(batch, dim, seqlen)) return 0;
   if (batch == 0 || dim == 0 || seqlen == 0) return 0;
-  return ssm::bwd_layout(batch, dim, seqlen, dstate).bytes;
+  return ssm::bwd_layout(batch, dim, seqlen, dstate, sm_count_current()).bytes;
 }
 
 int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, const float* A,
@@ -517,7 +524,7 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
     for (size_t j = i + 1; j < sizeof outs / sizeof outs[0]; ++j)
       if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return SSM_ERR_ARG;
   }
-  const ssm::BwdLayout lay = ssm::bwd_layout(batch, dim, seqlen, dstate);
+  const ssm::BwdLayout lay = ssm::bwd_layout(batch, dim, seqlen, dstate, sm_count_current());
   if (steps) {
     if (!workspace || workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
     for (const Span& q : outs)
@@ -562,6 +569,37 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* delta_bias, cons
   a.softplus = (delta_softplus & SSM_SOFTPLUS) != 0;
   a.euler = (delta_softplus & SSM_EULER_B) != 0;
   a.force_precise = io_dtype == SSM_F32;
+  a.nseg = lay.nseg;
+  a.seg_len = lay.seg_len;
+  if (lay.nseg > 1) {
+    a.fcarry_h = reinterpret_cast<float*>(ws + lay.o_fh);
+    a.fcarry_s = reinterpret_cast<float*>(ws + lay.o_fs);
+    a.acarry_l = reinterpret_cast<float*>(ws + lay.o_al);
+    a.acarry_s = reinterpret_cast<float*>(ws + lay.o_as);
+    if (!a.saved) {
+      // the forward's segment carries: the scan's first pass over the same
+      // segments (its bounded waits report to the library-wide status word)
+      ssm::ScanArgs f{};
+      f.u = u; f.delta = delta; f.z = nullptr; f.bias = delta_bias; f.A = A; f.B = B; f.C = C;
+      f.batch = batch; f.dim = dim; f.L = seqlen;
+      f.nseg = lay.nseg; f.seg_len = lay.seg_len;
+      f.carry_h = a.fcarry_h; f.carry_s = a.fcarry_s;
+      f.softplus = a.softplus; f.euler = a.euler; f.force_precise = a.force_precise;
+      f.bld = a.bld;
+      for (int k = 0; k < 4; ++k) {
+        int64_t* t = k == 0 ? f.st_u : k == 1 ? f.st_d : k == 2 ? f.st_z : f.st_y;
+        t[0] = dim * seqlen;
+        t[1] = a.bld ? 1 : seqlen;
+        t[2] = a.bld ? dim : 1;
+      }
+      const int64_t o = a.bld ? dim : seqlen;  // the stride other than the unit one
+      f.vec_io = (o * (int64_t)esz) % 16 == 0 && (dim * seqlen * (int64_t)esz) % 16 == 0;
+      f.vec_bc = (seqlen * 4) % 16 == 0;
+      f.test_limit_ns = 0;
+      const cudaError_t ef = ssm::scan_carries_launch(f, dstate, io_dtype, st);
+      if (ef != cudaSuccess) return SSM_ERR_CUDA;
+    }
+  }
   const cudaError_t e = ssm::bwd_launch(a, dstate, io_dtype, st);
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }

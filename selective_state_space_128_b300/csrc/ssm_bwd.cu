@@ -41,6 +41,8 @@
 namespace ssm {
 
 constexpr int kBwdThreads = 128;
+// Shortest segment of a sequence split across blocks (steps).
+constexpr int64_t kBwdMinSeg = 512;
 
 template <int N> struct BwdCfg {
   // states per lane: at most 16 (N = 128 spreads over 8 lanes of a channel)
@@ -220,6 +222,11 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
   const int nrows = (int)min64(CH, p.dim - d0);
   const int64_t L = p.L;
   const int nch = (int)((L + T - 1) / T);
+  // this block's segment of the sequence: chunks [k_begin, k_end)
+  const int seg = blockIdx.z;
+  // (a split plan's segments are whole chunks; the last one ends with the sequence)
+  const int k_begin = (int)((int64_t)seg * (p.seg_len / T));
+  const int k_end = seg == p.nseg - 1 ? nch : (int)min64(nch, (int64_t)(seg + 1) * (p.seg_len / T));
   // this thread's row and steps in the per-step (cooperative) phases
   const int r = tid / TPR, te = (tid % TPR) * E;
   const bool row_ok = r < nrows;
@@ -371,15 +378,25 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
 #pragma unroll
   for (int j = 0; j < NPT; ++j)
     h[j] = (p.init_state && chan_ok) ? p.init_state[(b * p.dim + d) * N + g * NPT + j] : 0.f;
+  if (chan_ok && !p.saved) {
+    // earlier segments: h <- exp(A ΣΔ_k) h + (segment k's end state from zero)
+    const int64_t row = b * p.dim + d;
+    for (int k = 0; k < seg; ++k) {
+      const float sk = p.fcarry_s[(int64_t)k * p.batch * p.dim + row];
+      const float* hk = p.fcarry_h + ((int64_t)k * p.batch * p.dim + row) * N + g * NPT;
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) h[j] = fmaf(expf(sk * Aj[j]), h[j], hk[j]);
+    }
+  }
   if constexpr (PAIRS) {
 #pragma unroll
     for (int q = 0; q < NP; ++q) hq[q] = pack2(h[2 * q], h[2 * q + 1]);
   }
   float dyv[E], zz[E], sg[E];
   BwdPre<N> pre;
-  const int nch1 = p.saved ? 0 : nch;  // a training forward already saved them
-  if (nch1 > 0) fetch(0, false, pre);
-  for (int k = 0; k < nch1; ++k) {
+  const int k1 = p.saved ? k_begin : k_end;  // a training forward already saved them
+  if (k_begin < k1) fetch(k_begin, false, pre);
+  for (int k = k_begin; k < k1; ++k) {
     if (fast_pairs) {
 #pragma unroll
       for (int q = 0; q < NP; ++q) unpack2(hq[q], h[2 * q], h[2 * q + 1]);
@@ -389,7 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
       sts_vec<NPT>(cp, h);  // (a global store; sts_vec only packs the vector)
     }
     stage(k, false, pre, dyv, zz, sg);
-    if (k + 1 < nch1) fetch(k + 1, false, pre);
+    if (k + 1 < k1) fetch(k + 1, false, pre);
     __syncthreads();
     const float* rDT = sDT + c * Cf::RowF;
     const float* rU = sU + c * Cf::RowF;
@@ -431,6 +448,17 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
     lam[j] = (p.d_final_state && chan_ok) ? p.d_final_state[(b * p.dim + d) * N + g * NPT + j] : 0.f;
     dAacc[j] = 0.f;
   }
+  if (chan_ok) {
+    // later segments, from the last: λ <- (segment k's adjoint at its start from
+    // a zero adjoint at its end) + exp(A ΣΔ_k) λ
+    const int64_t row = b * p.dim + d;
+    for (int k = p.nseg - 1; k > seg; --k) {
+      const float sk = p.acarry_s[(int64_t)(k - 1) * p.batch * p.dim + row];
+      const float* lk = p.acarry_l + ((int64_t)(k - 1) * p.batch * p.dim + row) * N + g * NPT;
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) lam[j] = fmaf(expf(sk * Aj[j]), lam[j], lk[j]);
+    }
+  }
   if constexpr (PAIRS) {
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
@@ -446,15 +474,15 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
   // part rq), VPT of them, and its share `part` of the channels
   const int part = tid % Cf::RS;
 
-  if (nch > 0) fetch(nch - 1, true, pre);
-  for (int k = nch - 1; k >= 0; --k) {
+  if (k_begin < k_end) fetch(k_end - 1, true, pre);
+  for (int k = k_end - 1; k >= k_begin; --k) {
     const int64_t t0 = (int64_t)k * T;
     const int tc = (int)min64(T, L - t0);
     // P1: stage the chunk; the next (earlier) chunk's loads go in flight
     stage(k, true, pre, dyv, zz, sg);
 #pragma unroll
     for (int j = 0; j < NPT; ++j) h[j] = pre.h[j];
-    if (k > 0) fetch(k - 1, true, pre);
+    if (k > k_begin) fetch(k - 1, true, pre);
     const float* rDT = sDT + c * Cf::RowF;
     const float* rU = sU + c * Cf::RowF;
     const float* rDS = sDS + c * Cf::RowF;
@@ -804,12 +832,14 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
       unpack2(kCarryH ? fma2(dA2q[q], iAp[q], dAq[q]) : dAq[q], dAacc[2 * q], dAacc[2 * q + 1]);
     }
   }
+  // this segment's slices of the per-batch-row sums; d init_state from the first
+  const int64_t segoff = (int64_t)seg * p.batch * p.dim;
   if (chan_ok) {
     const int64_t st = (b * p.dim + d) * N + g * NPT;
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
-      p.ws_A[st + j] = dAacc[j];
-      if (p.d_init_state) p.d_init_state[st + j] = lam[j];
+      p.ws_A[segoff * N + st + j] = dAacc[j];
+      if (p.d_init_state && seg == 0) p.d_init_state[st + j] = lam[j];
     }
   }
 #pragma unroll
@@ -818,13 +848,173 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
     dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, s);
   }
   if (te == 0 && row_ok) {
-    p.ws_D[b * p.dim + d0 + r] = dD_acc;
-    p.ws_bias[b * p.dim + d0 + r] = dbias_acc;
+    p.ws_D[segoff + b * p.dim + d0 + r] = dD_acc;
+    p.ws_bias[segoff + b * p.dim + d0 + r] = dbias_acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Adjoint carries of a split sequence
+// ---------------------------------------------------------------------------
+// The adjoint is linear in what enters a segment from the right: leaving segment
+// k it is (Π_t Ā_t) λ_in + l_k with Π_t Ā_t = exp(A ΣΔ_k), where l_k is what
+// leaves when λ_in = 0.  This kernel computes l_k and ΣΔ_k for segments 1 ..
+// nseg-1 (index k-1 of acarry_l / acarry_s); the backward kernel of segment s
+// starts from d final_state folded through segments nseg-1 .. s+1.  Each step,
+// from a segment's last to its first, is the adjoint sweep's own: λ += ds_t C_t,
+// then λ *= Ā_t.  The lane layout is the backward kernel's (G lanes of NPT
+// states per channel, CH channels a block); a chunk of TT steps of Δ and ds is
+// staged per channel in shared memory, C per step, the next chunk's raw inputs
+// in flight in registers meanwhile.
+template <int N> struct AdjCfg {
+  using Cf = BwdCfg<N>;
+  static constexpr int NPT = Cf::NPT, G = Cf::G, CH = Cf::CH;
+  // steps per chunk: at most 8 channel steps of each input and 16 floats of C a thread
+  static constexpr int TT = (1024 / CH < 2048 / N) ? 1024 / CH : 2048 / N;
+  static constexpr int E = CH * TT / kBwdThreads;   // channel steps a thread loads
+  static constexpr int TPR = TT / E;                // threads per channel row
+  static constexpr int PER = (TT * N + kBwdThreads - 1) / kBwdThreads;
+  static constexpr int RowF = TT + 1;
+  static_assert(E >= 1 && E <= 8 && TPR * E == TT && PER <= 16, "tiling");
+};
+
+template <typename IO, int N>
+__global__ void __launch_bounds__(kBwdThreads) adjoint_carry_kernel(const BwdArgs p) {
+  using Cf = AdjCfg<N>;
+  constexpr int NPT = Cf::NPT, CH = Cf::CH, TT = Cf::TT, E = Cf::E, TPR = Cf::TPR, PER = Cf::PER;
+  __shared__ float sDT[CH * Cf::RowF];
+  __shared__ float sDS[CH * Cf::RowF];
+  __shared__ __align__(16) float sC[TT * N];
+  __shared__ float sBias[CH];
+
+  const int tid = threadIdx.x;
+  const int g = tid / CH, c = tid % CH;  // a warp: consecutive channels of one state group
+  const int64_t b = blockIdx.y;
+  const int64_t d0 = (int64_t)blockIdx.x * CH;
+  const int64_t d = d0 + c;
+  const bool chan_ok = d < p.dim;
+  const int nrows = (int)min64(CH, p.dim - d0);
+  const int64_t L = p.L;
+  const int seg = blockIdx.z + 1;
+  const int64_t s0 = (int64_t)seg * p.seg_len;
+  const int64_t s1 = min64(L, s0 + p.seg_len);
+  const int nck = (int)((s1 - s0 + TT - 1) / TT);
+  // loads: channel rows of L steps (E consecutive steps a thread), or steps dim
+  // apart in (batch, L, dim) (consecutive channels across a warp)
+  const bool bld = p.bld != 0;
+  const int r = bld ? tid % CH : tid / TPR;
+  const int te = bld ? (tid / CH) * E : (tid % TPR) * E;
+  const bool row_ok = r < nrows;
+  const int64_t io_row = bld ? b * L * p.dim + d0 + (row_ok ? r : 0)
+                             : (b * p.dim + d0 + (row_ok ? r : 0)) * L;
+  const int64_t io_ts = bld ? p.dim : 1;
+  constexpr int kVecBytes = (sizeof(IO) == 2 && E == 4) ? 8 : 16;
+  const bool vec = !bld && E % 4 == 0 && (L * (int64_t)sizeof(IO)) % kVecBytes == 0;
+
+  for (int i = tid; i < CH; i += kBwdThreads)
+    sBias[i] = (p.bias && d0 + i < p.dim) ? p.bias[d0 + i] : 0.f;
+  float Aj[NPT], A2[NPT];
+  bool zeroA = false;
+#pragma unroll
+  for (int j = 0; j < NPT; ++j) {
+    Aj[j] = chan_ok ? p.A[d * N + g * NPT + j] : -1.f;
+    A2[j] = Aj[j] * kLog2e;
+    zeroA |= Aj[j] == 0.f;
+  }
+  // the flavour of the backward kernel's adjoint sweep (block-uniform)
+  const bool precise = __syncthreads_or(zeroA) || p.force_precise || p.euler;
+  const bool sp = p.softplus != 0;
+
+  float rdl[E], rdy[E], rz[E], rc[PER];
+  auto fetch = [&](int kk) {
+    const int64_t t0 = s0 + (int64_t)kk * TT;
+    const int tc = (int)min64(TT, s1 - t0);
+    const int64_t gi = io_row + (t0 + te) * io_ts;
+    bool done = false;
+    if constexpr (E % 4 == 0) {
+      if (row_ok && vec && te + E <= tc) {
+        vecio<IO, E>::load(static_cast<const IO*>(p.delta) + gi, rdl);
+        vecio<IO, E>::load(static_cast<const IO*>(p.dy) + gi, rdy);
+        if (p.z) vecio<IO, E>::load(static_cast<const IO*>(p.z) + gi, rz);
+        done = true;
+      }
+    }
+    if (!done) {
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const bool ok = row_ok && te + j < tc;
+        const int64_t gj = gi + j * io_ts;
+        rdl[j] = ok ? ld_io<IO>(p.delta, gj) : 0.f;
+        rdy[j] = ok ? ld_io<IO>(p.dy, gj) : 0.f;
+        rz[j] = (ok && p.z) ? ld_io<IO>(p.z, gj) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = tid + i * kBwdThreads;  // (n, t) of the chunk's C tile
+      const int n = e / TT, t = e - n * TT;
+      const bool ok = (TT * N % kBwdThreads == 0 || e < TT * N) && t < tc;
+      rc[i] = ok ? p.C[(b * N + n) * L + t0 + t] : 0.f;
+    }
+  };
+
+  float lam[NPT];
+#pragma unroll
+  for (int j = 0; j < NPT; ++j) lam[j] = 0.f;
+  float sdt = 0.f;
+  if (nck > 0) fetch(nck - 1);
+  for (int kk = nck - 1; kk >= 0; --kk) {
+    const int64_t t0 = s0 + (int64_t)kk * TT;
+    const int tc = (int)min64(TT, s1 - t0);
+    __syncthreads();  // the previous chunk's readers are done
+    {
+      const float bias = sBias[r];
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const bool ok = row_ok && te + j < tc;
+        const float x = rdl[j] + bias;
+        const float dt = sp ? (precise ? softplus_precise(x) : softplus_fast(x)) : x;
+        const float gate = p.z ? (precise ? silu_precise(rz[j]) : silu_fast(rz[j])) : 1.f;
+        sDT[r * Cf::RowF + te + j] = ok ? dt : 0.f;
+        sDS[r * Cf::RowF + te + j] = ok ? rdy[j] * gate : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int e = tid + i * kBwdThreads;
+        if (TT * N % kBwdThreads == 0 || e < TT * N) {
+          const int n = e / TT, t = e - n * TT;
+          sC[t * N + n] = rc[i];
+        }
+      }
+    }
+    __syncthreads();
+    if (kk > 0) fetch(kk - 1);
+    const float* rDT = sDT + c * Cf::RowF;
+    const float* rDS = sDS + c * Cf::RowF;
+#pragma unroll 4
+    for (int t = TT - 1; t >= 0; --t) {
+      const float dt = rDT[t], ds = rDS[t];
+      float Cv[NPT];
+      lds_vec<NPT>(sC + t * N + g * NPT, Cv);
+      sdt += dt;
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) {
+        lam[j] = fmaf(ds, Cv[j], lam[j]);
+        lam[j] *= precise ? expf(dt * Aj[j]) : ex2_fast(dt * A2[j]);
+      }
+    }
+  }
+  if (chan_ok) {
+    const int64_t row = b * p.dim + d;
+    const int64_t o = (int64_t)(seg - 1) * p.batch * p.dim + row;
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) p.acarry_l[o * N + g * NPT + j] = lam[j];
+    if (g == 0) p.acarry_s[o] = sdt;
   }
 }
 
 // Adds the per-block partial sums in a fixed order: dB, dC over the channel
-// blocks of each batch row; dA, dD, dbias over the batch.
+// blocks of each batch row; dA, dD, dbias over the segments and the batch.
 __global__ void bwd_reduce_kernel(const BwdArgs p, int64_t N) {
   const int64_t nbc = p.batch * N * p.L;
   const int64_t nA = p.dim * N;
@@ -842,7 +1032,7 @@ __global__ void bwd_reduce_kernel(const BwdArgs p, int64_t N) {
     } else if (i < 2 * nbc + nA) {
       const int64_t e = i - 2 * nbc;              // (d, n)
       float s = 0.f;
-      for (int64_t bb = 0; bb < p.batch; ++bb) s += p.ws_A[bb * nA + e];
+      for (int64_t sb = 0; sb < p.nseg * p.batch; ++sb) s += p.ws_A[sb * nA + e];
       p.dA[e] = s;
     } else {
       const int64_t e = i - 2 * nbc - nA;
@@ -852,7 +1042,7 @@ __global__ void bwd_reduce_kernel(const BwdArgs p, int64_t N) {
       if (!out) continue;
       const float* ws = isBias ? p.ws_bias : p.ws_D;
       float s = 0.f;
-      for (int64_t bb = 0; bb < p.batch; ++bb) s += ws[bb * p.dim + dd];
+      for (int64_t sb = 0; sb < p.nseg * p.batch; ++sb) s += ws[sb * p.dim + dd];
       out[dd] = s;
     }
   }
@@ -896,17 +1086,58 @@ int bwd_chunk(int64_t N) {
   }
 }
 
-BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t L, int64_t N) {
+// Resident backward blocks per SM (the kernel's launch bound).
+static int bwd_resident(int64_t N) {
+  switch (N) {
+    case 1: return BwdCfg<1>::MINB;
+    case 2: return BwdCfg<2>::MINB;
+    case 4: return BwdCfg<4>::MINB;
+    case 8: return BwdCfg<8>::MINB;
+    case 16: return BwdCfg<16>::MINB;
+    case 32: return BwdCfg<32>::MINB;
+    case 64: return BwdCfg<64>::MINB;
+    case 128: return BwdCfg<128>::MINB;
+    default: return 1;
+  }
+}
+
+BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t L, int64_t N, int sm_count) {
   BwdLayout w{};
   if (!bwd_geometry(N, dim, L, w.nblk, w.nch)) return w;
+  // Split the sequence when the (channel block, batch row) blocks fill less than
+  // half of one wave of resident blocks: segments of at least kBwdMinSeg steps,
+  // a multiple of 16 (the forward's and every backward chunk length), at most 64.
+  w.nseg = 1;
+  w.seg_len = L > 0 ? L : 1;
+  const int64_t blocks = w.nblk * batch;
+  const int64_t wave = (int64_t)sm_count * bwd_resident(N);
+  if (L > 0 && blocks > 0 && 2 * blocks <= wave) {
+    int64_t nseg = (wave + blocks - 1) / blocks;
+    if (nseg > L / kBwdMinSeg) nseg = L / kBwdMinSeg;
+    if (nseg > 64) nseg = 64;
+    if (nseg >= 2) {
+      int64_t seg_len = (L + nseg - 1) / nseg;
+      seg_len = (seg_len + 15) / 16 * 16;
+      nseg = (L + seg_len - 1) / seg_len;
+      if (nseg >= 2) {
+        w.nseg = (int)nseg;
+        w.seg_len = seg_len;
+      }
+    }
+  }
   const size_t B_ = (size_t)batch, D_ = (size_t)dim, N_ = (size_t)N, L_ = (size_t)L;
+  const size_t S_ = (size_t)w.nseg, rows = B_ * D_;
   w.o_ckpt = 0;
   w.o_B = w.o_ckpt + al256(B_ * (size_t)w.nch * D_ * N_ * 4);
   w.o_C = w.o_B + al256(B_ * (size_t)w.nblk * N_ * L_ * 4);
   w.o_A = w.o_C + al256(B_ * (size_t)w.nblk * N_ * L_ * 4);
-  w.o_D = w.o_A + al256(B_ * D_ * N_ * 4);
-  w.o_bias = w.o_D + al256(B_ * D_ * 4);
-  w.bytes = w.o_bias + al256(B_ * D_ * 4);
+  w.o_D = w.o_A + al256(S_ * rows * N_ * 4);
+  w.o_bias = w.o_D + al256(S_ * rows * 4);
+  w.o_fh = w.o_bias + al256(S_ * rows * 4);
+  w.o_fs = w.o_fh + al256((S_ - 1) * rows * N_ * 4);
+  w.o_al = w.o_fs + al256((S_ - 1) * rows * 4);
+  w.o_as = w.o_al + al256((S_ - 1) * rows * N_ * 4);
+  w.bytes = w.o_as + al256((S_ - 1) * rows * 4);
   return w;
 }
 
@@ -926,7 +1157,14 @@ static cudaError_t bwd_typed(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  const dim3 grid((unsigned)((a.dim + Cf::CH - 1) / Cf::CH), (unsigned)a.batch);
+  const unsigned nblk = (unsigned)((a.dim + Cf::CH - 1) / Cf::CH);
+  if (a.nseg > 1) {
+    adjoint_carry_kernel<IO, N><<<dim3(nblk, (unsigned)a.batch, (unsigned)(a.nseg - 1)), kBwdThreads,
+                                  0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid(nblk, (unsigned)a.batch, (unsigned)a.nseg);
   kern<<<grid, kBwdThreads, bytes, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

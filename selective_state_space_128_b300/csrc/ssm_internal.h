@@ -75,15 +75,18 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
 cudaError_t scan_launch(const ScanArgs& a, int64_t N, int io_dtype, const ScanPlan& plan,
                         cudaStream_t stream);
 
-// The warp-autonomous scan (ssm_scan_fast.cu) for N = 16 and bf16 I/O in the
-// (batch, dim, L) layout with 16-byte rows, zero-order hold: whether it applies,
-// and its launch (a.status must point at a device word).
+// The warp-autonomous scan (ssm_scan_fast.cu) for N = 16 and bf16 I/O whose views
+// TMA can stage, zero-order hold: whether it applies, whether it is the faster
+// choice for these sizes (enough 8-channel warps to give every SM 16 of them:
+// below that the block kernel's shared conversion wins), and its launch
+// (a.status must point at a device word).
 bool scan_fast_applies(const ScanArgs& a, int64_t N, int io_dtype);
+bool scan_fast_preferred(const ScanArgs& a);
 cudaError_t scan_fast_launch(const ScanArgs& a, cudaStream_t stream);
 
 // Channels per unit of work that the plan sizes the split for (the fast scan's
-// warp: 16 channels at N = 16).
-constexpr int kFastChannels = 16;
+// warp: 8 channels at N = 16).
+constexpr int kFastChannels = 8;
 
 struct UpdateArgs {
   float* state;
@@ -128,6 +131,10 @@ int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias,
 // no-allocation scan (0: none).
 size_t noalloc_test_limit();
 
+// The scan kernel the test mode asks for: 0 = chosen by size, 1 = the block kernel
+// (ssm_scan.cu), 2 = the warp kernel (ssm_scan_fast.cu) wherever it applies.
+int scan_kernel_choice();
+
 // Carry-record bytes of the split plan for these sizes on the current device (0:
 // the plan does not split).
 size_t scan_carry_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype);
@@ -160,15 +167,28 @@ struct BwdArgs {
   float* ckpt;     // [batch][nch][dim][N]: state at the start of every chunk
   float* ws_B;     // [batch][nblk][N][L]: per-block sums over the block's channels
   float* ws_C;     // [batch][nblk][N][L]
-  float* ws_A;     // [batch][dim][N]: per-batch-row dA
-  float* ws_D;     // [batch][dim]
-  float* ws_bias;  // [batch][dim]
+  float* ws_A;     // [nseg][batch][dim][N]: dA per segment and batch row
+  float* ws_D;     // [nseg][batch][dim]
+  float* ws_bias;  // [nseg][batch][dim]
   int64_t batch, dim, L, nblk;
   int softplus;
   int force_precise;
   int euler;
   int saved;  // ckpt already holds the chunk-start states (a training forward wrote them)
   int bld;    // u/delta/z/dy/du/ddelta/dz are (batch, L, dim)
+  // a sequence split into nseg segments of seg_len steps (grid.z), each folding
+  // the carries of the others: the forward's end state from zero and ΣΔ of
+  // segments 0 .. nseg-2 ([nseg-1][batch*dim][N], [nseg-1][batch*dim]), and the
+  // adjoint's value at the start from a zero adjoint at the end and ΣΔ of
+  // segments 1 .. nseg-1 (segment k at index k-1, same shapes); ws_A, ws_D,
+  // ws_bias hold one slice per segment ([nseg][batch][...])
+  int nseg;
+  int64_t seg_len;
+  float* fcarry_h;
+  float* fcarry_s;
+  float* acarry_l;
+  float* acarry_s;
+  int* status;  // device word for the forward carries' bounded waits
 };
 
 // Chunk length of the backward pass for state size N (the checkpoint interval).
@@ -178,13 +198,24 @@ int bwd_chunk(int64_t N);
 // and the total; nblk = channel blocks per batch row, nch = chunks per sequence.
 struct BwdLayout {
   int64_t nblk, nch;
-  size_t o_ckpt, o_B, o_C, o_A, o_D, o_bias, bytes;
+  int nseg;          // segments the sequence is split into (1: none)
+  int64_t seg_len;   // steps per segment (a multiple of 16 and of the chunk)
+  size_t o_ckpt, o_B, o_C, o_A, o_D, o_bias, o_fh, o_fs, o_al, o_as, bytes;
 };
 
-BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t L, int64_t N);
+// The plan splits the sequence into segments when its blocks would fill less
+// than half a wave on `sm_count` SMs.
+BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t L, int64_t N, int sm_count);
 
-// Enqueue the backward pass (two kernels).
+// Enqueue the backward pass: the adjoint's segment carries when the sequence is
+// split (the forward's come first, from scan_carries_launch, unless the states
+// were saved), the per-block kernel, the fixed-order sums.
 cudaError_t bwd_launch(const BwdArgs& a, int64_t N, int io_dtype, cudaStream_t stream);
+
+// The forward scan's first pass alone (the split plan's segment end states from
+// zero and ΣΔ into a.carry_h / a.carry_s for segments 0 .. a.nseg-2), with the
+// block kernel.
+cudaError_t scan_carries_launch(const ScanArgs& a, int64_t N, int io_dtype, cudaStream_t stream);
 
 // Arguments of the conv1d + SiLU front end (device pointers; layouts as in
 // include/ssm.h).  For the one-token update, state_out is the in/out state.
@@ -252,7 +283,13 @@ struct SsdArgs {
   int64_t batch, L, H, G, nch;
   int softplus;
   int euler;
+  int* status;  // device word set when a bounded wait runs out (the library-wide word)
 };
+
+// The chunk length of the SSD kernels and the floats of one (batch, chunk, head)
+// record of the step terms [s | β | w] in the workspace.
+constexpr int kSsdChunk = 64;
+constexpr int kSsdTermsRec = 3 * kSsdChunk;
 
 struct SsdLayout {
   int64_t nch;
@@ -261,5 +298,18 @@ struct SsdLayout {
 
 SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t N);
 cudaError_t ssd_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
+
+// The chunks' C Bᵀ on the tcgen05 tensor cores (ssm_ssd_tc.cu): one CTA per
+// (batch, chunk, group), fp32 rows of 64 into a.ws_cb (tiles on and below the
+// diagonal).
+cudaError_t ssd_cb_tc_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
+
+// The chunk outputs y = (mask ∘ C Bᵀ) X + exp(s_t) C Hᵀ + D x, gated, on tcgen05
+// (ssm_ssd_tc.cu): one CTA per (batch, chunk, head).
+cudaError_t ssd_chunk_tc_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
+
+// Device address of the library-wide status word on the current device (null on
+// error).
+int* library_status_word();
 
 }  // namespace ssm

@@ -931,12 +931,12 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
   if (!cfg_for(N, pl.chans, pl.chunk)) return pl;
   pl.seg_len = L > 0 ? L : 1;
   if (!allow_split || L <= 0 || batch <= 0 || dim <= 0) return pl;
-  // units of work that run at once: the fast scan's 16-channel warps (N = 16,
-  // bf16; split when fewer than 4 per SM) or this kernel's blocks (2 per SM)
+  // units of work that run at once: the fast scan's 8-channel warps (N = 16,
+  // bf16; split when fewer than 8 per SM) or this kernel's blocks (2 per SM)
   const bool fast = N == 16 && io_dtype == 1;
   const int64_t unit = fast ? kFastChannels : pl.chans;
   const int64_t blocks = ((dim + unit - 1) / unit) * batch;
-  const int64_t want = (int64_t)sm_count * (fast ? 4 : 2);
+  const int64_t want = (int64_t)sm_count * (fast ? 8 : 2);
   if (blocks >= want) return pl;
   int64_t nseg = (want + blocks - 1) / blocks;
   const int64_t max_by_len = L / (32 * (int64_t)pl.chunk);  // at least 32 chunks per segment
@@ -1048,6 +1048,40 @@ static cudaError_t launch_typed(ScanArgs a, cudaStream_t stream) {
   return launch_one<IO, N, 0>(a, m, a.nseg, stream);
 }
 
+template <typename IO, int N>
+static cudaError_t launch_carries(ScanArgs a, cudaStream_t stream) {
+  ScanMaps m;
+  memset(&m, 0, sizeof m);
+  const bool rows16 = a.vec_io && a.vec_bc;
+  const bool fits = a.L < (int64_t(1) << 31) && a.dim < (int64_t(1) << 31);
+  a.use_tma = rows16 && fits && make_maps<IO, N>(m, a);
+  if (a.nseg < 2) return cudaSuccess;
+  return launch_one<IO, N, 1>(a, m, a.nseg - 1, stream);
+}
+
+template <typename IO>
+static cudaError_t carries_io(const ScanArgs& a, int64_t N, cudaStream_t stream) {
+  switch (N) {
+    case 1: return launch_carries<IO, 1>(a, stream);
+    case 2: return launch_carries<IO, 2>(a, stream);
+    case 4: return launch_carries<IO, 4>(a, stream);
+    case 8: return launch_carries<IO, 8>(a, stream);
+    case 16: return launch_carries<IO, 16>(a, stream);
+    case 32: return launch_carries<IO, 32>(a, stream);
+    case 64: return launch_carries<IO, 64>(a, stream);
+    case 128: return launch_carries<IO, 128>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t scan_carries_launch(const ScanArgs& a, int64_t N, int io_dtype, cudaStream_t stream) {
+  if (a.batch == 0 || a.dim == 0 || a.L == 0) return cudaSuccess;
+  ScanArgs f = a;
+  if (!f.status) f.status = library_status_word();
+  if (!f.status) return cudaErrorInvalidValue;
+  return io_dtype == 0 ? carries_io<float>(f, N, stream) : carries_io<__nv_bfloat16>(f, N, stream);
+}
+
 template <typename IO>
 static cudaError_t launch_io(const ScanArgs& a, int64_t N, cudaStream_t stream) {
   switch (N) {
@@ -1065,7 +1099,7 @@ static cudaError_t launch_io(const ScanArgs& a, int64_t N, cudaStream_t stream) 
 
 // Device address of the library-wide status word on the current device (cached
 // per device; null on error).
-static int* library_status_ptr() {
+int* library_status_word() {
   static std::mutex mu;
   static int* ptrs[128] = {};
   int dev = 0;
@@ -1089,9 +1123,10 @@ cudaError_t scan_launch(const ScanArgs& a, int64_t N, int io_dtype, const ScanPl
     copy_state_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a.final_state, a.init_state, n);
     return cudaGetLastError();
   }
-  if (scan_fast_applies(a, N, io_dtype)) {
+  const int choice = scan_kernel_choice();
+  if (choice != 1 && scan_fast_applies(a, N, io_dtype) && (choice == 2 || scan_fast_preferred(a))) {
     ScanArgs f = a;
-    if (!f.status) f.status = library_status_ptr();
+    if (!f.status) f.status = library_status_word();
     if (!f.status) return cudaErrorInvalidValue;
     return scan_fast_launch(f, stream);
   }

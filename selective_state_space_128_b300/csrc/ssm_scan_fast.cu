@@ -652,6 +652,14 @@ bool scan_fast_applies(const ScanArgs& a, int64_t N, int io_dtype) {
          encode_fn() != nullptr;
 }
 
+bool scan_fast_preferred(const ScanArgs& a) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t warps = (a.dim + FastCfg<4>::CW - 1) / FastCfg<4>::CW * a.batch * a.nseg;
+  return warps >= (int64_t)sms * 16;
+}
+
 cudaError_t scan_fast_launch(const ScanArgs& a, cudaStream_t stream) {
   return launch_fast<4>(a, stream);
 }

@@ -14,25 +14,25 @@
 //   chunk output   y_t = Σ_{τ<=t} (C_t·B_τ) exp(s_t - s_τ) β_τ x_τ
 //                        + exp(s_t) C_t H_{c-1} + D_h x_t       (then · silu(z_t))
 //
-// Three launches: the chunks' step terms (all chunks in parallel), one walk
+// Four launches: the chunks' step terms (all chunks in parallel), one walk
 // over the chunks that forms each chunk's state contribution on the tensor
 // cores and passes the running state on (parallel over heads and slices of the
 // state's rows; the state never leaves the registers, only the bf16 copy each
-// chunk's outputs read), and the chunk outputs (all chunks in parallel).  The
-// products run on the tensor cores as mma.sync m16n8k16 bf16 with fp32
-// accumulation, operands staged in padded shared-memory rows (ldmatrix's eight
-// row addresses fall in distinct bank groups).  Layouts are Mamba-2's: x, z, y (batch, L, H,
+// chunk's outputs read), the chunks' C Bᵀ per group and the chunk outputs (all
+// chunks in parallel).  The last two run on the tcgen05 tensor cores with TMEM
+// accumulators (ssm_ssd_tc.cu); the walk runs its products as mma.sync
+// m16n8k16 bf16 with fp32 accumulation, operands staged in padded
+// shared-memory rows (ldmatrix's eight row addresses fall in distinct bank
+// groups).  Layouts are Mamba-2's: x, z, y (batch, L, H,
 // P); dt (batch, L, H); B, C (batch, L, G, N); states (batch, H, P, N).
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
 namespace ssm {
 
-constexpr int kSsdQ = 64;        // chunk length
+constexpr int kSsdQ = kSsdChunk;  // chunk length
 constexpr int kSsdP = 64;        // head dimension
 constexpr int kSsdThreads = 128;  // 4 warps: 16 rows each
-constexpr int kScanColSplit = 2;  // chunk outputs: two warps per 16-row tile, 32 columns each
-constexpr int kScanThreadsSsd = kSsdThreads * kScanColSplit;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -100,7 +100,7 @@ __device__ __forceinline__ void ssd_stage(__nv_bfloat16* dst, const __nv_bfloat1
 //    weight 0).  A lane takes two steps; s is a warp prefix sum.
 // ---------------------------------------------------------------------------
 constexpr int kTermsThreads = 128;
-constexpr int kTermsRec = 3 * kSsdQ;  // floats per (batch, chunk, head)
+constexpr int kTermsRec = kSsdTermsRec;  // floats per (batch, chunk, head)
 
 __global__ void __launch_bounds__(kTermsThreads) ssd_terms_kernel(const SsdArgs p) {
   constexpr int Q = kSsdQ;
@@ -289,209 +289,14 @@ __global__ void __launch_bounds__(SsdStateCfg<N, PR>::kThreads)
 
 // ---------------------------------------------------------------------------
 // 2. the chunks' C Bᵀ, once per (batch, chunk, group): every head of a group
-//    shares it.  G[t][τ] = C_t · B_τ for τ <= t (16 x 16 tiles on and below the
-//    diagonal; the others are never read), fp32, [t][τ] rows of 64.
+//    shares it.  G[t][τ] = C_t · B_τ, fp32, [t][τ] rows of 64, on the tcgen05
+//    tensor cores (ssm_ssd_tc.cu); the chunk outputs read the entries τ <= t.
 // ---------------------------------------------------------------------------
-template <int N>
-__global__ void __launch_bounds__(kSsdThreads) ssd_cb_kernel(const SsdArgs p) {
-  constexpr int Q = kSsdQ, RB = N + 8;
-  __shared__ __align__(16) __nv_bfloat16 sB[Q * RB];  // [τ][n]
-  __shared__ __align__(16) __nv_bfloat16 sC[Q * RB];  // [t][n]
-  const int c = blockIdx.x, g = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int64_t t0 = (int64_t)c * Q;
-  const int valid = (int)min64(Q, p.L - t0);
-  const int64_t bc = ((b * p.L + t0) * p.G + g) * N;
-  ssd_stage<Q, N, RB>(sB, static_cast<const __nv_bfloat16*>(p.B) + bc, p.G * N, valid);
-  ssd_stage<Q, N, RB>(sC, static_cast<const __nv_bfloat16*>(p.C) + bc, p.G * N, valid);
-  cp_async_wait_all();
-  __syncthreads();
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // warp w: rows t in [16w, 16w+16)
-  const int i8 = lane >> 3;
-  float cb[8][4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) cb[j][0] = cb[j][1] = cb[j][2] = cb[j][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < N / 16; ++ks) {
-    uint32_t a[4];
-    ldsm_x4(a, sC + (16 * w + (lane & 15)) * RB + 16 * ks + (lane >> 4) * 8);
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      if (jj > w) break;
-      // B operand = Bᵀ: k = n, columns τ; stored [τ][n] -> plain loads
-      uint32_t bf[4];
-      ldsm_x4(bf, sB + (16 * jj + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
-      mma_bf16(cb[2 * jj], a, bf[0], bf[1]);
-      mma_bf16(cb[2 * jj + 1], a, bf[2], bf[3]);
-    }
-  }
-  float* out = p.ws_cb + ((b * p.nch + c) * p.G + g) * (int64_t)(Q * Q);
-  const int r0 = 16 * w + (lane >> 2), cc = 2 * (lane & 3);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j / 2 > w) break;
-    *reinterpret_cast<float2*>(out + r0 * Q + 8 * j + cc) = make_float2(cb[j][0], cb[j][1]);
-    *reinterpret_cast<float2*>(out + (r0 + 8) * Q + 8 * j + cc) = make_float2(cb[j][2], cb[j][3]);
-  }
-}
 
 // ---------------------------------------------------------------------------
-// 3. chunk outputs: y = (mask ∘ C Bᵀ) X + exp(s_t) C Hᵀ + D x, gated
+// 3. chunk outputs: y = (mask ∘ C Bᵀ) X + exp(s_t) C Hᵀ + D x, gated, per
+//    (batch, chunk, head) on the tcgen05 tensor cores (ssm_ssd_tc.cu).
 // ---------------------------------------------------------------------------
-template <int N> struct SsdScanSmem {
-  static constexpr int Q = kSsdQ, P = kSsdP, RX = P + 8, RB = N + 8;
-  static constexpr int RG = Q + 8;  // fp32 C Bᵀ rows: 288 bytes
-  // bf16 tiles: x [τ][p], C [t][n], entering state [p][n], z [t][p]; then fp32
-  // C Bᵀ [t][τ] and the step terms s, β
-  static constexpr int oC = Q * RX, oH = oC + Q * RB, oZ = oH + P * RB, kTiles = oZ + Q * RX;
-  static constexpr size_t kBytes = (size_t)kTiles * 2 + (size_t)(Q * RG + 2 * Q) * 4;
-};
-
-template <int N>
-__global__ void __launch_bounds__(kScanThreadsSsd) ssd_chunk_scan_kernel(const SsdArgs p) {
-  using S = SsdScanSmem<N>;
-  constexpr int Q = kSsdQ, P = kSsdP, RX = S::RX, RB = S::RB, RG = S::RG, NT = kScanThreadsSsd;
-  constexpr int PC = P / kScanColSplit;  // output columns per warp
-  extern __shared__ float4 ssd_smem[];
-  __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(ssd_smem);
-  __nv_bfloat16* sC = sX + S::oC;
-  __nv_bfloat16* sH = sX + S::oH;
-  __nv_bfloat16* sZ = sX + S::oZ;
-  float* sG = reinterpret_cast<float*>(sX + S::kTiles);
-  float* sS = sG + Q * RG;
-  float* sBeta = sS + Q;
-  const int c = blockIdx.x, h = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int64_t t0 = (int64_t)c * Q;
-  const int valid = (int)min64(Q, p.L - t0);
-  const int g = h / (p.H / p.G);
-  const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
-  // two copy groups: C and the entering state first (the product C Hᵀ needs
-  // only them), then x, z, the group's C Bᵀ and the step terms, which arrive
-  // while it runs
-  ssd_stage<Q, N, RB, NT>(sC, static_cast<const __nv_bfloat16*>(p.C) + ((b * p.L + t0) * p.G + g) * N, p.G * N,
-                      valid);
-  ssd_stage<P, N, RB, NT>(sH, p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N), N, P);
-  cp_async_commit();
-  ssd_stage<Q, P, RX, NT>(sX, xg, p.H * P, valid);
-  if (p.z)
-    ssd_stage<Q, P, RX, NT>(sZ, static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P,
-                        p.H * P, valid);
-  // C Bᵀ rows of 64 fp32, copied as rows of 128 bf16-sized halves (plain bytes)
-  ssd_stage<Q, 2 * Q, 2 * RG, NT>(reinterpret_cast<__nv_bfloat16*>(sG),
-                              reinterpret_cast<const __nv_bfloat16*>(
-                                  p.ws_cb + ((b * p.nch + c) * p.G + g) * (int64_t)(Q * Q)),
-                              2 * Q, Q);
-  if (threadIdx.x < 2 * kSsdQ / 4) {  // s and β of the chunk's step terms
-    const float* src = p.ws_terms + ((b * p.nch + c) * p.H + h) * kTermsRec + 4 * threadIdx.x;
-    cp_async16(sS + 4 * threadIdx.x, src, true);
-  }
-  cp_async_commit();
-  cp_async_wait<1>();
-  __syncthreads();
-
-  // warp w: rows t in [16 wr, 16 wr + 16), output columns p in [PC wc, PC wc + PC)
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, wr = w & 3, wc = w >> 2;
-  const int i8 = lane >> 3;
-  // (a) O = C Hᵀ for this warp's rows and columns
-  float ov[PC / 8][4];
-#pragma unroll
-  for (int j = 0; j < PC / 8; ++j) ov[j][0] = ov[j][1] = ov[j][2] = ov[j][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < N / 16; ++ks) {
-    uint32_t a[4];
-    ldsm_x4(a, sC + (16 * wr + (lane & 15)) * RB + 16 * ks + (lane >> 4) * 8);
-#pragma unroll
-    for (int pp = 0; pp < PC / 16; ++pp) {
-      // B operand = Hᵀ: k = n, columns p; stored [p][n] -> plain loads
-      uint32_t bf[4];
-      ldsm_x4(bf, sH + (PC * wc + 16 * pp + (i8 >> 1) * 8 + (lane & 7)) * RB + 16 * ks + (i8 & 1) * 8);
-      mma_bf16(ov[2 * pp], a, bf[0], bf[1]);
-      mma_bf16(ov[2 * pp + 1], a, bf[2], bf[3]);
-    }
-  }
-  cp_async_wait<0>();  // x, z, C Bᵀ, terms
-  __syncthreads();
-  // (b) the decay mask and input weight: M[t][τ] = (τ <= t) C_t·B_τ exp(s_t - s_τ) β_τ,
-  //     packed as bf16 A fragments of the next product (two n8 tiles = one k16 step)
-  const int tr = 16 * wr + (lane >> 2);  // this thread's rows tr, tr + 8
-  const float s_r0 = sS[tr], s_r1 = sS[tr + 8];
-  uint32_t am[4][4];
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int tau = 16 * kk + 8 * half + 2 * (lane & 3);
-      float m[4] = {0.f, 0.f, 0.f, 0.f};
-      if (kk <= wr) {
-        const float2 g0 = *reinterpret_cast<const float2*>(sG + tr * RG + tau);
-        const float2 g1 = *reinterpret_cast<const float2*>(sG + (tr + 8) * RG + tau);
-        const float cbv[4] = {g0.x, g0.y, g1.x, g1.y};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = e < 2 ? tr : tr + 8, col = tau + (e & 1);
-          const float sr = e < 2 ? s_r0 : s_r1;
-          m[e] = col <= row ? cbv[e] * __expf(sr - sS[col]) * sBeta[col] : 0.f;
-        }
-      }
-      am[kk][2 * half] = pack_bf16(m[0], m[1]);
-      am[kk][2 * half + 1] = pack_bf16(m[2], m[3]);
-    }
-  }
-  // (c) Y = M X (k = τ up to the warp's rows)
-  float yv[PC / 8][4];
-#pragma unroll
-  for (int j = 0; j < PC / 8; ++j) yv[j][0] = yv[j][1] = yv[j][2] = yv[j][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    if (kk > wr) break;
-    const uint32_t a[4] = {am[kk][0], am[kk][1], am[kk][2], am[kk][3]};
-#pragma unroll
-    for (int pp = 0; pp < PC / 16; ++pp) {
-      // B operand = X: k = τ, columns p; stored [τ][p] -> transposed loads
-      uint32_t bf[4];
-      ldsm_x4_t(bf, sX + (16 * kk + (lane & 15)) * RX + PC * wc + 16 * pp + (lane >> 4) * 8);
-      mma_bf16(yv[2 * pp], a, bf[0], bf[1]);
-      mma_bf16(yv[2 * pp + 1], a, bf[2], bf[3]);
-    }
-  }
-  // (e) y = Y + exp(s_t) O + D x, gated, into a shared tile [t][p] (the C tile's
-  //     space: C is no longer read), then 16-byte coalesced stores of the rows
-  //     inside the sequence
-  const float Dh = p.D ? p.D[h] : 0.f;
-  const float e0 = __expf(s_r0), e1 = __expf(s_r1);
-  const bool gate = p.z != nullptr;
-  __nv_bfloat16* sY = sC;
-#pragma unroll
-  for (int j = 0; j < PC / 8; ++j) {
-    const int col = PC * wc + 8 * j + 2 * (lane & 3);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int row = half ? tr + 8 : tr;
-      const float ee = half ? e1 : e0;
-      const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162*>(sX + row * RX + col);
-      float v0 = fmaf(ee, ov[j][2 * half], yv[j][2 * half]) + Dh * __low2float(xv);
-      float v1 = fmaf(ee, ov[j][2 * half + 1], yv[j][2 * half + 1]) + Dh * __high2float(xv);
-      if (gate) {
-        const __nv_bfloat162 zv = *reinterpret_cast<const __nv_bfloat162*>(sZ + row * RX + col);
-        v0 *= silu_precise(__low2float(zv));
-        v1 *= silu_precise(__high2float(zv));
-      }
-      *reinterpret_cast<__nv_bfloat162*>(sY + row * RX + col) = __floats2bfloat162_rn(v0, v1);
-    }
-  }
-  __syncthreads();
-  __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y) + ((b * p.L + t0) * p.H + h) * P;
-  constexpr int VPR = P / 8;
-#pragma unroll
-  for (int k = 0; k < Q * VPR / NT; ++k) {
-    const int v = threadIdx.x + k * NT;
-    const int row = v / VPR, c8 = v % VPR;
-    if (row < valid)
-      *reinterpret_cast<uint4*>(yg + (int64_t)row * p.H * P + 8 * c8) =
-          *reinterpret_cast<const uint4*>(sY + row * RX + 8 * c8);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -534,22 +339,9 @@ static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = ssd_walk<N>(a, s);
   if (e != cudaSuccess) return e;
-  ssd_cb_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.G, (unsigned)a.batch), kSsdThreads, 0, s>>>(a);
-  e = cudaGetLastError();
+  e = ssd_cb_tc_launch(a, N, s);
   if (e != cudaSuccess) return e;
-  constexpr size_t bytes = SsdScanSmem<N>::kBytes;
-  static int configured_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(ssd_chunk_scan_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)bytes);
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
-  }
-  ssd_chunk_scan_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch), kScanThreadsSsd, bytes,
-                             s>>>(a);
-  return cudaGetLastError();
+  return ssd_chunk_tc_launch(a, N, s);
 }
 
 cudaError_t ssd_launch(const SsdArgs& a, int64_t N, cudaStream_t stream) {

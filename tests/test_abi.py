@@ -90,10 +90,11 @@ def test_stall_flag_is_refused_outside_test_mode():
     mode is on; the test mode checks its limits."""
     assert _scan(softplus=1 | ssm.SSM_TEST_STALL) == ssm.SSM_ERR_ARG
     l = lib()
-    assert l.ssm_set_test_mode(1, 10, 0) == ssm.SSM_ERR_ARG            # limit below 1 us
-    assert l.ssm_set_test_mode(1, 3_000_000_000, 0) == ssm.SSM_ERR_ARG  # above 2 s
-    assert l.ssm_set_test_mode(1, 1_000_000, -1) == ssm.SSM_ERR_ARG
-    assert l.ssm_set_test_mode(0, 0, 0) == ssm.SSM_OK
+    assert l.ssm_set_test_mode(1, 10, 0, 0) == ssm.SSM_ERR_ARG            # limit below 1 us
+    assert l.ssm_set_test_mode(1, 3_000_000_000, 0, 0) == ssm.SSM_ERR_ARG  # above 2 s
+    assert l.ssm_set_test_mode(1, 1_000_000, -1, 0) == ssm.SSM_ERR_ARG
+    assert l.ssm_set_test_mode(1, 1_000_000, 0, 3) == ssm.SSM_ERR_ARG     # no kernel 3
+    assert l.ssm_set_test_mode(0, 0, 0, 0) == ssm.SSM_OK
     assert _scan(softplus=1 | ssm.SSM_TEST_STALL) == ssm.SSM_ERR_ARG
 
 
@@ -182,6 +183,27 @@ def test_backward_workspace_size():
     assert ckpt + parts <= need <= ckpt + parts + 8 * 1536 * 18 * 4 + 6 * 256
     assert ssm.ssm_scan_bwd_workspace_bytes(0, 1536, 2048, 16) == 0
     assert ssm.ssm_scan_bwd_workspace_bytes(8, 1536, 2048, 3) == 0
+
+
+def test_backward_split_plan():
+    """One batch row of 1536 channels is 48 blocks of 32 channels, under half of one
+    wave of 148 SMs x 3 resident blocks: the plan splits the 2^20 steps into 10
+    segments of 104 864 (ceil(444 / 48) = 10; a multiple of 16), and the workspace
+    adds the per-segment sums and the forward's and the adjoint's carries of 9
+    segments.  With 8 batch rows (384 blocks) and 2048 steps it does not split."""
+    def al(x):
+        return (x + 255) // 256 * 256
+
+    b, d, L, N = 1, 1536, 1 << 20, 16
+    nseg, rows = 10, b * d
+    want = (al(b * (L // 16) * d * N * 4) + 2 * al(b * (d // 32) * N * L * 4)
+            + al(nseg * rows * N * 4) + 2 * al(nseg * rows * 4)
+            + 2 * (al((nseg - 1) * rows * N * 4) + al((nseg - 1) * rows * 4)))
+    assert ssm.ssm_scan_bwd_workspace_bytes(b, d, L, N) == want
+    b, L = 8, 2048
+    want = (al(b * (L // 16) * d * N * 4) + 2 * al(b * (d // 32) * N * L * 4)
+            + al(b * d * N * 4) + 2 * al(b * d * 4))
+    assert ssm.ssm_scan_bwd_workspace_bytes(b, d, L, N) == want
 
 
 def test_conv_argument_errors():

@@ -184,6 +184,57 @@ def test_backward_mamba130m_layer_full_size_sampled():
     assert oracle.rel_err(host64(out["dbias"][dsel_t]), db_ref) <= TOL
 
 
+def test_backward_million_length_one_call_sampled():
+    """The backward over the million-length sequence in one call (batch 1, d_inner 1536,
+    L 2^20, N 16, bf16), where the plan splits the sequence into segments that fold
+    each other's carries: du, ddelta, dz over the whole length, d_init_state, and
+    (one batch row) dA, dD, dbias of 16 sampled channels against the oracle; every
+    output finite.  dB and dC sum over all 1536 channels: the split cases of the
+    backward's parity tests check them in full at smaller sizes."""
+    w = synth.MILLION
+    L, dim, N = w.seqlen, w.dim, w.dstate
+    dev = "cuda"
+    step = 128
+    t = {k: torch.empty((1, dim, L), dtype=torch.bfloat16, device=dev)
+         for k in ("u", "delta", "z", "dy")}
+    for d0 in range(0, dim, step):
+        for k in ("u", "delta", "z"):
+            t[k][0, d0:d0 + step] = dev_io(synth.gen_rows(w, k, 0, d0, step))
+        dyk = synth.fill(w.seed, synth.S_DY, d0 * L, step * L, synth.NORMAL, 0.0, 1.0,
+                         dtype=w.io).reshape(step, L)
+        t["dy"][0, d0:d0 + step] = dev_io(dyk)
+    e = synth.make_bwd_inputs(synth.scaled(w, seqlen=1))  # init / d_final: (batch, dim, N)
+    h0 = e["init_state"].astype(np.float64)
+    dfin = e["d_final_state"].astype(np.float64)
+    A, D = synth.gen_A(dim, N), synth.gen_D(w)
+    bias = synth.gen_delta_bias(w.seed, dim)
+    B, C = synth.gen_bc(w, "B"), synth.gen_bc(w, "C")
+    out = ssm.scan_bwd(t["u"], t["delta"], dev_f32(A), dev_f32(B), dev_f32(C), dev_f32(D),
+                       t["z"], dev_f32(bias), True, init_state=dev_f32(e["init_state"]),
+                       dy=t["dy"], d_final_state=dev_f32(e["d_final_state"]),
+                       want_init_grad=True)
+    torch.cuda.synchronize()
+    for k in ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "dbias", "dinit"):
+        assert torch.isfinite(out[k].float()).all().item(), k
+    bs, ds = _sample_rows(w.batch, dim, 16, seed=9)
+    di = torch.from_numpy(ds).cuda()
+    got = {k: host64(out[k][0][di]) for k in ("du", "ddelta", "dz", "dinit")}
+    got.update({k: host64(out[k][di]) for k in ("dA", "dD", "dbias")})
+    del out, t
+    rows = {k: np.concatenate([synth.gen_rows(w, k, 0, int(d), 1) for d in ds])
+            for k in ("u", "delta", "z")}
+    dy64 = np.concatenate([synth.bf16_to_f32(synth.fill(w.seed, synth.S_DY, int(d) * L, L,
+                                                        synth.NORMAL, 0.0, 1.0, dtype=w.io))
+                           [None] for d in ds]).astype(np.float64)
+    r = oracle.scan_bwd_rows(rows["u"], rows["delta"], rows["z"], bs, ds, A, B, C, D, bias,
+                             True, dy64, h0[bs, ds], dfin[bs, ds], nbatch=1)
+    for k in ("du", "ddelta", "dz", "dinit"):
+        assert oracle.rel_err(got[k], r[k]) <= TOL, k
+    assert oracle.rel_err(got["dA"], r["dA_unit"]) <= TOL
+    assert oracle.rel_err(got["dD"], r["dD_unit"]) <= TOL
+    assert oracle.rel_err(got["dbias"], r["dbias_unit"]) <= TOL
+
+
 def test_conv1d_and_bld_scan_at_layer_size():
     """The front end at the bench's size (8 x 1536 x 2048 bf16, width 4) on 64 sampled
     rows, and the (batch, L, dim) scan of the layer equal, bit for bit, to the

@@ -43,7 +43,9 @@ def _call(g, w, flags, ws, stream):
     return y, h
 
 
-def test_stalled_block_reports_timeout_in_its_own_workspace():
+@pytest.mark.parametrize("kernel", [ssm.SCAN_KERNEL_BLOCK, ssm.SCAN_KERNEL_WARP])
+def test_stalled_block_reports_timeout_in_its_own_workspace(kernel):
+    """With either forward kernel (the block kernel and the warp kernel)."""
     w, x, g = _inputs()
     y_o, h_o = oracle.scan(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
                            x["delta_bias"])
@@ -52,12 +54,14 @@ def test_stalled_block_reports_timeout_in_its_own_workspace():
     ws_b = torch.empty(need, dtype=torch.uint8, device="cuda")
     sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
-    ssm.ssm_set_test_mode(True, 1_000_000)
+    ssm.ssm_set_test_mode(True, 1_000_000, scan_kernel=kernel)
     try:
         ya, ha = _call(g, w, ssm.SSM_SOFTPLUS | ssm.SSM_TEST_STALL, ws_a, sa)
         yb, hb = _call(g, w, ssm.SSM_SOFTPLUS, ws_b, sb)
         assert ssm.ssm_status(ws_a, sa) == ssm.SSM_ERR_TIMEOUT
         assert ssm.ssm_status(ws_b, sb) == ssm.SSM_OK
+        yc, hc = _call(g, w, ssm.SSM_SOFTPLUS, ws_a, sa)  # the same kernel, right after
+        assert ssm.ssm_status(ws_a, sa) == ssm.SSM_OK
     finally:
         ssm.ssm_set_test_mode(False)
     torch.cuda.synchronize()
@@ -70,8 +74,6 @@ def test_stalled_block_reports_timeout_in_its_own_workspace():
     # the stalled block left its final states unwritten
     assert torch.isnan(ha[0, 0]).all()
     # the context still works: a normal call on the same workspace, status OK, correct
-    yc, hc = _call(g, w, ssm.SSM_SOFTPLUS, ws_a, sa)
-    assert ssm.ssm_status(ws_a, sa) == ssm.SSM_OK
     assert torch.equal(yc, yb) and torch.equal(hc, hb)
     assert ssm.ssm_status(None) == ssm.SSM_OK   # the library-wide word was not touched
 
