@@ -305,7 +305,7 @@ cudaError_t ssd_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
 cudaError_t ssd_cb_tc_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
 
 // The chunk outputs y = (mask ∘ C Bᵀ) X + exp(s_t) C Hᵀ + D x, gated, on tcgen05
-// (ssm_ssd_tc.cu): one CTA per (batch, chunk, head).
+// (ssm_ssd_tc.cu): persistent CTAs over the (batch, chunk, head) items.
 cudaError_t ssd_chunk_tc_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
 
 // Device address of the library-wide status word on the current device (null on

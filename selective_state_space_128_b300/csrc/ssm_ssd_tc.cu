@@ -59,20 +59,6 @@ __device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t adesc, uint64_t 
       : "memory");
 }
 
-// 32 consecutive TMEM columns of this warp's 32 lanes (one per thread).
-__device__ __forceinline__ void tc_ld32(uint32_t (&r)[32], uint32_t taddr) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
 // 16-byte asynchronous copy global -> shared; with `valid` false nothing is read
 // and the destination is zero-filled.
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
@@ -212,51 +198,88 @@ __global__ void __launch_bounds__(kTcThreads) ssd_cb_tc_kernel(const SsdArgs p) 
 //   D1 = C Hᵀ            (K = N: the state entering the chunk, [p][n] bf16)
 //   D2 = M X,  M[t][τ] = (τ <= t) C_t·B_τ exp(s_t - s_τ) β_τ   (K = τ)
 // in two 64-column TMEM accumulators, then y = exp(s_t) D1 + D2 + D x, gated by
-// silu(z), through a shared tile and 16-byte stores.  C, H and M are K-major
-// operands; X ([τ][p], p contiguous) is the MN-major B operand of D2, whose
-// core matrices hold 8 steps x 8 channels and whose descriptor has the K-step
-// (1024 bytes) as its leading and the MN-step (128 bytes) as its stride byte
-// offset.
+// silu(z).  C, H and M are K-major operands; X ([τ][p], p contiguous) is the
+// MN-major B operand of D2, whose core matrices hold 8 steps x 8 channels and
+// whose descriptor has the K-step (1024 bytes) as its leading and the MN-step
+// (128 bytes) as its stride byte offset.
+//
+// Persistent CTAs (as many as fit on every SM) walk the (batch, chunk, head)
+// items, heads fastest so that the heads of a group reuse its C and C Bᵀ from
+// L2.  The operands of the next item (C, H, X and the step terms) are copied into
+// the other of two stages while the current one is computed, its C Bᵀ rows are
+// read into registers after the current M is built, and z is read into
+// registers, in the mapping of the final store, while the products run.  The
+// epilogue reads the accumulators with the 16-lane shape (16x256b: thread i
+// holds rows i/4 and i/4 + 8 of its warp's 16, columns 2(i%4) and 2(i%4)+1 of
+// each group of 8), so all 32 threads of a warp work on its 16 rows, stages y in
+// shared memory, and gates and stores it as 16-byte vectors.
 // ---------------------------------------------------------------------------
 template <int N> struct ChunkTcSmem {
   static constexpr int P = 64;
-  static constexpr size_t oC = 0;                                 // [t][n]  K-major
-  static constexpr size_t oH = oC + (size_t)kQ * N * 2;           // [p][n]  K-major
-  static constexpr size_t oM = oH + (size_t)P * N * 2;            // [t][τ]  K-major
-  static constexpr size_t oX = oM + (size_t)kQ * kQ * 2;          // [τ][p]  MN-major
-  static constexpr size_t oZ = oX + (size_t)kQ * P * 2;           // [t][p]  rows of 64 + 8
-  static constexpr int RZ = P + 8;
-  static constexpr size_t oG = oZ + (size_t)kQ * RZ * 2;          // C Bᵀ [t][τ] fp32, rows of 64 + 4
-  static constexpr int RG = kQ + 4;
-  static constexpr size_t oS = oG + (size_t)kQ * RG * 4;          // s, β
-  static constexpr size_t oBar = oS + 2 * kQ * 4;
+  static constexpr int RY = P + 8;                                // y rows: 64 + 8 bf16
+  // one stage: the operands of one item
+  static constexpr size_t sC = 0;                                 // [t][n]  K-major
+  static constexpr size_t sH = sC + (size_t)kQ * N * 2;           // [p][n]  K-major
+  static constexpr size_t sX = sH + (size_t)P * N * 2;            // [τ][p]  MN-major
+  static constexpr size_t sS = sX + (size_t)kQ * P * 2;           // s, β
+  static constexpr size_t kStage = sS + 2 * kQ * 4;
+  static constexpr size_t oM = 2 * kStage;                        // [t][τ]  K-major
+  static constexpr size_t oY = oM + (size_t)kQ * kQ * 2;          // [t][p]  rows of RY
+  static constexpr size_t oBar = oY + (size_t)kQ * RY * 2;
   static constexpr size_t oSlot = oBar + 8;
   static constexpr size_t kBytes = oSlot + 8;
   static constexpr size_t kLaunch = kBytes + 128;
+  static_assert(kStage % 128 == 0 && oM % 128 == 0 && oY % 16 == 0 && oBar % 8 == 0, "alignment");
 };
 
+// Four 32-bit TMEM columns pairs of 16 lanes (16x256b, one repetition): see above.
+__device__ __forceinline__ void tc_ld16x256(uint32_t (&r)[4], uint32_t taddr) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
+// Threads of a chunk-output CTA: two warps per TMEM lane quarter, each taking
+// half of the accumulators' columns.
+constexpr int kChunkThreads = 256;
+
+struct ChunkItem {
+  int64_t b;
+  int c, h, g, valid;
+  int64_t t0;
+};
+
+// (batch, chunk, head) of an item, heads fastest (the item count fits 32 bits:
+// the launcher checks)
+__device__ __forceinline__ ChunkItem chunk_item(const SsdArgs& p, uint32_t item) {
+  ChunkItem it;
+  const uint32_t H = (uint32_t)p.H, nch = (uint32_t)p.nch;
+  const uint32_t bc = item / H;
+  it.h = (int)(item - bc * H);
+  const uint32_t b = bc / nch;
+  it.c = (int)(bc - b * nch);
+  it.b = b;
+  it.g = it.h / (int)(p.H / p.G);
+  it.t0 = (int64_t)it.c * kQ;
+  it.valid = (int)min64(kQ, p.L - it.t0);
+  return it;
+}
+
 template <int N>
-__global__ void __launch_bounds__(kTcThreads) ssd_chunk_tc_kernel(const SsdArgs p) {
+__global__ void __launch_bounds__(kChunkThreads, 2) ssd_chunk_tc_kernel(const SsdArgs p) {
   using S = ChunkTcSmem<N>;
-  constexpr int P = S::P, KB = N / 8;
+  constexpr int P = S::P, KB = N / 8, RY = S::RY, NT = kChunkThreads;
+  constexpr int kMv = kQ * kQ / 8 / NT;      // 8-wide groups of M a thread builds
+  constexpr int kVec = kQ * (P / 8) / NT;    // 16-byte vectors of y a thread stores
   extern __shared__ unsigned char ck_smem_raw[];
   unsigned char* sm = ck_smem_raw + ((128u - (smem_u32(ck_smem_raw) & 127u)) & 127u);
-  unsigned char* sC = sm + S::oC;
-  unsigned char* sH = sm + S::oH;
   unsigned char* sM = sm + S::oM;
-  unsigned char* sX = sm + S::oX;
-  __nv_bfloat16* sZ = reinterpret_cast<__nv_bfloat16*>(sm + S::oZ);
-  float* sG = reinterpret_cast<float*>(sm + S::oG);
-  float* sS = reinterpret_cast<float*>(sm + S::oS);
-  float* sBeta = sS + kQ;
+  __nv_bfloat16* sY = reinterpret_cast<__nv_bfloat16*>(sm + S::oY);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S::oBar);
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, h = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int64_t t0 = (int64_t)c * kQ;
-  const int valid = (int)min64(kQ, p.L - t0);
-  const int g = h / (p.H / p.G);
+  const uint32_t total = (uint32_t)(p.batch * p.nch * p.H);
+  const int64_t io_step = p.H * P;  // elements between steps of x, z, y
 
   if (warp == 0) {  // the accumulators first: the copies below overlap the allocation
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
@@ -267,142 +290,264 @@ __global__ void __launch_bounds__(kTcThreads) ssd_chunk_tc_kernel(const SsdArgs 
     mbar_init(bar, 1);
     fence_mbar_init();
   }
-  // copies (16-byte cp.async; thread e's vector is row 8i + (e & 7) of core-matrix
-  // column e >> 3, so 8 consecutive threads fill one 128-byte core matrix)
-  const __nv_bfloat16* gC = static_cast<const __nv_bfloat16*>(p.C) + ((b * p.L + t0) * p.G + g) * N;
-  const __nv_bfloat16* gH = p.ws_hin + ((b * p.nch + c) * p.H + h) * (int64_t)(P * N);
-  for (int e = tid; e < kQ * KB; e += kTcThreads) {
-    const int kb = (e >> 3) % KB, r = ((e >> 3) / KB) * 8 + (e & 7);
-    const bool ok = r < valid;
-    cp_async16_zfill(sC + kmaj_off(r, 8 * kb, KB), gC + (int64_t)(ok ? r : 0) * p.G * N + 8 * kb, ok);
-    cp_async16_zfill(sH + kmaj_off(r, 8 * kb, KB), gH + (int64_t)r * N + 8 * kb, true);
-  }
-  const __nv_bfloat16* gX = static_cast<const __nv_bfloat16*>(p.x) + ((b * p.L + t0) * p.H + h) * P;
-  const __nv_bfloat16* gZ = static_cast<const __nv_bfloat16*>(p.z) + ((b * p.L + t0) * p.H + h) * P;
-  for (int e = tid; e < kQ * (P / 8); e += kTcThreads) {
-    const int nb = (e >> 3) % (P / 8), tau = ((e >> 3) / (P / 8)) * 8 + (e & 7);
-    const bool ok = tau < valid;
-    // X as the MN-major operand: core matrix (τ block, p block), 8 steps of 16 bytes
-    cp_async16_zfill(sX + mnmaj_off(tau, 8 * nb, P / 8), gX + (int64_t)(ok ? tau : 0) * p.H * P + 8 * nb, ok);
-    if (p.z)
-      cp_async16_zfill(sZ + tau * S::RZ + 8 * nb, gZ + (int64_t)(ok ? tau : 0) * p.H * P + 8 * nb, ok);
-  }
-  const float* gG = p.ws_cb + ((b * p.nch + c) * p.G + g) * (int64_t)(kQ * kQ);
-  for (int e = tid; e < kQ * kQ / 4; e += kTcThreads) {
-    const int r = e / (kQ / 4), v = e % (kQ / 4);
-    if (4 * v <= r)  // the tiles on and below the diagonal were written
-      cp_async16_zfill(sG + r * S::RG + 4 * v, gG + r * kQ + 4 * v, true);
-  }
-  if (tid < 2 * kQ / 4)
-    cp_async16_zfill(sS + 4 * tid, p.ws_terms + ((b * p.nch + c) * p.H + h) * kSsdTermsRec + 4 * tid, true);
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-  // M[t][τ] in bf16, K-major: thread e builds 8 consecutive τ of row t
-  for (int e = tid; e < kQ * kQ / 8; e += kTcThreads) {
-    const int kb = (e >> 3) % 8, t = ((e >> 3) / 8) * 8 + (e & 7);
-    const float st = sS[t];
-    float m[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int tau = 8 * kb + j;
-      m[j] = tau <= t ? sG[t * S::RG + tau] * __expf(st - sS[tau]) * sBeta[tau] : 0.f;
+
+  // the operands of one item into a stage (16-byte cp.async; thread e's vector is
+  // row 8i + (e & 7) of core-matrix column e >> 3, so 8 consecutive threads fill
+  // one 128-byte core matrix), as one commit group
+  auto copy_stage = [&](const ChunkItem& w, unsigned char* st) {
+    const __nv_bfloat16* gC =
+        static_cast<const __nv_bfloat16*>(p.C) + ((w.b * p.L + w.t0) * p.G + w.g) * N;
+    const __nv_bfloat16* gH = p.ws_hin + ((w.b * p.nch + w.c) * p.H + w.h) * (int64_t)(P * N);
+    for (int e = tid; e < kQ * KB; e += NT) {
+      const int kb = (e >> 3) % KB, r = ((e >> 3) / KB) * 8 + (e & 7);
+      const bool ok = r < w.valid;
+      cp_async16_zfill(st + S::sC + kmaj_off(r, 8 * kb, KB),
+                       gC + (int64_t)(ok ? r : 0) * p.G * N + 8 * kb, ok);
+      cp_async16_zfill(st + S::sH + kmaj_off(r, 8 * kb, KB), gH + (int64_t)r * N + 8 * kb, true);
     }
-    uint4 v;
-    v.x = pack_bf16x2(m[0], m[1]);
-    v.y = pack_bf16x2(m[2], m[3]);
-    v.z = pack_bf16x2(m[4], m[5]);
-    v.w = pack_bf16x2(m[6], m[7]);
-    *reinterpret_cast<uint4*>(sM + kmaj_off(t, 8 * kb, 8)) = v;
+    const __nv_bfloat16* gX =
+        static_cast<const __nv_bfloat16*>(p.x) + ((w.b * p.L + w.t0) * p.H + w.h) * P;
+    for (int e = tid; e < kQ * (P / 8); e += NT) {
+      const int nb = (e >> 3) % (P / 8), tau = ((e >> 3) / (P / 8)) * 8 + (e & 7);
+      const bool ok = tau < w.valid;
+      cp_async16_zfill(st + S::sX + mnmaj_off(tau, 8 * nb, P / 8),
+                       gX + (int64_t)(ok ? tau : 0) * io_step + 8 * nb, ok);
+    }
+    if (tid < 2 * kQ / 4)
+      cp_async16_zfill(st + S::sS + 16 * tid,
+                       p.ws_terms + ((w.b * p.nch + w.c) * p.H + w.h) * kSsdTermsRec + 4 * tid, true);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  // C Bᵀ rows of an item for M: thread e's 8 consecutive τ of row t (global, rows
+  // of 64 floats; the 16 x 16 tiles on and below the diagonal were written, and
+  // every 8-wide group that reaches τ <= t lies in one of them)
+  float4 gv[kMv][2];
+  float dh_pre = 0.f;  // the item's D
+  auto fetch_cb = [&](const ChunkItem& w) {  // and D of the head
+    dh_pre = p.D ? __ldg(p.D + w.h) : 0.f;
+    const float* gG = p.ws_cb + ((w.b * p.nch + w.c) * p.G + w.g) * (int64_t)(kQ * kQ);
+#pragma unroll
+    for (int i = 0; i < kMv; ++i) {
+      const int e = tid + i * NT, kb = (e >> 3) % 8, t = ((e >> 3) / 8) * 8 + (e & 7);
+      if (8 * kb <= t) {
+        gv[i][0] = __ldg(reinterpret_cast<const float4*>(gG + t * kQ + 8 * kb));
+        gv[i][1] = __ldg(reinterpret_cast<const float4*>(gG + t * kQ + 8 * kb + 4));
+      } else {
+        gv[i][0] = gv[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  };
+
+  uint32_t item = blockIdx.x;
+  ChunkItem w = chunk_item(p, item);
+  if (item < total) {
+    copy_stage(w, sm);
+    fetch_cb(w);
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *slot;
-  if (tid == 0) {
-    // D1 = C Hᵀ into columns 0..63
-    constexpr uint32_t id1 = tc_idesc_bf16(kQ, P);
-#pragma unroll
-    for (int k = 0; k < N / 16; ++k) {
-      const uint64_t ad = tc_desc(smem_u32(sC) + 256u * k, 128, KB * 128);
-      const uint64_t bd = tc_desc(smem_u32(sH) + 256u * k, 128, KB * 128);
-      tc_mma(tmem, ad, bd, id1, k > 0);
+  // epilogue share: lane quarter warp % 4, column groups 4 (warp / 4) .. + 3
+  const int quarter = warp & 3, jh = 4 * (warp >> 2);
+  const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16);
+  const int r0 = 16 * quarter + (lane >> 2), cq = 2 * (lane & 3);
+  bool ok = true;
+  for (int k = 0; item < total; ++k, item += gridDim.x) {
+    const float Dh = dh_pre;
+    unsigned char* st = sm + (size_t)(k & 1) * S::kStage;
+    const float* sS = reinterpret_cast<const float*>(st + S::sS);
+    const float* sBeta = sS + kQ;
+    const uint32_t next = item + gridDim.x;
+    const ChunkItem wn = chunk_item(p, next < total ? next : item);
+    if (next < total) {
+      copy_stage(wn, sm + (size_t)((k + 1) & 1) * S::kStage);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this item's group
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
-    // D2 = M X into columns 64..127 (X MN-major: bit 16 of the instruction descriptor)
-    constexpr uint32_t id2 = tc_idesc_bf16(kQ, P) | (1u << 16);
+    __syncthreads();
+    // M[t][τ] in bf16, K-major, in packed pairs: G β 2^((s_t - s_τ) log2 e)
 #pragma unroll
-    for (int k = 0; k < kQ / 16; ++k) {
-      const uint64_t ad = tc_desc(smem_u32(sM) + 256u * k, 128, 8 * 128);
-      const uint64_t bd = tc_desc(smem_u32(sX) + 2u * (P / 8) * 128 * k, (P / 8) * 128, 128);
-      tc_mma(tmem + kQ, ad, bd, id2, k > 0);
-    }
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-  }
-  const bool ok = mbar_wait_bounded(bar, 0);
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  // epilogue: warp q's lanes 0-15 hold row t = 16q + lane of both accumulators
-  __nv_bfloat16* sY = reinterpret_cast<__nv_bfloat16*>(sC);  // C is no longer read: [t][p] rows of RZ
-  const int t = 16 * warp + lane;
-  const float Dh = p.D ? p.D[h] : 0.f;
-  const float et = lane < 16 ? __expf(sS[t & (kQ - 1)]) : 0.f;
-  if (ok) {
+    for (int i = 0; i < kMv; ++i) {
+      const int e = tid + i * NT, kb = (e >> 3) % 8, t = ((e >> 3) / 8) * 8 + (e & 7);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (8 * kb <= t) {
+        f2 sq[4], bq[4];
+        lds_pairs(sS + 8 * kb, sq[0], sq[1]);
+        lds_pairs(sS + 8 * kb + 4, sq[2], sq[3]);
+        lds_pairs(sBeta + 8 * kb, bq[0], bq[1]);
+        lds_pairs(sBeta + 8 * kb + 4, bq[2], bq[3]);
+        const float stt = sS[t];
+        const f2 st2 = pack2(stt, stt), l2 = pack2(kLog2e, kLog2e);
+        const f2 gq[4] = {pack2(gv[i][0].x, gv[i][0].y), pack2(gv[i][0].z, gv[i][0].w),
+                          pack2(gv[i][1].x, gv[i][1].y), pack2(gv[i][1].z, gv[i][1].w)};
+        const bool diag = 8 * kb + 7 > t;  // the block holds τ > t: those are zero
+        uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t r1[32], r2[32];
-      tc_ld32(r1, tmem + ((uint32_t)(32 * warp) << 16) + 32 * hh);
-      tc_ld32(r2, tmem + ((uint32_t)(32 * warp) << 16) + kQ + 32 * hh);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      if (lane < 16) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int col = 32 * hh + j;
-          const __nv_bfloat162 xv =
-              *reinterpret_cast<const __nv_bfloat162*>(sX + mnmaj_off(t, col, P / 8));
-          float v0 = fmaf(et, __uint_as_float(r1[j]), __uint_as_float(r2[j])) + Dh * __low2float(xv);
-          float v1 = fmaf(et, __uint_as_float(r1[j + 1]), __uint_as_float(r2[j + 1])) +
-                     Dh * __high2float(xv);
-          if (p.z) {
-            const __nv_bfloat162 zv = *reinterpret_cast<const __nv_bfloat162*>(sZ + t * S::RZ + col);
-            v0 *= silu_precise(__low2float(zv));
-            v1 *= silu_precise(__high2float(zv));
+        for (int q = 0; q < 4; ++q) {
+          float x0, x1;
+          unpack2(mul2(sub2(st2, sq[q]), l2), x0, x1);
+          float m0, m1;
+          unpack2(mul2(mul2(gq[q], bq[q]), pack2(ex2_fast(x0), ex2_fast(x1))), m0, m1);
+          if (diag) {
+            m0 = 8 * kb + 2 * q <= t ? m0 : 0.f;
+            m1 = 8 * kb + 2 * q + 1 <= t ? m1 : 0.f;
           }
-          *reinterpret_cast<__nv_bfloat162*>(sY + t * S::RZ + col) = __floats2bfloat162_rn(v0, v1);
+          vw[q] = pack_bf16x2(m0, m1);
+        }
+      }
+      *reinterpret_cast<uint4*>(sM + kmaj_off(t, 8 * kb, 8)) = v;
+    }
+    if (next < total) fetch_cb(wn);
+    // z for the final store (row e / 8, channels (e % 8) * 8 .. + 7)
+    uint4 zr[kVec];
+    const __nv_bfloat16* gZ =
+        static_cast<const __nv_bfloat16*>(p.z) + ((w.b * p.L + w.t0) * p.H + w.h) * P;
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const int e = tid + i * NT, row = e >> 3, c8 = e & 7;
+      zr[i] = (p.z && row < w.valid)
+                  ? __ldg(reinterpret_cast<const uint4*>(gZ + (int64_t)row * io_step + 8 * c8))
+                  : make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (tid == 0) {
+      // D1 = C Hᵀ into columns 0..63
+      constexpr uint32_t id1 = tc_idesc_bf16(kQ, P);
+#pragma unroll
+      for (int kk = 0; kk < N / 16; ++kk) {
+        const uint64_t ad = tc_desc(smem_u32(st + S::sC) + 256u * kk, 128, KB * 128);
+        const uint64_t bd = tc_desc(smem_u32(st + S::sH) + 256u * kk, 128, KB * 128);
+        tc_mma(tmem, ad, bd, id1, kk > 0);
+      }
+      // D2 = M X into columns 64..127 (X MN-major: bit 16 of the instruction descriptor)
+      constexpr uint32_t id2 = tc_idesc_bf16(kQ, P) | (1u << 16);
+#pragma unroll
+      for (int kk = 0; kk < kQ / 16; ++kk) {
+        const uint64_t ad = tc_desc(smem_u32(sM) + 256u * kk, 128, 8 * 128);
+        const uint64_t bd = tc_desc(smem_u32(st + S::sX) + 2u * (P / 8) * 128 * kk, (P / 8) * 128, 128);
+        tc_mma(tmem + kQ, ad, bd, id2, kk > 0);
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_u32(bar))
+                   : "memory");
+    }
+    ok = mbar_wait_bounded(bar, (uint32_t)(k & 1));
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (__syncthreads_or(!ok)) {  // every thread leaves together
+      ok = false;
+      break;
+    }
+    // epilogue: rows 16q + lane/4 and 16q + lane/4 + 8 of quarter q, columns
+    // 8j + 2(lane%4) and the next for this warp's four j, of both accumulators
+    {
+      const unsigned char* sX = st + S::sX;
+      uint32_t d1[4][4], d2[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        tc_ld16x256(d1[j], ta + 8 * (jh + j));
+        tc_ld16x256(d2[j], ta + kQ + 8 * (jh + j));
+      }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const f2 dh2 = pack2(Dh, Dh);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int t = r0 + 8 * hf;
+        const float et = ex2_fast(sS[t] * kLog2e);
+        const f2 et2 = pack2(et, et);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int col = 8 * (jh + j) + cq;
+          const float2 xv = __bfloat1622float2(
+              *reinterpret_cast<const __nv_bfloat162*>(sX + mnmaj_off(t, col, P / 8)));
+          const f2 a = pack2(__uint_as_float(d1[j][2 * hf]), __uint_as_float(d1[j][2 * hf + 1]));
+          const f2 c2 = pack2(__uint_as_float(d2[j][2 * hf]), __uint_as_float(d2[j][2 * hf + 1]));
+          float v0, v1;
+          unpack2(fma2(dh2, pack2(xv.x, xv.y), fma2(et2, a, c2)), v0, v1);
+          *reinterpret_cast<uint32_t*>(sY + t * RY + col) = pack_bf16x2(v0, v1);
         }
       }
     }
-  } else if (tid == 0) {
-    atomicExch(p.status, 1);  // the MMAs never completed: report it, write nothing
+    // the accumulators are read: the next item's products may overwrite them
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    // gate and store: 16-byte vectors of y
+    __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y) + ((w.b * p.L + w.t0) * p.H + w.h) * P;
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const int e = tid + i * NT, row = e >> 3, c8 = e & 7;
+      if (row >= w.valid) continue;
+      uint4 v = *reinterpret_cast<const uint4*>(sY + row * RY + 8 * c8);
+      if (p.z) {
+        uint32_t* wv = reinterpret_cast<uint32_t*>(&v);
+        const uint32_t* zw = reinterpret_cast<const uint32_t*>(&zr[i]);
+        const f2 nl2 = pack2(-kLog2e, -kLog2e), one2 = pack2(1.f, 1.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // y silu(z) = y z / (1 + 2^(-z log2 e)), in packed pairs
+          const float2 yv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+          const float2 zv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zw[q]));
+          const f2 z2 = pack2(zv.x, zv.y);
+          float e0, e1;
+          unpack2(mul2(z2, nl2), e0, e1);
+          float d0, d1;
+          unpack2(add2(pack2(ex2_fast(e0), ex2_fast(e1)), one2), d0, d1);
+          float o0, o1;
+          unpack2(mul2(mul2(pack2(yv.x, yv.y), z2), pack2(rcp_fast(d0), rcp_fast(d1))), o0, o1);
+          wv[q] = pack_bf16x2(o0, o1);
+        }
+      }
+      *reinterpret_cast<uint4*>(yg + (int64_t)row * io_step + 8 * c8) = v;
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    w = wn;
   }
+  if (!ok && tid == 0) atomicExch(p.status, 1);  // products never completed: the rest is skipped
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy outlives the CTA
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kQ));
-  if (!ok) return;
-  __nv_bfloat16* yg = static_cast<__nv_bfloat16*>(p.y) + ((b * p.L + t0) * p.H + h) * P;
-  for (int e = tid; e < kQ * (P / 8); e += kTcThreads) {
-    const int row = e / (P / 8), c8 = e % (P / 8);
-    if (row < valid)
-      *reinterpret_cast<uint4*>(yg + (int64_t)row * p.H * P + 8 * c8) =
-          *reinterpret_cast<const uint4*>(sY + row * S::RZ + 8 * c8);
-  }
 }
 
 template <int N>
 cudaError_t chunk_tc_typed(const SsdArgs& a, cudaStream_t s) {
   constexpr size_t bytes = ChunkTcSmem<N>::kLaunch;
-  static int configured_dev = -1;
+  static int configured_dev = -1, resident = 1, sms = 148;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    const cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<N>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<N>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<N>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    // CTAs an SM holds: by shared memory (with the per-block reservation) and by
+    // registers; 128 TMEM columns a CTA allow at most 4
+    int smem_sm = 0, reserved = 0;
+    cudaFuncAttributes fa{};
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, ssd_chunk_tc_kernel<N>);
+    if (e != cudaSuccess) return e;
+    const int by_smem = smem_sm / (int)(bytes + (size_t)reserved);
+    const int regs = fa.numRegs > 0 ? fa.numRegs : 255;
+    const int by_regs = 65536 / (regs * kChunkThreads);
+    resident = by_smem < by_regs ? by_smem : by_regs;
+    resident = resident < 1 ? 1 : (resident > 4 ? 4 : resident);
     configured_dev = dev;
   }
-  ssd_chunk_tc_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch), kTcThreads, bytes,
-                           s>>>(a);
+  const int64_t total = a.batch * a.nch * a.H;
+  if (total >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  const int64_t grid = (int64_t)sms * resident < total ? (int64_t)sms * resident : total;
+  if (grid <= 0) return cudaSuccess;
+  ssd_chunk_tc_kernel<N><<<(unsigned)grid, kChunkThreads, bytes, s>>>(a);
   return cudaGetLastError();
 }
 
