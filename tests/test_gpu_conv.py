@@ -146,10 +146,13 @@ def test_conv1d_bwd_matches_oracle(io, K, L):
     _check_bwd(io, 3, 37, L, K, seed=70 + K + L)
 
 
-@pytest.mark.parametrize("case", ["no_silu", "no_state_no_bias", "long_rows", "bld", "bld_ragged"])
+@pytest.mark.parametrize("case", ["no_silu", "no_state_no_bias", "long_rows", "bld", "bld_ragged",
+                                  "f32_long_rows", "one_unit_and_a_bit", "long_rows_no_state"])
 def test_conv1d_bwd_variants(case):
     kw = dict(no_silu=dict(silu=False), no_state_no_bias=dict(state=False, bias=False),
-              long_rows=dict(L=5000), bld=dict(bld=True), bld_ragged=dict(bld=True, L=29))[case]
+              long_rows=dict(L=5000), bld=dict(bld=True), bld_ragged=dict(bld=True, L=29),
+              f32_long_rows=dict(io="f32", L=4100), one_unit_and_a_bit=dict(L=2056, K=3),
+              long_rows_no_state=dict(L=4104, state=False))[case]
     args = dict(io="bf16", batch=2, dim=24, L=136, K=4, seed=90)
     args.update(kw)
     _check_bwd(**args)
@@ -161,3 +164,20 @@ def test_conv1d_bwd_repeats_bit_for_bit():
     b = _check_bwd("bf16", 4, 16, 100, 4, seed=95)
     for k in ("dx", "dweight", "dbias", "dstate"):
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("io,L", [("bf16", 5000), ("f32", 2052)])
+def test_conv1d_bwd_staged_rows_equal_the_elementwise_kernel(io, L):
+    """Rows of whole 16-byte pieces in (batch, dim, L) go through the kernel that
+    stages them in shared memory; the (batch, L, dim) layout takes the element-wise
+    kernel.  Same arithmetic and order of sums: equal bit for bit."""
+    x, wt, b, st = _inputs(io, 2, 24, L, 4, 97, True)
+    dout = _dout(io, (2, 24, L), 98)
+    tr = lambda t: t.transpose(1, 2).contiguous()
+    args = (dev_f32(wt),)
+    a = ssm.conv1d_bwd(dev_io(x), *args, dev_io(dout), dev_f32(b), dev_io(st))
+    c = ssm.conv1d_bwd(tr(dev_io(x)), *args, tr(dev_io(dout)), dev_f32(b), dev_io(st), bld=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a["dx"], c["dx"].transpose(1, 2))
+    for k in ("dweight", "dbias", "dstate"):
+        assert torch.equal(a[k], c[k]), k
