@@ -672,6 +672,57 @@ def bench_backward(w, g, steps, warmup, world):
                 workspace_bytes=nbytes)
 
 
+def bench_backward_million(w, reps, world):
+    """ssm_scan_bwd over the million-length sequence in one call (batch 1, d_inner
+    1536, L 2^20, N 16, bf16): 48 channel blocks of one batch row, so the library's
+    plan splits the sequence into segments chained by their carries (the forward's
+    first pass, the adjoint's carry pass, the per-block kernel, the fixed-order sums:
+    4 launches a call).  Inputs drawn on the device with the workload's
+    distributions (u, z, dy ~ N(0, 1), Δ_raw ~ N(0, 0.5^2), B, C ~ N(0, 1); A, D and
+    the bias from the workload's generator): 4 x 3.2 GB in, 3 x 3.2 GB out."""
+    import torch
+    import selective_state_space_128_b300 as ssm
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2000 + w.seed)
+    bf = torch.bfloat16
+    shape = (w.batch, w.dim, w.seqlen)
+    N = w.dstate
+    f32 = dict(dtype=torch.float32, device="cuda")
+    u = torch.randn(shape, generator=gen, device="cuda").to(bf)
+    delta = (w.sigma_delta * torch.randn(shape, generator=gen, device="cuda")).to(bf)
+    z = torch.randn(shape, generator=gen, device="cuda").to(bf)
+    dy = torch.randn(shape, generator=gen, device="cuda").to(bf)
+    B = torch.randn((w.batch, N, w.seqlen), generator=gen, **f32)
+    C = torch.randn((w.batch, N, w.seqlen), generator=gen, **f32)
+    A = torch.from_numpy(synth.gen_A(w.dim, N)).cuda()
+    D = torch.from_numpy(synth.gen_D(w)).cuda()
+    bias = torch.from_numpy(synth.gen_delta_bias(w.seed, w.dim)).cuda()
+    du, ddelta, dz = torch.empty_like(u), torch.empty_like(u), torch.empty_like(u)
+    dA, dD, dbias = torch.empty((w.dim, N), **f32), torch.empty(w.dim, **f32), torch.empty(w.dim, **f32)
+    dB, dC = torch.empty_like(B), torch.empty_like(C)
+    nbytes = ssm.ssm_scan_bwd_workspace_bytes(w.batch, w.dim, w.seqlen, N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        ssm.ssm_scan_bwd(u, delta, bias, A, B, C, D, z, ssm.SSM_SOFTPLUS, None, dy, None, du,
+                         ddelta, dA, dB, dC, dD, dz, dbias, None, ws, nbytes, stream=stream)
+
+    call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / reps
+    del u, delta, z, dy, du, ddelta, dz, ws
+    return dict(ms=ms, reps=reps, workspace_bytes=nbytes)
+
+
 # ---------------------------------------------------------------------------
 # decode: batch 256, d_inner 5120, N 16, one token per step
 # ---------------------------------------------------------------------------
@@ -842,6 +893,7 @@ def main():
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
     ap.add_argument("--no-million", action="store_true")
+    ap.add_argument("--no-bwd-million", action="store_true")
     ap.add_argument("--million-reps", type=int, default=3)
     ap.add_argument("--million-launches", type=int, default=None,
                     help="time only the first K of the 16 launches (for profiling a smaller case)")
@@ -874,6 +926,8 @@ def main():
                                                     cpu=(rank == 0 and world == 1
                                                          and not args.no_cpu),
                                                     launches=args.million_launches)
+    torch.cuda.empty_cache()
+    bmil = None if (args.no_bwd or args.no_bwd_million) else bench_backward_million(wm, 2, world)
     torch.cuda.empty_cache()
     conv = None if args.no_conv else bench_conv(w1, 50, args.warmup, world)
     ssd = None if args.no_ssd else bench_ssd(20, args.warmup, world)
@@ -951,6 +1005,22 @@ def main():
         if "cpu" in mil:
             mo["cpu_baseline"] = mil["cpu"]
         line["million_length"] = mo
+    if bmil is not None:
+        bs = bmil["ms"] / 1e3
+        esz = 2
+        # the method's bytes: u, Δ, z, dy read and du, dΔ, dz written; B, C read and
+        # dB, dC written; A, D, bias and dA, dD, dbias
+        bb = (7 * wm.channel_steps * esz + 4 * wm.batch * wm.dstate * wm.seqlen * 4
+              + 2 * (wm.dim * wm.dstate + 2 * wm.dim) * 4)
+        line["backward_million_length"] = {
+            "workload": wm.name + " backward, one call over the whole length",
+            "config": workload_config(wm), "reps": bmil["reps"], "ms_per_call": bmil["ms"],
+            "channel_steps_per_s": wm.channel_steps / bs * world,
+            "hbm_gbs_algorithmic": bb / bs / 1e9, "hbm_frac": bb / bs / 1e9 / hbm_peak,
+            "bytes_per_call": bb, "workspace_bytes": bmil["workspace_bytes"],
+            "gpu_launches": 4 * bmil["reps"],
+            "call": "ssm_scan_bwd: the plan splits the sequence into segments (forward "
+                    "carries, adjoint carries, per-block kernel, fixed-order sums)"}
     if dec is not None:
         db = decode_bytes(synth.DECODE.batch, synth.DECODE.dim, synth.DECODE.dstate)
         st = dec["step_ms"] / 1e3

@@ -862,24 +862,26 @@ __global__ void __launch_bounds__(kBwdThreads, BwdCfg<N>::MINB) scan_bwd_kernel(
 // nseg-1 (index k-1 of acarry_l / acarry_s); the backward kernel of segment s
 // starts from d final_state folded through segments nseg-1 .. s+1.  Each step,
 // from a segment's last to its first, is the adjoint sweep's own: λ += ds_t C_t,
-// then λ *= Ā_t.  The lane layout is the backward kernel's (G lanes of NPT
-// states per channel, CH channels a block); a chunk of TT steps of Δ and ds is
-// staged per channel in shared memory, C per step, the next chunk's raw inputs
-// in flight in registers meanwhile.
+// then λ *= Ā_t.  A channel's states sit on G lanes of NPT as in the backward
+// kernel, in blocks of two warps (64 / G channels); a chunk of TT steps of Δ
+// and ds is staged per channel in shared memory, C per step, the next chunk's
+// raw inputs in flight in registers meanwhile.
+constexpr int kAdjThreads = 64;  // two warps a block: many small blocks keep loads in flight
+
 template <int N> struct AdjCfg {
   using Cf = BwdCfg<N>;
-  static constexpr int NPT = Cf::NPT, G = Cf::G, CH = Cf::CH;
+  static constexpr int NPT = Cf::NPT, G = Cf::G, CH = kAdjThreads / G;
   // steps per chunk: at most 8 channel steps of each input and 16 floats of C a thread
-  static constexpr int TT = (1024 / CH < 2048 / N) ? 1024 / CH : 2048 / N;
-  static constexpr int E = CH * TT / kBwdThreads;   // channel steps a thread loads
+  static constexpr int TT = (512 / CH < 1024 / N) ? 512 / CH : 1024 / N;
+  static constexpr int E = CH * TT / kAdjThreads;   // channel steps a thread loads
   static constexpr int TPR = TT / E;                // threads per channel row
-  static constexpr int PER = (TT * N + kBwdThreads - 1) / kBwdThreads;
+  static constexpr int PER = (TT * N + kAdjThreads - 1) / kAdjThreads;
   static constexpr int RowF = TT + 1;
-  static_assert(E >= 1 && E <= 8 && TPR * E == TT && PER <= 16, "tiling");
+  static_assert(CH >= 1 && E >= 1 && E <= 8 && TPR * E == TT && PER <= 16, "tiling");
 };
 
 template <typename IO, int N>
-__global__ void __launch_bounds__(kBwdThreads) adjoint_carry_kernel(const BwdArgs p) {
+__global__ void __launch_bounds__(kAdjThreads) adjoint_carry_kernel(const BwdArgs p) {
   using Cf = AdjCfg<N>;
   constexpr int NPT = Cf::NPT, CH = Cf::CH, TT = Cf::TT, E = Cf::E, TPR = Cf::TPR, PER = Cf::PER;
   __shared__ float sDT[CH * Cf::RowF];
@@ -911,7 +913,7 @@ __global__ void __launch_bounds__(kBwdThreads) adjoint_carry_kernel(const BwdArg
   constexpr int kVecBytes = (sizeof(IO) == 2 && E == 4) ? 8 : 16;
   const bool vec = !bld && E % 4 == 0 && (L * (int64_t)sizeof(IO)) % kVecBytes == 0;
 
-  for (int i = tid; i < CH; i += kBwdThreads)
+  for (int i = tid; i < CH; i += kAdjThreads)
     sBias[i] = (p.bias && d0 + i < p.dim) ? p.bias[d0 + i] : 0.f;
   float Aj[NPT], A2[NPT];
   bool zeroA = false;
@@ -951,9 +953,9 @@ __global__ void __launch_bounds__(kBwdThreads) adjoint_carry_kernel(const BwdArg
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int e = tid + i * kBwdThreads;  // (n, t) of the chunk's C tile
+      const int e = tid + i * kAdjThreads;  // (n, t) of the chunk's C tile
       const int n = e / TT, t = e - n * TT;
-      const bool ok = (TT * N % kBwdThreads == 0 || e < TT * N) && t < tc;
+      const bool ok = (TT * N % kAdjThreads == 0 || e < TT * N) && t < tc;
       rc[i] = ok ? p.C[(b * N + n) * L + t0 + t] : 0.f;
     }
   };
@@ -980,8 +982,8 @@ __global__ void __launch_bounds__(kBwdThreads) adjoint_carry_kernel(const BwdArg
       }
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
-        const int e = tid + i * kBwdThreads;
-        if (TT * N % kBwdThreads == 0 || e < TT * N) {
+        const int e = tid + i * kAdjThreads;
+        if (TT * N % kAdjThreads == 0 || e < TT * N) {
           const int n = e / TT, t = e - n * TT;
           sC[t * N + n] = rc[i];
         }
@@ -1105,14 +1107,16 @@ BwdLayout bwd_layout(int64_t batch, int64_t dim, int64_t L, int64_t N, int sm_co
   BwdLayout w{};
   if (!bwd_geometry(N, dim, L, w.nblk, w.nch)) return w;
   // Split the sequence when the (channel block, batch row) blocks fill less than
-  // half of one wave of resident blocks: segments of at least kBwdMinSeg steps,
-  // a multiple of 16 (the forward's and every backward chunk length), at most 64.
+  // half of one wave of resident blocks: as many segments as still fit in one
+  // wave (a second, mostly idle wave would cost a whole segment's time), each of
+  // at least kBwdMinSeg steps and a multiple of 16 (the forward's and every
+  // backward chunk length), at most 64.
   w.nseg = 1;
   w.seg_len = L > 0 ? L : 1;
   const int64_t blocks = w.nblk * batch;
   const int64_t wave = (int64_t)sm_count * bwd_resident(N);
   if (L > 0 && blocks > 0 && 2 * blocks <= wave) {
-    int64_t nseg = (wave + blocks - 1) / blocks;
+    int64_t nseg = wave / blocks;
     if (nseg > L / kBwdMinSeg) nseg = L / kBwdMinSeg;
     if (nseg > 64) nseg = 64;
     if (nseg >= 2) {
@@ -1159,7 +1163,8 @@ static cudaError_t bwd_typed(const BwdArgs& a, cudaStream_t stream) {
   }
   const unsigned nblk = (unsigned)((a.dim + Cf::CH - 1) / Cf::CH);
   if (a.nseg > 1) {
-    adjoint_carry_kernel<IO, N><<<dim3(nblk, (unsigned)a.batch, (unsigned)(a.nseg - 1)), kBwdThreads,
+    const unsigned ablk = (unsigned)((a.dim + AdjCfg<N>::CH - 1) / AdjCfg<N>::CH);
+    adjoint_carry_kernel<IO, N><<<dim3(ablk, (unsigned)a.batch, (unsigned)(a.nseg - 1)), kAdjThreads,
                                   0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

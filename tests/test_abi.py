@@ -187,15 +187,16 @@ def test_backward_workspace_size():
 
 def test_backward_split_plan():
     """One batch row of 1536 channels is 48 blocks of 32 channels, under half of one
-    wave of 148 SMs x 3 resident blocks: the plan splits the 2^20 steps into 10
-    segments of 104 864 (ceil(444 / 48) = 10; a multiple of 16), and the workspace
-    adds the per-segment sums and the forward's and the adjoint's carries of 9
-    segments.  With 8 batch rows (384 blocks) and 2048 steps it does not split."""
+    wave of 148 SMs x 3 resident blocks: the plan splits the 2^20 steps into as
+    many segments as fit in that wave, 9 of 116 512 steps (444 // 48 = 9; a
+    multiple of 16), and the workspace adds the per-segment sums and the forward's
+    and the adjoint's carries of 8 segments.  With 8 batch rows (384 blocks) and
+    2048 steps it does not split."""
     def al(x):
         return (x + 255) // 256 * 256
 
     b, d, L, N = 1, 1536, 1 << 20, 16
-    nseg, rows = 10, b * d
+    nseg, rows = 9, b * d
     want = (al(b * (L // 16) * d * N * 4) + 2 * al(b * (d // 32) * N * L * 4)
             + al(nseg * rows * N * 4) + 2 * al(nseg * rows * 4)
             + 2 * (al((nseg - 1) * rows * N * 4) + al((nseg - 1) * rows * 4)))
