@@ -493,9 +493,11 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
  * Backward of ssm_ssd_fwd (the chapter page's §5.1: SSD is the selective scan
  * of each channel of a head with the scalar A[h] for every state, the head's
  * step shared by its channels and the group's B, C): the derivatives of
- * Σ y·dy + Σ final_state·d_final_state.  Computed through ssm_scan_bwd on each
- * group's channels (fp32 I/O) and summed over the channels that share a
- * parameter in a fixed order, so results repeat bit for bit.
+ * Σ y·dy + Σ final_state·d_final_state, in the chunked form: the states
+ * entering the chunks recomputed by a forward walk (fp32), the derivatives
+ * reaching the chunks' end states by a reverse walk, then every derivative of
+ * a chunk from its 64 steps, all in fp32; sums over a group's heads and over
+ * chunks in a fixed order, so results repeat bit for bit.
  *
  * Inputs, layouts, flags and supported shapes as ssm_ssd_fwd; dy (batch,
  * seqlen, nheads, headdim) bf16; d_final_state (batch, nheads, headdim,
@@ -503,8 +505,9 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
  * when z is given), ddt like dt (bf16), dA (nheads) fp32 required, dB, dC like
  * B (fp32, (batch, seqlen, ngroups, dstate)), dD and d_dt_bias (nheads) fp32
  * nullable, d_init_state like init_state (fp32, nullable).  Workspace: device
- * memory of at least ssm_ssd_bwd_workspace_bytes() bytes (one group's fp32
- * copies and the scan backward's workspace).  Errors as ssm_ssd_fwd.
+ * memory of at least ssm_ssd_bwd_workspace_bytes() bytes (the step terms, the
+ * fp32 states and state derivatives of every chunk, per-head partial dB and
+ * dC).  Errors as ssm_ssd_fwd.
  * Asynchronous on `stream`.
  */
 size_t ssm_ssd_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,

@@ -299,6 +299,10 @@ struct SsdLayout {
 SsdLayout ssd_layout(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t N);
 cudaError_t ssd_launch(const SsdArgs& a, int64_t N, cudaStream_t stream);
 
+// The step terms alone: per (batch, chunk, head) the record [s | β | w] of
+// kSsdTermsRec floats in a.ws_terms (reads dt, dt_bias, A, softplus, euler).
+cudaError_t ssd_terms_launch(const SsdArgs& a, cudaStream_t stream);
+
 // The chunks' C Bᵀ on the tcgen05 tensor cores (ssm_ssd_tc.cu): one CTA per
 // (batch, chunk, group), fp32 rows of 64 into a.ws_cb (tiles on and below the
 // diagonal).

@@ -330,12 +330,17 @@ static cudaError_t ssd_walk(const SsdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int N>
-static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
+cudaError_t ssd_terms_launch(const SsdArgs& a, cudaStream_t s) {
   const int64_t units = a.batch * a.nch * a.H;
+  if (units == 0) return cudaSuccess;
   constexpr int kUnitsPerBlock = kTermsThreads / 32;
   ssd_terms_kernel<<<(unsigned)((units + kUnitsPerBlock - 1) / kUnitsPerBlock), kTermsThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <int N>
+static cudaError_t ssd_typed(const SsdArgs& a, cudaStream_t s) {
+  cudaError_t e = ssd_terms_launch(a, s);
   if (e != cudaSuccess) return e;
   e = ssd_walk<N>(a, s);
   if (e != cudaSuccess) return e;

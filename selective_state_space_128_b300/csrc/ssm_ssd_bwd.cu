@@ -1,161 +1,712 @@
-// Backward of Mamba-2's scalar-A SSM (SSD), through the selective scan's
-// backward.
+// Backward of Mamba-2's scalar-A SSM (SSD), in the chunked form.
 //
 // The chapter page ("14.1 SSM(State Space Models)과 Mamba 아키텍처의 부상",
-// §5.1) restricts A to a scalar per step times the identity: per head h, SSD
-// is the selective scan of each of the head's P channels with A[n] = a_h for
-// every state n, the head's step Δ_t shared by its channels, and the B, C of
-// the head's group.  Its derivatives are therefore the scan backward's
-// per-channel derivatives (ssm_scan_bwd: states recomputed per chunk, the
-// adjoint in reverse) summed over the channels that share each parameter:
-// the head's P channels for dΔ, dA, dD and d dt_bias, every channel of the
-// group for dB and dC (the scan backward already sums a batch row's channels).
+// §5.1-5.2) computes SSD chunk by chunk: per head h (P channels sharing the
+// step Δ_t and the scalar a = A[h]; B, C of the head's group), with the chunk's
+// cumulative log decay s_t = Σ_{k<=t in the chunk} Δ_k a, the input weight β_t
+// ((exp(Δ_t a) - 1)/a, or Δ_t for the Euler flag) and H_{c-1} the state
+// entering chunk c (P x N):
 //
-// Per group g the call gathers the group's channels into the scan's layout
-// (batch, channels, L) in fp32 (x, the per-channel Δ, z, dy; B, C as (batch, N,
-// L); the per-channel A, D, bias tables; the states), runs ssm_scan_bwd with
-// float32 I/O (so no derivative is rounded before its sums over channels),
-// then scatters dx, dz, dB, dC, d init_state back to SSD's layouts and adds the
-// per-head sums in a fixed order.
+//   y_t  = exp(s_t) H_{c-1} C_t + Σ_{τ<=t} M[t][τ] x_τ + D x_t,
+//          M[t][τ] = (C_t·B_τ) exp(s_t - s_τ) β_τ                (τ <= t)
+//   H_c  = exp(s_end) H_{c-1} + Σ_τ exp(s_end - s_τ) β_τ x_τ B_τᵀ,
+//
+// and the output is y_t · silu(z_t).  The summary page ("Mamba: Linear-Time
+// Sequence Modeling", §4c) trains without storing the expanded states: the
+// backward recomputes them.  Its derivatives follow from that chunked form by
+// the chain rule.  With ḡ_t = dy_t · silu(z_t) (the derivative reaching y_t)
+// and dH_c the derivative reaching chunk c's end state from the chunks after it
+// (d final_state for the last; dH_{c-1} = exp(s_end(c)) dH_c + Σ_{t in c}
+// exp(s_t) ḡ_t C_tᵀ, and d init_state = dH_{-1}):
+//
+//   dx_τ  = D ḡ_τ + Σ_t M[t][τ] ḡ_t + β_τ exp(s_end - s_τ) dH_c B_τ
+//   dC_t  = exp(s_t) H_{c-1}ᵀ ḡ_t + Σ_τ dML[t][τ] B_τ
+//   dB_τ  = Σ_t dML[t][τ] C_t + β_τ exp(s_end - s_τ) dH_cᵀ x_τ
+//   with dM[t][τ] = ḡ_t·x_τ and dML = dM ∘ (exp(s_t - s_τ) β_τ)  (τ <= t);
+//   dβ_τ  = Σ_t dM[t][τ] (C_t·B_τ) exp(s_t - s_τ) + r_τ,
+//           r_τ = exp(s_end - s_τ) x_τ·(dH_c B_τ);
+//   ds_t  = Σ_τ K[t][τ] - Σ_τ' K[τ'][t] + exp(s_t) ḡ_t·(H_{c-1} C_t) - β_t r_t,
+//           K = dM ∘ M, and ds_end gains exp(s_end) <dH_c, H_{c-1}> + Σ_τ β_τ r_τ;
+//   dℓ_k  = Σ_{t>=k in the chunk} ds_t   (s is the running sum of ℓ_k = Δ_k a),
+//   dΔ_k  = dℓ_k a + dβ_k exp(ℓ_k) (Euler: + dβ_k),
+//   da   += dℓ_k Δ_k + dβ_k (Δ_k exp(ℓ_k) - β_k)/a (the limit Δ²/2 at a = 0;
+//           Euler: no β term), then dΔ_raw = dΔ σ(Δ_raw + bias) for softplus;
+//   dz_t  = dy_t · y_t (before the gate) · silu'(z_t),  dD += Σ ḡ·x.
+//
+// Kernels (all arithmetic in fp32 on the CUDA cores: the parameter
+// derivatives sum many products of fp32 intermediates, which bf16 tensor-core
+// operands would round to 8 bits):
+//  1. the forward's step terms (s, β) per (batch, chunk, head);
+//  2. a forward walk over the chunks writing each chunk's entering state H_{c-1}
+//     in fp32, and a reverse walk writing each dH_c and d init_state; both are
+//     parallel over (batch, head, a quarter of the state's rows);
+//  3. one block per (batch, chunk, head) for everything above: the chunk's
+//     operands in shared memory, its products as register-tiled loops over
+//     shared memory; per-head partial dB, dC, da, d dt_bias, dD to a workspace;
+//  4. the sums over a group's heads (dB, dC) and over batch and chunks (da,
+//     d dt_bias, dD) in a fixed order, so results repeat bit for bit.
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "../../include/ssm.h"
 #include "ssm_device.cuh"
+#include "ssm_internal.h"
 
 namespace ssm {
+namespace {
 
-struct SsdBwdGlue {
-  // SSD side (Mamba-2 layouts)
+constexpr int kQ = kSsdChunk;  // chunk length
+constexpr int kP = 64;         // head dimension
+constexpr int kWalkThreads = 128;
+constexpr int kChunkThreads = 256;  // 8 warps: 8 rows of every 64-row product each
+
+struct SsdBwd {
   const __nv_bfloat16 *x, *dt, *z, *dy, *B, *C;
   const float *A, *D, *dt_bias, *init, *dfin;
   __nv_bfloat16 *dx, *ddt, *dz;
   float *dA, *dB, *dC, *dD, *ddt_bias, *dinit;
-  // scan side (one group): (batch, Dc, L) rows, (batch, N, L) B/C, (Dc, N) A
-  float *u, *dl, *zz, *dyy, *du, *ddl, *dzz, *Bg, *Cg, *dBg, *dCg, *Ag, *dAg, *Dg, *biasg, *dDg,
-      *dbiasg, *initg, *dfing, *dinitg;
-  int64_t batch, L, H, P, G, N, hpg, Dc, g;
+  const float* terms;  // [b][c][h][kSsdTermsRec]: s | β | w
+  float* Hin;          // [b][c][h][P][N]: the state entering chunk c
+  float* dHc;          // [b][c][h][P][N]: the derivative reaching chunk c's end state
+  float* dBp;          // [b][c][h][Q][N]: per-head dB
+  float* dCp;          // [b][c][h][Q][N]: per-head dC
+  float* hpart;        // [b][c][h][4]: da, d dt_bias, dD
+  int64_t batch, L, H, G, nch;
+  int softplus, euler;
 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float sigmoid_precise(float x) { return 1.0f / (1.0f + expf(-x)); }
 
-// the group's inputs in the scan's layouts
-__global__ void ssd_bwd_gather_kernel(const SsdBwdGlue a) {
-  const int64_t HP = a.H * a.P, c0 = a.g * a.hpg * a.P, h0 = a.g * a.hpg;
-  const int64_t nrow = a.batch * a.Dc * a.L;      // (b, c, t), t fastest
-  const int64_t nbc = a.batch * a.N * a.L;        // (b, n, t)
-  const int64_t nst = a.batch * a.Dc * a.N;       // (b, c, n)
-  const int64_t ntab = a.Dc * a.N;                // (c, n)
-  const int64_t total = nrow + nbc + nst + ntab + a.Dc;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    if (i < nrow) {
-      const int64_t t = i % a.L, bc = i / a.L, c = bc % a.Dc, b = bc / a.Dc;
-      const int64_t src = (b * a.L + t) * HP + c0 + c;
-      a.u[i] = bf(a.x[src]);
-      a.dyy[i] = bf(a.dy[src]);
-      if (a.z) a.zz[i] = bf(a.z[src]);
-      a.dl[i] = bf(a.dt[(b * a.L + t) * a.H + h0 + c / a.P]);
-    } else if (i < nrow + nbc) {
-      const int64_t e = i - nrow;
-      const int64_t t = e % a.L, bn = e / a.L, n = bn % a.N, b = bn / a.N;
-      const int64_t src = ((b * a.L + t) * a.G + a.g) * a.N + n;
-      a.Bg[e] = bf(a.B[src]);
-      a.Cg[e] = bf(a.C[src]);
-    } else if (i < nrow + nbc + nst) {
-      const int64_t e = i - nrow - nbc;
-      const int64_t n = e % a.N, bc = e / a.N, c = bc % a.Dc, b = bc / a.Dc;
-      const int64_t src = (b * HP + c0 + c) * a.N + n;
-      if (a.init) a.initg[e] = a.init[src];
-      if (a.dfin) a.dfing[e] = a.dfin[src];
-    } else if (i < nrow + nbc + nst + ntab) {
-      const int64_t e = i - nrow - nbc - nst;
-      a.Ag[e] = a.A[h0 + (e / a.N) / a.P];
-    } else {
-      const int64_t c = i - nrow - nbc - nst - ntab;
-      if (a.D) a.Dg[c] = a.D[h0 + c / a.P];
-      if (a.dt_bias) a.biasg[c] = a.dt_bias[h0 + c / a.P];
-    }
+// ---------------------------------------------------------------------------
+// 2a. Forward walk: H_c = exp(s_end) H_{c-1} + Σ_τ w_τ x_τ B_τᵀ, storing every
+//     H_{c-1}.  Block (quarter of the rows, head, batch); thread t holds row
+//     p = 16 q + t / 8 and the columns n = 4 (t % 8 + 8 j) .. + 3.
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(kWalkThreads) ssd_bwd_fwalk_kernel(const SsdBwd a) {
+  constexpr int NV = N / 32;  // float4 column groups a thread holds
+  __shared__ __align__(16) float sB[kQ * N];
+  __shared__ float sX[kQ * 16];  // w_τ x_τ[p] for the block's 16 rows
+  __shared__ float sEnd;
+  const int tid = threadIdx.x;
+  const int q = blockIdx.x, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int pl = tid / 8, p = 16 * q + pl, g = h / (int)(a.H / a.G);
+  float4 hv[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int n = 4 * (tid % 8 + 8 * j);
+    hv[j] = a.init ? *reinterpret_cast<const float4*>(a.init + ((b * a.H + h) * kP + p) * N + n)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-}
-
-// the group's derivatives back in SSD's layouts; the per-head sums over the
-// head's P channels (and, for dA, its N states) in a fixed order
-__global__ void ssd_bwd_scatter_kernel(const SsdBwdGlue a) {
-  const int64_t HP = a.H * a.P, c0 = a.g * a.hpg * a.P, h0 = a.g * a.hpg;
-  const int64_t nrow = a.batch * a.Dc * a.L;      // (b, c, t)
-  const int64_t nbc = a.batch * a.N * a.L;        // (b, n, t)
-  const int64_t nst = a.batch * a.Dc * a.N;       // (b, c, n)
-  const int64_t ndt = a.batch * a.L * a.hpg;      // (b, t, head of the group)
-  const int64_t total = nrow + nbc + nst + ndt + a.hpg;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    if (i < nrow) {
-      const int64_t t = i % a.L, bc = i / a.L, c = bc % a.Dc, b = bc / a.Dc;
-      const int64_t dst = (b * a.L + t) * HP + c0 + c;
-      a.dx[dst] = __float2bfloat16_rn(a.du[i]);
-      if (a.dz) a.dz[dst] = __float2bfloat16_rn(a.dzz[i]);
-    } else if (i < nrow + nbc) {
-      const int64_t e = i - nrow;
-      const int64_t t = e % a.L, bn = e / a.L, n = bn % a.N, b = bn / a.N;
-      const int64_t dst = ((b * a.L + t) * a.G + a.g) * a.N + n;
-      a.dB[dst] = a.dBg[e];
-      a.dC[dst] = a.dCg[e];
-    } else if (i < nrow + nbc + nst) {
-      const int64_t e = i - nrow - nbc;
-      const int64_t n = e % a.N, bc = e / a.N, c = bc % a.Dc, b = bc / a.Dc;
-      if (a.dinit) a.dinit[(b * HP + c0 + c) * a.N + n] = a.dinitg[e];
-    } else if (i < nrow + nbc + nst + ndt) {
-      const int64_t e = i - nrow - nbc - nst;
-      const int64_t hl = e % a.hpg, bt = e / a.hpg, t = bt % a.L, b = bt / a.L;
-      float s = 0.f;
-      for (int64_t p = 0; p < a.P; ++p) s += a.ddl[(b * a.Dc + hl * a.P + p) * a.L + t];
-      a.ddt[(b * a.L + t) * a.H + h0 + hl] = __float2bfloat16_rn(s);
-    } else {
-      const int64_t hl = i - nrow - nbc - nst - ndt;
-      float sa = 0.f, sd = 0.f, sb = 0.f;
-      for (int64_t p = 0; p < a.P; ++p) {
-        const int64_t c = hl * a.P + p;
-        for (int64_t n = 0; n < a.N; ++n) sa += a.dAg[c * a.N + n];
-        sd += a.dDg[c];
-        sb += a.dbiasg[c];
+  for (int64_t c = 0; c < a.nch; ++c) {
+    const int64_t unit = (b * a.nch + c) * a.H + h;
+    float* out = a.Hin + unit * kP * N + (int64_t)p * N;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
+    const int64_t t0 = c * kQ;
+    const int valid = (int)min64(kQ, a.L - t0);
+    const float* tr = a.terms + unit * kSsdTermsRec;
+    __syncthreads();  // the previous chunk's readers are done
+    for (int e = tid; e < kQ * N / 8; e += kWalkThreads) {  // B: 8 bf16 a vector
+      const int tau = e / (N / 8), n8 = e % (N / 8);
+      float v[8];
+      if (tau < valid) {
+        vecio<__nv_bfloat16, 8>::load(a.B + ((b * a.L + t0 + tau) * a.G + g) * N + 8 * n8, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
       }
-      a.dA[h0 + hl] = sa;
-      if (a.dD) a.dD[h0 + hl] = sd;
-      if (a.ddt_bias) a.ddt_bias[h0 + hl] = sb;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sB[tau * N + 8 * n8 + i] = v[i];
+    }
+    for (int e = tid; e < kQ * 16; e += kWalkThreads) {
+      const int tau = e / 16, pp = e % 16;
+      sX[e] = tau < valid ? tr[2 * kQ + tau] * bf(a.x[((b * a.L + t0 + tau) * a.H + h) * kP + 16 * q + pp])
+                          : 0.f;
+    }
+    if (tid == 0) sEnd = expf(tr[kQ - 1]);
+    __syncthreads();
+    const float e_end = sEnd;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      hv[j].x *= e_end; hv[j].y *= e_end; hv[j].z *= e_end; hv[j].w *= e_end;
+    }
+    for (int tau = 0; tau < kQ; ++tau) {
+      const float xv = sX[tau * 16 + pl];
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const float4 bv = *reinterpret_cast<const float4*>(sB + tau * N + 4 * (tid % 8 + 8 * j));
+        hv[j].x = fmaf(xv, bv.x, hv[j].x);
+        hv[j].y = fmaf(xv, bv.y, hv[j].y);
+        hv[j].z = fmaf(xv, bv.z, hv[j].z);
+        hv[j].w = fmaf(xv, bv.w, hv[j].w);
+      }
     }
   }
 }
 
-}  // namespace ssm
+// ---------------------------------------------------------------------------
+// 2b. Reverse walk: dH_{c-1} = exp(s_end(c)) dH_c + Σ_{t in c} exp(s_t) ḡ_t C_tᵀ
+//     from dH_{last} = d final_state, storing every dH_c; d init_state = dH_{-1}.
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(kWalkThreads) ssd_bwd_rwalk_kernel(const SsdBwd a) {
+  constexpr int NV = N / 32;
+  __shared__ __align__(16) float sC[kQ * N];
+  __shared__ float sG[kQ * 16];  // exp(s_t) ḡ_t[p] for the block's 16 rows
+  __shared__ float sEnd;
+  const int tid = threadIdx.x;
+  const int q = blockIdx.x, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int pl = tid / 8, p = 16 * q + pl, g = h / (int)(a.H / a.G);
+  float4 hv[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int n = 4 * (tid % 8 + 8 * j);
+    hv[j] = a.dfin ? *reinterpret_cast<const float4*>(a.dfin + ((b * a.H + h) * kP + p) * N + n)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int64_t c = a.nch - 1; c >= 0; --c) {
+    const int64_t unit = (b * a.nch + c) * a.H + h;
+    float* out = a.dHc + unit * kP * N + (int64_t)p * N;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
+    const int64_t t0 = c * kQ;
+    const int valid = (int)min64(kQ, a.L - t0);
+    const float* tr = a.terms + unit * kSsdTermsRec;
+    __syncthreads();
+    for (int e = tid; e < kQ * N / 8; e += kWalkThreads) {
+      const int t = e / (N / 8), n8 = e % (N / 8);
+      float v[8];
+      if (t < valid) {
+        vecio<__nv_bfloat16, 8>::load(a.C + ((b * a.L + t0 + t) * a.G + g) * N + 8 * n8, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sC[t * N + 8 * n8 + i] = v[i];
+    }
+    for (int e = tid; e < kQ * 16; e += kWalkThreads) {
+      const int t = e / 16, pp = e % 16;
+      float gv = 0.f;
+      if (t < valid) {
+        const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + 16 * q + pp;
+        gv = bf(a.dy[o]);
+        if (a.z) gv *= silu_precise(bf(a.z[o]));
+        gv *= expf(tr[t]);
+      }
+      sG[e] = gv;
+    }
+    if (tid == 0) sEnd = expf(tr[kQ - 1]);
+    __syncthreads();
+    const float e_end = sEnd;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      hv[j].x *= e_end; hv[j].y *= e_end; hv[j].z *= e_end; hv[j].w *= e_end;
+    }
+    for (int t = 0; t < kQ; ++t) {
+      const float gv = sG[t * 16 + pl];
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const float4 cv = *reinterpret_cast<const float4*>(sC + t * N + 4 * (tid % 8 + 8 * j));
+        hv[j].x = fmaf(gv, cv.x, hv[j].x);
+        hv[j].y = fmaf(gv, cv.y, hv[j].y);
+        hv[j].z = fmaf(gv, cv.z, hv[j].z);
+        hv[j].w = fmaf(gv, cv.w, hv[j].w);
+      }
+    }
+  }
+  if (a.dinit) {
+    float* out = a.dinit + ((b * a.H + h) * kP + p) * N;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
+  }
+}
 
-namespace {
+// ---------------------------------------------------------------------------
+// 3. Per (batch, chunk, head): every derivative of the chunk.
+// ---------------------------------------------------------------------------
+// acc[i][r] += Σ_k A(k, i0 + i) B(k, lane + 32 r), A(k, i) = A[k ak + i ai],
+// B(k, j) = Bm[k bk + j bj]: a warp's 32 lanes take interleaved columns (the
+// strides along j are 1 or odd, so the lanes' loads hit distinct banks) and
+// share its RM rows (broadcast loads).
+template <int RM, int RN>
+__device__ __forceinline__ void mm_acc(float (&acc)[RM][RN], int K, const float* A, int ak, int ai,
+                                       int i0, const float* Bm, int bk, int bj, int lane) {
+#pragma unroll 4
+  for (int k = 0; k < K; ++k) {
+    float av[RM], bv[RN];
+#pragma unroll
+    for (int i = 0; i < RM; ++i) av[i] = A[k * ak + (i0 + i) * ai];
+#pragma unroll
+    for (int r = 0; r < RN; ++r) bv[r] = Bm[k * bk + (lane + 32 * r) * bj];
+#pragma unroll
+    for (int i = 0; i < RM; ++i)
+#pragma unroll
+      for (int r = 0; r < RN; ++r) acc[i][r] = fmaf(av[i], bv[r], acc[i][r]);
+  }
+}
+template <int RM, int RN> __device__ __forceinline__ void mm_zero(float (&acc)[RM][RN]) {
+#pragma unroll
+  for (int i = 0; i < RM; ++i)
+#pragma unroll
+    for (int r = 0; r < RN; ++r) acc[i][r] = 0.f;
+}
+
+// Shared memory of the chunk kernel (floats; rows padded to odd lengths).
+template <int N> struct ChunkBwdSmem {
+  static constexpr int LP = kP + 1, LN = N + 1, LQ = kQ + 1;
+  static constexpr int oX = 0;                 // x      [τ][p]
+  static constexpr int oG = oX + kQ * LP;      // ḡ      [t][p]
+  static constexpr int oC = oG + kQ * LP;      // C      [t][n]
+  static constexpr int oB = oC + kQ * LN;      // B      [τ][n]
+  static constexpr int oH = oB + kQ * LN;      // H_{c-1} [p][n]
+  static constexpr int oD = oH + kP * LN;      // dH_c   [p][n]
+  static constexpr int oE = oD + kP * LN;      // (C_t·B_τ) exp(s_t - s_τ), τ <= t   [t][τ]
+  static constexpr int oL = oE + kQ * LQ;      // dML    [t][τ]
+  static constexpr int oS = oL + kQ * LQ;      // s, β, exp(s), exp(s_end - s)
+  static constexpr int oR = oS + 4 * kQ;       // per-warp column sums [2][8][Q]
+  static constexpr int oV = oR + 2 * 8 * kQ;   // ds parts, dβ, r, row and column sums [6][Q]; scalars
+  static constexpr int kFloats = oV + 6 * kQ + 8;
+  static constexpr size_t kBytes = (size_t)kFloats * 4;
+};
+
+template <int N>
+__global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const SsdBwd a) {
+  using S = ChunkBwdSmem<N>;
+  constexpr int LP = S::LP, LN = S::LN, LQ = S::LQ;
+  constexpr int RN = N / 32;
+  extern __shared__ float sm[];
+  float* sX = sm + S::oX;
+  float* sG = sm + S::oG;
+  float* sC = sm + S::oC;
+  float* sB = sm + S::oB;
+  float* sH = sm + S::oH;
+  float* sD = sm + S::oD;
+  float* sE = sm + S::oE;
+  float* sL = sm + S::oL;
+  float* sS = sm + S::oS;        // s
+  float* sBeta = sS + kQ;        // β
+  float* sEs = sS + 2 * kQ;      // exp(s_t)
+  float* sEe = sS + 3 * kQ;      // exp(s_end - s_t)
+  float* sR = sm + S::oR;        // [2][8][Q]
+  float* sV = sm + S::oV;
+  float* vRowK = sV;             // Σ_τ K[t][τ]
+  float* vInter = sV + kQ;       // exp(s_t) ḡ_t·(H C_t)
+  float* vDbeta = sV + 2 * kQ;   // Σ_t dM CB exp   (then + r)
+  float* vR = sV + 3 * kQ;       // r_τ
+  float* vColK = sV + 4 * kQ;    // Σ_t K[t][τ]
+  float* vScal = sV + 6 * kQ;    // <dH, H>, Σ ḡ·x
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int g = h / (int)(a.H / a.G);
+  const int64_t unit = (b * a.nch + c) * a.H + h;
+  const int64_t t0 = (int64_t)c * kQ;
+  const int valid = (int)min64(kQ, a.L - t0);
+  const float ah = a.A[h];
+  const float Dh = a.D ? a.D[h] : 0.f;
+  const int i0 = 8 * warp;  // this warp's 8 rows of every product
+
+  // ---- stage the chunk ----
+  const float* tr = a.terms + unit * kSsdTermsRec;
+  for (int e = tid; e < kQ; e += kChunkThreads) {
+    sS[e] = tr[e];
+    sBeta[e] = tr[kQ + e];
+    sEs[e] = expf(tr[e]);
+    sEe[e] = expf(tr[kQ - 1] - tr[e]);
+  }
+  float gx = 0.f;  // Σ ḡ·x over this thread's elements (for dD)
+  for (int e = tid; e < kQ * kP; e += kChunkThreads) {
+    const int t = e / kP, pp = e % kP;
+    float xv = 0.f, gv = 0.f;
+    if (t < valid) {
+      const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + pp;
+      xv = bf(a.x[o]);
+      gv = bf(a.dy[o]);
+      if (a.z) gv *= silu_precise(bf(a.z[o]));
+    }
+    sX[t * LP + pp] = xv;
+    sG[t * LP + pp] = gv;
+    gx = fmaf(gv, xv, gx);
+  }
+  for (int e = tid; e < kQ * N; e += kChunkThreads) {
+    const int t = e / N, n = e % N;
+    float cv = 0.f, bv = 0.f;
+    if (t < valid) {
+      const int64_t o = ((b * a.L + t0 + t) * a.G + g) * N + n;
+      cv = bf(a.C[o]);
+      bv = bf(a.B[o]);
+    }
+    sC[t * LN + n] = cv;
+    sB[t * LN + n] = bv;
+  }
+  float hd = 0.f;  // <dH, H> over this thread's elements
+  for (int e = tid; e < kP * N; e += kChunkThreads) {
+    const int pp = e / N, n = e % N;
+    const float hv = a.Hin[unit * kP * N + e], dv = a.dHc[unit * kP * N + e];
+    sH[pp * LN + n] = hv;
+    sD[pp * LN + n] = dv;
+    hd = fmaf(hv, dv, hd);
+  }
+  // block sums of hd and gx: warp shuffles, then warp 0
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    hd += __shfl_xor_sync(0xffffffffu, hd, o);
+    gx += __shfl_xor_sync(0xffffffffu, gx, o);
+  }
+  if (lane == 0) {
+    sR[warp] = hd;
+    sR[8 + warp] = gx;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float s1 = 0.f, s2 = 0.f;
+    for (int w = 0; w < 8; ++w) {
+      s1 += sR[w];
+      s2 += sR[8 + w];
+    }
+    vScal[0] = s1;
+    vScal[1] = s2;
+  }
+  __syncthreads();
+
+  // ---- E = (C_t·B_τ) exp(s_t - s_τ) for τ <= t (else 0) ----
+  {
+    float acc[8][2];
+    mm_zero(acc);
+    mm_acc<8, 2>(acc, N, sC, 1, LN, i0, sB, 1, LN, lane);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int t = i0 + i, tau = lane + 32 * r;
+        sE[t * LQ + tau] = tau <= t ? acc[i][r] * expf(sS[t] - sS[tau]) : 0.f;
+      }
+  }
+  __syncthreads();
+
+  // ---- y before the gate (for dz) and the inter-chunk ds term ----
+  {
+    float acc[8][2];
+    mm_zero(acc);
+    mm_acc<8, 2>(acc, N, sC, 1, LN, i0, sH, 1, LN, lane);  // (C Hᵀ)[t][p]
+    float inter[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = i0 + i;
+      float part = 0.f;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        acc[i][r] *= sEs[t];
+        part = fmaf(sG[t * LP + lane + 32 * r], acc[i][r], part);
+      }
+      inter[i] = part;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) inter[i] += __shfl_xor_sync(0xffffffffu, inter[i], o);
+      if (lane == i) vInter[i0 + i] = inter[i];
+    }
+    // + Σ_τ E[t][τ] β_τ x_τ[p] + D x_t[p]
+    float accm[8][2];
+    mm_zero(accm);
+#pragma unroll 4
+    for (int k = 0; k < kQ; ++k) {
+      float av[8], bv[2];
+      const float bk = sBeta[k];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) av[i] = sE[(i0 + i) * LQ + k];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) bv[r] = bk * sX[k * LP + lane + 32 * r];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) accm[i][r] = fmaf(av[i], bv[r], accm[i][r]);
+    }
+    if (a.dz) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int t = i0 + i;
+        if (t >= valid) continue;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int pp = lane + 32 * r;
+          const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + pp;
+          const float y = acc[i][r] + accm[i][r] + Dh * sX[t * LP + pp];
+          const float zv = bf(a.z[o]);
+          const float sg = sigmoid_precise(zv);
+          a.dz[o] = __float2bfloat16_rn(bf(a.dy[o]) * y * sg * fmaf(zv, 1.f - sg, 1.f));
+        }
+      }
+    }
+  }
+
+  // ---- dM = ḡ xᵀ: dML, K = dM ∘ M, the dβ sums ----
+  {
+    float acc[8][2];
+    mm_zero(acc);
+    mm_acc<8, 2>(acc, kP, sG, 1, LP, i0, sX, 1, LP, lane);  // dM[t][τ]
+    float rowK[8], colK[2] = {0.f, 0.f}, colB[2] = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = i0 + i;
+      float rk = 0.f;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int tau = lane + 32 * r;
+        const float e = sE[t * LQ + tau];        // 0 above the diagonal
+        const float dm = tau <= t ? acc[i][r] : 0.f;
+        const float k = dm * e * sBeta[tau];     // dM ∘ M
+        rk += k;
+        colK[r] += k;
+        colB[r] = fmaf(dm, e, colB[r]);          // dM (C·B) exp
+        sL[t * LQ + tau] = tau <= t ? dm * expf(sS[t] - sS[tau]) * sBeta[tau] : 0.f;
+      }
+      rowK[i] = rk;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) rowK[i] += __shfl_xor_sync(0xffffffffu, rowK[i], o);
+      if (lane == i) vRowK[i0 + i] = rowK[i];
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      sR[warp * kQ + lane + 32 * r] = colK[r];
+      sR[8 * kQ + warp * kQ + lane + 32 * r] = colB[r];
+    }
+  }
+  __syncthreads();
+  if (tid < kQ) {  // column sums over the 8 warps, in order
+    float ck = 0.f, cb = 0.f;
+    for (int w = 0; w < 8; ++w) {
+      ck += sR[w * kQ + tid];
+      cb += sR[8 * kQ + w * kQ + tid];
+    }
+    vColK[tid] = ck;
+    vDbeta[tid] = cb;
+  }
+  __syncthreads();
+
+  // ---- dx = D ḡ + Mᵀ ḡ + β exp(s_end - s) dH B; r_τ = exp(s_end - s_τ) x_τ·(dH B_τ) ----
+  {
+    float acc[8][2], accd[8][2];
+    mm_zero(acc);
+    mm_zero(accd);
+    mm_acc<8, 2>(acc, kQ, sE, LQ, 1, i0, sG, LP, 1, lane);   // Σ_t E[t][τ] ḡ_t[p]
+    mm_acc<8, 2>(accd, N, sB, 1, LN, i0, sD, 1, LN, lane);  // (B dHᵀ)[τ][p]
+    float rr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int tau = i0 + i;
+      float part = 0.f;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) part = fmaf(sX[tau * LP + lane + 32 * r], accd[i][r], part);
+      rr[i] = part;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) rr[i] += __shfl_xor_sync(0xffffffffu, rr[i], o);
+      if (lane == i) vR[i0 + i] = rr[i] * sEe[i0 + i];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int tau = i0 + i;
+      if (tau >= valid) continue;
+      const float be = sBeta[tau], bee = be * sEe[tau];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int pp = lane + 32 * r;
+        const float v = fmaf(Dh, sG[tau * LP + pp], fmaf(be, acc[i][r], bee * accd[i][r]));
+        a.dx[((b * a.L + t0 + tau) * a.H + h) * kP + pp] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+
+  // ---- dC = exp(s) ḡ H + dML B;  dB = dMLᵀ C + β exp(s_end - s) x dH ----
+  {
+    float acc[8][RN];
+    mm_zero(acc);
+    mm_acc<8, RN>(acc, kP, sG, 1, LP, i0, sH, LN, 1, lane);  // (ḡ H)[t][n]
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int r = 0; r < RN; ++r) acc[i][r] *= sEs[i0 + i];
+    mm_acc<8, RN>(acc, kQ, sL, 1, LQ, i0, sB, LN, 1, lane);  // + (dML B)[t][n]
+    float* out = a.dCp + unit * kQ * N;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int r = 0; r < RN; ++r) out[(i0 + i) * N + lane + 32 * r] = acc[i][r];
+  }
+  {
+    float acc[8][RN], accx[8][RN];
+    mm_zero(acc);
+    mm_zero(accx);
+    mm_acc<8, RN>(acc, kQ, sL, LQ, 1, i0, sC, LN, 1, lane);  // (dMLᵀ C)[τ][n]
+    mm_acc<8, RN>(accx, kP, sX, 1, LP, i0, sD, LN, 1, lane);  // (x dH)[τ][n]
+    float* out = a.dBp + unit * kQ * N;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float w = sBeta[i0 + i] * sEe[i0 + i];
+#pragma unroll
+      for (int r = 0; r < RN; ++r) out[(i0 + i) * N + lane + 32 * r] = fmaf(w, accx[i][r], acc[i][r]);
+    }
+  }
+  __syncthreads();
+
+  // ---- ds, dℓ (reverse running sum), dΔ, da, d dt_bias ----
+  if (warp == 0) {
+    float dsv[2], dbv[2];
+    float qsum = 0.f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = lane + 32 * r;
+      const float q = sBeta[t] * vR[t];  // β_t r_t
+      qsum += q;
+      dsv[r] = vRowK[t] - vColK[t] + vInter[t] - q;
+      dbv[r] = vDbeta[t] + vR[t];
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
+    if (lane == 31) dsv[1] += sEs[kQ - 1] * vScal[0] + qsum;  // ds_end (s_end = s_{Q-1})
+    // dℓ_k = Σ_{t >= k} ds_t: suffix sums over the 64 steps (lane holds k and k + 32)
+    float hi = dsv[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_down_sync(0xffffffffu, hi, o);
+      if (lane + o < 32) hi += v;
+    }
+    const float hi_total = __shfl_sync(0xffffffffu, hi, 0);
+    float lo = dsv[0];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_down_sync(0xffffffffu, lo, o);
+      if (lane + o < 32) lo += v;
+    }
+    const float dl[2] = {lo + hi_total, hi};
+    const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
+    float da = 0.f, dbias = 0.f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = lane + 32 * r;
+      if (t >= valid) continue;
+      const int64_t o = (b * a.L + t0 + t) * a.H + h;
+      const float xr = bf(a.dt[o]) + bias;
+      const float dtv = a.softplus ? softplus_precise(xr) : xr;
+      const float sig = a.softplus ? sigmoid_precise(xr) : 1.f;
+      const float ell = dtv * ah, el = expf(ell);
+      const float be = sBeta[t];
+      float ddt = dl[r] * ah + dbv[r] * (a.euler ? 1.f : el);
+      float dav = dl[r] * dtv;
+      if (!a.euler) dav += dbv[r] * (ah != 0.f ? (dtv * el - be) / ah : 0.5f * dtv * dtv);
+      const float draw = ddt * sig;
+      a.ddt[o] = __float2bfloat16_rn(draw);
+      da += dav;
+      dbias += draw;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      da += __shfl_xor_sync(0xffffffffu, da, o);
+      dbias += __shfl_xor_sync(0xffffffffu, dbias, o);
+    }
+    if (lane == 0) {
+      float* hp = a.hpart + unit * 4;
+      hp[0] = da;
+      hp[1] = dbias;
+      hp[2] = vScal[1];
+      hp[3] = 0.f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 4. Sums in a fixed order: dB, dC over the group's heads; dA, d dt_bias, dD
+//    over batch rows and chunks.
+// ---------------------------------------------------------------------------
+__global__ void ssd_bwd_reduce_kernel(const SsdBwd a, int N) {
+  const int64_t hpg = a.H / a.G;
+  const int64_t nbc = a.batch * a.L * a.G * N;  // (b, t, g, n)
+  const int64_t total = 2 * nbc + a.H;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < 2 * nbc) {
+      const bool isC = i >= nbc;
+      const int64_t e = isC ? i - nbc : i;
+      const int64_t n = e % N, bt = e / N / a.G, gg = (e / N) % a.G;
+      const int64_t t = bt % a.L, b = bt / a.L, c = t / kQ;
+      const float* part = (isC ? a.dCp : a.dBp) +
+                          (((b * a.nch + c) * a.H + gg * hpg) * kQ + (t - c * kQ)) * N + n;
+      float s = 0.f;
+      for (int64_t k = 0; k < hpg; ++k) s += part[k * kQ * N];
+      (isC ? a.dC : a.dB)[e] = s;
+    } else {
+      const int64_t h = i - 2 * nbc;
+      float da = 0.f, db = 0.f, dd = 0.f;
+      for (int64_t bc = 0; bc < a.batch * a.nch; ++bc) {
+        const float* hp = a.hpart + (bc * a.H + h) * 4;
+        da += hp[0];
+        db += hp[1];
+        dd += hp[2];
+      }
+      a.dA[h] = da;
+      if (a.ddt_bias) a.ddt_bias[h] = db;
+      if (a.dD) a.dD[h] = dd;
+    }
+  }
+}
+
+template <int N>
+cudaError_t ssd_bwd_typed(const SsdBwd& a, cudaStream_t st) {
+  const dim3 wg(kP / 16, (unsigned)a.H, (unsigned)a.batch);
+  ssd_bwd_fwalk_kernel<N><<<wg, kWalkThreads, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ssd_bwd_rwalk_kernel<N><<<wg, kWalkThreads, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  constexpr size_t bytes = ChunkBwdSmem<N>::kBytes;
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(ssd_bwd_chunk_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bytes);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  ssd_bwd_chunk_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch), kChunkThreads,
+                            bytes, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t total = 2 * a.batch * a.L * a.G * N + a.H;
+  const int64_t blocks = (total + 255) / 256;
+  ssd_bwd_reduce_kernel<<<(unsigned)(blocks < 148 * 16 ? blocks : 148 * 16), 256, 0, st>>>(a, N);
+  return cudaGetLastError();
+}
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct SsdBwdLayout {
-  size_t o[20];  // the group buffers, in SsdBwdGlue's scan-side order
-  size_t o_scan, scan_bytes, bytes;
+  size_t o_terms, o_hin, o_dh, o_db, o_dc, o_hp, bytes;
 };
 
-SsdBwdLayout ssd_bwd_layout(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N) {
+SsdBwdLayout ssd_bwd_layout(int64_t batch, int64_t L, int64_t H, int64_t N) {
   SsdBwdLayout w{};
-  const size_t Dc = (size_t)(H / G) * (size_t)P;
-  const size_t row = up256((size_t)batch * Dc * (size_t)L * 4);
-  const size_t bc = up256((size_t)batch * (size_t)N * (size_t)L * 4);
-  const size_t tab = up256(Dc * (size_t)N * 4), vec = up256(Dc * 4);
-  const size_t st = up256((size_t)batch * Dc * (size_t)N * 4);
-  // u dl zz dyy du ddl dzz | Bg Cg dBg dCg | Ag dAg | Dg biasg dDg dbiasg | initg dfing dinitg
-  const size_t sizes[20] = {row, row, row, row, row, row, row, bc, bc, bc, bc,
-                            tab, tab, vec, vec, vec, vec, st, st, st};
-  size_t off = 0;
-  for (int k = 0; k < 20; ++k) {
-    w.o[k] = off;
-    off += sizes[k];
-  }
-  w.o_scan = off;
-  w.scan_bytes = up256(ssm_scan_bwd_workspace_bytes(batch, (int64_t)Dc, L, N));
-  w.bytes = off + w.scan_bytes;
+  const size_t nch = (size_t)((L + kQ - 1) / kQ);
+  const size_t units = (size_t)batch * nch * (size_t)H;
+  w.o_terms = 0;
+  w.o_hin = w.o_terms + up256(units * kSsdTermsRec * 4);
+  w.o_dh = w.o_hin + up256(units * kP * (size_t)N * 4);
+  w.o_db = w.o_dh + up256(units * kP * (size_t)N * 4);
+  w.o_dc = w.o_db + up256(units * kQ * (size_t)N * 4);
+  w.o_hp = w.o_dc + up256(units * kQ * (size_t)N * 4);
+  w.bytes = w.o_hp + up256(units * 4 * 4);
   return w;
 }
 
@@ -163,17 +714,19 @@ bool ssd_shape_ok(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim
                   int64_t dstate) {
   if (batch <= 0 || seqlen <= 0 || nheads <= 0 || ngroups <= 0 || nheads % ngroups != 0) return false;
   if (headdim != 64 || (dstate != 64 && dstate != 128) || batch > 65535) return false;
-  return (double)batch * (double)nheads * (double)headdim * (double)seqlen < 9.0e18;
+  const int64_t units = batch * ((seqlen + kQ - 1) / kQ) * nheads;
+  return units < (int64_t(1) << 31) && (double)batch * (double)nheads * (double)headdim * (double)seqlen < 9.0e18;
 }
 
 }  // namespace
+}  // namespace ssm
 
 extern "C" {
 
 size_t ssm_ssd_bwd_workspace_bytes(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                                    int64_t ngroups, int64_t dstate) {
-  if (!ssd_shape_ok(batch, seqlen, nheads, headdim, ngroups, dstate)) return 0;
-  return ssd_bwd_layout(batch, seqlen, nheads, headdim, ngroups, dstate).bytes;
+  if (!ssm::ssd_shape_ok(batch, seqlen, nheads, headdim, ngroups, dstate)) return 0;
+  return ssm::ssd_bwd_layout(batch, seqlen, nheads, dstate).bytes;
 }
 
 int ssm_ssd_bwd(const void* x, const void* dt, const float* dt_bias, const float* A, const void* B,
@@ -210,19 +763,28 @@ int ssm_ssd_bwd(const void* x, const void* dt, const float* dt_bias, const float
     }
     return SSM_OK;
   }
-  if (!ssd_shape_ok(batch, seqlen, nheads, headdim, ngroups, dstate)) return SSM_ERR_ARG;
+  if (!ssm::ssd_shape_ok(batch, seqlen, nheads, headdim, ngroups, dstate)) return SSM_ERR_ARG;
   if (!x || !dt || !A || !B || !C || !dy || !dx || !ddt || !dA || !dB || !dC || (z && !dz))
     return SSM_ERR_ARG;
   const void* ptrs[] = {x, dt, dt_bias, A, B, C, D, z, init_state, dy, d_final_state, dx, ddt, dA,
                         dB, dC, dD, dz, d_dt_bias, d_init_state, workspace};
   for (const void* q : ptrs)
     if (reinterpret_cast<uintptr_t>(q) & 15u) return SSM_ERR_ALIGN;
-  const SsdBwdLayout lay = ssd_bwd_layout(batch, seqlen, nheads, headdim, ngroups, dstate);
+  const ssm::SsdBwdLayout lay = ssm::ssd_bwd_layout(batch, seqlen, nheads, dstate);
   if (!workspace || workspace_bytes < lay.bytes) return SSM_ERR_WORKSPACE;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  auto f = [&](int k) { return reinterpret_cast<float*>(ws + lay.o[k]); };
-  ssm::SsdBwdGlue a{};
+  const int64_t nch = (seqlen + ssm::kQ - 1) / ssm::kQ;
+  // the forward's step terms
+  ssm::SsdArgs t{};
+  t.dt = dt; t.dt_bias = dt_bias; t.A = A;
+  t.ws_terms = reinterpret_cast<float*>(ws + lay.o_terms);
+  t.batch = batch; t.L = seqlen; t.H = nheads; t.G = ngroups; t.nch = nch;
+  t.softplus = (flags & SSM_SOFTPLUS) != 0;
+  t.euler = (flags & SSM_EULER_B) != 0;
+  if (ssm::ssd_terms_launch(t, st) != cudaSuccess) return SSM_ERR_CUDA;
+
+  ssm::SsdBwd a{};
   a.x = static_cast<const __nv_bfloat16*>(x); a.dt = static_cast<const __nv_bfloat16*>(dt);
   a.z = static_cast<const __nv_bfloat16*>(z); a.dy = static_cast<const __nv_bfloat16*>(dy);
   a.B = static_cast<const __nv_bfloat16*>(B); a.C = static_cast<const __nv_bfloat16*>(C);
@@ -230,28 +792,16 @@ int ssm_ssd_bwd(const void* x, const void* dt, const float* dt_bias, const float
   a.dx = static_cast<__nv_bfloat16*>(dx); a.ddt = static_cast<__nv_bfloat16*>(ddt);
   a.dz = static_cast<__nv_bfloat16*>(dz);
   a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.ddt_bias = d_dt_bias; a.dinit = d_init_state;
-  a.u = f(0); a.dl = f(1); a.zz = f(2); a.dyy = f(3); a.du = f(4); a.ddl = f(5); a.dzz = f(6);
-  a.Bg = f(7); a.Cg = f(8); a.dBg = f(9); a.dCg = f(10); a.Ag = f(11); a.dAg = f(12);
-  a.Dg = f(13); a.biasg = f(14); a.dDg = f(15); a.dbiasg = f(16);
-  a.initg = f(17); a.dfing = f(18); a.dinitg = f(19);
-  a.batch = batch; a.L = seqlen; a.H = nheads; a.P = headdim; a.G = ngroups; a.N = dstate;
-  a.hpg = nheads / ngroups; a.Dc = a.hpg * headdim;
-  void* scan_ws = ws + lay.o_scan;
-  for (int64_t g = 0; g < ngroups; ++g) {
-    a.g = g;
-    ssm::ssd_bwd_gather_kernel<<<148 * 8, 256, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-    const int rc = ssm_scan_bwd(a.u, a.dl, dt_bias ? a.biasg : nullptr, a.Ag, a.Bg, a.Cg,
-                                D ? a.Dg : nullptr, z ? a.zz : nullptr, flags,
-                                init_state ? a.initg : nullptr, a.dyy,
-                                d_final_state ? a.dfing : nullptr, a.du, a.ddl, a.dAg, a.dBg, a.dCg,
-                                a.dDg, z ? a.dzz : nullptr, a.dbiasg, d_init_state ? a.dinitg : nullptr,
-                                batch, a.Dc, seqlen, dstate, SSM_F32, scan_ws, lay.scan_bytes, st);
-    if (rc != SSM_OK) return rc;
-    ssm::ssd_bwd_scatter_kernel<<<148 * 8, 256, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
-  }
-  return SSM_OK;
+  a.terms = t.ws_terms;
+  a.Hin = reinterpret_cast<float*>(ws + lay.o_hin);
+  a.dHc = reinterpret_cast<float*>(ws + lay.o_dh);
+  a.dBp = reinterpret_cast<float*>(ws + lay.o_db);
+  a.dCp = reinterpret_cast<float*>(ws + lay.o_dc);
+  a.hpart = reinterpret_cast<float*>(ws + lay.o_hp);
+  a.batch = batch; a.L = seqlen; a.H = nheads; a.G = ngroups; a.nch = nch;
+  a.softplus = t.softplus; a.euler = t.euler;
+  const cudaError_t e = dstate == 64 ? ssm::ssd_bwd_typed<64>(a, st) : ssm::ssd_bwd_typed<128>(a, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // extern "C"
