@@ -100,34 +100,52 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_fwalk_kernel(const SsdBw
     hv[j] = a.init ? *reinterpret_cast<const float4*>(a.init + ((b * a.H + h) * kP + p) * N + n)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // a chunk's B (8-wide vectors) and w x (the block's 16 rows), loaded one chunk
+  // ahead into registers
+  constexpr int NBV = kQ * N / 8 / kWalkThreads, NXV = kQ * 16 / kWalkThreads;
+  uint4 rb[NBV];
+  float rx[NXV];
+  auto fetch = [&](int64_t c) {
+    const int64_t t0 = c * kQ;
+    const int valid = (int)min64(kQ, a.L - t0);
+    const float* tr = a.terms + ((b * a.nch + c) * a.H + h) * kSsdTermsRec;
+#pragma unroll
+    for (int i = 0; i < NBV; ++i) {
+      const int e = tid + i * kWalkThreads, tau = e / (N / 8), n8 = e % (N / 8);
+      rb[i] = tau < valid ? __ldg(reinterpret_cast<const uint4*>(a.B + ((b * a.L + t0 + tau) * a.G + g) * N + 8 * n8))
+                          : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < NXV; ++i) {
+      const int e = tid + i * kWalkThreads, tau = e / 16, pp = e % 16;
+      rx[i] = tau < valid ? __ldg(tr + 2 * kQ + tau) *
+                                bf(a.x[((b * a.L + t0 + tau) * a.H + h) * kP + 16 * q + pp])
+                          : 0.f;
+    }
+  };
+  if (a.nch > 0) fetch(0);
   for (int64_t c = 0; c < a.nch; ++c) {
     const int64_t unit = (b * a.nch + c) * a.H + h;
     float* out = a.Hin + unit * kP * N + (int64_t)p * N;
 #pragma unroll
     for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
-    const int64_t t0 = c * kQ;
-    const int valid = (int)min64(kQ, a.L - t0);
     const float* tr = a.terms + unit * kSsdTermsRec;
     __syncthreads();  // the previous chunk's readers are done
-    for (int e = tid; e < kQ * N / 8; e += kWalkThreads) {  // B: 8 bf16 a vector
-      const int tau = e / (N / 8), n8 = e % (N / 8);
-      float v[8];
-      if (tau < valid) {
-        vecio<__nv_bfloat16, 8>::load(a.B + ((b * a.L + t0 + tau) * a.G + g) * N + 8 * n8, v);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int i = 0; i < NBV; ++i) {
+      const int e = tid + i * kWalkThreads, tau = e / (N / 8), n8 = e % (N / 8);
+      const uint32_t w[4] = {rb[i].x, rb[i].y, rb[i].z, rb[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sB[tau * N + 8 * n8 + 2 * k] = __uint_as_float(w[k] << 16);
+        sB[tau * N + 8 * n8 + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
       }
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sB[tau * N + 8 * n8 + i] = v[i];
-    }
-    for (int e = tid; e < kQ * 16; e += kWalkThreads) {
-      const int tau = e / 16, pp = e % 16;
-      sX[e] = tau < valid ? tr[2 * kQ + tau] * bf(a.x[((b * a.L + t0 + tau) * a.H + h) * kP + 16 * q + pp])
-                          : 0.f;
-    }
+    for (int i = 0; i < NXV; ++i) sX[tid + i * kWalkThreads] = rx[i];
     if (tid == 0) sEnd = expf(tr[kQ - 1]);
     __syncthreads();
+    if (c + 1 < a.nch) fetch(c + 1);
     const float e_end = sEnd;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
@@ -168,40 +186,57 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_rwalk_kernel(const SsdBw
     hv[j] = a.dfin ? *reinterpret_cast<const float4*>(a.dfin + ((b * a.H + h) * kP + p) * N + n)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int64_t c = a.nch - 1; c >= 0; --c) {
-    const int64_t unit = (b * a.nch + c) * a.H + h;
-    float* out = a.dHc + unit * kP * N + (int64_t)p * N;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
+  // a chunk's C (8-wide vectors) and exp(s_t) ḡ_t (the block's 16 rows), loaded
+  // one chunk ahead into registers
+  constexpr int NBV = kQ * N / 8 / kWalkThreads, NXV = kQ * 16 / kWalkThreads;
+  uint4 rc[NBV];
+  float rg[NXV];
+  auto fetch = [&](int64_t c) {
     const int64_t t0 = c * kQ;
     const int valid = (int)min64(kQ, a.L - t0);
-    const float* tr = a.terms + unit * kSsdTermsRec;
-    __syncthreads();
-    for (int e = tid; e < kQ * N / 8; e += kWalkThreads) {
-      const int t = e / (N / 8), n8 = e % (N / 8);
-      float v[8];
-      if (t < valid) {
-        vecio<__nv_bfloat16, 8>::load(a.C + ((b * a.L + t0 + t) * a.G + g) * N + 8 * n8, v);
-      } else {
+    const float* tr = a.terms + ((b * a.nch + c) * a.H + h) * kSsdTermsRec;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sC[t * N + 8 * n8 + i] = v[i];
+    for (int i = 0; i < NBV; ++i) {
+      const int e = tid + i * kWalkThreads, t = e / (N / 8), n8 = e % (N / 8);
+      rc[i] = t < valid ? __ldg(reinterpret_cast<const uint4*>(a.C + ((b * a.L + t0 + t) * a.G + g) * N + 8 * n8))
+                        : make_uint4(0, 0, 0, 0);
     }
-    for (int e = tid; e < kQ * 16; e += kWalkThreads) {
-      const int t = e / 16, pp = e % 16;
+#pragma unroll
+    for (int i = 0; i < NXV; ++i) {
+      const int e = tid + i * kWalkThreads, t = e / 16, pp = e % 16;
       float gv = 0.f;
       if (t < valid) {
         const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + 16 * q + pp;
         gv = bf(a.dy[o]);
         if (a.z) gv *= silu_precise(bf(a.z[o]));
-        gv *= expf(tr[t]);
+        gv *= expf(__ldg(tr + t));
       }
-      sG[e] = gv;
+      rg[i] = gv;
     }
+  };
+  if (a.nch > 0) fetch(a.nch - 1);
+  for (int64_t c = a.nch - 1; c >= 0; --c) {
+    const int64_t unit = (b * a.nch + c) * a.H + h;
+    float* out = a.dHc + unit * kP * N + (int64_t)p * N;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
+    const float* tr = a.terms + unit * kSsdTermsRec;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < NBV; ++i) {
+      const int e = tid + i * kWalkThreads, t = e / (N / 8), n8 = e % (N / 8);
+      const uint32_t w[4] = {rc[i].x, rc[i].y, rc[i].z, rc[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sC[t * N + 8 * n8 + 2 * k] = __uint_as_float(w[k] << 16);
+        sC[t * N + 8 * n8 + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NXV; ++i) sG[tid + i * kWalkThreads] = rg[i];
     if (tid == 0) sEnd = expf(tr[kQ - 1]);
     __syncthreads();
+    if (c > 0) fetch(c - 1);
     const float e_end = sEnd;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
@@ -320,38 +355,93 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
     sEs[e] = expf(tr[e]);
     sEe[e] = expf(tr[kQ - 1] - tr[e]);
   }
+  // Every 16-byte load of an array is issued before any of its stores (loads
+  // through the read-only path, so they may all be in flight at once).
+  auto unpack8 = [](const uint4 q, float (&v)[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  };
   float gx = 0.f;  // Σ ḡ·x over this thread's elements (for dD)
-  for (int e = tid; e < kQ * kP; e += kChunkThreads) {
-    const int t = e / kP, pp = e % kP;
-    float xv = 0.f, gv = 0.f;
-    if (t < valid) {
-      const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + pp;
-      xv = bf(a.x[o]);
-      gv = bf(a.dy[o]);
-      if (a.z) gv *= silu_precise(bf(a.z[o]));
+  {
+    constexpr int NV = kQ * kP / 8 / kChunkThreads;  // 8-wide vectors of x, dy, z a thread loads
+    uint4 xr[NV], yr[NV], zr[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = tid + i * kChunkThreads, t = e / (kP / 8), p8 = e % (kP / 8);
+      const bool ok = t < valid;
+      const int64_t o = ((b * a.L + t0 + (ok ? t : 0)) * a.H + h) * kP + 8 * p8;
+      const uint4 zero = make_uint4(0, 0, 0, 0);
+      xr[i] = ok ? __ldg(reinterpret_cast<const uint4*>(a.x + o)) : zero;
+      yr[i] = ok ? __ldg(reinterpret_cast<const uint4*>(a.dy + o)) : zero;
+      zr[i] = (ok && a.z) ? __ldg(reinterpret_cast<const uint4*>(a.z + o)) : zero;
     }
-    sX[t * LP + pp] = xv;
-    sG[t * LP + pp] = gv;
-    gx = fmaf(gv, xv, gx);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = tid + i * kChunkThreads, t = e / (kP / 8), p8 = e % (kP / 8);
+      float xv[8], gv[8], zv[8];
+      unpack8(xr[i], xv);
+      unpack8(yr[i], gv);
+      unpack8(zr[i], zv);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (a.z) gv[k] *= silu_precise(zv[k]);
+        sX[t * LP + 8 * p8 + k] = xv[k];
+        sG[t * LP + 8 * p8 + k] = gv[k];
+        gx = fmaf(gv[k], xv[k], gx);
+      }
+    }
   }
-  for (int e = tid; e < kQ * N; e += kChunkThreads) {
-    const int t = e / N, n = e % N;
-    float cv = 0.f, bv = 0.f;
-    if (t < valid) {
-      const int64_t o = ((b * a.L + t0 + t) * a.G + g) * N + n;
-      cv = bf(a.C[o]);
-      bv = bf(a.B[o]);
+  {
+    constexpr int NV = kQ * N / 8 / kChunkThreads;  // 8-wide vectors of C and B a thread loads
+    uint4 cr[NV], br[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = tid + i * kChunkThreads, t = e / (N / 8), n8 = e % (N / 8);
+      const bool ok = t < valid;
+      const int64_t o = ((b * a.L + t0 + (ok ? t : 0)) * a.G + g) * N + 8 * n8;
+      cr[i] = ok ? __ldg(reinterpret_cast<const uint4*>(a.C + o)) : make_uint4(0, 0, 0, 0);
+      br[i] = ok ? __ldg(reinterpret_cast<const uint4*>(a.B + o)) : make_uint4(0, 0, 0, 0);
     }
-    sC[t * LN + n] = cv;
-    sB[t * LN + n] = bv;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = tid + i * kChunkThreads, t = e / (N / 8), n8 = e % (N / 8);
+      float cv[8], bv[8];
+      unpack8(cr[i], cv);
+      unpack8(br[i], bv);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        sC[t * LN + 8 * n8 + k] = cv[k];
+        sB[t * LN + 8 * n8 + k] = bv[k];
+      }
+    }
   }
   float hd = 0.f;  // <dH, H> over this thread's elements
-  for (int e = tid; e < kP * N; e += kChunkThreads) {
-    const int pp = e / N, n = e % N;
-    const float hv = a.Hin[unit * kP * N + e], dv = a.dHc[unit * kP * N + e];
-    sH[pp * LN + n] = hv;
-    sD[pp * LN + n] = dv;
-    hd = fmaf(hv, dv, hd);
+  {
+    constexpr int NV = kP * N / 4 / kChunkThreads;  // float4 of H and dH a thread loads
+    float4 hr[NV], dr[NV];
+    const float4* hsrc = reinterpret_cast<const float4*>(a.Hin + unit * kP * N);
+    const float4* dsrc = reinterpret_cast<const float4*>(a.dHc + unit * kP * N);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      hr[i] = __ldg(hsrc + tid + i * kChunkThreads);
+      dr[i] = __ldg(dsrc + tid + i * kChunkThreads);
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = 4 * (tid + i * kChunkThreads), pp = e / N, n = e % N;
+      const float hv[4] = {hr[i].x, hr[i].y, hr[i].z, hr[i].w};
+      const float dv[4] = {dr[i].x, dr[i].y, dr[i].z, dr[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sH[pp * LN + n + k] = hv[k];
+        sD[pp * LN + n + k] = dv[k];
+        hd = fmaf(hv[k], dv[k], hd);
+      }
+    }
   }
   // block sums of hd and gx: warp shuffles, then warp 0
 #pragma unroll
