@@ -585,7 +585,7 @@ def bench_ssd(steps, warmup, world, seed=5):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(world, e0.elapsed_time(e1)) / steps
-    # the backward on the same layer (ssm_ssd_bwd: the scan backward per group), a few steps
+    # the backward on the same layer (ssm_ssd_bwd, the chunked form), a few steps
     dy = torch.randn((b, L, H, P), generator=gen, device="cuda").to(bf)
     f32 = dict(dtype=torch.float32, device="cuda")
     dx, dz, ddt = torch.empty_like(x), torch.empty_like(z), torch.empty_like(dt)
