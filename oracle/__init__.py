@@ -404,3 +404,57 @@ def rel_err(got, ref):
     if den == 0.0:
         return float(num)
     return float(num / den)
+
+
+def scan_complex(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 init_state=None, euler=False):
+    """The selective scan with a complex diagonal A (and complex B, C), in complex128.
+
+    The summary page ("Mamba: Linear-Time Sequence Modeling") names complex S4 only as
+    an ablation row (§5.4) and defines no complex form, so this is the plainest
+    reading of its equations (2) and (4) over complex numbers, for each (b, d):
+        Δ_t = softplus(delta_t + bias_d) (or delta_t + bias_d),
+        Ā = exp(Δ A_{d,n}),  B̄ = (Ā - 1)/A_{d,n} (A = 0: Δ; Euler flag: Δ),
+        h_t = Ā h_{t-1} + B̄ B_{b,n,t} u_t,
+        y_t = Re(Σ_n C_{b,n,t} h_t[n]) + D_d u_t, then · silu(z_t),
+    the real part taken once, without doubling for conjugate pairs (a caller who
+    keeps one state of each conjugate pair doubles C).
+
+    u, delta, z: (batch, dim, L) float32 or bfloat16 bits; A: (dim, N) complex;
+    B, C: (batch, N, L) complex; D, delta_bias: (dim,) or None; init_state:
+    (batch, dim, N) complex or None.  Returns y (batch, dim, L) float64 and the
+    final state (batch, dim, N) complex128."""
+    u64 = _f64(u)
+    d64 = _f64(delta)
+    z64 = None if z is None else _f64(z)
+    batch, dim, L = u64.shape
+    A = np.asarray(A, dtype=np.complex128)
+    N = A.shape[1]
+    B = np.asarray(B, dtype=np.complex128)
+    C = np.asarray(C, dtype=np.complex128)
+    bias = np.zeros(dim) if delta_bias is None else np.asarray(delta_bias, np.float64)
+    Dv = np.zeros(dim) if D is None else np.asarray(D, np.float64)
+    h = (np.zeros((batch, dim, N), np.complex128) if init_state is None
+         else np.array(init_state, dtype=np.complex128))
+    y = np.empty((batch, dim, L))
+    zero = A == 0
+    Asafe = np.where(zero, 1.0, A)
+    for t in range(L):
+        x = d64[:, :, t] + bias[None, :]
+        if delta_softplus:
+            dt = np.where(x > 0, x + np.log1p(np.exp(-np.abs(x))), np.log1p(np.exp(np.minimum(x, 0))))
+        else:
+            dt = x
+        dA = dt[:, :, None] * A[None, :, :]
+        Abar = np.exp(dA)
+        if euler:
+            Bbar = np.broadcast_to(dt[:, :, None], dA.shape).astype(np.complex128)
+        else:
+            Bbar = np.where(zero[None], dt[:, :, None], np.expm1(dA) / Asafe[None])
+        h = Abar * h + Bbar * B[:, None, :, t] * u64[:, :, t][:, :, None]
+        yt = np.real(np.sum(C[:, None, :, t] * h, axis=2)) + Dv[None, :] * u64[:, :, t]
+        if z64 is not None:
+            zt = z64[:, :, t]
+            yt = yt * (zt / (1.0 + np.exp(-zt)))
+        y[:, :, t] = yt
+    return y, h
