@@ -490,6 +490,34 @@ int ssm_ssd_fwd(const void* x, const void* dt, const float* dt_bias, const float
                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The selective scan with a complex diagonal A.  The summary page ("Mamba:
+ * Linear-Time Sequence Modeling") names a complex S4 only as an ablation row
+ * (§5.4) and defines no complex form; this computes the plainest reading of its
+ * equations (2) and (4) over complex numbers, per (batch, channel):
+ *   Δ_t = softplus(delta_t + bias) (or delta_t + bias), Ā = exp(Δ A_n),
+ *   B̄ = (Ā - 1)/A_n (A_n = 0, or the SSM_EULER_B flag: Δ),
+ *   h_t = Ā h_{t-1} + B̄ B_{n,t} u_t,  y_t = Re(Σ_n C_{n,t} h_t[n]) + D u_t,
+ * then y · silu(z) when z is given.  The real part is taken once: a caller who
+ * keeps one state of each conjugate pair doubles C.
+ *
+ * Layouts: u, delta, z, y (batch, dim, seqlen) in io_dtype; A (dim, dstate),
+ * B and C (batch, dstate, seqlen), init_state and final_state (batch, dim,
+ * dstate), all complex as interleaved (re, im) fp32 pairs; delta_bias and D
+ * (dim) fp32.  Nullable: delta_bias, D, z, final_state, init_state (zeros).
+ * Flags: SSM_SOFTPLUS, SSM_EULER_B.  dstate: a power of two up to 64
+ * (SSM_ERR_UNSUPPORTED otherwise).  All pointers 16-byte aligned
+ * (SSM_ERR_ALIGN).  y must not overlap an input, final_state no input but
+ * init_state, which it may equal exactly (an in-place carry).  The arithmetic is
+ * the precise flavour (libm expf, expm1f, sincosf) for both I/O dtypes; no
+ * workspace; asynchronous on `stream`.
+ */
+int ssm_scan_fwd_complex(const void* u, const void* delta, const float* delta_bias,
+                         const float* A, const float* B, const float* C, const float* D,
+                         const void* z, int delta_softplus, void* y, float* final_state,
+                         const float* init_state, int64_t batch, int64_t dim, int64_t seqlen,
+                         int64_t dstate, int io_dtype, void* stream);
+
+/*
  * Backward of ssm_ssd_fwd (the chapter page's §5.1: SSD is the selective scan
  * of each channel of a head with the scalar A[h] for every state, the head's
  * step shared by its channels and the group's B, C): the derivatives of

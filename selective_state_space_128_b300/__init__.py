@@ -63,6 +63,8 @@ def load():
     lib.ssm_scan_fwd_strided.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp,
                                                      vp, sz, vp]
     lib.ssm_scan_fwd_strided.restype = i32
+    lib.ssm_scan_fwd_complex.argtypes = [vp] * 8 + [i32, vp, vp, vp, i64, i64, i64, i64, i32, vp]
+    lib.ssm_scan_fwd_complex.restype = i32
     lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 8 + [i32, vp, vp, i64, i64, i64, i64, i32, vp, vp]
     lib.ssm_scan_fwd_noalloc.restype = i32
     lib.ssm_status.argtypes = [vp, vp]
@@ -464,6 +466,42 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True
             ws = torch.empty(nbytes, dtype=torch.uint8, device=u.device)
     ssm_scan_fwd_ex(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler, bld), y,
                     h, init_state, ws, stream=stream)
+    return y, h
+
+
+def ssm_scan_fwd_complex(u, delta, delta_bias, A, B, C, D, z, delta_softplus, y, final_state,
+                         init_state=None, stream=None):
+    """Tensor form of ``ssm_scan_fwd_complex``: A (dim, N), B, C (batch, N, L) and the
+    states (batch, dim, N) are torch.complex64 tensors (passed as their interleaved
+    (re, im) float pairs); u, delta, z, y (batch, dim, L) in the I/O dtype."""
+    _check_dev(u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state)
+    for t in (A, B, C, final_state, init_state):
+        if t is not None and t.dtype != _torch_complex64():
+            raise TypeError("A, B, C and the states must be complex64")
+    batch, dim, L = int(B.shape[0]), int(A.shape[0]), int(B.shape[2])
+    N = int(A.shape[1])
+    rc = load().ssm_scan_fwd_complex(_ptr(u), _ptr(delta), _ptr(delta_bias), _ptr(A), _ptr(B),
+                                     _ptr(C), _ptr(D), _ptr(z), _flags(delta_softplus), _ptr(y),
+                                     _ptr(final_state), _ptr(init_state), batch, dim, L, N,
+                                     _io_dtype(u), _stream(stream))
+    _call("ssm_scan_fwd_complex", rc)
+
+
+def _torch_complex64():
+    import torch
+    return torch.complex64
+
+
+def scan_complex(u, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 init_state=None, euler=False, stream=None):
+    """y, final_state = scan_complex(...): the scan with a complex diagonal A; allocates
+    y (dtype of u) and the complex64 final state."""
+    import torch
+    batch, dim = int(B.shape[0]), int(A.shape[0])
+    y = torch.empty_like(u)
+    h = torch.empty((batch, dim, A.shape[1]), dtype=torch.complex64, device=u.device)
+    ssm_scan_fwd_complex(u, delta, delta_bias, A, B, C, D, z, _flags(delta_softplus, euler), y,
+                         h, init_state, stream)
     return y, h
 
 

@@ -416,6 +416,60 @@ int ssm_scan_fwd_strided(const void* u, const void* delta, const float* delta_bi
                              workspace_bytes, nullptr, 0, false, stream, strides);
 }
 
+int ssm_scan_fwd_complex(const void* u, const void* delta, const float* delta_bias,
+                         const float* A, const float* B, const float* C, const float* D,
+                         const void* z, int delta_softplus, void* y, float* final_state,
+                         const float* init_state, int64_t batch, int64_t dim, int64_t seqlen,
+                         int64_t dstate, int io_dtype, void* stream) {
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_ARG;
+  if (!flags_ok(delta_softplus)) return SSM_ERR_ARG;
+  if (!sizes_ok(batch, dim, seqlen) || dstate <= 0) return SSM_ERR_ARG;
+  if (dstate > 64 || (dstate & (dstate - 1)) != 0) return SSM_ERR_UNSUPPORTED;
+  const bool work = batch > 0 && dim > 0 && seqlen > 0;
+  if (work && (!u || !delta || !A || !B || !C || !y)) return SSM_ERR_ARG;
+  const void* ptrs[] = {u, delta, delta_bias, A, B, C, D, z, y, final_state, init_state};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SSM_ERR_ALIGN;
+  const size_t esz = io_dtype == SSM_F32 ? 4 : 2;
+  const size_t nio = (size_t)batch * (size_t)dim * (size_t)seqlen * esz;
+  const size_t nst = (size_t)batch * (size_t)dim * (size_t)dstate * 8;
+  const size_t nbc = (size_t)batch * (size_t)dstate * (size_t)seqlen * 8;
+  const size_t nA = (size_t)dim * (size_t)dstate * 8, nd = (size_t)dim * 4;
+  const void* ins[] = {u, delta, z, B, C, A, delta_bias, D, init_state};
+  const size_t in_bytes[] = {nio, nio, nio, nbc, nbc, nA, nd, nd, nst};
+  for (int k = 0; k < 9; ++k) {
+    if (overlaps(y, nio, ins[k], in_bytes[k])) return SSM_ERR_ARG;
+    if (k < 8 && overlaps(final_state, nst, ins[k], in_bytes[k])) return SSM_ERR_ARG;
+  }
+  if (overlaps(y, nio, final_state, nst)) return SSM_ERR_ARG;
+  if (final_state && init_state && final_state != init_state &&
+      overlaps(final_state, nst, init_state, nst))
+    return SSM_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (batch > 0 && dim > 0 && seqlen == 0) {
+    // no step: the final state is the initial one (zeros without it)
+    if (!final_state || final_state == init_state) return SSM_OK;
+    const cudaError_t e = init_state ? cudaMemcpyAsync(final_state, init_state, nst,
+                                                       cudaMemcpyDeviceToDevice, st)
+                                     : cudaMemsetAsync(final_state, 0, nst, st);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  }
+  if (!work) return SSM_OK;
+  ssm::ComplexScanArgs a{};
+  a.u = u; a.delta = delta; a.z = z; a.bias = delta_bias;
+  a.A = reinterpret_cast<const float2*>(A);
+  a.B = reinterpret_cast<const float2*>(B);
+  a.C = reinterpret_cast<const float2*>(C);
+  a.D = D; a.y = y;
+  a.final_state = reinterpret_cast<float2*>(final_state);
+  a.init_state = reinterpret_cast<const float2*>(init_state);
+  a.batch = batch; a.dim = dim; a.L = seqlen;
+  a.softplus = (delta_softplus & SSM_SOFTPLUS) != 0;
+  a.euler = (delta_softplus & SSM_EULER_B) != 0;
+  const cudaError_t e = ssm::scan_complex_launch(a, dstate, io_dtype, st);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 int ssm_status(const void* workspace, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int code = 0;

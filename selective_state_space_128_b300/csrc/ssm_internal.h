@@ -88,6 +88,28 @@ cudaError_t scan_fast_launch(const ScanArgs& a, cudaStream_t stream);
 // warp: 8 channels at N = 16).
 constexpr int kFastChannels = 8;
 
+// Arguments of the scan with a complex diagonal A (ssm_scan_complex.cu): A (dim, N),
+// B, C (batch, N, L) and the states (batch, dim, N) as (re, im) pairs; u, delta, z,
+// y (batch, dim, L) in the I/O dtype.
+struct ComplexScanArgs {
+  const void* u;
+  const void* delta;
+  const void* z;
+  const float* bias;
+  const float2* A;
+  const float2* B;
+  const float2* C;
+  const float* D;
+  void* y;
+  float2* final_state;
+  const float2* init_state;
+  int64_t batch, dim, L;
+  int softplus;
+  int euler;
+};
+
+cudaError_t scan_complex_launch(const ComplexScanArgs& a, int64_t N, int io_dtype, cudaStream_t stream);
+
 struct UpdateArgs {
   float* state;
   const void* u;

@@ -402,3 +402,32 @@ def test_strided_argument_errors():
     assert _strided(dense * 4, y=FAKE + 0x200) == ssm.SSM_ERR_ARG
     # empty problems succeed without touching the device
     assert _strided(dense * 4, batch=0) == ssm.SSM_OK
+
+
+def _cx(**kw):
+    a = dict(u=FAKE, delta=FAKE + 0x1000000, bias=None, A=FAKE + 0x2000000, B=FAKE + 0x3000000,
+             C=FAKE + 0x4000000, D=None, z=None, flags=1, y=FAKE + 0x5000000, h=None, init=None,
+             batch=2, dim=64, L=128, N=16, io=ssm.SSM_BF16, stream=None)
+    a.update(kw)
+    return lib().ssm_scan_fwd_complex(a["u"], a["delta"], a["bias"], a["A"], a["B"], a["C"],
+                                      a["D"], a["z"], a["flags"], a["y"], a["h"], a["init"],
+                                      a["batch"], a["dim"], a["L"], a["N"], a["io"], a["stream"])
+
+
+def test_complex_scan_argument_errors():
+    assert _cx(io=3) == ssm.SSM_ERR_ARG
+    assert _cx(flags=ssm.SSM_LAYOUT_BLD | 1) == ssm.SSM_ERR_ARG   # (batch, dim, L) only
+    assert _cx(N=3) == ssm.SSM_ERR_UNSUPPORTED
+    assert _cx(N=128) == ssm.SSM_ERR_UNSUPPORTED
+    assert _cx(batch=-1) == ssm.SSM_ERR_ARG
+    for name in ("u", "delta", "A", "B", "C", "y"):
+        assert _cx(**{name: None}) == ssm.SSM_ERR_ARG, name
+    assert _cx(B=FAKE + 0x3000008) == ssm.SSM_ERR_ALIGN
+    assert _cx(h=FAKE + 0x6000004) == ssm.SSM_ERR_ALIGN
+    # y over u; the final state over B; the final state partly over the initial one
+    assert _cx(y=FAKE + 0x100) == ssm.SSM_ERR_ARG
+    assert _cx(h=FAKE + 0x3000100) == ssm.SSM_ERR_ARG
+    assert _cx(h=FAKE + 0x6000000, init=FAKE + 0x6000100) == ssm.SSM_ERR_ARG
+    # nothing to do: no channel, or no step and no state asked for
+    assert _cx(dim=0, u=None, delta=None, A=None, B=None, C=None, y=None) == ssm.SSM_OK
+    assert _cx(L=0, h=None) == ssm.SSM_OK
