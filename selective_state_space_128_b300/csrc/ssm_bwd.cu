@@ -886,7 +886,7 @@ __global__ void __launch_bounds__(kAdjThreads) adjoint_carry_kernel(const BwdArg
   constexpr int NPT = Cf::NPT, CH = Cf::CH, TT = Cf::TT, E = Cf::E, TPR = Cf::TPR, PER = Cf::PER;
   __shared__ float sDT[CH * Cf::RowF];
   __shared__ float sDS[CH * Cf::RowF];
-  __shared__ __align__(16) float sC[TT * N];
+  __shared__ float sC[N * (TT + 1)];  // [n][t]: staged along t without bank conflicts
   __shared__ float sBias[CH];
 
   const int tid = threadIdx.x;
@@ -985,7 +985,7 @@ __global__ void __launch_bounds__(kAdjThreads) adjoint_carry_kernel(const BwdArg
         const int e = tid + i * kAdjThreads;
         if (TT * N % kAdjThreads == 0 || e < TT * N) {
           const int n = e / TT, t = e - n * TT;
-          sC[t * N + n] = rc[i];
+          sC[n * (TT + 1) + t] = rc[i];
         }
       }
     }
@@ -993,16 +993,27 @@ __global__ void __launch_bounds__(kAdjThreads) adjoint_carry_kernel(const BwdArg
     if (kk > 0) fetch(kk - 1);
     const float* rDT = sDT + c * Cf::RowF;
     const float* rDS = sDS + c * Cf::RowF;
-#pragma unroll 4
-    for (int t = TT - 1; t >= 0; --t) {
-      const float dt = rDT[t], ds = rDS[t];
-      float Cv[NPT];
-      lds_vec<NPT>(sC + t * N + g * NPT, Cv);
-      sdt += dt;
+    const float* rC = sC + g * NPT * (TT + 1);
+    if (precise) {
+      for (int t = TT - 1; t >= 0; --t) {
+        const float dt = rDT[t], ds = rDS[t];
+        sdt += dt;
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        lam[j] = fmaf(ds, Cv[j], lam[j]);
-        lam[j] *= precise ? expf(dt * Aj[j]) : ex2_fast(dt * A2[j]);
+        for (int j = 0; j < NPT; ++j) {
+          lam[j] = fmaf(ds, rC[j * (TT + 1) + t], lam[j]);
+          lam[j] *= expf(dt * Aj[j]);
+        }
+      }
+    } else {
+#pragma unroll 4
+      for (int t = TT - 1; t >= 0; --t) {
+        const float dt = rDT[t], ds = rDS[t];
+        sdt += dt;
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+          lam[j] = fmaf(ds, rC[j * (TT + 1) + t], lam[j]);
+          lam[j] *= ex2_fast(dt * A2[j]);
+        }
       }
     }
   }

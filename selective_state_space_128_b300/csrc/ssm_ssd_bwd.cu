@@ -76,6 +76,14 @@ struct SsdBwd {
 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ void unpack_bf16x8(const uint4 q, float (&v)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = __uint_as_float(w[k] << 16);
+    v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+  }
+}
 __device__ __forceinline__ float sigmoid_precise(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // ---------------------------------------------------------------------------
@@ -87,7 +95,7 @@ template <int N>
 __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_fwalk_kernel(const SsdBwd a) {
   constexpr int NV = N / 32;  // float4 column groups a thread holds
   __shared__ __align__(16) float sB[kQ * N];
-  __shared__ float sX[kQ * 16];  // w_τ x_τ[p] for the block's 16 rows
+  __shared__ __align__(16) float sX[kQ * 16];  // w_τ x_τ[p] for the block's 16 rows
   __shared__ float sEnd;
   const int tid = threadIdx.x;
   const int q = blockIdx.x, h = blockIdx.y;
@@ -102,9 +110,12 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_fwalk_kernel(const SsdBw
   }
   // a chunk's B (8-wide vectors) and w x (the block's 16 rows), loaded one chunk
   // ahead into registers
-  constexpr int NBV = kQ * N / 8 / kWalkThreads, NXV = kQ * 16 / kWalkThreads;
+  // (thread t's x vector: step t / 2, rows 8 (t % 2) .. + 7 of the block's 16)
+  constexpr int NBV = kQ * N / 8 / kWalkThreads;
+  static_assert(kQ * 2 == kWalkThreads, "one 8-wide x vector a thread");
   uint4 rb[NBV];
-  float rx[NXV];
+  uint4 rx;
+  float rw;
   auto fetch = [&](int64_t c) {
     const int64_t t0 = c * kQ;
     const int valid = (int)min64(kQ, a.L - t0);
@@ -115,13 +126,11 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_fwalk_kernel(const SsdBw
       rb[i] = tau < valid ? __ldg(reinterpret_cast<const uint4*>(a.B + ((b * a.L + t0 + tau) * a.G + g) * N + 8 * n8))
                           : make_uint4(0, 0, 0, 0);
     }
-#pragma unroll
-    for (int i = 0; i < NXV; ++i) {
-      const int e = tid + i * kWalkThreads, tau = e / 16, pp = e % 16;
-      rx[i] = tau < valid ? __ldg(tr + 2 * kQ + tau) *
-                                bf(a.x[((b * a.L + t0 + tau) * a.H + h) * kP + 16 * q + pp])
-                          : 0.f;
-    }
+    const int tau = tid / 2;
+    const bool ok = tau < valid;
+    rx = ok ? __ldg(reinterpret_cast<const uint4*>(a.x + ((b * a.L + t0 + tau) * a.H + h) * kP + 16 * q + 8 * (tid % 2)))
+            : make_uint4(0, 0, 0, 0);
+    rw = ok ? __ldg(tr + 2 * kQ + tau) : 0.f;
   };
   if (a.nch > 0) fetch(0);
   for (int64_t c = 0; c < a.nch; ++c) {
@@ -134,15 +143,19 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_fwalk_kernel(const SsdBw
 #pragma unroll
     for (int i = 0; i < NBV; ++i) {
       const int e = tid + i * kWalkThreads, tau = e / (N / 8), n8 = e % (N / 8);
-      const uint32_t w[4] = {rb[i].x, rb[i].y, rb[i].z, rb[i].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sB[tau * N + 8 * n8 + 2 * k] = __uint_as_float(w[k] << 16);
-        sB[tau * N + 8 * n8 + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-      }
+      float v[8];
+      unpack_bf16x8(rb[i], v);
+      float4* dst = reinterpret_cast<float4*>(sB + tau * N + 8 * n8);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
-#pragma unroll
-    for (int i = 0; i < NXV; ++i) sX[tid + i * kWalkThreads] = rx[i];
+    {
+      float v[8];
+      unpack_bf16x8(rx, v);
+      float4* dst = reinterpret_cast<float4*>(sX + tid * 8);
+      dst[0] = make_float4(rw * v[0], rw * v[1], rw * v[2], rw * v[3]);
+      dst[1] = make_float4(rw * v[4], rw * v[5], rw * v[6], rw * v[7]);
+    }
     if (tid == 0) sEnd = expf(tr[kQ - 1]);
     __syncthreads();
     if (c + 1 < a.nch) fetch(c + 1);
@@ -173,7 +186,7 @@ template <int N>
 __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_rwalk_kernel(const SsdBwd a) {
   constexpr int NV = N / 32;
   __shared__ __align__(16) float sC[kQ * N];
-  __shared__ float sG[kQ * 16];  // exp(s_t) ḡ_t[p] for the block's 16 rows
+  __shared__ __align__(16) float sG[kQ * 16];  // exp(s_t) ḡ_t[p] for the block's 16 rows
   __shared__ float sEnd;
   const int tid = threadIdx.x;
   const int q = blockIdx.x, h = blockIdx.y;
@@ -188,9 +201,12 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_rwalk_kernel(const SsdBw
   }
   // a chunk's C (8-wide vectors) and exp(s_t) ḡ_t (the block's 16 rows), loaded
   // one chunk ahead into registers
-  constexpr int NBV = kQ * N / 8 / kWalkThreads, NXV = kQ * 16 / kWalkThreads;
+  // (thread t's dy and z vectors: step t / 2, rows 8 (t % 2) .. + 7 of the block's 16)
+  constexpr int NBV = kQ * N / 8 / kWalkThreads;
+  static_assert(kQ * 2 == kWalkThreads, "one 8-wide dy vector a thread");
   uint4 rc[NBV];
-  float rg[NXV];
+  uint4 rdy, rz;
+  float rs;
   auto fetch = [&](int64_t c) {
     const int64_t t0 = c * kQ;
     const int valid = (int)min64(kQ, a.L - t0);
@@ -201,18 +217,12 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_rwalk_kernel(const SsdBw
       rc[i] = t < valid ? __ldg(reinterpret_cast<const uint4*>(a.C + ((b * a.L + t0 + t) * a.G + g) * N + 8 * n8))
                         : make_uint4(0, 0, 0, 0);
     }
-#pragma unroll
-    for (int i = 0; i < NXV; ++i) {
-      const int e = tid + i * kWalkThreads, t = e / 16, pp = e % 16;
-      float gv = 0.f;
-      if (t < valid) {
-        const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + 16 * q + pp;
-        gv = bf(a.dy[o]);
-        if (a.z) gv *= silu_precise(bf(a.z[o]));
-        gv *= expf(__ldg(tr + t));
-      }
-      rg[i] = gv;
-    }
+    const int t = tid / 2;
+    const bool ok = t < valid;
+    const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + 16 * q + 8 * (tid % 2);
+    rdy = ok ? __ldg(reinterpret_cast<const uint4*>(a.dy + o)) : make_uint4(0, 0, 0, 0);
+    rz = (ok && a.z) ? __ldg(reinterpret_cast<const uint4*>(a.z + o)) : make_uint4(0, 0, 0, 0);
+    rs = ok ? __ldg(tr + t) : 0.f;
   };
   if (a.nch > 0) fetch(a.nch - 1);
   for (int64_t c = a.nch - 1; c >= 0; --c) {
@@ -225,15 +235,24 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_rwalk_kernel(const SsdBw
 #pragma unroll
     for (int i = 0; i < NBV; ++i) {
       const int e = tid + i * kWalkThreads, t = e / (N / 8), n8 = e % (N / 8);
-      const uint32_t w[4] = {rc[i].x, rc[i].y, rc[i].z, rc[i].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sC[t * N + 8 * n8 + 2 * k] = __uint_as_float(w[k] << 16);
-        sC[t * N + 8 * n8 + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-      }
+      float v[8];
+      unpack_bf16x8(rc[i], v);
+      float4* dst = reinterpret_cast<float4*>(sC + t * N + 8 * n8);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
+    {
+      // exp(s_t) ḡ_t with ḡ = dy · silu(z) (steps past the end: dy = 0)
+      float gv[8], zv[8];
+      unpack_bf16x8(rdy, gv);
+      unpack_bf16x8(rz, zv);
+      const float es = expf(rs);
 #pragma unroll
-    for (int i = 0; i < NXV; ++i) sG[tid + i * kWalkThreads] = rg[i];
+      for (int k = 0; k < 8; ++k) gv[k] *= (a.z ? silu_precise(zv[k]) : 1.f) * es;
+      float4* dst = reinterpret_cast<float4*>(sG + tid * 8);
+      dst[0] = make_float4(gv[0], gv[1], gv[2], gv[3]);
+      dst[1] = make_float4(gv[4], gv[5], gv[6], gv[7]);
+    }
     if (tid == 0) sEnd = expf(tr[kQ - 1]);
     __syncthreads();
     if (c > 0) fetch(c - 1);
