@@ -165,7 +165,6 @@ template <int N, int PR> struct SsdStateCfg {
   static constexpr int kTermVecs = kTermsRec * 4 / 16;
   static constexpr int kOutVecs = PR * N / 8;                   // 16-byte vectors of the tile
   static_assert(PR % 16 == 0 && kSsdP % PR == 0, "tiling");
-  static_assert(kTermVecs <= kThreads, "one 16-byte copy of the terms per thread");
   static_assert(kOutVecs % kThreads == 0, "whole vectors per thread in the state copy-out");
 };
 constexpr int kWalkRows = 32;  // state rows per block: 2 warps, 2 x 24 x 8 blocks on a 24-head layer
@@ -192,9 +191,10 @@ __global__ void __launch_bounds__(SsdStateCfg<N, PR>::kThreads)
     ssd_stage<Q, N, RB, NT>(st + Cf::oB,
                             static_cast<const __nv_bfloat16*>(p.B) + ((b * p.L + t0) * p.G + g) * N,
                             p.G * N, valid);
-    if (threadIdx.x < Cf::kTermVecs) {
+    {
       const float* src = p.ws_terms + ((b * p.nch + c) * p.H + h) * kTermsRec;
-      cp_async16(reinterpret_cast<float*>(st + Cf::oT) + 4 * threadIdx.x, src + 4 * threadIdx.x, true);
+      for (int e = threadIdx.x; e < Cf::kTermVecs; e += NT)
+        cp_async16(reinterpret_cast<float*>(st + Cf::oT) + 4 * e, src + 4 * e, true);
     }
     cp_async_commit();
   };
