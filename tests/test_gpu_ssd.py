@@ -141,3 +141,36 @@ def test_ssd_backward_empty_sequence():
     for k in ("dA", "dD", "ddt_bias"):
         assert out[k].abs().max().item() == 0.0, k
     assert np.array_equal(host64(out["dinit"]), dfin.astype(np.float64))
+
+
+@pytest.mark.slow
+def test_ssd_backward_bench_shape_sampled():
+    """The backward at the bench's layer size (batch 8, L 2048, 24 heads x 64, N 128): dx,
+    ddt, dz of 3 sampled (batch, head) pairs over the whole sequence, and dB, dC of one
+    batch row in full (they sum over its 24 heads), against the oracle; every output
+    finite."""
+    cfg = dict(batch=8, L=2048, H=24, G=1, N=128)
+    x = _inputs(seed=360, **cfg)
+    rng = np.random.default_rng(9)
+    dy = synth.f32_to_bf16(rng.standard_normal(x["x"].shape).astype(np.float32))
+    out = ssm.ssd_bwd(dev_io(x["x"]), dev_io(x["dt"]), dev_f32(x["A"]), dev_io(x["B"]),
+                      dev_io(x["C"]), dev_f32(x["D"]), dev_io(x["z"]), dev_f32(x["bias"]), True,
+                      dy=dev_io(dy))
+    torch.cuda.synchronize()
+    for k in ("dx", "ddt", "dz", "dB", "dC", "dA", "dD", "ddt_bias"):
+        assert torch.isfinite(out[k].float()).all().item(), k
+    dy64 = _f32(dy).astype(np.float64)
+    for b, hd in ((0, 0), (3, 11), (7, 23)):
+        sl = lambda a: np.ascontiguousarray(a[b:b + 1, :, hd:hd + 1])
+        ref = oracle.ssd_bwd(sl(x["x"]), sl(x["dt"]), x["A"][hd:hd + 1], _f32(x["B"][b:b + 1]),
+                             _f32(x["C"][b:b + 1]), x["D"][hd:hd + 1], sl(x["z"]),
+                             x["bias"][hd:hd + 1], True, dy=sl(dy64))
+        for k in ("dx", "dz"):
+            assert oracle.rel_err(host64(out[k][b:b + 1, :, hd:hd + 1]), ref[k]) <= TOL, k
+        assert oracle.rel_err(host64(out["ddt"][b:b + 1, :, hd:hd + 1]), ref["ddt"]) <= TOL
+    b = 5
+    sb = lambda a: np.ascontiguousarray(a[b:b + 1])
+    ref = oracle.ssd_bwd(sb(x["x"]), sb(x["dt"]), x["A"], _f32(sb(x["B"])), _f32(sb(x["C"])),
+                         x["D"], sb(x["z"]), x["bias"], True, dy=sb(dy64))
+    for k in ("dB", "dC"):
+        assert oracle.rel_err(host64(out[k][b:b + 1]), ref[k]) <= 1e-4, k
