@@ -354,14 +354,22 @@ int ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* delta_bi
  * Workspace: ssm_scan_bwd_workspace_bytes() bytes of device memory (16-byte
  * aligned), required whenever batch, dim and seqlen are all non-zero; it
  * holds the chunk-start states of the recomputation and per-block partial
- * sums, nothing that outlives the call.
+ * sums, nothing that outlives the call.  Its size depends on the plan for the
+ * current device: when the (channel block, batch row) blocks fill less than
+ * half a wave of the GPU, the sequence is split into segments run in parallel
+ * (the workspace then also holds the segments' forward and adjoint carries and
+ * per-segment sums), so size it on the device that runs the call.
  *
  * Precision: fp32 arithmetic; bf16 outputs are rounded to nearest even.  The
- * channel sums (dB, dC) and batch sums (dA, dD, d_delta_bias) are added in a
- * fixed order, so results are the same from run to run.
+ * channel sums (dB, dC), batch sums (dA, dD, d_delta_bias) and segment sums
+ * are added in a fixed order, so results are the same from run to run.
  * Errors: as ssm_scan_fwd_ex; outputs may not overlap inputs or each other.
+ * A split plan's forward-carry pass stages through TMA with bounded waits; a
+ * wait that runs out sets the library-wide status word (ssm_status with a null
+ * workspace returns SSM_ERR_TIMEOUT), as for the scans without a workspace.
  * Execution: asynchronous on `stream` (two kernels: the pass and the
- * fixed-order sums; memsets and a copy instead when a size is zero).
+ * fixed-order sums; four with a split plan: the forward carries and the
+ * adjoint carries first; memsets and a copy instead when a size is zero).
  */
 size_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
 
