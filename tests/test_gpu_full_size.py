@@ -235,6 +235,31 @@ def test_backward_million_length_one_call_sampled():
     assert oracle.rel_err(got["dbias"], r["dbias_unit"]) <= TOL
 
 
+def test_conv1d_backward_at_layer_size_sampled():
+    """The front end's backward at the bench's size (8 x 1536 x 2048 bf16, width 4, rows
+    staged through the shared-memory ring): dx, dweight, dbias and d state of 24
+    sampled channels over all 8 batch rows against the oracle; every output finite."""
+    w = synth.MAMBA_130M
+    x = synth.make_scan_inputs(w)
+    wt = synth.fill(7, synth.S_B, 0, w.dim * 4, synth.NORMAL, 0.0, 0.5).reshape(w.dim, 4)
+    bias = synth.fill(7, synth.S_D, 0, w.dim, synth.NORMAL, 0.0, 0.2)
+    st = synth.fill(7, synth.S_H0, 0, w.batch * w.dim * 3, synth.NORMAL, 0.0, 1.0,
+                    dtype="bf16").reshape(w.batch, w.dim, 3)
+    dout = synth.make_bwd_inputs(w, init_state=False, d_final_state=False)["dy"]
+    out = ssm.conv1d_bwd(dev_io(x["u"]), dev_f32(wt), dev_io(dout), dev_f32(bias), dev_io(st))
+    torch.cuda.synchronize()
+    for k in ("dx", "dweight", "dbias", "dstate"):
+        assert torch.isfinite(out[k].float()).all().item(), k
+    dsel = np.sort(np.random.default_rng(10).choice(w.dim, 24, replace=False))
+    ref = oracle.conv1d_bwd(np.ascontiguousarray(x["u"][:, dsel]), wt[dsel], bias[dsel],
+                            synth.bf16_to_f32(st[:, dsel]), True, np.ascontiguousarray(dout[:, dsel]))
+    di = torch.from_numpy(dsel).cuda()
+    assert oracle.rel_err(host64(out["dx"][:, di]), ref["dx"]) <= TOL
+    assert oracle.rel_err(host64(out["dweight"][di]), ref["dweight"]) <= 1e-3
+    assert oracle.rel_err(host64(out["dbias"][di]), ref["dbias"]) <= 1e-3
+    assert oracle.rel_err(host64(out["dstate"][:, di]), ref["dstate"]) <= 1e-3
+
+
 def test_conv1d_and_bld_scan_at_layer_size():
     """The front end at the bench's size (8 x 1536 x 2048 bf16, width 4) on 64 sampled
     rows, and the (batch, L, dim) scan of the layer equal, bit for bit, to the
