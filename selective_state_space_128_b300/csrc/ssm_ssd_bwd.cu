@@ -40,9 +40,10 @@
 //  2. a forward walk over the chunks writing each chunk's entering state H_{c-1}
 //     in fp32, and a reverse walk writing each dH_c and d init_state; both are
 //     parallel over (batch, head, a quarter of the state's rows);
-//  3. one block per (batch, chunk, head) for everything above: the chunk's
-//     operands in shared memory, its products as register-tiled loops over
-//     shared memory; per-head partial dB, dC, da, d dt_bias, dD to a workspace;
+//  3. one block of 16 warps per (batch, chunk, head) for everything above: the
+//     chunk's operands in shared memory, its products as register-tiled loops
+//     over shared memory (4 rows a warp); per-head partial dB, dC, da, d dt_bias,
+//     dD to a workspace;
 //  4. the sums over a group's heads (dB, dC) and over batch and chunks (da,
 //     d dt_bias, dD) in a fixed order, so results repeat bit for bit.
 #include <cstdint>
@@ -58,7 +59,9 @@ namespace {
 constexpr int kQ = kSsdChunk;  // chunk length
 constexpr int kP = 64;         // head dimension
 constexpr int kWalkThreads = 128;
-constexpr int kChunkThreads = 256;  // 8 warps: 8 rows of every 64-row product each
+constexpr int kChunkThreads = 512;  // 16 warps: 4 rows of every 64-row product each
+constexpr int kChunkWarps = kChunkThreads / 32;
+constexpr int kRM = kQ / kChunkWarps;  // rows of every product a warp takes
 
 struct SsdBwd {
   const __nv_bfloat16 *x, *dt, *z, *dy, *B, *C;
@@ -322,8 +325,8 @@ template <int N> struct ChunkBwdSmem {
   static constexpr int oE = oD + kP * LN;      // (C_t·B_τ) exp(s_t - s_τ), τ <= t   [t][τ]
   static constexpr int oL = oE + kQ * LQ;      // dML    [t][τ]
   static constexpr int oS = oL + kQ * LQ;      // s, β, exp(s), exp(s_end - s)
-  static constexpr int oR = oS + 4 * kQ;       // per-warp column sums [2][8][Q]
-  static constexpr int oV = oR + 2 * 8 * kQ;   // ds parts, dβ, r, row and column sums [6][Q]; scalars
+  static constexpr int oR = oS + 4 * kQ;       // per-warp column sums [2][warps][Q]
+  static constexpr int oV = oR + 2 * kChunkWarps * kQ;   // ds parts, dβ, r, row and column sums [6][Q]; scalars
   static constexpr int kFloats = oV + 6 * kQ + 8;
   static constexpr size_t kBytes = (size_t)kFloats * 4;
 };
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
   float* sBeta = sS + kQ;        // β
   float* sEs = sS + 2 * kQ;      // exp(s_t)
   float* sEe = sS + 3 * kQ;      // exp(s_end - s_t)
-  float* sR = sm + S::oR;        // [2][8][Q]
+  float* sR = sm + S::oR;        // [2][warps][Q]
   float* sV = sm + S::oV;
   float* vRowK = sV;             // Σ_τ K[t][τ]
   float* vInter = sV + kQ;       // exp(s_t) ḡ_t·(H C_t)
@@ -364,7 +367,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
   const int valid = (int)min64(kQ, a.L - t0);
   const float ah = a.A[h];
   const float Dh = a.D ? a.D[h] : 0.f;
-  const int i0 = 8 * warp;  // this warp's 8 rows of every product
+  constexpr int RM = kRM, NW = kChunkWarps;
+  const int i0 = RM * warp;  // this warp's rows of every product
 
   // ---- stage the chunk ----
   const float* tr = a.terms + unit * kSsdTermsRec;
@@ -470,14 +474,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
   }
   if (lane == 0) {
     sR[warp] = hd;
-    sR[8 + warp] = gx;
+    sR[NW + warp] = gx;
   }
   __syncthreads();
   if (tid == 0) {
     float s1 = 0.f, s2 = 0.f;
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < NW; ++w) {
       s1 += sR[w];
-      s2 += sR[8 + w];
+      s2 += sR[NW + w];
     }
     vScal[0] = s1;
     vScal[1] = s2;
@@ -486,11 +490,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 
   // ---- E = (C_t·B_τ) exp(s_t - s_τ) for τ <= t (else 0) ----
   {
-    float acc[8][2];
+    float acc[RM][2];
     mm_zero(acc);
-    mm_acc<8, 2>(acc, N, sC, 1, LN, i0, sB, 1, LN, lane);
+    mm_acc<RM, 2>(acc, N, sC, 1, LN, i0, sB, 1, LN, lane);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < RM; ++i)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int t = i0 + i, tau = lane + 32 * r;
@@ -501,12 +505,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 
   // ---- y before the gate (for dz) and the inter-chunk ds term ----
   {
-    float acc[8][2];
+    float acc[RM][2];
     mm_zero(acc);
-    mm_acc<8, 2>(acc, N, sC, 1, LN, i0, sH, 1, LN, lane);  // (C Hᵀ)[t][p]
-    float inter[8];
+    mm_acc<RM, 2>(acc, N, sC, 1, LN, i0, sH, 1, LN, lane);  // (C Hᵀ)[t][p]
+    float inter[RM];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RM; ++i) {
       const int t = i0 + i;
       float part = 0.f;
 #pragma unroll
@@ -517,30 +521,30 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
       inter[i] = part;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RM; ++i) {
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) inter[i] += __shfl_xor_sync(0xffffffffu, inter[i], o);
       if (lane == i) vInter[i0 + i] = inter[i];
     }
     // + Σ_τ E[t][τ] β_τ x_τ[p] + D x_t[p]
-    float accm[8][2];
+    float accm[RM][2];
     mm_zero(accm);
 #pragma unroll 4
     for (int k = 0; k < kQ; ++k) {
-      float av[8], bv[2];
+      float av[RM], bv[2];
       const float bk = sBeta[k];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) av[i] = sE[(i0 + i) * LQ + k];
+      for (int i = 0; i < RM; ++i) av[i] = sE[(i0 + i) * LQ + k];
 #pragma unroll
       for (int r = 0; r < 2; ++r) bv[r] = bk * sX[k * LP + lane + 32 * r];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < RM; ++i)
 #pragma unroll
         for (int r = 0; r < 2; ++r) accm[i][r] = fmaf(av[i], bv[r], accm[i][r]);
     }
     if (a.dz) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < RM; ++i) {
         const int t = i0 + i;
         if (t >= valid) continue;
 #pragma unroll
@@ -558,12 +562,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 
   // ---- dM = ḡ xᵀ: dML, K = dM ∘ M, the dβ sums ----
   {
-    float acc[8][2];
+    float acc[RM][2];
     mm_zero(acc);
-    mm_acc<8, 2>(acc, kP, sG, 1, LP, i0, sX, 1, LP, lane);  // dM[t][τ]
-    float rowK[8], colK[2] = {0.f, 0.f}, colB[2] = {0.f, 0.f};
+    mm_acc<RM, 2>(acc, kP, sG, 1, LP, i0, sX, 1, LP, lane);  // dM[t][τ]
+    float rowK[RM], colK[2] = {0.f, 0.f}, colB[2] = {0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RM; ++i) {
       const int t = i0 + i;
       float rk = 0.f;
 #pragma unroll
@@ -580,7 +584,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
       rowK[i] = rk;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RM; ++i) {
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) rowK[i] += __shfl_xor_sync(0xffffffffu, rowK[i], o);
       if (lane == i) vRowK[i0 + i] = rowK[i];
@@ -588,15 +592,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       sR[warp * kQ + lane + 32 * r] = colK[r];
-      sR[8 * kQ + warp * kQ + lane + 32 * r] = colB[r];
+      sR[NW * kQ + warp * kQ + lane + 32 * r] = colB[r];
     }
   }
   __syncthreads();
-  if (tid < kQ) {  // column sums over the 8 warps, in order
+  if (tid < kQ) {  // column sums over the warps, in order
     float ck = 0.f, cb = 0.f;
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < NW; ++w) {
       ck += sR[w * kQ + tid];
-      cb += sR[8 * kQ + w * kQ + tid];
+      cb += sR[NW * kQ + w * kQ + tid];
     }
     vColK[tid] = ck;
     vDbeta[tid] = cb;
@@ -605,14 +609,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 
   // ---- dx = D ḡ + Mᵀ ḡ + β exp(s_end - s) dH B; r_τ = exp(s_end - s_τ) x_τ·(dH B_τ) ----
   {
-    float acc[8][2], accd[8][2];
+    float acc[RM][2], accd[RM][2];
     mm_zero(acc);
     mm_zero(accd);
-    mm_acc<8, 2>(acc, kQ, sE, LQ, 1, i0, sG, LP, 1, lane);   // Σ_t E[t][τ] ḡ_t[p]
-    mm_acc<8, 2>(accd, N, sB, 1, LN, i0, sD, 1, LN, lane);  // (B dHᵀ)[τ][p]
-    float rr[8];
+    mm_acc<RM, 2>(acc, kQ, sE, LQ, 1, i0, sG, LP, 1, lane);   // Σ_t E[t][τ] ḡ_t[p]
+    mm_acc<RM, 2>(accd, N, sB, 1, LN, i0, sD, 1, LN, lane);  // (B dHᵀ)[τ][p]
+    float rr[RM];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RM; ++i) {
       const int tau = i0 + i;
       float part = 0.f;
 #pragma unroll
@@ -620,13 +624,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
       rr[i] = part;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RM; ++i) {
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) rr[i] += __shfl_xor_sync(0xffffffffu, rr[i], o);
       if (lane == i) vR[i0 + i] = rr[i] * sEe[i0 + i];
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RM; ++i) {
       const int tau = i0 + i;
       if (tau >= valid) continue;
       const float be = sBeta[tau], bee = be * sEe[tau];
@@ -641,29 +645,29 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 
   // ---- dC = exp(s) ḡ H + dML B;  dB = dMLᵀ C + β exp(s_end - s) x dH ----
   {
-    float acc[8][RN];
+    float acc[RM][RN];
     mm_zero(acc);
-    mm_acc<8, RN>(acc, kP, sG, 1, LP, i0, sH, LN, 1, lane);  // (ḡ H)[t][n]
+    mm_acc<RM, RN>(acc, kP, sG, 1, LP, i0, sH, LN, 1, lane);  // (ḡ H)[t][n]
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < RM; ++i)
 #pragma unroll
       for (int r = 0; r < RN; ++r) acc[i][r] *= sEs[i0 + i];
-    mm_acc<8, RN>(acc, kQ, sL, 1, LQ, i0, sB, LN, 1, lane);  // + (dML B)[t][n]
+    mm_acc<RM, RN>(acc, kQ, sL, 1, LQ, i0, sB, LN, 1, lane);  // + (dML B)[t][n]
     float* out = a.dCp + unit * kQ * N;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < RM; ++i)
 #pragma unroll
       for (int r = 0; r < RN; ++r) out[(i0 + i) * N + lane + 32 * r] = acc[i][r];
   }
   {
-    float acc[8][RN], accx[8][RN];
+    float acc[RM][RN], accx[RM][RN];
     mm_zero(acc);
     mm_zero(accx);
-    mm_acc<8, RN>(acc, kQ, sL, LQ, 1, i0, sC, LN, 1, lane);  // (dMLᵀ C)[τ][n]
-    mm_acc<8, RN>(accx, kP, sX, 1, LP, i0, sD, LN, 1, lane);  // (x dH)[τ][n]
+    mm_acc<RM, RN>(acc, kQ, sL, LQ, 1, i0, sC, LN, 1, lane);  // (dMLᵀ C)[τ][n]
+    mm_acc<RM, RN>(accx, kP, sX, 1, LP, i0, sD, LN, 1, lane);  // (x dH)[τ][n]
     float* out = a.dBp + unit * kQ * N;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RM; ++i) {
       const float w = sBeta[i0 + i] * sEe[i0 + i];
 #pragma unroll
       for (int r = 0; r < RN; ++r) out[(i0 + i) * N + lane + 32 * r] = fmaf(w, accx[i][r], acc[i][r]);
