@@ -203,12 +203,14 @@ __global__ void __launch_bounds__(kTcThreads) ssd_cb_tc_kernel(const SsdArgs p) 
 // whose descriptor has the K-step (1024 bytes) as its leading and the MN-step
 // (128 bytes) as its stride byte offset.
 //
-// Persistent CTAs (as many as fit on every SM) walk the (batch, chunk, head)
-// items, heads fastest so that the heads of a group reuse its C and C Bᵀ from
-// L2.  The operands of the next item (C, H, X and the step terms) are copied into
-// the other of two stages while the current one is computed, its C Bᵀ rows are
-// read into registers after the current M is built, and z is read into
-// registers, in the mapping of the final store, while the products run.  The
+// Persistent CTAs (as many as fit on every SM) walk contiguous ranges of the
+// (batch, chunk, head) items, heads fastest, so that consecutive items of one
+// group reuse its C tile (each stage remembers whose C it holds) and its C Bᵀ
+// rows (kept in registers).  The operands of the next item (C when its group
+// changes, H, X and the step terms) are copied into the other of two stages
+// while the current one is computed, its C Bᵀ rows are read into registers
+// after the current M is built, and z is read into registers, in the mapping
+// of the final store, while the products run.  The
 // epilogue reads the accumulators with the 16-lane shape (16x256b: thread i
 // holds rows i/4 and i/4 + 8 of its warp's 16, columns 2(i%4) and 2(i%4)+1 of
 // each group of 8), so all 32 threads of a warp work on its 16 rows, stages y in
@@ -294,15 +296,16 @@ __global__ void __launch_bounds__(kChunkThreads, 2) ssd_chunk_tc_kernel(const Ss
   // the operands of one item into a stage (16-byte cp.async; thread e's vector is
   // row 8i + (e & 7) of core-matrix column e >> 3, so 8 consecutive threads fill
   // one 128-byte core matrix), as one commit group
-  auto copy_stage = [&](const ChunkItem& w, unsigned char* st) {
+  auto copy_stage = [&](const ChunkItem& w, unsigned char* st, bool with_c) {
     const __nv_bfloat16* gC =
         static_cast<const __nv_bfloat16*>(p.C) + ((w.b * p.L + w.t0) * p.G + w.g) * N;
     const __nv_bfloat16* gH = p.ws_hin + ((w.b * p.nch + w.c) * p.H + w.h) * (int64_t)(P * N);
     for (int e = tid; e < kQ * KB; e += NT) {
       const int kb = (e >> 3) % KB, r = ((e >> 3) / KB) * 8 + (e & 7);
       const bool ok = r < w.valid;
-      cp_async16_zfill(st + S::sC + kmaj_off(r, 8 * kb, KB),
-                       gC + (int64_t)(ok ? r : 0) * p.G * N + 8 * kb, ok);
+      if (with_c)
+        cp_async16_zfill(st + S::sC + kmaj_off(r, 8 * kb, KB),
+                         gC + (int64_t)(ok ? r : 0) * p.G * N + 8 * kb, ok);
       cp_async16_zfill(st + S::sH + kmaj_off(r, 8 * kb, KB), gH + (int64_t)r * N + 8 * kb, true);
     }
     const __nv_bfloat16* gX =
@@ -323,8 +326,7 @@ __global__ void __launch_bounds__(kChunkThreads, 2) ssd_chunk_tc_kernel(const Ss
   // every 8-wide group that reaches τ <= t lies in one of them)
   float4 gv[kMv][2];
   float dh_pre = 0.f;  // the item's D
-  auto fetch_cb = [&](const ChunkItem& w) {  // and D of the head
-    dh_pre = p.D ? __ldg(p.D + w.h) : 0.f;
+  auto fetch_cb = [&](const ChunkItem& w) {
     const float* gG = p.ws_cb + ((w.b * p.nch + w.c) * p.G + w.g) * (int64_t)(kQ * kQ);
 #pragma unroll
     for (int i = 0; i < kMv; ++i) {
@@ -338,11 +340,20 @@ __global__ void __launch_bounds__(kChunkThreads, 2) ssd_chunk_tc_kernel(const Ss
     }
   };
 
-  uint32_t item = blockIdx.x;
+  // this CTA's items: a contiguous range (heads fastest), so consecutive items of
+  // one (batch, chunk, group) reuse its C tile (kept per stage) and C Bᵀ rows
+  const uint32_t beg = (uint32_t)((uint64_t)blockIdx.x * total / gridDim.x);
+  const uint32_t end = (uint32_t)((uint64_t)(blockIdx.x + 1) * total / gridDim.x);
+  auto group_key = [&](const ChunkItem& w) { return (uint32_t)((w.b * p.nch + w.c) * p.G + w.g); };
+  uint32_t ckey0 = 0xffffffffu, ckey1 = 0xffffffffu;  // the group whose C each stage holds
+  uint32_t item = beg;
   ChunkItem w = chunk_item(p, item);
-  if (item < total) {
-    copy_stage(w, sm);
+  uint32_t gkey = group_key(w);  // the group whose C Bᵀ rows gv holds
+  if (item < end) {
+    copy_stage(w, sm, true);
+    ckey0 = gkey;
     fetch_cb(w);
+    dh_pre = p.D ? __ldg(p.D + w.h) : 0.f;
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -353,15 +364,19 @@ __global__ void __launch_bounds__(kChunkThreads, 2) ssd_chunk_tc_kernel(const Ss
   const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16);
   const int r0 = 16 * quarter + (lane >> 2), cq = 2 * (lane & 3);
   bool ok = true;
-  for (int k = 0; item < total; ++k, item += gridDim.x) {
+  for (int k = 0; item < end; ++k, ++item) {
     const float Dh = dh_pre;
     unsigned char* st = sm + (size_t)(k & 1) * S::kStage;
     const float* sS = reinterpret_cast<const float*>(st + S::sS);
     const float* sBeta = sS + kQ;
-    const uint32_t next = item + gridDim.x;
-    const ChunkItem wn = chunk_item(p, next < total ? next : item);
-    if (next < total) {
-      copy_stage(wn, sm + (size_t)((k + 1) & 1) * S::kStage);
+    const uint32_t next = item + 1;
+    const ChunkItem wn = chunk_item(p, next < end ? next : item);
+    const uint32_t nkey = group_key(wn);
+    if (next < end) {
+      const int ns = (k + 1) & 1;
+      copy_stage(wn, sm + (size_t)ns * S::kStage, (ns ? ckey1 : ckey0) != nkey);
+      if (ns) ckey1 = nkey;
+      else ckey0 = nkey;
       asm volatile("cp.async.wait_group 1;" ::: "memory");  // this item's group
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -399,7 +414,11 @@ __global__ void __launch_bounds__(kChunkThreads, 2) ssd_chunk_tc_kernel(const Ss
       }
       *reinterpret_cast<uint4*>(sM + kmaj_off(t, 8 * kb, 8)) = v;
     }
-    if (next < total) fetch_cb(wn);
+    if (next < end) {
+      if (nkey != gkey) fetch_cb(wn);  // else gv already holds these rows
+      gkey = nkey;
+      dh_pre = p.D ? __ldg(p.D + wn.h) : 0.f;
+    }
     // z for the final store (row e / 8, channels (e % 8) * 8 .. + 7)
     uint4 zr[kVec];
     const __nv_bfloat16* gZ =
