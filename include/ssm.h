@@ -244,7 +244,7 @@ int ssm_status(const void* workspace, void* stream);
  *   - noalloc_limit_bytes > 0 lowers the scratch limit of ssm_scan_fwd_noalloc
  *     to that many bytes, so that its refusal can be tested;
  *   - scan_kernel picks the forward scan's kernel: 0 = by size (the default),
- *     1 = the block kernel, 2 = the warp kernel wherever it applies (N = 16,
+ *     1 = the block kernel, 2 = the two-warp-block kernel wherever it applies (N = 16,
  *     bf16, zero-order hold, views TMA can stage), so that both can be tested
  *     on small sizes.
  * enable = 0 restores the defaults.  Process-wide; for tests and tuning only.

@@ -293,7 +293,7 @@ def ssm_status(workspace=None, stream=None) -> int:
     return int(load().ssm_status(_ptr(workspace), _stream(stream)))
 
 
-SCAN_KERNEL_AUTO, SCAN_KERNEL_BLOCK, SCAN_KERNEL_WARP = 0, 1, 2
+SCAN_KERNEL_AUTO, SCAN_KERNEL_BLOCK, SCAN_KERNEL_PAIR = 0, 1, 2
 
 
 def ssm_set_test_mode(enable, wait_limit_ns=1000000, noalloc_limit_bytes=0,

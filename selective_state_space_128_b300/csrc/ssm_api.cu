@@ -64,7 +64,7 @@ bool flags_ok(int f) { return (f & ~(SSM_SOFTPLUS | SSM_EULER_B)) == 0; }
 std::atomic<int> g_test_mode{0};
 std::atomic<int64_t> g_test_limit_ns{1000000};
 std::atomic<int64_t> g_test_noalloc_limit{0};
-std::atomic<int> g_test_scan_kernel{0};  // 0: by size, 1: the block kernel, 2: the warp kernel
+std::atomic<int> g_test_scan_kernel{0};  // 0: by size, 1: the block kernel, 2: the two-warp-block kernel
 
 bool sizes_ok(int64_t batch, int64_t dim, int64_t seqlen) {
   // every flat index must fit in int64 with room to spare

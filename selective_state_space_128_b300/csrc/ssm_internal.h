@@ -75,11 +75,11 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
 cudaError_t scan_launch(const ScanArgs& a, int64_t N, int io_dtype, const ScanPlan& plan,
                         cudaStream_t stream);
 
-// The warp-autonomous scan (ssm_scan_fast.cu) for N = 16 and bf16 I/O whose views
+// The two-warp-block scan (ssm_scan_fast.cu) for N = 16 and bf16 I/O whose views
 // TMA can stage, zero-order hold: whether it applies, whether it is the faster
-// choice for these sizes (enough 8-channel warps to give every SM 16 of them:
-// below that the block kernel's shared conversion wins), and its launch
-// (a.status must point at a device word).
+// choice for these sizes (enough of its warps, one per 8 channels, to give every
+// SM 16 of them: below that the block kernel's shared conversion wins), and its
+// launch (a.status must point at a device word).
 bool scan_fast_applies(const ScanArgs& a, int64_t N, int io_dtype);
 bool scan_fast_preferred(const ScanArgs& a);
 cudaError_t scan_fast_launch(const ScanArgs& a, cudaStream_t stream);
@@ -154,7 +154,7 @@ int scan_fwd_internal(const void* u, const void* delta, const float* delta_bias,
 size_t noalloc_test_limit();
 
 // The scan kernel the test mode asks for: 0 = chosen by size, 1 = the block kernel
-// (ssm_scan.cu), 2 = the warp kernel (ssm_scan_fast.cu) wherever it applies.
+// (ssm_scan.cu), 2 = the two-warp-block kernel (ssm_scan_fast.cu) wherever it applies.
 int scan_kernel_choice();
 
 // Carry-record bytes of the split plan for these sizes on the current device (0:

@@ -931,8 +931,8 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
   if (!cfg_for(N, pl.chans, pl.chunk)) return pl;
   pl.seg_len = L > 0 ? L : 1;
   if (!allow_split || L <= 0 || batch <= 0 || dim <= 0) return pl;
-  // units of work that run at once: the fast scan's 8-channel warps (N = 16,
-  // bf16; split when fewer than 8 per SM) or this kernel's blocks (2 per SM)
+  // units of work that run at once: the fast scan's warps (one per 8 channels;
+  // N = 16, bf16; split when fewer than 8 per SM) or this kernel's blocks (2 per SM)
   const bool fast = N == 16 && io_dtype == 1;
   const int64_t unit = fast ? kFastChannels : pl.chans;
   const int64_t blocks = ((dim + unit - 1) / unit) * batch;

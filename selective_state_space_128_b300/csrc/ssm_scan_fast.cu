@@ -1,48 +1,52 @@
-// Selective-scan forward, warp-autonomous form, for N = 16 states and bf16 I/O.
+// Selective-scan forward for N = 16 states and bf16 I/O: blocks of two warps.
 //
 // Computes what ssm_scan.cu computes ("Mamba: Linear-Time Sequence Modeling"
 // summary page, section 4b equations (2), (4) and Algorithm 2; section 4a shape
 // table for the gate; the SSM/Mamba chapter's section 3.1 for D):
 //   Δ_t = softplus(delta + bias), Ā = exp(Δ A), B̄ u = (exp(Δ A) - 1)/A · B u,
 //   h_t = Ā h_{t-1} + B̄ u_t,  y_t = (C_t · h_t + D u_t) · silu(z_t),
-// for the common case (N = 16, bf16 u/Δ/z/y, zero-order hold, the
-// (batch, dim, L) layout with 16-byte rows).
+// for the common case (N = 16, bf16 u/Δ/z/y, zero-order hold, views TMA can
+// stage, time-major or channel-major).
 //
-// Design (B300).  The work is bound by instruction issue and the FP32 pipe:
-// per channel step it needs 16 exponentials and 6 FP32 operations per state
-// but moves only 8 bytes.  So every instruction that is not the recurrence is
-// overhead to cut, and the SMs must stay busy to the end of the grid.
+// Design (B300).  The work is bound by instruction issue, shared-memory
+// wavefronts and latency, not by HBM: per channel step it needs 16
+// exponentials and 6 FP32 operations per state but moves only 8 bytes.  So
+// every instruction that is not the recurrence is overhead to cut, and the SMs
+// must stay busy to the end of the grid.
 //
-//  * One warp is one unit of work: 32 / G channels of one batch row over one
-//    segment of the sequence, with its own TMA ring (u, Δ, z boxes of T x 32/G
-//    and the B, C boxes of T x N) and its own buffers.  No warp ever waits for
-//    another, so there is no block barrier; blocks are single warps, which the
-//    block scheduler spreads evenly over the SMs.
-//  * Each channel's 16 states sit on G lanes (NPT = 16 / G states each, in
-//    fp32 registers for the whole segment).  A state update is one MUFU ex2
-//    and packed f32x2 arithmetic: Ā = 2^(Δ·A·log2 e), v = -B u / A,
-//    h = Ā (h - v) + v (= Ā h + B̄ u); each lane writes its partial readout
-//    Σ_{its n} C_n h_n to a partial tile.
+//  * A block of 64 threads (two warps) owns 16 channels of one batch row over
+//    one segment of the sequence, with its own TMA ring (u, Δ, z boxes of
+//    T x 16 and the B, C boxes of T x N) and its own buffers; blocks are small,
+//    so the block scheduler spreads them evenly over the SMs.
+//  * Each channel's 16 states sit on G = 4 threads (4 states each, in fp32
+//    registers for the whole segment); warp w holds state groups 2w and 2w + 1
+//    of all 16 channels (thread (w, lane l): channel l & 15, group 2w + (l >> 4)),
+//    so the warp-wide load of a B or C row touches two 16-byte addresses (two
+//    shared-memory wavefronts; four when one warp holds all four groups of 8
+//    channels).  A state update is one MUFU ex2 and packed f32x2 arithmetic:
+//    Ā = 2^(Δ·A·log2 e), v = -B u / A, h = Ā (h - v) + v (= Ā h + B̄ u); each
+//    thread writes its partial readout Σ_{its n} C_n h_n to a partial tile.
 //  * The per-channel-step work that is not per state runs once per channel
-//    step, split over the channel's G lanes (T / G steps each): the
+//    step, split over the channel's 4 threads (T / 4 steps each): the
 //    conversion (Δ = softplus(.) once, u, the gate silu(z) and D u) and the
-//    finalisation (y = (Σ partials + D u) · gate, rounded, one 16-byte store
-//    per lane and chunk).  The conversion of chunk i+1 is placed inside the
-//    unrolled step loop of chunk i's recurrence, whose dependency gaps it fills.
-//  * B and C are transposed to [t][n] once per chunk by the warp (2 loads and
-//    8 stores per lane and tensor, bank-conflict free), so a lane's NPT values
-//    of a step are two 16-byte loads.
+//    finalisation (y = (Σ partials + D u) · gate, rounded, one 8-byte store per
+//    thread and chunk).
+//  * B and C are transposed to [t][n] once per chunk (warp 0: B, warp 1: C; 2
+//    loads and 8 stores per lane, bank-conflict free), so a thread's 4 values of
+//    a step are one 16-byte load.
+//  * Two block barriers per chunk: after the conversion and transposition,
+//    after the recurrence.
 //
 // Long sequences with few channels are split into segments exactly as in
 // ssm_scan.cu (same carry records): pass 1 computes each segment's end state
 // from zero and its ΣΔ, pass 0 folds the carries of earlier segments into its
 // initial state and recomputes its segment with outputs.
 //
-// A warp whose channels have some A = 0 runs a plain per-lane loop in the
+// A block whose channels have some A = 0 runs a plain per-thread loop in the
 // precise flavour (CUDA libm expf / expm1f; A = 0 takes the limit Δ B) instead.
-// The only waits are on the warp's own TMA barriers; they are bounded, and a
+// The only waits are on the block's own TMA barriers; they are bounded, and a
 // wait that runs out records an error in the call's status word and ends the
-// warp after its copies in flight have landed.
+// block after its copies in flight have landed.
 #include <cuda.h>
 
 #include <cstring>
@@ -58,37 +62,7 @@ constexpr int kN = 16;    // states
 constexpr int kT = 16;    // steps per chunk
 constexpr int kNSU = 2;   // stages of the u / Δ / z ring (B, C: one stage)
 
-template <int G> struct FastCfg {
-  static constexpr int NPT = kN / G;  // states per lane
-  static constexpr int NP = NPT / 2;  // packed pairs per lane
-  static constexpr int CW = 32 / G;   // channels per warp
-  static constexpr int TE = kT / G;   // steps of a chunk each lane converts and finalises
-  static_assert(NPT % 4 == 0 && TE % 4 == 0, "16-byte vectors per lane");
-};
-
 __host__ __device__ constexpr size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// Shared memory of one warp (bytes; TMA destinations 128-byte aligned).
-template <int G> struct FastSmem {
-  using Cf = FastCfg<G>;
-  static constexpr int CW = Cf::CW;
-  static constexpr size_t kRawIO = (size_t)CW * kT * 2;      // one of u / Δ / z (bf16, [c][t])
-  static constexpr size_t kRawBC = (size_t)kN * kT * 4;      // one of B / C (fp32, [n][t])
-  static constexpr size_t kStageU = up(3 * kRawIO, 128);     // u | Δ | z
-  static constexpr size_t oStageU = 0;
-  static constexpr size_t oStageBC = kNSU * kStageU;         // B | C
-  static constexpr int RowBT = kN + 4;                       // floats per [t] row of B^T, C^T
-  static constexpr size_t kBT = (size_t)kT * RowBT * 4;      // B^T or C^T [t][n]
-  static constexpr size_t oBT = oStageBC + 2 * kRawBC;       // B^T | C^T
-  static constexpr int RowW = kT + 2;                        // pairs per [c] row of (Δ, u)
-  static constexpr size_t oW = oBT + 2 * kBT;                // (Δ, u) pairs [c][t]
-  static constexpr size_t kW = (size_t)CW * RowW * 8;
-  static constexpr size_t oP = oW + kW;                      // partials [g][c][t], swizzled
-  static constexpr size_t kP = (size_t)G * CW * kT * 4;
-  static constexpr size_t oBar = up(oP + kP, 8);             // kNSU + 1 mbarriers
-  static constexpr size_t kBytes = oBar + 8 * (kNSU + 1);
-  static constexpr size_t kLaunch = kBytes + 128;            // room to align the base
-};
 
 struct FastMaps {
   CUtensorMap u, d, z, b, c;
@@ -103,41 +77,34 @@ __device__ __forceinline__ void tma3d(void* dst, const CUtensorMap* map, uint64_
       : "memory");
 }
 
-// Index (in floats) of steps 4u..4u+3 of partial row `row` = g * CW + c (64 bytes
-// a row).  The 16-byte unit is XOR-swizzled so that the 8 lanes of a quarter warp
-// -- consecutive channels c, all state groups g -- touch 8 distinct bank groups
-// when they store one unit of their rows or read the units of one g.
-template <int G> __device__ __forceinline__ int pidx(int row, int unit) {
-  constexpr int CW = 32 / G;
-  const int g = row / CW, c = row % CW;
-  const int s = G == 4 ? g : ((c >> 1) & 1) | ((g & 1) << 1);
-  return row * kT + ((unit ^ s) << 2);
-}
-
 // Column of B^T / C^T where state n of step t is stored: the halves of a row are
 // swapped for t in 8..15, which spreads the transposition's stores over all 32
 // banks and keeps every aligned group of four states contiguous.
 __device__ __forceinline__ int bt_col(int t, int n) { return n ^ (((t >> 3) & 1) << 3); }
 
-// One lane's view of the launch.
+constexpr int kG = 4;             // state groups (threads per channel)
+constexpr int kNPT = kN / kG;     // states per thread
+constexpr int kCB = 16;           // channels per block
+constexpr int kThreads = 64;
+constexpr int kTE = kT / kG;      // steps of a chunk each thread converts and finalises
+static_assert(kTE == 4, "a thread's steps are one 16-byte unit of the partial tile");
+
+// One thread's view of the launch (the recurrence's mapping).
 struct FastLane {
-  int lane, c, g;     // lane, channel within the warp, state group
-  int64_t b, d0, d;   // batch row, first channel of the warp, this lane's channel
+  int lane, c, g;     // lane, channel within the block, state group
+  int64_t b, d0, d;   // batch row, first channel of the block, this thread's channel
   bool chan_ok;
 };
 
-// ---------------------------------------------------------------------------
-// Precise per-lane loop for warps with some A = 0 (rare; no TMA, plain loads).
-// ---------------------------------------------------------------------------
 template <int NPT> struct LaneStates {
   float h[NPT];
 };
 
 // The final state (pass 0, last segment) or the segment's carry record (pass 1).
-template <int G, int PASS>
+template <int PASS>
 __device__ __forceinline__ void write_lane_states(const ScanArgs& p, const FastLane& L, int seg,
                                                   const float* h) {
-  constexpr int NPT = FastCfg<G>::NPT;
+  constexpr int NPT = kNPT;
   if (!L.chan_ok) return;
   const int64_t row = L.b * p.dim + L.d;
   float* dst = nullptr;
@@ -153,18 +120,47 @@ __device__ __forceinline__ void write_lane_states(const ScanArgs& p, const FastL
   }
 }
 
-template <int G, int PASS>
-__device__ __noinline__ void precise_warp(const ScanArgs& p, const FastLane& L, int64_t t_begin,
-                                          int64_t t_end, LaneStates<FastCfg<G>::NPT> hs) {
-  using Cf = FastCfg<G>;
-  constexpr int NPT = Cf::NPT;
+// Shared memory of one block (bytes; TMA destinations 128-byte aligned).
+struct PairSmem {
+  static constexpr size_t kRawIO = (size_t)kCB * kT * 2;     // one of u / Δ / z (bf16)
+  static constexpr size_t kStageU = up(3 * kRawIO, 128);      // u | Δ | z
+  static constexpr size_t oStageU = 0;
+  static constexpr size_t kRawBC = (size_t)kN * kT * 4;       // one of B / C (fp32, [n][t])
+  static constexpr size_t oStageBC = kNSU * kStageU;          // B | C
+  static constexpr int RowBT = kN + 4;
+  static constexpr size_t kBT = (size_t)kT * RowBT * 4;       // B^T or C^T [t][n]
+  static constexpr size_t oBT = oStageBC + 2 * kRawBC;
+  static constexpr size_t oW = oBT + 2 * kBT;                 // (Δ, u) pairs [t][c]
+  static constexpr size_t kW = (size_t)kT * kCB * 8;
+  static constexpr size_t oP = oW + kW;                       // partials [g][c][t], swizzled
+  static constexpr size_t kP = (size_t)kG * kCB * kT * 4;
+  static constexpr size_t oBar = up(oP + kP, 8);              // kNSU + 1 mbarriers
+  static constexpr size_t kBytes = oBar + 8 * (kNSU + 1);
+  static constexpr size_t kLaunch = kBytes + 128;             // room to align the base
+};
+
+// Index (in floats) of steps 4u..4u+3 of partial row (g, c) (64 bytes a row).  The
+// 16-byte unit is XOR-swizzled by (c >> 1) & 3: the 8 threads of a quarter warp
+// (one group, 8 consecutive channels) touch 8 distinct bank groups.
+__device__ __forceinline__ int pair_pidx(int g, int c, int unit) {
+  return (g * kCB + c) * kT + ((unit ^ ((c >> 1) & 3)) << 2);
+}
+
+// Precise per-thread loop for blocks with some A = 0 (rare; plain loads through
+// the tensors' strides).  The four groups' partial readouts of a step meet in
+// `red` (two buffers of 4 x 16 floats, alternating by step: one barrier a step).
+template <int PASS>
+__device__ __noinline__ void precise_pair(const ScanArgs& p, const FastLane& L, int64_t t_begin,
+                                          int64_t t_end, LaneStates<kNPT> hs, float* red) {
+  constexpr int NPT = kNPT;
   float* h = hs.h;
   const __nv_bfloat16* u = static_cast<const __nv_bfloat16*>(p.u);
   const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(p.delta);
   const __nv_bfloat16* z = static_cast<const __nv_bfloat16*>(p.z);
   __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
-  const int64_t dd = L.chan_ok ? L.d : 0;  // lanes past dim read channel 0 and store nothing
-  const int64_t row = (L.b * p.dim + dd) * p.L;
+  const int64_t dd = L.chan_ok ? L.d : 0;  // threads past dim read channel 0 and store nothing
+  const int64_t ou = L.b * p.st_u[0] + dd * p.st_u[1], od = L.b * p.st_d[0] + dd * p.st_d[1];
+  const int64_t oz = L.b * p.st_z[0] + dd * p.st_z[1], oy = L.b * p.st_y[0] + dd * p.st_y[1];
   float Aj[NPT], invA[NPT];
 #pragma unroll
   for (int j = 0; j < NPT; ++j) {
@@ -180,9 +176,9 @@ __device__ __noinline__ void precise_warp(const ScanArgs& p, const FastLane& L, 
 #pragma unroll
       for (int j = 0; j < NPT; ++j) cp[j] = h[j];
     }
-    const float x = __bfloat162float(dl[row + t]) + bias;
+    const float x = __bfloat162float(dl[od + t * p.st_d[2]]) + bias;
     const float dt = p.softplus ? softplus_precise(x) : x;
-    const float ut = __bfloat162float(u[row + t]);
+    const float ut = __bfloat162float(u[ou + t * p.st_u[2]]);
     sumDt += dt;
     float acc = 0.f;
     const int64_t bc = L.b * kN * p.L + t;
@@ -195,49 +191,36 @@ __device__ __noinline__ void precise_warp(const ScanArgs& p, const FastLane& L, 
       if (PASS == 0) acc = fmaf(p.C[bc + (int64_t)n * p.L], h[j], acc);
     }
     if (PASS == 0) {
-#pragma unroll
-      for (int o = 1; o < G; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      float* r = red + ((t - t_begin) & 1) * (kG * kCB);
+      r[L.g * kCB + L.c] = acc;
+      __syncthreads();
       if (L.g == 0 && L.chan_ok) {
-        const float gate = z ? silu_precise(__bfloat162float(z[row + t])) : 1.f;
-        y[row + t] = __float2bfloat16_rn(fmaf(Dd, ut, acc) * gate);
+        const float s = (r[L.c] + r[kCB + L.c]) + (r[2 * kCB + L.c] + r[3 * kCB + L.c]);
+        const float gate = z ? silu_precise(__bfloat162float(z[oz + t * p.st_z[2]])) : 1.f;
+        y[oy + t * p.st_y[2]] = __float2bfloat16_rn(fmaf(Dd, ut, s) * gate);
       }
     }
   }
-  write_lane_states<G, PASS>(p, L, (int)blockIdx.z, h);
+  write_lane_states<PASS>(p, L, (int)blockIdx.z, h);
   if (PASS == 1 && L.chan_ok && L.g == 0)
     p.carry_s[(int64_t)blockIdx.z * p.batch * p.dim + L.b * p.dim + L.d] = sumDt;
 }
 
-// ---------------------------------------------------------------------------
-// The kernel.  PASS 0: outputs (y, final state).  PASS 1: segment end state
-// from a zero start and ΣΔ, for the split plan.
-//
-// Per chunk i the warp runs four phases, each separated by __syncwarp:
-//   1. wait for chunk i's copies; convert this lane's T/G steps of its channel
-//      (Δ = softplus(delta + bias) once per channel step, u, D u and the gate)
-//      into the (Δ, u) tile and registers; transpose B, C to [t][n];
-//   2. refill the stages just read (u / Δ / z of chunk i+NSU, B / C of i+1);
-//   3. the recurrence of chunk i (every lane, NPT states), partial readouts to
-//      the partial tile;
-//   4. finalise this lane's T/G steps: y = (Σ partials + D u) · gate.
-// Latency is hidden across warps (a warp needs about 10 KB of shared memory and
-// at most 112 registers at G = 4, so 18 fit on an SM), not inside one.
-// ---------------------------------------------------------------------------
-template <int G, int PASS>
-__global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
-    scan_fast_kernel(const ScanArgs p, const __grid_constant__ FastMaps maps) {
-  using Cf = FastCfg<G>;
-  using S = FastSmem<G>;
-  constexpr int NPT = Cf::NPT, NP = Cf::NP, CW = Cf::CW, TE = Cf::TE;
+template <int PASS>
+__global__ void __launch_bounds__(kThreads, 9)
+    scan_pair_kernel(const ScanArgs p, const __grid_constant__ FastMaps maps) {
+  using S = PairSmem;
+  constexpr int G = kG, NPT = kNPT, NP = NPT / 2, CB = kCB, TE = kTE;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
 
+  const int tid = threadIdx.x, warp = tid >> 5;
   FastLane L;
-  L.lane = threadIdx.x;
-  L.c = L.lane / G;
-  L.g = L.lane % G;
+  L.lane = tid & 31;
+  L.c = tid & (CB - 1);
+  L.g = 2 * warp + (L.lane >> 4);
   L.b = blockIdx.y;
-  L.d0 = (int64_t)blockIdx.x * CW;
+  L.d0 = (int64_t)blockIdx.x * CB;
   L.d = L.d0 + L.c;
   L.chan_ok = L.d < p.dim;
   const int seg = blockIdx.z;
@@ -247,7 +230,7 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
   const int nchunks = (seg_steps + kT - 1) / kT;
   const bool has_z = PASS == 0 && p.z != nullptr;
 
-  // this lane's states n = g*NPT + j: A, and the initial state
+  // this thread's states n = g*NPT + j: A, and the initial state
   float Aj[NPT];
   bool zeroA = false;
 #pragma unroll
@@ -271,11 +254,11 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
       for (int j = 0; j < NPT; ++j) h[j] = fmaf(expf(sk * Aj[j]), h[j], hk[j]);
     }
   }
-  if (__any_sync(0xffffffffu, zeroA)) {
+  if (__syncthreads_or(zeroA)) {
     LaneStates<NPT> hs;
 #pragma unroll
     for (int j = 0; j < NPT; ++j) hs.h[j] = h[j];
-    precise_warp<G, PASS>(p, L, t_begin, t_end, hs);
+    precise_pair<PASS>(p, L, t_begin, t_end, hs, reinterpret_cast<float*>(sm + S::oP));
     return;
   }
 
@@ -287,13 +270,13 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
   const uint64_t wlim = stall ? (uint64_t)p.test_limit_ns : kWaitLimitNs;
   const uint32_t bytes_u = (uint32_t)(S::kRawIO * (has_z ? 3 : 2));
   const uint32_t bytes_bc = (uint32_t)(S::kRawBC * (PASS == 0 ? 2 : 1));
-  // lane 0: the copies of chunk k (u / Δ / z into stage k % NSU; B / C into the B/C stage)
+  // thread 0: the copies of chunk k (u / Δ / z into stage k % NSU; B / C into the B/C stage)
   auto issue_u = [&](int k) {
     unsigned char* st = sm + S::oStageU + (k % kNSU) * S::kStageU;
     uint64_t* bar = &bar_u[k % kNSU];
     mbar_arrive_expect_tx(bar, bytes_u);
     if (stall && k == 1) return;  // the failure-path test: armed, never copied
-    // time-major boxes (T steps, CW channels) or channel-major ones (CW, T)
+    // time-major boxes (T steps, CB channels) or channel-major ones (CB, T)
     const int tk = (int)(t_begin + (int64_t)k * kT);
     const int x = p.bld ? (int)L.d0 : tk, y = p.bld ? tk : (int)L.d0, zc = (int)L.b;
     tma3d(st, &maps.u, bar, x, y, zc);
@@ -306,17 +289,17 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
     tma3d(sm + S::oStageBC, &maps.b, bar_bc, x, 0, zc);
     if (PASS == 0) tma3d(sm + S::oStageBC + S::kRawBC, &maps.c, bar_bc, x, 0, zc);
   };
-  // chunks whose u / Δ / z copies were issued and waited for (the same in every lane)
+  // chunks whose u / Δ / z copies were issued and waited for (the same in every thread)
   int issued = min(kNSU, nchunks), consumed = 0;
-  if (L.lane == 0) {
+  if (tid == 0) {
     for (int s = 0; s <= kNSU; ++s) mbar_init(&bar_u[s], 1);
     fence_mbar_init();
     for (int k = 0; k < issued; ++k) issue_u(k);
     if (nchunks > 0) issue_bc(0);
   }
-  __syncwarp();
+  __syncthreads();
 
-  // per-lane constants: A·log2(e) and -1/A as packed pairs, the channel's bias and D
+  // per-thread constants: A·log2(e) and -1/A as packed pairs, the channel's bias and D
   f2 A2p[NP], nIp[NP], hp[NP];
 #pragma unroll
   for (int q = 0; q < NP; ++q) {
@@ -332,21 +315,17 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
   float* const BT = reinterpret_cast<float*>(sm + S::oBT);
   float* const CT = BT + S::kBT / 4;
   float* const P = reinterpret_cast<float*>(sm + S::oP);
-  // this lane's first output of the segment
+  // this thread's first output of the segment
   __nv_bfloat16* const ybase =
       PASS == 0 ? static_cast<__nv_bfloat16*>(p.y) + L.b * p.st_y[0] +
                       (L.chan_ok ? L.d : 0) * p.st_y[1] + (t_begin + L.g * TE) * p.st_y[2]
                 : nullptr;
   bool failed = false;
-  int i = 0;
-  for (; i < nchunks; ++i) {
-    // 1. chunk i's copies, conversion and transposition
-    if (!mbar_wait_bounded(&bar_u[i % kNSU], (uint32_t)((i / kNSU) & 1), wlim) ||
-        !mbar_wait_bounded(bar_bc, (uint32_t)(i & 1), wlim)) {
-      failed = true;
-      break;
-    }
-    consumed = i + 1;
+  for (int i = 0; i < nchunks; ++i) {
+    // 1. chunk i's copies; conversion of this thread's TE steps of its channel;
+    //    B (warp 0) and C (warp 1) transposed to [t][n]
+    const bool ok = mbar_wait_bounded(&bar_u[i % kNSU], (uint32_t)((i / kNSU) & 1), wlim) &&
+                    mbar_wait_bounded(bar_bc, (uint32_t)(i & 1), wlim);
     const int tc = min(kT, seg_steps - i * kT);
     float du[TE], gate[TE];
     {
@@ -356,67 +335,62 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
       const __nv_bfloat16* sz = reinterpret_cast<const __nv_bfloat16*>(st + 2 * S::kRawIO);
       float dl[TE], uu[TE], zz[TE];
       if (!p.bld) {
-        const int off = L.c * kT + L.g * TE;  // this lane's steps in a [c][t] box
+        const int off = L.c * kT + L.g * TE;  // this thread's steps in a [c][t] box
         vecio<__nv_bfloat16, TE>::load(sd + off, dl);
         vecio<__nv_bfloat16, TE>::load(su + off, uu);
         if (has_z) vecio<__nv_bfloat16, TE>::load(sz + off, zz);
       } else {
-        // a [t][c] box: this lane's steps are CW elements apart
+        // a [t][c] box: this thread's steps are CB elements apart
 #pragma unroll
         for (int j = 0; j < TE; ++j) {
-          const int e = (L.g * TE + j) * CW + L.c;
+          const int e = (L.g * TE + j) * CB + L.c;
           dl[j] = __bfloat162float(sd[e]);
           uu[j] = __bfloat162float(su[e]);
           if (has_z) zz[j] = __bfloat162float(sz[e]);
         }
       }
       const bool whole = tc == kT;
-      float wv[2 * TE];
 #pragma unroll
       for (int j = 0; j < TE; ++j) {
         const float x = dl[j] + bias;
         float dt = sp ? softplus_fast(x) : x;
         float u = uu[j];
         if (!whole) {  // steps past the segment: exact no-ops (Δ = 0, u = 0)
-          const bool ok = L.g * TE + j < tc;
-          dt = ok ? dt : 0.f;
-          u = ok ? u : 0.f;
+          const bool in = L.g * TE + j < tc;
+          dt = in ? dt : 0.f;
+          u = in ? u : 0.f;
         }
-        wv[2 * j] = dt;
-        wv[2 * j + 1] = u;
-        if (PASS == 1) sumDt += dt;  // every lane of the channel sums its own steps
+        W[(L.g * TE + j) * CB + L.c] = make_float2(dt, u);
+        if (PASS == 1) sumDt += dt;  // every thread of the channel sums its own steps
         if (PASS == 0) {
           du[j] = Dd * u;
           gate[j] = has_z ? silu_fast(zz[j]) : 1.f;
         }
       }
-      {  // this lane's (Δ, u) pairs, two per 16-byte store
-        float4* wrow = reinterpret_cast<float4*>(W + L.c * S::RowW + L.g * TE);
+      // warp 0: B, warp 1: C, to [t][n]; lane l moves [n = (l >> 2) + 8 r][t = 4 (l & 3) .. + 3]
+      if (PASS == 0 || warp == 0) {
+        const unsigned char* src = sm + S::oStageBC + warp * S::kRawBC;
+        float* dst = warp == 0 ? BT : CT;
+        const int t0 = 4 * (L.lane & 3);
 #pragma unroll
-        for (int j = 0; j < TE / 2; ++j)
-          wrow[j] = make_float4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
-      }
-      // B, C to [t][n]: lane l moves [n = (l >> 2) + 8 r][t = 4 (l & 3) .. + 3]
-      const int t0 = 4 * (L.lane & 3);
+        for (int r = 0; r < 2; ++r) {
+          const int n = (L.lane >> 2) + 8 * r;
+          const float4 q = *reinterpret_cast<const float4*>(src + (n * kT + t0) * 4);
+          const float v[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int n = (L.lane >> 2) + 8 * r;
-        const float4 bq = *reinterpret_cast<const float4*>(sm + S::oStageBC + (n * kT + t0) * 4);
-        const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) BT[(t0 + e) * S::RowBT + bt_col(t0 + e, n)] = bv[e];
-        if (PASS == 0) {
-          const float4 cq = *reinterpret_cast<const float4*>(sm + S::oStageBC + S::kRawBC +
-                                                             (n * kT + t0) * 4);
-          const float cv[4] = {cq.x, cq.y, cq.z, cq.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) CT[(t0 + e) * S::RowBT + bt_col(t0 + e, n)] = cv[e];
+          for (int e = 0; e < 4; ++e) dst[(t0 + e) * S::RowBT + bt_col(t0 + e, n)] = v[e];
         }
       }
     }
-    __syncwarp();
+    // every thread's copies landed (else the block leaves together); the stages
+    // just read are free, the (Δ, u) and B^T / C^T tiles complete
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    consumed = i + 1;
     // 2. refill: u / Δ / z of chunk i + NSU into the stage just converted, B / C of i+1
-    if (L.lane == 0) {
+    if (tid == 0) {
       if (issued < nchunks) issue_u(issued);
       if (i + 1 < nchunks) issue_bc(i + 1);
     }
@@ -443,7 +417,7 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
         }
       };
       auto load_step = [&](int t, f2& du2, f2 (&bq)[NP], f2 (&cq)[NP]) {
-        const float2 w = W[L.c * S::RowW + t];
+        const float2 w = W[t * CB + L.c];
         du2 = pack2(w.x, w.y);
         const int col = bt_col(t, L.g * NPT);  // NPT >= 4: the group stays contiguous
         load_row(BT + t * S::RowBT + col, bq);
@@ -489,7 +463,7 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
           unpack2(acc2, lo, hi);
           acc[t % 4] = lo + hi;
           if (t % 4 == 3)
-            *reinterpret_cast<float4*>(P + pidx<G>(L.g * CW + L.c, t / 4)) =
+            *reinterpret_cast<float4*>(P + pair_pidx(L.g, L.c, t / 4)) =
                 make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
         if (t + 1 < kT) {
@@ -510,23 +484,20 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
         }
       }
     }
-    __syncwarp();
-    // 4. finalise this lane's steps of chunk i
+    // the partials are complete; the next chunk's conversion may overwrite the tiles
+    __syncthreads();
+    // 4. finalise this thread's steps of chunk i (unit g of its channel's row)
     if (PASS == 0) {
+      float4 s4 = *reinterpret_cast<const float4*>(P + pair_pidx(0, L.c, L.g));
+#pragma unroll
+      for (int gg = 1; gg < G; ++gg) {
+        const float4 o = *reinterpret_cast<const float4*>(P + pair_pidx(gg, L.c, L.g));
+        s4.x += o.x; s4.y += o.y; s4.z += o.z; s4.w += o.w;
+      }
+      const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
       float y[TE];
 #pragma unroll
-      for (int u4 = 0; u4 < TE / 4; ++u4) {
-        const int unit = (L.g * TE) / 4 + u4;
-        float4 s4 = *reinterpret_cast<const float4*>(P + pidx<G>(L.c, unit));
-#pragma unroll
-        for (int gg = 1; gg < G; ++gg) {
-          const float4 o = *reinterpret_cast<const float4*>(P + pidx<G>(gg * CW + L.c, unit));
-          s4.x += o.x; s4.y += o.y; s4.z += o.z; s4.w += o.w;
-        }
-        const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[4 * u4 + e] = (sv[e] + du[4 * u4 + e]) * gate[4 * u4 + e];
-      }
+      for (int e = 0; e < TE; ++e) y[e] = (sv[e] + du[e]) * gate[e];
       __nv_bfloat16* dst = ybase + (int64_t)i * kT * p.st_y[2];
       if (L.chan_ok) {
         if (p.vec_y && L.g * TE + TE <= tc) {
@@ -538,12 +509,11 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
         }
       }
     }
-    __syncwarp();  // the tiles are free for the next chunk
   }
   if (failed) {
-    // a wait ran out: record it, let this warp's copies still in flight land
+    // a wait ran out: record it, let this block's copies still in flight land
     // (bounded) and leave without writing a state
-    if (L.lane == 0) {
+    if (tid == 0) {
       atomicExch(p.status, 1);
       for (int k = consumed; k < issued; ++k)
         (void)mbar_wait_bounded(&bar_u[k % kNSU], (uint32_t)((k / kNSU) & 1), wlim);
@@ -553,13 +523,15 @@ __global__ void __launch_bounds__(32, G == 2 ? 12 : 18)
   }
 #pragma unroll
   for (int q = 0; q < NP; ++q) unpack2(hp[q], h[2 * q], h[2 * q + 1]);
-  write_lane_states<G, PASS>(p, L, seg, h);
+  write_lane_states<PASS>(p, L, seg, h);
   if (PASS == 1) {
-    // the channel's ΣΔ: each of its G lanes summed its own steps
-#pragma unroll
-    for (int o = 1; o < G; o <<= 1) sumDt += __shfl_xor_sync(0xffffffffu, sumDt, o);
+    // the channel's ΣΔ: each of its G threads summed its own steps
+    float* R = P;
+    R[L.g * CB + L.c] = sumDt;
+    __syncthreads();
     if (L.chan_ok && L.g == 0)
-      p.carry_s[(int64_t)seg * p.batch * p.dim + L.b * p.dim + L.d] = sumDt;
+      p.carry_s[(int64_t)seg * p.batch * p.dim + L.b * p.dim + L.d] =
+          (R[L.c] + R[CB + L.c]) + (R[2 * CB + L.c] + R[3 * CB + L.c]);
   }
 }
 
@@ -598,10 +570,10 @@ bool map3(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t esz, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int G, int PASS>
-cudaError_t launch_fast_one(const ScanArgs& a, const FastMaps& m, int nz, cudaStream_t stream) {
-  constexpr size_t bytes = FastSmem<G>::kLaunch;
-  auto kern = scan_fast_kernel<G, PASS>;
+template <int PASS>
+cudaError_t launch_pair_one(const ScanArgs& a, const FastMaps& m, int nz, cudaStream_t stream) {
+  constexpr size_t bytes = PairSmem::kLaunch;
+  auto kern = scan_pair_kernel<PASS>;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -613,20 +585,18 @@ cudaError_t launch_fast_one(const ScanArgs& a, const FastMaps& m, int nz, cudaSt
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  dim3 grid((unsigned)((a.dim + FastCfg<G>::CW - 1) / FastCfg<G>::CW), (unsigned)a.batch,
-            (unsigned)nz);
-  kern<<<grid, 32, bytes, stream>>>(a, m);
+  dim3 grid((unsigned)((a.dim + kCB - 1) / kCB), (unsigned)a.batch, (unsigned)nz);
+  kern<<<grid, kThreads, bytes, stream>>>(a, m);
   return cudaGetLastError();
 }
 
-template <int G>
-cudaError_t launch_fast(const ScanArgs& a, cudaStream_t stream) {
-  FastMaps m;
+// Tensor maps of one launch: u / Δ / z boxes of T steps x CW channels, B / C boxes
+// of T steps x N states.
+bool fast_maps(const ScanArgs& a, uint32_t CW, FastMaps& m) {
   memset(&m, 0, sizeof m);
   const uint64_t L = (uint64_t)a.L, D = (uint64_t)a.dim, Bt = (uint64_t)a.batch;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                             f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  constexpr uint32_t CW = FastCfg<G>::CW;
   // u / Δ / z: time-major (L, dim, batch) with (T, CW) boxes, or channel-major
   // (dim, L, batch) with (CW, T) boxes
   const uint64_t i0 = a.bld ? D : L, i1 = a.bld ? L : D;
@@ -636,12 +606,17 @@ cudaError_t launch_fast(const ScanArgs& a, cudaStream_t stream) {
             map3(&m.d, a.delta, bf, 2, i0, i1, Bt, b0, b1, a.st_d[o1], a.st_d[0]) &&
             map3(&m.b, a.B, f32, 4, L, kN, Bt, kT, kN) && map3(&m.c, a.C, f32, 4, L, kN, Bt, kT, kN);
   if (ok && a.z) ok = map3(&m.z, a.z, bf, 2, i0, i1, Bt, b0, b1, a.st_z[o1], a.st_z[0]);
-  if (!ok) return cudaErrorInvalidValue;
+  return ok;
+}
+
+cudaError_t launch_pair(const ScanArgs& a, cudaStream_t stream) {
+  FastMaps m;
+  if (!fast_maps(a, kCB, m)) return cudaErrorInvalidValue;
   if (a.nseg > 1) {
-    const cudaError_t e = launch_fast_one<G, 1>(a, m, a.nseg - 1, stream);
+    const cudaError_t e = launch_pair_one<1>(a, m, a.nseg - 1, stream);
     if (e != cudaSuccess) return e;
   }
-  return launch_fast_one<G, 0>(a, m, a.nseg, stream);
+  return launch_pair_one<0>(a, m, a.nseg, stream);
 }
 
 }  // namespace
@@ -656,12 +631,12 @@ bool scan_fast_preferred(const ScanArgs& a) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t warps = (a.dim + FastCfg<4>::CW - 1) / FastCfg<4>::CW * a.batch * a.nseg;
+  const int64_t warps = (a.dim + kCB - 1) / kCB * 2 * a.batch * a.nseg;
   return warps >= (int64_t)sms * 16;
 }
 
 cudaError_t scan_fast_launch(const ScanArgs& a, cudaStream_t stream) {
-  return launch_fast<4>(a, stream);
+  return launch_pair(a, stream);
 }
 
 }  // namespace ssm

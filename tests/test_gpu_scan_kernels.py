@@ -1,17 +1,18 @@
-"""GPU parity of the warp-autonomous scan kernel on small sizes.
+"""GPU parity of the two-warp-block scan kernel on small sizes.
 
 The forward scan has two kernels: the block kernel (blocks of 32 channels that
-share their conversion; every dstate and dtype) and the warp kernel (one warp
-per 8 channels, no block barriers; N = 16, bf16, zero-order hold, views TMA can
-stage), chosen by size: the warp kernel when there are enough of its warps to give
-every SM 16.  The test mode's kernel choice runs the warp kernel here on sizes
-that span several warps, chunks and a ragged tail, against the fp64 oracle (bar
-1e-2 for bf16 I/O), with the cases its own code paths handle: steps past the
-sequence, channels past dim, no gate / D / bias / softplus, a zero A (its precise
-per-lane loop), an initial state and a carry over two calls, a sequence split
-across warps (both passes), the channel-major layout and strided halves of one
-projection (bit-equal to the time-major contiguous run), and the training
-forward's saved states (the backward from them equals the backward that
+share their conversion; every dstate and dtype) and the two-warp-block kernel
+(blocks of 64 threads for 16 channels, each warp holding two of a channel's
+four state groups; N = 16, bf16, zero-order hold, views TMA can stage), chosen
+by size: the second when there are enough of its warps to give every SM 16.  The
+test mode's kernel choice runs it here on sizes that span several blocks, chunks
+and a ragged tail, against the fp64 oracle (bar 1e-2 for bf16 I/O), with the
+cases its own code paths handle: steps past the sequence, channels past dim, no
+gate / D / bias / softplus, a zero A (its precise per-thread loop, also through
+channel-major and strided views), an initial state and a carry over two calls, a
+sequence split across blocks (both passes), the channel-major layout and strided
+halves of one projection (bit-equal to the time-major contiguous run), and the
+training forward's saved states (the backward from them equals the backward that
 recomputes them)."""
 import numpy as np
 import pytest
@@ -28,8 +29,8 @@ TOL = 1e-2
 
 
 @pytest.fixture(autouse=True)
-def warp_kernel():
-    ssm.ssm_set_test_mode(True, 1_000_000, scan_kernel=ssm.SCAN_KERNEL_WARP)
+def pair_kernel():
+    ssm.ssm_set_test_mode(True, 1_000_000, scan_kernel=ssm.SCAN_KERNEL_PAIR)
     yield
     ssm.ssm_set_test_mode(False)
 
@@ -77,7 +78,7 @@ def test_zero_A_takes_the_precise_path():
     w = synth.scaled(synth.MAMBA_130M, batch=2, dim=32, seqlen=96, seed=530)
     x = synth.make_scan_inputs(w)
     x["A"] = x["A"].copy()
-    x["A"][3, 5] = 0.0      # warp 0's channels take the precise loop, the others the fast path
+    x["A"][3, 5] = 0.0      # block 0's channels take the precise loop, the others the fast path
     _, y, h = _run(w, x)
     y_o, h_o = _oracle(x)
     assert oracle.rel_err(host64(y), y_o) <= TOL
@@ -134,6 +135,30 @@ def test_channel_major_and_strided_views_are_bit_equal():
     assert torch.equal(y2, y0) and torch.equal(h2, h0)
     y_o, _ = _oracle(x)
     assert oracle.rel_err(host64(y0), y_o) <= TOL
+
+
+def test_zero_A_channel_major_and_strided_views_are_bit_equal():
+    # the precise loop reads and writes through the tensors' strides
+    w = synth.scaled(synth.MAMBA_130M, batch=2, dim=48, seqlen=200, seed=565)
+    x = synth.make_scan_inputs(w)
+    x["A"] = x["A"].copy()
+    x["A"][5, 3] = 0.0
+    x["A"][40, 0] = 0.0
+    g, y0, h0 = _run(w, x)
+    t = {k: g[k].transpose(1, 2).contiguous() for k in ("u", "delta", "z")}
+    y1, h1 = ssm.scan(t["u"], t["delta"], g["A"], g["B"], g["C"], g["D"], t["z"], g["delta_bias"],
+                      bld=True)
+    xz = torch.cat([g["u"], g["z"]], dim=1)
+    y2 = torch.empty_like(y0)
+    h2 = torch.empty_like(h0)
+    ssm.ssm_scan_fwd_strided(xz[:, :48], g["delta"], g["delta_bias"], g["A"], g["B"], g["C"],
+                             g["D"], xz[:, 48:], True, y2, h2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.transpose(1, 2), y0) and torch.equal(h1, h0)
+    assert torch.equal(y2, y0) and torch.equal(h2, h0)
+    y_o, h_o = _oracle(x)
+    assert oracle.rel_err(host64(y0), y_o) <= TOL
+    assert oracle.rel_err(host64(h0), h_o) <= TOL
 
 
 def test_training_forward_saves_the_backward_states():

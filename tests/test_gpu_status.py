@@ -43,9 +43,9 @@ def _call(g, w, flags, ws, stream):
     return y, h
 
 
-@pytest.mark.parametrize("kernel", [ssm.SCAN_KERNEL_BLOCK, ssm.SCAN_KERNEL_WARP])
+@pytest.mark.parametrize("kernel", [ssm.SCAN_KERNEL_BLOCK, ssm.SCAN_KERNEL_PAIR])
 def test_stalled_block_reports_timeout_in_its_own_workspace(kernel):
-    """With either forward kernel (the block kernel and the warp kernel)."""
+    """With either forward kernel (the block kernel and the two-warp-block kernel)."""
     w, x, g = _inputs()
     y_o, h_o = oracle.scan(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
                            x["delta_bias"])
