@@ -13,7 +13,8 @@ alternate between steps, so a step never reads data the previous step left in L2
   loop timed;
 * the Mamba-130M-shaped layer (batch 8, d_inner 1536, L 2048, N 16);
 * the one-token decode step (batch 256, d_inner 5120, N 16; four such groups
-  advanced round-robin so that the 336 MB of state exceeds L2);
+  advanced round-robin so that the 336 MB of state exceeds L2), launched step by
+  step and as the 1000 steps captured in one CUDA graph and replayed;
 * the backward, the conv1d front end and Mamba-2 SSD;
 * end-to-end figures through the C ABI with host buffers, the oracle's CPU
   throughput, the roofline of the scan kernel and the SM clocks sampled during
@@ -735,7 +736,9 @@ def bench_decode(dw, steps, world, groups=4):
     a state that is not in the 126 MB L2 and the write-back of earlier states'
     updates happens inside the timed region (336 MB of state in total).  Inputs are
     drawn on the device (seeded torch generator, the workload's distributions); the
-    states start from a GPU scan over a 256-step prefill."""
+    states start from a GPU scan over a 256-step prefill.  The same steps are also
+    captured once in a CUDA graph and replayed: the device time without a host call
+    per step."""
     import torch
     import selective_state_space_128_b300 as ssm
     gen = torch.Generator(device="cuda")
@@ -786,7 +789,29 @@ def bench_decode(dw, steps, world, groups=4):
     g1.record(stream)
     torch.cuda.synchronize()
     l2_ms = max_over_ranks(world, g0.elapsed_time(g1)) / steps
-    return dict(step_ms=step_ms, l2_resident_ms=l2_ms, steps=steps, groups=groups)
+    # the same round-robin steps captured once as a CUDA graph and replayed `replays`
+    # times: the device time of the steps without a host call per step
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cs = torch.cuda.current_stream()
+        for i in range(steps):
+            ssm.ssm_state_update_ex(states[i % groups], u[i], dl[i], bias, True, A, Bs[i], Cs[i],
+                                    Dp, z[i], y[i], stream=cs)
+    graph.replay()
+    torch.cuda.synchronize()
+    replays = 5
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    r0.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(world, r0.elapsed_time(r1)) / (replays * steps)
+    del graph
+    return dict(step_ms=step_ms, l2_resident_ms=l2_ms, steps=steps, groups=groups,
+                graph_step_ms=graph_ms, graph_replays=replays)
 
 
 # ---------------------------------------------------------------------------
@@ -1034,6 +1059,17 @@ def main():
                                     dec["groups"], dec["groups"] * 4.0 * synth.DECODE.batch *
                                     synth.DECODE.dim * synth.DECODE.dstate / 1e6),
                           "us_per_step_one_group_back_to_back": dec["l2_resident_ms"] * 1e3,
+                          "graph": {"us_per_step": dec["graph_step_ms"] * 1e3,
+                                    "tokens_per_s": synth.DECODE.batch /
+                                                    (dec["graph_step_ms"] / 1e3) * world,
+                                    "hbm_gbs": db / (dec["graph_step_ms"] / 1e3) / 1e9,
+                                    "hbm_frac": db / (dec["graph_step_ms"] / 1e3) / 1e9 / hbm_peak,
+                                    "replays": dec["graph_replays"],
+                                    "call": "the same %d round-robin steps captured once in a "
+                                            "CUDA graph (torch.cuda.CUDAGraph around "
+                                            "ssm_state_update_ex), replayed %d times" % (
+                                                dec["steps"], dec["graph_replays"]),
+                                    "gpu_launches": dec["steps"] * dec["graph_replays"]},
                           "one_group_note": "one 84 MB state advanced back to back; the "
                                             "state's loads and stores carry evict-first "
                                             "hints, so it streams from HBM as well",

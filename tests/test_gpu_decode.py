@@ -1,5 +1,6 @@
 """GPU parity of ssm_state_update / ssm_state_update_ex (one-token decode) against the
-fp64 oracle, and the decode == scan invariant."""
+fp64 oracle, the decode == scan invariant, and a loop of steps replayed from a CUDA
+graph."""
 import numpy as np
 import pytest
 import torch
@@ -127,3 +128,47 @@ def test_whole_channel_blocks_with_zero_A(gate, softplus):
         assert oracle.rel_err(host64(y), y_ref) <= 1e-2
         assert oracle.rel_err(host64(st), st_ref) <= 1e-2
     assert ssm.ssm_status(None) == ssm.SSM_OK
+
+
+def test_decode_steps_replayed_from_a_cuda_graph():
+    """The decode entry point makes no synchronising call, so a loop of steps can be
+    captured once in a CUDA graph and replayed: the replay equals the same steps
+    launched one by one, bit for bit, and the oracle."""
+    dw, s = _decode_case(4, 96, 16, 12, seed=44)
+    A = dev_f32(synth.gen_A(dw.dim, 16))
+    D = dev_f32(synth.fill(45, synth.S_D, 0, dw.dim, synth.UNIFORM, 0.5, 1.5))
+    bias_h = synth.gen_delta_bias(45, dw.dim)
+    bias = dev_f32(bias_h)
+    st0 = np.random.default_rng(46).standard_normal((dw.batch, dw.dim, 16)).astype(np.float32)
+    ins = [dict(u=dev_io(s["u"][i]), delta=dev_io(s["delta"][i]), z=dev_io(s["z"][i]),
+                B=dev_f32(s["B"][i]), C=dev_f32(s["C"][i])) for i in range(dw.steps)]
+
+    def run(st, ys, stream):
+        for i, x in enumerate(ins):
+            ssm.ssm_state_update_ex(st, x["u"], x["delta"], bias, True, A, x["B"], x["C"], D,
+                                    x["z"], ys[i], stream=stream)
+
+    st_a = dev_f32(st0)
+    ys_a = [torch.empty((dw.batch, dw.dim), dtype=torch.bfloat16, device="cuda")
+            for _ in range(dw.steps)]
+    run(st_a, ys_a, torch.cuda.current_stream())
+    st_b = dev_f32(st0)
+    ys_b = [torch.empty_like(y) for y in ys_a]
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(st_b, ys_b, torch.cuda.current_stream())
+    st_b.copy_(dev_f32(st0))   # the capture recorded the steps without running them
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(st_b, st_a)
+    assert all(torch.equal(yb, ya) for yb, ya in zip(ys_b, ys_a))
+    st_ref = st0.astype(np.float64)
+    Ah = synth.gen_A(dw.dim, 16)
+    Dh = synth.fill(45, synth.S_D, 0, dw.dim, synth.UNIFORM, 0.5, 1.5)
+    for i in range(dw.steps):
+        y_ref, st_ref = oracle.step(st_ref, s["u"][i], s["delta"][i], Ah, s["B"][i], s["C"][i], Dh,
+                                    s["z"][i], bias_h, True)
+        assert oracle.rel_err(host64(ys_b[i]), y_ref) <= 1e-2
+    assert oracle.rel_err(host64(st_b), st_ref) <= 1e-2
