@@ -932,12 +932,15 @@ ScanPlan scan_plan(int64_t batch, int64_t dim, int64_t L, int64_t N, int io_dtyp
   pl.seg_len = L > 0 ? L : 1;
   if (!allow_split || L <= 0 || batch <= 0 || dim <= 0) return pl;
   // units of work that run at once: the fast scan's warps (one per 8 channels;
-  // N = 16, bf16; split when fewer than 8 per SM) or this kernel's blocks (2 per SM)
+  // N = 16, bf16: split when fewer than 8 per SM, into segments for 16 per SM,
+  // enough for both passes to run on the two-warp-block kernel) or this
+  // kernel's blocks (2 per SM)
   const bool fast = N == 16 && io_dtype == 1;
   const int64_t unit = fast ? kFastChannels : pl.chans;
   const int64_t blocks = ((dim + unit - 1) / unit) * batch;
-  const int64_t want = (int64_t)sm_count * (fast ? 8 : 2);
-  if (blocks >= want) return pl;
+  const int64_t need = (int64_t)sm_count * (fast ? 8 : 2);
+  const int64_t want = (int64_t)sm_count * (fast ? 16 : 2);
+  if (blocks >= need) return pl;
   int64_t nseg = (want + blocks - 1) / blocks;
   const int64_t max_by_len = L / (32 * (int64_t)pl.chunk);  // at least 32 chunks per segment
   if (nseg > max_by_len) nseg = max_by_len;
