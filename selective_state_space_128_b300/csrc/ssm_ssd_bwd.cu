@@ -33,17 +33,18 @@
 //           Euler: no β term), then dΔ_raw = dΔ σ(Δ_raw + bias) for softplus;
 //   dz_t  = dy_t · y_t (before the gate) · silu'(z_t),  dD += Σ ḡ·x.
 //
-// Kernels (all arithmetic in fp32 on the CUDA cores: the parameter
-// derivatives sum many products of fp32 intermediates, which bf16 tensor-core
-// operands would round to 8 bits):
+// Kernels:
 //  1. the forward's step terms (s, β) per (batch, chunk, head);
 //  2. a forward walk over the chunks writing each chunk's entering state H_{c-1}
 //     in fp32, and a reverse walk writing each dH_c and d init_state; both are
-//     parallel over (batch, head, a quarter of the state's rows);
+//     parallel over (batch, head, half of the state's rows) and run their
+//     products on the tensor cores (mma.sync), the fp32 operand split into two
+//     bf16 parts so that the sums keep about 16 bits;
 //  3. one block of 16 warps per (batch, chunk, head) for everything above: the
-//     chunk's operands in shared memory, its products as register-tiled loops
-//     over shared memory (4 rows a warp); per-head partial dB, dC, da, d dt_bias,
-//     dD to a workspace;
+//     chunk's operands in shared memory, its products as register-tiled fp32
+//     loops over shared memory on the CUDA cores (4 rows a warp; the parameter
+//     derivatives sum many products of fp32 intermediates); per-head partial
+//     dB, dC, da, d dt_bias, dD to a workspace;
 //  4. the sums over a group's heads (dB, dC) and over batch and chunks (da,
 //     d dt_bias, dD) in a fixed order, so results repeat bit for bit.
 #include <cstdint>
@@ -52,13 +53,13 @@
 #include "../../include/ssm.h"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
+#include "ssm_mma.cuh"
 
 namespace ssm {
 namespace {
 
 constexpr int kQ = kSsdChunk;  // chunk length
 constexpr int kP = 64;         // head dimension
-constexpr int kWalkThreads = 128;
 constexpr int kChunkThreads = 512;  // 16 warps: 4 rows of every 64-row product each
 constexpr int kChunkWarps = kChunkThreads / 32;
 constexpr int kRM = kQ / kChunkWarps;  // rows of every product a warp takes
@@ -79,207 +80,169 @@ struct SsdBwd {
 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16 v) { return __bfloat162float(v); }
-__device__ __forceinline__ void unpack_bf16x8(const uint4 q, float (&v)[8]) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    v[2 * k] = __uint_as_float(w[k] << 16);
-    v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-  }
-}
 __device__ __forceinline__ float sigmoid_precise(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // ---------------------------------------------------------------------------
-// 2a. Forward walk: H_c = exp(s_end) H_{c-1} + Σ_τ w_τ x_τ B_τᵀ, storing every
-//     H_{c-1}.  Block (quarter of the rows, head, batch); thread t holds row
-//     p = 16 q + t / 8 and the columns n = 4 (t % 8 + 8 j) .. + 3.
+// 2. The walks, on the tensor cores.  Both are S <- exp(s_end(c)) S + A_cᵀ K_c
+//    over the chunks, storing S before each update:
+//      forward: S = H, chunks in order, A_c[τ][p] = w_τ x_τ[p], K_c = B; the
+//               stored S of chunk c is H_{c-1}, the state entering it;
+//      reverse: S = dH, from the last chunk, A_c[t][p] = exp(s_t) ḡ_t[p],
+//               K_c = C; the stored S of chunk c is dH_c, and the S left at
+//               the end is d init_state.
+//    A block owns 32 rows p of one head's P x N state: two warps, each holding
+//    16 rows in mma accumulators (fp32) for the whole walk.  A_cᵀ K_c runs as
+//    mma.sync m16n8k16: K_c (bf16 inputs, exact) through transposed ldmatrix
+//    loads, A_c formed in fp32 in registers from its staged bf16 inputs and
+//    split into two bf16 parts (hi = A rounded, lo = A - hi rounded), two
+//    products per fragment, so the sum is within about 2^-16 of the fp32 one.
+//    The next chunk's inputs and step terms are in flight (cp.async, two
+//    stages) while a chunk is used.
 // ---------------------------------------------------------------------------
-template <int N>
-__global__ void __launch_bounds__(kWalkThreads) ssd_bwd_fwalk_kernel(const SsdBwd a) {
-  constexpr int NV = N / 32;  // float4 column groups a thread holds
-  __shared__ __align__(16) float sB[kQ * N];
-  __shared__ __align__(16) float sX[kQ * 16];  // w_τ x_τ[p] for the block's 16 rows
-  __shared__ float sEnd;
-  const int tid = threadIdx.x;
-  const int q = blockIdx.x, h = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int pl = tid / 8, p = 16 * q + pl, g = h / (int)(a.H / a.G);
-  float4 hv[NV];
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int n = 4 * (tid % 8 + 8 * j);
-    hv[j] = a.init ? *reinterpret_cast<const float4*>(a.init + ((b * a.H + h) * kP + p) * N + n)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  // a chunk's B (8-wide vectors) and w x (the block's 16 rows), loaded one chunk
-  // ahead into registers
-  // (thread t's x vector: step t / 2, rows 8 (t % 2) .. + 7 of the block's 16)
-  constexpr int NBV = kQ * N / 8 / kWalkThreads;
-  static_assert(kQ * 2 == kWalkThreads, "one 8-wide x vector a thread");
-  uint4 rb[NBV];
-  uint4 rx;
-  float rw;
-  auto fetch = [&](int64_t c) {
-    const int64_t t0 = c * kQ;
-    const int valid = (int)min64(kQ, a.L - t0);
-    const float* tr = a.terms + ((b * a.nch + c) * a.H + h) * kSsdTermsRec;
-#pragma unroll
-    for (int i = 0; i < NBV; ++i) {
-      const int e = tid + i * kWalkThreads, tau = e / (N / 8), n8 = e % (N / 8);
-      rb[i] = tau < valid ? __ldg(reinterpret_cast<const uint4*>(a.B + ((b * a.L + t0 + tau) * a.G + g) * N + 8 * n8))
-                          : make_uint4(0, 0, 0, 0);
-    }
-    const int tau = tid / 2;
-    const bool ok = tau < valid;
-    rx = ok ? __ldg(reinterpret_cast<const uint4*>(a.x + ((b * a.L + t0 + tau) * a.H + h) * kP + 16 * q + 8 * (tid % 2)))
-            : make_uint4(0, 0, 0, 0);
-    rw = ok ? __ldg(tr + 2 * kQ + tau) : 0.f;
-  };
-  if (a.nch > 0) fetch(0);
-  for (int64_t c = 0; c < a.nch; ++c) {
-    const int64_t unit = (b * a.nch + c) * a.H + h;
-    float* out = a.Hin + unit * kP * N + (int64_t)p * N;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
-    const float* tr = a.terms + unit * kSsdTermsRec;
-    __syncthreads();  // the previous chunk's readers are done
-#pragma unroll
-    for (int i = 0; i < NBV; ++i) {
-      const int e = tid + i * kWalkThreads, tau = e / (N / 8), n8 = e % (N / 8);
-      float v[8];
-      unpack_bf16x8(rb[i], v);
-      float4* dst = reinterpret_cast<float4*>(sB + tau * N + 8 * n8);
-      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-    }
-    {
-      float v[8];
-      unpack_bf16x8(rx, v);
-      float4* dst = reinterpret_cast<float4*>(sX + tid * 8);
-      dst[0] = make_float4(rw * v[0], rw * v[1], rw * v[2], rw * v[3]);
-      dst[1] = make_float4(rw * v[4], rw * v[5], rw * v[6], rw * v[7]);
-    }
-    if (tid == 0) sEnd = expf(tr[kQ - 1]);
-    __syncthreads();
-    if (c + 1 < a.nch) fetch(c + 1);
-    const float e_end = sEnd;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      hv[j].x *= e_end; hv[j].y *= e_end; hv[j].z *= e_end; hv[j].w *= e_end;
-    }
-    for (int tau = 0; tau < kQ; ++tau) {
-      const float xv = sX[tau * 16 + pl];
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const float4 bv = *reinterpret_cast<const float4*>(sB + tau * N + 4 * (tid % 8 + 8 * j));
-        hv[j].x = fmaf(xv, bv.x, hv[j].x);
-        hv[j].y = fmaf(xv, bv.y, hv[j].y);
-        hv[j].z = fmaf(xv, bv.z, hv[j].z);
-        hv[j].w = fmaf(xv, bv.w, hv[j].w);
-      }
-    }
-  }
+constexpr int kWalkRows = 32;                  // state rows per block
+constexpr int kWalkThreads = kWalkRows / 16 * 32;
+
+template <int N, bool REV> struct WalkCfg {
+  static constexpr int RX = kWalkRows + 8;     // [τ][p] slice rows (bf16): 80 bytes
+  static constexpr int RK = N + 8;             // [τ][n] tile rows (bf16)
+  static constexpr int oA = 0;                             // x or dy slice
+  static constexpr int oZ = oA + kQ * RX;                  // z slice (reverse)
+  static constexpr int oK = oZ + (REV ? kQ * RX : 0);      // B or C tile
+  static constexpr int oT = oK + kQ * RK;                  // step terms [s | β | w] (fp32)
+  static constexpr int kStage = oT + 2 * kSsdTermsRec;     // bf16 elements per stage
+  static constexpr size_t kBytes = (size_t)2 * kStage * 2;
+  static_assert((oK * 2) % 16 == 0 && (oT * 2) % 16 == 0 && (kStage * 2) % 16 == 0, "16-byte rows");
+};
+
+// the fp32 values v0, v1 (consecutive columns of one fragment row) as bf16 pairs
+// hi = (v0, v1) rounded and lo = the remainders rounded
+__device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(v0, v1);
+  lo = pack_bf16(v0 - __uint_as_float(hi << 16), v1 - __uint_as_float(hi & 0xffff0000u));
 }
 
-// ---------------------------------------------------------------------------
-// 2b. Reverse walk: dH_{c-1} = exp(s_end(c)) dH_c + Σ_{t in c} exp(s_t) ḡ_t C_tᵀ
-//     from dH_{last} = d final_state, storing every dH_c; d init_state = dH_{-1}.
-// ---------------------------------------------------------------------------
-template <int N>
-__global__ void __launch_bounds__(kWalkThreads) ssd_bwd_rwalk_kernel(const SsdBwd a) {
-  constexpr int NV = N / 32;
-  __shared__ __align__(16) float sC[kQ * N];
-  __shared__ __align__(16) float sG[kQ * 16];  // exp(s_t) ḡ_t[p] for the block's 16 rows
-  __shared__ float sEnd;
-  const int tid = threadIdx.x;
-  const int q = blockIdx.x, h = blockIdx.y;
+template <int N, bool REV>
+__global__ void __launch_bounds__(kWalkThreads) ssd_bwd_walk_kernel(const SsdBwd a) {
+  using Cf = WalkCfg<N, REV>;
+  constexpr int RX = Cf::RX, RK = Cf::RK, NT = kWalkThreads;
+  extern __shared__ float4 walk_smem[];
+  __nv_bfloat16* tiles = reinterpret_cast<__nv_bfloat16*>(walk_smem);
+  const int p0 = blockIdx.x * kWalkRows, h = blockIdx.y;
   const int64_t b = blockIdx.z;
-  const int pl = tid / 8, p = 16 * q + pl, g = h / (int)(a.H / a.G);
-  float4 hv[NV];
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int n = 4 * (tid % 8 + 8 * j);
-    hv[j] = a.dfin ? *reinterpret_cast<const float4*>(a.dfin + ((b * a.H + h) * kP + p) * N + n)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  // a chunk's C (8-wide vectors) and exp(s_t) ḡ_t (the block's 16 rows), loaded
-  // one chunk ahead into registers
-  // (thread t's dy and z vectors: step t / 2, rows 8 (t % 2) .. + 7 of the block's 16)
-  constexpr int NBV = kQ * N / 8 / kWalkThreads;
-  static_assert(kQ * 2 == kWalkThreads, "one 8-wide dy vector a thread");
-  uint4 rc[NBV];
-  uint4 rdy, rz;
-  float rs;
-  auto fetch = [&](int64_t c) {
+  const int g = h / (int)(a.H / a.G);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t nch = a.nch;
+  const bool gate = REV && a.z != nullptr;
+
+  auto stage = [&](int64_t c, int buf) {
+    __nv_bfloat16* st = tiles + buf * Cf::kStage;
     const int64_t t0 = c * kQ;
     const int valid = (int)min64(kQ, a.L - t0);
-    const float* tr = a.terms + ((b * a.nch + c) * a.H + h) * kSsdTermsRec;
-#pragma unroll
-    for (int i = 0; i < NBV; ++i) {
-      const int e = tid + i * kWalkThreads, t = e / (N / 8), n8 = e % (N / 8);
-      rc[i] = t < valid ? __ldg(reinterpret_cast<const uint4*>(a.C + ((b * a.L + t0 + t) * a.G + g) * N + 8 * n8))
-                        : make_uint4(0, 0, 0, 0);
-    }
-    const int t = tid / 2;
-    const bool ok = t < valid;
-    const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + 16 * q + 8 * (tid % 2);
-    rdy = ok ? __ldg(reinterpret_cast<const uint4*>(a.dy + o)) : make_uint4(0, 0, 0, 0);
-    rz = (ok && a.z) ? __ldg(reinterpret_cast<const uint4*>(a.z + o)) : make_uint4(0, 0, 0, 0);
-    rs = ok ? __ldg(tr + t) : 0.f;
+    const int64_t row0 = ((b * a.L + t0) * a.H + h) * kP + p0;
+    ssd_stage<kQ, kWalkRows, RX, NT>(st + Cf::oA, (REV ? a.dy : a.x) + row0, a.H * kP, valid);
+    if (gate) ssd_stage<kQ, kWalkRows, RX, NT>(st + Cf::oZ, a.z + row0, a.H * kP, valid);
+    ssd_stage<kQ, N, RK, NT>(st + Cf::oK, (REV ? a.C : a.B) + ((b * a.L + t0) * a.G + g) * N,
+                             a.G * N, valid);
+    const float* src = a.terms + ((b * nch + c) * a.H + h) * kSsdTermsRec;
+    for (int e = threadIdx.x; e < kSsdTermsRec / 4; e += NT)
+      cp_async16(reinterpret_cast<float*>(st + Cf::oT) + 4 * e, src + 4 * e, true);
+    cp_async_commit();
   };
-  if (a.nch > 0) fetch(a.nch - 1);
-  for (int64_t c = a.nch - 1; c >= 0; --c) {
-    const int64_t unit = (b * a.nch + c) * a.H + h;
-    float* out = a.dHc + unit * kP * N + (int64_t)p * N;
+
+  // this thread's accumulator elements: rows rl, rl + 8 of the block's slice
+  // (head rows p0 + rl, + 8); columns 8j + cc, +1
+  const int rl = 16 * w + (lane >> 2), cc = 2 * (lane & 3);
+  const int64_t head = (b * a.H + h) * (int64_t)(kP * N) + (int64_t)(p0 + rl) * N + cc;
+  const float* s0 = REV ? a.dfin : a.init;
+  float acc[N / 8][4];
 #pragma unroll
-    for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
-    const float* tr = a.terms + unit * kSsdTermsRec;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < NBV; ++i) {
-      const int e = tid + i * kWalkThreads, t = e / (N / 8), n8 = e % (N / 8);
-      float v[8];
-      unpack_bf16x8(rc[i], v);
-      float4* dst = reinterpret_cast<float4*>(sC + t * N + 8 * n8);
-      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-    }
-    {
-      // exp(s_t) ḡ_t with ḡ = dy · silu(z) (steps past the end: dy = 0)
-      float gv[8], zv[8];
-      unpack_bf16x8(rdy, gv);
-      unpack_bf16x8(rz, zv);
-      const float es = expf(rs);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) gv[k] *= (a.z ? silu_precise(zv[k]) : 1.f) * es;
-      float4* dst = reinterpret_cast<float4*>(sG + tid * 8);
-      dst[0] = make_float4(gv[0], gv[1], gv[2], gv[3]);
-      dst[1] = make_float4(gv[4], gv[5], gv[6], gv[7]);
-    }
-    if (tid == 0) sEnd = expf(tr[kQ - 1]);
-    __syncthreads();
-    if (c > 0) fetch(c - 1);
-    const float e_end = sEnd;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      hv[j].x *= e_end; hv[j].y *= e_end; hv[j].z *= e_end; hv[j].w *= e_end;
-    }
-    for (int t = 0; t < kQ; ++t) {
-      const float gv = sG[t * 16 + pl];
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const float4 cv = *reinterpret_cast<const float4*>(sC + t * N + 4 * (tid % 8 + 8 * j));
-        hv[j].x = fmaf(gv, cv.x, hv[j].x);
-        hv[j].y = fmaf(gv, cv.y, hv[j].y);
-        hv[j].z = fmaf(gv, cv.z, hv[j].z);
-        hv[j].w = fmaf(gv, cv.w, hv[j].w);
-      }
+  for (int j = 0; j < N / 8; ++j) {
+    if (s0) {
+      const float2 u = *reinterpret_cast<const float2*>(s0 + head + 8 * j);
+      const float2 v = *reinterpret_cast<const float2*>(s0 + head + 8 * N + 8 * j);
+      acc[j][0] = u.x; acc[j][1] = u.y; acc[j][2] = v.x; acc[j][3] = v.y;
+    } else {
+      acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     }
   }
-  if (a.dinit) {
-    float* out = a.dinit + ((b * a.H + h) * kP + p) * N;
+  float* const outbase = REV ? a.dHc : a.Hin;
+  const int64_t dir = REV ? -1 : 1;
+  int64_t c = REV ? nch - 1 : 0;
+  if (nch > 0) stage(c, 0);
+  for (int64_t k = 0; k < nch; ++k, c += dir) {
+    const int buf = (int)(k & 1);
+    const bool more = k + 1 < nch;
+    if (more) stage(c + dir, buf ^ 1);
+    {  // S before the update
+      float* out = outbase + ((b * nch + c) * a.H + h) * (int64_t)(kP * N) + (int64_t)(p0 + rl) * N + cc;
 #pragma unroll
-    for (int j = 0; j < NV; ++j) *reinterpret_cast<float4*>(out + 4 * (tid % 8 + 8 * j)) = hv[j];
+      for (int j = 0; j < N / 8; ++j) {
+        *reinterpret_cast<float2*>(out + 8 * j) = make_float2(acc[j][0], acc[j][1]);
+        *reinterpret_cast<float2*>(out + 8 * N + 8 * j) = make_float2(acc[j][2], acc[j][3]);
+      }
+    }
+    if (more) cp_async_wait<1>(); else cp_async_wait<0>();
+    __syncthreads();  // chunk c's slices, tile and terms are visible
+    const __nv_bfloat16* st = tiles + buf * Cf::kStage;
+    const __nv_bfloat16* sA = st + Cf::oA;
+    const __nv_bfloat16* sZ = st + Cf::oZ;
+    const __nv_bfloat16* sK = st + Cf::oK;
+    const float* sT = reinterpret_cast<const float*>(st + Cf::oT);  // [s | β | w]
+    const float decay = expf(sT[kQ - 1]);
+#pragma unroll
+    for (int j = 0; j < N / 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][e] *= decay;
+#pragma unroll
+    for (int ks = 0; ks < kQ / 16; ++ks) {
+      // A_cᵀ fragment: rows p, k = τ; the slices are stored [τ][p] -> transposed
+      // loads; fragment registers 0, 1 hold steps tau, tau + 1, registers 2, 3
+      // steps tau + 8, tau + 9
+      uint32_t ah[4], al[4];
+      {
+        const int i = lane >> 3;
+        const int off = (16 * ks + (i >> 1) * 8 + (lane & 7)) * RX + 16 * w + (i & 1) * 8;
+        uint32_t af[4], zf[4];
+        ldsm_x4_t(af, sA + off);
+        if (gate) ldsm_x4_t(zf, sZ + off);
+        const int tau = 16 * ks + cc;
+        float cw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = tau + (e >> 1) * 8 + (e & 1);
+          cw[e] = REV ? expf(sT[t]) : sT[2 * kQ + t];  // exp(s_t) or w_τ
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          float v0 = __uint_as_float(af[r] << 16), v1 = __uint_as_float(af[r] & 0xffff0000u);
+          if (gate) {
+            v0 *= silu_precise(__uint_as_float(zf[r] << 16));
+            v1 *= silu_precise(__uint_as_float(zf[r] & 0xffff0000u));
+          }
+          const int e = (r >> 1) * 2;
+          split_bf16x2(v0 * cw[e], v1 * cw[e + 1], ah[r], al[r]);
+        }
+      }
+#pragma unroll
+      for (int nn = 0; nn < N / 16; ++nn) {
+        // K_c: k = τ, n; stored [τ][n] -> transposed loads, two n8 tiles
+        uint32_t kf[4];
+        ldsm_x4_t(kf, sK + (16 * ks + (lane & 15)) * RK + 16 * nn + (lane >> 4) * 8);
+        mma_bf16(acc[2 * nn], ah, kf[0], kf[1]);
+        mma_bf16(acc[2 * nn], al, kf[0], kf[1]);
+        mma_bf16(acc[2 * nn + 1], ah, kf[2], kf[3]);
+        mma_bf16(acc[2 * nn + 1], al, kf[2], kf[3]);
+      }
+    }
+    __syncthreads();  // the next iteration's copies reuse this stage
+  }
+  if (REV && a.dinit) {
+    float* out = a.dinit + head;
+#pragma unroll
+    for (int j = 0; j < N / 8; ++j) {
+      *reinterpret_cast<float2*>(out + 8 * j) = make_float2(acc[j][0], acc[j][1]);
+      *reinterpret_cast<float2*>(out + 8 * N + 8 * j) = make_float2(acc[j][2], acc[j][3]);
+    }
   }
 }
 
@@ -778,22 +741,29 @@ __global__ void ssd_bwd_reduce_kernel(const SsdBwd a, int N) {
 
 template <int N>
 cudaError_t ssd_bwd_typed(const SsdBwd& a, cudaStream_t st) {
-  const dim3 wg(kP / 16, (unsigned)a.H, (unsigned)a.batch);
-  ssd_bwd_fwalk_kernel<N><<<wg, kWalkThreads, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ssd_bwd_rwalk_kernel<N><<<wg, kWalkThreads, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   constexpr size_t bytes = ChunkBwdSmem<N>::kBytes;
+  constexpr size_t fbytes = WalkCfg<N, false>::kBytes, rbytes = WalkCfg<N, true>::kBytes;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
+  cudaError_t e;
   if (configured_dev != dev) {
     e = cudaFuncSetAttribute(ssd_bwd_chunk_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)bytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(ssd_bwd_walk_kernel<N, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fbytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(ssd_bwd_walk_kernel<N, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rbytes);
+    if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
+  const dim3 wg(kP / kWalkRows, (unsigned)a.H, (unsigned)a.batch);
+  ssd_bwd_walk_kernel<N, false><<<wg, kWalkThreads, fbytes, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ssd_bwd_walk_kernel<N, true><<<wg, kWalkThreads, rbytes, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ssd_bwd_chunk_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch), kChunkThreads,
                             bytes, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
