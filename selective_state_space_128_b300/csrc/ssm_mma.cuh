@@ -11,8 +11,13 @@
 
 namespace ssm {
 
-// Four 8x8 bf16 matrices from shared memory, transposed (each lane gives one
-// row address: lanes 8i..8i+7 the rows of matrix i).
+// Four 8x8 bf16 matrices from shared memory (each lane gives one row address:
+// lanes 8i..8i+7 the rows of matrix i); the _t form transposes each.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
 __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

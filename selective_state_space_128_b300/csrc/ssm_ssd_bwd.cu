@@ -41,10 +41,9 @@
 //     products on the tensor cores (mma.sync), the fp32 operand split into two
 //     bf16 parts so that the sums keep about 16 bits;
 //  3. one block of 16 warps per (batch, chunk, head) for everything above: the
-//     chunk's operands in shared memory, its products as register-tiled fp32
-//     loops over shared memory on the CUDA cores (4 rows a warp; the parameter
-//     derivatives sum many products of fp32 intermediates); per-head partial
-//     dB, dC, da, d dt_bias, dD to a workspace;
+//     chunk's operands in shared memory as bf16 tiles (the fp32 intermediates
+//     split in two parts the same way), its ten products on the tensor cores;
+//     per-head partial dB, dC, da, d dt_bias, dD to a workspace;
 //  4. the sums over a group's heads (dB, dC) and over batch and chunks (da,
 //     d dt_bias, dD) in a fixed order, so results repeat bit for bit.
 #include <cstdint>
@@ -60,9 +59,8 @@ namespace {
 
 constexpr int kQ = kSsdChunk;  // chunk length
 constexpr int kP = 64;         // head dimension
-constexpr int kChunkThreads = 512;  // 16 warps: 4 rows of every 64-row product each
+constexpr int kChunkThreads = 512;  // 16 warps: a 16-row block and a column quarter each
 constexpr int kChunkWarps = kChunkThreads / 32;
-constexpr int kRM = kQ / kChunkWarps;  // rows of every product a warp takes
 
 struct SsdBwd {
   const __nv_bfloat16 *x, *dt, *z, *dy, *B, *C;
@@ -247,79 +245,110 @@ __global__ void __launch_bounds__(kWalkThreads) ssd_bwd_walk_kernel(const SsdBwd
 }
 
 // ---------------------------------------------------------------------------
-// 3. Per (batch, chunk, head): every derivative of the chunk.
+// 3. Per (batch, chunk, head): every derivative of the chunk, its ten products
+//    on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation).
+//    x, B and C are bf16 inputs (exact operands); each fp32 intermediate (ḡ,
+//    H_{c-1}, dH_c, E β, dML) is held as two bf16 tiles, the rounded value and
+//    the rounded remainder, and a product takes three part products when both
+//    operands are split (hi hi + hi lo + lo hi: the lo lo term lies below 2^-16
+//    of the result) and two when one is exact, so the sums keep about 16 bits.
+//    Tiles are [row][col] bf16 with rows padded by 8 elements (ldmatrix's eight
+//    row addresses fall in distinct bank groups).  16 warps: warp w owns the
+//    16-row block w % 4 of every product's output and the quarter w / 4 of its
+//    columns, so the values an earlier product left in a warp's registers sit
+//    at the positions a later one needs.
 // ---------------------------------------------------------------------------
-// acc[i][r] += Σ_k A(k, i0 + i) B(k, lane + 32 r), A(k, i) = A[k ak + i ai],
-// B(k, j) = Bm[k bk + j bj]: a warp's 32 lanes take interleaved columns (the
-// strides along j are 1 or odd, so the lanes' loads hit distinct banks) and
-// share its RM rows (broadcast loads).
-template <int RM, int RN>
-__device__ __forceinline__ void mm_acc(float (&acc)[RM][RN], int K, const float* A, int ak, int ai,
-                                       int i0, const float* Bm, int bk, int bj, int lane) {
-#pragma unroll 4
-  for (int k = 0; k < K; ++k) {
-    float av[RM], bv[RN];
-#pragma unroll
-    for (int i = 0; i < RM; ++i) av[i] = A[k * ak + (i0 + i) * ai];
-#pragma unroll
-    for (int r = 0; r < RN; ++r) bv[r] = Bm[k * bk + (lane + 32 * r) * bj];
-#pragma unroll
-    for (int i = 0; i < RM; ++i)
-#pragma unroll
-      for (int r = 0; r < RN; ++r) acc[i][r] = fmaf(av[i], bv[r], acc[i][r]);
-  }
+// A fragment (rows m0.., k0..k0+15) of a row-major [m][k] tile with row stride ld
+__device__ __forceinline__ void frag_a(uint32_t (&f)[4], const __nv_bfloat16* t, int ld, int m0,
+                                       int k0, int lane) {
+  ldsm_x4(f, t + (m0 + (lane & 15)) * ld + k0 + (lane >> 4) * 8);
 }
-template <int RM, int RN> __device__ __forceinline__ void mm_zero(float (&acc)[RM][RN]) {
-#pragma unroll
-  for (int i = 0; i < RM; ++i)
-#pragma unroll
-    for (int r = 0; r < RN; ++r) acc[i][r] = 0.f;
+// A fragment of the transpose of a [k][m] tile
+__device__ __forceinline__ void frag_at(uint32_t (&f)[4], const __nv_bfloat16* t, int ld, int m0,
+                                        int k0, int lane) {
+  ldsm_x4_t(f, t + (k0 + (lane & 7) + (lane >> 4) * 8) * ld + m0 + ((lane >> 3) & 1) * 8);
+}
+// B fragments of the two n8 tiles n0.., n0+8.. (k0..k0+15) of a [k][n] tile:
+// f[0], f[1] the first, f[2], f[3] the second
+__device__ __forceinline__ void frag_b_kn(uint32_t (&f)[4], const __nv_bfloat16* t, int ld, int k0,
+                                          int n0, int lane) {
+  ldsm_x4_t(f, t + (k0 + (lane & 15)) * ld + n0 + (lane >> 4) * 8);
+}
+// ... of an [n][k] tile
+__device__ __forceinline__ void frag_b_nk(uint32_t (&f)[4], const __nv_bfloat16* t, int ld, int k0,
+                                          int n0, int lane) {
+  ldsm_x4(f, t + (n0 + (lane & 7) + (lane >> 4) * 8) * ld + k0 + ((lane >> 3) & 1) * 8);
+}
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+// the value of a split pair of tiles at (row, col .. col + 1)
+__device__ __forceinline__ float2 split_at(const __nv_bfloat16* hi, const __nv_bfloat16* lo, int off) {
+  const uint32_t h = *reinterpret_cast<const uint32_t*>(hi + off);
+  const uint32_t l = *reinterpret_cast<const uint32_t*>(lo + off);
+  return make_float2(bf_lo(h) + bf_lo(l), bf_hi(h) + bf_hi(l));
 }
 
-// Shared memory of the chunk kernel (floats; rows padded to odd lengths).
+// Shared memory of the chunk kernel: bf16 tiles, then fp32 arrays.
 template <int N> struct ChunkBwdSmem {
-  static constexpr int LP = kP + 1, LN = N + 1, LQ = kQ + 1;
-  static constexpr int oX = 0;                 // x      [τ][p]
-  static constexpr int oG = oX + kQ * LP;      // ḡ      [t][p]
-  static constexpr int oC = oG + kQ * LP;      // C      [t][n]
-  static constexpr int oB = oC + kQ * LN;      // B      [τ][n]
-  static constexpr int oH = oB + kQ * LN;      // H_{c-1} [p][n]
-  static constexpr int oD = oH + kP * LN;      // dH_c   [p][n]
-  static constexpr int oE = oD + kP * LN;      // (C_t·B_τ) exp(s_t - s_τ), τ <= t   [t][τ]
-  static constexpr int oL = oE + kQ * LQ;      // dML    [t][τ]
-  static constexpr int oS = oL + kQ * LQ;      // s, β, exp(s), exp(s_end - s)
-  static constexpr int oR = oS + 4 * kQ;       // per-warp column sums [2][warps][Q]
-  static constexpr int oV = oR + 2 * kChunkWarps * kQ;   // ds parts, dβ, r, row and column sums [6][Q]; scalars
-  static constexpr int kFloats = oV + 6 * kQ + 8;
-  static constexpr size_t kBytes = (size_t)kFloats * 4;
+  static constexpr int L64 = kQ + 8, LN = N + 8;  // bf16 row strides
+  static constexpr int oX = 0;                    // x [τ][p]
+  static constexpr int oGh = oX + kQ * L64;       // ḡ [t][p], rounded
+  static constexpr int oGl = oGh + kQ * L64;      //   remainder
+  static constexpr int oEh = oGl + kQ * L64;      // E β [t][τ] (0 above the diagonal)
+  static constexpr int oEl = oEh + kQ * L64;
+  static constexpr int oLh = oEl + kQ * L64;      // dML [t][τ]
+  static constexpr int oLl = oLh + kQ * L64;
+  static constexpr int oC = oLl + kQ * L64;       // C [t][n]
+  static constexpr int oB = oC + kQ * LN;         // B [τ][n]
+  static constexpr int oHh = oB + kQ * LN;        // H_{c-1} [p][n]
+  static constexpr int oHl = oHh + kP * LN;
+  static constexpr int oDh = oHl + kP * LN;       // dH_c [p][n]
+  static constexpr int oDl = oDh + kP * LN;
+  static constexpr int kTileElems = oDl + kP * LN;
+  // fp32 arrays (float offsets after the tiles)
+  static constexpr int fS = 0;                    // s, β, exp(s), exp(s_end - s)
+  static constexpr int fRow = fS + 4 * kQ;        // row partials [K | inter | r][column quarter][Q]
+  static constexpr int fCol = fRow + 3 * 4 * kQ;  // column partials [K | dM E][row block][Q]
+  static constexpr int fV = fCol + 2 * 4 * kQ;    // rowK, colK, inter, dβ, r; scalars [8]
+  static constexpr int kFloats = fV + 5 * kQ + 8;
+  static constexpr size_t kBytes = (size_t)kTileElems * 2 + (size_t)kFloats * 4;
+  static_assert((kQ * L64 * 2) % 16 == 0 && (kQ * LN * 2) % 16 == 0, "16-byte tile rows");
 };
 
 template <int N>
 __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const SsdBwd a) {
   using S = ChunkBwdSmem<N>;
-  constexpr int LP = S::LP, LN = S::LN, LQ = S::LQ;
-  constexpr int RN = N / 32;
-  extern __shared__ float sm[];
-  float* sX = sm + S::oX;
-  float* sG = sm + S::oG;
-  float* sC = sm + S::oC;
-  float* sB = sm + S::oB;
-  float* sH = sm + S::oH;
-  float* sD = sm + S::oD;
-  float* sE = sm + S::oE;
-  float* sL = sm + S::oL;
-  float* sS = sm + S::oS;        // s
-  float* sBeta = sS + kQ;        // β
-  float* sEs = sS + 2 * kQ;      // exp(s_t)
-  float* sEe = sS + 3 * kQ;      // exp(s_end - s_t)
-  float* sR = sm + S::oR;        // [2][warps][Q]
-  float* sV = sm + S::oV;
-  float* vRowK = sV;             // Σ_τ K[t][τ]
-  float* vInter = sV + kQ;       // exp(s_t) ḡ_t·(H C_t)
-  float* vDbeta = sV + 2 * kQ;   // Σ_t dM CB exp   (then + r)
-  float* vR = sV + 3 * kQ;       // r_τ
-  float* vColK = sV + 4 * kQ;    // Σ_t K[t][τ]
-  float* vScal = sV + 6 * kQ;    // <dH, H>, Σ ḡ·x
+  constexpr int L64 = S::L64, LN = S::LN;
+  constexpr int NQ = N / 4;   // columns of an N-wide product a warp owns
+  constexpr int NT = NQ / 8;  // its n8 tiles
+  extern __shared__ float4 chunk_smem[];
+  __nv_bfloat16* const tl = reinterpret_cast<__nv_bfloat16*>(chunk_smem);
+  float* const fs = reinterpret_cast<float*>(tl + S::kTileElems);
+  __nv_bfloat16* const sX = tl + S::oX;
+  __nv_bfloat16* const sGh = tl + S::oGh;
+  __nv_bfloat16* const sGl = tl + S::oGl;
+  __nv_bfloat16* const sEh = tl + S::oEh;
+  __nv_bfloat16* const sEl = tl + S::oEl;
+  __nv_bfloat16* const sLh = tl + S::oLh;
+  __nv_bfloat16* const sLl = tl + S::oLl;
+  __nv_bfloat16* const sC = tl + S::oC;
+  __nv_bfloat16* const sB = tl + S::oB;
+  __nv_bfloat16* const sHh = tl + S::oHh;
+  __nv_bfloat16* const sHl = tl + S::oHl;
+  __nv_bfloat16* const sDh = tl + S::oDh;
+  __nv_bfloat16* const sDl = tl + S::oDl;
+  float* const sS = fs + S::fS;       // s
+  float* const sBeta = sS + kQ;       // β
+  float* const sEs = sS + 2 * kQ;     // exp(s_t)
+  float* const sEe = sS + 3 * kQ;     // exp(s_end - s_t)
+  float* const pRow = fs + S::fRow;   // [3][4][Q]
+  float* const pCol = fs + S::fCol;   // [2][4][Q]
+  float* const vRowK = fs + S::fV;    // Σ_τ K[t][τ]
+  float* const vColK = vRowK + kQ;    // Σ_t K[t][τ]
+  float* const vInter = vRowK + 2 * kQ;  // exp(s_t) ḡ_t·(H C_t)
+  float* const vDbeta = vRowK + 3 * kQ;  // Σ_t dM (C·B) exp   (then + r)
+  float* const vR = vRowK + 4 * kQ;      // r_τ
+  float* const vScal = vRowK + 5 * kQ;   // <dH, H>, Σ ḡ·x
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y;
@@ -330,8 +359,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
   const int valid = (int)min64(kQ, a.L - t0);
   const float ah = a.A[h];
   const float Dh = a.D ? a.D[h] : 0.f;
-  constexpr int RM = kRM, NW = kChunkWarps;
-  const int i0 = RM * warp;  // this warp's rows of every product
+  const int mb = warp & 3, cq = warp >> 2;  // row block, column quarter
+  const int m0 = 16 * mb, q0 = 16 * cq, n0 = NQ * cq;
+  const int r0 = m0 + (lane >> 2), c2 = 2 * (lane & 3);  // accumulator rows r0, r0 + 8
 
   // ---- stage the chunk ----
   const float* tr = a.terms + unit * kSsdTermsRec;
@@ -341,48 +371,36 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
     sEs[e] = expf(tr[e]);
     sEe[e] = expf(tr[kQ - 1] - tr[e]);
   }
-  // Every 16-byte load of an array is issued before any of its stores (loads
-  // through the read-only path, so they may all be in flight at once).
-  auto unpack8 = [](const uint4 q, float (&v)[8]) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      v[2 * k] = __uint_as_float(w[k] << 16);
-      v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-    }
-  };
   float gx = 0.f;  // Σ ḡ·x over this thread's elements (for dD)
   {
-    constexpr int NV = kQ * kP / 8 / kChunkThreads;  // 8-wide vectors of x, dy, z a thread loads
-    uint4 xr[NV], yr[NV], zr[NV];
+    static_assert(kQ * kP / 8 == kChunkThreads, "one 8-wide vector of x, dy, z a thread");
+    const int t = tid / (kP / 8), p8 = tid % (kP / 8);
+    const bool ok = t < valid;
+    const int64_t o = ((b * a.L + t0 + (ok ? t : 0)) * a.H + h) * kP + 8 * p8;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const uint4 xr = ok ? __ldg(reinterpret_cast<const uint4*>(a.x + o)) : zero;
+    const uint4 yr = ok ? __ldg(reinterpret_cast<const uint4*>(a.dy + o)) : zero;
+    const uint4 zr = (ok && a.z) ? __ldg(reinterpret_cast<const uint4*>(a.z + o)) : zero;
+    *reinterpret_cast<uint4*>(sX + t * L64 + 8 * p8) = xr;
+    const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w}, yw[4] = {yr.x, yr.y, yr.z, yr.w},
+                   zw[4] = {zr.x, zr.y, zr.z, zr.w};
+    uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = tid + i * kChunkThreads, t = e / (kP / 8), p8 = e % (kP / 8);
-      const bool ok = t < valid;
-      const int64_t o = ((b * a.L + t0 + (ok ? t : 0)) * a.H + h) * kP + 8 * p8;
-      const uint4 zero = make_uint4(0, 0, 0, 0);
-      xr[i] = ok ? __ldg(reinterpret_cast<const uint4*>(a.x + o)) : zero;
-      yr[i] = ok ? __ldg(reinterpret_cast<const uint4*>(a.dy + o)) : zero;
-      zr[i] = (ok && a.z) ? __ldg(reinterpret_cast<const uint4*>(a.z + o)) : zero;
-    }
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = tid + i * kChunkThreads, t = e / (kP / 8), p8 = e % (kP / 8);
-      float xv[8], gv[8], zv[8];
-      unpack8(xr[i], xv);
-      unpack8(yr[i], gv);
-      unpack8(zr[i], zv);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (a.z) gv[k] *= silu_precise(zv[k]);
-        sX[t * LP + 8 * p8 + k] = xv[k];
-        sG[t * LP + 8 * p8 + k] = gv[k];
-        gx = fmaf(gv[k], xv[k], gx);
+    for (int k = 0; k < 4; ++k) {
+      float g0 = bf_lo(yw[k]), g1 = bf_hi(yw[k]);
+      if (a.z) {
+        g0 *= silu_precise(bf_lo(zw[k]));
+        g1 *= silu_precise(bf_hi(zw[k]));
       }
+      gx = fmaf(g0, bf_lo(xw[k]), gx);
+      gx = fmaf(g1, bf_hi(xw[k]), gx);
+      split_bf16x2(g0, g1, hw[k], lw[k]);
     }
+    *reinterpret_cast<uint4*>(sGh + t * L64 + 8 * p8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(sGl + t * L64 + 8 * p8) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
   {
-    constexpr int NV = kQ * N / 8 / kChunkThreads;  // 8-wide vectors of C and B a thread loads
+    constexpr int NV = kQ * N / 8 / kChunkThreads;  // 8-wide vectors of C and B a thread copies
     uint4 cr[NV], br[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -395,14 +413,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = tid + i * kChunkThreads, t = e / (N / 8), n8 = e % (N / 8);
-      float cv[8], bv[8];
-      unpack8(cr[i], cv);
-      unpack8(br[i], bv);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        sC[t * LN + 8 * n8 + k] = cv[k];
-        sB[t * LN + 8 * n8 + k] = bv[k];
-      }
+      *reinterpret_cast<uint4*>(sC + t * LN + 8 * n8) = cr[i];
+      *reinterpret_cast<uint4*>(sB + t * LN + 8 * n8) = br[i];
     }
   }
   float hd = 0.f;  // <dH, H> over this thread's elements
@@ -419,221 +431,359 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = 4 * (tid + i * kChunkThreads), pp = e / N, n = e % N;
-      const float hv[4] = {hr[i].x, hr[i].y, hr[i].z, hr[i].w};
-      const float dv[4] = {dr[i].x, dr[i].y, dr[i].z, dr[i].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sH[pp * LN + n + k] = hv[k];
-        sD[pp * LN + n + k] = dv[k];
-        hd = fmaf(hv[k], dv[k], hd);
-      }
+      hd = fmaf(hr[i].x, dr[i].x, fmaf(hr[i].y, dr[i].y, fmaf(hr[i].z, dr[i].z, fmaf(hr[i].w, dr[i].w, hd))));
+      uint32_t h0, h1, l0, l1;
+      split_bf16x2(hr[i].x, hr[i].y, h0, l0);
+      split_bf16x2(hr[i].z, hr[i].w, h1, l1);
+      *reinterpret_cast<uint2*>(sHh + pp * LN + n) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(sHl + pp * LN + n) = make_uint2(l0, l1);
+      split_bf16x2(dr[i].x, dr[i].y, h0, l0);
+      split_bf16x2(dr[i].z, dr[i].w, h1, l1);
+      *reinterpret_cast<uint2*>(sDh + pp * LN + n) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(sDl + pp * LN + n) = make_uint2(l0, l1);
     }
   }
-  // block sums of hd and gx: warp shuffles, then warp 0
+  // block sums of hd and gx: warp shuffles, then thread 0 (partials in pCol)
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     hd += __shfl_xor_sync(0xffffffffu, hd, o);
     gx += __shfl_xor_sync(0xffffffffu, gx, o);
   }
   if (lane == 0) {
-    sR[warp] = hd;
-    sR[NW + warp] = gx;
+    pCol[warp] = hd;
+    pCol[kChunkWarps + warp] = gx;
   }
   __syncthreads();
   if (tid == 0) {
     float s1 = 0.f, s2 = 0.f;
-    for (int w = 0; w < NW; ++w) {
-      s1 += sR[w];
-      s2 += sR[NW + w];
+    for (int w = 0; w < kChunkWarps; ++w) {
+      s1 += pCol[w];
+      s2 += pCol[kChunkWarps + w];
     }
     vScal[0] = s1;
     vScal[1] = s2;
   }
   __syncthreads();
 
-  // ---- E = (C_t·B_τ) exp(s_t - s_τ) for τ <= t (else 0) ----
+  // ---- the products of the staged operands ----
+  // E' = C Bᵀ and dM = ḡ xᵀ on rows t = m0.., columns τ = q0..q0+15: then
+  // E = E' exp(s_t - s_τ) (τ <= t), M = E β, K = dM ∘ M, dML = dM exp(s_t - s_τ) β
   {
-    float acc[RM][2];
-    mm_zero(acc);
-    mm_acc<RM, 2>(acc, N, sC, 1, LN, i0, sB, 1, LN, lane);
+    float accE[2][4] = {}, accM[2][4] = {};
 #pragma unroll
-    for (int i = 0; i < RM; ++i)
+    for (int ks = 0; ks < N / 16; ++ks) {
+      uint32_t fa[4], fb[4];
+      frag_a(fa, sC, LN, m0, 16 * ks, lane);
+      frag_b_nk(fb, sB, LN, 16 * ks, q0, lane);
+      mma_bf16(accE[0], fa, fb[0], fb[1]);
+      mma_bf16(accE[1], fa, fb[2], fb[3]);
+    }
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t = i0 + i, tau = lane + 32 * r;
-        sE[t * LQ + tau] = tau <= t ? acc[i][r] * expf(sS[t] - sS[tau]) : 0.f;
+    for (int ks = 0; ks < kP / 16; ++ks) {
+      uint32_t gh[4], gl[4], fb[4];
+      frag_a(gh, sGh, L64, m0, 16 * ks, lane);
+      frag_a(gl, sGl, L64, m0, 16 * ks, lane);
+      frag_b_nk(fb, sX, L64, 16 * ks, q0, lane);
+      mma_bf16(accM[0], gh, fb[0], fb[1]);
+      mma_bf16(accM[0], gl, fb[0], fb[1]);
+      mma_bf16(accM[1], gh, fb[2], fb[3]);
+      mma_bf16(accM[1], gl, fb[2], fb[3]);
+    }
+    float rowK[2] = {0.f, 0.f}, colK[2][2] = {}, colB[2][2] = {};
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int hr2 = 0; hr2 < 2; ++hr2) {
+        const int t = r0 + 8 * hr2;
+        float mv[2], lv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tau = q0 + 8 * j + c2 + e;
+          const bool lower = tau <= t;
+          const float ex = lower ? expf(sS[t] - sS[tau]) : 0.f;
+          const float E = accE[j][2 * hr2 + e] * ex;
+          const float dm = lower ? accM[j][2 * hr2 + e] : 0.f;
+          const float be = sBeta[tau];
+          const float m = E * be;                 // M[t][τ]
+          const float k = dm * m;                 // dM ∘ M
+          rowK[hr2] += k;
+          colK[j][e] += k;
+          colB[j][e] = fmaf(dm, E, colB[j][e]);  // dM (C·B) exp
+          mv[e] = m;
+          lv[e] = dm * ex * be;                   // dML
+        }
+        const int off = t * L64 + q0 + 8 * j + c2;
+        uint32_t hi, lo;
+        split_bf16x2(mv[0], mv[1], hi, lo);
+        *reinterpret_cast<uint32_t*>(sEh + off) = hi;
+        *reinterpret_cast<uint32_t*>(sEl + off) = lo;
+        split_bf16x2(lv[0], lv[1], hi, lo);
+        *reinterpret_cast<uint32_t*>(sLh + off) = hi;
+        *reinterpret_cast<uint32_t*>(sLl + off) = lo;
       }
-  }
-  __syncthreads();
-
-  // ---- y before the gate (for dz) and the inter-chunk ds term ----
-  {
-    float acc[RM][2];
-    mm_zero(acc);
-    mm_acc<RM, 2>(acc, N, sC, 1, LN, i0, sH, 1, LN, lane);  // (C Hᵀ)[t][p]
-    float inter[RM];
+    // row sums over the warp's 16 columns (a quad holds a row), column sums over
+    // its 16 rows (lanes 4 apart hold a column)
 #pragma unroll
-    for (int i = 0; i < RM; ++i) {
-      const int t = i0 + i;
-      float part = 0.f;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        acc[i][r] *= sEs[t];
-        part = fmaf(sG[t * LP + lane + 32 * r], acc[i][r], part);
-      }
-      inter[i] = part;
+    for (int hr2 = 0; hr2 < 2; ++hr2) {
+      float v = rowK[hr2];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if ((lane & 3) == 0) pRow[(0 * 4 + cq) * kQ + r0 + 8 * hr2] = v;
     }
 #pragma unroll
-    for (int i = 0; i < RM; ++i) {
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) inter[i] += __shfl_xor_sync(0xffffffffu, inter[i], o);
-      if (lane == i) vInter[i0 + i] = inter[i];
-    }
-    // + Σ_τ E[t][τ] β_τ x_τ[p] + D x_t[p]
-    float accm[RM][2];
-    mm_zero(accm);
-#pragma unroll 4
-    for (int k = 0; k < kQ; ++k) {
-      float av[RM], bv[2];
-      const float bk = sBeta[k];
+      for (int e = 0; e < 2; ++e) {
+        float u = colK[j][e], v = colB[j][e];
 #pragma unroll
-      for (int i = 0; i < RM; ++i) av[i] = sE[(i0 + i) * LQ + k];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) bv[r] = bk * sX[k * LP + lane + 32 * r];
-#pragma unroll
-      for (int i = 0; i < RM; ++i)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) accm[i][r] = fmaf(av[i], bv[r], accm[i][r]);
-    }
-    if (a.dz) {
-#pragma unroll
-      for (int i = 0; i < RM; ++i) {
-        const int t = i0 + i;
-        if (t >= valid) continue;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int pp = lane + 32 * r;
-          const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + pp;
-          const float y = acc[i][r] + accm[i][r] + Dh * sX[t * LP + pp];
-          const float zv = bf(a.z[o]);
-          const float sg = sigmoid_precise(zv);
-          a.dz[o] = __float2bfloat16_rn(bf(a.dy[o]) * y * sg * fmaf(zv, 1.f - sg, 1.f));
+        for (int o = 4; o < 32; o <<= 1) {
+          u += __shfl_xor_sync(0xffffffffu, u, o);
+          v += __shfl_xor_sync(0xffffffffu, v, o);
+        }
+        if (lane < 4) {
+          const int tau = q0 + 8 * j + c2 + e;
+          pCol[(0 * 4 + mb) * kQ + tau] = u;
+          pCol[(1 * 4 + mb) * kQ + tau] = v;
         }
       }
-    }
   }
-
-  // ---- dM = ḡ xᵀ: dML, K = dM ∘ M, the dβ sums ----
+  // exp(s) C Hᵀ on rows t, columns p = q0..: kept for y; the inter-chunk ds term
+  float chv[2][4] = {};
   {
-    float acc[RM][2];
-    mm_zero(acc);
-    mm_acc<RM, 2>(acc, kP, sG, 1, LP, i0, sX, 1, LP, lane);  // dM[t][τ]
-    float rowK[RM], colK[2] = {0.f, 0.f}, colB[2] = {0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < RM; ++i) {
-      const int t = i0 + i;
-      float rk = 0.f;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int tau = lane + 32 * r;
-        const float e = sE[t * LQ + tau];        // 0 above the diagonal
-        const float dm = tau <= t ? acc[i][r] : 0.f;
-        const float k = dm * e * sBeta[tau];     // dM ∘ M
-        rk += k;
-        colK[r] += k;
-        colB[r] = fmaf(dm, e, colB[r]);          // dM (C·B) exp
-        sL[t * LQ + tau] = tau <= t ? dm * expf(sS[t] - sS[tau]) * sBeta[tau] : 0.f;
-      }
-      rowK[i] = rk;
+    for (int ks = 0; ks < N / 16; ++ks) {
+      uint32_t fa[4], hh[4], hl[4];
+      frag_a(fa, sC, LN, m0, 16 * ks, lane);
+      frag_b_nk(hh, sHh, LN, 16 * ks, q0, lane);
+      frag_b_nk(hl, sHl, LN, 16 * ks, q0, lane);
+      mma_bf16(chv[0], fa, hh[0], hh[1]);
+      mma_bf16(chv[0], fa, hl[0], hl[1]);
+      mma_bf16(chv[1], fa, hh[2], hh[3]);
+      mma_bf16(chv[1], fa, hl[2], hl[3]);
     }
 #pragma unroll
-    for (int i = 0; i < RM; ++i) {
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) rowK[i] += __shfl_xor_sync(0xffffffffu, rowK[i], o);
-      if (lane == i) vRowK[i0 + i] = rowK[i];
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      sR[warp * kQ + lane + 32 * r] = colK[r];
-      sR[NW * kQ + warp * kQ + lane + 32 * r] = colB[r];
-    }
-  }
-  __syncthreads();
-  if (tid < kQ) {  // column sums over the warps, in order
-    float ck = 0.f, cb = 0.f;
-    for (int w = 0; w < NW; ++w) {
-      ck += sR[w * kQ + tid];
-      cb += sR[NW * kQ + w * kQ + tid];
-    }
-    vColK[tid] = ck;
-    vDbeta[tid] = cb;
-  }
-  __syncthreads();
-
-  // ---- dx = D ḡ + Mᵀ ḡ + β exp(s_end - s) dH B; r_τ = exp(s_end - s_τ) x_τ·(dH B_τ) ----
-  {
-    float acc[RM][2], accd[RM][2];
-    mm_zero(acc);
-    mm_zero(accd);
-    mm_acc<RM, 2>(acc, kQ, sE, LQ, 1, i0, sG, LP, 1, lane);   // Σ_t E[t][τ] ḡ_t[p]
-    mm_acc<RM, 2>(accd, N, sB, 1, LN, i0, sD, 1, LN, lane);  // (B dHᵀ)[τ][p]
-    float rr[RM];
-#pragma unroll
-    for (int i = 0; i < RM; ++i) {
-      const int tau = i0 + i;
+    for (int hr2 = 0; hr2 < 2; ++hr2) {
+      const int t = r0 + 8 * hr2;
+      const float es = sEs[t];
       float part = 0.f;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) part = fmaf(sX[tau * LP + lane + 32 * r], accd[i][r], part);
-      rr[i] = part;
+      for (int j = 0; j < 2; ++j) {
+        chv[j][2 * hr2] *= es;
+        chv[j][2 * hr2 + 1] *= es;
+        const float2 gv = split_at(sGh, sGl, t * L64 + q0 + 8 * j + c2);
+        part = fmaf(gv.x, chv[j][2 * hr2], fmaf(gv.y, chv[j][2 * hr2 + 1], part));
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if ((lane & 3) == 0) pRow[(1 * 4 + cq) * kQ + t] = part;
+    }
+  }
+  // B dHᵀ on rows τ, columns p = q0..: kept for dx; r_τ = exp(s_end - s_τ) x_τ·(dH B_τ)
+  float bdh[2][4] = {};
+  {
+#pragma unroll
+    for (int ks = 0; ks < N / 16; ++ks) {
+      uint32_t fa[4], dh[4], dl[4];
+      frag_a(fa, sB, LN, m0, 16 * ks, lane);
+      frag_b_nk(dh, sDh, LN, 16 * ks, q0, lane);
+      frag_b_nk(dl, sDl, LN, 16 * ks, q0, lane);
+      mma_bf16(bdh[0], fa, dh[0], dh[1]);
+      mma_bf16(bdh[0], fa, dl[0], dl[1]);
+      mma_bf16(bdh[1], fa, dh[2], dh[3]);
+      mma_bf16(bdh[1], fa, dl[2], dl[3]);
     }
 #pragma unroll
-    for (int i = 0; i < RM; ++i) {
+    for (int hr2 = 0; hr2 < 2; ++hr2) {
+      const int tau = r0 + 8 * hr2;
+      float part = 0.f;
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) rr[i] += __shfl_xor_sync(0xffffffffu, rr[i], o);
-      if (lane == i) vR[i0 + i] = rr[i] * sEe[i0 + i];
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t xv = *reinterpret_cast<const uint32_t*>(sX + tau * L64 + q0 + 8 * j + c2);
+        part = fmaf(bf_lo(xv), bdh[j][2 * hr2], fmaf(bf_hi(xv), bdh[j][2 * hr2 + 1], part));
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if ((lane & 3) == 0) pRow[(2 * 4 + cq) * kQ + tau] = part;
+    }
+  }
+  __syncthreads();  // E β, dML tiles and the partial sums complete
+  if (tid < kQ) {   // the partial sums, in a fixed order
+    const int i = tid;
+    auto rsum = [&](int k) {
+      return ((pRow[(k * 4 + 0) * kQ + i] + pRow[(k * 4 + 1) * kQ + i]) + pRow[(k * 4 + 2) * kQ + i]) +
+             pRow[(k * 4 + 3) * kQ + i];
+    };
+    auto csum = [&](int k) {
+      return ((pCol[(k * 4 + 0) * kQ + i] + pCol[(k * 4 + 1) * kQ + i]) + pCol[(k * 4 + 2) * kQ + i]) +
+             pCol[(k * 4 + 3) * kQ + i];
+    };
+    vRowK[i] = rsum(0);
+    vInter[i] = rsum(1);
+    vR[i] = rsum(2) * sEe[i];
+    vColK[i] = csum(0);
+    vDbeta[i] = csum(1);
+  }
+
+  // ---- y (for dz) = exp(s) C Hᵀ + (E β) x + D x on rows t, columns p ----
+  if (a.dz) {
+    float acc[2][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < kQ / 16; ++ks) {
+      uint32_t eh[4], el[4], fb[4];
+      frag_a(eh, sEh, L64, m0, 16 * ks, lane);
+      frag_a(el, sEl, L64, m0, 16 * ks, lane);
+      frag_b_kn(fb, sX, L64, 16 * ks, q0, lane);
+      mma_bf16(acc[0], eh, fb[0], fb[1]);
+      mma_bf16(acc[0], el, fb[0], fb[1]);
+      mma_bf16(acc[1], eh, fb[2], fb[3]);
+      mma_bf16(acc[1], el, fb[2], fb[3]);
     }
 #pragma unroll
-    for (int i = 0; i < RM; ++i) {
-      const int tau = i0 + i;
-      if (tau >= valid) continue;
-      const float be = sBeta[tau], bee = be * sEe[tau];
+    for (int hr2 = 0; hr2 < 2; ++hr2) {
+      const int t = r0 + 8 * hr2;
+      if (t >= valid) continue;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int pp = lane + 32 * r;
-        const float v = fmaf(Dh, sG[tau * LP + pp], fmaf(be, acc[i][r], bee * accd[i][r]));
-        a.dx[((b * a.L + t0 + tau) * a.H + h) * kP + pp] = __float2bfloat16_rn(v);
+      for (int j = 0; j < 2; ++j) {
+        const int pp = q0 + 8 * j + c2;
+        const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + pp;
+        const uint32_t xv = *reinterpret_cast<const uint32_t*>(sX + t * L64 + pp);
+        const uint32_t zv = *reinterpret_cast<const uint32_t*>(a.z + o);
+        const uint32_t dv = *reinterpret_cast<const uint32_t*>(a.dy + o);
+        float r[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float x = e ? bf_hi(xv) : bf_lo(xv), z = e ? bf_hi(zv) : bf_lo(zv);
+          const float d = e ? bf_hi(dv) : bf_lo(dv);
+          const float y = chv[j][2 * hr2 + e] + acc[j][2 * hr2 + e] + Dh * x;
+          const float sg = sigmoid_precise(z);
+          r[e] = d * y * sg * fmaf(z, 1.f - sg, 1.f);
+        }
+        *reinterpret_cast<__nv_bfloat162*>(a.dz + o) = __floats2bfloat162_rn(r[0], r[1]);
       }
     }
   }
-
-  // ---- dC = exp(s) ḡ H + dML B;  dB = dMLᵀ C + β exp(s_end - s) x dH ----
+  // ---- dx = D ḡ + (E β)ᵀ ḡ + β exp(s_end - s) B dHᵀ on rows τ, columns p ----
   {
-    float acc[RM][RN];
-    mm_zero(acc);
-    mm_acc<RM, RN>(acc, kP, sG, 1, LP, i0, sH, LN, 1, lane);  // (ḡ H)[t][n]
+    float acc[2][4] = {};
 #pragma unroll
-    for (int i = 0; i < RM; ++i)
+    for (int ks = 0; ks < kQ / 16; ++ks) {
+      uint32_t eh[4], el[4], gh[4], gl[4];
+      frag_at(eh, sEh, L64, m0, 16 * ks, lane);
+      frag_at(el, sEl, L64, m0, 16 * ks, lane);
+      frag_b_kn(gh, sGh, L64, 16 * ks, q0, lane);
+      frag_b_kn(gl, sGl, L64, 16 * ks, q0, lane);
+      mma_bf16(acc[0], eh, gh[0], gh[1]);
+      mma_bf16(acc[0], eh, gl[0], gl[1]);
+      mma_bf16(acc[0], el, gh[0], gh[1]);
+      mma_bf16(acc[1], eh, gh[2], gh[3]);
+      mma_bf16(acc[1], eh, gl[2], gl[3]);
+      mma_bf16(acc[1], el, gh[2], gh[3]);
+    }
 #pragma unroll
-      for (int r = 0; r < RN; ++r) acc[i][r] *= sEs[i0 + i];
-    mm_acc<RM, RN>(acc, kQ, sL, 1, LQ, i0, sB, LN, 1, lane);  // + (dML B)[t][n]
+    for (int hr2 = 0; hr2 < 2; ++hr2) {
+      const int tau = r0 + 8 * hr2;
+      if (tau >= valid) continue;
+      const float bee = sBeta[tau] * sEe[tau];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int pp = q0 + 8 * j + c2;
+        const float2 gv = split_at(sGh, sGl, tau * L64 + pp);
+        const float v0 = fmaf(Dh, gv.x, fmaf(bee, bdh[j][2 * hr2], acc[j][2 * hr2]));
+        const float v1 = fmaf(Dh, gv.y, fmaf(bee, bdh[j][2 * hr2 + 1], acc[j][2 * hr2 + 1]));
+        *reinterpret_cast<__nv_bfloat162*>(a.dx + ((b * a.L + t0 + tau) * a.H + h) * kP + pp) =
+            __floats2bfloat162_rn(v0, v1);
+      }
+    }
+  }
+  // ---- dC = exp(s) ḡ H + dML B on rows t, columns n = n0.. ----
+  {
+    float acc[NT][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < kP / 16; ++ks) {
+      uint32_t gh[4], gl[4];
+      frag_a(gh, sGh, L64, m0, 16 * ks, lane);
+      frag_a(gl, sGl, L64, m0, 16 * ks, lane);
+#pragma unroll
+      for (int nn = 0; nn < NT / 2; ++nn) {
+        uint32_t hh[4], hl[4];
+        frag_b_kn(hh, sHh, LN, 16 * ks, n0 + 16 * nn, lane);
+        frag_b_kn(hl, sHl, LN, 16 * ks, n0 + 16 * nn, lane);
+        mma_bf16(acc[2 * nn], gh, hh[0], hh[1]);
+        mma_bf16(acc[2 * nn], gh, hl[0], hl[1]);
+        mma_bf16(acc[2 * nn], gl, hh[0], hh[1]);
+        mma_bf16(acc[2 * nn + 1], gh, hh[2], hh[3]);
+        mma_bf16(acc[2 * nn + 1], gh, hl[2], hl[3]);
+        mma_bf16(acc[2 * nn + 1], gl, hh[2], hh[3]);
+      }
+    }
+    const float e0 = sEs[r0], e1 = sEs[r0 + 8];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      acc[j][0] *= e0; acc[j][1] *= e0; acc[j][2] *= e1; acc[j][3] *= e1;
+    }
+#pragma unroll
+    for (int ks = 0; ks < kQ / 16; ++ks) {
+      uint32_t lh[4], ll[4];
+      frag_a(lh, sLh, L64, m0, 16 * ks, lane);
+      frag_a(ll, sLl, L64, m0, 16 * ks, lane);
+#pragma unroll
+      for (int nn = 0; nn < NT / 2; ++nn) {
+        uint32_t fb[4];
+        frag_b_kn(fb, sB, LN, 16 * ks, n0 + 16 * nn, lane);
+        mma_bf16(acc[2 * nn], lh, fb[0], fb[1]);
+        mma_bf16(acc[2 * nn], ll, fb[0], fb[1]);
+        mma_bf16(acc[2 * nn + 1], lh, fb[2], fb[3]);
+        mma_bf16(acc[2 * nn + 1], ll, fb[2], fb[3]);
+      }
+    }
     float* out = a.dCp + unit * kQ * N;
 #pragma unroll
-    for (int i = 0; i < RM; ++i)
-#pragma unroll
-      for (int r = 0; r < RN; ++r) out[(i0 + i) * N + lane + 32 * r] = acc[i][r];
+    for (int j = 0; j < NT; ++j) {
+      *reinterpret_cast<float2*>(out + r0 * N + n0 + 8 * j + c2) = make_float2(acc[j][0], acc[j][1]);
+      *reinterpret_cast<float2*>(out + (r0 + 8) * N + n0 + 8 * j + c2) = make_float2(acc[j][2], acc[j][3]);
+    }
   }
+  // ---- dB = dMLᵀ C + β exp(s_end - s) x dH on rows τ, columns n = n0.. ----
   {
-    float acc[RM][RN], accx[RM][RN];
-    mm_zero(acc);
-    mm_zero(accx);
-    mm_acc<RM, RN>(acc, kQ, sL, LQ, 1, i0, sC, LN, 1, lane);  // (dMLᵀ C)[τ][n]
-    mm_acc<RM, RN>(accx, kP, sX, 1, LP, i0, sD, LN, 1, lane);  // (x dH)[τ][n]
+    float acc[NT][4] = {}, accx[NT][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < kQ / 16; ++ks) {
+      uint32_t lh[4], ll[4];
+      frag_at(lh, sLh, L64, m0, 16 * ks, lane);
+      frag_at(ll, sLl, L64, m0, 16 * ks, lane);
+#pragma unroll
+      for (int nn = 0; nn < NT / 2; ++nn) {
+        uint32_t fb[4];
+        frag_b_kn(fb, sC, LN, 16 * ks, n0 + 16 * nn, lane);
+        mma_bf16(acc[2 * nn], lh, fb[0], fb[1]);
+        mma_bf16(acc[2 * nn], ll, fb[0], fb[1]);
+        mma_bf16(acc[2 * nn + 1], lh, fb[2], fb[3]);
+        mma_bf16(acc[2 * nn + 1], ll, fb[2], fb[3]);
+      }
+    }
+#pragma unroll
+    for (int ks = 0; ks < kP / 16; ++ks) {
+      uint32_t fa[4];
+      frag_a(fa, sX, L64, m0, 16 * ks, lane);
+#pragma unroll
+      for (int nn = 0; nn < NT / 2; ++nn) {
+        uint32_t dh[4], dl[4];
+        frag_b_kn(dh, sDh, LN, 16 * ks, n0 + 16 * nn, lane);
+        frag_b_kn(dl, sDl, LN, 16 * ks, n0 + 16 * nn, lane);
+        mma_bf16(accx[2 * nn], fa, dh[0], dh[1]);
+        mma_bf16(accx[2 * nn], fa, dl[0], dl[1]);
+        mma_bf16(accx[2 * nn + 1], fa, dh[2], dh[3]);
+        mma_bf16(accx[2 * nn + 1], fa, dl[2], dl[3]);
+      }
+    }
+    const float w0 = sBeta[r0] * sEe[r0], w1 = sBeta[r0 + 8] * sEe[r0 + 8];
     float* out = a.dBp + unit * kQ * N;
 #pragma unroll
-    for (int i = 0; i < RM; ++i) {
-      const float w = sBeta[i0 + i] * sEe[i0 + i];
-#pragma unroll
-      for (int r = 0; r < RN; ++r) out[(i0 + i) * N + lane + 32 * r] = fmaf(w, accx[i][r], acc[i][r]);
+    for (int j = 0; j < NT; ++j) {
+      *reinterpret_cast<float2*>(out + r0 * N + n0 + 8 * j + c2) =
+          make_float2(fmaf(w0, accx[j][0], acc[j][0]), fmaf(w0, accx[j][1], acc[j][1]));
+      *reinterpret_cast<float2*>(out + (r0 + 8) * N + n0 + 8 * j + c2) =
+          make_float2(fmaf(w1, accx[j][2], acc[j][2]), fmaf(w1, accx[j][3], acc[j][3]));
     }
   }
   __syncthreads();
