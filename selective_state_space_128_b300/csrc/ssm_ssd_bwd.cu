@@ -854,37 +854,54 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
 }
 
 // ---------------------------------------------------------------------------
-// 4. Sums in a fixed order: dB, dC over the group's heads; dA, d dt_bias, dD
-//    over batch rows and chunks.
+// 4. Sums in a fixed order: dB, dC over the group's heads (4 states a thread,
+//    heads in order); dA, d dt_bias, dD over batch rows and chunks (a warp a
+//    head: lane l adds items l, l + 32, ... in order, then a fixed shuffle tree).
 // ---------------------------------------------------------------------------
 __global__ void ssd_bwd_reduce_kernel(const SsdBwd a, int N) {
   const int64_t hpg = a.H / a.G;
-  const int64_t nbc = a.batch * a.L * a.G * N;  // (b, t, g, n)
-  const int64_t total = 2 * nbc + a.H;
+  const int64_t nbc4 = a.batch * a.L * a.G * N / 4;  // 4-state groups of (b, t, g, n)
+  const int64_t hbase = (2 * nbc4 + 31) / 32 * 32;    // the heads' warps start here
+  const int64_t total = hbase + 32 * a.H;
+  const int64_t nbc = a.batch * a.nch;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    if (i < 2 * nbc) {
-      const bool isC = i >= nbc;
-      const int64_t e = isC ? i - nbc : i;
+    if (i < 2 * nbc4) {
+      const bool isC = i >= nbc4;
+      const int64_t e = (isC ? i - nbc4 : i) * 4;
       const int64_t n = e % N, bt = e / N / a.G, gg = (e / N) % a.G;
       const int64_t t = bt % a.L, b = bt / a.L, c = t / kQ;
-      const float* part = (isC ? a.dCp : a.dBp) +
-                          (((b * a.nch + c) * a.H + gg * hpg) * kQ + (t - c * kQ)) * N + n;
-      float s = 0.f;
-      for (int64_t k = 0; k < hpg; ++k) s += part[k * kQ * N];
-      (isC ? a.dC : a.dB)[e] = s;
-    } else {
-      const int64_t h = i - 2 * nbc;
+      const float4* part = reinterpret_cast<const float4*>(
+          (isC ? a.dCp : a.dBp) + (((b * a.nch + c) * a.H + gg * hpg) * kQ + (t - c * kQ)) * N + n);
+      const int64_t hs = (int64_t)kQ * N / 4;
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int64_t k = 0; k < hpg; ++k) {
+        const float4 v = __ldg(part + k * hs);
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+      }
+      *reinterpret_cast<float4*>((isC ? a.dC : a.dB) + e) = s;
+    } else if (i >= hbase) {  // whole warps
+      const int64_t h = (i - hbase) / 32;
+      const int l = (int)((i - hbase) % 32);
       float da = 0.f, db = 0.f, dd = 0.f;
-      for (int64_t bc = 0; bc < a.batch * a.nch; ++bc) {
+      for (int64_t bc = l; bc < nbc; bc += 32) {
         const float* hp = a.hpart + (bc * a.H + h) * 4;
         da += hp[0];
         db += hp[1];
         dd += hp[2];
       }
-      a.dA[h] = da;
-      if (a.ddt_bias) a.ddt_bias[h] = db;
-      if (a.dD) a.dD[h] = dd;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        da += __shfl_xor_sync(0xffffffffu, da, o);
+        db += __shfl_xor_sync(0xffffffffu, db, o);
+        dd += __shfl_xor_sync(0xffffffffu, dd, o);
+      }
+      if (l == 0) {
+        a.dA[h] = da;
+        if (a.ddt_bias) a.ddt_bias[h] = db;
+        if (a.dD) a.dD[h] = dd;
+      }
     }
   }
 }
@@ -917,7 +934,7 @@ cudaError_t ssd_bwd_typed(const SsdBwd& a, cudaStream_t st) {
   ssd_bwd_chunk_kernel<N><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)a.batch), kChunkThreads,
                             bytes, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t total = 2 * a.batch * a.L * a.G * N + a.H;
+  const int64_t total = (2 * a.batch * a.L * a.G * N / 4 + 31) / 32 * 32 + 32 * a.H;
   const int64_t blocks = (total + 255) / 256;
   ssd_bwd_reduce_kernel<<<(unsigned)(blocks < 148 * 16 ? blocks : 148 * 16), 256, 0, st>>>(a, N);
   return cudaGetLastError();
