@@ -24,16 +24,18 @@
 //    so the warp-wide load of a B or C row touches two 16-byte addresses (two
 //    shared-memory wavefronts; four when one warp holds all four groups of 8
 //    channels).  A state update is one MUFU ex2 and packed f32x2 arithmetic:
-//    Ā = 2^(Δ·A·log2 e), v = -B u / A, h = Ā (h - v) + v (= Ā h + B̄ u); each
-//    thread writes its partial readout Σ_{its n} C_n h_n to a partial tile.
-//  * The per-channel-step work that is not per state runs once per channel
-//    step, split over the channel's 4 threads (T / 4 steps each): the
+//    Ā = 2^(Δ·A·log2 e), v = -B u / A, h = Ā (h - v) + v (= Ā h + B̄ u); the
+//    partial readouts Σ_{its n} C_n h_n of a warp's two groups of a channel are
+//    added by a shuffle and written to a partial tile.
+//  * Chunks of T = 32 steps for the outputs (16 for the split plan's first
+//    pass).  The per-channel-step work that is not per state runs once per
+//    channel step, split over the channel's 4 threads (T / 4 steps each): the
 //    conversion (Δ = softplus(.) once, u, the gate silu(z) and D u) and the
-//    finalisation (y = (Σ partials + D u) · gate, rounded, one 8-byte store per
-//    thread and chunk).
+//    finalisation (y = (Σ partials + D u) · gate, rounded, one 16-byte store
+//    per thread and chunk).
 //  * B and C are transposed to [t][n] once per chunk (warp 0: B, warp 1: C; 2
-//    loads and 8 stores per lane, bank-conflict free), so a thread's 4 values of
-//    a step are one 16-byte load.
+//    loads and 8 stores per lane and 16 steps, bank-conflict free), so a
+//    thread's 4 values of a step are one 16-byte load.
 //  * Two block barriers per chunk: after the conversion and transposition,
 //    after the recurrence.
 //
@@ -59,7 +61,7 @@ namespace ssm {
 namespace {
 
 constexpr int kN = 16;    // states
-constexpr int kT = 16;    // steps per chunk
+constexpr int kCk = 16;   // steps between the chunk-start states a training forward saves
 constexpr int kNSU = 2;   // stages of the u / Δ / z ring (B, C: one stage)
 
 __host__ __device__ constexpr size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -86,8 +88,10 @@ constexpr int kG = 4;             // state groups (threads per channel)
 constexpr int kNPT = kN / kG;     // states per thread
 constexpr int kCB = 16;           // channels per block
 constexpr int kThreads = 64;
-constexpr int kTE = kT / kG;      // steps of a chunk each thread converts and finalises
-static_assert(kTE == 4, "a thread's steps are one 16-byte unit of the partial tile");
+// Chunks: T = 32 steps for the output pass (fewer barriers, waits and pipeline
+// fills per step), T = 16 for the split plan's first pass (which has no readout
+// and whose 32-step form spills); a thread converts and finalises T / 4 steps.
+constexpr int kTOut = 32, kTCarry = 16;
 
 // One thread's view of the launch (the recurrence's mapping).
 struct FastLane {
@@ -121,29 +125,32 @@ __device__ __forceinline__ void write_lane_states(const ScanArgs& p, const FastL
 }
 
 // Shared memory of one block (bytes; TMA destinations 128-byte aligned).
-struct PairSmem {
-  static constexpr size_t kRawIO = (size_t)kCB * kT * 2;     // one of u / Δ / z (bf16)
+template <int T> struct PairSmem {
+  static constexpr size_t kRawIO = (size_t)kCB * T * 2;      // one of u / Δ / z (bf16)
   static constexpr size_t kStageU = up(3 * kRawIO, 128);      // u | Δ | z
   static constexpr size_t oStageU = 0;
-  static constexpr size_t kRawBC = (size_t)kN * kT * 4;       // one of B / C (fp32, [n][t])
+  static constexpr size_t kRawBC = (size_t)kN * T * 4;        // one of B / C (fp32, [n][t])
   static constexpr size_t oStageBC = kNSU * kStageU;          // B | C
   static constexpr int RowBT = kN + 4;
-  static constexpr size_t kBT = (size_t)kT * RowBT * 4;       // B^T or C^T [t][n]
+  static constexpr size_t kBT = (size_t)T * RowBT * 4;        // B^T or C^T [t][n]
   static constexpr size_t oBT = oStageBC + 2 * kRawBC;
   static constexpr size_t oW = oBT + 2 * kBT;                 // (Δ, u) pairs [t][c]
-  static constexpr size_t kW = (size_t)kT * kCB * 8;
-  static constexpr size_t oP = oW + kW;                       // partials [g][c][t], swizzled
-  static constexpr size_t kP = (size_t)kG * kCB * kT * 4;
+  static constexpr size_t kW = (size_t)T * kCB * 8;
+  static constexpr size_t oP = oW + kW;                       // partials [warp][c][t], swizzled
+  static constexpr size_t kP = (size_t)2 * kCB * T * 4;       // a warp's two groups pre-added
   static constexpr size_t oBar = up(oP + kP, 8);              // kNSU + 1 mbarriers
   static constexpr size_t kBytes = oBar + 8 * (kNSU + 1);
   static constexpr size_t kLaunch = kBytes + 128;             // room to align the base
 };
 
-// Index (in floats) of steps 4u..4u+3 of partial row (g, c) (64 bytes a row).  The
-// 16-byte unit is XOR-swizzled by (c >> 1) & 3: the 8 threads of a quarter warp
-// (one group, 8 consecutive channels) touch 8 distinct bank groups.
-__device__ __forceinline__ int pair_pidx(int g, int c, int unit) {
-  return (g * kCB + c) * kT + ((unit ^ ((c >> 1) & 3)) << 2);
+// Index (in floats) of steps 4u..4u+3 of partial row (w, c) (4T bytes a row).  The
+// 16-byte unit is XOR-swizzled by the channel so that the 8 threads of a quarter
+// warp (one warp's groups, 8 consecutive channels) touch 8 distinct bank groups:
+// by (c >> 1) & 3 for rows of 4 units (their bank group also depends on c & 1),
+// by c & 7 for rows of 8.
+template <int T> __device__ __forceinline__ int pair_pidx(int w, int c, int unit) {
+  const int sw = T == 16 ? ((c >> 1) & 3) : (c & 7);
+  return (w * kCB + c) * T + ((unit ^ sw) << 2);
 }
 
 // Precise per-thread loop for blocks with some A = 0 (rare; plain loads through
@@ -171,8 +178,8 @@ __device__ __noinline__ void precise_pair(const ScanArgs& p, const FastLane& L, 
   const float Dd = p.D ? p.D[dd] : 0.f;
   float sumDt = 0.f;
   for (int64_t t = t_begin; t < t_end; ++t) {
-    if (PASS == 0 && p.ckpt != nullptr && ((t - t_begin) % kT) == 0 && L.chan_ok) {
-      float* cp = p.ckpt + ((L.b * p.ckpt_nch + t / kT) * p.dim + L.d) * kN + L.g * NPT;
+    if (PASS == 0 && p.ckpt != nullptr && ((t - t_begin) % kCk) == 0 && L.chan_ok) {
+      float* cp = p.ckpt + ((L.b * p.ckpt_nch + t / kCk) * p.dim + L.d) * kN + L.g * NPT;
 #pragma unroll
       for (int j = 0; j < NPT; ++j) cp[j] = h[j];
     }
@@ -206,11 +213,12 @@ __device__ __noinline__ void precise_pair(const ScanArgs& p, const FastLane& L, 
     p.carry_s[(int64_t)blockIdx.z * p.batch * p.dim + L.b * p.dim + L.d] = sumDt;
 }
 
-template <int PASS>
+template <int PASS, int T>
 __global__ void __launch_bounds__(kThreads, 9)
     scan_pair_kernel(const ScanArgs p, const __grid_constant__ FastMaps maps) {
-  using S = PairSmem;
-  constexpr int G = kG, NPT = kNPT, NP = NPT / 2, CB = kCB, TE = kTE;
+  using S = PairSmem<T>;
+  constexpr int NPT = kNPT, NP = NPT / 2, CB = kCB, TE = T / kG;
+  static_assert(TE % 4 == 0 && T % kCk == 0, "whole 16-byte units; whole saved units");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
 
@@ -227,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 9)
   const int64_t t_begin = (int64_t)seg * p.seg_len;
   const int64_t t_end = min(p.L, t_begin + p.seg_len);
   const int seg_steps = (int)(t_end - t_begin);
-  const int nchunks = (seg_steps + kT - 1) / kT;
+  const int nchunks = (seg_steps + T - 1) / T;
   const bool has_z = PASS == 0 && p.z != nullptr;
 
   // this thread's states n = g*NPT + j: A, and the initial state
@@ -277,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 9)
     mbar_arrive_expect_tx(bar, bytes_u);
     if (stall && k == 1) return;  // the failure-path test: armed, never copied
     // time-major boxes (T steps, CB channels) or channel-major ones (CB, T)
-    const int tk = (int)(t_begin + (int64_t)k * kT);
+    const int tk = (int)(t_begin + (int64_t)k * T);
     const int x = p.bld ? (int)L.d0 : tk, y = p.bld ? tk : (int)L.d0, zc = (int)L.b;
     tma3d(st, &maps.u, bar, x, y, zc);
     tma3d(st + S::kRawIO, &maps.d, bar, x, y, zc);
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 9)
   };
   auto issue_bc = [&](int k) {
     mbar_arrive_expect_tx(bar_bc, bytes_bc);
-    const int x = (int)(t_begin + (int64_t)k * kT), zc = (int)L.b;
+    const int x = (int)(t_begin + (int64_t)k * T), zc = (int)L.b;
     tma3d(sm + S::oStageBC, &maps.b, bar_bc, x, 0, zc);
     if (PASS == 0) tma3d(sm + S::oStageBC + S::kRawBC, &maps.c, bar_bc, x, 0, zc);
   };
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 9)
     //    B (warp 0) and C (warp 1) transposed to [t][n]
     const bool ok = mbar_wait_bounded(&bar_u[i % kNSU], (uint32_t)((i / kNSU) & 1), wlim) &&
                     mbar_wait_bounded(bar_bc, (uint32_t)(i & 1), wlim);
-    const int tc = min(kT, seg_steps - i * kT);
+    const int tc = min(T, seg_steps - i * T);
     float du[TE], gate[TE];
     {
       const unsigned char* st = sm + S::oStageU + (i % kNSU) * S::kStageU;
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 9)
       const __nv_bfloat16* sz = reinterpret_cast<const __nv_bfloat16*>(st + 2 * S::kRawIO);
       float dl[TE], uu[TE], zz[TE];
       if (!p.bld) {
-        const int off = L.c * kT + L.g * TE;  // this thread's steps in a [c][t] box
+        const int off = L.c * T + L.g * TE;  // this thread's steps in a [c][t] box
         vecio<__nv_bfloat16, TE>::load(sd + off, dl);
         vecio<__nv_bfloat16, TE>::load(su + off, uu);
         if (has_z) vecio<__nv_bfloat16, TE>::load(sz + off, zz);
@@ -349,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 9)
           if (has_z) zz[j] = __bfloat162float(sz[e]);
         }
       }
-      const bool whole = tc == kT;
+      const bool whole = tc == T;
 #pragma unroll
       for (int j = 0; j < TE; ++j) {
         const float x = dl[j] + bias;
@@ -367,18 +375,21 @@ __global__ void __launch_bounds__(kThreads, 9)
           gate[j] = has_z ? silu_fast(zz[j]) : 1.f;
         }
       }
-      // warp 0: B, warp 1: C, to [t][n]; lane l moves [n = (l >> 2) + 8 r][t = 4 (l & 3) .. + 3]
+      // warp 0: B, warp 1: C, to [t][n]; lane l moves [n = (l >> 2) + 8 r][t = 16 h + 4 (l & 3) .. + 3]
       if (PASS == 0 || warp == 0) {
         const unsigned char* src = sm + S::oStageBC + warp * S::kRawBC;
         float* dst = warp == 0 ? BT : CT;
-        const int t0 = 4 * (L.lane & 3);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int n = (L.lane >> 2) + 8 * r;
-          const float4 q = *reinterpret_cast<const float4*>(src + (n * kT + t0) * 4);
-          const float v[4] = {q.x, q.y, q.z, q.w};
+        for (int h16 = 0; h16 < T / 16; ++h16) {
+          const int t0 = 16 * h16 + 4 * (L.lane & 3);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[(t0 + e) * S::RowBT + bt_col(t0 + e, n)] = v[e];
+          for (int r = 0; r < 2; ++r) {
+            const int n = (L.lane >> 2) + 8 * r;
+            const float4 q = *reinterpret_cast<const float4*>(src + (n * T + t0) * 4);
+            const float v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[(t0 + e) * S::RowBT + bt_col(t0 + e, n)] = v[e];
+          }
         }
       }
     }
@@ -395,9 +406,11 @@ __global__ void __launch_bounds__(kThreads, 9)
       if (i + 1 < nchunks) issue_bc(i + 1);
     }
     if (issued < nchunks) ++issued;
-    // training forward: the state at the start of chunk i, for the backward
+    // training forward: the state at the start of chunk i (and below, after every kCk
+    // steps inside it), for the backward
     if (PASS == 0 && p.ckpt != nullptr && L.chan_ok) {
-      float* cp = p.ckpt + ((L.b * p.ckpt_nch + t_begin / kT + i) * p.dim + L.d) * kN + L.g * NPT;
+      float* cp = p.ckpt + ((L.b * p.ckpt_nch + t_begin / kCk + i * (T / kCk)) * p.dim + L.d) * kN +
+                  L.g * NPT;
 #pragma unroll
       for (int q = 0; q < NP; q += 2) {
         float a0, a1, a2, a3;
@@ -448,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 9)
       }
       float acc[4];
 #pragma unroll
-      for (int t = 0; t < kT; ++t) {
+      for (int t = 0; t < T; ++t) {
         f2 du_n;
         f2 b_n[NP], c_n[NP], a_n[NP], v_n[NP];
-        if (t + 2 < kT) load_step(t + 2, du_n, b_n, c_n);
-        if (t + 1 < kT) discretise(du_l, b_l, a_n, v_n);
+        if (t + 2 < T) load_step(t + 2, du_n, b_n, c_n);
+        if (t + 1 < T) discretise(du_l, b_l, a_n, v_n);
 #pragma unroll
         for (int q = 0; q < NP; ++q) hp[q] = fma2(a_c[q], sub2(hp[q], v_c[q]), v_c[q]);
         if (PASS == 0) {
@@ -462,11 +475,28 @@ __global__ void __launch_bounds__(kThreads, 9)
           float lo, hi;
           unpack2(acc2, lo, hi);
           acc[t % 4] = lo + hi;
-          if (t % 4 == 3)
-            *reinterpret_cast<float4*>(P + pair_pidx(L.g, L.c, t / 4)) =
-                make_float4(acc[0], acc[1], acc[2], acc[3]);
+          if (t % 4 == 3) {  // the warp's two groups of the channel (lanes l, l ^ 16) added
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = __shfl_xor_sync(0xffffffffu, acc[e], 16);
+            if (L.lane < 16)
+              *reinterpret_cast<float4*>(P + pair_pidx<T>(warp, L.c, t / 4)) =
+                  make_float4(acc[0] + o[0], acc[1] + o[1], acc[2] + o[2], acc[3] + o[3]);
+          }
         }
-        if (t + 1 < kT) {
+        if (PASS == 0 && (t + 1) % kCk == 0 && t + 1 < T && p.ckpt != nullptr && L.chan_ok &&
+            i * T + t + 1 < seg_steps) {
+          float* cp = p.ckpt + ((L.b * p.ckpt_nch + t_begin / kCk + i * (T / kCk) + (t + 1) / kCk) *
+                                    p.dim + L.d) * kN + L.g * NPT;
+#pragma unroll
+          for (int q = 0; q < NP; q += 2) {
+            float a0, a1, a2, a3;
+            unpack2(hp[q], a0, a1);
+            unpack2(hp[q + 1], a2, a3);
+            *reinterpret_cast<float4*>(cp + 2 * q) = make_float4(a0, a1, a2, a3);
+          }
+        }
+        if (t + 1 < T) {
 #pragma unroll
           for (int q = 0; q < NP; ++q) {
             a_c[q] = a_n[q];
@@ -474,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 9)
             c_c[q] = c_l[q];
           }
         }
-        if (t + 2 < kT) {
+        if (t + 2 < T) {
           du_l = du_n;
 #pragma unroll
           for (int q = 0; q < NP; ++q) {
@@ -486,19 +516,19 @@ __global__ void __launch_bounds__(kThreads, 9)
     }
     // the partials are complete; the next chunk's conversion may overwrite the tiles
     __syncthreads();
-    // 4. finalise this thread's steps of chunk i (unit g of its channel's row)
+    // 4. finalise this thread's steps of chunk i (units g TE/4 .. of its channel's rows)
     if (PASS == 0) {
-      float4 s4 = *reinterpret_cast<const float4*>(P + pair_pidx(0, L.c, L.g));
-#pragma unroll
-      for (int gg = 1; gg < G; ++gg) {
-        const float4 o = *reinterpret_cast<const float4*>(P + pair_pidx(gg, L.c, L.g));
-        s4.x += o.x; s4.y += o.y; s4.z += o.z; s4.w += o.w;
-      }
-      const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
       float y[TE];
 #pragma unroll
-      for (int e = 0; e < TE; ++e) y[e] = (sv[e] + du[e]) * gate[e];
-      __nv_bfloat16* dst = ybase + (int64_t)i * kT * p.st_y[2];
+      for (int u4 = 0; u4 < TE / 4; ++u4) {
+        const int unit = L.g * (TE / 4) + u4;
+        const float4 s0 = *reinterpret_cast<const float4*>(P + pair_pidx<T>(0, L.c, unit));
+        const float4 s1 = *reinterpret_cast<const float4*>(P + pair_pidx<T>(1, L.c, unit));
+        const float sv[4] = {s0.x + s1.x, s0.y + s1.y, s0.z + s1.z, s0.w + s1.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[4 * u4 + e] = (sv[e] + du[4 * u4 + e]) * gate[4 * u4 + e];
+      }
+      __nv_bfloat16* dst = ybase + (int64_t)i * T * p.st_y[2];
       if (L.chan_ok) {
         if (p.vec_y && L.g * TE + TE <= tc) {
           vecio<__nv_bfloat16, TE>::store(dst, y);
@@ -570,10 +600,10 @@ bool map3(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t esz, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int PASS>
+template <int PASS, int T>
 cudaError_t launch_pair_one(const ScanArgs& a, const FastMaps& m, int nz, cudaStream_t stream) {
-  constexpr size_t bytes = PairSmem::kLaunch;
-  auto kern = scan_pair_kernel<PASS>;
+  constexpr size_t bytes = PairSmem<T>::kLaunch;
+  auto kern = scan_pair_kernel<PASS, T>;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -592,7 +622,7 @@ cudaError_t launch_pair_one(const ScanArgs& a, const FastMaps& m, int nz, cudaSt
 
 // Tensor maps of one launch: u / Δ / z boxes of T steps x CW channels, B / C boxes
 // of T steps x N states.
-bool fast_maps(const ScanArgs& a, uint32_t CW, FastMaps& m) {
+bool fast_maps(const ScanArgs& a, uint32_t CW, uint32_t T, FastMaps& m) {
   memset(&m, 0, sizeof m);
   const uint64_t L = (uint64_t)a.L, D = (uint64_t)a.dim, Bt = (uint64_t)a.batch;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -600,23 +630,24 @@ bool fast_maps(const ScanArgs& a, uint32_t CW, FastMaps& m) {
   // u / Δ / z: time-major (L, dim, batch) with (T, CW) boxes, or channel-major
   // (dim, L, batch) with (CW, T) boxes
   const uint64_t i0 = a.bld ? D : L, i1 = a.bld ? L : D;
-  const uint32_t b0 = a.bld ? CW : kT, b1 = a.bld ? kT : CW;
+  const uint32_t b0 = a.bld ? CW : T, b1 = a.bld ? T : CW;
   const int o1 = a.bld ? 2 : 1;
   bool ok = map3(&m.u, a.u, bf, 2, i0, i1, Bt, b0, b1, a.st_u[o1], a.st_u[0]) &&
             map3(&m.d, a.delta, bf, 2, i0, i1, Bt, b0, b1, a.st_d[o1], a.st_d[0]) &&
-            map3(&m.b, a.B, f32, 4, L, kN, Bt, kT, kN) && map3(&m.c, a.C, f32, 4, L, kN, Bt, kT, kN);
+            map3(&m.b, a.B, f32, 4, L, kN, Bt, T, kN) && map3(&m.c, a.C, f32, 4, L, kN, Bt, T, kN);
   if (ok && a.z) ok = map3(&m.z, a.z, bf, 2, i0, i1, Bt, b0, b1, a.st_z[o1], a.st_z[0]);
   return ok;
 }
 
 cudaError_t launch_pair(const ScanArgs& a, cudaStream_t stream) {
   FastMaps m;
-  if (!fast_maps(a, kCB, m)) return cudaErrorInvalidValue;
   if (a.nseg > 1) {
-    const cudaError_t e = launch_pair_one<1>(a, m, a.nseg - 1, stream);
+    if (!fast_maps(a, kCB, kTCarry, m)) return cudaErrorInvalidValue;
+    const cudaError_t e = launch_pair_one<1, kTCarry>(a, m, a.nseg - 1, stream);
     if (e != cudaSuccess) return e;
   }
-  return launch_pair_one<0>(a, m, a.nseg, stream);
+  if (!fast_maps(a, kCB, kTOut, m)) return cudaErrorInvalidValue;
+  return launch_pair_one<0, kTOut>(a, m, a.nseg, stream);
 }
 
 }  // namespace
