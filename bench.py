@@ -977,7 +977,7 @@ def main():
                 "bytes_per_step": nbytes},
         "roofline": scan_roofline(w, r["ms"] / args.steps, hbm_peak, sm_max, peak_kind,
                                   "scan_kernel@" + w.name,
-                                  "scan_pair_kernel<0> (blocks of two warps: 16 channels a block)"),
+                                  "scan_pair_kernel<0, 32> (blocks of two warps: 16 channels a block, 32-step chunks)"),
         "e2e": {"value": nbytes * r["e2e_steps"] / (r["e2e_ms"] / 1e3) / 1e9 * world,
                 "unit": "GB/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "steps": r["e2e_steps"],
