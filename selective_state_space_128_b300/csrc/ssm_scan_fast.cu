@@ -140,7 +140,7 @@ template <int T> struct PairSmem {
   static constexpr size_t kP = (size_t)2 * kCB * T * 4;       // a warp's two groups pre-added
   static constexpr size_t oBar = up(oP + kP, 8);              // kNSU + 1 mbarriers
   static constexpr size_t kBytes = oBar + 8 * (kNSU + 1);
-  static constexpr size_t kLaunch = kBytes + 128;             // room to align the base
+  static constexpr size_t kLaunch = kBytes + 1024;            // room to align the base
 };
 
 // Index (in floats) of steps 4u..4u+3 of partial row (w, c) (4T bytes a row).  The
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 9)
   constexpr int NPT = kNPT, NP = NPT / 2, CB = kCB, TE = T / kG;
   static_assert(TE % 4 == 0 && T % kCk == 0, "whole 16-byte units; whole saved units");
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   FastLane L;
@@ -343,7 +343,9 @@ __global__ void __launch_bounds__(kThreads, 9)
       const __nv_bfloat16* sz = reinterpret_cast<const __nv_bfloat16*>(st + 2 * S::kRawIO);
       float dl[TE], uu[TE], zz[TE];
       if (!p.bld) {
-        const int off = L.c * T + L.g * TE;  // this thread's steps in a [c][t] box
+        // this thread's steps in a [c][t] box; 32-step rows (64 bytes) arrive with the
+        // 16-byte chunks of row c permuted by (c >> 1) & 3
+        const int off = L.c * T + (T == 32 ? ((L.g ^ ((L.c >> 1) & 3)) * TE) : L.g * TE);
         vecio<__nv_bfloat16, TE>::load(sd + off, dl);
         vecio<__nv_bfloat16, TE>::load(su + off, uu);
         if (has_z) vecio<__nv_bfloat16, TE>::load(sz + off, zz);
@@ -588,7 +590,8 @@ EncodeTiledFn encode_fn() {
 // 3-D map over a (d2, d1, d0) tensor (d0 fastest, unit stride) with element strides
 // s1, s2 of d1, d2 (0: dense) and box (1, b1, b0).
 bool map3(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t esz, uint64_t d0,
-          uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint64_t s1 = 0, uint64_t s2 = 0) {
+          uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint64_t s1 = 0, uint64_t s2 = 0,
+          CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !base) return false;
   const cuuint64_t dims[3] = {d0, d1, d2};
@@ -596,7 +599,7 @@ bool map3(CUtensorMap* m, const void* base, CUtensorMapDataType dt, size_t esz, 
   const cuuint32_t box[3] = {b0, b1, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -632,10 +635,11 @@ bool fast_maps(const ScanArgs& a, uint32_t CW, uint32_t T, FastMaps& m) {
   const uint64_t i0 = a.bld ? D : L, i1 = a.bld ? L : D;
   const uint32_t b0 = a.bld ? CW : T, b1 = a.bld ? T : CW;
   const int o1 = a.bld ? 2 : 1;
-  bool ok = map3(&m.u, a.u, bf, 2, i0, i1, Bt, b0, b1, a.st_u[o1], a.st_u[0]) &&
-            map3(&m.d, a.delta, bf, 2, i0, i1, Bt, b0, b1, a.st_d[o1], a.st_d[0]) &&
+  const CUtensorMapSwizzle sw = (!a.bld && T == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  bool ok = map3(&m.u, a.u, bf, 2, i0, i1, Bt, b0, b1, a.st_u[o1], a.st_u[0], sw) &&
+            map3(&m.d, a.delta, bf, 2, i0, i1, Bt, b0, b1, a.st_d[o1], a.st_d[0], sw) &&
             map3(&m.b, a.B, f32, 4, L, kN, Bt, T, kN) && map3(&m.c, a.C, f32, 4, L, kN, Bt, T, kN);
-  if (ok && a.z) ok = map3(&m.z, a.z, bf, 2, i0, i1, Bt, b0, b1, a.st_z[o1], a.st_z[0]);
+  if (ok && a.z) ok = map3(&m.z, a.z, bf, 2, i0, i1, Bt, b0, b1, a.st_z[o1], a.st_z[0], sw);
   return ok;
 }
 
