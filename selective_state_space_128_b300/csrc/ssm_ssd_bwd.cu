@@ -305,7 +305,9 @@ template <int N> struct ChunkBwdSmem {
   static constexpr int oHl = oHh + kP * LN;
   static constexpr int oDh = oHl + kP * LN;       // dH_c [p][n]
   static constexpr int oDl = oDh + kP * LN;
-  static constexpr int kTileElems = oDl + kP * LN;
+  static constexpr int oDy = oDl + kP * LN;       // dy [t][p] (for dz)
+  static constexpr int oZ = oDy + kQ * L64;       // z [t][p]
+  static constexpr int kTileElems = oZ + kQ * L64;
   // fp32 arrays (float offsets after the tiles)
   static constexpr int fS = 0;                    // s, β, exp(s), exp(s_end - s)
   static constexpr int fRow = fS + 4 * kQ;        // row partials [K | inter | r][column quarter][Q]
@@ -338,6 +340,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
   __nv_bfloat16* const sHl = tl + S::oHl;
   __nv_bfloat16* const sDh = tl + S::oDh;
   __nv_bfloat16* const sDl = tl + S::oDl;
+  __nv_bfloat16* const sDy = tl + S::oDy;
+  __nv_bfloat16* const sZ = tl + S::oZ;
   float* const sS = fs + S::fS;       // s
   float* const sBeta = sS + kQ;       // β
   float* const sEs = sS + 2 * kQ;     // exp(s_t)
@@ -372,6 +376,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
     sEs[e] = expf(tr[e]);
     sEe[e] = expf(tr[kQ - 1] - tr[e]);
   }
+  // warp 0's steps (lane, lane + 32) of dt for the last phase, read now
+  float dt_raw[2] = {0.f, 0.f};
+  if (warp == 0) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = lane + 32 * r;
+      if (t < valid) dt_raw[r] = bf(a.dt[(b * a.L + t0 + t) * a.H + h]);
+    }
+  }
   float gx = 0.f;  // Σ ḡ·x over this thread's elements (for dD)
   {
     static_assert(kQ * kP / 8 == kChunkThreads, "one 8-wide vector of x, dy, z a thread");
@@ -383,6 +396,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
     const uint4 yr = ok ? __ldg(reinterpret_cast<const uint4*>(a.dy + o)) : zero;
     const uint4 zr = (ok && a.z) ? __ldg(reinterpret_cast<const uint4*>(a.z + o)) : zero;
     *reinterpret_cast<uint4*>(sX + t * L64 + 8 * p8) = xr;
+    *reinterpret_cast<uint4*>(sDy + t * L64 + 8 * p8) = yr;
+    *reinterpret_cast<uint4*>(sZ + t * L64 + 8 * p8) = zr;
     const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w}, yw[4] = {yr.x, yr.y, yr.z, yr.w},
                    zw[4] = {zr.x, zr.y, zr.z, zr.w};
     uint32_t hw[4], lw[4];
@@ -648,8 +663,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
         const int pp = q0 + 8 * j + c2;
         const int64_t o = ((b * a.L + t0 + t) * a.H + h) * kP + pp;
         const uint32_t xv = *reinterpret_cast<const uint32_t*>(sX + t * L64 + pp);
-        const uint32_t zv = *reinterpret_cast<const uint32_t*>(a.z + o);
-        const uint32_t dv = *reinterpret_cast<const uint32_t*>(a.dy + o);
+        const uint32_t zv = *reinterpret_cast<const uint32_t*>(sZ + t * L64 + pp);
+        const uint32_t dv = *reinterpret_cast<const uint32_t*>(sDy + t * L64 + pp);
         float r[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -826,7 +841,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1) ssd_bwd_chunk_kernel(const S
       const int t = lane + 32 * r;
       if (t >= valid) continue;
       const int64_t o = (b * a.L + t0 + t) * a.H + h;
-      const float xr = bf(a.dt[o]) + bias;
+      const float xr = dt_raw[r] + bias;
       const float dtv = a.softplus ? softplus_precise(xr) : xr;
       const float sig = a.softplus ? sigmoid_precise(xr) : 1.f;
       const float ell = dtv * ah, el = expf(ell);
