@@ -530,9 +530,11 @@ int ssm_scan_fwd_complex(const void* u, const void* delta, const float* delta_bi
  * of each channel of a head with the scalar A[h] for every state, the head's
  * step shared by its channels and the group's B, C): the derivatives of
  * Σ y·dy + Σ final_state·d_final_state, in the chunked form: the states
- * entering the chunks recomputed by a forward walk (fp32), the derivatives
- * reaching the chunks' end states by a reverse walk, then every derivative of
- * a chunk from its 64 steps, all in fp32; sums over a group's heads and over
+ * entering the chunks recomputed by a forward walk (held in fp32), the
+ * derivatives reaching the chunks' end states by a reverse walk, then every
+ * derivative of a chunk from its 64 steps; the products run on the tensor
+ * cores with each fp32 operand split into two bf16 parts (about 16 bits kept),
+ * sums and elementwise steps in fp32; sums over a group's heads and over
  * chunks in a fixed order, so results repeat bit for bit.
  *
  * Inputs, layouts, flags and supported shapes as ssm_ssd_fwd; dy (batch,
