@@ -92,12 +92,13 @@ def test_ssd_bench_shape_sampled():
 # the backward (ssm_ssd_bwd) against oracle.ssd_bwd
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("case", ["n64_g2", "n128_g1", "euler", "no_gate_no_D", "single_step",
-                                  "three_heads_per_group", "no_init_no_dfinal"])
+@pytest.mark.parametrize("case", ["n64_g2", "n128_g1", "n128_g2_three_chunks", "euler",
+                                  "no_gate_no_D", "single_step", "three_heads_per_group",
+                                  "no_init_no_dfinal"])
 def test_ssd_backward_matches_oracle(case):
     cfg = dict(batch=2, L=90, H=4, G=2, N=64)
-    cfg.update(dict(n128_g1=dict(N=128, G=1, L=70), single_step=dict(L=1),
-                    three_heads_per_group=dict(H=6, G=2, L=50)).get(case, {}))
+    cfg.update(dict(n128_g1=dict(N=128, G=1, L=70), n128_g2_three_chunks=dict(N=128, G=2, L=150),
+                    single_step=dict(L=1), three_heads_per_group=dict(H=6, G=2, L=50)).get(case, {}))
     x = _inputs(seed=400 + len(case), **cfg)
     use_z = use_D = case != "no_gate_no_D"
     euler = case == "euler"
